@@ -1,0 +1,481 @@
+"""Plain, slow CPU oracle for quantized-KV speculative decode attention.
+
+TEST INFRASTRUCTURE ONLY.  The library's product path never imports, calls or
+links anything in this package.  Only the test suite, the smoke check and the
+benchmark's CPU-baseline leg do.  This package shares no code with the CUDA
+library: no kernels, headers, helpers or tables.  It computes the method the way
+the pages state it, step by step:
+
+* Quantizer.  KIVI-style asymmetric min/max quantization.  Keys are grouped per
+  channel over G tokens; values per token over G channels.  The code is
+  round-half-even((x - min) * (1/scale)), computed in fp32 and clamped.
+  (SpeCache page, Approach / Measured effects: "2-bit KIVI (g=32)", "1-bit
+  KIVI"; QuantSpec page, Experimental setup: builds on KIVI.)
+* Hierarchical INT8 code.  The upper nibble is the INT4 draft code; upper plus
+  lower nibble rebuild the INT8 target code.  No separate draft copy is stored.
+  (QuantSpec page, Approach.)
+* Double full-precision buffer of 2G tokens.  It keeps recent tokens in bf16.
+  When full, the oldest G tokens are quantized.  (QuantSpec page, Approach.)
+* Attention.  Softmax attention, in fp64, over the dequantized cache plus the
+  bf16 residual tokens plus gamma causal speculative tokens.  Selected tokens
+  use their 16-bit K/V in place of the low-bit copy.  (SpeCache page,
+  Approach; QuantSpec page, Approach.)
+* Top-k.  Per KV head, the k tokens that score highest under the low-bit keys,
+  scored with the speculative token's query.  (SpeCache page, Approach.)
+
+Where the pages are silent, the reading taken is stated at the function.  Those
+readings are also listed in the repository's design notes.  The "parity
+unpinned" functions are named in the module docstring of ``tests/test_oracle_pins.py``
+(none at present).
+"""
+from __future__ import annotations
+
+import math
+from typing import Iterable, Optional, Sequence
+
+import numpy as np
+
+F32 = np.float32
+
+FORMAT_BITS = {"hier8": 8, "int2": 2, "int1": 1}
+# mode -> (storage format it reads, code bits seen by the mode, scale multiplier)
+MODES = {
+    "int8": ("hier8", 8, 1),
+    "int4": ("hier8", 4, 16),
+    "int2": ("int2", 2, 1),
+    "int1": ("int1", 1, 1),
+}
+SLAB = 32  # tokens per value-plane slab (storage layout, see pack_v_plane)
+
+
+# ================================================================================
+# Quantizer
+# ================================================================================
+
+
+def quantize_minmax(x: np.ndarray, bits: int, axis: int):
+    """Asymmetric min/max quantization of ``x`` along ``axis``.
+
+    Follows the KIVI-style quantizer the pages build on (SpeCache page, Approach
+    and Measured effects table; QuantSpec page, Experimental setup).  Every step
+    is an fp32 operation rounded to nearest even.  No step is fused.
+
+      1. mn = min(x) + 0, mx = max(x) + 0      (the + 0 turns -0 into +0)
+      2. scale = (mx - mn) / (2^bits - 1)
+      3. inv = 0 if scale == 0 else 1 / scale  (a constant group gets codes 0)
+      4. code = clamp(rint((x - mn) * inv), 0, 2^bits - 1), with half-even rint
+      5. zero point = mn
+
+    Returns (codes uint8, scale f32, zero f32); the reduced axis is dropped from
+    scale and zero.  Non-finite inputs are rejected.
+    """
+    x = np.asarray(x, dtype=F32)
+    if not np.all(np.isfinite(x)):
+        raise ValueError("non-finite input to the quantizer")
+    levels = F32(2 ** bits - 1)
+    mn = (x.min(axis=axis, keepdims=True) + F32(0)).astype(F32)
+    mx = (x.max(axis=axis, keepdims=True) + F32(0)).astype(F32)
+    scale = ((mx - mn) / levels).astype(F32)
+    with np.errstate(divide="ignore"):
+        inv = np.where(scale == F32(0), F32(0), (F32(1) / scale)).astype(F32)
+    t = ((x - mn).astype(F32) * inv).astype(F32)
+    codes = np.clip(np.rint(t), F32(0), levels).astype(np.uint8)
+    return codes, np.squeeze(scale, axis=axis), np.squeeze(mn, axis=axis)
+
+
+def quantize_key_group(kg: np.ndarray, bits: int):
+    """Keys of one token group ``[..., G, D]``: one (scale, zero) per channel over
+    the G tokens.  Returns codes ``[..., G, D]``, scale/zero ``[..., D]``."""
+    return quantize_minmax(kg, bits, axis=-2)
+
+
+def quantize_value_group(vg: np.ndarray, bits: int, G: int):
+    """Values ``[..., T, D]``: one (scale, zero) per token per block of G channels.
+    Returns codes ``[..., T, D]``, scale/zero ``[..., T, D/G]``."""
+    shp = vg.shape
+    D = shp[-1]
+    x = vg.reshape(shp[:-1] + (D // G, G))
+    c, s, z = quantize_minmax(x, bits, axis=-1)
+    return c.reshape(shp), s, z
+
+
+def split_hierarchical(codes8: np.ndarray):
+    """Hierarchical INT8 code -> (upper nibble, lower nibble).  The upper nibble
+    is the INT4 draft code (QuantSpec page, Approach)."""
+    c = codes8.astype(np.uint8)
+    return (c >> 4).astype(np.uint8), (c & 15).astype(np.uint8)
+
+
+def mode_codes_scale(mode: str, codes: np.ndarray, scale: np.ndarray):
+    """The (code, scale) pair a read mode sees.
+
+    INT8 reads the full hierarchical code with its scale.  INT4 reads only the
+    upper nibble, with 16 x scale.  So INT4 dequant equals INT8 dequant with the
+    lower nibble zeroed (QuantSpec page, Approach).  INT2/INT1 read their own
+    codes and scale.
+    """
+    _, _, mult = MODES[mode]
+    if mode == "int4":
+        return (codes >> 4).astype(np.uint8), scale.astype(np.float64) * 16.0
+    return codes, scale.astype(np.float64) * mult
+
+
+# ================================================================================
+# Packed storage layout (the bytes the device library stores)
+# ================================================================================
+
+
+def pack_k_plane(codes: np.ndarray, pb: int) -> np.ndarray:
+    """Key plane, token-major: row t holds the D channel codes of token t.  Each
+    byte j packs channels (8/pb)*j + e at bits [pb*e, pb*e + pb).
+    ``codes [..., T, D]`` (values < 2^pb) -> ``[..., T, D*pb/8]`` uint8."""
+    per = 8 // pb
+    c = codes.astype(np.uint8)
+    shp = c.shape
+    c = c.reshape(shp[:-1] + (shp[-1] // per, per))
+    out = np.zeros(c.shape[:-1], dtype=np.uint8)
+    for e in range(per):
+        out |= (c[..., e] << (pb * e)).astype(np.uint8)
+    return out
+
+
+def pack_v_plane(codes: np.ndarray, pb: int) -> np.ndarray:
+    """Value plane, in 32-token slabs: slab s, row d holds the codes of channel d
+    for tokens 32s..32s+31.  Each byte j packs tokens 32s + (8/pb)*j + e at bits
+    [pb*e, pb*e + pb).  ``codes [..., T, D]`` (T a multiple of 32) ->
+    ``[..., T/32, D, 32*pb/8]`` uint8."""
+    per = 8 // pb
+    c = codes.astype(np.uint8)
+    *lead, T, D = c.shape
+    c = c.reshape(tuple(lead) + (T // SLAB, SLAB, D))
+    c = np.swapaxes(c, -1, -2)                         # [..., T/32, D, 32]
+    c = c.reshape(c.shape[:-1] + (SLAB // per, per))
+    out = np.zeros(c.shape[:-1], dtype=np.uint8)
+    for e in range(per):
+        out |= (c[..., e] << (pb * e)).astype(np.uint8)
+    return out
+
+
+# ================================================================================
+# The cache: quantized history + 2G bf16 residual buffer
+# ================================================================================
+
+
+class OracleCache:
+    """One layer's cache for ``batch`` sequences and ``num_kv_heads`` KV heads.
+
+    State (Lq, r).  Lq counts quantized tokens, a multiple of G.  r counts
+    residual bf16 tokens, 0 <= r < 2G.  The residual buffer is linear: slot 0
+    holds the oldest token.  Appending one token goes like this (QuantSpec page,
+    Approach: a double full-precision buffer of size 2G):
+
+      1. write it to slot r; r += 1
+      2. if r == 2G: quantize slots [0, G) as token group [Lq, Lq + G);
+         move slots [G, 2G) to [0, G); Lq += G; r = G
+
+    So once N >= 2G tokens have arrived, at least G recent tokens stay in bf16.
+    Closed form: Lq = G*(floor(N/G) - 1), r = N - Lq.  Keys and values are both
+    quantized when their group is flushed.
+    """
+
+    def __init__(self, batch: int, num_kv_heads: int, head_dim: int, group_size: int,
+                 fmt: str, capacity: int):
+        if fmt not in FORMAT_BITS:
+            raise ValueError(fmt)
+        if capacity % group_size:
+            raise ValueError("capacity must be a multiple of the group size")
+        if head_dim % group_size:
+            raise ValueError("value groups span G channels: G must divide head_dim")
+        self.B, self.H, self.D, self.G = batch, num_kv_heads, head_dim, group_size
+        self.fmt, self.bits, self.capacity = fmt, FORMAT_BITS[fmt], capacity
+        B, H, D, G = self.B, self.H, self.D, self.G
+        self.k_codes = np.zeros((B, H, capacity, D), np.uint8)
+        self.v_codes = np.zeros((B, H, capacity, D), np.uint8)
+        self.k_scale = np.zeros((B, H, capacity // G, D), F32)
+        self.k_zero = np.zeros((B, H, capacity // G, D), F32)
+        self.v_scale = np.zeros((B, H, capacity, D // G), F32)
+        self.v_zero = np.zeros((B, H, capacity, D // G), F32)
+        self.res_k = np.zeros((B, H, 2 * G, D), F32)
+        self.res_v = np.zeros((B, H, 2 * G, D), F32)
+        self.Lq = 0
+        self.r = 0
+
+    # -- appending ---------------------------------------------------------------
+
+    def _flush(self):
+        G, L = self.G, self.Lq
+        if L + G > self.capacity:
+            raise OverflowError("quantized capacity exceeded")
+        kc, ks, kz = quantize_key_group(self.res_k[:, :, :G], self.bits)
+        vc, vs, vz = quantize_value_group(self.res_v[:, :, :G], self.bits, G)
+        self.k_codes[:, :, L:L + G] = kc
+        self.k_scale[:, :, L // G] = ks
+        self.k_zero[:, :, L // G] = kz
+        self.v_codes[:, :, L:L + G] = vc
+        self.v_scale[:, :, L:L + G] = vs
+        self.v_zero[:, :, L:L + G] = vz
+        self.res_k[:, :, :G] = self.res_k[:, :, G:].copy()
+        self.res_v[:, :, :G] = self.res_v[:, :, G:].copy()
+        self.Lq += G
+        self.r = G
+
+    def append_token(self, k1: np.ndarray, v1: np.ndarray):
+        """Append one token: ``k1, v1`` are ``[B, Hkv, D]`` bf16-valued float32."""
+        self.res_k[:, :, self.r] = k1
+        self.res_v[:, :, self.r] = v1
+        self.r += 1
+        if self.r == 2 * self.G:
+            self._flush()
+
+    def append(self, k_new: np.ndarray, v_new: np.ndarray):
+        """Append ``n`` tokens (``[B, Hkv, n, D]``) as n single-token steps."""
+        n = k_new.shape[2]
+        T = self.r + n
+        f = 0 if T < 2 * self.G else T // self.G - 1
+        if self.Lq + f * self.G > self.capacity:
+            raise OverflowError("quantized capacity exceeded")
+        for i in range(n):
+            self.append_token(k_new[:, :, i], v_new[:, :, i])
+
+    # -- views -------------------------------------------------------------------
+
+    def residual(self):
+        return self.res_k[:, :, :self.r], self.res_v[:, :, :self.r]
+
+    def packed_k_planes(self):
+        """Stored key planes ``[B, Hkv, Lq, rowbytes]``: [upper, lower] nibble
+        planes for the hierarchical format, [codes] otherwise."""
+        c = self.k_codes[:, :, :self.Lq]
+        if self.fmt == "hier8":
+            hi, lo = split_hierarchical(c)
+            return [pack_k_plane(hi, 4), pack_k_plane(lo, 4)]
+        return [pack_k_plane(c, self.bits)]
+
+    def packed_v_planes(self):
+        """Stored value planes ``[B, Hkv, Lq/32, D, slabbytes]``."""
+        c = self.v_codes[:, :, :self.Lq]
+        if self.fmt == "hier8":
+            hi, lo = split_hierarchical(c)
+            return [pack_v_plane(hi, 4), pack_v_plane(lo, 4)]
+        return [pack_v_plane(c, self.bits)]
+
+    def dequant_unit(self, mode: str, b: int, h: int):
+        """Dequantized keys and values of (b, kv head h) in fp64, ``[Lq, D]`` each:
+        x_hat = code * scale + zero under the mode's (code, scale)."""
+        fmt, _, _ = MODES[mode]
+        if fmt != self.fmt:
+            raise ValueError(f"mode {mode} cannot read format {self.fmt}")
+        L, G, D = self.Lq, self.G, self.D
+        kc, ks = mode_codes_scale(mode, self.k_codes[b, h, :L], self.k_scale[b, h, :L // G])
+        vc, vs = mode_codes_scale(mode, self.v_codes[b, h, :L], self.v_scale[b, h, :L])
+        kz = self.k_zero[b, h, :L // G].astype(np.float64)
+        vz = self.v_zero[b, h, :L].astype(np.float64)
+        khat = kc.astype(np.float64) * np.repeat(ks, G, axis=0) + np.repeat(kz, G, axis=0)
+        vhat = (vc.astype(np.float64).reshape(L, D // G, G) * vs[:, :, None] + vz[:, :, None]).reshape(L, D)
+        return khat, vhat
+
+
+# ================================================================================
+# Attention (fp64)
+# ================================================================================
+
+
+def _units(B: int, H: int, units: Optional[Iterable]):
+    if units is None:
+        return [(b, h) for b in range(B) for h in range(H)]
+    return list(units)
+
+
+def attend(cache: OracleCache, mode: str, q: np.ndarray,
+           pend_k: Optional[np.ndarray] = None, pend_v: Optional[np.ndarray] = None,
+           sel_idx: Optional[np.ndarray] = None, sel_k: Optional[np.ndarray] = None,
+           sel_v: Optional[np.ndarray] = None, sm_scale: Optional[float] = None,
+           units: Optional[Sequence] = None):
+    """Decode attention of gamma query tokens over the cache, in fp64.
+
+    ``q [B, gamma, Hq, D]``.  Query head h uses KV head floor(h / (Hq/Hkv)),
+    i.e. consecutive grouping.  Query token i sees these keys:
+
+    * every quantized token t in [0, Lq), dequantized under ``mode``.  If t
+      appears in ``sel_idx[b, kvh]``, the 16-bit ``sel_k/sel_v`` row replaces its
+      low-bit copy (SpeCache page, Approach: the top-k 16-bit KV pairs).
+      Entries outside [0, Lq) are ignored.  Valid entries must be distinct.
+    * every residual bf16 token (QuantSpec page, Approach: the full-precision
+      buffer keeps recent tokens unquantized).
+    * pending speculative token p in [0, P) when p <= P - gamma + i.  That is
+      causal masking among the gamma query tokens, which are the last gamma of
+      the P pending tokens.
+
+    logit = sm_scale * (q . k), with sm_scale = 1/sqrt(D) by default.
+    Returns ``out [B, gamma, Hq, D]`` (fp64) and ``lse [B, gamma, Hq]``
+    (natural log of the softmax denominator).  A query with no visible key gets
+    out = 0 and lse = -inf.  Only the (b, kv head) pairs in ``units`` are
+    computed; the rest stay 0 / -inf.
+    """
+    B, gamma, Hq, D = q.shape
+    H = cache.H
+    if Hq % H:
+        raise ValueError("Hq must be a multiple of Hkv")
+    hg = Hq // H
+    P = 0 if pend_k is None else pend_k.shape[2]
+    if P and P < gamma:
+        raise ValueError("need at least gamma pending tokens")
+    if sm_scale is None or sm_scale <= 0:
+        sm_scale = 1.0 / math.sqrt(D)
+    out = np.zeros((B, gamma, Hq, D), np.float64)
+    lse = np.full((B, gamma, Hq), -np.inf, np.float64)
+    rk, rv = cache.residual()
+    for (b, h) in _units(B, H, units):
+        khat, vhat = cache.dequant_unit(mode, b, h)
+        keep = np.ones(cache.Lq, bool)
+        xk, xv = [], []
+        if sel_idx is not None:
+            for j in range(sel_idx.shape[2]):
+                t = int(sel_idx[b, h, j])
+                if 0 <= t < cache.Lq:
+                    if not keep[t]:
+                        raise ValueError("duplicate selected index")
+                    keep[t] = False
+                    xk.append(sel_k[b, h, j].astype(np.float64))
+                    xv.append(sel_v[b, h, j].astype(np.float64))
+        base_k = [khat[keep], rk[b, h].astype(np.float64)]
+        base_v = [vhat[keep], rv[b, h].astype(np.float64)]
+        if xk:
+            base_k.append(np.stack(xk))
+            base_v.append(np.stack(xv))
+        for i in range(gamma):
+            nvis = (P - gamma + i + 1) if P else 0
+            keys = np.concatenate(base_k + [pend_k[b, h, :nvis].astype(np.float64)] if P else base_k)
+            vals = np.concatenate(base_v + [pend_v[b, h, :nvis].astype(np.float64)] if P else base_v)
+            if keys.shape[0] == 0:
+                continue
+            for hh in range(hg):
+                hq = h * hg + hh
+                logits = sm_scale * (keys @ q[b, i, hq].astype(np.float64))
+                m = logits.max()
+                e = np.exp(logits - m)
+                s = e.sum()
+                out[b, i, hq] = (e @ vals) / s
+                lse[b, i, hq] = m + math.log(s)
+    return out, lse
+
+
+# ================================================================================
+# Top-k under the low-bit keys (exact integer scoring)
+# ================================================================================
+
+W_BITS = 21          # magnitude bits of the integer-rounded folded query weights
+E_MIN = -100         # floor on the weight exponent (keeps the unit a normal fp32)
+
+
+def _ordered_pair_tree(p: Sequence[np.float32]) -> np.float32:
+    """Pairwise (balanced binary tree) fp32 sum in index order:
+    ((p0 + p1) + (p2 + p3)) + ...; the length must be a power of two."""
+    vals = [F32(v) for v in p]
+    while len(vals) > 1:
+        vals = [F32(vals[2 * i] + vals[2 * i + 1]) for i in range(len(vals) // 2)]
+    return vals[0]
+
+
+def score_group(qs: np.ndarray, scale_eff: np.ndarray, zero: np.ndarray,
+                codes: np.ndarray) -> np.ndarray:
+    """Top-k score of the G tokens of one key group for one summed query.
+
+    The pages say only that the k tokens attended most, as predicted from the
+    speculative token under the low-bit keys, are prefetched (SpeCache page,
+    Approach).  The score is the logit qs . k_hat, with k_hat = code * scale +
+    zero per channel.  It is computed so that any correct implementation gets
+    the same fp32 value, bit for bit:
+
+      w_d   = fp32(qs_d * scale_d)                           (folded weight)
+      e     = exponent of max_d |w_d| (max|w| < 2^e), floored at -100
+      W_d   = rint(w_d * 2^(21 - e))                         (|W_d| <= 2^21)
+      S_t   = sum_d W_d * code_{t,d}                         (exact integer)
+      beta  = pairwise-tree sum over 32 channel chunks of a sequential fp32 sum
+              of fp32(qs_d * zero_d) within each chunk
+      score = fp32( fp32(fp32(S_t) * 2^(e - 21)) + beta )
+
+    The integer dot product is exact, so summation order cannot change it.
+    The only roundings are the weights' 2^-21 relative rounding, fp32(S_t), one
+    exact power-of-two scaling and the final add.
+    """
+    D = qs.shape[0]
+    w = (qs.astype(F32) * scale_eff.astype(F32)).astype(F32)
+    M = float(np.max(np.abs(w))) if D else 0.0
+    e = math.frexp(M)[1] if M > 0 else 0
+    e = max(e, E_MIN)
+    W = np.rint(w.astype(np.float64) * (2.0 ** (W_BITS - e))).astype(np.int64)
+    S = codes.astype(np.int64) @ W                       # exact integer dot products
+    Sf = S.astype(np.float64).astype(F32)                # |S| < 2^53: one rounding
+    unit = F32(2.0 ** (e - W_BITS))
+    chunk = D // 32
+    partials = []
+    for c in range(32):
+        p = F32(0)
+        for d in range(c * chunk, (c + 1) * chunk):
+            p = F32(p + F32(qs[d] * zero[d]))
+        partials.append(p)
+    beta = _ordered_pair_tree(partials)
+    return ((Sf * unit).astype(F32) + beta).astype(F32)
+
+
+def summed_query(q_spec_b: np.ndarray, h: int, hg: int) -> np.ndarray:
+    """fp32 sum, ascending head order, of the speculative token's query heads
+    that share KV head h.  Under MHA (hg = 1) it is that head's query.  The
+    pages do not say how grouped heads are combined; the sum makes the score
+    the summed logit of the group."""
+    qs = np.zeros(q_spec_b.shape[-1], F32)
+    for hh in range(hg):
+        qs = (qs + q_spec_b[h * hg + hh].astype(F32)).astype(F32)
+    return qs
+
+
+def topk(cache: OracleCache, mode: str, q_spec: np.ndarray, k: int,
+         units: Optional[Sequence] = None):
+    """Per KV head, the k quantized tokens with the highest low-bit score.
+
+    ``q_spec [B, Hq, D]`` is the speculative token's query (SpeCache page,
+    Approach).  Candidates are the quantized tokens t in [0, Lq); residual
+    tokens are already 16-bit on the device.  Tokens are ordered by (score
+    descending, index ascending).  Slots beyond Lq get index -1 and score -inf.
+    Returns ``idx [B, Hkv, k] int32`` and ``score [B, Hkv, k] float32``.
+    """
+    B, Hq, D = q_spec.shape
+    H, G, L = cache.H, cache.G, cache.Lq
+    hg = Hq // H
+    fmt, _, mult = MODES[mode]
+    if fmt != cache.fmt:
+        raise ValueError(f"mode {mode} cannot read format {cache.fmt}")
+    idx = np.full((B, H, k), -1, np.int32)
+    score = np.full((B, H, k), -np.inf, F32)
+    for (b, h) in _units(B, H, units):
+        qs = summed_query(q_spec[b], h, hg)
+        sc = np.empty(L, F32)
+        for g in range(L // G):
+            codes = cache.k_codes[b, h, g * G:(g + 1) * G]
+            s = cache.k_scale[b, h, g].astype(F32)
+            if mode == "int4":
+                codes = codes >> 4
+                s = (s * F32(16)).astype(F32)
+            sc[g * G:(g + 1) * G] = score_group(qs, s, cache.k_zero[b, h, g], codes)
+        order = sorted(range(L), key=lambda t: (-float(sc[t]), t))[:k]
+        idx[b, h, :len(order)] = order
+        score[b, h, :len(order)] = sc[order]
+    return idx, score
+
+
+def all_scores(cache: OracleCache, mode: str, q_spec: np.ndarray, b: int, h: int) -> np.ndarray:
+    """Scores of every quantized token of (b, kv head h) (used by tests)."""
+    Hq = q_spec.shape[1]
+    hg = Hq // cache.H
+    qs = summed_query(q_spec[b], h, hg)
+    G = cache.G
+    out = np.empty(cache.Lq, F32)
+    for g in range(cache.Lq // G):
+        codes = cache.k_codes[b, h, g * G:(g + 1) * G]
+        s = cache.k_scale[b, h, g].astype(F32)
+        if mode == "int4":
+            codes = codes >> 4
+            s = (s * F32(16)).astype(F32)
+        out[g * G:(g + 1) * G] = score_group(qs, s, cache.k_zero[b, h, g], codes)
+    return out
