@@ -1,0 +1,498 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized-KV speculative decode-attention hot path.
+
+One step = one pass over every stage of the path for one layer of a
+Llama-2-7B-shaped model (32 heads, head_dim 128, hierarchical INT8/INT4 cache
+with G = 128, 8K quantized context):
+  1. INT8 verify attention: gamma = 8 causal query tokens over the quantized
+     cache, the bf16 residual buffer and the 8 pending speculative tokens
+     (split-K dequant + QK^T + online softmax + PV, bf16 tail, fused combine);
+  2. top-64 per KV head under the INT4 (upper-nibble) keys, for the last query token;
+  3. quantize-append of the 8 accepted tokens.  This includes a flush of G tokens
+     from the 2G residual buffer into the quantized cache.
+The host counters are restored after each step, so every step is identical.
+Each step runs as one CUDA-graph replay of the C-ABI calls.  The steps rotate
+over 4 cache copies (4 x 76 MB > L2), so no step reads L2-resident inputs.
+
+``--impl reference`` times the CPU oracle on the same workload and metric.
+Under torchrun with N > 1, each rank runs an independent replica.  The path
+has no cross-GPU exchange.
+"""
+import os
+
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import tempfile  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+import kvq_inputs as ki  # noqa: E402
+
+METRIC = "quant-KV decode attention: ms/call, KV tok/s, HBM GB/s (% of ~8 TB/s)"
+UNIT = "KV tok/s"
+WORKLOAD = "llama7b-layer-verify-8k"
+
+
+# --------------------------------------------------------------------------------------
+# workload
+# --------------------------------------------------------------------------------------
+
+class Spec:
+    B, Hq, Hkv, D, G = 1, 32, 32, 128, 128
+    Lq = 8192
+    r0 = 2 * 128 - 4            # residual fill before the step: the append flushes a group
+    gamma = 8
+    P = 8                       # pending speculative tokens (all visible causally)
+    top_k = 64
+    n_accept = 8
+    copies = 4
+
+    @property
+    def n_prefill(self):
+        return self.Lq + self.r0
+
+    @property
+    def kv_tokens_per_step(self):
+        return self.B * (self.Lq + self.r0 + self.P)
+
+    def attend_bytes(self):
+        """Algorithmic bytes of the INT8 verify call: both nibble planes of
+        keys and values, key/value scale+zero, and the bf16 residual tokens."""
+        per_tok = 4 * self.D // 2 + 2 * self.D * 4 // self.G + 2 * 4 * (self.D // self.G)
+        return self.B * self.Hkv * (self.Lq * per_tok + self.r0 * 2 * self.D * 2)
+
+    def topk_bytes(self):
+        per_tok = self.D // 2 + 2 * self.D * 4 // self.G
+        return self.B * self.Hkv * self.Lq * per_tok
+
+
+def make_inputs(spec: Spec, seed: int = 0):
+    K, V = ki.kv_stream(seed, spec.B, spec.Hkv, spec.n_prefill + spec.n_accept, spec.D)
+    q = ki.queries(seed, spec.B, spec.gamma, spec.Hq, spec.D)
+    pk, pv = ki.pending(seed, spec.B, spec.Hkv, spec.P, spec.D)
+    return dict(K=K[:, :, :spec.n_prefill], V=V[:, :, :spec.n_prefill],
+                Knew=K[:, :, spec.n_prefill:], Vnew=V[:, :, spec.n_prefill:], q=q, pk=pk, pv=pv)
+
+
+# --------------------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------------------
+# device arm
+# --------------------------------------------------------------------------------------
+
+def run_device(args, rank, world):
+    import quantized_kv_speculative_gb300 as kvq
+    from quantized_kv_speculative_gb300 import _build
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    lib = kvq.load_library()
+    spec = Spec()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = make_inputs(spec)
+    up = lambda x: ki.f32_to_bf16_tensor(x, dev)
+    K, V = up(inp["K"]), up(inp["V"])
+    q, pk, pv = up(inp["q"]), up(inp["pk"]), up(inp["pv"])
+    kn, vn = up(inp["Knew"]), up(inp["Vnew"])
+    q_spec = q[:, -1].contiguous()
+    caches, wss = [], []
+    for _ in range(spec.copies):
+        c = kvq.QuantizedKVCache(spec.B, spec.Hkv, spec.D, spec.G, "hier8", spec.Lq + 2 * spec.G)
+        kvq.kvq_quantize_append(c, K, V)                      # bulk cache build (prefill)
+        caches.append(c)
+        wss.append(kvq.make_workspace(c, spec.Hq, spec.gamma, spec.top_k))
+    torch.cuda.synchronize()
+    assert caches[0].state() == (spec.Lq, spec.r0, 0), caches[0].state()
+    out = torch.empty_like(q)
+    lse = torch.empty((spec.B, spec.gamma, spec.Hq), dtype=torch.float32, device=dev)
+    idx = torch.empty((spec.B, spec.Hkv, spec.top_k), dtype=torch.int32, device=dev)
+    sc = torch.empty((spec.B, spec.Hkv, spec.top_k), dtype=torch.float32, device=dev)
+
+    def step(i, stream=None):
+        c = caches[i % spec.copies]
+        ws = wss[i % spec.copies]
+        st = c.state()
+        kvq.kvq_attend(c, "int8", q, pk, pv, out=out, lse=lse, workspace=ws, stream=stream)
+        kvq.kvq_topk(c, "int4", q_spec, spec.top_k, idx_out=idx, score_out=sc, workspace=ws, stream=stream)
+        kvq.kvq_quantize_append(c, kn, vn, stream=stream)
+        c.set_state(st)
+
+    launches_per_step = 4     # attend, top-k, flush, residual write
+    # warm-up eagerly (also sets kernel attributes outside any capture)
+    for i in range(max(args.warmup, spec.copies)):
+        step(i)
+    torch.cuda.synchronize()
+    for ws in wss:
+        assert kvq.kvq_workspace_status(ws) == 0
+
+    # one graph per cache copy
+    cap_stream = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(cap_stream):
+        for j in range(spec.copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap_stream):
+                step(j, stream=cap_stream)
+            graphs.append(g)
+    torch.cuda.synchronize()
+    for i in range(args.warmup):
+        graphs[i % spec.copies].replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record()
+    for i in range(args.steps):
+        graphs[i % spec.copies].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    value = spec.kv_tokens_per_step * world / (ms_step * 1e-3)
+
+    # ---- dominant kernel: INT8 verify attention, back-to-back launches ----
+    def per_call_ms(fn, reps=64, rounds=8):
+        gk = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap_stream):
+            with torch.cuda.graph(gk, stream=cap_stream):
+                for i in range(reps):
+                    fn(i, cap_stream)
+        torch.cuda.synchronize()
+        gk.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(rounds):
+            gk.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (reps * rounds)
+
+    def attend_only(i, s):
+        kvq.kvq_attend(caches[i % spec.copies], "int8", q, pk, pv, out=out, lse=lse,
+                       workspace=wss[i % spec.copies], stream=s)
+
+    def topk_only(i, s):
+        kvq.kvq_topk(caches[i % spec.copies], "int4", q_spec, spec.top_k, idx_out=idx, score_out=sc,
+                     workspace=wss[i % spec.copies], stream=s)
+
+    def append_only(i, s):
+        c = caches[i % spec.copies]
+        st = c.state()
+        kvq.kvq_quantize_append(c, kn, vn, stream=s)
+        c.set_state(st)
+
+    att_ms = per_call_ms(attend_only)
+    topk_ms = per_call_ms(topk_only)
+    app_ms = per_call_ms(append_only)
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured"
+    if not peak:
+        peak, peak_src = 6800.0, "fallback"
+    att_gbs = spec.attend_bytes() / (att_ms * 1e-3) / 1e9
+    traffic = measured_traffic()
+
+    # ---- e2e: public API with pinned host inputs and a host read of the results ----
+    h_q = torch.from_numpy(ki.to_bf16_bits(inp["q"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_pk = torch.from_numpy(ki.to_bf16_bits(inp["pk"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_pv = torch.from_numpy(ki.to_bf16_bits(inp["pv"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_kn = torch.from_numpy(ki.to_bf16_bits(inp["Knew"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_vn = torch.from_numpy(ki.to_bf16_bits(inp["Vnew"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_idx = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+    d_q, d_pk, d_pv, d_kn, d_vn = (torch.empty_like(x) for x in (q, pk, pv, kn, vn))
+    d_qs = torch.empty_like(q_spec)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_pk, h_pv, h_kn, h_vn))
+    d2h = h_out.numel() * h_out.element_size() + h_idx.numel() * h_idx.element_size()
+    n_e2e = max(10, min(args.steps, 400))
+
+    def e2e_step(i):
+        d_q.copy_(h_q, non_blocking=True)
+        d_pk.copy_(h_pk, non_blocking=True)
+        d_pv.copy_(h_pv, non_blocking=True)
+        d_kn.copy_(h_kn, non_blocking=True)
+        d_vn.copy_(h_vn, non_blocking=True)
+        d_qs.copy_(d_q[:, -1])
+        c = caches[i % spec.copies]
+        ws = wss[i % spec.copies]
+        st = c.state()
+        kvq.kvq_attend(c, "int8", d_q, d_pk, d_pv, out=out, lse=lse, workspace=ws)
+        kvq.kvq_topk(c, "int4", d_qs, spec.top_k, idx_out=idx, score_out=sc, workspace=ws)
+        kvq.kvq_quantize_append(c, d_kn, d_vn)
+        c.set_state(st)
+        h_out.copy_(out, non_blocking=True)
+        h_idx.copy_(idx, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for i in range(3):
+        e2e_step(i)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        e2e_step(i)
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    if world > 1:
+        tt = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    for ws in wss:
+        assert kvq.kvq_workspace_status(ws) == 0, "device status word set"
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8 codes, f16 mma / fp32 accumulate, bf16 io",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/Q, 4 of 128 key channels x8 per head)",
+        "config": {"workload": WORKLOAD, "batch": spec.B, "q_heads": spec.Hq, "kv_heads": spec.Hkv,
+                   "head_dim": spec.D, "group": spec.G, "quantized_tokens": spec.Lq, "residual_tokens": spec.r0,
+                   "gamma": spec.gamma, "pending": spec.P, "top_k": spec.top_k, "append_per_step": spec.n_accept,
+                   "step": "int8 verify attend + int4 top-k + quantize-append with one group flush",
+                   "timing": "CUDA graph per step, CUDA events over the K steps",
+                   "l2": f"rotating {spec.copies} cache copies of {spec.attend_bytes() / 1e6:.1f} MB each (> L2)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "calls": {"attend_int8_verify_ms": att_ms, "attend_gbs": att_gbs,
+                  "topk_int4_ms": topk_ms, "topk_gbs": spec.topk_bytes() / (topk_ms * 1e-3) / 1e9,
+                  "append_8_with_flush_ms": app_ms, "hbm_gbs_step": (spec.attend_bytes() + spec.topk_bytes()) / (ms_step * 1e-3) / 1e9},
+        "roofline": {"kernel": "attend_kernel<INT8,128,1> (verify, gamma=8)", "bound": "hbm", "achieved": att_gbs,
+                     "peak": peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s", "frac": att_gbs / peak,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": spec.attend_bytes(),
+                     "timing": "64 back-to-back launches over 4 rotating caches, CUDA events"},
+        "e2e": {"value": spec.kv_tokens_per_step * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed": wall,
+    }
+    return result, spec, inp
+
+
+# --------------------------------------------------------------------------------------
+# oracle (CPU) arm
+# --------------------------------------------------------------------------------------
+
+def kernel_source_hash() -> str:
+    """sha256 over the sources the attention kernel is built from."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("kvq_attend.cu", "kvq_modes.cuh", "kvq_device.cuh", "kvq_internal.h"):
+        h.update(open(os.path.join(ROOT, "quantized_kv_speculative_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def measured_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None if there is none or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", "attend_int8_verify_8k.json")
+    try:
+        rec = json.load(open(path))
+    except Exception:
+        return None
+    if rec.get("source_sha256") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class OracleSample:
+    """The CPU oracle on a bounded sample of the workload: every query row of a
+    few KV heads, over the first ``lq`` quantized tokens of the same context plus
+    the residual and pending tokens, then their top-k and the 8-token append."""
+
+    def __init__(self, spec: Spec, inp, units=(0,), lq=None):
+        import oracle
+        self.oracle = oracle
+        self.spec = spec
+        self.units = list(units)
+        self.lq = spec.Lq if lq is None else lq
+        h = self.units
+        n = self.lq + spec.r0
+        self.c = oracle.OracleCache(1, len(h), spec.D, spec.G, "hier8", self.lq + 2 * spec.G)
+        self.c.append(inp["K"][:, h, :n], inp["V"][:, h, :n])
+        hg = spec.Hq // spec.Hkv
+        qh = [x for u in h for x in range(u * hg, (u + 1) * hg)]
+        self.q = inp["q"][:, :, qh]
+        self.pk, self.pv = inp["pk"][:, h], inp["pv"][:, h]
+        self.kn, self.vn = inp["Knew"][:, h], inp["Vnew"][:, h]
+
+    def run_once(self):
+        o = self.oracle
+        o.attend(self.c, "int8", self.q, self.pk, self.pv)
+        o.topk(self.c, "int4", self.q[:, -1], self.spec.top_k)
+        saved = (self.c.Lq, self.c.r, self.c.res_k.copy(), self.c.res_v.copy())
+        self.c.append(self.kn, self.vn)
+        self.c.Lq, self.c.r, self.c.res_k, self.c.res_v = saved
+
+    def kv_tok_per_s(self, seconds):
+        """KV tokens/s in the workload's units (one KV token = all B*Hkv heads):
+        unit-tokens processed by the sample / (B*Hkv) / time."""
+        unit_tokens = len(self.units) * (self.lq + self.spec.r0 + self.spec.P)
+        return unit_tokens / (self.spec.B * self.spec.Hkv) / seconds
+
+
+def cpu_baseline(spec, inp, budget_s=12.0):
+    s = OracleSample(spec, inp, units=(0,))
+    s.run_once()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        s.run_once()
+        n += 1
+        if time.perf_counter() - t0 >= budget_s or n >= 50:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": s.kv_tok_per_s(dt), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"1 of {spec.Hkv} KV heads: all {spec.gamma} query rows over the full context, its top-k "
+                      f"and 8-token append; {n} repetitions; numpy single-threaded; scaled by the head fraction"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    spec = Spec()
+    inp = make_inputs(spec)
+    s = OracleSample(spec, inp, units=(0,))
+    t0 = time.perf_counter()
+    s.run_once()
+    t_full = time.perf_counter() - t0
+    budget = 150.0
+    per_step = budget / max(1, args.steps + args.warmup)
+    if per_step < t_full:
+        lq = max(spec.G, int(spec.Lq * per_step / t_full) // spec.G * spec.G)
+        s = OracleSample(spec, inp, units=(0,), lq=lq)
+    for _ in range(args.warmup):
+        s.run_once()
+    times = []
+    t_start = time.perf_counter()
+    for i in range(args.steps):
+        t1 = time.perf_counter()
+        s.run_once()
+        times.append(time.perf_counter() - t1)
+        if time.perf_counter() - t_start > 1.3 * budget:
+            break
+    dt = sum(times) / len(times)
+    v = s.kv_tok_per_s(dt)
+    sample = (f"per step: 1 of {spec.Hkv} KV heads, all {spec.gamma} query rows over {s.lq} quantized "
+              f"+ {spec.r0} residual + {spec.P} pending tokens, its top-{spec.top_k} and the 8-token append; "
+              f"numpy single-threaded; tokens scaled to the workload's KV-token unit")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 0,
+            "steps": len(times), "steps_requested": args.steps, "warmup": args.warmup,
+            "ms_per_step": spec.kv_tokens_per_step / v * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 quantizer, f64 attention", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# --------------------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    res, spec, inp = run_device(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(spec, inp)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

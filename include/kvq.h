@@ -1,0 +1,250 @@
+/*
+ * kvq.h: C ABI of the GB300 quantized-KV speculative decode-attention library.
+ *
+ * The library computes the data-parallel hot path shared by three methods:
+ *   - QuantSpec (QuantSpec: Self-Speculative Decoding with Hierarchical Quantized
+ *     KV Cache, "Approach"): a hierarchical 4-bit/8-bit KV cache in which the upper
+ *     4 bits are the INT4 draft cache and upper+lower 4 bits rebuild the INT8
+ *     target cache, plus a double full-precision buffer of 2G recent tokens;
+ *   - SpeCache (SpeCache: Speculative Key-Value Caching for Efficient Generation of
+ *     LLMs, "Approach"): a 1/2-bit KIVI copy of the KV cache on the GPU, a
+ *     speculative token decoded with the output token, and the top-k KV pairs it
+ *     predicts, used at 16 bits at the next step;
+ *   - MSpecKV (project page, abstract): quantized storage of KV and reconstruction
+ *     of only the needed subsets.
+ *
+ * Entry points: kvq_quantize_append (quantize + append), kvq_attend (fused
+ * dequantization + split-K flash-decoding attention with a fused combine) and
+ * kvq_topk (per-KV-head top-k under the low-bit keys).
+ *
+ * Conventions shared by every call:
+ *   - Ownership.  The caller owns every buffer: the cache memory handed to
+ *     kvq_cache_init, inputs, outputs and the workspace.  The library allocates
+ *     no memory.  The only state it keeps is the tuning constants in its code.
+ *     A kvq_cache is plain host memory owned by the caller.  It holds device
+ *     pointers plus the host-side counters (quantized length, residual fill,
+ *     residual start), and kvq_quantize_append updates those counters.
+ *   - Asynchrony.  Every call that takes a stream only enqueues work on that
+ *     stream (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *     None of them synchronizes the device.  Argument errors are returned
+ *     before any launch and change nothing.
+ *   - Device errors.  Kernels never trap or spin without a bound.  Every wait on
+ *     an mbarrier gives up after a bounded time.  A kernel that gives up writes
+ *     KVQ_ERR_DEVICE_TIMEOUT into the workspace status word, drains its own
+ *     in-flight copies and returns.  kvq_workspace_status reads that word.
+ *   - Launch errors are returned as KVQ_ERR_CUDA (from cudaGetLastError).
+ *   - Alignment.  Every device pointer must be 16-byte aligned.  The cache memory
+ *     must be 256-byte aligned.
+ *   - Element types.  bf16 for keys, values and queries (raw 16-bit patterns),
+ *     fp32 for scales, zero points, scores and log-sum-exp, int32 for indices.
+ *   - Shapes.  head_dim D in {64, 128}.  Group size G in {32, 64, 128} with G
+ *     dividing D.  Every sequence of a batch has the same lengths.
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* kvq_stream_t; /* a cudaStream_t */
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad shape or count */
+  KVQ_ERR_UNSUPPORTED = 2,    /* valid but not built: mode vs format, rows > 8, ... */
+  KVQ_ERR_CAPACITY = 3,       /* the append would exceed the quantized capacity */
+  KVQ_ERR_WORKSPACE = 4,      /* workspace missing or too small */
+  KVQ_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed */
+  KVQ_ERR_DEVICE_TIMEOUT = 6, /* a kernel gave up a bounded wait (see above) */
+  KVQ_ERR_NOT_INITIALIZED = 7 /* the cache struct was not set up by kvq_cache_init */
+} kvq_status;
+
+/* Storage format of the quantized cache. */
+typedef enum kvq_format {
+  KVQ_FMT_HIER8 = 8, /* hierarchical INT8: upper and lower nibble planes (QuantSpec) */
+  KVQ_FMT_INT2 = 2,  /* 2-bit KIVI codes (SpeCache)                                 */
+  KVQ_FMT_INT1 = 1   /* 1-bit KIVI codes (SpeCache)                                 */
+} kvq_format;
+
+/* Read mode of attention / top-k.  INT8 and INT4 read KVQ_FMT_HIER8: INT8 both
+ * nibble planes, INT4 only the upper plane, with scale x16.  So INT4 dequant
+ * equals INT8 dequant with the lower nibble zeroed.  INT2 and INT1 read their
+ * own format.  Any other pairing returns KVQ_ERR_UNSUPPORTED. */
+typedef enum kvq_mode {
+  KVQ_MODE_INT8 = 0,
+  KVQ_MODE_INT4 = 1,
+  KVQ_MODE_INT2 = 2,
+  KVQ_MODE_INT1 = 3
+} kvq_mode;
+
+typedef struct kvq_cache_desc {
+  int32_t batch;           /* B  >= 1                                             */
+  int32_t num_kv_heads;    /* Hkv >= 1                                            */
+  int32_t head_dim;        /* D  in {64, 128}                                     */
+  int32_t group_size;      /* G  in {32, 64, 128}, G divides D                    */
+  int32_t format;          /* kvq_format                                          */
+  int32_t reserved0;       /* must be 0                                           */
+  int64_t capacity_tokens; /* C: max quantized tokens per sequence, multiple of G */
+} kvq_cache_desc;
+
+/*
+ * One layer's cache.  Device layout, all regions inside the caller's memory at
+ * 256-byte aligned offsets, with u = b*Hkv + kvh:
+ *
+ *  key planes    [u][C][D*pb/8] u8, token-major.  Byte j of token row t packs
+ *                channels (8/pb)*j + e at bits [pb*e, pb*e+pb).  For HIER8 there
+ *                are two planes with pb = 4: upper nibbles (INT4 draft code) and
+ *                lower nibbles.  For INT2 and INT1 there is one plane with
+ *                pb = 2 or 1.
+ *  value planes  [u][C/32][D][32*pb/8] u8, in 32-token slabs.  Slab s, row d
+ *                holds the codes of channel d for tokens 32s..32s+31.  Byte j
+ *                packs tokens 32s + (8/pb)*j + e at bits [pb*e, pb*e+pb).  Same
+ *                planes as the keys.
+ *  key scale/zero   [u][C/G][2][D] f32: per (token group, channel), scale row
+ *                   then zero-point row.
+ *  value scale/zero [u][C][2][D/G] f32: per (token, block of G channels),
+ *                   scales then zero points.
+ *  residual K, V [u][2G][D] bf16: the double buffer of recent tokens.  The r
+ *                live tokens sit in slots (residual_start + i) mod 2G, i in [0, r),
+ *                oldest first.  residual_start is 0 or G.  At a flush the older
+ *                half is quantized in place, and the other half becomes the
+ *                oldest.
+ *
+ * Codes (KIVI-style asymmetric min/max, fp32, round-half-even): scale =
+ * (max - min)/(2^b - 1), code = clamp(rint((x - min) * (1/scale)), 0, 2^b - 1),
+ * with zero point = min.  A constant group gets scale 0 and codes 0.  Keys are
+ * grouped per channel over G tokens, values per token over G channels.
+ */
+typedef struct kvq_cache {
+  kvq_cache_desc desc;
+  void* base;                 /* caller's device memory                            */
+  uint64_t bytes;             /* its size                                          */
+  uint64_t off_k_plane[2];    /* key planes: [0] upper/only, [1] lower (HIER8)     */
+  uint64_t off_v_plane[2];    /* value planes, same order                          */
+  uint64_t off_k_sz;          /* key scale/zero                                    */
+  uint64_t off_v_sz;          /* value scale/zero                                  */
+  uint64_t off_res_k;         /* residual keys                                     */
+  uint64_t off_res_v;         /* residual values                                   */
+  int64_t quantized_len;      /* Lq: quantized tokens per sequence (multiple of G) */
+  int32_t residual_len;       /* r: live residual tokens, 0 <= r < 2G              */
+  int32_t residual_start;     /* 0 or G                                            */
+  uint32_t magic;             /* set by kvq_cache_init                             */
+  uint32_t reserved1;
+} kvq_cache;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* kvq_status_string(kvq_status s);
+
+/* Bytes of device memory a cache with this descriptor needs (0 if the descriptor
+ * is invalid). */
+size_t kvq_cache_bytes(const kvq_cache_desc* desc);
+
+/* Lay out a cache in caller memory `dev_mem` (>= kvq_cache_bytes, 256-B aligned)
+ * and set it empty (Lq = r = 0).  Writes only the host struct: the device
+ * memory's contents are ignored until written by kvq_quantize_append. */
+kvq_status kvq_cache_init(kvq_cache* cache, const kvq_cache_desc* desc, void* dev_mem,
+                          size_t bytes);
+
+/*
+ * Append n_new tokens of every sequence.  k_new and v_new are bf16
+ * [B][Hkv][n_new][D], contiguous, on the device.
+ *
+ * The double full-precision buffer (QuantSpec page, "Approach") works token by
+ * token.  The token goes to residual slot r and r += 1.  When r reaches 2G, the
+ * oldest G residual tokens are quantized as token group [Lq, Lq+G), Lq += G and
+ * r = G.  After N tokens from empty: Lq = G*(floor(N/G) - 1) once N >= 2G.  A
+ * multi-token call gives the same bytes as n single-token calls.  All complete
+ * groups are quantized in one launch, which is the bulk path for a prefill.
+ * Speculative tokens never enter the cache: pass them to kvq_attend as pending
+ * tokens, and append only the accepted ones, so rollback needs no undo.
+ *
+ * Capacity is checked before anything is enqueued (KVQ_ERR_CAPACITY).  Enqueues
+ * at most two kernels.  The host counters are updated at once, so later calls
+ * on the same stream see the new state.
+ */
+kvq_status kvq_quantize_append(kvq_cache* cache, const void* k_new, const void* v_new,
+                               int32_t n_new, kvq_stream_t stream);
+
+/* Bytes of workspace that kvq_attend / kvq_topk need for this cache, at any fill
+ * up to capacity.  Rows per KV head R = gamma * num_q_heads / num_kv_heads must be
+ * <= 8.  top_k <= 1024.  The workspace must be zero-filled once before its first
+ * use.  Every call that finishes leaves it reusable.  Returns 0 for invalid
+ * arguments. */
+size_t kvq_workspace_bytes(const kvq_cache* cache, int32_t num_q_heads, int32_t gamma,
+                           int32_t top_k);
+
+/*
+ * Decode attention of gamma query tokens over the cache (QuantSpec page,
+ * "Approach": the draft reads INT4, the target verifies with INT8; SpeCache page,
+ * "Approach": attention over the low-bit copy, with the top-k tokens at 16 bits).
+ *
+ *  q        bf16 [B][gamma][Hq][D].  Query head h reads KV head h / (Hq/Hkv).
+ *  pend_k/v bf16 [B][Hkv][n_pend][D]: speculative tokens not yet committed.
+ *           Query token i sees pending token p iff p <= n_pend - gamma + i (the
+ *           gamma queries are the last gamma pending tokens).  n_pend = 0 means no
+ *           pending tokens (pointers may be NULL).  Otherwise n_pend >= gamma.
+ *  sel_idx  int32 [B][Hkv][top_k], sel_k/v bf16 [B][Hkv][top_k][D].  An entry
+ *           with 0 <= idx < Lq replaces quantized token idx by the given 16-bit
+ *           key and value.  Other entries are ignored (-1 pads).  Valid entries
+ *           of a (b, kvh) must be distinct.  top_k = 0 means none (NULL allowed).
+ *  sm_scale logits are sm_scale * q.k.  A value <= 0 selects 1/sqrt(D).
+ *  out      bf16 [B][gamma][Hq][D] (written).
+ *  lse      fp32 [B][gamma][Hq] natural-log softmax denominators, or NULL.  A
+ *           query that sees no key gets out = 0 and lse = -inf.
+ *  Every residual token is visible to every query.  Results do not depend on
+ *  how the work is split.
+ * Enqueues one kernel.  It splits the quantized context over CTAs, runs one
+ * extra CTA per (b, kvh) for the bf16 tail, and merges the partials in whichever
+ * CTA of each (b, kvh) finishes last.
+ */
+kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int32_t num_q_heads,
+                      int32_t gamma, const void* pend_k, const void* pend_v, int32_t n_pend,
+                      const int32_t* sel_idx, const void* sel_k, const void* sel_v, int32_t top_k,
+                      float sm_scale, void* out, float* lse, void* workspace, size_t ws_bytes,
+                      kvq_stream_t stream);
+
+/*
+ * Per KV head, the top_k quantized tokens that score highest under the
+ * low-bit keys for the speculative token's query (SpeCache page, "Approach").
+ * The query heads sharing a KV head are summed in fp32, in ascending head order.
+ * Per key group g the score is exact up to stated roundings:
+ *   w_d = fp32(qs_d * s_d)   (s = the mode's key scale: x16 for INT4)
+ *   e   = exponent with max_d|w_d| < 2^e, floored at -100
+ *   W_d = rint(w_d * 2^(21-e)),  S_t = sum_d W_d * code_{t,d} (exact integer)
+ *   beta = pairwise-tree sum of 32 channel-chunk partial sums, each a
+ *          sequential fp32 sum of fp32(qs_d * zero_d)
+ *   score_t = fp32(fp32(fp32(S_t) * 2^(e-21)) + beta)
+ * Tokens are ordered by (score descending, index ascending).  Positions beyond
+ * Lq get index -1 and score -inf.
+ *  mode     KVQ_MODE_INT4, INT2 or INT1 (INT8 returns KVQ_ERR_UNSUPPORTED).
+ *  q_spec   bf16 [B][Hq][D].
+ *  idx_out  int32 [B][Hkv][top_k], in that order.  score_out fp32, same shape,
+ *           or NULL.
+ *  1 <= top_k <= 1024.  Enqueues one kernel.
+ */
+kvq_status kvq_topk(const kvq_cache* cache, kvq_mode mode, const void* q_spec,
+                    int32_t num_q_heads, int32_t top_k, int32_t* idx_out, float* score_out,
+                    void* workspace, size_t ws_bytes, kvq_stream_t stream);
+
+/* Synchronously read (and then clear) the device status word of a workspace:
+ * KVQ_OK, or KVQ_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait since the
+ * last read.  Synchronizes `stream`. */
+kvq_status kvq_workspace_status(void* workspace, size_t ws_bytes, kvq_stream_t stream);
+
+/* Self-test of the bounded-wait path.  Launches one CTA that waits on an
+ * mbarrier that nothing ever arrives at, with a limit of `limit_cycles` SM
+ * clocks (1..2^31).  On giving up it records KVQ_ERR_DEVICE_TIMEOUT in the
+ * workspace status word and returns, so kvq_workspace_status then reports
+ * it.  It neither traps nor hangs. */
+kvq_status kvq_selftest_bounded_wait(void* workspace, size_t ws_bytes, int64_t limit_cycles,
+                                     kvq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

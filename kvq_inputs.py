@@ -187,3 +187,44 @@ WORKLOADS = {
 
 # Single-layer INT4 draft-attention sweep over context lengths (gamma = 1).
 SWEEP_CONTEXTS = (8192, 16384, 32768, 65536, 131072, 262144)
+
+
+# --------------------------------------------------------------------------------
+# Device-side draws for the large workloads (seeded torch generator on the GPU).
+# The oracle side downloads the slices it needs; those are inputs, not results.
+# --------------------------------------------------------------------------------
+
+
+def kv_stream_torch(seed: int, batch: int, num_kv_heads: int, n_tokens: int, head_dim: int,
+                    outlier_channels: int = 4, outlier_gain: float = 8.0, device="cuda"):
+    """bf16 ``[B, Hkv, N, D]`` keys and values ~ N(0,1) drawn on ``device``.  A
+    seeded set of ``outlier_channels`` key channels per (b, kv head) is scaled by
+    ``outlier_gain``."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    shape = (batch, num_kv_heads, n_tokens, head_dim)
+    k = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    v = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    if outlier_channels > 0:
+        cpu = np.random.Generator(np.random.PCG64([seed, 77]))
+        gain = torch.ones((batch, num_kv_heads, 1, head_dim), device=device)
+        for b in range(batch):
+            for h in range(num_kv_heads):
+                ch = cpu.choice(head_dim, size=outlier_channels, replace=False)
+                gain[b, h, 0, torch.as_tensor(ch, device=device)] = outlier_gain
+        k.mul_(gain)
+    return k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
+def bf16_tensor_to_f32(t) -> np.ndarray:
+    """Download a bf16 torch tensor as float32 numpy (exact widening)."""
+    import torch
+    return t.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16).astype(np.uint32).__lshift__(16).view(np.float32)
+
+
+def f32_to_bf16_tensor(x: np.ndarray, device="cuda"):
+    """Upload bf16-valued float32 numpy data as a bf16 torch tensor."""
+    import torch
+    bits = to_bf16_bits(x)
+    return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(device)

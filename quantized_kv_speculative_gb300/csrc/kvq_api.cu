@@ -1,0 +1,402 @@
+// Host side of the C ABI declared in include/kvq.h: argument validation, the
+// 2G double-buffer state machine, split sizing, workspace layout and launches.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "kvq_internal.h"
+
+using namespace kvq;
+
+namespace {
+
+constexpr uint32_t kMagic = 0x4B565131u;  // "KVQ1"
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_desc(const kvq_cache_desc* d) {
+  if (!d) return false;
+  if (d->batch < 1 || d->num_kv_heads < 1) return false;
+  if (d->head_dim != 64 && d->head_dim != 128) return false;
+  if (d->group_size != 32 && d->group_size != 64 && d->group_size != 128) return false;
+  if (d->head_dim % d->group_size) return false;
+  if (d->format != KVQ_FMT_HIER8 && d->format != KVQ_FMT_INT2 && d->format != KVQ_FMT_INT1) return false;
+  if (d->reserved0 != 0) return false;
+  if (d->capacity_tokens < 0 || d->capacity_tokens % d->group_size) return false;
+  if (d->capacity_tokens > (1LL << 30)) return false;
+  const long long units = static_cast<long long>(d->batch) * d->num_kv_heads;
+  if (units > (1LL << 24)) return false;
+  return true;
+}
+
+struct Regions {
+  int np;
+  size_t k_plane, v_plane, k_sz, v_sz, res, total;
+};
+
+Regions regions(const kvq_cache_desc* d) {
+  Regions r{};
+  const size_t U = static_cast<size_t>(d->batch) * d->num_kv_heads;
+  const size_t C = static_cast<size_t>(d->capacity_tokens);
+  const size_t D = d->head_dim, G = d->group_size;
+  const size_t pb = (d->format == KVQ_FMT_HIER8) ? 4 : static_cast<size_t>(d->format);
+  r.np = (d->format == KVQ_FMT_HIER8) ? 2 : 1;
+  r.k_plane = align256(U * C * D * pb / 8);
+  r.v_plane = align256(U * C * D * pb / 8);
+  r.k_sz = align256(U * (C / G) * 2 * D * 4);
+  r.v_sz = align256(U * C * 2 * (D / G) * 4);
+  r.res = align256(U * 2 * G * D * 2);
+  r.total = r.np * (r.k_plane + r.v_plane) + r.k_sz + r.v_sz + 2 * r.res;
+  return r;
+}
+
+bool cache_ok(const kvq_cache* c) { return c && c->magic == kMagic && valid_desc(&c->desc); }
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+long long units_of(const kvq_cache* c) {
+  return static_cast<long long>(c->desc.batch) * c->desc.num_kv_heads;
+}
+
+// Quantized splits per (b, kvh) for attention, and the chunk size.
+int attend_splits(long long Lq, long long U, long long* chunk) {
+  if (Lq <= 0) {
+    *chunk = 0;
+    return 0;
+  }
+  const long long target = std::max(1LL, ceil_div(kTargetCtas, U));
+  long long S = std::min(ceil_div(Lq, kChunkAlign), target);
+  S = std::max(S, ceil_div(Lq, kMaxChunk));
+  S = std::max(S, 1LL);
+  long long ch = ceil_div(ceil_div(Lq, S), kChunkAlign) * kChunkAlign;
+  *chunk = ch;
+  return static_cast<int>(ceil_div(Lq, ch));
+}
+
+int attend_splits_max(const kvq_cache_desc* d) {
+  const long long U = static_cast<long long>(d->batch) * d->num_kv_heads;
+  const long long Lq = d->capacity_tokens;
+  if (Lq <= 0) return 0;
+  const long long target = std::max(1LL, ceil_div(kTargetCtas, U));
+  long long S = std::min(ceil_div(Lq, kChunkAlign), target);
+  S = std::max(S, ceil_div(Lq, kMaxChunk));
+  return static_cast<int>(std::max(S, 1LL));
+}
+
+int topk_splits(long long Lq, long long U, long long* chunk) {
+  if (Lq <= 0) {
+    *chunk = 0;
+    return 1;
+  }
+  const long long target = std::max(1LL, ceil_div(kTargetCtas, U));
+  long long S = std::min(ceil_div(Lq, 512), target);
+  S = std::max(S, ceil_div(Lq, kTopkMaxChunk));
+  S = std::max(S, 1LL);
+  long long ch = ceil_div(ceil_div(Lq, S), kChunkAlign) * kChunkAlign;
+  *chunk = ch;
+  return static_cast<int>(ceil_div(Lq, ch));
+}
+
+int topk_splits_max(const kvq_cache_desc* d) {
+  const long long U = static_cast<long long>(d->batch) * d->num_kv_heads;
+  const long long Lq = d->capacity_tokens;
+  if (Lq <= 0) return 1;
+  const long long target = std::max(1LL, ceil_div(kTargetCtas, U));
+  long long S = std::min(ceil_div(Lq, 512), target);
+  S = std::max(S, ceil_div(Lq, kTopkMaxChunk));
+  return static_cast<int>(std::max(S, 1LL));
+}
+
+size_t attend_ws_bytes(const kvq_cache_desc* d) {
+  const size_t U = static_cast<size_t>(d->batch) * d->num_kv_heads;
+  const size_t S = static_cast<size_t>(attend_splits_max(d)) + 1;
+  return align256(U * 4) + align256(U * S * kPartialFloats(d->head_dim) * 4);
+}
+
+size_t topk_ws_bytes(const kvq_cache_desc* d, int k) {
+  const size_t U = static_cast<size_t>(d->batch) * d->num_kv_heads;
+  const size_t S = static_cast<size_t>(topk_splits_max(d));
+  return align256(U * 4) + 2 * align256(U * S * static_cast<size_t>(k) * 4);
+}
+
+CacheView view_of(const kvq_cache* c) {
+  CacheView v{};
+  uint8_t* base = static_cast<uint8_t*>(c->base);
+  v.kplane[0] = base + c->off_k_plane[0];
+  v.kplane[1] = base + c->off_k_plane[1];
+  v.vplane[0] = base + c->off_v_plane[0];
+  v.vplane[1] = base + c->off_v_plane[1];
+  v.ksz = reinterpret_cast<const float*>(base + c->off_k_sz);
+  v.vsz = reinterpret_cast<const float*>(base + c->off_v_sz);
+  v.res_k = reinterpret_cast<const uint16_t*>(base + c->off_res_k);
+  v.res_v = reinterpret_cast<const uint16_t*>(base + c->off_res_v);
+  v.B = c->desc.batch;
+  v.Hkv = c->desc.num_kv_heads;
+  v.D = c->desc.head_dim;
+  v.G = c->desc.group_size;
+  v.fmt = c->desc.format;
+  v.C = c->desc.capacity_tokens;
+  v.Lq = c->quantized_len;
+  v.r = c->residual_len;
+  v.res_start = c->residual_start;
+  return v;
+}
+
+bool mode_reads(int mode, int fmt) {
+  switch (mode) {
+    case KVQ_MODE_INT8:
+    case KVQ_MODE_INT4: return fmt == KVQ_FMT_HIER8;
+    case KVQ_MODE_INT2: return fmt == KVQ_FMT_INT2;
+    case KVQ_MODE_INT1: return fmt == KVQ_FMT_INT1;
+    default: return false;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVQ_ERR_CAPACITY: return "quantized capacity exceeded";
+    case KVQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case KVQ_ERR_NOT_INITIALIZED: return "cache not initialized";
+    default: return "unknown status";
+  }
+}
+
+size_t kvq_cache_bytes(const kvq_cache_desc* desc) {
+  if (!valid_desc(desc)) return 0;
+  return regions(desc).total;
+}
+
+kvq_status kvq_cache_init(kvq_cache* cache, const kvq_cache_desc* desc, void* dev_mem, size_t bytes) {
+  if (!cache || !valid_desc(desc)) return KVQ_ERR_INVALID_ARG;
+  const Regions r = regions(desc);
+  if (r.total > 0 && (!dev_mem || (reinterpret_cast<uintptr_t>(dev_mem) & 255u))) return KVQ_ERR_INVALID_ARG;
+  if (bytes < r.total) return KVQ_ERR_INVALID_ARG;
+  std::memset(cache, 0, sizeof(*cache));
+  cache->desc = *desc;
+  cache->base = dev_mem;
+  cache->bytes = bytes;
+  uint64_t off = 0;
+  cache->off_k_plane[0] = off; off += r.k_plane;
+  cache->off_k_plane[1] = (r.np == 2) ? off : cache->off_k_plane[0];
+  if (r.np == 2) off += r.k_plane;
+  cache->off_v_plane[0] = off; off += r.v_plane;
+  cache->off_v_plane[1] = (r.np == 2) ? off : cache->off_v_plane[0];
+  if (r.np == 2) off += r.v_plane;
+  cache->off_k_sz = off; off += r.k_sz;
+  cache->off_v_sz = off; off += r.v_sz;
+  cache->off_res_k = off; off += r.res;
+  cache->off_res_v = off; off += r.res;
+  cache->quantized_len = 0;
+  cache->residual_len = 0;
+  cache->residual_start = 0;
+  cache->magic = kMagic;
+  return KVQ_OK;
+}
+
+kvq_status kvq_quantize_append(kvq_cache* cache, const void* k_new, const void* v_new, int32_t n_new,
+                               kvq_stream_t stream) {
+  if (!cache || cache->magic != kMagic) return KVQ_ERR_NOT_INITIALIZED;
+  if (!valid_desc(&cache->desc)) return KVQ_ERR_INVALID_ARG;
+  if (n_new < 0) return KVQ_ERR_INVALID_ARG;
+  if (n_new == 0) return KVQ_OK;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
+  const int G = cache->desc.group_size;
+  const long long r = cache->residual_len;
+  const long long T = r + n_new;
+  const long long f = (T < 2LL * G) ? 0 : T / G - 1;
+  if (cache->quantized_len + f * G > cache->desc.capacity_tokens) return KVQ_ERR_CAPACITY;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(cache->base);
+  if (f > 0) {
+    FlushParams p{};
+    p.kplane[0] = base + cache->off_k_plane[0];
+    p.kplane[1] = base + cache->off_k_plane[1];
+    p.vplane[0] = base + cache->off_v_plane[0];
+    p.vplane[1] = base + cache->off_v_plane[1];
+    p.ksz = reinterpret_cast<float*>(base + cache->off_k_sz);
+    p.vsz = reinterpret_cast<float*>(base + cache->off_v_sz);
+    p.res_k = reinterpret_cast<const uint16_t*>(base + cache->off_res_k);
+    p.res_v = reinterpret_cast<const uint16_t*>(base + cache->off_res_v);
+    p.k_new = static_cast<const uint16_t*>(k_new);
+    p.v_new = static_cast<const uint16_t*>(v_new);
+    p.B = cache->desc.batch;
+    p.Hkv = cache->desc.num_kv_heads;
+    p.D = cache->desc.head_dim;
+    p.G = G;
+    p.fmt = cache->desc.format;
+    p.C = cache->desc.capacity_tokens;
+    p.Lq = cache->quantized_len;
+    p.r = static_cast<int>(r);
+    p.res_start = cache->residual_start;
+    p.n = n_new;
+    p.nflush = static_cast<int>(f);
+    if (launch_flush(p, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  }
+  const long long first_new = std::max(r, f * G);
+  const long long count = T - first_new;
+  if (count > 0) {
+    ResidualWriteParams w{};
+    w.res_k = reinterpret_cast<uint16_t*>(base + cache->off_res_k);
+    w.res_v = reinterpret_cast<uint16_t*>(base + cache->off_res_v);
+    w.k_new = static_cast<const uint16_t*>(k_new);
+    w.v_new = static_cast<const uint16_t*>(v_new);
+    w.B = cache->desc.batch;
+    w.Hkv = cache->desc.num_kv_heads;
+    w.D = cache->desc.head_dim;
+    w.G = G;
+    w.n = n_new;
+    w.r = static_cast<int>(r);
+    w.res_start = cache->residual_start;
+    w.first_new = static_cast<int>(first_new);
+    w.count = static_cast<int>(count);
+    if (launch_residual_write(w, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  }
+  cache->quantized_len += f * G;
+  cache->residual_len = static_cast<int32_t>(T - f * G);
+  cache->residual_start = static_cast<int32_t>((cache->residual_start + f * G) % (2 * G));
+  return KVQ_OK;
+}
+
+size_t kvq_workspace_bytes(const kvq_cache* cache, int32_t num_q_heads, int32_t gamma, int32_t top_k) {
+  if (!cache_ok(cache)) return 0;
+  const int Hkv = cache->desc.num_kv_heads;
+  if (num_q_heads < Hkv || num_q_heads % Hkv) return 0;
+  if (gamma < 1 || static_cast<long long>(gamma) * (num_q_heads / Hkv) > kMaxRows) return 0;
+  if (top_k < 0 || top_k > kMaxTopk) return 0;
+  return kStatusBytes + attend_ws_bytes(&cache->desc) + topk_ws_bytes(&cache->desc, std::max(top_k, 1));
+}
+
+kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int32_t num_q_heads,
+                      int32_t gamma, const void* pend_k, const void* pend_v, int32_t n_pend,
+                      const int32_t* sel_idx, const void* sel_k, const void* sel_v, int32_t top_k,
+                      float sm_scale, void* out, float* lse, void* workspace, size_t ws_bytes,
+                      kvq_stream_t stream) {
+  if (!cache || cache->magic != kMagic) return KVQ_ERR_NOT_INITIALIZED;
+  if (!valid_desc(&cache->desc)) return KVQ_ERR_INVALID_ARG;
+  if (!mode_reads(mode, cache->desc.format)) return KVQ_ERR_UNSUPPORTED;
+  const int Hkv = cache->desc.num_kv_heads;
+  if (num_q_heads < Hkv || num_q_heads % Hkv || gamma < 1) return KVQ_ERR_INVALID_ARG;
+  const int HG = num_q_heads / Hkv;
+  if (static_cast<long long>(gamma) * HG > kMaxRows) return KVQ_ERR_UNSUPPORTED;
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return KVQ_ERR_INVALID_ARG;
+  if (n_pend < 0) return KVQ_ERR_INVALID_ARG;
+  if (n_pend > 0 && (n_pend < gamma || !pend_k || !pend_v || !aligned16(pend_k) || !aligned16(pend_v)))
+    return KVQ_ERR_INVALID_ARG;
+  if (top_k < 0 || top_k > kMaxTopk) return KVQ_ERR_INVALID_ARG;
+  if (top_k > 0 && (!sel_idx || !sel_k || !sel_v || !aligned16(sel_idx) || !aligned16(sel_k) ||
+                    !aligned16(sel_v)))
+    return KVQ_ERR_INVALID_ARG;
+  const size_t need = kStatusBytes + attend_ws_bytes(&cache->desc);
+  if (!workspace || !aligned16(workspace) || ws_bytes < need) return KVQ_ERR_WORKSPACE;
+  if (!(sm_scale > 0.f)) sm_scale = 1.0f / std::sqrt(static_cast<float>(cache->desc.head_dim));
+
+  AttendParams p{};
+  p.c = view_of(cache);
+  p.q = static_cast<const uint16_t*>(q);
+  p.Hq = num_q_heads;
+  p.gamma = gamma;
+  p.HG = HG;
+  p.R = gamma * HG;
+  p.pend_k = static_cast<const uint16_t*>(pend_k);
+  p.pend_v = static_cast<const uint16_t*>(pend_v);
+  p.P = n_pend;
+  p.sel_idx = sel_idx;
+  p.sel_k = static_cast<const uint16_t*>(sel_k);
+  p.sel_v = static_cast<const uint16_t*>(sel_v);
+  p.top_k = top_k;
+  p.qscale = sm_scale * 1.4426950408889634f;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const long long U = units_of(cache);
+  p.status = reinterpret_cast<int*>(ws);
+  p.counters = reinterpret_cast<unsigned*>(ws + kStatusBytes);
+  p.partials = reinterpret_cast<float*>(ws + kStatusBytes + align256(U * 4));
+  long long chunk = 0;
+  p.S_q = attend_splits(cache->quantized_len, U, &chunk);
+  p.chunk = chunk;
+  p.wait_limit = kDefaultWaitLimit;
+  if (p.S_q > attend_splits_max(&cache->desc)) return KVQ_ERR_WORKSPACE;
+  if (launch_attend(p, mode, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_topk(const kvq_cache* cache, kvq_mode mode, const void* q_spec, int32_t num_q_heads,
+                    int32_t top_k, int32_t* idx_out, float* score_out, void* workspace, size_t ws_bytes,
+                    kvq_stream_t stream) {
+  if (!cache || cache->magic != kMagic) return KVQ_ERR_NOT_INITIALIZED;
+  if (!valid_desc(&cache->desc)) return KVQ_ERR_INVALID_ARG;
+  if (mode == KVQ_MODE_INT8) return KVQ_ERR_UNSUPPORTED;
+  if (!mode_reads(mode, cache->desc.format)) return KVQ_ERR_UNSUPPORTED;
+  const int Hkv = cache->desc.num_kv_heads;
+  if (num_q_heads < Hkv || num_q_heads % Hkv) return KVQ_ERR_INVALID_ARG;
+  if (top_k < 1 || top_k > kMaxTopk) return KVQ_ERR_INVALID_ARG;
+  if (!q_spec || !idx_out || !aligned16(q_spec) || !aligned16(idx_out)) return KVQ_ERR_INVALID_ARG;
+  if (score_out && !aligned16(score_out)) return KVQ_ERR_INVALID_ARG;
+  const size_t att = attend_ws_bytes(&cache->desc);
+  const size_t need = kStatusBytes + att + topk_ws_bytes(&cache->desc, top_k);
+  if (!workspace || !aligned16(workspace) || ws_bytes < need) return KVQ_ERR_WORKSPACE;
+  const long long U = units_of(cache);
+  long long chunk = 0;
+  const int S = topk_splits(cache->quantized_len, U, &chunk);
+  if (static_cast<long long>(S) * top_k > kTopkMaxCand) return KVQ_ERR_UNSUPPORTED;
+  TopkParams p{};
+  p.c = view_of(cache);
+  p.q = static_cast<const uint16_t*>(q_spec);
+  p.Hq = num_q_heads;
+  p.HG = num_q_heads / Hkv;
+  p.k = top_k;
+  p.idx_out = idx_out;
+  p.score_out = score_out;
+  uint8_t* ws = static_cast<uint8_t*>(workspace) + kStatusBytes + att;
+  p.status = static_cast<int*>(workspace);
+  p.counters = reinterpret_cast<unsigned*>(ws);
+  const size_t Smax = static_cast<size_t>(topk_splits_max(&cache->desc));
+  p.cand_score = reinterpret_cast<float*>(ws + align256(U * 4));
+  p.cand_idx = reinterpret_cast<int32_t*>(ws + align256(U * 4) + align256(U * Smax * top_k * 4));
+  p.S = S;
+  p.chunk = chunk;
+  p.wait_limit = kDefaultWaitLimit;
+  if (static_cast<size_t>(S) > Smax) return KVQ_ERR_WORKSPACE;
+  if (launch_topk(p, mode, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_workspace_status(void* workspace, size_t ws_bytes, kvq_stream_t stream) {
+  if (!workspace || ws_bytes < static_cast<size_t>(kStatusBytes)) return KVQ_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (word != 0) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KVQ_ERR_CUDA;
+  }
+  return static_cast<kvq_status>(word);
+}
+
+kvq_status kvq_selftest_bounded_wait(void* workspace, size_t ws_bytes, int64_t limit_cycles,
+                                     kvq_stream_t stream) {
+  if (!workspace || !aligned16(workspace) || ws_bytes < static_cast<size_t>(kStatusBytes))
+    return KVQ_ERR_WORKSPACE;
+  if (limit_cycles < 1 || limit_cycles > (1LL << 31)) return KVQ_ERR_INVALID_ARG;
+  if (launch_wait_selftest(static_cast<int*>(workspace), limit_cycles,
+                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,206 @@
+// Device-side building blocks shared by the kernels of this library:
+// mbarrier + 1-D bulk (TMA) copies, bounded waits, the m16n8k16 tensor-core
+// MMA, and the integer-code -> f16 conversions used for in-register
+// dequantization.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+
+// ------------------------------------------------------------------------------
+// Shared-memory addresses, mbarriers, bulk copies
+// ------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, giving up after
+// `limit` SM clocks.  Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > limit) return false;
+  }
+}
+
+// 1-D bulk copy global -> shared through the TMA unit, completing on `bar`.
+// dst, src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// ------------------------------------------------------------------------------
+// Tensor-core MMA: D[16x8] += A[16x16] (row) * B[16x8] (col), f16 in, f32 acc.
+//   a[0] = (row g,   k 2q..2q+1)   a[1] = (row g+8, k 2q..2q+1)
+//   a[2] = (row g,   k 2q+8..+9)   a[3] = (row g+8, k 2q+8..+9)
+//   b[0] = (k 2q..2q+1, col g)     b[1] = (k 2q+8..+9, col g)
+//   c[0..1] = (row g, col 2q..2q+1), c[2..3] = (row g+8, col 2q..2q+1)
+// with g = lane / 4, q = lane % 4; the lower half of a register is the lower
+// index.
+// ------------------------------------------------------------------------------
+
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------------------------
+// Code -> f16 conversion.  A b-bit code c placed in the top b mantissa bits of
+// an f16 whose exponent field encodes 1.0 gives exactly 1 + c / 2^b.  Two codes
+// that sit 16 bits apart in a 32-bit word become one half2 with one shift and
+// one LOP3.  The constant 1 is removed algebraically by the callers (weights
+// pre-scaled by 2^b and a per-row correction).
+// ------------------------------------------------------------------------------
+
+template <int SH>
+__device__ __forceinline__ uint32_t shl_signed(uint32_t x) {
+  if constexpr (SH >= 0) return x << SH;
+  else return x >> (-SH);
+}
+
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t x, uint32_t m, uint32_t c) {
+  uint32_t r;
+  // r = (x & m) | c
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(m), "r"(c));
+  return r;
+}
+
+constexpr uint32_t F16_ONE2 = 0x3C003C00u;
+
+// 4-bit codes: nibble i (bits 4i..4i+3) and nibble i+4 (bits 16+4i..) -> half2.
+template <int I>
+__device__ __forceinline__ uint32_t cvt4_pair(uint32_t w) {
+  return lop_and_or(shl_signed<6 - 4 * I>(w), 0x03C003C0u, F16_ONE2);
+}
+
+// 8-bit codes from an upper-nibble word H and a lower-nibble word L (same
+// positions): code = 16*hi + lo placed at mantissa bits 2..9.
+template <int I>
+__device__ __forceinline__ uint32_t cvt8_pair(uint32_t h, uint32_t l) {
+  const uint32_t t = lop_and_or(shl_signed<6 - 4 * I>(h), 0x03C003C0u, F16_ONE2);
+  return lop_and_or(shl_signed<2 - 4 * I>(l), 0x003C003Cu, t);
+}
+
+// 2-bit codes: code i (bits 2i..2i+1) and code i+8 (bits 16+2i..) -> half2.
+template <int I>
+__device__ __forceinline__ uint32_t cvt2_pair(uint32_t w) {
+  return lop_and_or(shl_signed<8 - 2 * I>(w), 0x03000300u, F16_ONE2);
+}
+
+// 1-bit codes: bit i and bit i+16 -> half2.
+template <int I>
+__device__ __forceinline__ uint32_t cvt1_pair(uint32_t w) {
+  return lop_and_or(shl_signed<9 - I>(w), 0x02000200u, F16_ONE2);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 unpack_half2(uint32_t v) {
+  __half2 h = *reinterpret_cast<__half2*>(&v);
+  return __half22float2(h);
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t v) {
+  return __uint_as_float(static_cast<uint32_t>(v) << 16);
+}
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+}  // namespace kvq
+
+namespace kvq {
+// Opt a kernel into more than 48 KB of dynamic shared memory, once per device
+// (also keeps the call out of CUDA-graph captures after the first launch).
+inline cudaError_t set_smem_once(const void* func, int bytes) {
+  constexpr int kMaxDev = 64;
+  static int done_bytes[kMaxDev][8] = {};
+  static const void* done_func[kMaxDev][8] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  for (int i = 0; i < 8; ++i) {
+    if (done_func[dev][i] == func && done_bytes[dev][i] >= bytes) return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < 8; ++i) {
+    if (done_func[dev][i] == nullptr || done_func[dev][i] == func) {
+      done_func[dev][i] = func;
+      done_bytes[dev][i] = bytes;
+      break;
+    }
+  }
+  return cudaSuccess;
+}
+}  // namespace kvq

@@ -1,0 +1,107 @@
+// Internal declarations shared by the host API (kvq_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kMaxRows = 8;            // rows (gamma x query heads per KV head) per kernel
+constexpr int kChunkAlign = 128;       // split boundaries are multiples of this many tokens
+constexpr int kMaxChunk = 32768;       // tokens per attention split (bounds the selection bitmap)
+constexpr int kTargetCtas = 608;       // 4 x 152 SMs: split-count target per launch
+constexpr int kTopkMaxChunk = 8192;    // tokens per top-k split (scores held in shared memory)
+constexpr int kTopkMaxCand = 4096;     // splits x k candidates merged by the last CTA
+constexpr int kMaxTopk = 1024;
+constexpr int kStatusBytes = 256;      // workspace header (status word)
+constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s at 2 GHz
+__host__ __device__ constexpr int kPartialFloats(int D) { return 2 * kMaxRows + kMaxRows * D; }
+
+// Device view of one cache (all pointers already offset to the regions).
+struct CacheView {
+  const uint8_t* kplane[2];
+  const uint8_t* vplane[2];
+  const float* ksz;   // [u][C/G][2][D]
+  const float* vsz;   // [u][C][2][D/G]
+  const uint16_t* res_k;  // [u][2G][D] bf16
+  const uint16_t* res_v;
+  int B, Hkv, D, G, fmt;
+  long long C;        // capacity tokens
+  long long Lq;
+  int r, res_start;
+};
+
+struct AttendParams {
+  CacheView c;
+  const uint16_t* q;        // [B][gamma][Hq][D]
+  int Hq, gamma, HG, R;
+  const uint16_t* pend_k;   // [B][Hkv][P][D]
+  const uint16_t* pend_v;
+  int P;
+  const int32_t* sel_idx;   // [B][Hkv][top_k]
+  const uint16_t* sel_k;
+  const uint16_t* sel_v;
+  int top_k;
+  float qscale;             // sm_scale * log2(e)
+  uint16_t* out;            // [B][gamma][Hq][D]
+  float* lse;               // [B][gamma][Hq] or null
+  int* status;
+  unsigned* counters;       // [B*Hkv]
+  float* partials;          // [B*Hkv][S_q+1][kPartialFloats(D)]
+  int S_q;                  // quantized splits per (b, kvh)
+  long long chunk;          // tokens per split (multiple of kChunkAlign)
+  long long wait_limit;
+};
+
+struct TopkParams {
+  CacheView c;
+  const uint16_t* q;        // [B][Hq][D]
+  int Hq, HG, k;
+  int32_t* idx_out;         // [B][Hkv][k]
+  float* score_out;         // [B][Hkv][k] or null
+  int* status;
+  unsigned* counters;       // [B*Hkv]
+  float* cand_score;        // [B*Hkv][S][k]
+  int32_t* cand_idx;
+  int S;
+  long long chunk;
+  long long wait_limit;
+};
+
+struct FlushParams {
+  // writable views of the cache regions
+  uint8_t* kplane[2];
+  uint8_t* vplane[2];
+  float* ksz;
+  float* vsz;
+  const uint16_t* res_k;
+  const uint16_t* res_v;
+  const uint16_t* k_new;    // [B][Hkv][n][D]
+  const uint16_t* v_new;
+  int B, Hkv, D, G, fmt;
+  long long C, Lq;          // Lq before this call
+  int r, res_start, n;      // residual state before this call, tokens in this call
+  int nflush;               // groups quantized by this launch
+};
+
+struct ResidualWriteParams {
+  uint16_t* res_k;
+  uint16_t* res_v;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  int B, Hkv, D, G, n;
+  int r, res_start;         // before this call
+  int first_new;            // first stream position (>= r) kept in the residual
+  int count;                // tokens to write
+};
+
+cudaError_t launch_flush(const FlushParams& p, cudaStream_t s);
+cudaError_t launch_residual_write(const ResidualWriteParams& p, cudaStream_t s);
+cudaError_t launch_attend(const AttendParams& p, int mode, cudaStream_t s);
+cudaError_t launch_topk(const TopkParams& p, int mode, cudaStream_t s);
+cudaError_t launch_wait_selftest(int* status, long long limit, cudaStream_t s);
+
+}  // namespace kvq

@@ -1,0 +1,185 @@
+// Read modes and the register-level fragment builders for the quantized planes.
+//
+// Storage (see kvq.h): key planes are token-major with channels packed; value
+// planes are 32-token slabs with rows = channels and tokens packed.  Read modes
+// (QuantSpec page, "Approach"; SpeCache page, "Approach"):
+//   INT8: both nibble planes of the hierarchical code, 8-bit codes, scale x1
+//   INT4: the upper nibble plane only (the draft code), scale x16
+//   INT2 / INT1: the 2-/1-bit planes, scale x1
+//
+// Tensor-core mapping (m16n8k16, see kvq_device.cuh).  Lane = 4*g + q.
+// Logits are computed transposed, S^T = W x K^T:
+//  * A = folded query weights (rows g: high f16 part, rows g+8: low part)
+//  * B = key codes (col n = token, k = channel)
+// Thread q owns channels [q*D/4, (q+1)*D/4) of every token.  It turns them into
+// D/8 half2 "pairs" P[p]; k-step kk consumes P[2kk] and P[2kk+1].  pair_chan()
+// gives the channels of pair p, so A is built with the same permutation.
+// In n-tile j the thread's column-n token is 4n + j of the 32-token slab.  So
+// C column 2q holds token 8q + j and column 2q+1 holds token 8q + j + 4.  These
+// are exactly the token pairs the value conversion below produces, so the
+// logit registers become the B operand of P.V with no shuffle.
+#pragma once
+
+#include <type_traits>
+
+#include "kvq_device.cuh"
+
+namespace kvq {
+
+template <int MODE>
+struct Mode;
+template <>
+struct Mode<KVQ_MODE_INT8> {
+  static constexpr int NP = 2, PB = 4, CB = 8, MULT = 1, TT = 32;
+};
+template <>
+struct Mode<KVQ_MODE_INT4> {
+  static constexpr int NP = 1, PB = 4, CB = 4, MULT = 16, TT = 64;
+};
+template <>
+struct Mode<KVQ_MODE_INT2> {
+  static constexpr int NP = 1, PB = 2, CB = 2, MULT = 1, TT = 64;
+};
+template <>
+struct Mode<KVQ_MODE_INT1> {
+  static constexpr int NP = 1, PB = 1, CB = 1, MULT = 1, TT = 64;
+};
+
+// Bytes of one key row per plane, and of one value slab row per plane.
+template <int MODE, int D>
+struct Rows {
+  static constexpr int KROW = D * Mode<MODE>::PB / 8;
+  static constexpr int VROW = 32 * Mode<MODE>::PB / 8;
+  static constexpr int KCHUNK = KROW / 4;  // bytes of a key row owned by one lane
+};
+
+// Channels (relative to q*D/4) of pair p.
+template <int MODE, int D>
+__device__ __forceinline__ int2 pair_chan(int p) {
+  if constexpr (Mode<MODE>::PB == 4) {
+    return make_int2(8 * (p / 4) + p % 4, 8 * (p / 4) + p % 4 + 4);
+  } else if constexpr (Mode<MODE>::PB == 2) {
+    return make_int2(16 * (p / 8) + p % 8, 16 * (p / 8) + p % 8 + 8);
+  } else {
+    constexpr int HALF = (D == 128) ? 16 : 8;
+    return make_int2(p, p + HALF);
+  }
+}
+
+template <int I, int N, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+  if constexpr (I < N) {
+    f(std::integral_constant<int, I>{});
+    static_for<I + 1, N>(f);
+  }
+}
+
+// Convert this lane's chunk of one key row into D/8 code pairs (1 + c/2^CB).
+// `k0` points at the chunk in plane 0; plane 1 (INT8 lower nibbles) lies
+// `plane_stride` bytes further.
+template <int MODE, int D>
+__device__ __forceinline__ void key_pairs(const uint8_t* k0, int plane_stride, uint32_t (&P)[D / 8]) {
+  using M = Mode<MODE>;
+  if constexpr (M::PB == 4) {
+    constexpr int NWD = D / 32;  // words per chunk
+    uint32_t h[NWD], l[NWD];
+    if constexpr (NWD == 4) {
+      const uint4 v = *reinterpret_cast<const uint4*>(k0);
+      h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
+      if constexpr (M::NP == 2) {
+        const uint4 w = *reinterpret_cast<const uint4*>(k0 + plane_stride);
+        l[0] = w.x; l[1] = w.y; l[2] = w.z; l[3] = w.w;
+      }
+    } else {
+      const uint2 v = *reinterpret_cast<const uint2*>(k0);
+      h[0] = v.x; h[1] = v.y;
+      if constexpr (M::NP == 2) {
+        const uint2 w = *reinterpret_cast<const uint2*>(k0 + plane_stride);
+        l[0] = w.x; l[1] = w.y;
+      }
+    }
+#pragma unroll
+    for (int w = 0; w < NWD; ++w) {
+      static_for<0, 4>([&](auto I) {
+        constexpr int i = decltype(I)::value;
+        if constexpr (M::NP == 2) P[4 * w + i] = cvt8_pair<i>(h[w], l[w]);
+        else P[4 * w + i] = cvt4_pair<i>(h[w]);
+      });
+    }
+  } else if constexpr (M::PB == 2) {
+    constexpr int NWD = D / 64;
+    uint32_t h[NWD];
+    if constexpr (NWD == 2) {
+      const uint2 v = *reinterpret_cast<const uint2*>(k0);
+      h[0] = v.x; h[1] = v.y;
+    } else {
+      h[0] = *reinterpret_cast<const uint32_t*>(k0);
+    }
+#pragma unroll
+    for (int w = 0; w < NWD; ++w) {
+      static_for<0, 8>([&](auto I) {
+        constexpr int i = decltype(I)::value;
+        P[8 * w + i] = cvt2_pair<i>(h[w]);
+      });
+    }
+  } else {
+    if constexpr (D == 128) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(k0);
+      static_for<0, 16>([&](auto I) {
+        constexpr int i = decltype(I)::value;
+        P[i] = cvt1_pair<i>(w);
+      });
+    } else {
+      const uint32_t h = *reinterpret_cast<const uint16_t*>(k0);
+      const uint32_t w = (h & 0xFFu) | ((h & 0xFF00u) << 8);
+      static_for<0, 8>([&](auto I) {
+        constexpr int i = decltype(I)::value;
+        P[i] = cvt1_pair<i>(w);
+      });
+    }
+  }
+}
+
+// A-operand fragments of P.V for one m-tile (channel rows ca = 16mt+g and
+// cb = ca+8) of one 32-token slab: a[s] for k-steps s = 0, 1.  Lane q's tokens
+// are 8q..8q+7.  k-step s covers the pairs (8q+2s, 8q+2s+4) and
+// (8q+2s+1, 8q+2s+5).  `va`/`vb` point at rows ca/cb of plane 0.
+template <int MODE>
+__device__ __forceinline__ void value_frags(const uint8_t* va, const uint8_t* vb, int plane_stride,
+                                            int q, uint32_t (&a)[2][4]) {
+  using M = Mode<MODE>;
+  if constexpr (M::PB == 4) {
+    const uint32_t wa = *reinterpret_cast<const uint32_t*>(va + 4 * q);
+    const uint32_t wb = *reinterpret_cast<const uint32_t*>(vb + 4 * q);
+    if constexpr (M::NP == 2) {
+      const uint32_t la = *reinterpret_cast<const uint32_t*>(va + plane_stride + 4 * q);
+      const uint32_t lb = *reinterpret_cast<const uint32_t*>(vb + plane_stride + 4 * q);
+      a[0][0] = cvt8_pair<0>(wa, la); a[0][1] = cvt8_pair<0>(wb, lb);
+      a[0][2] = cvt8_pair<1>(wa, la); a[0][3] = cvt8_pair<1>(wb, lb);
+      a[1][0] = cvt8_pair<2>(wa, la); a[1][1] = cvt8_pair<2>(wb, lb);
+      a[1][2] = cvt8_pair<3>(wa, la); a[1][3] = cvt8_pair<3>(wb, lb);
+    } else {
+      a[0][0] = cvt4_pair<0>(wa); a[0][1] = cvt4_pair<0>(wb);
+      a[0][2] = cvt4_pair<1>(wa); a[0][3] = cvt4_pair<1>(wb);
+      a[1][0] = cvt4_pair<2>(wa); a[1][1] = cvt4_pair<2>(wb);
+      a[1][2] = cvt4_pair<3>(wa); a[1][3] = cvt4_pair<3>(wb);
+    }
+  } else if constexpr (M::PB == 2) {
+    const uint32_t xa = *reinterpret_cast<const uint16_t*>(va + 2 * q);
+    const uint32_t xb = *reinterpret_cast<const uint16_t*>(vb + 2 * q);
+    const uint32_t y = prmt(xa, xb, 0x5140u);   // [a.b0, b.b0, a.b1, b.b1]
+    a[0][0] = cvt2_pair<0>(y); a[0][1] = cvt2_pair<4>(y);
+    a[0][2] = cvt2_pair<1>(y); a[0][3] = cvt2_pair<5>(y);
+    a[1][0] = cvt2_pair<2>(y); a[1][1] = cvt2_pair<6>(y);
+    a[1][2] = cvt2_pair<3>(y); a[1][3] = cvt2_pair<7>(y);
+  } else {
+    const uint32_t x = static_cast<uint32_t>(va[q]) | (static_cast<uint32_t>(vb[q]) << 8);
+    const uint32_t y = (x & 0x0F0Fu) | ((x & 0xF0F0u) << 12);
+    a[0][0] = cvt1_pair<0>(y); a[0][1] = cvt1_pair<8>(y);
+    a[0][2] = cvt1_pair<1>(y); a[0][3] = cvt1_pair<9>(y);
+    a[1][0] = cvt1_pair<2>(y); a[1][1] = cvt1_pair<10>(y);
+    a[1][2] = cvt1_pair<3>(y); a[1][3] = cvt1_pair<11>(y);
+  }
+}
+
+}  // namespace kvq

@@ -1,0 +1,76 @@
+"""Helpers for the GPU parity tests: build the same cache with the CUDA library
+and with the CPU oracle from the same seeded inputs, then compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import kvq_inputs as ki
+import oracle
+import quantized_kv_speculative_gb300 as kvq
+
+TOL_REL = 2e-3   # |err| <= 2e-3 * max|ref| + 1e-3 over the whole output of a call
+TOL_ABS = 1e-3
+
+
+def dev(x: np.ndarray) -> torch.Tensor:
+    return ki.f32_to_bf16_tensor(x, "cuda")
+
+
+def build_pair(fmt, B, Hkv, D, G, cap, K, V, chunks):
+    """Append K/V ``[B, Hkv, N, D]`` in the given chunk sizes to a device cache
+    and to an oracle cache (which appends token by token)."""
+    gc = kvq.QuantizedKVCache(B, Hkv, D, G, fmt, cap)
+    oc = oracle.OracleCache(B, Hkv, D, G, fmt, cap)
+    pos = 0
+    for n in chunks:
+        kvq.kvq_quantize_append(gc, dev(K[:, :, pos:pos + n]), dev(V[:, :, pos:pos + n]))
+        oc.append(K[:, :, pos:pos + n], V[:, :, pos:pos + n])
+        pos += n
+    torch.cuda.synchronize()
+    assert (gc.quantized_len, gc.residual_len) == (oc.Lq, oc.r)
+    return gc, oc
+
+
+def compare_cache(gc: kvq.QuantizedKVCache, oc: oracle.OracleCache):
+    """Bit-exact comparison of codes, scales, zeros and the residual buffer."""
+    L, G = oc.Lq, oc.G
+    U = oc.B * oc.H
+    for i, plane in enumerate(oc.packed_k_planes()):
+        got = gc.k_plane(i)[:, :L].cpu().numpy()
+        np.testing.assert_array_equal(got, plane.reshape(U, L, -1), err_msg=f"key plane {i}")
+    for i, plane in enumerate(oc.packed_v_planes()):
+        got = gc.v_plane(i)[:, :L // 32].cpu().numpy()
+        np.testing.assert_array_equal(got, plane.reshape(U, L // 32, oc.D, -1), err_msg=f"value plane {i}")
+    ksz = gc.k_scale_zero()[:, :L // G].cpu().numpy()
+    np.testing.assert_array_equal(ksz[:, :, 0].view(np.uint32), oc.k_scale[:, :, :L // G].reshape(U, L // G, -1).view(np.uint32))
+    np.testing.assert_array_equal(ksz[:, :, 1].view(np.uint32), oc.k_zero[:, :, :L // G].reshape(U, L // G, -1).view(np.uint32))
+    vsz = gc.v_scale_zero()[:, :L].cpu().numpy()
+    np.testing.assert_array_equal(vsz[:, :, 0].view(np.uint32), oc.v_scale[:, :, :L].reshape(U, L, -1).view(np.uint32))
+    np.testing.assert_array_equal(vsz[:, :, 1].view(np.uint32), oc.v_zero[:, :, :L].reshape(U, L, -1).view(np.uint32))
+    rk, rv = gc.residual()
+    slots = [(gc.residual_start + i) % (2 * G) for i in range(gc.residual_len)]
+    ork, orv = oc.residual()
+    got_k = ki.bf16_tensor_to_f32(rk[:, slots]) if slots else np.zeros((U, 0, oc.D), np.float32)
+    got_v = ki.bf16_tensor_to_f32(rv[:, slots]) if slots else np.zeros((U, 0, oc.D), np.float32)
+    np.testing.assert_array_equal(got_k, ork.reshape(U, -1, oc.D))
+    np.testing.assert_array_equal(got_v, orv.reshape(U, -1, oc.D))
+
+
+def assert_attention_close(out_dev: torch.Tensor, lse_dev, ref_out: np.ndarray, ref_lse: np.ndarray, what=""):
+    got = ki.bf16_tensor_to_f32(out_dev).astype(np.float64)
+    err = np.abs(got - ref_out).max() if got.size else 0.0
+    tol = TOL_REL * (np.abs(ref_out).max() if got.size else 0.0) + TOL_ABS
+    assert err <= tol, f"{what}: max |err| {err:.3e} > tol {tol:.3e}"
+    if lse_dev is not None:
+        gl = lse_dev.cpu().numpy().astype(np.float64)
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(np.isfinite(gl), fin), f"{what}: lse finiteness differs"
+        if fin.any():
+            dl = np.abs(gl[fin] - ref_lse[fin]).max()
+            assert dl <= 1e-3 + 1e-4 * np.abs(ref_lse[fin]).max(), f"{what}: max |dlse| {dl:.3e}"
+    return err
+
+
+def mode_fmt(mode):
+    return kvq.MODE_FORMAT[mode]

@@ -1,0 +1,234 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+* Codes, scales, zero points and the residual buffer match bit for bit.
+* Top-k indices and scores match bit for bit.
+* Attention matches within |err| <= 2e-3 * max|ref| + 1e-3 over a call's output,
+  and log-sum-exp matches within 1e-3 + 1e-4 |lse|.
+Sizes span several tiles, warps and splits, plus a ragged tail.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kvq_inputs as ki
+import oracle
+import quantized_kv_speculative_gb300 as kvq
+from quantized_kv_speculative_gb300 import _build
+
+from kvq_testlib import assert_attention_close, build_pair, compare_cache, dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    _build.build()
+    kvq.load_library()
+    torch.cuda.init()
+
+
+# ------------------------------------------------------------------------------------
+# quantize + append
+# ------------------------------------------------------------------------------------
+
+CACHE_SHAPES = [
+    ("hier8", 64, 32), ("hier8", 128, 128), ("hier8", 128, 64), ("hier8", 64, 64),
+    ("int2", 128, 32), ("int2", 64, 64), ("int2", 128, 128), ("int1", 128, 32), ("int1", 64, 32),
+]
+
+
+@pytest.mark.parametrize("fmt,D,G", CACHE_SHAPES)
+def test_quantize_append_bit_exact(fmt, D, G):
+    """Bulk prefill, then single tokens and chunks that cross flushes, in the
+    same call pattern as a decode loop.  The state after every call matches the
+    oracle's token-by-token buffer."""
+    B, Hkv = 2, 3
+    N = 5 * G + 7 + 1 + 3 + 2 * G + 1 + G + 5
+    K, V = ki.kv_stream(100 + D + G, B, Hkv, N, D)
+    chunks = [5 * G + 7, 1, 3, 2 * G + 1, G, 5]
+    cap = (N // G + 1) * G
+    gc = kvq.QuantizedKVCache(B, Hkv, D, G, fmt, cap)
+    oc = oracle.OracleCache(B, Hkv, D, G, fmt, cap)
+    pos = 0
+    for n in chunks:
+        kvq.kvq_quantize_append(gc, dev(K[:, :, pos:pos + n]), dev(V[:, :, pos:pos + n]))
+        oc.append(K[:, :, pos:pos + n], V[:, :, pos:pos + n])
+        pos += n
+        torch.cuda.synchronize()
+        assert (gc.quantized_len, gc.residual_len) == (oc.Lq, oc.r)
+        compare_cache(gc, oc)
+
+
+def test_quantize_degenerate_groups_and_signed_zero():
+    """Constant groups (scale 0), -0.0 values and extreme bf16 magnitudes."""
+    B, Hkv, D, G = 1, 2, 64, 32
+    N = 3 * G + 4
+    K = np.zeros((B, Hkv, N, D), np.float32)
+    V = np.zeros((B, Hkv, N, D), np.float32)
+    K[0, 0] = -0.0
+    K[0, 1, :, :8] = 3.5
+    K[0, 1, :, 8:] = ki.normal_bf16(ki.rng(5), (N, D - 8))
+    V[0, 0, :, :32] = -0.0
+    V[0, 1] = ki.round_bf16(ki.rng(6).standard_normal((N, D)).astype(np.float32) * np.float32(1e30))
+    for fmt in ("hier8", "int2", "int1"):
+        gc, oc = build_pair(fmt, B, Hkv, D, G, 4 * G, K, V, [N])
+        compare_cache(gc, oc)
+
+
+# ------------------------------------------------------------------------------------
+# attention
+# ------------------------------------------------------------------------------------
+
+ATTN_CASES = [
+    # mode, B, Hkv, Hq, D, G, N, gamma, P, top_k, needles
+    ("int8", 1, 4, 4, 64, 32, 544, 1, 1, 0, False),         # tiny-d64-g32 shape
+    ("int4", 1, 4, 4, 64, 32, 544, 1, 1, 0, False),
+    ("int8", 2, 2, 16, 128, 128, 1150, 2, 3, 0, False),     # GQA 8:1, 8 rows, ragged residual
+    ("int4", 2, 2, 16, 128, 128, 1150, 2, 3, 0, True),
+    ("int8", 1, 3, 3, 128, 128, 4000, 8, 8, 0, True),       # gamma = 8 verify, MHA
+    ("int4", 1, 3, 3, 128, 64, 2500, 1, 0, 0, False),       # no pending tokens
+    ("int8", 1, 2, 12, 128, 64, 3100, 2, 2, 0, False),      # 6 rows
+    ("int2", 3, 2, 8, 128, 32, 2100, 2, 2, 16, False),      # SpeCache shape, selected tokens
+    ("int1", 3, 2, 8, 128, 32, 2100, 2, 2, 16, True),
+    ("int2", 1, 2, 2, 64, 32, 900, 1, 1, 5, False),
+    ("int1", 1, 2, 4, 64, 64, 1000, 2, 2, 0, False),
+    ("int4", 2, 2, 8, 128, 32, 1700, 2, 2, 0, False),       # hierarchical format with G = 32
+]
+
+
+def _attn_case(mode, B, Hkv, Hq, D, G, N, gamma, P, top_k, needles, seed=0):
+    fmt = kvq.MODE_FORMAT[mode]
+    K, V = ki.kv_stream(seed + 7, B, Hkv, N, D)
+    q = ki.queries(seed + 7, B, gamma, Hq, D)
+    if needles:
+        K, _ = ki.plant_needles(K, q, seed + 7, limit=N - 2 * G)
+    cap = (N // G + 1) * G
+    gc, oc = build_pair(fmt, B, Hkv, D, G, cap, K, V, [N - 3, 1, 2])
+    pk = pv = None
+    if P:
+        pk, pv = ki.pending(seed + 7, B, Hkv, P, D)
+    sel = sk = sv = None
+    if top_k:
+        g = ki.rng(seed + 7, 9)
+        sel = np.stack([np.stack([g.choice(oc.Lq, top_k, replace=False) for _ in range(Hkv)]) for _ in range(B)])
+        sel = sel.astype(np.int32)
+        sel[0, 0, -1] = -1                       # padding entry
+        sk = ki.normal_bf16(g, (B, Hkv, top_k, D))
+        sv = ki.normal_bf16(g, (B, Hkv, top_k, D))
+    return gc, oc, q, pk, pv, sel, sk, sv
+
+
+@pytest.mark.parametrize("case", ATTN_CASES, ids=lambda c: f"{c[0]}-B{c[1]}-Hkv{c[2]}-Hq{c[3]}-D{c[4]}-G{c[5]}-N{c[6]}-g{c[7]}-P{c[8]}-k{c[9]}{'-needle' if c[10] else ''}")
+def test_attend_matches_oracle(case):
+    mode = case[0]
+    gc, oc, q, pk, pv, sel, sk, sv = _attn_case(*case)
+    ref_out, ref_lse = oracle.attend(oc, mode, q, pk, pv, sel, sk, sv)
+    out, lse = kvq.kvq_attend(gc, mode, dev(q), None if pk is None else dev(pk), None if pv is None else dev(pv),
+                              None if sel is None else torch.from_numpy(sel).cuda(),
+                              None if sk is None else dev(sk), None if sv is None else dev(sv))
+    torch.cuda.synchronize()
+    assert_attention_close(out, lse, ref_out, ref_lse, what=str(case))
+
+
+def test_attend_deterministic_and_split_independent():
+    """Two calls give identical bytes.  The result does not depend on the
+    workspace's history, because the ticket counters reset themselves."""
+    case = ("int8", 2, 2, 16, 128, 128, 1150, 2, 3, 0, False)
+    gc, oc, q, pk, pv, _, _, _ = _attn_case(*case)
+    ws = kvq.make_workspace(gc, 16, 2, 0)
+    outs = []
+    for _ in range(3):
+        o, l = kvq.kvq_attend(gc, "int8", dev(q), dev(pk), dev(pv), workspace=ws)
+        outs.append((o.clone(), l.clone()))
+    torch.cuda.synchronize()
+    for o, l in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0][0].view(torch.int16))
+        assert torch.equal(l, outs[0][1])
+    assert kvq.kvq_workspace_status(ws) == 0
+
+
+def test_attend_edge_cases():
+    """An empty cache gives out 0 and lse -inf.  Residual only (Lq = 0);
+    pending == gamma; selected entries all padding; k > Lq."""
+    D, G, Hkv = 64, 32, 2
+    q = ki.queries(3, 1, 2, 2, D)
+    gc = kvq.QuantizedKVCache(1, Hkv, D, G, "hier8", 256)
+    out, lse = kvq.kvq_attend(gc, "int8", dev(q))
+    torch.cuda.synchronize()
+    assert torch.all(out.float() == 0) and torch.all(torch.isneginf(lse))
+    # residual only
+    K, V = ki.kv_stream(4, 1, Hkv, 50, D)
+    gc, oc = build_pair("hier8", 1, Hkv, D, G, 256, K, V, [50])
+    assert oc.Lq == 0
+    pk, pv = ki.pending(4, 1, Hkv, 2, D)
+    ref = oracle.attend(oc, "int4", q, pk, pv)
+    out, lse = kvq.kvq_attend(gc, "int4", dev(q), dev(pk), dev(pv))
+    assert_attention_close(out, lse, *ref, what="residual only")
+    # exactly one quantized group, all selected entries padding
+    K, V = ki.kv_stream(5, 1, Hkv, 2 * G + 1, D)
+    gc, oc = build_pair("int2", 1, Hkv, D, G, 256, K, V, [2 * G + 1])
+    sel = -np.ones((1, Hkv, 3), np.int32)
+    sk = ki.normal_bf16(ki.rng(1), (1, Hkv, 3, D))
+    ref = oracle.attend(oc, "int2", q, pk, pv, sel, sk, sk)
+    out, lse = kvq.kvq_attend(gc, "int2", dev(q), dev(pk), dev(pv), torch.from_numpy(sel).cuda(), dev(sk), dev(sk))
+    assert_attention_close(out, lse, *ref, what="padding selection")
+
+
+def test_bounded_wait_reports_timeout_without_hanging():
+    """A kernel that waits on an mbarrier nothing arrives at gives up after its
+    limit, records KVQ_ERR_DEVICE_TIMEOUT, and leaves the context usable."""
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    kvq.kvq_selftest_bounded_wait(ws, 100000)
+    assert kvq.kvq_workspace_status(ws) == 6
+    assert kvq.kvq_workspace_status(ws) == 0      # read clears it
+    x = torch.ones(16, device="cuda")
+    assert float(x.sum()) == 16.0
+
+
+# ------------------------------------------------------------------------------------
+# top-k
+# ------------------------------------------------------------------------------------
+
+TOPK_CASES = [
+    # mode, B, Hkv, Hq, D, G, N, k
+    ("int4", 1, 2, 2, 128, 128, 3000, 64),
+    ("int4", 2, 2, 8, 64, 32, 1500, 17),
+    ("int2", 3, 2, 8, 128, 32, 2100, 64),
+    ("int2", 1, 1, 4, 128, 32, 20000, 100),     # several splits, ragged last chunk
+    ("int1", 3, 2, 8, 128, 32, 2100, 64),
+    ("int1", 1, 2, 2, 64, 64, 700, 1),
+    ("int2", 1, 2, 2, 64, 32, 130, 80),         # k > Lq: padded with -1
+]
+
+
+@pytest.mark.parametrize("case", TOPK_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_topk_matches_oracle(case):
+    mode, B, Hkv, Hq, D, G, N, k = case
+    fmt = kvq.MODE_FORMAT[mode]
+    K, V = ki.kv_stream(11, B, Hkv, N, D)
+    K[:, :, 7] = K[:, :, 3]                       # a planted score tie
+    gc, oc = build_pair(fmt, B, Hkv, D, G, (N // G + 1) * G, K, V, [N])
+    qspec = ki.queries(11, B, 1, Hq, D)[:, 0]
+    ref_idx, ref_sc = oracle.topk(oc, mode, qspec, k)
+    idx, sc = kvq.kvq_topk(gc, mode, dev(qspec), k)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), ref_sc.view(np.uint32))
+
+
+def test_topk_then_attend_specache_step():
+    """One SpeCache step: top-k from the speculative token (query row 1), then
+    attention that uses those tokens at 16 bits.  Both match the oracle."""
+    B, Hkv, Hq, D, G, N, k = 2, 2, 8, 128, 32, 2100, 32
+    K, V = ki.kv_stream(12, B, Hkv, N, D)
+    gc, oc = build_pair("int2", B, Hkv, D, G, (N // G + 1) * G, K, V, [N])
+    q = ki.queries(12, B, 2, Hq, D)
+    idx, _ = kvq.kvq_topk(gc, "int2", dev(q[:, 1]), k)
+    ref_idx, _ = oracle.topk(oc, "int2", q[:, 1], k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    sk = np.take_along_axis(K, ref_idx[..., None].astype(np.int64), axis=2)
+    sv = np.take_along_axis(V, ref_idx[..., None].astype(np.int64), axis=2)
+    pk, pv = ki.pending(12, B, Hkv, 2, D)
+    ref = oracle.attend(oc, "int2", q, pk, pv, ref_idx, sk, sv)
+    out, lse = kvq.kvq_attend(gc, "int2", dev(q), dev(pk), dev(pv), idx, dev(sk), dev(sv))
+    assert_attention_close(out, lse, *ref, what="specache step")
