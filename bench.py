@@ -462,6 +462,233 @@ def run_reference(args, rank, world):
 
 
 # --------------------------------------------------------------------------------------
+# other workloads (one JSON line each; the default run above is the headline)
+# --------------------------------------------------------------------------------------
+
+def _graph(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            fn(stream)
+    torch.cuda.synchronize()
+    return g
+
+
+def _time_graph(g, reps):
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def _peak():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"], "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _bytes_per_token(mode, D, G):
+    """Algorithmic bytes per quantized token per KV head read by a mode."""
+    codes = {"int8": D, "int4": D // 2, "int2": D // 4, "int1": D // 8}[mode]   # keys + values
+    return 2 * codes + 2 * D * 4 // G + 2 * 4 * (D // G)
+
+
+def run_multilayer_spec(layers, lq, r0, gamma, drafts, append, reps=3, seed=0):
+    """A 32-layer QuantSpec cycle: `drafts` INT4 draft steps (gamma = 1, the
+    drafts so far pending) over every layer, one INT8 verify over every layer,
+    and optionally the quantize-append of the accepted tokens."""
+    import quantized_kv_speculative_gb300 as kvq
+    from quantized_kv_speculative_gb300 import _build
+    _build.build()
+    B, H, D, G = 1, 32, 128, 128
+    dev = torch.device("cuda")
+    caches, wss = [], []
+    n = lq + r0
+    for layer in range(layers):
+        K, V = ki.kv_stream_torch(seed + layer, B, H, n, D)
+        c = kvq.QuantizedKVCache(B, H, D, G, "hier8", lq + 2 * G * (1 + append // G + 1))
+        kvq.kvq_quantize_append(c, K, V)
+        del K, V
+        caches.append(c)
+        wss.append(kvq.make_workspace(c, H, gamma, 0))
+    torch.cuda.synchronize()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed + 999)
+    rnd = lambda *shape: torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16)
+    qd = rnd(B, 1, H, D)
+    qv = rnd(B, gamma, H, D)
+    pk, pv = rnd(B, H, max(gamma, drafts), D), rnd(B, H, max(gamma, drafts), D)
+    kn, vn = rnd(B, H, max(append, 1), D), rnd(B, H, max(append, 1), D)
+    out_d, out_v = torch.empty_like(qd), torch.empty_like(qv)
+    lse_d = torch.empty((B, 1, H), device=dev)
+    lse_v = torch.empty((B, gamma, H), device=dev)
+    pend = [(pk[:, :, :j].contiguous(), pv[:, :, :j].contiguous()) for j in range(1, drafts + 1)]
+    pver = (pk[:, :, :gamma].contiguous(), pv[:, :, :gamma].contiguous())
+    s = torch.cuda.Stream()
+
+    def draft_step(j):
+        def f(st):
+            for L in range(layers):
+                kvq.kvq_attend(caches[L], "int4", qd, pend[j][0], pend[j][1], out=out_d, lse=lse_d,
+                               workspace=wss[L], stream=st)
+        return f
+
+    def verify(st):
+        for L in range(layers):
+            kvq.kvq_attend(caches[L], "int8", qv, pver[0], pver[1], out=out_v, lse=lse_v, workspace=wss[L], stream=st)
+
+    def commit(st):
+        for L in range(layers):
+            c = caches[L]
+            sv = c.state()
+            kvq.kvq_quantize_append(c, kn[:, :, :append].contiguous(), vn[:, :, :append].contiguous(), stream=st)
+            c.set_state(sv)
+
+    # eager warm-up (kernel attributes are set outside any capture)
+    draft_step(0)(None)
+    verify(None)
+    if append:
+        commit(None)
+    torch.cuda.synchronize()
+    gd = [_graph(draft_step(j), s) for j in range(drafts)]
+    gv = _graph(verify, s)
+    gc_ = _graph(commit, s) if append else None
+    t_draft = [_time_graph(g, reps) for g in gd]
+    t_ver = _time_graph(gv, reps)
+    t_app = _time_graph(gc_, reps) if append else 0.0
+    for ws in wss:
+        assert kvq.kvq_workspace_status(ws) == 0
+    peak, src = _peak()
+    res_b = r0 * 2 * D * 2 * H * B
+    b_draft = layers * (B * H * lq * _bytes_per_token("int4", D, G) + res_b)
+    b_ver = layers * (B * H * lq * _bytes_per_token("int8", D, G) + res_b)
+    td = statistics.mean(t_draft)
+    cycle_ms = sum(t_draft) + t_ver + t_app
+    toks = B * layers * (sum(lq + r0 + j for j in range(1, drafts + 1)) + (lq + r0 + gamma))
+    return {
+        "draft_step_ms": td, "draft_step_gbs": b_draft / (td * 1e-3) / 1e9,
+        "draft_frac": b_draft / (td * 1e-3) / 1e9 / peak,
+        "draft_call_ms": td / layers,
+        "verify_ms": t_ver, "verify_gbs": b_ver / (t_ver * 1e-3) / 1e9, "verify_frac": b_ver / (t_ver * 1e-3) / 1e9 / peak,
+        "verify_call_ms": t_ver / layers,
+        "append_ms": t_app, "cycle_ms": cycle_ms, "kv_tok_per_s": toks / (cycle_ms * 1e-3),
+        "peak_gbs": peak, "peak_source": src, "launches_per_cycle": layers * (drafts + 1 + (2 if append else 0)),
+    }
+
+
+def run_specache(fmt, seed=0, reps=20):
+    """SpeCache-style batched decode: batch 36, 32 q / 8 kv heads, D 128, G 32,
+    32768 quantized + 32 residual tokens; top-64 from the speculative token,
+    then attention (gamma = 2) with those 64 tokens at 16 bits."""
+    import quantized_kv_speculative_gb300 as kvq
+    from quantized_kv_speculative_gb300 import _build
+    _build.build()
+    B, Hq, H, D, G, lq, r0, k = 36, 32, 8, 128, 32, 32768, 32, 64
+    K, V = ki.kv_stream_torch(seed, B, H, lq + r0, D)
+    c = kvq.QuantizedKVCache(B, H, D, G, fmt, lq + 2 * G)
+    kvq.kvq_quantize_append(c, K, V)
+    ws = kvq.make_workspace(c, Hq, 2, k)
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed + 5)
+    q = torch.randn((B, 2, Hq, D), generator=gen, device=dev).to(torch.bfloat16)
+    pk = torch.randn((B, H, 2, D), generator=gen, device=dev).to(torch.bfloat16)
+    pv = torch.randn((B, H, 2, D), generator=gen, device=dev).to(torch.bfloat16)
+    qs = q[:, 1].contiguous()
+    idx, sc = kvq.kvq_topk(c, fmt, qs, k, workspace=ws)
+    gi = idx.long().clamp_min(0)[..., None].expand(-1, -1, -1, D)
+    sk, sv = torch.gather(K, 2, gi).contiguous(), torch.gather(V, 2, gi).contiguous()
+    del K, V
+    out = torch.empty_like(q)
+    lse = torch.empty((B, 2, Hq), device=dev)
+    s = torch.cuda.Stream()
+    kvq.kvq_attend(c, fmt, q, pk, pv, idx, sk, sv, out=out, lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+    ga = _graph(lambda st: kvq.kvq_attend(c, fmt, q, pk, pv, idx, sk, sv, out=out, lse=lse, workspace=ws, stream=st), s)
+    gt = _graph(lambda st: kvq.kvq_topk(c, fmt, qs, k, idx_out=idx, score_out=sc, workspace=ws, stream=st), s)
+    ta, tt = _time_graph(ga, reps), _time_graph(gt, reps)
+    assert kvq.kvq_workspace_status(ws) == 0
+    peak, src = _peak()
+    mode = fmt
+    ba = B * H * (lq * _bytes_per_token(mode, D, G) + r0 * 2 * D * 2)
+    codes_k = {"int2": D // 4, "int1": D // 8}[mode]
+    bt = B * H * lq * (codes_k + 2 * D * 4 // G)
+    return {"attend_ms": ta, "attend_gbs": ba / (ta * 1e-3) / 1e9, "attend_frac": ba / (ta * 1e-3) / 1e9 / peak,
+            "attend_bytes": ba, "sel_kv_bytes": B * H * k * 2 * D * 2,
+            "topk_ms": tt, "topk_gbs": bt / (tt * 1e-3) / 1e9, "topk_frac": bt / (tt * 1e-3) / 1e9 / peak,
+            "step_ms": ta + tt, "kv_tok_per_s": B * (lq + r0 + 2) / ((ta + tt) * 1e-3),
+            "peak_gbs": peak, "peak_source": src}
+
+
+def run_sweep(seed=0):
+    """Single-layer INT4 draft attention (gamma = 1, r = 128) over 8K..256K."""
+    import quantized_kv_speculative_gb300 as kvq
+    from quantized_kv_speculative_gb300 import _build
+    _build.build()
+    B, H, D, G = 1, 32, 128, 128
+    dev = torch.device("cuda")
+    peak, src = _peak()
+    rows = []
+    for lq in ki.SWEEP_CONTEXTS:
+        n = lq + 128 + 128
+        per_copy = B * H * lq * _bytes_per_token("int4", D, G)
+        copies = max(1, min(8, math.ceil(4 * 129e6 / (B * H * lq * _bytes_per_token("int8", D, G)))))
+        K, V = ki.kv_stream_torch(seed, B, H, n, D)
+        caches = []
+        for _ in range(copies):
+            c = kvq.QuantizedKVCache(B, H, D, G, "hier8", lq + 2 * G)
+            kvq.kvq_quantize_append(c, K, V)
+            caches.append(c)
+        del K, V
+        wss = [kvq.make_workspace(c, H, 1, 0) for c in caches]
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed + lq)
+        q = torch.randn((B, 1, H, D), generator=gen, device=dev).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        lse = torch.empty((B, 1, H), device=dev)
+        for i in range(copies):
+            kvq.kvq_attend(caches[i], "int4", q, out=out, lse=lse, workspace=wss[i])
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        reps_in = 8 * copies
+
+        def f(st):
+            for i in range(reps_in):
+                kvq.kvq_attend(caches[i % copies], "int4", q, out=out, lse=lse, workspace=wss[i % copies], stream=st)
+        g = _graph(f, s)
+        t = _time_graph(g, 5) / reps_in
+        b = per_copy + B * H * 128 * 2 * D * 2
+        rows.append({"context": lq, "ms": t, "gbs": b / (t * 1e-3) / 1e9, "frac": b / (t * 1e-3) / 1e9 / peak,
+                     "copies_rotated": copies, "kv_tok_per_s": B * (lq + 128) / (t * 1e-3)})
+        del caches, wss, g
+        torch.cuda.empty_cache()
+    return {"rows": rows, "peak_gbs": peak, "peak_source": src}
+
+
+def run_workload(name):
+    t0 = time.perf_counter()
+    if name == "llama7b-32l-spec-32k":
+        r = run_multilayer_spec(32, 32768, 128, 8, 8, 0)
+    elif name == "llama7b-32l-spec-128k":
+        r = run_multilayer_spec(32, 131072, 253, 6, 6, 6)
+    elif name in ("specache-b36-32k-int2", "specache-b36-32k-int1"):
+        r = run_specache(name.split("-")[-1])
+    elif name == "sweep-int4":
+        r = run_sweep()
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    r["workload"] = name
+    r["wall_s"] = time.perf_counter() - t0
+    return r
+
+
+# --------------------------------------------------------------------------------------
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
@@ -470,6 +697,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=None,
+                    help="extra measurement instead of the headline step: llama7b-32l-spec-32k, "
+                         "llama7b-32l-spec-128k, specache-b36-32k-int2, specache-b36-32k-int1, sweep-int4, all")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -482,6 +712,13 @@ def main():
             print(json.dumps(res), flush=True)
         return
     torch.cuda.set_device(local)
+    if args.workload:
+        names = (["llama7b-32l-spec-32k", "specache-b36-32k-int2", "specache-b36-32k-int1", "sweep-int4",
+                  "llama7b-32l-spec-128k"] if args.workload == "all" else [args.workload])
+        for nm in names:
+            print(json.dumps(run_workload(nm)), flush=True)
+            torch.cuda.empty_cache()
+        return
     if world > 1:
         torch.distributed.init_process_group("nccl")
     res, spec, inp = run_device(args, rank, world)

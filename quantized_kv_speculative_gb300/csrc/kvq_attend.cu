@@ -13,7 +13,8 @@
 //    mode's planes and scales into shared memory with 1-D bulk (TMA) copies on
 //    an mbarrier ring.  Four consumer warps each own a contiguous run of tiles.
 //    They dequantize in registers and run QK^T and PV on tensor cores
-//    (m16n8k16, f16 codes exact, weights split into high + low f16 parts).
+//    (m16n8k16, f16 codes exact; the folded key weights and the folded
+//    probabilities are each split into high + low f16 parts).
 //    Softmax is online in fp32 (base-2 logits).
 //  * Tail CTA: the bf16 residual buffer, the pending speculative tokens (causal)
 //    and the 16-bit selected tokens, on CUDA cores.
@@ -412,9 +413,6 @@ __global__ void __launch_bounds__(NTHREADS) attend_kernel(AttendParams p) {
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     float m_run = neg_inf(), l_run = 0.f;
-    float corrv[NJ];
-#pragma unroll
-    for (int jv = 0; jv < NJ; ++jv) corrv[jv] = 0.f;
     uint32_t wa[D / 16][4];
     float corr = 0.f;
     long long cur_grp = -1;
@@ -505,51 +503,68 @@ __global__ void __launch_bounds__(NTHREADS) attend_kernel(AttendParams p) {
         }
         l_run = l_run * alpha + psum;
         m_run = m_new;
-        // rescale O^T (rows 2q, 2q+1 live in this lane) and the value corrections
+        // rows 2q, 2q+1 of O^T live in this lane: their rescale factors
         const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * q);
         const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * q + 4);
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-          o[mt][0] *= a_lo; o[mt][1] *= a_hi; o[mt][2] *= a_lo; o[mt][3] *= a_hi;
-        }
-#pragma unroll
-        for (int jv = 0; jv < NJ; ++jv) corrv[jv] *= alpha;
 
-        // ---- P.V ----
+        // ---- P.V, one channel block (G channels) at a time ----
+        // The slab's products go into fresh accumulators.  Its correction
+        // sum_t (p_t z_t - P'_t), which removes the zero points and the
+        // encoding's constant 1, is added before the merge into the running
+        // output.  So the running sum only ever holds output-sized values.
         const uint8_t* vslab = sbase + L::V_OFF + sl * D * RW::VROW;
         const float vmul = qmul;  // 2^CB * MULT
-        uint32_t bq[2][2];
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-          const int jv = (16 * mt) / G;
-          if ((16 * mt) % G == 0) {
-            // B fragments: P'_t = 2^CB * MULT * p_t * s_t for this channel block
-            float pq[4][2];
+        for (int jv = 0; jv < NJ; ++jv) {
+          // P'_t = 2^CB * MULT * p_t * s_t, split into f16 high + low parts
+          float pq[4][2];
+          float zc = 0.f;
 #pragma unroll
-            for (int jt = 0; jt < 4; ++jt) {
+          for (int jt = 0; jt < 4; ++jt) {
 #pragma unroll
-              for (int e2 = 0; e2 < 2; ++e2) {
-                const int tk = 32 * sl + 8 * q + jt + 4 * e2;   // token within the tile
-                const float s = vsz[tk * 2 * NJ + jv];
-                const float z = vsz[tk * 2 * NJ + NJ + jv];
-                pq[jt][e2] = pr[jt][e2] * s * vmul;
-                corrv[jv] += pr[jt][e2] * z;
-              }
-            }
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-              bq[ks][0] = pack_half2(pq[2 * ks][0], pq[2 * ks][1]);
-              bq[ks][1] = pack_half2(pq[2 * ks + 1][0], pq[2 * ks + 1][1]);
-              const float2 f0 = unpack_half2(bq[ks][0]);
-              const float2 f1 = unpack_half2(bq[ks][1]);
-              corrv[jv] -= (f0.x + f0.y) + (f1.x + f1.y);
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const int tk = 32 * sl + 8 * q + jt + 4 * e2;   // token within the tile
+              const float s = vsz[tk * 2 * NJ + jv];
+              const float z = vsz[tk * 2 * NJ + NJ + jv];
+              pq[jt][e2] = pr[jt][e2] * s * vmul;
+              zc += pr[jt][e2] * z;
             }
           }
-          uint32_t a[2][4];
-          const uint8_t* va = vslab + (16 * mt + g) * RW::VROW;
-          value_frags<MODE>(va, va + 8 * RW::VROW, L::VPLANE, q, a);
-          mma16816(o[mt], a[0], bq[0][0], bq[0][1]);
-          mma16816(o[mt], a[1], bq[1][0], bq[1][1]);
+          uint32_t bq[2][2][2];   // [k-step][high/low][register]
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+            for (int r2 = 0; r2 < 2; ++r2) {
+              const float x0 = pq[2 * ks + r2][0], x1 = pq[2 * ks + r2][1];
+              const uint32_t hi = pack_half2(x0, x1);
+              const float2 fh = unpack_half2(hi);
+              const uint32_t lo = pack_half2(x0 - fh.x, x1 - fh.y);
+              const float2 fl = unpack_half2(lo);
+              bq[ks][0][r2] = hi;
+              bq[ks][1][r2] = lo;
+              zc -= (fh.x + fh.y) + (fl.x + fl.y);
+            }
+          }
+          // row g's correction for this slab, then the values for rows 2q, 2q+1
+          zc += __shfl_xor_sync(0xffffffffu, zc, 1);
+          zc += __shfl_xor_sync(0xffffffffu, zc, 2);
+          const float z_lo = __shfl_sync(0xffffffffu, zc, 8 * q);
+          const float z_hi = __shfl_sync(0xffffffffu, zc, 8 * q + 4);
+#pragma unroll
+          for (int mt = jv * (G / 16); mt < (jv + 1) * (G / 16); ++mt) {
+            uint32_t a[2][4];
+            const uint8_t* va = vslab + (16 * mt + g) * RW::VROW;
+            value_frags<MODE>(va, va + 8 * RW::VROW, L::VPLANE, q, a);
+            float os[4] = {0.f, 0.f, 0.f, 0.f};
+            mma16816(os, a[0], bq[0][0][0], bq[0][0][1]);
+            mma16816(os, a[0], bq[0][1][0], bq[0][1][1]);
+            mma16816(os, a[1], bq[1][0][0], bq[1][0][1]);
+            mma16816(os, a[1], bq[1][1][0], bq[1][1][1]);
+            o[mt][0] = fmaf(o[mt][0], a_lo, os[0] + z_lo);
+            o[mt][1] = fmaf(o[mt][1], a_hi, os[1] + z_hi);
+            o[mt][2] = fmaf(o[mt][2], a_lo, os[2] + z_lo);
+            o[mt][3] = fmaf(o[mt][3], a_hi, os[3] + z_hi);
+          }
         }
       }
       __syncwarp();
@@ -560,24 +575,14 @@ __global__ void __launch_bounds__(NTHREADS) attend_kernel(AttendParams p) {
     float lsum = l_run;
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-    float cv[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int jv = 0; jv < NJ; ++jv) {
-      cv[jv] = corrv[jv];
-      cv[jv] += __shfl_xor_sync(0xffffffffu, cv[jv], 1);
-      cv[jv] += __shfl_xor_sync(0xffffffffu, cv[jv], 2);
-    }
     // the stage ring must be idle before the slot area is reused
     asm volatile("bar.sync 1, %0;" ::"n"(NW * 32));
     float* wm = reinterpret_cast<float*>(smem + L::WM_OFF);
     float* wl = reinterpret_cast<float*>(smem + L::WL_OFF);
-    float* wc = reinterpret_cast<float*>(smem + L::WC_OFF);
     float* wo = reinterpret_cast<float*>(smem + L::WO_OFF);
     if (q == 0) {
       wm[warp * 8 + g] = m_run;
       wl[warp * 8 + g] = lsum;
-#pragma unroll
-      for (int jv = 0; jv < 4; ++jv) wc[(warp * 8 + g) * 4 + jv] = cv[jv];
     }
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
@@ -608,7 +613,6 @@ __global__ void __launch_bounds__(NTHREADS) attend_kernel(AttendParams p) {
   {
     const float* wm = reinterpret_cast<const float*>(smem + L::WM_OFF);
     const float* wl = reinterpret_cast<const float*>(smem + L::WL_OFF);
-    const float* wc = reinterpret_cast<const float*>(smem + L::WC_OFF);
     const float* wo = reinterpret_cast<const float*>(smem + L::WO_OFF);
     const int PF = kPartialFloats(D);
     float* dst = p.partials + (u * (p.S_q + 1) + split) * PF;
@@ -619,14 +623,13 @@ __global__ void __launch_bounds__(NTHREADS) attend_kernel(AttendParams p) {
       for (int w = 0; w < NW; ++w) Mx = fmaxf(Mx, wm[w * 8 + rho]);
       float lt = 0.f, ot = 0.f;
       if (Mx != neg_inf()) {
-        const int jv = d / G;
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
           const float mw = wm[w * 8 + rho];
           if (mw == neg_inf()) continue;
           const float f = fast_exp2(mw - Mx);
           lt += f * wl[w * 8 + rho];
-          ot += f * (wo[(w * 8 + rho) * D + d] + wc[(w * 8 + rho) * 4 + jv]);
+          ot += f * wo[(w * 8 + rho) * D + d];
         }
       }
       dst[2 * kMaxRows + rho * D + d] = ot;

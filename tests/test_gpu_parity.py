@@ -83,11 +83,11 @@ ATTN_CASES = [
     # mode, B, Hkv, Hq, D, G, N, gamma, P, top_k, needles
     ("int8", 1, 4, 4, 64, 32, 544, 1, 1, 0, False),         # tiny-d64-g32 shape
     ("int4", 1, 4, 4, 64, 32, 544, 1, 1, 0, False),
-    ("int8", 2, 2, 16, 128, 128, 1150, 2, 3, 0, False),     # GQA 8:1, 8 rows, ragged residual
-    ("int4", 2, 2, 16, 128, 128, 1150, 2, 3, 0, True),
+    ("int8", 2, 2, 8, 128, 128, 1150, 2, 3, 0, False),      # GQA 4:1, 8 rows, ragged residual
+    ("int4", 2, 2, 8, 128, 128, 1150, 2, 3, 0, True),
     ("int8", 1, 3, 3, 128, 128, 4000, 8, 8, 0, True),       # gamma = 8 verify, MHA
     ("int4", 1, 3, 3, 128, 64, 2500, 1, 0, 0, False),       # no pending tokens
-    ("int8", 1, 2, 12, 128, 64, 3100, 2, 2, 0, False),      # 6 rows
+    ("int8", 1, 2, 6, 128, 64, 3100, 2, 2, 0, False),       # 6 rows
     ("int2", 3, 2, 8, 128, 32, 2100, 2, 2, 16, False),      # SpeCache shape, selected tokens
     ("int1", 3, 2, 8, 128, 32, 2100, 2, 2, 16, True),
     ("int2", 1, 2, 2, 64, 32, 900, 1, 1, 5, False),
@@ -133,9 +133,9 @@ def test_attend_matches_oracle(case):
 def test_attend_deterministic_and_split_independent():
     """Two calls give identical bytes.  The result does not depend on the
     workspace's history, because the ticket counters reset themselves."""
-    case = ("int8", 2, 2, 16, 128, 128, 1150, 2, 3, 0, False)
+    case = ("int8", 2, 2, 8, 128, 128, 1150, 2, 3, 0, False)
     gc, oc, q, pk, pv, _, _, _ = _attn_case(*case)
-    ws = kvq.make_workspace(gc, 16, 2, 0)
+    ws = kvq.make_workspace(gc, 8, 2, 0)
     outs = []
     for _ in range(3):
         o, l = kvq.kvq_attend(gc, "int8", dev(q), dev(pk), dev(pv), workspace=ws)
