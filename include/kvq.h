@@ -230,6 +230,36 @@ kvq_status kvq_topk(const kvq_cache* cache, kvq_mode mode, const void* q_spec,
                     int32_t num_q_heads, int32_t top_k, int32_t* idx_out, float* score_out,
                     void* workspace, size_t ws_bytes, kvq_stream_t stream);
 
+/*
+ * kvq_attend for callers that cannot allocate device memory.  The paper has no
+ * counterpart: this is a deployment variant.  A decode loop that must not
+ * allocate after start-up is one such caller: an allocation can synchronize
+ * the device or disturb a pre-reserved memory pool.  A host integration with no
+ * device allocator of its own is another.
+ *
+ * Same arguments and results as kvq_attend, minus the workspace.  The workspace
+ * is a fixed 16 MiB array compiled into the library, so the call allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine).  Every GPU
+ * that loads the library holds that array until the process exits.
+ *  - Limit: the cache must need at most 16 MiB of attention workspace
+ *    (kvq_workspace_bytes(cache, num_q_heads, gamma, 0) <= 16 MiB).  Otherwise
+ *    the call returns KVQ_ERR_WORKSPACE and enqueues nothing.
+ *  - Set-up: the first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and keeps it.  Make that
+ *    first call before any stream capture.
+ *  - Sharing: every call uses the same array and leaves its last contents there.
+ *    Each call clears the ticket counters it needs on `stream` first.  Calls
+ *    that overlap on the GPU (other streams, other threads) race on the array:
+ *    issue them in order on one stream.
+ *  - Device timeouts are recorded in the array's status word, which this entry
+ *    point does not report.
+ */
+kvq_status kvq_attend_static_scratch(const kvq_cache* cache, kvq_mode mode, const void* q,
+                                     int32_t num_q_heads, int32_t gamma, const void* pend_k,
+                                     const void* pend_v, int32_t n_pend, const int32_t* sel_idx,
+                                     const void* sel_k, const void* sel_v, int32_t top_k,
+                                     float sm_scale, void* out, float* lse, kvq_stream_t stream);
+
 /* Synchronously read (and then clear) the device status word of a workspace:
  * KVQ_OK, or KVQ_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait since the
  * last read.  Synchronizes `stream`. */

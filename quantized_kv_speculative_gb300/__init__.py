@@ -34,7 +34,7 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "K
 EXPORTED = (
     "kvq_status_string", "kvq_cache_bytes", "kvq_cache_init", "kvq_quantize_append",
     "kvq_workspace_bytes", "kvq_attend", "kvq_topk", "kvq_workspace_status",
-    "kvq_selftest_bounded_wait",
+    "kvq_selftest_bounded_wait", "kvq_attend_static_scratch",
 )
 
 
@@ -88,6 +88,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kvq_attend.argtypes = [cache_p, ctypes.c_int, vp, i32, i32, vp, vp, i32, vp, vp, vp, i32, f32,
                                vp, vp, vp, sz, vp]
     lib.kvq_attend.restype = ctypes.c_int
+    lib.kvq_attend_static_scratch.argtypes = [cache_p, ctypes.c_int, vp, i32, i32, vp, vp, i32, vp, vp, vp,
+                                              i32, f32, vp, vp, vp]
+    lib.kvq_attend_static_scratch.restype = ctypes.c_int
     lib.kvq_topk.argtypes = [cache_p, ctypes.c_int, vp, i32, i32, vp, vp, vp, sz, vp]
     lib.kvq_topk.restype = ctypes.c_int
     lib.kvq_workspace_status.argtypes = [vp, sz, vp]
@@ -246,6 +249,29 @@ def kvq_attend(cache: QuantizedKVCache, mode: str, q: torch.Tensor, pend_k=None,
                           _ptr(lse, torch.float32, "lse"), _ptr(workspace, torch.uint8, "workspace"),
                           workspace.numel(), _stream(stream)),
            "kvq_attend")
+    return out, lse
+
+
+def kvq_attend_static_scratch(cache: QuantizedKVCache, mode: str, q: torch.Tensor, pend_k=None, pend_v=None,
+                              sel_idx=None, sel_k=None, sel_v=None, sm_scale: float = 0.0, out=None, lse=None,
+                              stream=None):
+    """``kvq_attend`` for callers that cannot allocate device memory: the
+    workspace is a fixed 16 MiB array inside the library (see kvq.h).  The output
+    and LSE buffers must still be passed in; nothing is allocated here either."""
+    B, gamma, Hq, D = q.shape
+    if out is None or lse is None:
+        raise ValueError("pass preallocated out and lse")
+    n_pend = 0 if pend_k is None else pend_k.shape[2]
+    top_k = 0 if sel_idx is None else sel_idx.shape[2]
+    lib = load_library()
+    _check(lib.kvq_attend_static_scratch(ctypes.byref(cache.struct), MODES[mode], _ptr(q, torch.bfloat16, "q"),
+                                         Hq, gamma, _ptr(pend_k, torch.bfloat16, "pend_k"),
+                                         _ptr(pend_v, torch.bfloat16, "pend_v"), n_pend,
+                                         _ptr(sel_idx, torch.int32, "sel_idx"), _ptr(sel_k, torch.bfloat16, "sel_k"),
+                                         _ptr(sel_v, torch.bfloat16, "sel_v"), top_k, float(sm_scale),
+                                         _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+                                         _stream(stream)),
+           "kvq_attend_static_scratch")
     return out, lse
 
 
