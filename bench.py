@@ -671,6 +671,62 @@ def run_sweep(seed=0):
     return {"rows": rows, "peak_gbs": peak, "peak_source": src}
 
 
+def run_profile_case(name, launches):
+    """A few eager launches of one call, for ncu captures (no graphs, no timing)."""
+    import quantized_kv_speculative_gb300 as kvq
+    from quantized_kv_speculative_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    rnd = lambda *shape: torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16)
+    if name in ("attend-int8-verify-8k", "attend-int4-draft-32k", "topk-int4-8k"):
+        B, H, D, G = 1, 32, 128, 128
+        lq, r0 = (8192, 252) if name != "attend-int4-draft-32k" else (32768, 128)
+        copies = 4
+        K, V = ki.kv_stream_torch(0, B, H, lq + r0, D)
+        caches = []
+        for _ in range(copies):
+            c = kvq.QuantizedKVCache(B, H, D, G, "hier8", lq + 2 * G)
+            kvq.kvq_quantize_append(c, K, V)
+            caches.append(c)
+        gamma = 8 if name == "attend-int8-verify-8k" else 1
+        ws = [kvq.make_workspace(c, H, gamma, 64) for c in caches]
+        q = rnd(B, gamma, H, D)
+        pk, pv = rnd(B, H, gamma, D), rnd(B, H, gamma, D)
+        out = torch.empty_like(q)
+        lse = torch.empty((B, gamma, H), device=dev)
+        idx = torch.empty((B, H, 64), dtype=torch.int32, device=dev)
+        for i in range(launches):
+            c = caches[i % copies]
+            if name == "topk-int4-8k":
+                kvq.kvq_topk(c, "int4", q[:, 0].contiguous(), 64, idx_out=idx, workspace=ws[i % copies])
+            else:
+                mode = "int8" if gamma == 8 else "int4"
+                kvq.kvq_attend(c, mode, q, pk, pv, out=out, lse=lse, workspace=ws[i % copies])
+    elif name in ("attend-int2-specache-32k", "topk-int2-specache-32k"):
+        B, Hq, H, D, G, lq, r0, k = 36, 32, 8, 128, 32, 32768, 32, 64
+        K, V = ki.kv_stream_torch(0, B, H, lq + r0, D)
+        c = kvq.QuantizedKVCache(B, H, D, G, "int2", lq + 2 * G)
+        kvq.kvq_quantize_append(c, K, V)
+        ws = kvq.make_workspace(c, Hq, 2, k)
+        q = rnd(B, 2, Hq, D)
+        pk, pv = rnd(B, H, 2, D), rnd(B, H, 2, D)
+        idx, _ = kvq.kvq_topk(c, "int2", q[:, 1].contiguous(), k, workspace=ws)
+        gi = idx.long().clamp_min(0)[..., None].expand(-1, -1, -1, D)
+        sk, sv = torch.gather(K, 2, gi).contiguous(), torch.gather(V, 2, gi).contiguous()
+        del K, V
+        for i in range(launches):
+            if name.startswith("topk"):
+                kvq.kvq_topk(c, "int2", q[:, 1].contiguous(), k, idx_out=idx, workspace=ws)
+            else:
+                kvq.kvq_attend(c, "int2", q, pk, pv, idx, sk, sv, workspace=ws)
+    else:
+        raise SystemExit(f"unknown profile case {name}")
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": name, "launches": launches}))
+
+
 def run_workload(name):
     t0 = time.perf_counter()
     if name == "llama7b-32l-spec-32k":
@@ -697,6 +753,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", default=None, help="eager launches of one call for ncu captures")
+    ap.add_argument("--launches", type=int, default=4)
     ap.add_argument("--workload", default=None,
                     help="extra measurement instead of the headline step: llama7b-32l-spec-32k, "
                          "llama7b-32l-spec-128k, specache-b36-32k-int2, specache-b36-32k-int1, sweep-int4, all")
@@ -712,6 +770,9 @@ def main():
             print(json.dumps(res), flush=True)
         return
     torch.cuda.set_device(local)
+    if args.profile_case:
+        run_profile_case(args.profile_case, args.launches)
+        return
     if args.workload:
         names = (["llama7b-32l-spec-32k", "specache-b36-32k-int2", "specache-b36-32k-int1", "sweep-int4",
                   "llama7b-32l-spec-128k"] if args.workload == "all" else [args.workload])

@@ -25,7 +25,7 @@ bool valid_desc(const kvq_cache_desc* d) {
   if (d->format != KVQ_FMT_HIER8 && d->format != KVQ_FMT_INT2 && d->format != KVQ_FMT_INT1) return false;
   if (d->reserved0 != 0) return false;
   if (d->capacity_tokens < 0 || d->capacity_tokens % d->group_size) return false;
-  if (d->capacity_tokens > (1LL << 30)) return false;
+  if (d->capacity_tokens > static_cast<long long>(kMaxQuantSplits) * kMaxChunk) return false;
   const long long units = static_cast<long long>(d->batch) * d->num_kv_heads;
   if (units > (1LL << 24)) return false;
   return true;
@@ -60,13 +60,16 @@ long long units_of(const kvq_cache* c) {
   return static_cast<long long>(c->desc.batch) * c->desc.num_kv_heads;
 }
 
-// Quantized splits per (b, kvh) for attention, and the chunk size.
-int attend_splits(long long Lq, long long U, long long* chunk) {
+// Quantized splits per (b, kvh) for attention, and the chunk size.  `slots` is
+// how many CTAs of the kernel fit on the device at once: the splits fill whole
+// waves of it.
+int attend_splits(long long Lq, long long U, long long slots, long long* chunk) {
   if (Lq <= 0) {
     *chunk = 0;
     return 0;
   }
-  const long long target = std::max(1LL, ceil_div(kTargetCtas, U));
+  const long long want = slots > 0 ? std::max(1LL, slots / U) : ceil_div(kTargetCtas, U);
+  const long long target = std::min<long long>(kMaxQuantSplits, std::min(want, std::max(1LL, ceil_div(kTargetCtas, U))));
   long long S = std::min(ceil_div(Lq, kChunkAlign), target);
   S = std::max(S, ceil_div(Lq, kMaxChunk));
   S = std::max(S, 1LL);
@@ -79,7 +82,7 @@ int attend_splits_max(const kvq_cache_desc* d) {
   const long long U = static_cast<long long>(d->batch) * d->num_kv_heads;
   const long long Lq = d->capacity_tokens;
   if (Lq <= 0) return 0;
-  const long long target = std::max(1LL, ceil_div(kTargetCtas, U));
+  const long long target = std::min<long long>(kMaxQuantSplits, std::max(1LL, ceil_div(kTargetCtas, U)));
   long long S = std::min(ceil_div(Lq, kChunkAlign), target);
   S = std::max(S, ceil_div(Lq, kMaxChunk));
   return static_cast<int>(std::max(S, 1LL));
@@ -111,7 +114,7 @@ int topk_splits_max(const kvq_cache_desc* d) {
 
 size_t attend_ws_bytes(const kvq_cache_desc* d) {
   const size_t U = static_cast<size_t>(d->batch) * d->num_kv_heads;
-  const size_t S = static_cast<size_t>(attend_splits_max(d)) + 1;
+  const size_t S = static_cast<size_t>(attend_splits_max(d)) + kMaxTailSplits;
   return align256(U * 4) + align256(U * S * kPartialFloats(d->head_dim) * 4);
 }
 
@@ -325,8 +328,13 @@ kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int3
   p.counters = reinterpret_cast<unsigned*>(ws + kStatusBytes);
   p.partials = reinterpret_cast<float*>(ws + kStatusBytes + align256(U * 4));
   long long chunk = 0;
-  p.S_q = attend_splits(cache->quantized_len, U, &chunk);
+  const long long slots = attend_resident_ctas(mode, cache->desc.head_dim, cache->desc.group_size);
+  p.S_q = attend_splits(cache->quantized_len, U, slots, &chunk);
   p.chunk = chunk;
+  {
+    const long long nt = static_cast<long long>(cache->residual_len) + n_pend + top_k;
+    p.S_t = static_cast<int>(std::min<long long>(kMaxTailSplits, std::max(1LL, ceil_div(nt, kTailTokensPerSplit))));
+  }
   p.wait_limit = kDefaultWaitLimit;
   if (p.S_q > attend_splits_max(&cache->desc)) return KVQ_ERR_WORKSPACE;
   if (launch_attend(p, mode, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;

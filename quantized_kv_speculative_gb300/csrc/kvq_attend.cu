@@ -39,7 +39,23 @@ constexpr int NSLOT = NW * SPW;
 constexpr int NTHREADS = (NW + 1) * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int MODE, int D>
+// Tail-CTA shared layout (overlays the slot area of the same dynamic buffer).
+// K and V rows of one 64-token chunk are staged with a padded row stride so
+// that lanes reading different rows hit different banks.
+template <int D>
+struct TailSmem {
+  static constexpr int TC = 32;                               // tokens per chunk
+  static constexpr int ROW = D * 2 + 16;                      // padded bf16 row, bytes
+  static constexpr int QT_OFF = 0;                            // q~ [8][D] f32
+  static constexpr int K_OFF = QT_OFF + kMaxRows * D * 4;     // [TC][ROW]
+  static constexpr int V_OFF = K_OFF + TC * ROW;              // [TC][ROW]
+  static constexpr int LG_OFF = V_OFF + TC * ROW;             // logits / p [8][TC]
+  static constexpr int ST_OFF = LG_OFF + kMaxRows * TC * 4;   // m[8], l[8], alpha[8]
+  static constexpr int OK_OFF = ST_OFF + 3 * kMaxRows * 4;    // per-token flags [TC]
+  static constexpr int TOTAL = OK_OFF + TC * 4;
+};
+
+template <int MODE, int D, int NJ>
 struct Smem {
   using M = Mode<MODE>;
   using RW = Rows<MODE, D>;
@@ -49,16 +65,20 @@ struct Smem {
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = M::NP * KPLANE;
   static constexpr int KSZ_OFF = V_OFF + M::NP * VPLANE;
-  static constexpr int KSZ_BYTES = (TT / 32) * 2 * D * 4;
+  static constexpr int G = D / NJ;
+  static constexpr int KSZ_BYTES = (TT > G ? TT / G : 1) * 2 * D * 4;   // key groups a tile touches
   static constexpr int VSZ_OFF = KSZ_OFF + KSZ_BYTES;
-  static constexpr int VSZ_BYTES = TT * 2 * (D / 32) * 4;
+  static constexpr int VSZ_BYTES = TT * 2 * NJ * 4;
   static constexpr int SLOT = VSZ_OFF + VSZ_BYTES;
-  static constexpr int QT_OFF = NSLOT * SLOT;                 // q~  [8][D] f32
-  static constexpr int QH_OFF = QT_OFF + kMaxRows * D * 4;    // q^  [8][D] f32
-  static constexpr int BM_OFF = QH_OFF + kMaxRows * D * 4;    // selection bitmap
+  static constexpr int QX_OFF = NSLOT * SLOT;                 // folded query, [D/8][32 lanes] float2
+  static constexpr int BM_OFF = QX_OFF + (D / 8) * 32 * 8;    // selection bitmap
   static constexpr int BM_WORDS = kMaxChunk / 32;
   static constexpr int BAR_OFF = BM_OFF + BM_WORDS * 4;
-  static constexpr int MISC_OFF = BAR_OFF + 2 * NSLOT * 8;
+  static constexpr int RING_END = BAR_OFF + 2 * NSLOT * 8;
+  static constexpr int COMBINE_END = (2 * kMaxCombine * 8 + 16) * 4;
+  // the ticket flag sits after whichever layout (ring, tail CTA, combine) is largest
+  static constexpr int MISC_OFF0 = RING_END > TailSmem<D>::TOTAL ? RING_END : TailSmem<D>::TOTAL;
+  static constexpr int MISC_OFF = (MISC_OFF0 > COMBINE_END ? MISC_OFF0 : COMBINE_END + 15) / 16 * 16;
   static constexpr int TOTAL = MISC_OFF + 64;
   // warp-merge scratch (after the pipeline drains), inside the slot area
   static constexpr int WM_OFF = 0;                            // [NW][8]
@@ -67,49 +87,83 @@ struct Smem {
   static constexpr int WO_OFF = WC_OFF + NW * 8 * 4 * 4;      // [NW][8][D]
   static constexpr int SCRATCH = WO_OFF + NW * 8 * D * 4;
   static_assert(SCRATCH <= NSLOT * SLOT, "merge scratch must fit in the slot area");
+  static_assert(TailSmem<D>::TOTAL <= MISC_OFF, "the tail layout must not reach the ticket flag");
+  static_assert((2 * kMaxCombine * 8 + 16) * 4 <= MISC_OFF, "the combine scratch must not reach the ticket flag");
   static_assert(SLOT % 16 == 0, "slots must stay 16-byte aligned");
 };
 
-// Tail-CTA shared layout (overlays the slot area of the same dynamic buffer).
-template <int D>
-struct TailSmem {
-  static constexpr int TC = NTHREADS;                         // tokens per chunk
-  static constexpr int QT_OFF = 0;                            // [8][D]
-  static constexpr int LG_OFF = QT_OFF + kMaxRows * D * 4;    // [8][TC]
-  static constexpr int ST_OFF = LG_OFF + kMaxRows * TC * 4;   // m[8], l[8], alpha[8]
-  static constexpr int TOTAL = ST_OFF + 3 * kMaxRows * 4;
-};
-
-__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+// 2^x with the hardware approximation (ex2.approx.ftz: relative error near
+// 2^-22; -inf gives +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // ------------------------------------------------------------------------------
-// Combine: merge the S_total partials of unit u into out/lse.
+// Combine: merge the S_total partials of unit u into out/lse.  The split
+// maxima and weights are staged in shared memory (S_total <= 256), then each
+// thread streams float4 rows of the partial outputs with several splits in
+// flight.
 // ------------------------------------------------------------------------------
 template <int D>
-__device__ void combine_unit(const AttendParams& p, long long u, int S_total) {
+__device__ void combine_unit(const AttendParams& p, long long u, int S_total, float* sm) {
   const int PF = kPartialFloats(D);
   const float* base = p.partials + u * static_cast<long long>(S_total) * PF;
   const int b = static_cast<int>(u / p.c.Hkv), kvh = static_cast<int>(u % p.c.Hkv);
-  for (int e = threadIdx.x; e < p.R * D; e += blockDim.x) {
-    const int rho = e / D, d = e % D;
+  float* ms = sm;                       // [S_total][8] split maxima
+  float* wt = sm + kMaxCombine * 8;     // [S_total][8] l, then weights
+  float* ml = wt + kMaxCombine * 8;     // M[8], L[8]
+  const int tid = threadIdx.x;
+  for (int e = tid; e < S_total * 8; e += blockDim.x) {
+    const int s = e >> 3, r = e & 7;
+    ms[e] = __ldcg(base + s * PF + r);
+    wt[e] = __ldcg(base + s * PF + kMaxRows + r);
+  }
+  __syncthreads();
+  if (tid < p.R) {
     float M = neg_inf();
-    for (int s = 0; s < S_total; ++s) M = fmaxf(M, __ldcg(base + s * PF + rho));
-    float L = 0.f, O = 0.f;
+    for (int s = 0; s < S_total; ++s) M = fmaxf(M, ms[s * 8 + tid]);
+    float L = 0.f;
     if (M != neg_inf()) {
       for (int s = 0; s < S_total; ++s) {
-        const float ms = __ldcg(base + s * PF + rho);
-        if (ms == neg_inf()) continue;
-        const float f = fast_exp2(ms - M);
-        L += f * __ldcg(base + s * PF + kMaxRows + rho);
-        O += f * __ldcg(base + s * PF + 2 * kMaxRows + rho * D + d);
+        const float m = ms[s * 8 + tid];
+        const float f = (m == neg_inf()) ? 0.f : fast_exp2(m - M);
+        L += f * wt[s * 8 + tid];
+        wt[s * 8 + tid] = f;
       }
+    }
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+    for (int s = 0; s < S_total; ++s) wt[s * 8 + tid] = (M == neg_inf()) ? 0.f : wt[s * 8 + tid] * inv;
+    ml[tid] = M;
+    ml[8 + tid] = L;
+  }
+  __syncthreads();
+  constexpr int D4 = D / 4;
+  for (int item = tid; item < p.R * D4; item += blockDim.x) {
+    const int rho = item / D4, d4 = item % D4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4* src = reinterpret_cast<const float4*>(base + 2 * kMaxRows + rho * D) + d4;
+#pragma unroll 8
+    for (int s = 0; s < S_total; ++s) {
+      const float w = wt[s * 8 + rho];
+      const float4 v = __ldcg(src + static_cast<long long>(s) * (PF / 4));
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
     }
     const int i = rho / p.HG, hh = rho % p.HG;
     const int h = kvh * p.HG + hh;
     const long long orow = (static_cast<long long>(b) * p.gamma + i) * p.Hq + h;
-    const float val = (L > 0.f) ? O / L : 0.f;
-    p.out[orow * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
-    if (p.lse && d == 0) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p.out + orow * D + 4 * d4) = pk;
+    if (p.lse && d4 == 0) {
+      const float M = ml[rho], L = ml[8 + rho];
       p.lse[orow] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : neg_inf();
     }
   }
@@ -117,10 +171,10 @@ __device__ void combine_unit(const AttendParams& p, long long u, int S_total) {
 
 // Arrive at the per-unit ticket; the last arriving CTA merges and resets it.
 template <int D>
-__device__ void ticket_and_combine(const AttendParams& p, long long u, int* sh_flag) {
+__device__ void ticket_and_combine(const AttendParams& p, long long u, int* sh_flag, float* combine_scratch) {
   __threadfence();
   __syncthreads();
-  const int S_total = p.S_q + 1;
+  const int S_total = p.S_q + p.S_t;
   if (threadIdx.x == 0) {
     const unsigned prev = atomicAdd(p.counters + u, 1u);
     const int last = (prev == static_cast<unsigned>(S_total - 1));
@@ -130,25 +184,33 @@ __device__ void ticket_and_combine(const AttendParams& p, long long u, int* sh_f
   __syncthreads();
   if (*sh_flag) {
     __threadfence();
-    combine_unit<D>(p, u, S_total);
+    combine_unit<D>(p, u, S_total, combine_scratch);
   }
 }
 
 // ------------------------------------------------------------------------------
-// Tail CTA: residual bf16 tokens + causal pending tokens + selected 16-bit
-// tokens, fp32 on CUDA cores, online softmax over chunks of TC tokens.
+// Tail CTAs: residual bf16 tokens + causal pending tokens + selected 16-bit
+// tokens, fp32 on CUDA cores.  The tail of one (b, kv head) is split over
+// S_t CTAs.  Each stages 64-token chunks of K and V rows in shared memory (all
+// loads in flight), then computes logits (thread <-> (row, token)), an online
+// softmax, and P.V (thread <-> channel) from shared memory.
 // ------------------------------------------------------------------------------
 template <int D>
-__device__ void tail_partial(const AttendParams& p, long long u, uint8_t* smem) {
+__device__ void tail_partial(const AttendParams& p, long long u, int tsplit, uint8_t* smem) {
   using TS = TailSmem<D>;
   float* qt = reinterpret_cast<float*>(smem + TS::QT_OFF);
+  uint8_t* ks = smem + TS::K_OFF;
+  uint8_t* vs = smem + TS::V_OFF;
   float* lg = reinterpret_cast<float*>(smem + TS::LG_OFF);
   float* st_m = reinterpret_cast<float*>(smem + TS::ST_OFF);
   float* st_l = st_m + kMaxRows;
   float* st_a = st_l + kMaxRows;
+  int* tok_pend = reinterpret_cast<int*>(smem + TS::OK_OFF);   // -2 absent, -1 always visible, else pending index
   const int tid = threadIdx.x;
   const int b = static_cast<int>(u / p.c.Hkv), kvh = static_cast<int>(u % p.c.Hkv);
   const int R = p.R;
+  const int G = p.c.G;
+#pragma unroll 8
   for (int e = tid; e < kMaxRows * D; e += blockDim.x) {
     const int rho = e / D, d = e % D;
     float v = 0.f;
@@ -163,98 +225,102 @@ __device__ void tail_partial(const AttendParams& p, long long u, uint8_t* smem) 
     st_m[tid] = neg_inf();
     st_l[tid] = 0.f;
   }
-  __syncthreads();
-
-  const int G = p.c.G;
+  // this CTA's token range of the unit's tail list
   const int NT = p.c.r + p.P + p.top_k;
+  const int per = (NT + p.S_t - 1) / p.S_t;
+  const int t_lo = min(NT, tsplit * per), t_hi = min(NT, t_lo + per);
   float o[kMaxRows];
 #pragma unroll
   for (int r = 0; r < kMaxRows; ++r) o[r] = 0.f;
+  __syncthreads();
 
-  // K/V row pointer of tail token `t`, and whether it exists at all.
-  auto tail_row = [&](int t, const uint16_t*& kp, const uint16_t*& vp, int& pend) -> bool {
-    pend = -1;
-    if (t < p.c.r) {
-      const int slot = (p.c.res_start + t) % (2 * G);
-      const long long off = (u * 2 * G + slot) * D;
-      kp = p.c.res_k + off;
-      vp = p.c.res_v + off;
-      return true;
-    }
-    t -= p.c.r;
-    if (t < p.P) {
-      const long long off = (u * p.P + t) * D;
-      kp = p.pend_k + off;
-      vp = p.pend_v + off;
-      pend = t;
-      return true;
-    }
-    t -= p.P;
-    const int idx = p.sel_idx[u * p.top_k + t];
-    if (idx < 0 || idx >= p.c.Lq) return false;
-    const long long off = (u * p.top_k + t) * D;
-    kp = p.sel_k + off;
-    vp = p.sel_v + off;
-    return true;
-  };
-
-  for (int c0 = 0; c0 < NT; c0 += TS::TC) {
-    // logits
-    {
-      const int t = c0 + tid;
-      float acc[kMaxRows];
-#pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
+  constexpr int VEC = D / 8;   // 16-byte vectors per row
+  for (int c0 = t_lo; c0 < t_hi; c0 += TS::TC) {
+    const int nt = min(TS::TC, t_hi - c0);
+    // ---- stage K and V rows (16-byte vectors, all in flight) ----
+#pragma unroll 4
+    for (int e = tid; e < nt * VEC; e += blockDim.x) {
+      const int j = e / VEC, c = e % VEC;
+      int t = c0 + j;
       const uint16_t *kp = nullptr, *vp = nullptr;
-      int pend = -1;
-      const bool ok = (t < NT) && tail_row(t, kp, vp, pend);
-      if (ok) {
-        for (int d0 = 0; d0 < D; d0 += 8) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(kp + d0);
-          const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-          float kf[8];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            kf[2 * k] = __uint_as_float(w4[k] << 16);
-            kf[2 * k + 1] = __uint_as_float(w4[k] & 0xFFFF0000u);
-          }
-#pragma unroll
-          for (int r = 0; r < kMaxRows; ++r) {
-            if (r < R) {
-#pragma unroll
-              for (int k = 0; k < 8; ++k) acc[r] = fmaf(qt[r * D + d0 + k], kf[k], acc[r]);
-            }
-          }
+      int flag = -2;
+      if (t < p.c.r) {
+        const int slot = (p.c.res_start + t) % (2 * G);
+        const long long off = (u * 2 * G + slot) * D;
+        kp = p.c.res_k + off;
+        vp = p.c.res_v + off;
+        flag = -1;
+      } else if ((t -= p.c.r) < p.P) {
+        const long long off = (u * p.P + t) * D;
+        kp = p.pend_k + off;
+        vp = p.pend_v + off;
+        flag = t;
+      } else {
+        t -= p.P;
+        const int idx = p.sel_idx[u * p.top_k + t];
+        if (idx >= 0 && idx < p.c.Lq) {
+          const long long off = (u * p.top_k + t) * D;
+          kp = p.sel_k + off;
+          vp = p.sel_v + off;
+          flag = -1;
         }
       }
-#pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) {
-        bool vis = ok && r < R;
-        if (vis && pend >= 0) vis = pend <= p.P - p.gamma + r / p.HG;
-        lg[r * TS::TC + tid] = vis ? acc[r] : neg_inf();
+      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+      if (kp) {
+        kv = reinterpret_cast<const uint4*>(kp)[c];
+        vv = reinterpret_cast<const uint4*>(vp)[c];
       }
+      *reinterpret_cast<uint4*>(ks + j * TS::ROW + c * 16) = kv;
+      *reinterpret_cast<uint4*>(vs + j * TS::ROW + c * 16) = vv;
+      if (c == 0) tok_pend[j] = flag;
     }
     __syncthreads();
-    // row statistics (one warp per row)
+    // ---- logits: thread <-> (row, token) ----
+    for (int e = tid; e < kMaxRows * TS::TC; e += blockDim.x) {
+      const int rho = e / TS::TC, j = e % TS::TC;
+      float acc = neg_inf();
+      const int flag = (j < nt) ? tok_pend[j] : -2;
+      bool vis = (rho < R) && (flag != -2);
+      if (vis && flag >= 0) vis = flag <= p.P - p.gamma + rho / p.HG;
+      if (vis) {
+        acc = 0.f;
+        const float* qr = qt + rho * D;
+        const uint8_t* kr = ks + j * TS::ROW;
+#pragma unroll 4
+        for (int c = 0; c < VEC; ++c) {
+          const uint4 kw = *reinterpret_cast<const uint4*>(kr + c * 16);
+          const float4 qa = *reinterpret_cast<const float4*>(qr + 8 * c);
+          const float4 qb = *reinterpret_cast<const float4*>(qr + 8 * c + 4);
+          acc = fmaf(qa.x, __uint_as_float(kw.x << 16), acc);
+          acc = fmaf(qa.y, __uint_as_float(kw.x & 0xFFFF0000u), acc);
+          acc = fmaf(qa.z, __uint_as_float(kw.y << 16), acc);
+          acc = fmaf(qa.w, __uint_as_float(kw.y & 0xFFFF0000u), acc);
+          acc = fmaf(qb.x, __uint_as_float(kw.z << 16), acc);
+          acc = fmaf(qb.y, __uint_as_float(kw.z & 0xFFFF0000u), acc);
+          acc = fmaf(qb.z, __uint_as_float(kw.w << 16), acc);
+          acc = fmaf(qb.w, __uint_as_float(kw.w & 0xFFFF0000u), acc);
+        }
+      }
+      lg[rho * TS::TC + j] = acc;
+    }
+    __syncthreads();
+    // ---- online softmax statistics (one warp per row) ----
     {
       const int warp = tid / 32, lane = tid % 32;
+      static_assert(TS::TC == 32, "one token per lane");
       for (int r = warp; r < R; r += NTHREADS / 32) {
-        float mx = neg_inf();
-        for (int t = lane; t < TS::TC; t += 32) mx = fmaxf(mx, lg[r * TS::TC + t]);
+        const float x0 = lg[r * TS::TC + lane];
+        float mx = x0;
 #pragma unroll
-        for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+        for (int s2 = 16; s2 > 0; s2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s2));
         const float m_old = st_m[r];
         const float m_new = fmaxf(m_old, mx);
-        float sum = 0.f;
         const float msafe = (m_new == neg_inf()) ? 0.f : m_new;
-        for (int t = lane; t < TS::TC; t += 32) {
-          const float x = lg[r * TS::TC + t];
-          const float pr = (x == neg_inf()) ? 0.f : fast_exp2(x - msafe);
-          lg[r * TS::TC + t] = pr;
-          sum += pr;
-        }
+        const float p0 = (x0 == neg_inf()) ? 0.f : fast_exp2(x0 - msafe);
+        lg[r * TS::TC + lane] = p0;
+        float sum = p0;
 #pragma unroll
-        for (int s = 16; s > 0; s >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, s);
+        for (int s2 = 16; s2 > 0; s2 >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, s2);
         if (lane == 0) {
           const float alpha = (m_old == neg_inf()) ? 0.f : fast_exp2(m_old - msafe);
           st_a[r] = alpha;
@@ -264,17 +330,13 @@ __device__ void tail_partial(const AttendParams& p, long long u, uint8_t* smem) 
       }
     }
     __syncthreads();
-    // P.V: thread d accumulates channel d for all rows
+    // ---- P.V: thread d accumulates channel d for all rows ----
     if (tid < D) {
 #pragma unroll
       for (int r = 0; r < kMaxRows; ++r)
         if (r < R) o[r] *= st_a[r];
-      const int nt = min(TS::TC, NT - c0);
       for (int j = 0; j < nt; ++j) {
-        const uint16_t *kp = nullptr, *vp = nullptr;
-        int pend;
-        if (!tail_row(c0 + j, kp, vp, pend)) continue;
-        const float v = bf16_to_f32(vp[tid]);
+        const float v = bf16_to_f32(*reinterpret_cast<const uint16_t*>(vs + j * TS::ROW + tid * 2));
 #pragma unroll
         for (int r = 0; r < kMaxRows; ++r)
           if (r < R) o[r] = fmaf(lg[r * TS::TC + j], v, o[r]);
@@ -282,9 +344,9 @@ __device__ void tail_partial(const AttendParams& p, long long u, uint8_t* smem) 
     }
     __syncthreads();
   }
-  // write the partial (slot S_q of this unit)
+  // write the partial (index S_q + tsplit of this unit)
   const int PF = kPartialFloats(D);
-  float* dst = p.partials + (u * (p.S_q + 1) + p.S_q) * PF;
+  float* dst = p.partials + (u * (p.S_q + p.S_t) + p.S_q + tsplit) * PF;
   if (tid < kMaxRows) {
     dst[tid] = (tid < R) ? st_m[tid] : neg_inf();
     dst[kMaxRows + tid] = (tid < R) ? st_l[tid] : 0.f;
@@ -299,11 +361,13 @@ __device__ void tail_partial(const AttendParams& p, long long u, uint8_t* smem) 
 // ------------------------------------------------------------------------------
 // Quantized split
 // ------------------------------------------------------------------------------
+// Three CTAs per SM for one channel block per token (G = D, the hierarchical
+// cache's usual shape); the other variants keep more state per lane.
 template <int MODE, int D, int NJ>
-__global__ void __launch_bounds__(NTHREADS) attend_kernel(AttendParams p) {
+__global__ void __launch_bounds__(NTHREADS, (NJ == 1 ? 3 : 1)) attend_kernel(AttendParams p) {
   using M = Mode<MODE>;
   using RW = Rows<MODE, D>;
-  using L = Smem<MODE, D>;
+  using L = Smem<MODE, D, NJ>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int g = lane >> 2, q = lane & 3;
@@ -311,14 +375,16 @@ __global__ void __launch_bounds__(NTHREADS) attend_kernel(AttendParams p) {
   int* sh_flag = reinterpret_cast<int*>(smem + L::MISC_OFF);
   int* sh_abort = sh_flag + 1;
 
-  if (blockIdx.x < nunits) {  // ---------------- tail CTA ----------------
-    const long long u = blockIdx.x;
-    tail_partial<D>(p, u, smem);
-    ticket_and_combine<D>(p, u, sh_flag);
+  const long long ntail = nunits * p.S_t;
+  if (blockIdx.x < ntail) {  // ---------------- tail CTAs ----------------
+    const long long u = blockIdx.x / p.S_t;
+    tail_partial<D>(p, u, static_cast<int>(blockIdx.x % p.S_t), smem);
+    __syncthreads();
+    ticket_and_combine<D>(p, u, sh_flag, reinterpret_cast<float*>(smem));
     return;
   }
 
-  const long long qi = blockIdx.x - nunits;
+  const long long qi = blockIdx.x - ntail;
   const long long u = qi / p.S_q;
   const int split = static_cast<int>(qi % p.S_q);
   const int b = static_cast<int>(u / p.c.Hkv), kvh = static_cast<int>(u % p.c.Hkv);
@@ -330,13 +396,13 @@ __global__ void __launch_bounds__(NTHREADS) attend_kernel(AttendParams p) {
   constexpr int G = D / NJ;
   const int R = p.R;
 
-  float* qt = reinterpret_cast<float*>(smem + L::QT_OFF);
-  float* qh = reinterpret_cast<float*>(smem + L::QH_OFF);
+  float2* qx = reinterpret_cast<float2*>(smem + L::QX_OFF);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L::BM_OFF);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* empty = full + NSLOT;
 
-  // ---- setup ----
+  // ---- setup: barriers first, so the producer can start loading at once ----
+  const int bm_words = (ntok_chunk + 31) / 32;
   if (tid == 0) {
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(full + s, 1);
@@ -345,31 +411,39 @@ __global__ void __launch_bounds__(NTHREADS) attend_kernel(AttendParams p) {
     *sh_abort = 0;
     fence_mbar_init();
   }
-  const float qmul = static_cast<float>((1 << M::CB) * M::MULT);
-  for (int e = tid; e < kMaxRows * D; e += blockDim.x) {
-    const int rho = e / D, d = e % D;
-    float v = 0.f;
-    if (rho < R) {
-      const int i = rho / p.HG, hh = rho % p.HG;
-      const long long qoff = ((static_cast<long long>(b) * p.gamma + i) * p.Hq + kvh * p.HG + hh) * D + d;
-      v = bf16_to_f32(p.q[qoff]) * p.qscale;
-    }
-    qt[e] = v;
-    qh[e] = v * qmul;
-  }
-  const int bm_words = (ntok_chunk + 31) / 32;
   for (int e = tid; e < bm_words; e += blockDim.x) bitmap[e] = 0u;
   __syncthreads();
-  for (int j = tid; j < p.top_k; j += blockDim.x) {
-    const long long idx = p.sel_idx[u * p.top_k + j];
-    if (idx >= t_begin && idx < t_end) {
-      const int rel = static_cast<int>(idx - t_begin);
-      atomicOr(bitmap + rel / 32, 1u << (rel % 32));
-    }
-  }
-  __syncthreads();
-
   const long long u_tok = u * p.c.C;  // first token row of this unit in the planes
+  const float qmul = static_cast<float>((1 << M::CB) * M::MULT);
+  if (warp < NW) {
+    // consumers: folded queries and the selection bitmap, while the first tiles load
+    constexpr int NC = NW * 32;
+    // q^ = 2^CB * MULT * sm_scale * log2(e) * q, stored per (pair, lane) as the
+    // two channels that lane needs for that pair: conflict-free 8-byte reads
+#pragma unroll 4
+    for (int e = tid; e < (D / 8) * 32; e += NC) {
+      const int pp = e / 32, ln = e % 32;
+      const int rho = ln >> 2, qq = ln & 3;
+      float2 v = make_float2(0.f, 0.f);
+      if (rho < R) {
+        const int i = rho / p.HG, hh = rho % p.HG;
+        const long long qrow = ((static_cast<long long>(b) * p.gamma + i) * p.Hq + kvh * p.HG + hh) * D;
+        const int2 ch = pair_chan<MODE, D>(pp);
+        const int c0 = qq * (D / 4) + ch.x, c1 = qq * (D / 4) + ch.y;
+        v.x = bf16_to_f32(p.q[qrow + c0]) * p.qscale * qmul;
+        v.y = bf16_to_f32(p.q[qrow + c1]) * p.qscale * qmul;
+      }
+      qx[e] = v;
+    }
+    for (int j = tid; j < p.top_k; j += NC) {
+      const long long idx = p.sel_idx[u * p.top_k + j];
+      if (idx >= t_begin && idx < t_end) {
+        const int rel = static_cast<int>(idx - t_begin);
+        atomicOr(bitmap + rel / 32, 1u << (rel % 32));
+      }
+    }
+    asm volatile("bar.sync 2, %0;" ::"n"(NW * 32));
+  }
 
   if (warp == NW) {
     // ---------------- producer ----------------
@@ -445,20 +519,24 @@ __global__ void __launch_bounds__(NTHREADS) attend_kernel(AttendParams p) {
           cur_grp = grp;
           const float* ks = ksz + (grp - g_first) * 2 * D;
           const float* kz = ks + D;
-          float cpart = 0.f;
+          // correction sum_d (q~_d z_d - w'_d), with q~ = q^ / (2^CB MULT) exactly
+          float zsum = 0.f, wsum = 0.f;
 #pragma unroll
           for (int pp = 0; pp < D / 8; ++pp) {
             const int2 ch = pair_chan<MODE, D>(pp);
             const int c0 = qbase + ch.x, c1 = qbase + ch.y;
-            const float w0 = qh[g * D + c0] * ks[c0];
-            const float w1 = qh[g * D + c1] * ks[c1];
+            const float2 qv = qx[pp * 32 + lane];
+            const float w0 = qv.x * ks[c0];
+            const float w1 = qv.y * ks[c1];
             const uint32_t hi = pack_half2(w0, w1);
             const float2 hf = unpack_half2(hi);
             const uint32_t lo = pack_half2(w0 - hf.x, w1 - hf.y);
             wa[pp / 2][(pp % 2) * 2 + 0] = hi;
             wa[pp / 2][(pp % 2) * 2 + 1] = lo;
-            cpart += qt[g * D + c0] * kz[c0] + qt[g * D + c1] * kz[c1] - w0 - w1;
+            zsum = fmaf(qv.x, kz[c0], fmaf(qv.y, kz[c1], zsum));
+            wsum += w0 + w1;
           }
+          float cpart = fmaf(zsum, 1.0f / qmul, -wsum);
           cpart += __shfl_xor_sync(0xffffffffu, cpart, 1);
           cpart += __shfl_xor_sync(0xffffffffu, cpart, 2);
           corr = cpart;
@@ -466,13 +544,18 @@ __global__ void __launch_bounds__(NTHREADS) attend_kernel(AttendParams p) {
         // ---- S^T = W x K^T over 4 n-tiles of 8 tokens ----
         float c[4][4];
         const uint8_t* kslab = sbase + L::K_OFF + (32 * sl) * RW::KROW + q * RW::KCHUNK;
+        {
+          // the four n-tiles are independent accumulation chains: k-step outer
+          uint32_t P[4][D / 8];
 #pragma unroll
-        for (int jt = 0; jt < 4; ++jt) {
-          c[jt][0] = corr; c[jt][1] = corr; c[jt][2] = 0.f; c[jt][3] = 0.f;
-          uint32_t P[D / 8];
-          key_pairs<MODE, D>(kslab + (4 * g + jt) * RW::KROW, L::KPLANE, P);
+          for (int jt = 0; jt < 4; ++jt) {
+            c[jt][0] = corr; c[jt][1] = corr; c[jt][2] = 0.f; c[jt][3] = 0.f;
+            key_pairs<MODE, D>(kslab + (4 * g + jt) * RW::KROW, L::KPLANE, P[jt]);
+          }
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) mma16816(c[jt], wa[kk], P[2 * kk], P[2 * kk + 1]);
+          for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+            for (int jt = 0; jt < 4; ++jt) mma16816(c[jt], wa[kk], P[jt][2 * kk], P[jt][2 * kk + 1]);
         }
         // ---- mask + online softmax (row g; tokens 8q+jt and 8q+jt+4) ----
         const uint32_t bm = bitmap[static_cast<int>(tok0 - t_begin) / 32] >> (8 * q);
@@ -615,7 +698,7 @@ __global__ void __launch_bounds__(NTHREADS) attend_kernel(AttendParams p) {
     const float* wl = reinterpret_cast<const float*>(smem + L::WL_OFF);
     const float* wo = reinterpret_cast<const float*>(smem + L::WO_OFF);
     const int PF = kPartialFloats(D);
-    float* dst = p.partials + (u * (p.S_q + 1) + split) * PF;
+    float* dst = p.partials + (u * (p.S_q + p.S_t) + split) * PF;
     for (int e = tid; e < R * D; e += blockDim.x) {
       const int rho = e / D, d = e % D;
       float Mx = neg_inf();
@@ -639,19 +722,53 @@ __global__ void __launch_bounds__(NTHREADS) attend_kernel(AttendParams p) {
       }
     }
   }
-  ticket_and_combine<D>(p, u, sh_flag);
+  __syncthreads();
+  ticket_and_combine<D>(p, u, sh_flag, reinterpret_cast<float*>(smem));
 }
 
 template <int MODE, int D, int NJ>
 cudaError_t launch_t(const AttendParams& p, cudaStream_t s) {
-  using L = Smem<MODE, D>;
+  using L = Smem<MODE, D, NJ>;
   constexpr int smem = (L::TOTAL > TailSmem<D>::TOTAL) ? L::TOTAL : TailSmem<D>::TOTAL;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&attend_kernel<MODE, D, NJ>), smem);
   if (e != cudaSuccess) return e;
   const long long nunits = static_cast<long long>(p.c.B) * p.c.Hkv;
-  const long long grid = nunits * (p.S_q + 1);
+  const long long grid = nunits * (p.S_q + p.S_t);
   attend_kernel<MODE, D, NJ><<<static_cast<unsigned>(grid), NTHREADS, smem, s>>>(p);
   return cudaGetLastError();
+}
+
+// Resident CTAs per SM of one kernel variant times the SM count, queried once
+// per device (the split count is sized to fill whole waves).
+template <int MODE, int D, int NJ>
+int resident_ctas_t() {
+  constexpr int kMaxDev = 64;
+  static int cached[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  if (cached[dev] > 0) return cached[dev];
+  using L = Smem<MODE, D, NJ>;
+  constexpr int smem = (L::TOTAL > TailSmem<D>::TOTAL) ? L::TOTAL : TailSmem<D>::TOTAL;
+  if (set_smem_once(reinterpret_cast<const void*>(&attend_kernel<MODE, D, NJ>), smem) != cudaSuccess) return 0;
+  int per_sm = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attend_kernel<MODE, D, NJ>, NTHREADS, smem) != cudaSuccess)
+    return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cached[dev] = per_sm * sms;
+  return cached[dev];
+}
+
+template <int MODE>
+int resident_mode(int D, int NJ) {
+  if (D == 128) {
+    if (NJ == 1) return resident_ctas_t<MODE, 128, 1>();
+    if (NJ == 2) return resident_ctas_t<MODE, 128, 2>();
+    if (NJ == 4) return resident_ctas_t<MODE, 128, 4>();
+  } else if (D == 64) {
+    if (NJ == 1) return resident_ctas_t<MODE, 64, 1>();
+    if (NJ == 2) return resident_ctas_t<MODE, 64, 2>();
+  }
+  return 0;
 }
 
 template <int MODE>
@@ -669,6 +786,17 @@ cudaError_t launch_mode(const AttendParams& p, cudaStream_t s) {
 }
 
 }  // namespace
+
+int attend_resident_ctas(int mode, int D, int G) {
+  const int NJ = D / G;
+  switch (mode) {
+    case KVQ_MODE_INT8: return resident_mode<KVQ_MODE_INT8>(D, NJ);
+    case KVQ_MODE_INT4: return resident_mode<KVQ_MODE_INT4>(D, NJ);
+    case KVQ_MODE_INT2: return resident_mode<KVQ_MODE_INT2>(D, NJ);
+    case KVQ_MODE_INT1: return resident_mode<KVQ_MODE_INT1>(D, NJ);
+    default: return 0;
+  }
+}
 
 cudaError_t launch_attend(const AttendParams& p, int mode, cudaStream_t s) {
   switch (mode) {

@@ -16,6 +16,10 @@ constexpr int kTargetCtas = 608;       // 4 x 152 SMs: split-count target per la
 constexpr int kTopkMaxChunk = 8192;    // tokens per top-k split (scores held in shared memory)
 constexpr int kTopkMaxCand = 4096;     // splits x k candidates merged by the last CTA
 constexpr int kMaxTopk = 1024;
+constexpr int kMaxTailSplits = 8;      // CTAs per (b, kvh) for the bf16 tail
+constexpr int kMaxCombine = 256;       // partials per (b, kvh) merged by the combine
+constexpr int kMaxQuantSplits = kMaxCombine - kMaxTailSplits;
+constexpr int kTailTokensPerSplit = 48;
 constexpr int kStatusBytes = 256;      // workspace header (status word)
 constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s at 2 GHz
 __host__ __device__ constexpr int kPartialFloats(int D) { return 2 * kMaxRows + kMaxRows * D; }
@@ -50,8 +54,9 @@ struct AttendParams {
   float* lse;               // [B][gamma][Hq] or null
   int* status;
   unsigned* counters;       // [B*Hkv]
-  float* partials;          // [B*Hkv][S_q+1][kPartialFloats(D)]
+  float* partials;          // [B*Hkv][S_q+S_t][kPartialFloats(D)]
   int S_q;                  // quantized splits per (b, kvh)
+  int S_t;                  // tail splits per (b, kvh): residual + pending + selected tokens
   long long chunk;          // tokens per split (multiple of kChunkAlign)
   long long wait_limit;
 };
@@ -101,6 +106,9 @@ struct ResidualWriteParams {
 cudaError_t launch_flush(const FlushParams& p, cudaStream_t s);
 cudaError_t launch_residual_write(const ResidualWriteParams& p, cudaStream_t s);
 cudaError_t launch_attend(const AttendParams& p, int mode, cudaStream_t s);
+// CTAs of the attention kernel variant that fit on the current device at once
+// (0 if unknown).
+int attend_resident_ctas(int mode, int D, int G);
 cudaError_t launch_topk(const TopkParams& p, int mode, cudaStream_t s);
 cudaError_t launch_wait_selftest(int* status, long long limit, cudaStream_t s);
 

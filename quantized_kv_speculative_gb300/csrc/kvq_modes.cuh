@@ -34,7 +34,7 @@ struct Mode<KVQ_MODE_INT8> {
 };
 template <>
 struct Mode<KVQ_MODE_INT4> {
-  static constexpr int NP = 1, PB = 4, CB = 4, MULT = 16, TT = 64;
+  static constexpr int NP = 1, PB = 4, CB = 4, MULT = 16, TT = 32;
 };
 template <>
 struct Mode<KVQ_MODE_INT2> {

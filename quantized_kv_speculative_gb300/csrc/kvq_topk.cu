@@ -209,13 +209,22 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
           neg_lo = -slo;
         }
         const uint8_t* kslab = sbase + (32 * sl) * RW::KROW + q * RW::KCHUNK;
+        float cc[4][4];
+        {
+          uint32_t P[4][D / 8];
+#pragma unroll
+          for (int jt = 0; jt < 4; ++jt) {
+            cc[jt][0] = neg_hi; cc[jt][1] = neg_hi; cc[jt][2] = neg_lo; cc[jt][3] = neg_lo;
+            key_pairs<MODE, D>(kslab + (4 * g + jt) * RW::KROW, 0, P[jt]);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+            for (int jt = 0; jt < 4; ++jt) mma16816(cc[jt], wa[kk], P[jt][2 * kk], P[jt][2 * kk + 1]);
+        }
 #pragma unroll
         for (int jt = 0; jt < 4; ++jt) {
-          float c[4] = {neg_hi, neg_hi, neg_lo, neg_lo};
-          uint32_t P[D / 8];
-          key_pairs<MODE, D>(kslab + (4 * g + jt) * RW::KROW, 0, P);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) mma16816(c, wa[kk], P[2 * kk], P[2 * kk + 1]);
+          const float* c = cc[jt];
           if (g == 0) {
             const int rel = static_cast<int>(tok0 - t_begin) + 8 * q + jt;
 #pragma unroll
@@ -259,24 +268,53 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
       for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0u;
       __syncthreads();
       const uint32_t prefix = static_cast<uint32_t>(st[0]), mask = static_cast<uint32_t>(st[1]);
-      for (int i = tid; i < n; i += blockDim.x) {
-        const uint32_t key = order_key(scores[i]);
-        if ((key & mask) == prefix) atomicAdd(hist + ((key >> shift) & 255u), 1u);
+      // warp-aggregated histogram: lanes with the same bin add once
+      const int nround = (n + blockDim.x - 1) / blockDim.x * blockDim.x;
+      for (int i = tid; i < nround; i += blockDim.x) {
+        bool take = false;
+        uint32_t bin = 0xFFFFFFFFu;
+        if (i < n) {
+          const uint32_t key = order_key(scores[i]);
+          take = (key & mask) == prefix;
+          if (take) bin = (key >> shift) & 255u;
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+        if (take && (__ffs(peers) - 1) == lane) atomicAdd(hist + bin, static_cast<uint32_t>(__popc(peers)));
       }
       __syncthreads();
-      if (tid == 0) {
-        int remaining = st[2], cum = 0, digit = 0;
-        for (int dg = 255; dg >= 0; --dg) {
-          const int h = static_cast<int>(hist[dg]);
-          if (cum + h >= remaining) {
-            digit = dg;
-            break;
-          }
-          cum += h;
+      if (warp == 0) {
+        // Find the digit holding the `remaining`-th largest key: lane l owns bins
+        // 255-8l .. 248-8l (descending); a warp scan gives the count above each lane.
+        uint32_t c[8];
+        uint32_t tot = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          c[k] = hist[255 - 8 * lane - k];
+          tot += c[k];
         }
-        st[2] = remaining - cum;
-        st[0] = static_cast<int>(prefix | (static_cast<uint32_t>(digit) << shift));
-        st[1] = static_cast<int>(mask | (255u << shift));
+        uint32_t inc = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += v;
+        }
+        const uint32_t excl = inc - tot;
+        const uint32_t remaining = static_cast<uint32_t>(st[2]);
+        if (excl < remaining && remaining <= inc) {
+          uint32_t cum = excl;
+          int digit = 255 - 8 * lane - 7;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            if (cum + c[k] >= remaining) {
+              digit = 255 - 8 * lane - k;
+              break;
+            }
+            cum += c[k];
+          }
+          st[2] = static_cast<int>(remaining - cum);
+          st[0] = static_cast<int>(prefix | (static_cast<uint32_t>(digit) << shift));
+          st[1] = static_cast<int>(mask | (255u << shift));
+        }
       }
       __syncthreads();
     }
