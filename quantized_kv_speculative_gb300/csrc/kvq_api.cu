@@ -88,13 +88,16 @@ int attend_splits_max(const kvq_cache_desc* d) {
   return static_cast<int>(std::max(S, 1LL));
 }
 
-int topk_splits(long long Lq, long long U, long long* chunk) {
+// Top-k splits per (b, kvh) and the chunk size.  The splits fill one wave of
+// the `slots` CTAs that fit on the device, within the candidate and chunk limits.
+int topk_splits(long long Lq, long long U, long long slots, int k, long long* chunk) {
   if (Lq <= 0) {
     *chunk = 0;
     return 1;
   }
-  const long long target = std::max(1LL, ceil_div(kTargetCtas, U));
-  long long S = std::min(ceil_div(Lq, 512), target);
+  const long long want = slots > 0 ? std::max(1LL, std::min<long long>(slots, kTopkMaxCtas) / U)
+                                   : std::max(1LL, ceil_div(kTargetCtas, U));
+  long long S = std::min(std::min(ceil_div(Lq, kTopkMinChunk), want), std::max(1LL, static_cast<long long>(kTopkMaxCand / k)));
   S = std::max(S, ceil_div(Lq, kTopkMaxChunk));
   S = std::max(S, 1LL);
   long long ch = ceil_div(ceil_div(Lq, S), kChunkAlign) * kChunkAlign;
@@ -102,12 +105,13 @@ int topk_splits(long long Lq, long long U, long long* chunk) {
   return static_cast<int>(ceil_div(Lq, ch));
 }
 
-int topk_splits_max(const kvq_cache_desc* d) {
+// Largest split count topk_splits can return for this cache and k (any fill, any device).
+int topk_splits_max(const kvq_cache_desc* d, int k) {
   const long long U = static_cast<long long>(d->batch) * d->num_kv_heads;
   const long long Lq = d->capacity_tokens;
   if (Lq <= 0) return 1;
-  const long long target = std::max(1LL, ceil_div(kTargetCtas, U));
-  long long S = std::min(ceil_div(Lq, 512), target);
+  const long long want = std::max(std::max(1LL, kTopkMaxCtas / U), std::max(1LL, ceil_div(kTargetCtas, U)));
+  long long S = std::min(std::min(ceil_div(Lq, kTopkMinChunk), want), std::max(1LL, static_cast<long long>(kTopkMaxCand / k)));
   S = std::max(S, ceil_div(Lq, kTopkMaxChunk));
   return static_cast<int>(std::max(S, 1LL));
 }
@@ -120,7 +124,7 @@ size_t attend_ws_bytes(const kvq_cache_desc* d) {
 
 size_t topk_ws_bytes(const kvq_cache_desc* d, int k) {
   const size_t U = static_cast<size_t>(d->batch) * d->num_kv_heads;
-  const size_t S = static_cast<size_t>(topk_splits_max(d));
+  const size_t S = static_cast<size_t>(topk_splits_max(d, k));
   return align256(U * 4) + 2 * align256(U * S * static_cast<size_t>(k) * 4);
 }
 
@@ -358,7 +362,7 @@ kvq_status kvq_topk(const kvq_cache* cache, kvq_mode mode, const void* q_spec, i
   if (!workspace || !aligned16(workspace) || ws_bytes < need) return KVQ_ERR_WORKSPACE;
   const long long U = units_of(cache);
   long long chunk = 0;
-  const int S = topk_splits(cache->quantized_len, U, &chunk);
+  const int S = topk_splits(cache->quantized_len, U, topk_resident_ctas(mode, cache->desc.head_dim), top_k, &chunk);
   if (static_cast<long long>(S) * top_k > kTopkMaxCand) return KVQ_ERR_UNSUPPORTED;
   TopkParams p{};
   p.c = view_of(cache);
@@ -371,7 +375,7 @@ kvq_status kvq_topk(const kvq_cache* cache, kvq_mode mode, const void* q_spec, i
   uint8_t* ws = static_cast<uint8_t*>(workspace) + kStatusBytes + att;
   p.status = static_cast<int*>(workspace);
   p.counters = reinterpret_cast<unsigned*>(ws);
-  const size_t Smax = static_cast<size_t>(topk_splits_max(&cache->desc));
+  const size_t Smax = static_cast<size_t>(topk_splits_max(&cache->desc, top_k));
   p.cand_score = reinterpret_cast<float*>(ws + align256(U * 4));
   p.cand_idx = reinterpret_cast<int32_t*>(ws + align256(U * 4) + align256(U * Smax * top_k * 4));
   p.S = S;

@@ -15,6 +15,8 @@ constexpr int kMaxChunk = 32768;       // tokens per attention split (bounds the
 constexpr int kTargetCtas = 608;       // 4 x 152 SMs: split-count target per launch
 constexpr int kTopkMaxChunk = 8192;    // tokens per top-k split (scores held in shared memory)
 constexpr int kTopkMaxCand = 4096;     // splits x k candidates merged by the last CTA
+constexpr int kTopkMaxCtas = 2048;     // bound on the CTAs of one top-k wave (sizes the workspace)
+constexpr int kTopkMinChunk = 512;     // fewest tokens per top-k split
 constexpr int kMaxTopk = 1024;
 constexpr int kMaxTailSplits = 8;      // CTAs per (b, kvh) for the bf16 tail
 constexpr int kMaxCombine = 256;       // partials per (b, kvh) merged by the combine
@@ -110,6 +112,8 @@ cudaError_t launch_attend(const AttendParams& p, int mode, cudaStream_t s);
 // (0 if unknown).
 int attend_resident_ctas(int mode, int D, int G);
 cudaError_t launch_topk(const TopkParams& p, int mode, cudaStream_t s);
+// CTAs of the top-k kernel variant that fit on the current device at once (0 if unknown).
+int topk_resident_ctas(int mode, int D);
 cudaError_t launch_wait_selftest(int* status, long long limit, cudaStream_t s);
 
 }  // namespace kvq

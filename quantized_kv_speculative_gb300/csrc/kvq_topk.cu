@@ -15,11 +15,12 @@
 // fp32 accumulation is exact in any order.  fp32(S_t) = fp32(2048 S_hi + S_lo) is
 // then a single correctly rounded fp32 add of two exact values.
 //
-// One launch: B*Hkv*S CTAs.  Each CTA scores one chunk (bulk-copied tiles on an
-// mbarrier ring, as in attention), radix-selects its top k by (score desc,
-// index asc), and writes k candidates.  The last CTA of each (b, kvh), found
-// through an atomic ticket, sorts the S*k candidates (bitonic, 64-bit keys)
-// and writes the final list.
+// One launch: B*Hkv*S CTAs, sized to run in a single wave.  Each CTA scores one
+// chunk (bulk-copied tiles on an mbarrier ring, as in attention) into 32-bit
+// order keys, radix-selects its top k by (score desc, index asc), and writes k
+// candidates.  The last CTA of each (b, kvh), found through an atomic ticket,
+// radix-selects the k best of the S*k candidates under the unique composite key
+// (order key, ~index), then places each winner by counting the winners above it.
 #include "kvq_modes.cuh"
 
 namespace kvq {
@@ -39,7 +40,7 @@ struct TopkSmem {
   static constexpr int KSZ_OFF = KPLANE;                      // only the upper/only plane is read
   static constexpr int KSZ_BYTES = (TT / 32) * 2 * D * 4;
   static constexpr int SLOT = KSZ_OFF + KSZ_BYTES;
-  static constexpr int SC_OFF = NSLOT * SLOT;                 // scores / merge keys
+  static constexpr int SC_OFF = NSLOT * SLOT;                 // order keys / merge keys
   static constexpr int SC_BYTES = kTopkMaxCand * 8;           // >= kTopkMaxChunk * 4
   static constexpr int QS_OFF = SC_OFF + SC_BYTES;            // qs[D]
   static constexpr int HIST_OFF = QS_OFF + D * 4;             // hist[256]
@@ -48,6 +49,7 @@ struct TopkSmem {
   static constexpr int TOTAL = MISC_OFF + 64;
   static_assert(kTopkMaxChunk * 4 <= SC_BYTES, "chunk scores must fit");
   static_assert(SLOT % 16 == 0, "slots must stay 16-byte aligned");
+  static_assert(NSLOT * SLOT >= 2 * kMaxTopk * 4, "the merge winners reuse the stage area");
 };
 
 __device__ __forceinline__ uint32_t order_key(float s) {
@@ -62,6 +64,74 @@ __device__ __forceinline__ float key_to_score(uint32_t k) {
 
 __device__ __forceinline__ float pow2f(int e) {  // 2^e for -126 <= e <= 127
   return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+
+// Block-wide radix select, 8-bit digits from the most significant.  Among the
+// i < n for which take(i, key) is true, it finds the kth largest key T
+// (1 <= kth <= number taken).  On return st[0] = T and st[2] = how many of the
+// taken keys equal to T belong to the kth largest.  Every thread of the block
+// calls it; st[0..2] and hist[256] are shared memory.
+template <typename F>
+__device__ void radix_select(int n, int kth, F take, uint32_t* hist, int* st) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    st[0] = 0;
+    st[1] = 0;
+    st[2] = kth;
+  }
+  const int nround = (n + blockDim.x - 1) / blockDim.x * blockDim.x;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0u;
+    __syncthreads();
+    const uint32_t prefix = static_cast<uint32_t>(st[0]), mask = static_cast<uint32_t>(st[1]);
+    // warp-aggregated histogram: lanes with the same bin add once
+    for (int i = tid; i < nround; i += blockDim.x) {
+      uint32_t key = 0, bin = 0xFFFFFFFFu;
+      bool ok = false;
+      if (i < n) {
+        ok = take(i, key) && (key & mask) == prefix;
+        if (ok) bin = (key >> shift) & 255u;
+      }
+      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+      if (ok && (__ffs(peers) - 1) == lane) atomicAdd(hist + bin, static_cast<uint32_t>(__popc(peers)));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // Lane l owns bins 255-8l .. 248-8l (descending); a warp scan gives the
+      // count above each lane, and the lane holding the kth key picks its digit.
+      uint32_t c[8];
+      uint32_t tot = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        c[k] = hist[255 - 8 * lane - k];
+        tot += c[k];
+      }
+      uint32_t inc = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v;
+      }
+      const uint32_t excl = inc - tot;
+      const uint32_t remaining = static_cast<uint32_t>(st[2]);
+      if (excl < remaining && remaining <= inc) {
+        uint32_t cum = excl;
+        int digit = 255 - 8 * lane - 7;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (cum + c[k] >= remaining) {
+            digit = 255 - 8 * lane - k;
+            break;
+          }
+          cum += c[k];
+        }
+        st[2] = static_cast<int>(remaining - cum);
+        st[0] = static_cast<int>(prefix | (static_cast<uint32_t>(digit) << shift));
+        st[1] = static_cast<int>(mask | (255u << shift));
+      }
+    }
+    __syncthreads();
+  }
 }
 
 template <int MODE, int D>
@@ -83,7 +153,7 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   const int per_warp = (ntiles + NW - 1) / NW;
   const int K = p.k;
 
-  float* scores = reinterpret_cast<float*>(smem + L::SC_OFF);
+  uint32_t* okeys = reinterpret_cast<uint32_t*>(smem + L::SC_OFF);
   float* qs = reinterpret_cast<float*>(smem + L::QS_OFF);
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L::HIST_OFF);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -232,7 +302,7 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
               const float shi_t = __fmul_rn(c[e2], cbmul);       // exact integer
               const float slo_t = __fmul_rn(c[2 + e2], cbmul);
               const float sf = __fadd_rn(__fmul_rn(2048.f, shi_t), slo_t);
-              scores[rel + 4 * e2] = __fadd_rn(__fmul_rn(sf, unit), beta);
+              okeys[rel + 4 * e2] = order_key(__fadd_rn(__fmul_rn(sf, unit), beta));
             }
           }
         }
@@ -253,83 +323,24 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   }
   __syncthreads();
 
-  // ---------------- radix select of the chunk's top k ----------------
+  // ---------------- the chunk's top k: radix select on the order keys ----------------
   const int keff = min(K, n);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + L::SC_OFF);
   int* st = misc + 2;  // st[0] prefix, st[1] mask, st[2] remaining, st[3] count
-  if (tid == 0) {
-    st[0] = 0;
-    st[1] = 0;
-    st[2] = keff;
-    st[3] = 0;
-  }
-  __syncthreads();
-  if (keff > 0) {
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0u;
-      __syncthreads();
-      const uint32_t prefix = static_cast<uint32_t>(st[0]), mask = static_cast<uint32_t>(st[1]);
-      // warp-aggregated histogram: lanes with the same bin add once
-      const int nround = (n + blockDim.x - 1) / blockDim.x * blockDim.x;
-      for (int i = tid; i < nround; i += blockDim.x) {
-        bool take = false;
-        uint32_t bin = 0xFFFFFFFFu;
-        if (i < n) {
-          const uint32_t key = order_key(scores[i]);
-          take = (key & mask) == prefix;
-          if (take) bin = (key >> shift) & 255u;
-        }
-        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-        if (take && (__ffs(peers) - 1) == lane) atomicAdd(hist + bin, static_cast<uint32_t>(__popc(peers)));
-      }
-      __syncthreads();
-      if (warp == 0) {
-        // Find the digit holding the `remaining`-th largest key: lane l owns bins
-        // 255-8l .. 248-8l (descending); a warp scan gives the count above each lane.
-        uint32_t c[8];
-        uint32_t tot = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          c[k] = hist[255 - 8 * lane - k];
-          tot += c[k];
-        }
-        uint32_t inc = tot;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
-          if (lane >= o) inc += v;
-        }
-        const uint32_t excl = inc - tot;
-        const uint32_t remaining = static_cast<uint32_t>(st[2]);
-        if (excl < remaining && remaining <= inc) {
-          uint32_t cum = excl;
-          int digit = 255 - 8 * lane - 7;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            if (cum + c[k] >= remaining) {
-              digit = 255 - 8 * lane - k;
-              break;
-            }
-            cum += c[k];
-          }
-          st[2] = static_cast<int>(remaining - cum);
-          st[0] = static_cast<int>(prefix | (static_cast<uint32_t>(digit) << shift));
-          st[1] = static_cast<int>(mask | (255u << shift));
-        }
-      }
-      __syncthreads();
-    }
-  }
-  const uint32_t T = static_cast<uint32_t>(st[0]);
-  const int need_eq = st[2];
-  const int n_gt = keff - need_eq;
   float* cs = p.cand_score + (u * p.S + split) * K;
   int32_t* ci = p.cand_idx + (u * p.S + split) * K;
   if (keff > 0) {
+    radix_select(n, keff, [&](int i, uint32_t& key) { key = keys[i]; return true; }, hist, st);
+    const uint32_t T = static_cast<uint32_t>(st[0]);
+    const int need_eq = st[2];
+    const int n_gt = keff - need_eq;
+    if (tid == 0) st[3] = 0;
+    __syncthreads();
     for (int i = tid; i < n; i += blockDim.x) {
-      const uint32_t key = order_key(scores[i]);
+      const uint32_t key = keys[i];
       if (key > T) {
         const int pos = atomicAdd(st + 3, 1);
-        cs[pos] = scores[i];
+        cs[pos] = key_to_score(key);
         ci[pos] = static_cast<int32_t>(t_begin + i);
       }
     }
@@ -337,11 +348,11 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
       int taken = 0;
       for (int base = 0; base < n && taken < need_eq; base += 32) {
         const int i = base + lane;
-        const bool eq = (i < n) && (order_key(scores[i]) == T);
+        const bool eq = (i < n) && (keys[i] == T);
         const uint32_t bal = __ballot_sync(0xffffffffu, eq);
         const int before = __popc(bal & ((1u << lane) - 1u));
         if (eq && taken + before < need_eq) {
-          cs[n_gt + taken + before] = scores[i];
+          cs[n_gt + taken + before] = key_to_score(T);
           ci[n_gt + taken + before] = static_cast<int32_t>(t_begin + i);
         }
         taken += __popc(bal);
@@ -353,7 +364,7 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
     ci[i] = -1;
   }
 
-  // ---------------- ticket: last CTA merges ----------------
+  // ---------------- ticket: the last CTA of the unit merges ----------------
   __threadfence();
   __syncthreads();
   if (tid == 0) {
@@ -361,54 +372,66 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
     const int last = (prev == static_cast<unsigned>(p.S - 1));
     if (last) atomicExch(p.counters + u, 0u);
     misc[1] = last;
+    st[3] = 0;
   }
   __syncthreads();
   if (!misc[1]) return;
   __threadfence();
+  // Candidates as unique composite keys (order key, ~index): larger is better.
   const int NC = p.S * K;
-  int N2 = 1;
-  while (N2 < NC) N2 <<= 1;
-  uint64_t* keys = reinterpret_cast<uint64_t*>(smem + L::SC_OFF);
+  uint32_t* khi = keys;                 // [NC] order keys, 0 for padding
+  uint32_t* klo = keys + kTopkMaxCand;  // [NC] ~index
   const float* us = p.cand_score + u * p.S * K;
   const int32_t* ui = p.cand_idx + u * p.S * K;
-  for (int i = tid; i < N2; i += blockDim.x) {
-    uint64_t key = 0;
-    if (i < NC) {
-      const int32_t idx = __ldcg(ui + i);
-      if (idx >= 0) {
-        key = (static_cast<uint64_t>(order_key(__ldcg(us + i))) << 32) |
-              static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(idx));
-      }
-    }
-    keys[i] = key;
+  for (int i = tid; i < NC; i += blockDim.x) {
+    const int32_t idx = __ldcg(ui + i);
+    const bool ok = idx >= 0;
+    khi[i] = ok ? order_key(__ldcg(us + i)) : 0u;
+    klo[i] = ok ? 0xFFFFFFFFu - static_cast<uint32_t>(idx) : 0u;
+    if (ok) atomicAdd(st + 3, 1);
   }
   __syncthreads();
-  for (int k2 = 2; k2 <= N2; k2 <<= 1) {
-    for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
-      for (int i = tid; i < N2; i += blockDim.x) {
-        const int ixj = i ^ j2;
-        if (ixj > i) {
-          const uint64_t a = keys[i], c = keys[ixj];
-          const bool swap = ((i & k2) == 0) ? (a < c) : (a > c);
-          if (swap) {
-            keys[i] = c;
-            keys[ixj] = a;
-          }
-        }
+  const int nvalid = st[3];
+  const int kf = min(K, nvalid);
+  uint32_t* whi = reinterpret_cast<uint32_t*>(smem);   // winners, in the (idle) stage area
+  uint32_t* wlo = whi + kMaxTopk;
+  if (kf > 0) {
+    // order keys first, then the index among keys equal to the k-th order key
+    radix_select(NC, kf, [&](int i, uint32_t& key) { key = khi[i]; return klo[i] != 0u; }, hist, st);
+    const uint32_t Thi = static_cast<uint32_t>(st[0]);
+    const int rem = st[2];
+    __syncthreads();
+    radix_select(NC, rem, [&](int i, uint32_t& key) { key = klo[i]; return klo[i] != 0u && khi[i] == Thi; },
+                 hist, st);
+    const uint32_t Tlo = static_cast<uint32_t>(st[0]);
+    if (tid == 0) st[3] = 0;
+    __syncthreads();
+    for (int i = tid; i < NC; i += blockDim.x) {
+      const uint32_t h = khi[i], l = klo[i];
+      if (l != 0u && (h > Thi || (h == Thi && l >= Tlo))) {
+        const int pos = atomicAdd(st + 3, 1);
+        whi[pos] = h;
+        wlo[pos] = l;
       }
-      __syncthreads();
+    }
+    __syncthreads();
+    // rank sort of the kf winners (all composite keys differ)
+    for (int i = tid; i < kf; i += blockDim.x) {
+      const uint32_t h = whi[i], l = wlo[i];
+      int rank = 0;
+      for (int j = 0; j < kf; ++j) {
+        const uint32_t hj = whi[j], lj = wlo[j];
+        rank += (hj > h || (hj == h && lj > l)) ? 1 : 0;
+      }
+      const long long o = u * K + rank;
+      p.idx_out[o] = static_cast<int32_t>(0xFFFFFFFFu - l);
+      if (p.score_out) p.score_out[o] = key_to_score(h);
     }
   }
-  for (int i = tid; i < K; i += blockDim.x) {
-    const uint64_t key = keys[i];
+  for (int i = kf + tid; i < K; i += blockDim.x) {
     const long long o = u * K + i;
-    if (key == 0) {
-      p.idx_out[o] = -1;
-      if (p.score_out) p.score_out[o] = neg_inf();
-    } else {
-      p.idx_out[o] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFu));
-      if (p.score_out) p.score_out[o] = key_to_score(static_cast<uint32_t>(key >> 32));
-    }
+    p.idx_out[o] = -1;
+    if (p.score_out) p.score_out[o] = neg_inf();
   }
 }
 
@@ -422,7 +445,34 @@ cudaError_t launch_t(const TopkParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Resident CTAs per SM of one variant times the SM count, queried once per device.
+template <int MODE, int D>
+int resident_ctas_t() {
+  constexpr int kMaxDev = 64;
+  static int cached[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  if (cached[dev] > 0) return cached[dev];
+  constexpr int smem = TopkSmem<MODE, D>::TOTAL;
+  if (set_smem_once(reinterpret_cast<const void*>(&topk_kernel<MODE, D>), smem) != cudaSuccess) return 0;
+  int per_sm = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<MODE, D>, NTHREADS, smem) != cudaSuccess)
+    return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cached[dev] = per_sm * sms;
+  return cached[dev];
+}
+
 }  // namespace
+
+int topk_resident_ctas(int mode, int D) {
+  switch (mode) {
+    case KVQ_MODE_INT4: return D == 128 ? resident_ctas_t<KVQ_MODE_INT4, 128>() : resident_ctas_t<KVQ_MODE_INT4, 64>();
+    case KVQ_MODE_INT2: return D == 128 ? resident_ctas_t<KVQ_MODE_INT2, 128>() : resident_ctas_t<KVQ_MODE_INT2, 64>();
+    case KVQ_MODE_INT1: return D == 128 ? resident_ctas_t<KVQ_MODE_INT1, 128>() : resident_ctas_t<KVQ_MODE_INT1, 64>();
+    default: return 0;
+  }
+}
 
 cudaError_t launch_topk(const TopkParams& p, int mode, cudaStream_t s) {
   const int D = p.c.D;
