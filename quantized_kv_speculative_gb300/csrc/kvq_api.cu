@@ -61,14 +61,14 @@ long long units_of(const kvq_cache* c) {
 }
 
 // Quantized splits per (b, kvh) for attention, and the chunk size.  `slots` is
-// how many CTAs of the kernel fit on the device at once: the splits fill whole
-// waves of it.
-int attend_splits(long long Lq, long long U, long long slots, long long* chunk) {
+// how many CTAs of the kernel fit on the device at once; together with the
+// `tail` CTAs per (b, kvh) the splits fill one wave of it where they can.
+int attend_splits(long long Lq, long long U, long long slots, long long tail, long long* chunk) {
   if (Lq <= 0) {
     *chunk = 0;
     return 0;
   }
-  const long long want = slots > 0 ? std::max(1LL, slots / U) : ceil_div(kTargetCtas, U);
+  const long long want = slots > 0 ? std::max(1LL, slots / U - tail) : ceil_div(kTargetCtas, U);
   const long long target = std::min<long long>(kMaxQuantSplits, std::min(want, std::max(1LL, ceil_div(kTargetCtas, U))));
   long long S = std::min(ceil_div(Lq, kChunkAlign), target);
   S = std::max(S, ceil_div(Lq, kMaxChunk));
@@ -88,30 +88,14 @@ int attend_splits_max(const kvq_cache_desc* d) {
   return static_cast<int>(std::max(S, 1LL));
 }
 
-// Top-k splits per (b, kvh) and the chunk size.  The splits fill one wave of
-// the `slots` CTAs that fit on the device, within the candidate and chunk limits.
-int topk_splits(long long Lq, long long U, long long slots, int k, long long* chunk) {
-  if (Lq <= 0) {
-    *chunk = 0;
-    return 1;
-  }
-  const long long want = slots > 0 ? std::max(1LL, std::min<long long>(slots, kTopkMaxCtas) / U)
-                                   : std::max(1LL, ceil_div(kTargetCtas, U));
-  long long S = std::min(std::min(ceil_div(Lq, kTopkMinChunk), want), std::max(1LL, static_cast<long long>(kTopkMaxCand / k)));
-  S = std::max(S, ceil_div(Lq, kTopkMaxChunk));
-  S = std::max(S, 1LL);
-  long long ch = ceil_div(ceil_div(Lq, S), kChunkAlign) * kChunkAlign;
-  *chunk = ch;
-  return static_cast<int>(ceil_div(Lq, ch));
-}
-
-// Largest split count topk_splits can return for this cache and k (any fill, any device).
+// Largest split count topk_plan can return for this cache and k (any fill,
+// any device): its chunks are multiples of kChunkAlign tokens and at most
+// kTopkMaxChunk, and S * k stays within kTopkMaxCand unless the chunk limit
+// alone needs more splits.
 int topk_splits_max(const kvq_cache_desc* d, int k) {
-  const long long U = static_cast<long long>(d->batch) * d->num_kv_heads;
   const long long Lq = d->capacity_tokens;
   if (Lq <= 0) return 1;
-  const long long want = std::max(std::max(1LL, kTopkMaxCtas / U), std::max(1LL, ceil_div(kTargetCtas, U)));
-  long long S = std::min(std::min(ceil_div(Lq, kTopkMinChunk), want), std::max(1LL, static_cast<long long>(kTopkMaxCand / k)));
+  long long S = std::min(ceil_div(Lq, kChunkAlign), std::max(1LL, static_cast<long long>(kTopkMaxCand / k)));
   S = std::max(S, ceil_div(Lq, kTopkMaxChunk));
   return static_cast<int>(std::max(S, 1LL));
 }
@@ -332,13 +316,13 @@ kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int3
   p.counters = reinterpret_cast<unsigned*>(ws + kStatusBytes);
   p.partials = reinterpret_cast<float*>(ws + kStatusBytes + align256(U * 4));
   long long chunk = 0;
-  const long long slots = attend_resident_ctas(mode, cache->desc.head_dim, cache->desc.group_size);
-  p.S_q = attend_splits(cache->quantized_len, U, slots, &chunk);
-  p.chunk = chunk;
+  const long long slots = attend_resident_ctas(mode, cache->desc.head_dim, cache->desc.group_size, gamma * HG);
   {
     const long long nt = static_cast<long long>(cache->residual_len) + n_pend + top_k;
     p.S_t = static_cast<int>(std::min<long long>(kMaxTailSplits, std::max(1LL, ceil_div(nt, kTailTokensPerSplit))));
   }
+  p.S_q = attend_splits(cache->quantized_len, U, slots, p.S_t, &chunk);
+  p.chunk = chunk;
   p.wait_limit = kDefaultWaitLimit;
   if (p.S_q > attend_splits_max(&cache->desc)) return KVQ_ERR_WORKSPACE;
   if (launch_attend(p, mode, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -362,7 +346,7 @@ kvq_status kvq_topk(const kvq_cache* cache, kvq_mode mode, const void* q_spec, i
   if (!workspace || !aligned16(workspace) || ws_bytes < need) return KVQ_ERR_WORKSPACE;
   const long long U = units_of(cache);
   long long chunk = 0;
-  const int S = topk_splits(cache->quantized_len, U, topk_resident_ctas(mode, cache->desc.head_dim), top_k, &chunk);
+  const int S = topk_plan(mode, cache->desc.head_dim, cache->desc.group_size, cache->quantized_len, U, top_k, &chunk);
   if (static_cast<long long>(S) * top_k > kTopkMaxCand) return KVQ_ERR_UNSUPPORTED;
   TopkParams p{};
   p.c = view_of(cache);

@@ -8,35 +8,39 @@
 // low-bit copy is attended with the output token and a speculative token, and
 // the top-k tokens use their 16-bit KV (SpeCache page, "Approach").
 //
-// One launch, grid = B*Hkv tail CTAs followed by B*Hkv*S_q quantized-split CTAs.
+// One launch, grid = B*Hkv*S_t tail CTAs followed by B*Hkv*S_q quantized-split CTAs.
 //  * Quantized split: one producer warp streams 32..64-token tiles of the
 //    mode's planes and scales into shared memory with 1-D bulk (TMA) copies on
 //    an mbarrier ring.  Four consumer warps each own a contiguous run of tiles.
-//    They dequantize in registers and run QK^T and PV on tensor cores
-//    (m16n8k16, f16 codes exact; the folded key weights and the folded
-//    probabilities are each split into high + low f16 parts).
-//    Softmax is online in fp32 (base-2 logits).
+//    They turn codes into f16 in registers and run QK^T and PV on tensor cores
+//    (m16n8k16): keys are the A operand (16 tokens x 16 channels) against the
+//    folded query weights, values the A operand of O^T = V^T P^T.  The folded
+//    weights and the folded probabilities are each split into high + low f16
+//    parts.  Softmax is online in fp32 (base-2 logits).
 //  * Tail CTA: the bf16 residual buffer, the pending speculative tokens (causal)
 //    and the 16-bit selected tokens, on CUDA cores.
 //  * Every CTA writes an (m, l, o) partial.  The CTA that arrives last at a
 //    per-(b, kvh) atomic ticket merges all partials into the bf16 output and LSE,
 //    then resets the ticket.  No CTA ever waits on another.
 //
-// Folding (no per-element dequant FMA): with q~ = q * sm_scale * log2(e) and
-// key codes c (scale s, zero z per group and channel),
-//   logit2 = sum_d q~_d (c s + z) = sum_d w'_d (1 + c/2^b) + sum_d (q~_d z_d - w'_d),
-// with w'_d = 2^b q~_d s_d.  The value scale folds into the probabilities:
-//   o = sum_t p_t (c s_t + z_t) = sum_t P'_t (1 + c/2^b) + sum_t (p_t z_t - P'_t),
-// with P'_t = 2^b p_t s_t.
+// Folding (no per-element dequant FMA).  A key code c reads as the f16 value
+// E = off + c / kw (INT8: off = 0, kw = 1; INT4/2/1: off = 1, kw = 2^b), so
+// with q~ = q * sm_scale * log2(e), step s (MULT x scale) and zero z per group
+// and channel:
+//   logit2 = sum_d q~_d (c s + z) = sum_d w_d E_d + (sum_d q~_d z_d - off sum_d w_d),
+// with w_d = q~_d s_d kw; the bracket starts the accumulator.  Value codes read
+// as the exact f16 values m c (m a power of two set by the code's bit position;
+// the encoding's offset of 1024 is subtracted exactly), so the long P.V
+// accumulation carries no offset:
+//   o = sum_t p_t (c s + z) = sum_t P'_t (m c) + sum_t p_t z_t,  P'_t = p_t s_t / m_t.
 #include "kvq_modes.cuh"
 
 namespace kvq {
 namespace {
 
-constexpr int NW = 4;                  // consumer warps
-constexpr int SPW = 2;                 // stage slots per consumer warp
-constexpr int NSLOT = NW * SPW;
-constexpr int NTHREADS = (NW + 1) * 32;
+constexpr int NW = 4;                  // warps per CTA; each streams and consumes its own tiles
+constexpr int NTHREADS = NW * 32;
+constexpr int kSmemPerSm = 228 * 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Tail-CTA shared layout (overlays the slot area of the same dynamic buffer).
@@ -55,7 +59,11 @@ struct TailSmem {
   static constexpr int TOTAL = OK_OFF + TC * 4;
 };
 
-template <int MODE, int D, int NJ>
+// Target CTAs per SM: four with one weight n-tile (rows <= 4), three with two.
+template <int NT>
+constexpr int target_ctas() { return NT == 1 ? 4 : 3; }
+
+template <int MODE, int D, int NJ, int NT>
 struct Smem {
   using M = Mode<MODE>;
   using RW = Rows<MODE, D>;
@@ -70,21 +78,26 @@ struct Smem {
   static constexpr int VSZ_OFF = KSZ_OFF + KSZ_BYTES;
   static constexpr int VSZ_BYTES = TT * 2 * NJ * 4;
   static constexpr int SLOT = VSZ_OFF + VSZ_BYTES;
-  static constexpr int QX_OFF = NSLOT * SLOT;                 // folded query, [D/8][32 lanes] float2
-  static constexpr int BM_OFF = QX_OFF + (D / 8) * 32 * 8;    // selection bitmap
+  static constexpr int FIXED = kMaxRows * D * 4 + (kMaxChunk / 32) * 4 + 8 * 16 * 8 + 1024;
+  // stage slots per warp: as many as fit (2..4) at the target CTAs per SM
+  static constexpr int SPW_FIT = (kSmemPerSm / target_ctas<NT>() - 1024 - FIXED) / (NW * SLOT);
+  static constexpr int SPW = SPW_FIT < 2 ? 2 : (SPW_FIT > 4 ? 4 : SPW_FIT);
+  static constexpr int NSLOT = NW * SPW;
+  static constexpr int QT_OFF = NSLOT * SLOT;                 // scaled queries q~ [8][D] f32
+  static constexpr int BM_OFF = QT_OFF + kMaxRows * D * 4;    // selection bitmap
   static constexpr int BM_WORDS = kMaxChunk / 32;
   static constexpr int BAR_OFF = BM_OFF + BM_WORDS * 4;
-  static constexpr int RING_END = BAR_OFF + 2 * NSLOT * 8;
+  static constexpr int RING_END = BAR_OFF + NSLOT * 8;
   static constexpr int COMBINE_END = (2 * kMaxCombine * 8 + 16) * 4;
   // the ticket flag sits after whichever layout (ring, tail CTA, combine) is largest
   static constexpr int MISC_OFF0 = RING_END > TailSmem<D>::TOTAL ? RING_END : TailSmem<D>::TOTAL;
   static constexpr int MISC_OFF = (MISC_OFF0 > COMBINE_END ? MISC_OFF0 : COMBINE_END + 15) / 16 * 16;
   static constexpr int TOTAL = MISC_OFF + 64;
   // warp-merge scratch (after the pipeline drains), inside the slot area
-  static constexpr int WM_OFF = 0;                            // [NW][8]
-  static constexpr int WL_OFF = WM_OFF + NW * 8 * 4;          // [NW][8]
-  static constexpr int WC_OFF = WL_OFF + NW * 8 * 4;          // [NW][8][4]
-  static constexpr int WO_OFF = WC_OFF + NW * 8 * 4 * 4;      // [NW][8][D]
+  static constexpr int WM_OFF = 0;                            // [NW][8] running max
+  static constexpr int WL_OFF = WM_OFF + NW * 8 * 4;          // [NW][8] running sum
+  static constexpr int WC_OFF = WL_OFF + NW * 8 * 4;          // [NW][8][NJ] value zero-point terms
+  static constexpr int WO_OFF = WC_OFF + NW * 8 * 4 * 4;      // [NW][8][D] output sums
   static constexpr int SCRATCH = WO_OFF + NW * 8 * D * 4;
   static_assert(SCRATCH <= NSLOT * SLOT, "merge scratch must fit in the slot area");
   static_assert(TailSmem<D>::TOTAL <= MISC_OFF, "the tail layout must not reach the ticket flag");
@@ -235,46 +248,67 @@ __device__ void tail_partial(const AttendParams& p, long long u, int tsplit, uin
   __syncthreads();
 
   constexpr int VEC = D / 8;   // 16-byte vectors per row
-  for (int c0 = t_lo; c0 < t_hi; c0 += TS::TC) {
+  // Chunk rows are loaded into registers one chunk ahead, so the next chunk's
+  // loads are in flight while this one is computed.
+  constexpr int PER_T = (TS::TC * VEC + NTHREADS - 1) / NTHREADS;
+  uint4 pk[PER_T], pv[PER_T];
+  int pf[PER_T];
+  auto load_chunk = [&](int c0) {
     const int nt = min(TS::TC, t_hi - c0);
-    // ---- stage K and V rows (16-byte vectors, all in flight) ----
-#pragma unroll 4
-    for (int e = tid; e < nt * VEC; e += blockDim.x) {
+#pragma unroll
+    for (int k = 0; k < PER_T; ++k) {
+      const int e = tid + k * NTHREADS;
       const int j = e / VEC, c = e % VEC;
-      int t = c0 + j;
-      const uint16_t *kp = nullptr, *vp = nullptr;
-      int flag = -2;
-      if (t < p.c.r) {
-        const int slot = (p.c.res_start + t) % (2 * G);
-        const long long off = (u * 2 * G + slot) * D;
-        kp = p.c.res_k + off;
-        vp = p.c.res_v + off;
-        flag = -1;
-      } else if ((t -= p.c.r) < p.P) {
-        const long long off = (u * p.P + t) * D;
-        kp = p.pend_k + off;
-        vp = p.pend_v + off;
-        flag = t;
-      } else {
-        t -= p.P;
-        const int idx = p.sel_idx[u * p.top_k + t];
-        if (idx >= 0 && idx < p.c.Lq) {
-          const long long off = (u * p.top_k + t) * D;
-          kp = p.sel_k + off;
-          vp = p.sel_v + off;
-          flag = -1;
+      pk[k] = make_uint4(0, 0, 0, 0);
+      pv[k] = make_uint4(0, 0, 0, 0);
+      pf[k] = -2;
+      if (j < nt) {
+        int t = c0 + j;
+        const uint16_t *kp = nullptr, *vp = nullptr;
+        if (t < p.c.r) {
+          const int slot = (p.c.res_start + t) % (2 * G);
+          const long long off = (u * 2 * G + slot) * D;
+          kp = p.c.res_k + off;
+          vp = p.c.res_v + off;
+          pf[k] = -1;
+        } else if ((t -= p.c.r) < p.P) {
+          const long long off = (u * p.P + t) * D;
+          kp = p.pend_k + off;
+          vp = p.pend_v + off;
+          pf[k] = t;
+        } else {
+          t -= p.P;
+          const int idx = p.sel_idx[u * p.top_k + t];
+          if (idx >= 0 && idx < p.c.Lq) {
+            const long long off = (u * p.top_k + t) * D;
+            kp = p.sel_k + off;
+            vp = p.sel_v + off;
+            pf[k] = -1;
+          }
+        }
+        if (kp) {
+          pk[k] = reinterpret_cast<const uint4*>(kp)[c];
+          pv[k] = reinterpret_cast<const uint4*>(vp)[c];
         }
       }
-      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-      if (kp) {
-        kv = reinterpret_cast<const uint4*>(kp)[c];
-        vv = reinterpret_cast<const uint4*>(vp)[c];
+    }
+  };
+  if (t_lo < t_hi) load_chunk(t_lo);
+  for (int c0 = t_lo; c0 < t_hi; c0 += TS::TC) {
+    const int nt = min(TS::TC, t_hi - c0);
+    // ---- stage K and V rows ----
+#pragma unroll
+    for (int k = 0; k < PER_T; ++k) {
+      const int e = tid + k * NTHREADS;
+      const int j = e / VEC, c = e % VEC;
+      if (j < TS::TC) {
+        *reinterpret_cast<uint4*>(ks + j * TS::ROW + c * 16) = pk[k];
+        *reinterpret_cast<uint4*>(vs + j * TS::ROW + c * 16) = pv[k];
+        if (c == 0) tok_pend[j] = pf[k];
       }
-      *reinterpret_cast<uint4*>(ks + j * TS::ROW + c * 16) = kv;
-      *reinterpret_cast<uint4*>(vs + j * TS::ROW + c * 16) = vv;
-      if (c == 0) tok_pend[j] = flag;
     }
     __syncthreads();
+    if (c0 + TS::TC < t_hi) load_chunk(c0 + TS::TC);
     // ---- logits: thread <-> (row, token) ----
     for (int e = tid; e < kMaxRows * TS::TC; e += blockDim.x) {
       const int rho = e / TS::TC, j = e % TS::TC;
@@ -361,13 +395,22 @@ __device__ void tail_partial(const AttendParams& p, long long u, int tsplit, uin
 // ------------------------------------------------------------------------------
 // Quantized split
 // ------------------------------------------------------------------------------
-// Three CTAs per SM for one channel block per token (G = D, the hierarchical
-// cache's usual shape); the other variants keep more state per lane.
-template <int MODE, int D, int NJ>
-__global__ void __launch_bounds__(NTHREADS, (NJ == 1 ? 3 : 1)) attend_kernel(AttendParams p) {
+// exponent of |x| as an integer (x finite, nonzero): floor(log2 |x|)
+__device__ __forceinline__ int exp2_floor(float x) {
+  return static_cast<int>((__float_as_uint(x) >> 23) & 0xFFu) - 127;
+}
+__device__ __forceinline__ float pow2i(int e) {   // 2^e, -126 <= e <= 127
+  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+
+// Four CTAs per SM when one weight n-tile serves all rows (rows <= 4); the
+// eight-row variant keeps two n-tiles of weights and two sets of P fragments.
+template <int MODE, int D, int NJ, int NT>
+__global__ void __launch_bounds__(NTHREADS, target_ctas<NT>()) attend_kernel(AttendParams p) {
   using M = Mode<MODE>;
   using RW = Rows<MODE, D>;
-  using L = Smem<MODE, D, NJ>;
+  using L = Smem<MODE, D, NJ, NT>;
+  using XP = XPair<MODE>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int g = lane >> 2, q = lane & 3;
@@ -376,7 +419,7 @@ __global__ void __launch_bounds__(NTHREADS, (NJ == 1 ? 3 : 1)) attend_kernel(Att
   int* sh_abort = sh_flag + 1;
 
   const long long ntail = nunits * p.S_t;
-  if (blockIdx.x < ntail) {  // ---------------- tail CTAs ----------------
+  if (blockIdx.x < ntail) {  // ---------------- tail CTAs (first, so they start in the first wave) ----
     const long long u = blockIdx.x / p.S_t;
     tail_partial<D>(p, u, static_cast<int>(blockIdx.x % p.S_t), smem);
     __syncthreads();
@@ -394,299 +437,427 @@ __global__ void __launch_bounds__(NTHREADS, (NJ == 1 ? 3 : 1)) attend_kernel(Att
   const int ntiles = (ntok_chunk + M::TT - 1) / M::TT;
   const int per_warp = (ntiles + NW - 1) / NW;
   constexpr int G = D / NJ;
+  constexpr int NPK = D / 8;          // key pairs per lane chunk
+  constexpr int KSTEPS = D / 16;
+  constexpr float MULT = static_cast<float>(M::MULT);   // INT4 reads the upper nibble: step 16 scale
   const int R = p.R;
 
-  float2* qx = reinterpret_cast<float2*>(smem + L::QX_OFF);
+  float* qt = reinterpret_cast<float*>(smem + L::QT_OFF);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L::BM_OFF);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-  uint64_t* empty = full + NSLOT;
-
-  // ---- setup: barriers first, so the producer can start loading at once ----
-  const int bm_words = (ntok_chunk + 31) / 32;
-  if (tid == 0) {
-    for (int s = 0; s < NSLOT; ++s) {
-      mbar_init(full + s, 1);
-      mbar_init(empty + s, 1);
-    }
-    *sh_abort = 0;
-    fence_mbar_init();
-  }
-  for (int e = tid; e < bm_words; e += blockDim.x) bitmap[e] = 0u;
-  __syncthreads();
+  constexpr int SPW = L::SPW;
+  // this warp's tiles: a contiguous run of the chunk
+  const int my_first = warp * per_warp;
+  const int my_tiles = max(0, min(per_warp, ntiles - my_first));
   const long long u_tok = u * p.c.C;  // first token row of this unit in the planes
-  const float qmul = static_cast<float>((1 << M::CB) * M::MULT);
-  if (warp < NW) {
-    // consumers: folded queries and the selection bitmap, while the first tiles load
-    constexpr int NC = NW * 32;
-    // q^ = 2^CB * MULT * sm_scale * log2(e) * q, stored per (pair, lane) as the
-    // two channels that lane needs for that pair: conflict-free 8-byte reads
-#pragma unroll 4
-    for (int e = tid; e < (D / 8) * 32; e += NC) {
-      const int pp = e / 32, ln = e % 32;
-      const int rho = ln >> 2, qq = ln & 3;
-      float2 v = make_float2(0.f, 0.f);
-      if (rho < R) {
-        const int i = rho / p.HG, hh = rho % p.HG;
-        const long long qrow = ((static_cast<long long>(b) * p.gamma + i) * p.Hq + kvh * p.HG + hh) * D;
-        const int2 ch = pair_chan<MODE, D>(pp);
-        const int c0 = qq * (D / 4) + ch.x, c1 = qq * (D / 4) + ch.y;
-        v.x = bf16_to_f32(p.q[qrow + c0]) * p.qscale * qmul;
-        v.y = bf16_to_f32(p.q[qrow + c1]) * p.qscale * qmul;
-      }
-      qx[e] = v;
+
+  // Each warp streams its own tiles: lane 0 puts tile j into slot j % SPW of
+  // the warp's ring with 1-D bulk copies that complete on the slot's mbarrier.
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](int j) {
+    const int slot = warp * SPW + (j % SPW);
+    const long long t0 = t_begin + static_cast<long long>(my_first + j) * M::TT;
+    const int nt = static_cast<int>(min(static_cast<long long>(M::TT), t_end - t0));
+    const long long g_first = t0 / G, g_last = (t0 + nt - 1) / G;
+    const uint32_t kb = nt * RW::KROW, vb = (nt / 32) * D * RW::VROW;
+    const uint32_t kszb = static_cast<uint32_t>(g_last - g_first + 1) * 2 * D * 4;
+    const uint32_t vszb = nt * 2 * NJ * 4;
+    uint8_t* sbase = smem + slot * L::SLOT;
+    // order this warp's earlier reads of the slot before the async-proxy writes
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(full + slot, M::NP * (kb + vb) + kszb + vszb);
+#pragma unroll
+    for (int pl = 0; pl < M::NP; ++pl) {
+      bulk_g2s(sbase + L::K_OFF + pl * L::KPLANE, p.c.kplane[pl] + (u_tok + t0) * RW::KROW, kb, full + slot, pol);
+      bulk_g2s(sbase + L::V_OFF + pl * L::VPLANE, p.c.vplane[pl] + ((u_tok + t0) / 32) * D * RW::VROW, vb,
+               full + slot, pol);
     }
-    for (int j = tid; j < p.top_k; j += NC) {
+    bulk_g2s(sbase + L::KSZ_OFF, p.c.ksz + (u * (p.c.C / G) + g_first) * 2 * D, kszb, full + slot, pol);
+    bulk_g2s(sbase + L::VSZ_OFF, p.c.vsz + (u_tok + t0) * 2 * NJ, vszb, full + slot, pol);
+  };
+
+  // ---- setup: each warp's barriers first, so its first tiles load at once ----
+  if (lane == 0) {
+    for (int s2 = 0; s2 < SPW; ++s2) mbar_init(full + warp * SPW + s2, 1);
+    fence_mbar_init();
+    for (int j = 0; j < min(SPW, my_tiles); ++j) issue(j);
+  }
+  int issued = min(SPW, my_tiles), consumed = 0;
+  const int bm_words = (ntok_chunk + 31) / 32;
+  if (tid == 0) *sh_abort = 0;
+  const bool has_sel = p.top_k > 0;
+  if (has_sel)
+    for (int e = tid; e < bm_words; e += blockDim.x) bitmap[e] = 0u;
+  // scaled queries q~ = q * sm_scale * log2(e) (rows >= R are zero)
+  for (int e = tid; e < kMaxRows * D; e += blockDim.x) {
+    const int rho = e / D, d = e % D;
+    float v = 0.f;
+    if (rho < R) {
+      const int i = rho / p.HG, hh = rho % p.HG;
+      const long long qrow = ((static_cast<long long>(b) * p.gamma + i) * p.Hq + kvh * p.HG + hh) * D;
+      v = bf16_to_f32(p.q[qrow + d]) * p.qscale;
+    }
+    qt[e] = v;
+  }
+  __syncthreads();
+  if (has_sel) {
+    for (int j = tid; j < p.top_k; j += blockDim.x) {
       const long long idx = p.sel_idx[u * p.top_k + j];
       if (idx >= t_begin && idx < t_end) {
         const int rel = static_cast<int>(idx - t_begin);
         atomicOr(bitmap + rel / 32, 1u << (rel % 32));
       }
     }
-    asm volatile("bar.sync 2, %0;" ::"n"(NW * 32));
+    __syncthreads();
   }
 
-  if (warp == NW) {
-    // ---------------- producer ----------------
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      for (int j = 0; j < per_warp && !*reinterpret_cast<volatile int*>(sh_abort); ++j) {
-        for (int w = 0; w < NW; ++w) {
-          const int ti = w * per_warp + j;
-          if (ti >= ntiles || j >= per_warp) continue;
-          const int slot = w * SPW + (j % SPW);
-          const uint32_t par = ((j / SPW) & 1) ^ 1;
-          if (!mbar_wait_bounded(empty + slot, par, p.wait_limit)) {
-            record_status(p.status, KVQ_ERR_DEVICE_TIMEOUT);
-            *reinterpret_cast<volatile int*>(sh_abort) = 1;
-            break;
-          }
-          const long long t0 = t_begin + static_cast<long long>(ti) * M::TT;
-          const int nt = static_cast<int>(min(static_cast<long long>(M::TT), t_end - t0));
-          const long long g_first = t0 / G, g_last = (t0 + nt - 1) / G;
-          const uint32_t kb = nt * RW::KROW, vb = (nt / 32) * D * RW::VROW;
-          const uint32_t kszb = static_cast<uint32_t>(g_last - g_first + 1) * 2 * D * 4;
-          const uint32_t vszb = nt * 2 * NJ * 4;
-          uint8_t* sbase = smem + slot * L::SLOT;
-          mbar_arrive_expect_tx(full + slot, M::NP * (kb + vb) + kszb + vszb);
-#pragma unroll
-          for (int pl = 0; pl < M::NP; ++pl) {
-            bulk_g2s(sbase + L::K_OFF + pl * L::KPLANE, p.c.kplane[pl] + (u_tok + t0) * RW::KROW, kb,
-                     full + slot, pol);
-            bulk_g2s(sbase + L::V_OFF + pl * L::VPLANE,
-                     p.c.vplane[pl] + ((u_tok + t0) / 32) * D * RW::VROW, vb, full + slot, pol);
-          }
-          bulk_g2s(sbase + L::KSZ_OFF, p.c.ksz + (u * (p.c.C / G) + g_first) * 2 * D, kszb,
-                   full + slot, pol);
-          bulk_g2s(sbase + L::VSZ_OFF, p.c.vsz + (u_tok + t0) * 2 * NJ, vszb, full + slot, pol);
-        }
-      }
-    }
-  } else {
+  {
     // ---------------- consumers ----------------
-    float o[D / 16][4];
+    // Keys are the A operand (rows = 16 tokens of an m-tile, k = channels), the
+    // folded query weights the B operand (column 2r + h = row 4nt + r, h = high
+    // / low f16 part).  Values are the A operand of O^T = V^T P^T (rows =
+    // channels, k = tokens).  In m-tile s the lane's rows g and g+8 are the
+    // tokens of value pair 2s + (g & 1) of token octet g >> 1, so the P values a
+    // lane computes are a whole B register of P.V for one destination lane.
+    const int qbase = q * (D / 4);
+    const int oct = 8 * (g >> 1), par = g & 1;
+    int tokA[2], tokB[2];
+    float vinv[2];          // 1 / value factor of the lane's pair, per m-tile
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int i = 2 * s + par;
+      tokA[s] = oct + (MODE == KVQ_MODE_INT8 ? s + 4 * par : i);
+      tokB[s] = tokA[s] + (MODE == KVQ_MODE_INT8 ? 2 : 4);
+      vinv[s] = 1.0f / vx_mult<MODE>(i);
+    }
+    // max |q~| over the valid rows, for the weight normalizer
+    float qmax = 0.f;
+    for (int e = lane; e < R * D; e += 32) qmax = fmaxf(qmax, fabsf(qt[e]));
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, o2));
+
+    uint32_t W[NT][NPK];                 // weights: this lane's B column part, per key pair
+    float cinit[NT];                     // accumulator start (correction x 2^e) for row 4nt + q
+    float kscale = 1.f;                  // 2^-e of the current group
+    float o[D / 16][4];                  // O^T, channel m-tile x (col 2q, 2q+1)
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    float m_run = neg_inf(), l_run = 0.f;
-    uint32_t wa[D / 16][4];
-    float corr = 0.f;
+    float m_run[NT], l_run[NT], vcorr[NT][NJ];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m_run[nt] = neg_inf();
+      l_run[nt] = 0.f;
+#pragma unroll
+      for (int jv = 0; jv < NJ; ++jv) vcorr[nt][jv] = 0.f;
+      cinit[nt] = 0.f;
+#pragma unroll
+      for (int pp = 0; pp < NPK; ++pp) W[nt][pp] = 0u;
+    }
+    float evs = 0.f;                     // value normalizer 2^ev (0: not chosen yet)
     long long cur_grp = -1;
-    const int qbase = q * (D / 4);
-    const bool row_ok = g < R;
 
-    for (int j = 0; j < per_warp; ++j) {
-      const int ti = warp * per_warp + j;
-      if (ti >= ntiles) break;
+    for (int j = 0; j < my_tiles; ++j) {
+      const int ti = my_first + j;
       const int slot = warp * SPW + (j % SPW);
-      const uint32_t par = (j / SPW) & 1;
-      if (!mbar_wait_bounded(full + slot, par, p.wait_limit)) {
+      const uint32_t parity = (j / SPW) & 1;
+      if (!mbar_wait_bounded(full + slot, parity, p.wait_limit)) {
         record_status(p.status, KVQ_ERR_DEVICE_TIMEOUT);
         *reinterpret_cast<volatile int*>(sh_abort) = 1;
         break;
       }
       if (*reinterpret_cast<volatile int*>(sh_abort)) break;
       const long long t0 = t_begin + static_cast<long long>(ti) * M::TT;
-      const int nt = static_cast<int>(min(static_cast<long long>(M::TT), t_end - t0));
+      const int nt_tok = static_cast<int>(min(static_cast<long long>(M::TT), t_end - t0));
       const long long g_first = t0 / G;
       const uint8_t* sbase = smem + slot * L::SLOT;
       const float* ksz = reinterpret_cast<const float*>(sbase + L::KSZ_OFF);
       const float* vsz = reinterpret_cast<const float*>(sbase + L::VSZ_OFF);
 
-      for (int sl = 0; sl < nt / 32; ++sl) {
+      for (int sl = 0; sl < nt_tok / 32; ++sl) {
         const long long tok0 = t0 + 32 * sl;
         const long long grp = tok0 / G;
         if (grp != cur_grp) {
-          // ---- folded key weights for this group (high + low f16 parts) ----
+          // ---- folded key weights of this group ----
+          // w_c = q~_c * MULT * s_c * kx_weight, scaled by 2^e so that the
+          // largest possible |w| sits near 2^13, split into f16 high + low
+          // parts.  The accumulator starts at 2^e sum_c q~_c z_c minus the
+          // encoding's offset times sum_c (hi + lo)_c.
           cur_grp = grp;
           const float* ks = ksz + (grp - g_first) * 2 * D;
           const float* kz = ks + D;
-          // correction sum_d (q~_d z_d - w'_d), with q~ = q^ / (2^CB MULT) exactly
-          float zsum = 0.f, wsum = 0.f;
+          float sv[D / 4];
 #pragma unroll
-          for (int pp = 0; pp < D / 8; ++pp) {
-            const int2 ch = pair_chan<MODE, D>(pp);
-            const int c0 = qbase + ch.x, c1 = qbase + ch.y;
-            const float2 qv = qx[pp * 32 + lane];
-            const float w0 = qv.x * ks[c0];
-            const float w1 = qv.y * ks[c1];
-            const uint32_t hi = pack_half2(w0, w1);
-            const float2 hf = unpack_half2(hi);
-            const uint32_t lo = pack_half2(w0 - hf.x, w1 - hf.y);
-            wa[pp / 2][(pp % 2) * 2 + 0] = hi;
-            wa[pp / 2][(pp % 2) * 2 + 1] = lo;
-            zsum = fmaf(qv.x, kz[c0], fmaf(qv.y, kz[c1], zsum));
-            wsum += w0 + w1;
+          for (int c4 = 0; c4 < D / 16; ++c4) {
+            const float4 v4 = *reinterpret_cast<const float4*>(ks + qbase + 4 * c4);
+            sv[4 * c4] = v4.x; sv[4 * c4 + 1] = v4.y; sv[4 * c4 + 2] = v4.z; sv[4 * c4 + 3] = v4.w;
           }
-          float cpart = fmaf(zsum, 1.0f / qmul, -wsum);
-          cpart += __shfl_xor_sync(0xffffffffu, cpart, 1);
-          cpart += __shfl_xor_sync(0xffffffffu, cpart, 2);
-          corr = cpart;
+          float smax = 0.f;
+#pragma unroll
+          for (int c = 0; c < D / 4; ++c) smax = fmaxf(smax, sv[c]);
+          smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1));
+          smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 2));
+          constexpr float KW = MULT * kx_weight<MODE>();
+          const float bound = qmax * smax * KW;
+          const int e = (bound > 0.f) ? max(-100, min(100, 13 - exp2_floor(bound))) : 0;
+          const float E2 = pow2i(e);
+          kscale = pow2i(-e);
+          const float f = E2 * KW;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const float* qr = qt + (4 * nt + (g >> 1)) * D + qbase;
+            float wsum = 0.f, zsum = 0.f;
+#pragma unroll
+            for (int pp = 0; pp < NPK; ++pp) {
+              const int c0 = kx_chan<MODE, D>(pp, 0), c1 = kx_chan<MODE, D>(pp, 1);
+              const float q0 = qr[c0], q1 = qr[c1];
+              const float w0 = q0 * sv[c0] * f, w1 = q1 * sv[c1] * f;
+              const uint32_t hi = pack_half2(w0, w1);
+              const float2 hf = unpack_half2(hi);
+              const uint32_t lo = pack_half2(w0 - hf.x, w1 - hf.y);
+              W[nt][pp] = par ? lo : hi;
+              if constexpr (kx_offset<MODE>() != 0.f) {
+                const float2 lf = unpack_half2(lo);
+                wsum += (hf.x + lf.x) + (hf.y + lf.y);
+              }
+              zsum = fmaf(q0, kz[qbase + c0], fmaf(q1, kz[qbase + c1], zsum));
+            }
+            float cw = fmaf(zsum, E2, -kx_offset<MODE>() * wsum);
+            cw += __shfl_xor_sync(0xffffffffu, cw, 1);
+            cw += __shfl_xor_sync(0xffffffffu, cw, 2);
+            // this lane's C rows belong to row 4nt + q, whose weights lanes g = 2q hold
+            cinit[nt] = __shfl_sync(0xffffffffu, cw, 8 * q);
+          }
         }
-        // ---- S^T = W x K^T over 4 n-tiles of 8 tokens ----
-        float c[4][4];
         const uint8_t* kslab = sbase + L::K_OFF + (32 * sl) * RW::KROW + q * RW::KCHUNK;
-        {
-          // the four n-tiles are independent accumulation chains: k-step outer
-          uint32_t P[4][D / 8];
+        const uint8_t* vslab = sbase + L::V_OFF + sl * D * RW::VROW;
+
+        // ---- logits: S = K W, two m-tiles of 16 tokens ----
+        float x[2][NT][2];
 #pragma unroll
-          for (int jt = 0; jt < 4; ++jt) {
-            c[jt][0] = corr; c[jt][1] = corr; c[jt][2] = 0.f; c[jt][3] = 0.f;
-            key_pairs<MODE, D>(kslab + (4 * g + jt) * RW::KROW, L::KPLANE, P[jt]);
+        for (int s = 0; s < 2; ++s) {
+          uint32_t PA[NPK], PB[NPK];
+          key_pairs_x<MODE, D>(kslab + tokA[s] * RW::KROW, L::KPLANE, PA);
+          key_pairs_x<MODE, D>(kslab + tokB[s] * RW::KROW, L::KPLANE, PB);
+          float acc[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            acc[nt][0] = cinit[nt]; acc[nt][1] = 0.f; acc[nt][2] = cinit[nt]; acc[nt][3] = 0.f;
           }
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            const uint32_t a[4] = {PA[2 * kk], PB[2 * kk], PA[2 * kk + 1], PB[2 * kk + 1]};
 #pragma unroll
-            for (int jt = 0; jt < 4; ++jt) mma16816(c[jt], wa[kk], P[jt][2 * kk], P[jt][2 * kk + 1]);
-        }
-        // ---- mask + online softmax (row g; tokens 8q+jt and 8q+jt+4) ----
-        const uint32_t bm = bitmap[static_cast<int>(tok0 - t_begin) / 32] >> (8 * q);
-        float x[4][2];
-        float mx = neg_inf();
+            for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt], a, W[nt][2 * kk], W[nt][2 * kk + 1]);
+          }
 #pragma unroll
-        for (int jt = 0; jt < 4; ++jt) {
-          const bool m0 = !row_ok || ((bm >> jt) & 1u);
-          const bool m1 = !row_ok || ((bm >> (jt + 4)) & 1u);
-          x[jt][0] = m0 ? neg_inf() : c[jt][0] + c[jt][2];
-          x[jt][1] = m1 ? neg_inf() : c[jt][1] + c[jt][3];
-          mx = fmaxf(mx, fmaxf(x[jt][0], x[jt][1]));
-        }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float msafe = (m_new == neg_inf()) ? 0.f : m_new;
-        const float alpha = (m_run == neg_inf()) ? 0.f : fast_exp2(m_run - msafe);
-        float pr[4][2];
-        float psum = 0.f;
-#pragma unroll
-        for (int jt = 0; jt < 4; ++jt) {
-#pragma unroll
-          for (int e2 = 0; e2 < 2; ++e2) {
-            pr[jt][e2] = (x[jt][e2] == neg_inf()) ? 0.f : fast_exp2(x[jt][e2] - msafe);
-            psum += pr[jt][e2];
+          for (int nt = 0; nt < NT; ++nt) {
+            x[s][nt][0] = (acc[nt][0] + acc[nt][1]) * kscale;
+            x[s][nt][1] = (acc[nt][2] + acc[nt][3]) * kscale;
           }
         }
-        l_run = l_run * alpha + psum;
-        m_run = m_new;
-        // rows 2q, 2q+1 of O^T live in this lane: their rescale factors
-        const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * q);
-        const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * q + 4);
+        if (has_sel) {
+          const uint32_t bm = bitmap[static_cast<int>(tok0 - t_begin) / 32];
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            const bool ma = (bm >> tokA[s]) & 1u, mb = (bm >> tokB[s]) & 1u;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              if (ma) x[s][nt][0] = neg_inf();
+              if (mb) x[s][nt][1] = neg_inf();
+            }
+          }
+        }
+        // ---- online softmax ----
+        float m_new[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float mx = fmaxf(fmaxf(x[0][nt][0], x[0][nt][1]), fmaxf(x[1][nt][0], x[1][nt][1]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          m_new[nt] = fmaxf(m_run[nt], mx);
+        }
+        float alpha[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          alpha[nt] = (m_run[nt] == m_new[nt]) ? 1.f
+                      : (m_run[nt] == neg_inf()) ? 0.f : fast_exp2(m_run[nt] - m_new[nt]);
+          m_run[nt] = m_new[nt];
+          l_run[nt] *= alpha[nt];
+#pragma unroll
+          for (int jv = 0; jv < NJ; ++jv) vcorr[nt][jv] *= alpha[nt];
+        }
+        // rows of this lane's O^T columns: their rescale factors
+        float a_lo, a_hi;
+        if constexpr (NT == 1) {
+          a_lo = a_hi = alpha[0];
+        } else {
+          const int src_lo = 4 * g + ((2 * q) & 3), src_hi = 4 * g + ((2 * q + 1) & 3);
+          const float l0 = __shfl_sync(0xffffffffu, alpha[0], src_lo), l1 = __shfl_sync(0xffffffffu, alpha[1], src_lo);
+          const float h0 = __shfl_sync(0xffffffffu, alpha[0], src_hi), h1 = __shfl_sync(0xffffffffu, alpha[1], src_hi);
+          a_lo = (q >> 1) ? l1 : l0;
+          a_hi = (q >> 1) ? h1 : h0;
+        }
+        // value scales of the lane's tokens; the value normalizer keeps P' below 2^15
+        float sA[2][NJ], zA[2][NJ], sB[2][NJ], zB[2][NJ];
+        float smx = 0.f;
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const float* va = vsz + (32 * sl + tokA[s]) * 2 * NJ;
+          const float* vb = vsz + (32 * sl + tokB[s]) * 2 * NJ;
+#pragma unroll
+          for (int jv = 0; jv < NJ; ++jv) {
+            sA[s][jv] = va[jv] * MULT; zA[s][jv] = va[NJ + jv];
+            sB[s][jv] = vb[jv] * MULT; zB[s][jv] = vb[NJ + jv];
+            smx = fmaxf(smx, fmaxf(sA[s][jv], sB[s][jv]));
+          }
+        }
+        if (__any_sync(0xffffffffu, smx * evs >= 32768.f || evs == 0.f)) {
+          float wmx = smx;
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) wmx = fmaxf(wmx, __shfl_xor_sync(0xffffffffu, wmx, o2));
+          const float nev = (wmx > 0.f) ? pow2i(max(-100, min(100, 13 - exp2_floor(wmx)))) : 1.f;
+          const float fac = (evs == 0.f) ? 0.f : nev / evs;
+          evs = nev;
+          a_lo *= fac;
+          a_hi *= fac;
+        }
+        float pr[2][NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float msafe = (m_run[nt] == neg_inf()) ? 0.f : m_run[nt];
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            pr[s][nt][0] = fast_exp2(x[s][nt][0] - msafe);
+            pr[s][nt][1] = fast_exp2(x[s][nt][1] - msafe);
+            l_run[nt] += pr[s][nt][0] + pr[s][nt][1];
+          }
+        }
 
         // ---- P.V, one channel block (G channels) at a time ----
-        // The slab's products go into fresh accumulators.  Its correction
-        // sum_t (p_t z_t - P'_t), which removes the zero points and the
-        // encoding's constant 1, is added before the merge into the running
-        // output.  So the running sum only ever holds output-sized values.
-        const uint8_t* vslab = sbase + L::V_OFF + sl * D * RW::VROW;
-        const float vmul = qmul;  // 2^CB * MULT
 #pragma unroll
         for (int jv = 0; jv < NJ; ++jv) {
-          // P'_t = 2^CB * MULT * p_t * s_t, split into f16 high + low parts
-          float pq[4][2];
-          float zc = 0.f;
+          // P' = p * s * MULT * 2^ev / vx_mult as f16 high + low parts, per m-tile
+          uint32_t H[2][NT], Lo[2][NT];
 #pragma unroll
-          for (int jt = 0; jt < 4; ++jt) {
+          for (int s = 0; s < 2; ++s) {
+            const float fa = sA[s][jv] * (evs * vinv[s]), fb = sB[s][jv] * (evs * vinv[s]);
+            const float za = zA[s][jv], zb = zB[s][jv];
 #pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-              const int tk = 32 * sl + 8 * q + jt + 4 * e2;   // token within the tile
-              const float s = vsz[tk * 2 * NJ + jv];
-              const float z = vsz[tk * 2 * NJ + NJ + jv];
-              pq[jt][e2] = pr[jt][e2] * s * vmul;
-              zc += pr[jt][e2] * z;
+            for (int nt = 0; nt < NT; ++nt) {
+              const float pa = pr[s][nt][0] * fa, pb = pr[s][nt][1] * fb;
+              H[s][nt] = pack_half2(pa, pb);
+              const float2 hf = unpack_half2(H[s][nt]);
+              Lo[s][nt] = pack_half2(pa - hf.x, pb - hf.y);
+              vcorr[nt][jv] = fmaf(pr[s][nt][0], za, fmaf(pr[s][nt][1], zb, vcorr[nt][jv]));
             }
           }
-          uint32_t bq[2][2][2];   // [k-step][high/low][register]
+          // B fragments of P^T for k-step s: b0 from lane (g = 2q), b1 from lane (g = 2q + 1)
+          uint32_t bh[2][2], bl[2][2];
+          if constexpr (NT == 1) {
+            // column g = 2 * row + part
+            const int r = g >> 1;
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
+            for (int s = 0; s < 2; ++s) {
 #pragma unroll
-            for (int r2 = 0; r2 < 2; ++r2) {
-              const float x0 = pq[2 * ks + r2][0], x1 = pq[2 * ks + r2][1];
-              const uint32_t hi = pack_half2(x0, x1);
-              const float2 fh = unpack_half2(hi);
-              const uint32_t lo = pack_half2(x0 - fh.x, x1 - fh.y);
-              const float2 fl = unpack_half2(lo);
-              bq[ks][0][r2] = hi;
-              bq[ks][1][r2] = lo;
-              zc -= (fh.x + fh.y) + (fl.x + fl.y);
+              for (int k2 = 0; k2 < 2; ++k2) {
+                const int src = 8 * q + 4 * k2 + r;
+                const uint32_t vh = __shfl_sync(0xffffffffu, H[s][0], src);
+                const uint32_t vl = __shfl_sync(0xffffffffu, Lo[s][0], src);
+                bh[s][k2] = par ? vl : vh;
+              }
+            }
+          } else {
+            // column g = row; high and low parts go through separate MMAs
+            const int r = g & 3;
+            const bool hi_nt = g >= 4;
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+#pragma unroll
+              for (int k2 = 0; k2 < 2; ++k2) {
+                const int src = 8 * q + 4 * k2 + r;
+                const uint32_t h0 = __shfl_sync(0xffffffffu, H[s][0], src);
+                const uint32_t h1 = __shfl_sync(0xffffffffu, H[s][NT - 1], src);
+                const uint32_t l0 = __shfl_sync(0xffffffffu, Lo[s][0], src);
+                const uint32_t l1 = __shfl_sync(0xffffffffu, Lo[s][NT - 1], src);
+                bh[s][k2] = hi_nt ? h1 : h0;
+                bl[s][k2] = hi_nt ? l1 : l0;
+              }
             }
           }
-          // row g's correction for this slab, then the values for rows 2q, 2q+1
-          zc += __shfl_xor_sync(0xffffffffu, zc, 1);
-          zc += __shfl_xor_sync(0xffffffffu, zc, 2);
-          const float z_lo = __shfl_sync(0xffffffffu, zc, 8 * q);
-          const float z_hi = __shfl_sync(0xffffffffu, zc, 8 * q + 4);
+          // The slab's products go into a fresh accumulator, folded into the
+          // running output with one rounding per element: a long MMA chain
+          // would accumulate the tensor core's truncation.
 #pragma unroll
           for (int mt = jv * (G / 16); mt < (jv + 1) * (G / 16); ++mt) {
             uint32_t a[2][4];
             const uint8_t* va = vslab + (16 * mt + g) * RW::VROW;
-            value_frags<MODE>(va, va + 8 * RW::VROW, L::VPLANE, q, a);
+            value_frags_x<MODE>(va, va + 8 * RW::VROW, L::VPLANE, q, a);
             float os[4] = {0.f, 0.f, 0.f, 0.f};
-            mma16816(os, a[0], bq[0][0][0], bq[0][0][1]);
-            mma16816(os, a[0], bq[0][1][0], bq[0][1][1]);
-            mma16816(os, a[1], bq[1][0][0], bq[1][0][1]);
-            mma16816(os, a[1], bq[1][1][0], bq[1][1][1]);
-            o[mt][0] = fmaf(o[mt][0], a_lo, os[0] + z_lo);
-            o[mt][1] = fmaf(o[mt][1], a_hi, os[1] + z_hi);
-            o[mt][2] = fmaf(o[mt][2], a_lo, os[2] + z_lo);
-            o[mt][3] = fmaf(o[mt][3], a_hi, os[3] + z_hi);
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              mma16816(os, a[s], bh[s][0], bh[s][1]);
+              if constexpr (NT == 2) mma16816(os, a[s], bl[s][0], bl[s][1]);
+            }
+            o[mt][0] = fmaf(o[mt][0], a_lo, os[0]);
+            o[mt][1] = fmaf(o[mt][1], a_hi, os[1]);
+            o[mt][2] = fmaf(o[mt][2], a_lo, os[2]);
+            o[mt][3] = fmaf(o[mt][3], a_hi, os[3]);
           }
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty + slot);
+      consumed = j + 1;
+      if (issued < my_tiles) {
+        if (lane == 0) issue(issued);
+        ++issued;
+      }
     }
+    // after an abort: let this warp's copies still in flight land before exit
+    if (lane == 0) {
+      for (int jj = consumed; jj < issued; ++jj)
+        mbar_wait_bounded(full + warp * SPW + (jj % SPW), (jj / SPW) & 1, p.wait_limit);
+    }
+    __syncwarp();
 
     // ---- per-warp results to shared scratch (after everyone left the ring) ----
-    float lsum = l_run;
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-    // the stage ring must be idle before the slot area is reused
-    asm volatile("bar.sync 1, %0;" ::"n"(NW * 32));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) {
+        l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], o2);
+#pragma unroll
+        for (int jv = 0; jv < NJ; ++jv) vcorr[nt][jv] += __shfl_xor_sync(0xffffffffu, vcorr[nt][jv], o2);
+      }
+    }
+    // the stage rings must be idle before the slot area is reused
+    __syncthreads();
     float* wm = reinterpret_cast<float*>(smem + L::WM_OFF);
     float* wl = reinterpret_cast<float*>(smem + L::WL_OFF);
+    float* wc = reinterpret_cast<float*>(smem + L::WC_OFF);
     float* wo = reinterpret_cast<float*>(smem + L::WO_OFF);
-    if (q == 0) {
-      wm[warp * 8 + g] = m_run;
-      wl[warp * 8 + g] = lsum;
+    if (g == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int rho = 4 * nt + q;
+        wm[warp * 8 + rho] = m_run[nt];
+        wl[warp * 8 + rho] = l_run[nt];
+#pragma unroll
+        for (int jv = 0; jv < NJ; ++jv) wc[(warp * 8 + rho) * 4 + jv] = vcorr[nt][jv];
+      }
     }
+    const float oscale = (evs > 0.f) ? 1.0f / evs : 0.f;
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
       const int ca = 16 * mt + g, cb = ca + 8;
-      wo[(warp * 8 + 2 * q) * D + ca] = o[mt][0];
-      wo[(warp * 8 + 2 * q + 1) * D + ca] = o[mt][1];
-      wo[(warp * 8 + 2 * q) * D + cb] = o[mt][2];
-      wo[(warp * 8 + 2 * q + 1) * D + cb] = o[mt][3];
-    }
-  }
-  __syncthreads();
-
-  // ---- drain: the producer's copies must all have landed before exit ----
-  // (only matters after an abort; in normal runs every phase completed)
-  if (*reinterpret_cast<volatile int*>(sh_abort) && warp == NW && lane == 0) {
-    for (int w = 0; w < NW; ++w) {
-      const int issued = min(per_warp, max(0, ntiles - w * per_warp));
-      for (int s2 = 0; s2 < SPW && s2 < issued; ++s2) {
-        // last use of slot (w, s2): j = largest j < issued with j % SPW == s2
-        const int jl = ((issued - 1 - s2) / SPW) * SPW + s2;
-        mbar_wait_bounded(full + w * SPW + s2, (jl / SPW) & 1, p.wait_limit);
+      if constexpr (NT == 1) {
+        wo[(warp * 8 + q) * D + ca] = (o[mt][0] + o[mt][1]) * oscale;
+        wo[(warp * 8 + q) * D + cb] = (o[mt][2] + o[mt][3]) * oscale;
+      } else {
+        wo[(warp * 8 + 2 * q) * D + ca] = o[mt][0] * oscale;
+        wo[(warp * 8 + 2 * q + 1) * D + ca] = o[mt][1] * oscale;
+        wo[(warp * 8 + 2 * q) * D + cb] = o[mt][2] * oscale;
+        wo[(warp * 8 + 2 * q + 1) * D + cb] = o[mt][3] * oscale;
       }
     }
   }
@@ -696,6 +867,7 @@ __global__ void __launch_bounds__(NTHREADS, (NJ == 1 ? 3 : 1)) attend_kernel(Att
   {
     const float* wm = reinterpret_cast<const float*>(smem + L::WM_OFF);
     const float* wl = reinterpret_cast<const float*>(smem + L::WL_OFF);
+    const float* wc = reinterpret_cast<const float*>(smem + L::WC_OFF);
     const float* wo = reinterpret_cast<const float*>(smem + L::WO_OFF);
     const int PF = kPartialFloats(D);
     float* dst = p.partials + (u * (p.S_q + p.S_t) + split) * PF;
@@ -712,7 +884,7 @@ __global__ void __launch_bounds__(NTHREADS, (NJ == 1 ? 3 : 1)) attend_kernel(Att
           if (mw == neg_inf()) continue;
           const float f = fast_exp2(mw - Mx);
           lt += f * wl[w * 8 + rho];
-          ot += f * wo[(w * 8 + rho) * D + d];
+          ot += f * (wo[(w * 8 + rho) * D + d] + wc[(w * 8 + rho) * 4 + d / G]);
         }
       }
       dst[2 * kMaxRows + rho * D + d] = ot;
@@ -726,74 +898,90 @@ __global__ void __launch_bounds__(NTHREADS, (NJ == 1 ? 3 : 1)) attend_kernel(Att
   ticket_and_combine<D>(p, u, sh_flag, reinterpret_cast<float*>(smem));
 }
 
-template <int MODE, int D, int NJ>
+template <int MODE, int D, int NJ, int NT>
+constexpr int smem_bytes() {
+  using L = Smem<MODE, D, NJ, NT>;
+  return (L::TOTAL > TailSmem<D>::TOTAL) ? L::TOTAL : TailSmem<D>::TOTAL;
+}
+
+template <int MODE, int D, int NJ, int NT>
 cudaError_t launch_t(const AttendParams& p, cudaStream_t s) {
-  using L = Smem<MODE, D, NJ>;
-  constexpr int smem = (L::TOTAL > TailSmem<D>::TOTAL) ? L::TOTAL : TailSmem<D>::TOTAL;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&attend_kernel<MODE, D, NJ>), smem);
+  constexpr int smem = smem_bytes<MODE, D, NJ, NT>();
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&attend_kernel<MODE, D, NJ, NT>), smem);
   if (e != cudaSuccess) return e;
   const long long nunits = static_cast<long long>(p.c.B) * p.c.Hkv;
   const long long grid = nunits * (p.S_q + p.S_t);
-  attend_kernel<MODE, D, NJ><<<static_cast<unsigned>(grid), NTHREADS, smem, s>>>(p);
+  attend_kernel<MODE, D, NJ, NT><<<static_cast<unsigned>(grid), NTHREADS, smem, s>>>(p);
   return cudaGetLastError();
 }
 
 // Resident CTAs per SM of one kernel variant times the SM count, queried once
 // per device (the split count is sized to fill whole waves).
-template <int MODE, int D, int NJ>
+template <int MODE, int D, int NJ, int NT>
 int resident_ctas_t() {
   constexpr int kMaxDev = 64;
   static int cached[kMaxDev] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
   if (cached[dev] > 0) return cached[dev];
-  using L = Smem<MODE, D, NJ>;
-  constexpr int smem = (L::TOTAL > TailSmem<D>::TOTAL) ? L::TOTAL : TailSmem<D>::TOTAL;
-  if (set_smem_once(reinterpret_cast<const void*>(&attend_kernel<MODE, D, NJ>), smem) != cudaSuccess) return 0;
+  constexpr int smem = smem_bytes<MODE, D, NJ, NT>();
+  if (set_smem_once(reinterpret_cast<const void*>(&attend_kernel<MODE, D, NJ, NT>), smem) != cudaSuccess) return 0;
   int per_sm = 0, sms = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attend_kernel<MODE, D, NJ>, NTHREADS, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attend_kernel<MODE, D, NJ, NT>, NTHREADS, smem) !=
+      cudaSuccess)
     return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   cached[dev] = per_sm * sms;
   return cached[dev];
 }
 
-template <int MODE>
-int resident_mode(int D, int NJ) {
-  if (D == 128) {
-    if (NJ == 1) return resident_ctas_t<MODE, 128, 1>();
-    if (NJ == 2) return resident_ctas_t<MODE, 128, 2>();
-    if (NJ == 4) return resident_ctas_t<MODE, 128, 4>();
-  } else if (D == 64) {
-    if (NJ == 1) return resident_ctas_t<MODE, 64, 1>();
-    if (NJ == 2) return resident_ctas_t<MODE, 64, 2>();
+// Dispatch over (D, G): F<D, NJ>::run() with NJ = D / G.
+template <int MODE, int NT>
+struct Variant {
+  static int resident(int D, int NJ) {
+    if (D == 128) {
+      if (NJ == 1) return resident_ctas_t<MODE, 128, 1, NT>();
+      if (NJ == 2) return resident_ctas_t<MODE, 128, 2, NT>();
+      if (NJ == 4) return resident_ctas_t<MODE, 128, 4, NT>();
+    } else if (D == 64) {
+      if (NJ == 1) return resident_ctas_t<MODE, 64, 1, NT>();
+      if (NJ == 2) return resident_ctas_t<MODE, 64, 2, NT>();
+    }
+    return 0;
   }
-  return 0;
+  static cudaError_t launch(const AttendParams& p, cudaStream_t s) {
+    const int D = p.c.D, NJ = p.c.D / p.c.G;
+    if (D == 128) {
+      if (NJ == 1) return launch_t<MODE, 128, 1, NT>(p, s);
+      if (NJ == 2) return launch_t<MODE, 128, 2, NT>(p, s);
+      if (NJ == 4) return launch_t<MODE, 128, 4, NT>(p, s);
+    } else if (D == 64) {
+      if (NJ == 1) return launch_t<MODE, 64, 1, NT>(p, s);
+      if (NJ == 2) return launch_t<MODE, 64, 2, NT>(p, s);
+    }
+    return cudaErrorInvalidValue;
+  }
+};
+
+template <int MODE>
+int resident_mode(int D, int NJ, int R) {
+  return R <= 4 ? Variant<MODE, 1>::resident(D, NJ) : Variant<MODE, 2>::resident(D, NJ);
 }
 
 template <int MODE>
 cudaError_t launch_mode(const AttendParams& p, cudaStream_t s) {
-  const int D = p.c.D, NJ = p.c.D / p.c.G;
-  if (D == 128) {
-    if (NJ == 1) return launch_t<MODE, 128, 1>(p, s);
-    if (NJ == 2) return launch_t<MODE, 128, 2>(p, s);
-    if (NJ == 4) return launch_t<MODE, 128, 4>(p, s);
-  } else if (D == 64) {
-    if (NJ == 1) return launch_t<MODE, 64, 1>(p, s);
-    if (NJ == 2) return launch_t<MODE, 64, 2>(p, s);
-  }
-  return cudaErrorInvalidValue;
+  return p.R <= 4 ? Variant<MODE, 1>::launch(p, s) : Variant<MODE, 2>::launch(p, s);
 }
 
 }  // namespace
 
-int attend_resident_ctas(int mode, int D, int G) {
+int attend_resident_ctas(int mode, int D, int G, int R) {
   const int NJ = D / G;
   switch (mode) {
-    case KVQ_MODE_INT8: return resident_mode<KVQ_MODE_INT8>(D, NJ);
-    case KVQ_MODE_INT4: return resident_mode<KVQ_MODE_INT4>(D, NJ);
-    case KVQ_MODE_INT2: return resident_mode<KVQ_MODE_INT2>(D, NJ);
-    case KVQ_MODE_INT1: return resident_mode<KVQ_MODE_INT1>(D, NJ);
+    case KVQ_MODE_INT8: return resident_mode<KVQ_MODE_INT8>(D, NJ, R);
+    case KVQ_MODE_INT4: return resident_mode<KVQ_MODE_INT4>(D, NJ, R);
+    case KVQ_MODE_INT2: return resident_mode<KVQ_MODE_INT2>(D, NJ, R);
+    case KVQ_MODE_INT1: return resident_mode<KVQ_MODE_INT1>(D, NJ, R);
     default: return 0;
   }
 }

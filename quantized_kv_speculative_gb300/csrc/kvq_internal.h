@@ -11,17 +11,15 @@ namespace kvq {
 
 constexpr int kMaxRows = 8;            // rows (gamma x query heads per KV head) per kernel
 constexpr int kChunkAlign = 128;       // split boundaries are multiples of this many tokens
-constexpr int kMaxChunk = 32768;       // tokens per attention split (bounds the selection bitmap)
+constexpr int kMaxChunk = 8192;        // tokens per attention split (bounds the selection bitmap)
 constexpr int kTargetCtas = 608;       // 4 x 152 SMs: split-count target per launch
 constexpr int kTopkMaxChunk = 8192;    // tokens per top-k split (scores held in shared memory)
 constexpr int kTopkMaxCand = 4096;     // splits x k candidates merged by the last CTA
-constexpr int kTopkMaxCtas = 2048;     // bound on the CTAs of one top-k wave (sizes the workspace)
-constexpr int kTopkMinChunk = 512;     // fewest tokens per top-k split
 constexpr int kMaxTopk = 1024;
 constexpr int kMaxTailSplits = 8;      // CTAs per (b, kvh) for the bf16 tail
 constexpr int kMaxCombine = 256;       // partials per (b, kvh) merged by the combine
 constexpr int kMaxQuantSplits = kMaxCombine - kMaxTailSplits;
-constexpr int kTailTokensPerSplit = 48;
+constexpr int kTailTokensPerSplit = 320;  // bf16 tail tokens per tail CTA (usually one per (b, kvh))
 constexpr int kStatusBytes = 256;      // workspace header (status word)
 constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s at 2 GHz
 __host__ __device__ constexpr int kPartialFloats(int D) { return 2 * kMaxRows + kMaxRows * D; }
@@ -110,10 +108,11 @@ cudaError_t launch_residual_write(const ResidualWriteParams& p, cudaStream_t s);
 cudaError_t launch_attend(const AttendParams& p, int mode, cudaStream_t s);
 // CTAs of the attention kernel variant that fit on the current device at once
 // (0 if unknown).
-int attend_resident_ctas(int mode, int D, int G);
+int attend_resident_ctas(int mode, int D, int G, int R);
 cudaError_t launch_topk(const TopkParams& p, int mode, cudaStream_t s);
-// CTAs of the top-k kernel variant that fit on the current device at once (0 if unknown).
-int topk_resident_ctas(int mode, int D);
+// Top-k split plan for the current device: returns the split count S per
+// (b, kv head) and sets *chunk (tokens per split).
+int topk_plan(int mode, int D, int G, long long Lq, long long U, int k, long long* chunk);
 cudaError_t launch_wait_selftest(int* status, long long limit, cudaStream_t s);
 
 }  // namespace kvq

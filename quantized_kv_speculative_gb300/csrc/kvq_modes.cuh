@@ -182,4 +182,171 @@ __device__ __forceinline__ void value_frags(const uint8_t* va, const uint8_t* vb
   }
 }
 
+
+// ------------------------------------------------------------------------------
+// Offset encoding for attention.  An f16 whose upper byte is 0x64 has exponent
+// 10, so its value is 1024 + m, where m is the 10-bit mantissa field.  A b-bit
+// code c whose bits sit at mantissa positions k..k+b-1 (k + b <= 10) thus reads
+// as exactly 1024 + 2^k c, and one LOP3 (mask, or with 0x6400) turns two codes
+// 16 bits apart into a half2.  For the 8-bit target code the two nibble planes
+// are first merged into bytes (shift + LOP3 per four codes), then a PRMT drops
+// each byte under 0x64.  An exact f16x2 subtract then removes the 1024, which
+// leaves 2^k c.
+//
+// For values, a lane reads 8 consecutive tokens 8q..8q+7 of a channel row;
+// pair i covers tokens 8q + VA[i], 8q + VB[i] with factor vx_mult(i).  For the
+// key chunk of a lane (D/4 channels of a token row), pair p covers channels
+// kx_chan(p, 0) and kx_chan(p, 1).
+// ------------------------------------------------------------------------------
+
+constexpr uint32_t X1024 = 0x64006400u;   // half2(1024, 1024)
+constexpr uint32_t X64B = 0x64646464u;    // prmt source of the 0x64 bytes
+
+__device__ __forceinline__ uint32_t xsel(uint32_t w, uint32_t mask) { return (w & mask) | X1024; }
+
+// (1024 + m) - 1024 = m for both halves, exactly: value codes lose the offset
+// before they enter the long P.V accumulation.
+__device__ __forceinline__ uint32_t xoff(uint32_t x) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(X1024));
+  return r;
+}
+
+template <int MODE>
+struct XPair {
+  // value token pairs per pair index i (tokens relative to 8q)
+  static constexpr int VA[4] = {0, 1, 2, 3};
+  static constexpr int VB[4] = {4, 5, 6, 7};
+};
+template <>
+struct XPair<KVQ_MODE_INT8> {
+  static constexpr int VA[4] = {0, 4, 1, 5};
+  static constexpr int VB[4] = {2, 6, 3, 7};
+};
+
+// Value factor of pair i: the power of two at which the pair's codes sit.
+template <int MODE>
+__host__ __device__ constexpr float vx_mult(int i) {
+  if constexpr (MODE == KVQ_MODE_INT8) return 1.f;
+  else if constexpr (MODE == KVQ_MODE_INT4) return (i & 1) ? 16.f : 1.f;
+  else if constexpr (MODE == KVQ_MODE_INT2) return static_cast<float>(1 << (2 * i));
+  else return static_cast<float>(1 << i);
+}
+
+// Keys for attention.  INT8 keys become exact f16 codes (offset encoding, then
+// the 1024 removed); INT4/INT2/INT1 keys use the top-of-mantissa encoding of
+// key_pairs (1 + c/2^b), whose offset of 1 is at most about twice the code
+// term.  Either way the accumulator never carries an offset much larger than
+// the logit.  kx_weight is the factor that turns a code's scale into the
+// weight of the encoded value; kx_offset the value an all-zero code reads as.
+template <int MODE>
+__host__ __device__ constexpr float kx_weight() {
+  return MODE == KVQ_MODE_INT8 ? 1.f : static_cast<float>(1 << Mode<MODE>::CB);
+}
+template <int MODE>
+__host__ __device__ constexpr float kx_offset() {
+  return MODE == KVQ_MODE_INT8 ? 0.f : 1.f;
+}
+
+// Channels (relative to the lane chunk) of key pair p.
+template <int MODE, int D>
+__host__ __device__ constexpr int kx_chan(int p, int e) {
+  if constexpr (MODE == KVQ_MODE_INT8) {
+    constexpr int A8[4] = {0, 4, 1, 5};
+    return 8 * (p / 4) + A8[p % 4] + 2 * e;
+  } else if constexpr (MODE == KVQ_MODE_INT4) {
+    return 8 * (p / 4) + p % 4 + 4 * e;
+  } else if constexpr (MODE == KVQ_MODE_INT2) {
+    return 16 * (p / 8) + p % 8 + 8 * e;
+  } else {
+    return p + e * (D == 128 ? 16 : 8);
+  }
+}
+
+// The lane's key chunk of one token row as D/8 f16 pairs.  `k0` points at the
+// chunk in plane 0; plane 1 (INT8 lower nibbles) lies `plane_stride` bytes
+// further.
+template <int MODE, int D>
+__device__ __forceinline__ void key_pairs_x(const uint8_t* k0, int plane_stride, uint32_t (&P)[D / 8]) {
+  if constexpr (MODE == KVQ_MODE_INT8) {
+    constexpr int NWD = D / 32;
+    uint32_t h[NWD], l[NWD];
+    if constexpr (NWD == 4) {
+      const uint4 v = *reinterpret_cast<const uint4*>(k0);
+      const uint4 w = *reinterpret_cast<const uint4*>(k0 + plane_stride);
+      h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
+      l[0] = w.x; l[1] = w.y; l[2] = w.z; l[3] = w.w;
+    } else {
+      const uint2 v = *reinterpret_cast<const uint2*>(k0);
+      const uint2 w = *reinterpret_cast<const uint2*>(k0 + plane_stride);
+      h[0] = v.x; h[1] = v.y;
+      l[0] = w.x; l[1] = w.y;
+    }
+#pragma unroll
+    for (int w = 0; w < NWD; ++w) {
+      const uint32_t E = ((h[w] << 4) & 0xF0F0F0F0u) | (l[w] & 0x0F0F0F0Fu);
+      const uint32_t O = (h[w] & 0xF0F0F0F0u) | ((l[w] >> 4) & 0x0F0F0F0Fu);
+      P[4 * w + 0] = xoff(__byte_perm(E, X64B, 0x4140));
+      P[4 * w + 1] = xoff(__byte_perm(E, X64B, 0x4342));
+      P[4 * w + 2] = xoff(__byte_perm(O, X64B, 0x4140));
+      P[4 * w + 3] = xoff(__byte_perm(O, X64B, 0x4342));
+    }
+  } else {
+    key_pairs<MODE, D>(k0, plane_stride, P);
+  }
+}
+
+// A fragments of P.V for one channel m-tile (rows ca = 16mt+g and cb = ca+8) of
+// one 32-token slab, as exact f16 values vx_mult(i) * code (the offset removed).  a[s] serves k-step s: a[s][0..1] are pair
+// 2s of rows ca/cb (k = 2q, 2q+1), a[s][2..3] pair 2s+1 (k = 2q+8, 2q+9).
+// `va`/`vb` point at rows ca/cb of plane 0.
+template <int MODE>
+__device__ __forceinline__ void value_frags_x(const uint8_t* va, const uint8_t* vb, int plane_stride, int q,
+                                              uint32_t (&a)[2][4]) {
+  uint32_t pa[4], pb[4];
+  if constexpr (MODE == KVQ_MODE_INT8) {
+    const uint32_t ha = *reinterpret_cast<const uint32_t*>(va + 4 * q);
+    const uint32_t hb = *reinterpret_cast<const uint32_t*>(vb + 4 * q);
+    const uint32_t la = *reinterpret_cast<const uint32_t*>(va + plane_stride + 4 * q);
+    const uint32_t lb = *reinterpret_cast<const uint32_t*>(vb + plane_stride + 4 * q);
+    const uint32_t Ea = ((ha << 4) & 0xF0F0F0F0u) | (la & 0x0F0F0F0Fu);
+    const uint32_t Oa = (ha & 0xF0F0F0F0u) | ((la >> 4) & 0x0F0F0F0Fu);
+    const uint32_t Eb = ((hb << 4) & 0xF0F0F0F0u) | (lb & 0x0F0F0F0Fu);
+    const uint32_t Ob = (hb & 0xF0F0F0F0u) | ((lb >> 4) & 0x0F0F0F0Fu);
+    pa[0] = __byte_perm(Ea, X64B, 0x4140); pa[1] = __byte_perm(Ea, X64B, 0x4342);
+    pa[2] = __byte_perm(Oa, X64B, 0x4140); pa[3] = __byte_perm(Oa, X64B, 0x4342);
+    pb[0] = __byte_perm(Eb, X64B, 0x4140); pb[1] = __byte_perm(Eb, X64B, 0x4342);
+    pb[2] = __byte_perm(Ob, X64B, 0x4140); pb[3] = __byte_perm(Ob, X64B, 0x4342);
+  } else if constexpr (MODE == KVQ_MODE_INT4) {
+    const uint32_t wa = *reinterpret_cast<const uint32_t*>(va + 4 * q);
+    const uint32_t wb = *reinterpret_cast<const uint32_t*>(vb + 4 * q);
+    const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+    pa[0] = xsel(wa, 0x000F000Fu); pa[1] = xsel(wa, 0x00F000F0u);
+    pa[2] = xsel(wa8, 0x000F000Fu); pa[3] = xsel(wa8, 0x00F000F0u);
+    pb[0] = xsel(wb, 0x000F000Fu); pb[1] = xsel(wb, 0x00F000F0u);
+    pb[2] = xsel(wb8, 0x000F000Fu); pb[3] = xsel(wb8, 0x00F000F0u);
+  } else if constexpr (MODE == KVQ_MODE_INT2) {
+    const uint32_t xa = *reinterpret_cast<const uint16_t*>(va + 2 * q);
+    const uint32_t xb = *reinterpret_cast<const uint16_t*>(vb + 2 * q);
+    const uint32_t y = __byte_perm(xa, xb, 0x5140);   // [a.b0, b.b0, a.b1, b.b1]
+    const uint32_t y8 = y >> 8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      pa[j] = xsel(y, 0x00030003u << (2 * j));
+      pb[j] = xsel(y8, 0x00030003u << (2 * j));
+    }
+  } else {
+    const uint32_t x = static_cast<uint32_t>(va[q]) | (static_cast<uint32_t>(vb[q]) << 8);
+    const uint32_t y = (x & 0x0F0Fu) | ((x & 0xF0F0u) << 12);
+    const uint32_t y8 = y >> 8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      pa[j] = xsel(y, 0x00010001u << j);
+      pb[j] = xsel(y8, 0x00010001u << j);
+    }
+  }
+  a[0][0] = xoff(pa[0]); a[0][1] = xoff(pb[0]); a[0][2] = xoff(pa[1]); a[0][3] = xoff(pb[1]);
+  a[1][0] = xoff(pa[2]); a[1][1] = xoff(pb[2]); a[1][2] = xoff(pa[3]); a[1][3] = xoff(pb[3]);
+}
+
 }  // namespace kvq

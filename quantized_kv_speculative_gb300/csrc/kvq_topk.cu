@@ -9,18 +9,28 @@
 //   W_d = rint(fp32(qs_d * s_d) * 2^(21-e)), S_t = sum_d W_d c_{t,d},
 //   score_t = fp32(fp32(fp32(S_t) * 2^(e-21)) + beta),
 //   beta = pairwise tree over 32 lane-chunks of sequential fp32 sums of fp32(qs_d * z_d).
-// The dot product runs on tensor cores.  W is split into two f16-exact integer
-// halves (|hi|, |lo| <= 1024, W = 2048 hi + lo).  The codes are exact f16
-// values 1 + c/2^b.  Every partial sum is a multiple of 2^-b below 2^18, so the
-// fp32 accumulation is exact in any order.  fp32(S_t) = fp32(2048 S_hi + S_lo) is
-// then a single correctly rounded fp32 add of two exact values.
+// The dot product runs on tensor cores with the keys as the A operand (rows =
+// tokens) and W as the B operand: column 0 holds hi and column 1 holds lo,
+// where W = 2048 hi + lo and |hi|, |lo| <= 1024 are f16-exact integers.  The
+// codes are exact f16 values 1 + c/2^b.  Every partial sum is a multiple of
+// 2^-b below 2^18, so the fp32 accumulation is exact in any order.
+// fp32(S_t) = fp32(2048 S_hi + S_lo) is then a single correctly rounded fp32 add
+// of two exact values.  Each warp derives W for a key group cooperatively (D/32
+// channels per lane) and shares it through shared memory.
 //
-// One launch: B*Hkv*S CTAs, sized to run in a single wave.  Each CTA scores one
-// chunk (bulk-copied tiles on an mbarrier ring, as in attention) into 32-bit
-// order keys, radix-selects its top k by (score desc, index asc), and writes k
-// candidates.  The last CTA of each (b, kvh), found through an atomic ticket,
-// radix-selects the k best of the S*k candidates under the unique composite key
+// One launch: B*Hkv*S CTAs, with S chosen on the host to balance waves against
+// the merge.  Each CTA scores one chunk (bulk-copied tiles on an mbarrier ring,
+// as in attention) into 32-bit order keys and selects its top k by (score desc,
+// index asc).  The last CTA of each (b, kvh), found through an atomic ticket,
+// selects the k best of the S*k candidates under the unique composite key
 // (order key, ~index), then places each winner by counting the winners above it.
+//
+// Selection (select_kth): the block finds the smallest and largest key,
+// histograms the 8 bits below their common prefix and locates the bin that
+// holds the kth key.  When that bin holds few keys they are gathered and ranked
+// directly; otherwise the next 8 bits of that bin are histogrammed, and so on.
+#include <algorithm>
+
 #include "kvq_modes.cuh"
 
 namespace kvq {
@@ -30,6 +40,7 @@ constexpr int NW = 4;
 constexpr int SPW = 2;
 constexpr int NSLOT = NW * SPW;
 constexpr int NTHREADS = (NW + 1) * 32;
+constexpr int kGather = 64;            // bin size below which keys are ranked directly
 
 template <int MODE, int D>
 struct TopkSmem {
@@ -40,17 +51,28 @@ struct TopkSmem {
   static constexpr int KSZ_OFF = KPLANE;                      // only the upper/only plane is read
   static constexpr int KSZ_BYTES = (TT / 32) * 2 * D * 4;
   static constexpr int SLOT = KSZ_OFF + KSZ_BYTES;
-  static constexpr int SC_OFF = NSLOT * SLOT;                 // order keys / merge keys
-  static constexpr int SC_BYTES = kTopkMaxCand * 8;           // >= kTopkMaxChunk * 4
-  static constexpr int QS_OFF = SC_OFF + SC_BYTES;            // qs[D]
-  static constexpr int HIST_OFF = QS_OFF + D * 4;             // hist[256]
-  static constexpr int BAR_OFF = HIST_OFF + 256 * 4;
+  static constexpr int QS_OFF = NSLOT * SLOT;                 // qs[D]
+  static constexpr int WB_OFF = QS_OFF + D * 4;               // per warp: W halves in pair order [2][D] f16
+  static constexpr int HIST_OFF = WB_OFF + NW * 2 * D * 2;    // hist[256]
+  static constexpr int LIST_OFF = HIST_OFF + 256 * 4;         // gathered keys [kGather]
+  static constexpr int RED_OFF = LIST_OFF + kGather * 4;      // per-warp min/max, counts [16]
+  static constexpr int BAR_OFF = RED_OFF + 16 * 4;
   static constexpr int MISC_OFF = BAR_OFF + 2 * NSLOT * 8;
-  static constexpr int TOTAL = MISC_OFF + 64;
-  static_assert(kTopkMaxChunk * 4 <= SC_BYTES, "chunk scores must fit");
+  static constexpr int SC_OFF = MISC_OFF + 64;                // order keys / merge keys (sized per launch)
+  static constexpr int MAX_SC = kTopkMaxCand * 8;             // >= kTopkMaxChunk * 4
+  static constexpr int MAX_TOTAL = SC_OFF + MAX_SC;
+  static_assert(kTopkMaxChunk * 4 <= MAX_SC, "chunk scores must fit");
   static_assert(SLOT % 16 == 0, "slots must stay 16-byte aligned");
+  static_assert(BAR_OFF % 8 == 0, "mbarriers need 8-byte alignment");
   static_assert(NSLOT * SLOT >= 2 * kMaxTopk * 4, "the merge winners reuse the stage area");
 };
+
+template <int MODE, int D>
+int smem_bytes(long long chunk, int S, int k) {
+  using L = TopkSmem<MODE, D>;
+  const long long sc = std::max(chunk * 4, static_cast<long long>(S) * k * 8);
+  return static_cast<int>(L::SC_OFF + ((sc + 15) / 16) * 16);
+}
 
 __device__ __forceinline__ uint32_t order_key(float s) {
   const uint32_t b = __float_as_uint(__fadd_rn(s, 0.0f));  // -0 -> +0
@@ -66,39 +88,85 @@ __device__ __forceinline__ float pow2f(int e) {  // 2^e for -126 <= e <= 127
   return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 
-// Block-wide radix select, 8-bit digits from the most significant.  Among the
-// i < n for which take(i, key) is true, it finds the kth largest key T
-// (1 <= kth <= number taken).  On return st[0] = T and st[2] = how many of the
-// taken keys equal to T belong to the kth largest.  Every thread of the block
-// calls it; st[0..2] and hist[256] are shared memory.
-template <typename F>
-__device__ void radix_select(int n, int kth, F take, uint32_t* hist, int* st) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    st[0] = 0;
-    st[1] = 0;
-    st[2] = kth;
+// Position, in halves, of channel `local` (within a lane chunk of D/4
+// channels) in the pair order of key_pairs: 2 * pair + (0: low half, 1: high).
+template <int MODE, int D>
+__device__ __forceinline__ int pair_slot(int local) {
+  int pp, e;
+  if constexpr (Mode<MODE>::PB == 4) {
+    pp = 4 * (local / 8) + local % 4;
+    e = (local % 8) / 4;
+  } else if constexpr (Mode<MODE>::PB == 2) {
+    pp = 8 * (local / 16) + local % 8;
+    e = (local % 16) / 8;
+  } else {
+    constexpr int HALF = (D == 128) ? 16 : 8;
+    pp = local % HALF;
+    e = local / HALF;
   }
-  const int nround = (n + blockDim.x - 1) / blockDim.x * blockDim.x;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0u;
+  return 2 * pp + e;
+}
+
+// Block-wide selection of the kth largest key among the i < n for which
+// take(i, key) holds (1 <= kth <= number taken).  On return st[0] = T and
+// st[2] = how many of the taken keys equal to T belong to the kth largest.
+// Every thread of the block calls it.  hist[256], list[kGather], red[16] and
+// st[0..4] are shared memory.
+template <typename F>
+__device__ void select_kth(int n, int kth, F take, uint32_t* hist, uint32_t* list, uint32_t* red, int* st) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nw = (blockDim.x + 31) / 32;
+  // ---- smallest and largest taken key ----
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  for (int i = tid; i < n; i += blockDim.x) {
+    uint32_t key;
+    if (take(i, key)) {
+      lo = min(lo, key);
+      hi = max(hi, key);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if (lane == 0) {
+    red[2 * warp] = lo;
+    red[2 * warp + 1] = hi;
+  }
+  for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0u;
+  if (tid == 0) st[4] = 0;
+  __syncthreads();
+  lo = red[0];
+  hi = red[1];
+  for (int w = 1; w < nw; ++w) {
+    lo = min(lo, red[2 * w]);
+    hi = max(hi, red[2 * w + 1]);
+  }
+  if (lo == hi) {  // every taken key is equal
     __syncthreads();
-    const uint32_t prefix = static_cast<uint32_t>(st[0]), mask = static_cast<uint32_t>(st[1]);
-    // warp-aggregated histogram: lanes with the same bin add once
-    for (int i = tid; i < nround; i += blockDim.x) {
-      uint32_t key = 0, bin = 0xFFFFFFFFu;
-      bool ok = false;
-      if (i < n) {
-        ok = take(i, key) && (key & mask) == prefix;
-        if (ok) bin = (key >> shift) & 255u;
-      }
-      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-      if (ok && (__ffs(peers) - 1) == lane) atomicAdd(hist + bin, static_cast<uint32_t>(__popc(peers)));
+    if (tid == 0) {
+      st[0] = static_cast<int>(lo);
+      st[2] = kth;
+    }
+    __syncthreads();
+    return;
+  }
+  const int hb = 31 - __clz(lo ^ hi);                  // highest bit where taken keys differ
+  uint32_t mask = (hb == 31) ? 0u : ~((2u << hb) - 1u);
+  uint32_t prefix = lo & mask;
+  int shift = max(hb - 7, 0);
+  int remaining = kth;
+  while (true) {
+    // ---- histogram of the 8 bits at `shift` among keys matching the prefix ----
+    for (int i = tid; i < n; i += blockDim.x) {
+      uint32_t key;
+      if (take(i, key) && (key & mask) == prefix) atomicAdd(hist + ((key >> shift) & 255u), 1u);
     }
     __syncthreads();
     if (warp == 0) {
-      // Lane l owns bins 255-8l .. 248-8l (descending); a warp scan gives the
-      // count above each lane, and the lane holding the kth key picks its digit.
+      // lane l owns bins 255-8l .. 248-8l (descending); a warp scan gives the
+      // count above each lane, and the lane holding the kth key picks its digit
       uint32_t c[8];
       uint32_t tot = 0;
 #pragma unroll
@@ -113,23 +181,66 @@ __device__ void radix_select(int n, int kth, F take, uint32_t* hist, int* st) {
         if (lane >= o) inc += v;
       }
       const uint32_t excl = inc - tot;
-      const uint32_t remaining = static_cast<uint32_t>(st[2]);
-      if (excl < remaining && remaining <= inc) {
+      const uint32_t rem = static_cast<uint32_t>(remaining);
+      if (excl < rem && rem <= inc) {
         uint32_t cum = excl;
         int digit = 255 - 8 * lane - 7;
+        uint32_t bin = c[7];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          if (cum + c[k] >= remaining) {
+          if (cum + c[k] >= rem) {
             digit = 255 - 8 * lane - k;
+            bin = c[k];
             break;
           }
           cum += c[k];
         }
-        st[2] = static_cast<int>(remaining - cum);
-        st[0] = static_cast<int>(prefix | (static_cast<uint32_t>(digit) << shift));
-        st[1] = static_cast<int>(mask | (255u << shift));
+        st[0] = digit;
+        st[1] = static_cast<int>(rem - cum);
+        st[3] = static_cast<int>(bin);
       }
     }
+    __syncthreads();
+    const uint32_t digit = static_cast<uint32_t>(st[0]);
+    remaining = st[1];
+    const int bin = st[3];
+    prefix |= digit << shift;
+    mask |= 255u << shift;
+    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0u;
+    if (shift == 0) {  // the key is fully determined
+      __syncthreads();
+      if (tid == 0) {
+        st[0] = static_cast<int>(prefix);
+        st[2] = remaining;
+      }
+      __syncthreads();
+      return;
+    }
+    if (bin <= kGather) {
+      // ---- gather the bin's keys and rank them ----
+      for (int i = tid; i < n; i += blockDim.x) {
+        uint32_t key;
+        if (take(i, key) && (key & mask) == prefix) list[atomicAdd(st + 4, 1)] = key;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        for (int j = lane; j < bin; j += 32) {
+          const uint32_t kj = list[j];
+          int above = 0, eq = 0;
+          for (int i = 0; i < bin; ++i) {
+            above += list[i] > kj;
+            eq += list[i] == kj;
+          }
+          if (above < remaining && remaining <= above + eq) {  // every such lane writes the same
+            st[0] = static_cast<int>(kj);
+            st[2] = remaining - above;
+          }
+        }
+      }
+      __syncthreads();
+      return;
+    }
+    shift = max(shift - 8, 0);
     __syncthreads();
   }
 }
@@ -156,9 +267,11 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   uint32_t* okeys = reinterpret_cast<uint32_t*>(smem + L::SC_OFF);
   float* qs = reinterpret_cast<float*>(smem + L::QS_OFF);
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L::HIST_OFF);
+  uint32_t* list = reinterpret_cast<uint32_t*>(smem + L::LIST_OFF);
+  uint32_t* red = reinterpret_cast<uint32_t*>(smem + L::RED_OFF);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* empty = full + NSLOT;
-  int* misc = reinterpret_cast<int*>(smem + L::MISC_OFF);   // [0] abort, [1] flag, [2..] select state
+  int* misc = reinterpret_cast<int*>(smem + L::MISC_OFF);   // [0] abort, [1] flag, [2..6] select state
 
   if (tid == 0) {
     for (int s = 0; s < NSLOT; ++s) {
@@ -208,12 +321,17 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
       }
     }
   } else {
-    uint32_t wa[D / 16][4];
-    float neg_hi = 0.f, neg_lo = 0.f, unit = 1.f, beta = 0.f;
+    // B fragments: lane (g, q) holds column g of W for its channel chunk; only
+    // columns 0 (hi) and 1 (lo) are nonzero.
+    uint32_t wb[D / 8];
+#pragma unroll
+    for (int pp = 0; pp < D / 8; ++pp) wb[pp] = 0u;
+    float init0 = 0.f, init1 = 0.f, unit = 1.f, beta = 0.f;
     long long cur_grp = -1;
-    const int qbase = q * (D / 4);
     const float smul = static_cast<float>(M::MULT);
     const float cbmul = static_cast<float>(1 << M::CB);
+    uint16_t* whalf = reinterpret_cast<uint16_t*>(smem + L::WB_OFF) + warp * 2 * D;   // [hi D][lo D], pair order
+    constexpr int CPL = D / 32;   // channels per lane in the cooperative setup
     for (int j = 0; j < per_warp; ++j) {
       const int ti = warp * per_warp + j;
       if (ti >= ntiles) break;
@@ -233,14 +351,17 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
         const long long tok0 = t0 + 32 * sl;
         const long long grp = tok0 / G;
         if (grp != cur_grp) {
+          // ---- W of this group: lane l derives channels [l*D/32, (l+1)*D/32) ----
           cur_grp = grp;
           const float* ks = ksz + (grp - g_first) * 2 * D;
           const float* kz = ks + D;
-          // max |w| and beta over lane chunks of D/32 channels
+          float w[CPL];
           float mxw = 0.f, bp = 0.f;
-          for (int d = lane * (D / 32); d < (lane + 1) * (D / 32); ++d) {
-            const float w = __fmul_rn(qs[d], __fmul_rn(ks[d], smul));
-            mxw = fmaxf(mxw, fabsf(w));
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            const int d = lane * CPL + c;
+            w[c] = __fmul_rn(qs[d], __fmul_rn(ks[d], smul));
+            mxw = fmaxf(mxw, fabsf(w[c]));
             bp = __fadd_rn(bp, __fmul_rn(qs[d], kz[d]));
           }
 #pragma unroll
@@ -256,53 +377,52 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
           unit = pow2f(e - 21);
           float shi = 0.f, slo = 0.f;
 #pragma unroll
-          for (int pp = 0; pp < D / 8; ++pp) {
-            const int2 ch = pair_chan<MODE, D>(pp);
-            const int c0 = qbase + ch.x, c1 = qbase + ch.y;
-            const float W0 = rintf(__fmul_rn(__fmul_rn(qs[c0], __fmul_rn(ks[c0], smul)), up));
-            const float W1 = rintf(__fmul_rn(__fmul_rn(qs[c1], __fmul_rn(ks[c1], smul)), up));
-            const float h0 = floorf(__fmul_rn(__fadd_rn(W0, 1024.f), 1.0f / 2048.f));
-            const float h1 = floorf(__fmul_rn(__fadd_rn(W1, 1024.f), 1.0f / 2048.f));
-            const float l0 = __fsub_rn(W0, __fmul_rn(2048.f, h0));
-            const float l1 = __fsub_rn(W1, __fmul_rn(2048.f, h1));
-            const bool mine = (g == 0);
-            wa[pp / 2][(pp % 2) * 2 + 0] = mine ? pack_half2(h0, h1) : 0u;
-            wa[pp / 2][(pp % 2) * 2 + 1] = mine ? pack_half2(l0, l1) : 0u;
-            shi += h0 + h1;
-            slo += l0 + l1;
+          for (int c = 0; c < CPL; ++c) {
+            const int d = lane * CPL + c;
+            const float W = rintf(__fmul_rn(w[c], up));
+            const float h = floorf(__fmul_rn(__fadd_rn(W, 1024.f), 1.0f / 2048.f));
+            const float l = __fsub_rn(W, __fmul_rn(2048.f, h));
+            shi += h;
+            slo += l;
+            const int pos = (d / (D / 4)) * (D / 4) + pair_slot<MODE, D>(d % (D / 4));
+            whalf[pos] = __half_as_ushort(__float2half_rn(h));
+            whalf[D + pos] = __half_as_ushort(__float2half_rn(l));
           }
-          shi += __shfl_xor_sync(0xffffffffu, shi, 1);
-          shi += __shfl_xor_sync(0xffffffffu, shi, 2);
-          slo += __shfl_xor_sync(0xffffffffu, slo, 1);
-          slo += __shfl_xor_sync(0xffffffffu, slo, 2);
-          neg_hi = -shi;
-          neg_lo = -slo;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            shi += __shfl_xor_sync(0xffffffffu, shi, o);
+            slo += __shfl_xor_sync(0xffffffffu, slo, o);
+          }
+          init0 = -shi;
+          init1 = -slo;
+          __syncwarp();
+          if (g < 2) {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(whalf + g * D) + q * (D / 8);
+#pragma unroll
+            for (int pp = 0; pp < D / 8; ++pp) wb[pp] = src[pp];
+          }
+          __syncwarp();
         }
         const uint8_t* kslab = sbase + (32 * sl) * RW::KROW + q * RW::KCHUNK;
-        float cc[4][4];
-        {
-          uint32_t P[4][D / 8];
 #pragma unroll
-          for (int jt = 0; jt < 4; ++jt) {
-            cc[jt][0] = neg_hi; cc[jt][1] = neg_hi; cc[jt][2] = neg_lo; cc[jt][3] = neg_lo;
-            key_pairs<MODE, D>(kslab + (4 * g + jt) * RW::KROW, 0, P[jt]);
+        for (int s = 0; s < 2; ++s) {
+          uint32_t PA[D / 8], PB[D / 8];
+          key_pairs<MODE, D>(kslab + (16 * s + g) * RW::KROW, 0, PA);
+          key_pairs<MODE, D>(kslab + (16 * s + g + 8) * RW::KROW, 0, PB);
+          float cc[4] = {init0, init1, init0, init1};
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t a[4] = {PA[2 * kk], PB[2 * kk], PA[2 * kk + 1], PB[2 * kk + 1]};
+            mma16816(cc, a, wb[2 * kk], wb[2 * kk + 1]);
           }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-#pragma unroll
-            for (int jt = 0; jt < 4; ++jt) mma16816(cc[jt], wa[kk], P[jt][2 * kk], P[jt][2 * kk + 1]);
-        }
-#pragma unroll
-        for (int jt = 0; jt < 4; ++jt) {
-          const float* c = cc[jt];
-          if (g == 0) {
-            const int rel = static_cast<int>(tok0 - t_begin) + 8 * q + jt;
+          if (q == 0) {
+            const int rel = static_cast<int>(tok0 - t_begin) + 16 * s + g;
 #pragma unroll
             for (int e2 = 0; e2 < 2; ++e2) {
-              const float shi_t = __fmul_rn(c[e2], cbmul);       // exact integer
-              const float slo_t = __fmul_rn(c[2 + e2], cbmul);
+              const float shi_t = __fmul_rn(cc[2 * e2], cbmul);       // exact integer
+              const float slo_t = __fmul_rn(cc[2 * e2 + 1], cbmul);
               const float sf = __fadd_rn(__fmul_rn(2048.f, shi_t), slo_t);
-              okeys[rel + 4 * e2] = order_key(__fadd_rn(__fmul_rn(sf, unit), beta));
+              okeys[rel + 8 * e2] = order_key(__fadd_rn(__fmul_rn(sf, unit), beta));
             }
           }
         }
@@ -323,23 +443,29 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   }
   __syncthreads();
 
-  // ---------------- the chunk's top k: radix select on the order keys ----------------
+  // ---------------- the chunk's top k ----------------
   const int keff = min(K, n);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + L::SC_OFF);
-  int* st = misc + 2;  // st[0] prefix, st[1] mask, st[2] remaining, st[3] count
+  int* st = misc + 2;  // st[0] T, st[1] remaining, st[2] ties taken, st[3] bin / count, st[4] gather count
   float* cs = p.cand_score + (u * p.S + split) * K;
   int32_t* ci = p.cand_idx + (u * p.S + split) * K;
   if (keff > 0) {
-    radix_select(n, keff, [&](int i, uint32_t& key) { key = keys[i]; return true; }, hist, st);
+    select_kth(n, keff, [&](int i, uint32_t& key) { key = okeys[i]; return true; }, hist, list, red, st);
     const uint32_t T = static_cast<uint32_t>(st[0]);
     const int need_eq = st[2];
     const int n_gt = keff - need_eq;
+    __syncthreads();
     if (tid == 0) st[3] = 0;
     __syncthreads();
-    for (int i = tid; i < n; i += blockDim.x) {
-      const uint32_t key = keys[i];
-      if (key > T) {
-        const int pos = atomicAdd(st + 3, 1);
+    const int nround = (n + blockDim.x - 1) / blockDim.x * blockDim.x;
+    for (int i = tid; i < nround; i += blockDim.x) {
+      const uint32_t key = (i < n) ? okeys[i] : 0u;
+      const bool sel = (i < n) && key > T;
+      const uint32_t bal = __ballot_sync(0xffffffffu, sel);
+      int base = 0;
+      if (lane == 0 && bal) base = atomicAdd(st + 3, __popc(bal));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (sel) {
+        const int pos = base + __popc(bal & ((1u << lane) - 1u));
         cs[pos] = key_to_score(key);
         ci[pos] = static_cast<int32_t>(t_begin + i);
       }
@@ -348,7 +474,7 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
       int taken = 0;
       for (int base = 0; base < n && taken < need_eq; base += 32) {
         const int i = base + lane;
-        const bool eq = (i < n) && (keys[i] == T);
+        const bool eq = (i < n) && (okeys[i] == T);
         const uint32_t bal = __ballot_sync(0xffffffffu, eq);
         const int before = __popc(bal & ((1u << lane) - 1u));
         if (eq && taken + before < need_eq) {
@@ -372,44 +498,60 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
     const int last = (prev == static_cast<unsigned>(p.S - 1));
     if (last) atomicExch(p.counters + u, 0u);
     misc[1] = last;
-    st[3] = 0;
   }
   __syncthreads();
   if (!misc[1]) return;
   __threadfence();
   // Candidates as unique composite keys (order key, ~index): larger is better.
   const int NC = p.S * K;
-  uint32_t* khi = keys;                 // [NC] order keys, 0 for padding
-  uint32_t* klo = keys + kTopkMaxCand;  // [NC] ~index
+  uint32_t* khi = okeys;                // [NC] order keys, 0 for padding
+  uint32_t* klo = okeys + NC;           // [NC] ~index, 0 for padding
   const float* us = p.cand_score + u * p.S * K;
   const int32_t* ui = p.cand_idx + u * p.S * K;
+  int cnt = 0;
   for (int i = tid; i < NC; i += blockDim.x) {
     const int32_t idx = __ldcg(ui + i);
     const bool ok = idx >= 0;
     khi[i] = ok ? order_key(__ldcg(us + i)) : 0u;
     klo[i] = ok ? 0xFFFFFFFFu - static_cast<uint32_t>(idx) : 0u;
-    if (ok) atomicAdd(st + 3, 1);
+    cnt += ok;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if (lane == 0) red[warp] = static_cast<uint32_t>(cnt);
   __syncthreads();
-  const int nvalid = st[3];
+  int nvalid = 0;
+  for (int w = 0; w < NW + 1; ++w) nvalid += static_cast<int>(red[w]);
+  __syncthreads();
   const int kf = min(K, nvalid);
   uint32_t* whi = reinterpret_cast<uint32_t*>(smem);   // winners, in the (idle) stage area
   uint32_t* wlo = whi + kMaxTopk;
   if (kf > 0) {
-    // order keys first, then the index among keys equal to the k-th order key
-    radix_select(NC, kf, [&](int i, uint32_t& key) { key = khi[i]; return klo[i] != 0u; }, hist, st);
+    select_kth(NC, kf, [&](int i, uint32_t& key) { key = khi[i]; return klo[i] != 0u; }, hist, list, red, st);
     const uint32_t Thi = static_cast<uint32_t>(st[0]);
-    const int rem = st[2];
+    const int need = st[2];
     __syncthreads();
-    radix_select(NC, rem, [&](int i, uint32_t& key) { key = klo[i]; return klo[i] != 0u && khi[i] == Thi; },
-                 hist, st);
+    // the `need` largest ~index among the candidates whose order key is Thi
+    select_kth(NC, need, [&](int i, uint32_t& key) { key = klo[i]; return klo[i] != 0u && khi[i] == Thi; },
+               hist, list, red, st);
     const uint32_t Tlo = static_cast<uint32_t>(st[0]);
+    __syncthreads();
     if (tid == 0) st[3] = 0;
     __syncthreads();
-    for (int i = tid; i < NC; i += blockDim.x) {
-      const uint32_t h = khi[i], l = klo[i];
-      if (l != 0u && (h > Thi || (h == Thi && l >= Tlo))) {
-        const int pos = atomicAdd(st + 3, 1);
+    const int nround = (NC + blockDim.x - 1) / blockDim.x * blockDim.x;
+    for (int i = tid; i < nround; i += blockDim.x) {
+      uint32_t h = 0, l = 0;
+      if (i < NC) {
+        h = khi[i];
+        l = klo[i];
+      }
+      const bool win = l != 0u && (h > Thi || (h == Thi && l >= Tlo));
+      const uint32_t bal = __ballot_sync(0xffffffffu, win);
+      int base = 0;
+      if (lane == 0 && bal) base = atomicAdd(st + 3, __popc(bal));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (win) {
+        const int pos = base + __popc(bal & ((1u << lane) - 1u));
         whi[pos] = h;
         wlo[pos] = l;
       }
@@ -437,40 +579,103 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
 
 template <int MODE, int D>
 cudaError_t launch_t(const TopkParams& p, cudaStream_t s) {
-  constexpr int smem = TopkSmem<MODE, D>::TOTAL;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&topk_kernel<MODE, D>), smem);
+  const int smem = smem_bytes<MODE, D>(p.chunk, p.S, p.k);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&topk_kernel<MODE, D>), TopkSmem<MODE, D>::MAX_TOTAL);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.c.B) * p.c.Hkv * p.S;
   topk_kernel<MODE, D><<<static_cast<unsigned>(grid), NTHREADS, smem, s>>>(p);
   return cudaGetLastError();
 }
 
-// Resident CTAs per SM of one variant times the SM count, queried once per device.
+// CTAs per SM of one variant at `smem` bytes of dynamic shared memory, cached
+// per device in 1 KB steps (0 if unknown).
 template <int MODE, int D>
-int resident_ctas_t() {
+int per_sm_t(int smem) {
+  constexpr int kMaxDev = 64;
+  constexpr int kSteps = TopkSmem<MODE, D>::MAX_TOTAL / 1024 + 2;
+  static int cached[kMaxDev][kSteps] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  const int step = (smem + 1023) / 1024;
+  if (step >= kSteps) return 0;
+  if (cached[dev][step] > 0) return cached[dev][step];
+  if (set_smem_once(reinterpret_cast<const void*>(&topk_kernel<MODE, D>), TopkSmem<MODE, D>::MAX_TOTAL) != cudaSuccess)
+    return 0;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<MODE, D>, NTHREADS, step * 1024) !=
+      cudaSuccess)
+    return 0;
+  cached[dev][step] = per_sm;
+  return per_sm;
+}
+
+int sm_count() {
   constexpr int kMaxDev = 64;
   static int cached[kMaxDev] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
-  if (cached[dev] > 0) return cached[dev];
-  constexpr int smem = TopkSmem<MODE, D>::TOTAL;
-  if (set_smem_once(reinterpret_cast<const void*>(&topk_kernel<MODE, D>), smem) != cudaSuccess) return 0;
-  int per_sm = 0, sms = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<MODE, D>, NTHREADS, smem) != cudaSuccess)
-    return 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  cached[dev] = per_sm * sms;
+  if (cached[dev] == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = sms;
+  }
   return cached[dev];
+}
+
+long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
+
+// Split plan: over S from the fewest splits the chunk limit allows to the most
+// that the candidate limit and the chunk alignment allow, minimise
+// waves x (chunk + fixed per-CTA cost) + merge cost.  Chunks are multiples of
+// 4 x max(G, tile) tokens, so each consumer warp scores whole key groups.
+template <int MODE, int D>
+int plan_t(long long Lq, long long U, int G, int k, long long* chunk_out) {
+  const long long align = std::max<long long>(kChunkAlign, 4LL * std::max(G, Mode<MODE>::TT));
+  const long long s_lo = std::max(1LL, ceil_div_ll(Lq, kTopkMaxChunk));
+  const long long s_hi = std::max(s_lo, std::min(ceil_div_ll(Lq, align), static_cast<long long>(kTopkMaxCand / k)));
+  const int sms = sm_count();
+  long long best_s = 0, best_ch = 0;
+  double best_cost = 0.0;
+  for (long long S = s_lo; S <= s_hi; ++S) {
+    const long long ch = ceil_div_ll(ceil_div_ll(Lq, S), align) * align;
+    if (ch > kTopkMaxChunk && S < s_hi) continue;
+    const long long s_eff = ceil_div_ll(Lq, ch);
+    if (s_eff != S) continue;
+    const int per_sm = per_sm_t<MODE, D>(smem_bytes<MODE, D>(ch, static_cast<int>(S), k));
+    const long long slots = (per_sm > 0 && sms > 0) ? static_cast<long long>(per_sm) * sms : kTargetCtas;
+    const long long waves = ceil_div_ll(U * S, slots);
+    const double cost = static_cast<double>(waves) * static_cast<double>(ch + 1024) + 0.25 * static_cast<double>(S * k);
+    if (best_s == 0 || cost < best_cost) {
+      best_s = S;
+      best_ch = ch;
+      best_cost = cost;
+    }
+  }
+  if (best_s == 0) {  // the chunk limit alone
+    best_ch = std::min<long long>(kTopkMaxChunk, ceil_div_ll(ceil_div_ll(Lq, s_lo), kChunkAlign) * kChunkAlign);
+    best_s = ceil_div_ll(Lq, best_ch);
+  }
+  *chunk_out = best_ch;
+  return static_cast<int>(best_s);
 }
 
 }  // namespace
 
-int topk_resident_ctas(int mode, int D) {
+int topk_plan(int mode, int D, int G, long long Lq, long long U, int k, long long* chunk) {
+  if (Lq <= 0) {
+    *chunk = 0;
+    return 1;
+  }
   switch (mode) {
-    case KVQ_MODE_INT4: return D == 128 ? resident_ctas_t<KVQ_MODE_INT4, 128>() : resident_ctas_t<KVQ_MODE_INT4, 64>();
-    case KVQ_MODE_INT2: return D == 128 ? resident_ctas_t<KVQ_MODE_INT2, 128>() : resident_ctas_t<KVQ_MODE_INT2, 64>();
-    case KVQ_MODE_INT1: return D == 128 ? resident_ctas_t<KVQ_MODE_INT1, 128>() : resident_ctas_t<KVQ_MODE_INT1, 64>();
-    default: return 0;
+    case KVQ_MODE_INT4:
+      return D == 128 ? plan_t<KVQ_MODE_INT4, 128>(Lq, U, G, k, chunk) : plan_t<KVQ_MODE_INT4, 64>(Lq, U, G, k, chunk);
+    case KVQ_MODE_INT2:
+      return D == 128 ? plan_t<KVQ_MODE_INT2, 128>(Lq, U, G, k, chunk) : plan_t<KVQ_MODE_INT2, 64>(Lq, U, G, k, chunk);
+    case KVQ_MODE_INT1:
+      return D == 128 ? plan_t<KVQ_MODE_INT1, 128>(Lq, U, G, k, chunk) : plan_t<KVQ_MODE_INT1, 64>(Lq, U, G, k, chunk);
+    default:
+      *chunk = 0;
+      return 0;
   }
 }
 
