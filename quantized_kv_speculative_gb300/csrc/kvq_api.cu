@@ -232,11 +232,18 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const void* k_new, const void* 
     p.res_start = cache->residual_start;
     p.n = n_new;
     p.nflush = static_cast<int>(f);
+    if (f == 1) {
+      const long long first_new = std::max(r, f * G);
+      p.res_k_w = reinterpret_cast<uint16_t*>(base + cache->off_res_k);
+      p.res_v_w = reinterpret_cast<uint16_t*>(base + cache->off_res_v);
+      p.first_new = static_cast<int>(first_new);
+      p.res_count = static_cast<int>(T - first_new);
+    }
     if (launch_flush(p, s) != cudaSuccess) return KVQ_ERR_CUDA;
   }
   const long long first_new = std::max(r, f * G);
   const long long count = T - first_new;
-  if (count > 0) {
+  if (count > 0 && f != 1) {
     ResidualWriteParams w{};
     w.res_k = reinterpret_cast<uint16_t*>(base + cache->off_res_k);
     w.res_v = reinterpret_cast<uint16_t*>(base + cache->off_res_v);

@@ -59,9 +59,20 @@ struct TailSmem {
   static constexpr int TOTAL = OK_OFF + TC * 4;
 };
 
-// Target CTAs per SM: four with one weight n-tile (rows <= 4), three with two.
-template <int NT>
-constexpr int target_ctas() { return NT == 1 ? 4 : 3; }
+template <int MODE, int D, int NJ, int NT>
+struct Smem;
+
+// Target CTAs per SM: four with one weight n-tile (rows <= 4); with two n-tiles
+// three when their shared memory fits, else two (which also frees registers).
+template <int MODE, int D, int NJ, int NT>
+constexpr int target_ctas() {
+  if constexpr (NT == 1) {
+    return 4;
+  } else {
+    constexpr int need = Smem<MODE, D, NJ, NT>::MIN_TOTAL + 1024;
+    return 3 * need <= 228 * 1024 ? 3 : 2;
+  }
+}
 
 template <int MODE, int D, int NJ, int NT>
 struct Smem {
@@ -78,16 +89,20 @@ struct Smem {
   static constexpr int VSZ_OFF = KSZ_OFF + KSZ_BYTES;
   static constexpr int VSZ_BYTES = TT * 2 * NJ * 4;
   static constexpr int SLOT = VSZ_OFF + VSZ_BYTES;
-  static constexpr int FIXED = kMaxRows * D * 4 + (kMaxChunk / 32) * 4 + 8 * 16 * 8 + 1024;
+  static constexpr int WB_BYTES = NT == 1 ? NW * 16 * D : 0;     // staged weight fragments (one n-tile)
+  static constexpr int FIXED = kMaxRows * D * 4 + (kMaxChunk / 32) * 4 + 16 * 8 + WB_BYTES + NW * 48 + 272;
+  static constexpr int MIN_TOTAL = NW * 2 * SLOT + FIXED;
   // stage slots per warp: as many as fit (2..4) at the target CTAs per SM
-  static constexpr int SPW_FIT = (kSmemPerSm / target_ctas<NT>() - 1024 - FIXED) / (NW * SLOT);
+  static constexpr int SPW_FIT = (kSmemPerSm / target_ctas<MODE, D, NJ, NT>() - 1024 - FIXED) / (NW * SLOT);
   static constexpr int SPW = SPW_FIT < 2 ? 2 : (SPW_FIT > 4 ? 4 : SPW_FIT);
   static constexpr int NSLOT = NW * SPW;
   static constexpr int QT_OFF = NSLOT * SLOT;                 // scaled queries q~ [8][D] f32
   static constexpr int BM_OFF = QT_OFF + kMaxRows * D * 4;    // selection bitmap
   static constexpr int BM_WORDS = kMaxChunk / 32;
   static constexpr int BAR_OFF = BM_OFF + BM_WORDS * 4;
-  static constexpr int RING_END = BAR_OFF + NSLOT * 8;
+  static constexpr int WB_OFF = (BAR_OFF + NSLOT * 8 + 15) / 16 * 16;   // per warp: staged weight fragments
+  static constexpr int SRC_OFF = WB_OFF + WB_BYTES;                 // [8 cols][4 chunks][D/8 pairs] u32 per warp
+  static constexpr int RING_END = SRC_OFF + NW * 6 * 8 + 16;         // per warp: copy source pointers; max |q~|
   static constexpr int COMBINE_END = (2 * kMaxCombine * 8 + 16) * 4;
   // the ticket flag sits after whichever layout (ring, tail CTA, combine) is largest
   static constexpr int MISC_OFF0 = RING_END > TailSmem<D>::TOTAL ? RING_END : TailSmem<D>::TOTAL;
@@ -403,10 +418,11 @@ __device__ __forceinline__ float pow2i(int e) {   // 2^e, -126 <= e <= 127
   return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 
-// Four CTAs per SM when one weight n-tile serves all rows (rows <= 4); the
-// eight-row variant keeps two n-tiles of weights and two sets of P fragments.
+// Four CTAs per SM when one weight n-tile serves all rows (rows <= 4); two for
+// the eight-row variant, which keeps two n-tiles of weights and two sets of P
+// fragments.
 template <int MODE, int D, int NJ, int NT>
-__global__ void __launch_bounds__(NTHREADS, target_ctas<NT>()) attend_kernel(AttendParams p) {
+__global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) attend_kernel(AttendParams p) {
   using M = Mode<MODE>;
   using RW = Rows<MODE, D>;
   using L = Smem<MODE, D, NJ, NT>;
@@ -453,27 +469,47 @@ __global__ void __launch_bounds__(NTHREADS, target_ctas<NT>()) attend_kernel(Att
 
   // Each warp streams its own tiles: lane 0 puts tile j into slot j % SPW of
   // the warp's ring with 1-D bulk copies that complete on the slot's mbarrier.
-  const uint64_t pol = policy_evict_first();
+  // Source pointers of this warp's first tile; tile j adds j tiles.  Chunk
+  // starts are multiples of kChunkAlign, so of G, and offsets inside a chunk
+  // fit in 32 bits.
+  // (kept in shared memory: only lane 0 of the warp issues copies)
+  const int rel0 = my_first * M::TT;                       // first token of the run, chunk-relative
+  const uint8_t** src_tab = reinterpret_cast<const uint8_t**>(smem + L::SRC_OFF) + warp * 6;
+  if (lane == 0) {
+    const long long tok_first = u_tok + t_begin + rel0;
+#pragma unroll
+    for (int pl = 0; pl < M::NP; ++pl) {
+      src_tab[pl] = p.c.kplane[pl] + tok_first * RW::KROW;
+      src_tab[2 + pl] = p.c.vplane[pl] + (tok_first / 32) * D * RW::VROW;
+    }
+    src_tab[4] = reinterpret_cast<const uint8_t*>(p.c.vsz + tok_first * 2 * NJ);
+    src_tab[5] = reinterpret_cast<const uint8_t*>(p.c.ksz + (u * (p.c.C / G) + (t_begin + rel0) / G) * 2 * D);
+  }
+  // A tile loads key scales only when it starts a key group (or is the run's
+  // first tile): the group's weights are derived from that tile's copy.
   auto issue = [&](int j) {
     const int slot = warp * SPW + (j % SPW);
-    const long long t0 = t_begin + static_cast<long long>(my_first + j) * M::TT;
-    const int nt = static_cast<int>(min(static_cast<long long>(M::TT), t_end - t0));
-    const long long g_first = t0 / G, g_last = (t0 + nt - 1) / G;
+    const int rel = rel0 + j * M::TT;                        // chunk-relative first token
+    const int nt = min(M::TT, ntok_chunk - rel);
+    const bool new_grp = (j == 0) || (M::TT > G) || (rel % G == 0);
     const uint32_t kb = nt * RW::KROW, vb = (nt / 32) * D * RW::VROW;
-    const uint32_t kszb = static_cast<uint32_t>(g_last - g_first + 1) * 2 * D * 4;
+    const uint32_t kszb = new_grp ? static_cast<uint32_t>((nt + G - 1) / G) * 2 * D * 4 : 0u;
     const uint32_t vszb = nt * 2 * NJ * 4;
     uint8_t* sbase = smem + slot * L::SLOT;
+    const uint64_t pol = policy_evict_first();
     // order this warp's earlier reads of the slot before the async-proxy writes
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive_expect_tx(full + slot, M::NP * (kb + vb) + kszb + vszb);
 #pragma unroll
     for (int pl = 0; pl < M::NP; ++pl) {
-      bulk_g2s(sbase + L::K_OFF + pl * L::KPLANE, p.c.kplane[pl] + (u_tok + t0) * RW::KROW, kb, full + slot, pol);
-      bulk_g2s(sbase + L::V_OFF + pl * L::VPLANE, p.c.vplane[pl] + ((u_tok + t0) / 32) * D * RW::VROW, vb,
+      bulk_g2s(sbase + L::K_OFF + pl * L::KPLANE, src_tab[pl] + j * (M::TT * RW::KROW), kb, full + slot, pol);
+      bulk_g2s(sbase + L::V_OFF + pl * L::VPLANE, src_tab[2 + pl] + j * ((M::TT / 32) * D * RW::VROW), vb,
                full + slot, pol);
     }
-    bulk_g2s(sbase + L::KSZ_OFF, p.c.ksz + (u * (p.c.C / G) + g_first) * 2 * D, kszb, full + slot, pol);
-    bulk_g2s(sbase + L::VSZ_OFF, p.c.vsz + (u_tok + t0) * 2 * NJ, vszb, full + slot, pol);
+    if (new_grp)
+      bulk_g2s(sbase + L::KSZ_OFF, src_tab[5] + ((rel0 + j * M::TT) / G - rel0 / G) * (2 * D * 4), kszb,
+               full + slot, pol);
+    bulk_g2s(sbase + L::VSZ_OFF, src_tab[4] + j * (M::TT * 2 * NJ * 4), vszb, full + slot, pol);
   };
 
   // ---- setup: each warp's barriers first, so its first tiles load at once ----
@@ -500,6 +536,13 @@ __global__ void __launch_bounds__(NTHREADS, target_ctas<NT>()) attend_kernel(Att
     qt[e] = v;
   }
   __syncthreads();
+  if (warp == 0) {  // max |q~| over the valid rows, for the weight normalizer
+    float qm = 0.f;
+    for (int e = lane; e < R * D; e += 32) qm = fmaxf(qm, fabsf(qt[e]));
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o2));
+    if (lane == 0) *reinterpret_cast<float*>(smem + L::SRC_OFF + NW * 48) = qm;
+  }
   if (has_sel) {
     for (int j = tid; j < p.top_k; j += blockDim.x) {
       const long long idx = p.sel_idx[u * p.top_k + j];
@@ -508,8 +551,8 @@ __global__ void __launch_bounds__(NTHREADS, target_ctas<NT>()) attend_kernel(Att
         atomicOr(bitmap + rel / 32, 1u << (rel % 32));
       }
     }
-    __syncthreads();
   }
+  __syncthreads();
 
   {
     // ---------------- consumers ----------------
@@ -530,11 +573,6 @@ __global__ void __launch_bounds__(NTHREADS, target_ctas<NT>()) attend_kernel(Att
       tokB[s] = tokA[s] + (MODE == KVQ_MODE_INT8 ? 2 : 4);
       vinv[s] = 1.0f / vx_mult<MODE>(i);
     }
-    // max |q~| over the valid rows, for the weight normalizer
-    float qmax = 0.f;
-    for (int e = lane; e < R * D; e += 32) qmax = fmaxf(qmax, fabsf(qt[e]));
-#pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, o2));
 
     uint32_t W[NT][NPK];                 // weights: this lane's B column part, per key pair
     float cinit[NT];                     // accumulator start (correction x 2^e) for row 4nt + q
@@ -554,7 +592,8 @@ __global__ void __launch_bounds__(NTHREADS, target_ctas<NT>()) attend_kernel(Att
       for (int pp = 0; pp < NPK; ++pp) W[nt][pp] = 0u;
     }
     float evs = 0.f;                     // value normalizer 2^ev (0: not chosen yet)
-    long long cur_grp = -1;
+    int cur_grp = -1;
+
 
     for (int j = 0; j < my_tiles; ++j) {
       const int ti = my_first + j;
@@ -566,66 +605,136 @@ __global__ void __launch_bounds__(NTHREADS, target_ctas<NT>()) attend_kernel(Att
         break;
       }
       if (*reinterpret_cast<volatile int*>(sh_abort)) break;
-      const long long t0 = t_begin + static_cast<long long>(ti) * M::TT;
-      const int nt_tok = static_cast<int>(min(static_cast<long long>(M::TT), t_end - t0));
-      const long long g_first = t0 / G;
+      const int rel = ti * M::TT;                            // chunk-relative first token
+      const int nt_tok = min(M::TT, ntok_chunk - rel);
+      const int g_first = rel / G;
       const uint8_t* sbase = smem + slot * L::SLOT;
       const float* ksz = reinterpret_cast<const float*>(sbase + L::KSZ_OFF);
       const float* vsz = reinterpret_cast<const float*>(sbase + L::VSZ_OFF);
 
       for (int sl = 0; sl < nt_tok / 32; ++sl) {
-        const long long tok0 = t0 + 32 * sl;
-        const long long grp = tok0 / G;
+        const int tok0 = rel + 32 * sl;
+        const int grp = tok0 / G;
         if (grp != cur_grp) {
-          // ---- folded key weights of this group ----
+          // ---- folded key weights of this group, derived once per warp ----
           // w_c = q~_c * MULT * s_c * kx_weight, scaled by 2^e so that the
           // largest possible |w| sits near 2^13, split into f16 high + low
-          // parts.  The accumulator starts at 2^e sum_c q~_c z_c minus the
-          // encoding's offset times sum_c (hi + lo)_c.
+          // parts.  Lanes split the (row, channel pair) items of the rows in
+          // use (lpr lanes per row), stage the B fragments in the warp's
+          // weight buffer, then each lane loads its column.  The accumulator
+          // starts at 2^e sum_c q~_c z_c minus the encoding's offset times
+          // sum_c w_c.
           cur_grp = grp;
           const float* ks = ksz + (grp - g_first) * 2 * D;
           const float* kz = ks + D;
-          float sv[D / 4];
-#pragma unroll
-          for (int c4 = 0; c4 < D / 16; ++c4) {
-            const float4 v4 = *reinterpret_cast<const float4*>(ks + qbase + 4 * c4);
-            sv[4 * c4] = v4.x; sv[4 * c4 + 1] = v4.y; sv[4 * c4 + 2] = v4.z; sv[4 * c4 + 3] = v4.w;
-          }
-          float smax = 0.f;
-#pragma unroll
-          for (int c = 0; c < D / 4; ++c) smax = fmaxf(smax, sv[c]);
-          smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1));
-          smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 2));
+          // rows in use rounded up to a power of two, lpr lanes per row
+          const int rpow = R <= 1 ? 1 : (R <= 2 ? 2 : (R <= 4 ? 4 : 8));
+          const int lpr = 32 / rpow, wrow = lane / lpr, wsub = lane % lpr;
+          uint32_t* wb = reinterpret_cast<uint32_t*>(smem + L::WB_OFF) + warp * (4 * D);
+          (void)wb; (void)wrow; (void)wsub;
+          const float qmax = *reinterpret_cast<const float*>(smem + L::SRC_OFF + NW * 48);
+          constexpr int PPR = D / 2;           // channel pairs per row
           constexpr float KW = MULT * kx_weight<MODE>();
-          const float bound = qmax * smax * KW;
-          const int e = (bound > 0.f) ? max(-100, min(100, 13 - exp2_floor(bound))) : 0;
-          const float E2 = pow2i(e);
-          kscale = pow2i(-e);
-          const float f = E2 * KW;
+          float wsum = 0.f, zsum = 0.f;
+          float kscale_new, E2;
+          if constexpr (NT == 2) {
+            // eight rows: each lane derives its own B fragments (column g of both
+            // n-tiles for channel chunk q); the high-part lane and the low-part
+            // lane of a row both compute the row's weights
+            const float* ksc = ks + q * (D / 4);
+            const float* kzc = kz + q * (D / 4);
+            float kv[D / 4];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const float* qr = qt + (4 * nt + (g >> 1)) * D + qbase;
-            float wsum = 0.f, zsum = 0.f;
+            for (int c4 = 0; c4 < D / 16; ++c4) {
+              const float4 a4 = *reinterpret_cast<const float4*>(ksc + 4 * c4);
+              kv[4 * c4] = a4.x; kv[4 * c4 + 1] = a4.y; kv[4 * c4 + 2] = a4.z; kv[4 * c4 + 3] = a4.w;
+            }
+            float smax = 0.f;
 #pragma unroll
-            for (int pp = 0; pp < NPK; ++pp) {
-              const int c0 = kx_chan<MODE, D>(pp, 0), c1 = kx_chan<MODE, D>(pp, 1);
+            for (int c = 0; c < D / 4; ++c) smax = fmaxf(smax, kv[c]);
+            smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1));
+            smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 2));
+            const float bound = qmax * smax * KW;
+            const int e = (bound > 0.f) ? max(-100, min(100, 13 - exp2_floor(bound))) : 0;
+            E2 = pow2i(e);
+            kscale_new = pow2i(-e);
+            const float f = E2 * KW;
+#pragma unroll
+            for (int c = 0; c < D / 4; ++c) kv[c] *= f;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const float* qr = qt + (4 * nt + (g >> 1)) * D + q * (D / 4);
+              float ws = 0.f, zs = 0.f;
+#pragma unroll
+              for (int c4 = 0; c4 < D / 16; ++c4) {
+                const float4 q4 = *reinterpret_cast<const float4*>(qr + 4 * c4);
+                const float4 z4 = *reinterpret_cast<const float4*>(kzc + 4 * c4);
+                zs = fmaf(q4.x, z4.x, fmaf(q4.y, z4.y, fmaf(q4.z, z4.z, fmaf(q4.w, z4.w, zs))));
+              }
+#pragma unroll
+              for (int pp = 0; pp < D / 8; ++pp) {
+                const int c0 = kx_chan<MODE, D>(pp, 0), c1 = kx_chan<MODE, D>(pp, 1);
+                const float w0 = qr[c0] * kv[c0], w1 = qr[c1] * kv[c1];
+                const uint32_t hi = pack_half2(w0, w1);
+                const float2 hf = unpack_half2(hi);
+                const uint32_t lo = pack_half2(w0 - hf.x, w1 - hf.y);
+                W[nt][pp] = par ? lo : hi;
+                ws += w0 + w1;
+              }
+              float cwn = fmaf(zs, E2, -kx_offset<MODE>() * ws);
+              cwn += __shfl_xor_sync(0xffffffffu, cwn, 1);
+              cwn += __shfl_xor_sync(0xffffffffu, cwn, 2);
+              // this lane's C rows belong to row 4nt + q, whose weights lanes g = 2q hold
+              cinit[nt] = __shfl_sync(0xffffffffu, cwn, 8 * q);
+            }
+          } else {
+            float smax = 0.f;
+            for (int it = wsub; it < PPR; it += lpr) {
+              const int qq = it / (D / 8), pp = it % (D / 8);
+              const int c0 = qq * (D / 4) + kx_chan<MODE, D>(pp, 0), c1 = qq * (D / 4) + kx_chan<MODE, D>(pp, 1);
+              smax = fmaxf(smax, fmaxf(ks[c0], ks[c1]));
+            }
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o2));
+            const float bound = qmax * smax * KW;
+            const int e = (bound > 0.f) ? max(-100, min(100, 13 - exp2_floor(bound))) : 0;
+            E2 = pow2i(e);
+            kscale_new = pow2i(-e);
+            const float f = E2 * KW;
+            const float* qr = qt + wrow * D;
+            const int col = 2 * (wrow & 3), ntw = wrow >> 2;
+            for (int it = wsub; it < PPR; it += lpr) {
+              const int qq = it / (D / 8), pp = it % (D / 8);
+              const int c0 = qq * (D / 4) + kx_chan<MODE, D>(pp, 0), c1 = qq * (D / 4) + kx_chan<MODE, D>(pp, 1);
               const float q0 = qr[c0], q1 = qr[c1];
-              const float w0 = q0 * sv[c0] * f, w1 = q1 * sv[c1] * f;
+              const float w0 = q0 * ks[c0] * f, w1 = q1 * ks[c1] * f;
               const uint32_t hi = pack_half2(w0, w1);
               const float2 hf = unpack_half2(hi);
               const uint32_t lo = pack_half2(w0 - hf.x, w1 - hf.y);
-              W[nt][pp] = par ? lo : hi;
-              if constexpr (kx_offset<MODE>() != 0.f) {
-                const float2 lf = unpack_half2(lo);
-                wsum += (hf.x + lf.x) + (hf.y + lf.y);
-              }
-              zsum = fmaf(q0, kz[qbase + c0], fmaf(q1, kz[qbase + c1], zsum));
+              wb[((ntw * 8 + col) * 4 + qq) * (D / 8) + pp] = hi;
+              wb[((ntw * 8 + col + 1) * 4 + qq) * (D / 8) + pp] = lo;
+              wsum += w0 + w1;
+              zsum = fmaf(q0, kz[c0], fmaf(q1, kz[c1], zsum));
             }
-            float cw = fmaf(zsum, E2, -kx_offset<MODE>() * wsum);
-            cw += __shfl_xor_sync(0xffffffffu, cw, 1);
-            cw += __shfl_xor_sync(0xffffffffu, cw, 2);
-            // this lane's C rows belong to row 4nt + q, whose weights lanes g = 2q hold
-            cinit[nt] = __shfl_sync(0xffffffffu, cw, 8 * q);
+          }
+          kscale = kscale_new;
+          if constexpr (NT == 1) {
+            for (int o2 = 1; o2 < lpr; o2 <<= 1) {
+              wsum += __shfl_xor_sync(0xffffffffu, wsum, o2);
+              zsum += __shfl_xor_sync(0xffffffffu, zsum, o2);
+            }
+            const float cw = fmaf(zsum, E2, -kx_offset<MODE>() * wsum);
+            __syncwarp();
+            const int row_b = g >> 1, row_c = q;
+            const uint4* src = reinterpret_cast<const uint4*>(wb + (g * 4 + q) * (D / 8));
+#pragma unroll
+            for (int v = 0; v < D / 32; ++v) {
+              const uint4 x4 = (row_b < rpow) ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+              W[0][4 * v] = x4.x; W[0][4 * v + 1] = x4.y; W[0][4 * v + 2] = x4.z; W[0][4 * v + 3] = x4.w;
+            }
+            const float cv = __shfl_sync(0xffffffffu, cw, min(row_c, rpow - 1) * lpr);
+            cinit[0] = (row_c < rpow) ? cv : 0.f;
+            __syncwarp();
           }
         }
         const uint8_t* kslab = sbase + L::K_OFF + (32 * sl) * RW::KROW + q * RW::KCHUNK;
@@ -656,7 +765,7 @@ __global__ void __launch_bounds__(NTHREADS, target_ctas<NT>()) attend_kernel(Att
           }
         }
         if (has_sel) {
-          const uint32_t bm = bitmap[static_cast<int>(tok0 - t_begin) / 32];
+          const uint32_t bm = bitmap[tok0 / 32];
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
             const bool ma = (bm >> tokA[s]) & 1u, mb = (bm >> tokB[s]) & 1u;

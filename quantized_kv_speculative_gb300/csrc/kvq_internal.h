@@ -90,6 +90,11 @@ struct FlushParams {
   long long C, Lq;          // Lq before this call
   int r, res_start, n;      // residual state before this call, tokens in this call
   int nflush;               // groups quantized by this launch
+  // new tokens written into the residual buffer by the same launch (only
+  // with nflush == 1, after each CTA has read its head's old slots)
+  uint16_t* res_k_w;
+  uint16_t* res_v_w;
+  int first_new, res_count;
 };
 
 struct ResidualWriteParams {

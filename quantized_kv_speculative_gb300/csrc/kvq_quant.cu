@@ -18,7 +18,7 @@
 namespace kvq {
 namespace {
 
-constexpr int kFlushThreads = 256;
+constexpr int kFlushThreads = 512;
 
 __device__ __forceinline__ uint32_t quant_code(float x, float mn, float inv, float levels) {
   float t = rintf(__fmul_rn(__fsub_rn(x, mn), inv));
@@ -88,6 +88,22 @@ __global__ void __launch_bounds__(kFlushThreads) flush_kernel(FlushParams p) {
     }
   }
   __syncthreads();
+  // A single flushed group reads this head's old slots only in the gather
+  // above, so the new tokens that stay in the buffer can be written now.
+  if (p.res_count > 0) {
+    const int nv = p.res_count * vec_per_tok;
+    for (int e = tid; e < 2 * nv; e += kFlushThreads) {
+      const int kv = e >= nv, e2 = kv ? e - nv : e;
+      const int j = e2 / vec_per_tok, c = e2 % vec_per_tok;
+      const int pos = p.first_new + j;
+      const int slot = (p.res_start + pos) % (2 * G);
+      const long long src = (u * p.n + (pos - p.r)) * D;
+      const long long dst = (u * 2 * G + slot) * D;
+      const uint16_t* from = kv ? p.v_new : p.k_new;
+      uint16_t* to = kv ? p.res_v_w : p.res_k_w;
+      reinterpret_cast<uint4*>(to + dst)[c] = reinterpret_cast<const uint4*>(from + src)[c];
+    }
+  }
 
   constexpr int BITS = FMT;  // 8, 2 or 1
   const float levels = static_cast<float>((1 << BITS) - 1);
@@ -113,15 +129,17 @@ __global__ void __launch_bounds__(kFlushThreads) flush_kernel(FlushParams p) {
     part[kFlushThreads * 2 + st * D + 2 * cp + 1] = mx1;
   }
   // ---- value statistics: per token over each block of G channels ----
-  // item = (token i, block jv), D items; kFlushThreads / D lanes per item (adjacent lanes)
+  // item = (token i, block jv), D items; `per` adjacent lanes per item, each
+  // over a multiple of 8 channels
   {
-    const int per = kFlushThreads / D;          // 2 (D=128) or 4 (D=64)
+    const int per = min(kFlushThreads / D, G / 8);
     const int item = tid / per, sub = tid % per;
     const int i = item / NJ, jv = item % NJ;
-    const int cw = G / per;                     // channels per lane: 16..64, a multiple of 8
-    const uint16_t* src = Vs + i * D + jv * G + sub * cw;
+    const int cw = G / per;
+    const bool active = item < D;
+    const uint16_t* src = Vs + (active ? i * D + jv * G + sub * cw : 0);
     float mn = pinf, mx = -pinf;
-    for (int c = 0; c < cw; c += 8) {
+    for (int c = 0; active && c < cw; c += 8) {
       const uint4 w = *reinterpret_cast<const uint4*>(src + c);
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -135,7 +153,7 @@ __global__ void __launch_bounds__(kFlushThreads) flush_kernel(FlushParams p) {
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
-    if (sub == 0) {
+    if (active && sub == 0) {
       mn = __fadd_rn(mn, 0.0f);
       mx = __fadd_rn(mx, 0.0f);
       float scale, inv;
