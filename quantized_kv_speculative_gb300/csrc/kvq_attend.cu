@@ -24,15 +24,16 @@
 //    then resets the ticket.  No CTA ever waits on another.
 //
 // Folding (no per-element dequant FMA).  A key code c reads as the f16 value
-// E = off + c / kw (INT8: off = 0, kw = 1; INT4/2/1: off = 1, kw = 2^b), so
+// E = off + c / kw (INT8: off = 1024, kw = 1; INT4/2/1: off = 1, kw = 2^b), so
 // with q~ = q * sm_scale * log2(e), step s (MULT x scale) and zero z per group
 // and channel:
 //   logit2 = sum_d q~_d (c s + z) = sum_d w_d E_d + (sum_d q~_d z_d - off sum_d w_d),
 // with w_d = q~_d s_d kw; the bracket starts the accumulator.  Value codes read
-// as the exact f16 values m c (m a power of two set by the code's bit position;
-// the encoding's offset of 1024 is subtracted exactly), so the long P.V
-// accumulation carries no offset:
-//   o = sum_t p_t (c s + z) = sum_t P'_t (m c) + sum_t p_t z_t,  P'_t = p_t s_t / m_t.
+// as 1024 + m c (m a power of two set by the code's bit position); each slab's
+// P.V accumulator starts at -1024 sum_t P'_t, computed by one MMA with a
+// constant A operand, so the running output never carries the offset:
+//   o = sum_t p_t (c s + z) = sum_t P'_t (1024 + m c) - 1024 sum_t P'_t + sum_t p_t z_t,
+// with P'_t = p_t s_t / m_t.
 #include "kvq_modes.cuh"
 
 namespace kvq {
@@ -41,23 +42,6 @@ namespace {
 constexpr int NW = 4;                  // warps per CTA; each streams and consumes its own tiles
 constexpr int NTHREADS = NW * 32;
 constexpr int kSmemPerSm = 228 * 1024;
-constexpr float kLog2e = 1.4426950408889634f;
-
-// Tail-CTA shared layout (overlays the slot area of the same dynamic buffer).
-// K and V rows of one 64-token chunk are staged with a padded row stride so
-// that lanes reading different rows hit different banks.
-template <int D>
-struct TailSmem {
-  static constexpr int TC = 32;                               // tokens per chunk
-  static constexpr int ROW = D * 2 + 16;                      // padded bf16 row, bytes
-  static constexpr int QT_OFF = 0;                            // q~ [8][D] f32
-  static constexpr int K_OFF = QT_OFF + kMaxRows * D * 4;     // [TC][ROW]
-  static constexpr int V_OFF = K_OFF + TC * ROW;              // [TC][ROW]
-  static constexpr int LG_OFF = V_OFF + TC * ROW;             // logits / p [8][TC]
-  static constexpr int ST_OFF = LG_OFF + kMaxRows * TC * 4;   // m[8], l[8], alpha[8]
-  static constexpr int OK_OFF = ST_OFF + 3 * kMaxRows * 4;    // per-token flags [TC]
-  static constexpr int TOTAL = OK_OFF + TC * 4;
-};
 
 template <int MODE, int D, int NJ, int NT>
 struct Smem;
@@ -94,7 +78,13 @@ struct Smem {
   static constexpr int MIN_TOTAL = NW * 2 * SLOT + FIXED;
   // stage slots per warp: as many as fit (2..4) at the target CTAs per SM
   static constexpr int SPW_FIT = (kSmemPerSm / target_ctas<MODE, D, NJ, NT>() - 1024 - FIXED) / (NW * SLOT);
-  static constexpr int SPW = SPW_FIT < 2 ? 2 : (SPW_FIT > 4 ? 4 : SPW_FIT);
+  static constexpr int SPW_BASE = SPW_FIT < 2 ? 2 : (SPW_FIT > 4 ? 4 : SPW_FIT);
+  // the slot area is reused for the merge scratch: 2 NW entries (the warps'
+  // quantized runs, then the warps' shares of the bf16 tail)
+  static constexpr int NENT = 2 * NW;
+  static constexpr int SCRATCH_NEED = NENT * 8 * 4 * 7 + NENT * 8 * D * 4;
+  static constexpr int SPW_SCR = (SCRATCH_NEED + NW * SLOT - 1) / (NW * SLOT);
+  static constexpr int SPW = SPW_BASE > SPW_SCR ? SPW_BASE : SPW_SCR;
   static constexpr int NSLOT = NW * SPW;
   static constexpr int QT_OFF = NSLOT * SLOT;                 // scaled queries q~ [8][D] f32
   static constexpr int BM_OFF = QT_OFF + kMaxRows * D * 4;    // selection bitmap
@@ -102,20 +92,19 @@ struct Smem {
   static constexpr int BAR_OFF = BM_OFF + BM_WORDS * 4;
   static constexpr int WB_OFF = (BAR_OFF + NSLOT * 8 + 15) / 16 * 16;   // per warp: staged weight fragments
   static constexpr int SRC_OFF = WB_OFF + WB_BYTES;                 // [8 cols][4 chunks][D/8 pairs] u32 per warp
-  static constexpr int RING_END = SRC_OFF + NW * 6 * 8 + 16;         // per warp: copy source pointers; max |q~|
+  static constexpr int RING_END = SRC_OFF + NW * 6 * 8 + NW * 4;     // per warp: copy source pointers; max |q~|
   static constexpr int COMBINE_END = (2 * kMaxCombine * 8 + 16) * 4;
-  // the ticket flag sits after whichever layout (ring, tail CTA, combine) is largest
-  static constexpr int MISC_OFF0 = RING_END > TailSmem<D>::TOTAL ? RING_END : TailSmem<D>::TOTAL;
-  static constexpr int MISC_OFF = (MISC_OFF0 > COMBINE_END ? MISC_OFF0 : COMBINE_END + 15) / 16 * 16;
+  // the ticket flag sits after whichever layout (ring, combine) is largest
+  static constexpr int MISC_OFF = (RING_END > COMBINE_END ? RING_END + 15 : COMBINE_END + 15) / 16 * 16;
   static constexpr int TOTAL = MISC_OFF + 64;
-  // warp-merge scratch (after the pipeline drains), inside the slot area
-  static constexpr int WM_OFF = 0;                            // [NW][8] running max
-  static constexpr int WL_OFF = WM_OFF + NW * 8 * 4;          // [NW][8] running sum
-  static constexpr int WC_OFF = WL_OFF + NW * 8 * 4;          // [NW][8][NJ] value zero-point terms
-  static constexpr int WO_OFF = WC_OFF + NW * 8 * 4 * 4;      // [NW][8][D] output sums
-  static constexpr int SCRATCH = WO_OFF + NW * 8 * D * 4;
-  static_assert(SCRATCH <= NSLOT * SLOT, "merge scratch must fit in the slot area");
-  static_assert(TailSmem<D>::TOTAL <= MISC_OFF, "the tail layout must not reach the ticket flag");
+  // merge scratch (after the pipeline drains), inside the slot area
+  static constexpr int WM_OFF = 0;                            // [NENT][8] running max
+  static constexpr int WL_OFF = WM_OFF + NENT * 8 * 4;        // [NENT][8] running sum
+  static constexpr int WC_OFF = WL_OFF + NENT * 8 * 4;        // [NENT][8][4] value zero-point terms
+  static constexpr int FAC_OFF = WC_OFF + NENT * 8 * 4 * 4;   // [NENT][8] entry factors 2^(m_w - M)
+  static constexpr int WO_OFF = FAC_OFF + NENT * 8 * 4;       // [NENT][8][D] output sums
+  static constexpr int SCRATCH = WO_OFF + NENT * 8 * D * 4;
+  static_assert(SCRATCH <= NSLOT * SLOT, "the merge scratch must fit in the slot area");
   static_assert((2 * kMaxCombine * 8 + 16) * 4 <= MISC_OFF, "the combine scratch must not reach the ticket flag");
   static_assert(SLOT % 16 == 0, "slots must stay 16-byte aligned");
 };
@@ -126,6 +115,38 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Scaled queries q~ = q * sm_scale * log2(e) of unit (b, kvh) into qt [8][D]
+// (rows >= R zero): one 16-byte load of 8 channels per thread, all in flight
+// at once.  Returns the thread's max |q~|.
+template <int D>
+__device__ __forceinline__ float fill_qt(const AttendParams& p, int b, int kvh, float* qt) {
+  constexpr int V8 = D / 8;
+  float qm = 0.f;
+  for (int e = threadIdx.x; e < kMaxRows * V8; e += NTHREADS) {
+    const int rho = e / V8, c = e % V8;
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = 0.f;
+    if (rho < p.R) {
+      const int i = rho / p.HG, hh = rho % p.HG;
+      const long long qrow = ((static_cast<long long>(b) * p.gamma + i) * p.Hq + kvh * p.HG + hh) * D;
+      const uint4 w = *reinterpret_cast<const uint4*>(p.q + qrow + 8 * c);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        v[2 * k] = __uint_as_float(ww[k] << 16) * p.qscale;
+        v[2 * k + 1] = __uint_as_float(ww[k] & 0xFFFF0000u) * p.qscale;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) qm = fmaxf(qm, fabsf(v[k]));
+    }
+    float4* dst = reinterpret_cast<float4*>(qt + rho * D + 8 * c);
+    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+  return qm;
 }
 
 // ------------------------------------------------------------------------------
@@ -217,193 +238,223 @@ __device__ void ticket_and_combine(const AttendParams& p, long long u, int* sh_f
 }
 
 // ------------------------------------------------------------------------------
-// Tail CTAs: residual bf16 tokens + causal pending tokens + selected 16-bit
-// tokens, fp32 on CUDA cores.  The tail of one (b, kv head) is split over
-// S_t CTAs.  Each stages 64-token chunks of K and V rows in shared memory (all
-// loads in flight), then computes logits (thread <-> (row, token)), an online
-// softmax, and P.V (thread <-> channel) from shared memory.
+// The bf16 tail: the residual buffer, then the pending speculative tokens
+// (causal among themselves), then the selected 16-bit tokens.
 // ------------------------------------------------------------------------------
+// K / V rows of tail token t of unit u; returns its visibility: -1 always
+// visible, >= 0 the pending index, -2 absent (a selected slot without a token).
 template <int D>
-__device__ void tail_partial(const AttendParams& p, long long u, int tsplit, uint8_t* smem) {
-  using TS = TailSmem<D>;
-  float* qt = reinterpret_cast<float*>(smem + TS::QT_OFF);
-  uint8_t* ks = smem + TS::K_OFF;
-  uint8_t* vs = smem + TS::V_OFF;
-  float* lg = reinterpret_cast<float*>(smem + TS::LG_OFF);
-  float* st_m = reinterpret_cast<float*>(smem + TS::ST_OFF);
-  float* st_l = st_m + kMaxRows;
-  float* st_a = st_l + kMaxRows;
-  int* tok_pend = reinterpret_cast<int*>(smem + TS::OK_OFF);   // -2 absent, -1 always visible, else pending index
-  const int tid = threadIdx.x;
+__device__ __forceinline__ int tail_row(const AttendParams& p, long long u, int t, const uint16_t*& kp,
+                                        const uint16_t*& vp) {
+  if (t < p.c.r) {
+    const int slot = (p.c.res_start + t) % (2 * p.c.G);
+    const long long off = (u * 2 * p.c.G + slot) * D;
+    kp = p.c.res_k + off;
+    vp = p.c.res_v + off;
+    return -1;
+  }
+  t -= p.c.r;
+  if (t < p.P) {
+    const long long off = (u * p.P + t) * D;
+    kp = p.pend_k + off;
+    vp = p.pend_v + off;
+    return t;
+  }
+  t -= p.P;
+  const int idx = p.sel_idx[u * p.top_k + t];
+  if (idx >= 0 && idx < p.c.Lq) {
+    const long long off = (u * p.top_k + t) * D;
+    kp = p.sel_k + off;
+    vp = p.sel_v + off;
+    return -1;
+  }
+  kp = vp = nullptr;
+  return -2;
+}
+
+// Tail tokens [t_lo, t_hi) of unit u on tensor cores (bf16 in, f32 out), 16
+// tokens per warp step, steps dealt round-robin to the warps.  Each warp ends
+// with its own (m, l, o) in merge entry entry0 + warp.
+//  * S = K Q^T: keys are the A operand straight from global memory (lane
+//    (g, q) holds tokens g and g + 8, its quarter D/4 of the channels); the
+//    queries are the B operand over the same channel permutation.
+//  * O^T = V^T P^T: 8x8 blocks of value rows are transposed in registers
+//    (movmatrix), so m-tile 2i + jp row g is channel
+//    32 i + 8 (g >> 1) + 4 jp + (g & 1) (row g + 8: that + 2).  P^T comes
+//    from the logit fragments by the same transpose, split into high + low
+//    bf16 parts.
+template <int D>
+__device__ void tail_entries(const AttendParams& p, long long u, int t_lo, int t_hi, float* wm, float* wl,
+                             float* wc, float* wo, int entry0) {
+  constexpr int KS = D / 16;   // k-steps of S, m-tiles of O^T
+  constexpr int QC = D / 4;    // channels of a lane's key / query quarter
+  constexpr int VC = D / 32;   // 16-byte value chunks per lane and row
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int g = lane >> 2, q = lane & 3;
   const int b = static_cast<int>(u / p.c.Hkv), kvh = static_cast<int>(u % p.c.Hkv);
   const int R = p.R;
-  const int G = p.c.G;
-#pragma unroll 8
-  for (int e = tid; e < kMaxRows * D; e += blockDim.x) {
-    const int rho = e / D, d = e % D;
-    float v = 0.f;
-    if (rho < R) {
-      const int i = rho / p.HG, hh = rho % p.HG;
-      const long long qoff = ((static_cast<long long>(b) * p.gamma + i) * p.Hq + kvh * p.HG + hh) * D + d;
-      v = bf16_to_f32(p.q[qoff]) * p.qscale;
-    }
-    qt[e] = v;
-  }
-  if (tid < kMaxRows) {
-    st_m[tid] = neg_inf();
-    st_l[tid] = 0.f;
-  }
-  // this CTA's token range of the unit's tail list
-  const int NT = p.c.r + p.P + p.top_k;
-  const int per = (NT + p.S_t - 1) / p.S_t;
-  const int t_lo = min(NT, tsplit * per), t_hi = min(NT, t_lo + per);
-  float o[kMaxRows];
+  uint32_t qf[QC / 2];   // query row g, channels q QC .. q QC + QC - 1, bf16 pairs
+  if (g < R) {
+    const int i = g / p.HG, hh = g % p.HG;
+    const long long qrow = ((static_cast<long long>(b) * p.gamma + i) * p.Hq + kvh * p.HG + hh) * D;
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow + q * QC);
 #pragma unroll
-  for (int r = 0; r < kMaxRows; ++r) o[r] = 0.f;
-  __syncthreads();
+    for (int c = 0; c < QC / 8; ++c) {
+      const uint4 w = src[c];
+      qf[4 * c] = w.x;
+      qf[4 * c + 1] = w.y;
+      qf[4 * c + 2] = w.z;
+      qf[4 * c + 3] = w.w;
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < QC / 2; ++c) qf[c] = 0u;
+  }
+  float m_run[2] = {neg_inf(), neg_inf()}, l_run[2] = {0.f, 0.f};
+  float o[KS][4];
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-  constexpr int VEC = D / 8;   // 16-byte vectors per row
-  // Chunk rows are loaded into registers one chunk ahead, so the next chunk's
-  // loads are in flight while this one is computed.
-  constexpr int PER_T = (TS::TC * VEC + NTHREADS - 1) / NTHREADS;
-  uint4 pk[PER_T], pv[PER_T];
-  int pf[PER_T];
-  auto load_chunk = [&](int c0) {
-    const int nt = min(TS::TC, t_hi - c0);
+  const int nsteps = (t_hi - t_lo + 15) / 16;
+  for (int st = warp; st < nsteps; st += NW) {
+    const int t0 = t_lo + 16 * st;
+    uint4 kr[2][QC / 8], vr[2][VC];
+    int flag[2];
 #pragma unroll
-    for (int k = 0; k < PER_T; ++k) {
-      const int e = tid + k * NTHREADS;
-      const int j = e / VEC, c = e % VEC;
-      pk[k] = make_uint4(0, 0, 0, 0);
-      pv[k] = make_uint4(0, 0, 0, 0);
-      pf[k] = -2;
-      if (j < nt) {
-        int t = c0 + j;
-        const uint16_t *kp = nullptr, *vp = nullptr;
-        if (t < p.c.r) {
-          const int slot = (p.c.res_start + t) % (2 * G);
-          const long long off = (u * 2 * G + slot) * D;
-          kp = p.c.res_k + off;
-          vp = p.c.res_v + off;
-          pf[k] = -1;
-        } else if ((t -= p.c.r) < p.P) {
-          const long long off = (u * p.P + t) * D;
-          kp = p.pend_k + off;
-          vp = p.pend_v + off;
-          pf[k] = t;
-        } else {
-          t -= p.P;
-          const int idx = p.sel_idx[u * p.top_k + t];
-          if (idx >= 0 && idx < p.c.Lq) {
-            const long long off = (u * p.top_k + t) * D;
-            kp = p.sel_k + off;
-            vp = p.sel_v + off;
-            pf[k] = -1;
-          }
-        }
-        if (kp) {
-          pk[k] = reinterpret_cast<const uint4*>(kp)[c];
-          pv[k] = reinterpret_cast<const uint4*>(vp)[c];
-        }
+    for (int h = 0; h < 2; ++h) {
+      const int t = t0 + g + 8 * h;
+      const uint16_t *kp = nullptr, *vp = nullptr;
+      flag[h] = (t < t_hi) ? tail_row<D>(p, u, t, kp, vp) : -2;
+#pragma unroll
+      for (int c = 0; c < QC / 8; ++c)
+        kr[h][c] = kp ? reinterpret_cast<const uint4*>(kp + q * QC)[c] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int i = 0; i < VC; ++i)
+        vr[h][i] = vp ? *reinterpret_cast<const uint4*>(vp + 32 * i + 8 * q) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // ---- S: tokens g, g + 8 x rows 2q, 2q + 1 ----
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      const uint32_t* k0 = reinterpret_cast<const uint32_t*>(&kr[0][0]);
+      const uint32_t* k1 = reinterpret_cast<const uint32_t*>(&kr[1][0]);
+      const uint32_t a[4] = {k0[2 * kk], k1[2 * kk], k0[2 * kk + 1], k1[2 * kk + 1]};
+      mma16816_bf16(sc, a, qf[2 * kk], qf[2 * kk + 1]);
+    }
+    float x[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int h = e >> 1, rho = 2 * q + (e & 1);
+      bool vis = (flag[h] != -2) && (rho < R);
+      if (vis && flag[h] >= 0) vis = flag[h] <= p.P - p.gamma + rho / p.HG;
+      x[e] = vis ? sc[e] * p.qscale : neg_inf();
+    }
+    // ---- online softmax of rows 2q, 2q + 1 (the 8 lanes of this q) ----
+    float alpha[2], pr[4];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float mx = fmaxf(x[r], x[r + 2]);
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+      const float m_new = fmaxf(m_run[r], mx);
+      const float msafe = (m_new == neg_inf()) ? 0.f : m_new;
+      alpha[r] = (m_run[r] == neg_inf()) ? 0.f : fast_exp2(m_run[r] - msafe);
+      pr[r] = fast_exp2(x[r] - msafe);
+      pr[r + 2] = fast_exp2(x[r + 2] - msafe);
+      l_run[r] = l_run[r] * alpha[r] + (pr[r] + pr[r + 2]);
+      m_run[r] = m_new;
+    }
+    // ---- P^T fragments: (tokens 2q, 2q + 1; row g), high and low parts ----
+    uint32_t ph[2], pl[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(pr[2 * h]), h1 = __float2bfloat16_rn(pr[2 * h + 1]);
+      const __nv_bfloat16 l0 = __float2bfloat16_rn(pr[2 * h] - __bfloat162float(h0));
+      const __nv_bfloat16 l1 = __float2bfloat16_rn(pr[2 * h + 1] - __bfloat162float(h1));
+      ph[h] = transpose8x8(static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
+                           (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16));
+      pl[h] = transpose8x8(static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
+                           (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16));
+    }
+    // ---- O^T += V^T P^T, a fresh accumulator per step ----
+#pragma unroll
+    for (int i = 0; i < VC; ++i) {
+      const uint32_t* v0 = reinterpret_cast<const uint32_t*>(&vr[0][i]);
+      const uint32_t* v1 = reinterpret_cast<const uint32_t*>(&vr[1][i]);
+#pragma unroll
+      for (int jp = 0; jp < 2; ++jp) {
+        const int mt = 2 * i + jp;
+        const uint32_t a[4] = {transpose8x8(v0[2 * jp]), transpose8x8(v0[2 * jp + 1]), transpose8x8(v1[2 * jp]),
+                               transpose8x8(v1[2 * jp + 1])};
+        float os[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816_bf16(os, a, ph[0], ph[1]);
+        mma16816_bf16(os, a, pl[0], pl[1]);
+        o[mt][0] = fmaf(o[mt][0], alpha[0], os[0]);
+        o[mt][1] = fmaf(o[mt][1], alpha[1], os[1]);
+        o[mt][2] = fmaf(o[mt][2], alpha[0], os[2]);
+        o[mt][3] = fmaf(o[mt][3], alpha[1], os[3]);
       }
     }
-  };
-  if (t_lo < t_hi) load_chunk(t_lo);
-  for (int c0 = t_lo; c0 < t_hi; c0 += TS::TC) {
-    const int nt = min(TS::TC, t_hi - c0);
-    // ---- stage K and V rows ----
+  }
+  // ---- this warp's entry ----
 #pragma unroll
-    for (int k = 0; k < PER_T; ++k) {
-      const int e = tid + k * NTHREADS;
-      const int j = e / VEC, c = e % VEC;
-      if (j < TS::TC) {
-        *reinterpret_cast<uint4*>(ks + j * TS::ROW + c * 16) = pk[k];
-        *reinterpret_cast<uint4*>(vs + j * TS::ROW + c * 16) = pv[k];
-        if (c == 0) tok_pend[j] = pf[k];
-      }
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int o2 = 4; o2 < 32; o2 <<= 1) l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], o2);
+  const int e = entry0 + warp;
+  if (g == 0) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      wm[e * 8 + 2 * q + r] = m_run[r];
+      wl[e * 8 + 2 * q + r] = l_run[r];
+#pragma unroll
+      for (int jv = 0; jv < 4; ++jv) wc[(e * 8 + 2 * q + r) * 4 + jv] = 0.f;
     }
-    __syncthreads();
-    if (c0 + TS::TC < t_hi) load_chunk(c0 + TS::TC);
-    // ---- logits: thread <-> (row, token) ----
-    for (int e = tid; e < kMaxRows * TS::TC; e += blockDim.x) {
-      const int rho = e / TS::TC, j = e % TS::TC;
-      float acc = neg_inf();
-      const int flag = (j < nt) ? tok_pend[j] : -2;
-      bool vis = (rho < R) && (flag != -2);
-      if (vis && flag >= 0) vis = flag <= p.P - p.gamma + rho / p.HG;
-      if (vis) {
-        acc = 0.f;
-        const float* qr = qt + rho * D;
-        const uint8_t* kr = ks + j * TS::ROW;
+  }
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    const int ch = 32 * (mt >> 1) + 8 * (g >> 1) + 4 * (mt & 1) + (g & 1);
+    wo[(e * 8 + 2 * q) * D + ch] = o[mt][0];
+    wo[(e * 8 + 2 * q + 1) * D + ch] = o[mt][1];
+    wo[(e * 8 + 2 * q) * D + ch + 2] = o[mt][2];
+    wo[(e * 8 + 2 * q + 1) * D + ch + 2] = o[mt][3];
+  }
+}
+
+// Merge entries [0, nent) of the shared scratch into partial `part` of unit u.
+template <int D>
+__device__ void merge_to_partial(const AttendParams& p, long long u, int part, int nent, int G, const float* wm,
+                                 const float* wl, const float* wc, const float* wo, float* fac) {
+  const int tid = threadIdx.x, R = p.R;
+  float* dst = p.partials + (u * (p.S_q + p.S_t) + part) * kPartialFloats(D);
+  if (tid < R) {
+    float Mx = neg_inf();
+    for (int w = 0; w < nent; ++w) Mx = fmaxf(Mx, wm[w * 8 + tid]);
+    float lt = 0.f;
+    for (int w = 0; w < nent; ++w) {
+      const float mw = wm[w * 8 + tid];
+      const float f = (mw == neg_inf()) ? 0.f : fast_exp2(mw - Mx);
+      fac[w * 8 + tid] = f;
+      lt += f * wl[w * 8 + tid];
+    }
+    dst[tid] = Mx;
+    dst[kMaxRows + tid] = lt;
+  }
+  __syncthreads();
+  for (int e = 4 * tid; e < R * D; e += 4 * NTHREADS) {
+    const int rho = e / D, d = e % D;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-        for (int c = 0; c < VEC; ++c) {
-          const uint4 kw = *reinterpret_cast<const uint4*>(kr + c * 16);
-          const float4 qa = *reinterpret_cast<const float4*>(qr + 8 * c);
-          const float4 qb = *reinterpret_cast<const float4*>(qr + 8 * c + 4);
-          acc = fmaf(qa.x, __uint_as_float(kw.x << 16), acc);
-          acc = fmaf(qa.y, __uint_as_float(kw.x & 0xFFFF0000u), acc);
-          acc = fmaf(qa.z, __uint_as_float(kw.y << 16), acc);
-          acc = fmaf(qa.w, __uint_as_float(kw.y & 0xFFFF0000u), acc);
-          acc = fmaf(qb.x, __uint_as_float(kw.z << 16), acc);
-          acc = fmaf(qb.y, __uint_as_float(kw.z & 0xFFFF0000u), acc);
-          acc = fmaf(qb.z, __uint_as_float(kw.w << 16), acc);
-          acc = fmaf(qb.w, __uint_as_float(kw.w & 0xFFFF0000u), acc);
-        }
-      }
-      lg[rho * TS::TC + j] = acc;
+    for (int w = 0; w < nent; ++w) {
+      const float f = fac[w * 8 + rho];
+      const float c = wc[(w * 8 + rho) * 4 + d / G];
+      const float4 ov = *reinterpret_cast<const float4*>(wo + (w * 8 + rho) * D + d);
+      acc.x = fmaf(f, ov.x + c, acc.x);
+      acc.y = fmaf(f, ov.y + c, acc.y);
+      acc.z = fmaf(f, ov.z + c, acc.z);
+      acc.w = fmaf(f, ov.w + c, acc.w);
     }
-    __syncthreads();
-    // ---- online softmax statistics (one warp per row) ----
-    {
-      const int warp = tid / 32, lane = tid % 32;
-      static_assert(TS::TC == 32, "one token per lane");
-      for (int r = warp; r < R; r += NTHREADS / 32) {
-        const float x0 = lg[r * TS::TC + lane];
-        float mx = x0;
-#pragma unroll
-        for (int s2 = 16; s2 > 0; s2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s2));
-        const float m_old = st_m[r];
-        const float m_new = fmaxf(m_old, mx);
-        const float msafe = (m_new == neg_inf()) ? 0.f : m_new;
-        const float p0 = (x0 == neg_inf()) ? 0.f : fast_exp2(x0 - msafe);
-        lg[r * TS::TC + lane] = p0;
-        float sum = p0;
-#pragma unroll
-        for (int s2 = 16; s2 > 0; s2 >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, s2);
-        if (lane == 0) {
-          const float alpha = (m_old == neg_inf()) ? 0.f : fast_exp2(m_old - msafe);
-          st_a[r] = alpha;
-          st_l[r] = st_l[r] * alpha + sum;
-          st_m[r] = m_new;
-        }
-      }
-    }
-    __syncthreads();
-    // ---- P.V: thread d accumulates channel d for all rows ----
-    if (tid < D) {
-#pragma unroll
-      for (int r = 0; r < kMaxRows; ++r)
-        if (r < R) o[r] *= st_a[r];
-      for (int j = 0; j < nt; ++j) {
-        const float v = bf16_to_f32(*reinterpret_cast<const uint16_t*>(vs + j * TS::ROW + tid * 2));
-#pragma unroll
-        for (int r = 0; r < kMaxRows; ++r)
-          if (r < R) o[r] = fmaf(lg[r * TS::TC + j], v, o[r]);
-      }
-    }
-    __syncthreads();
-  }
-  // write the partial (index S_q + tsplit of this unit)
-  const int PF = kPartialFloats(D);
-  float* dst = p.partials + (u * (p.S_q + p.S_t) + p.S_q + tsplit) * PF;
-  if (tid < kMaxRows) {
-    dst[tid] = (tid < R) ? st_m[tid] : neg_inf();
-    dst[kMaxRows + tid] = (tid < R) ? st_l[tid] : 0.f;
-  }
-  if (tid < D) {
-#pragma unroll
-    for (int r = 0; r < kMaxRows; ++r)
-      if (r < R) dst[2 * kMaxRows + r * D + tid] = o[r];
+    *reinterpret_cast<float4*>(dst + 2 * kMaxRows + rho * D + d) = acc;
   }
 }
 
@@ -434,10 +485,20 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
   int* sh_flag = reinterpret_cast<int*>(smem + L::MISC_OFF);
   int* sh_abort = sh_flag + 1;
 
+  constexpr int G = D / NJ;
   const long long ntail = nunits * p.S_t;
   if (blockIdx.x < ntail) {  // ---------------- tail CTAs (first, so they start in the first wave) ----
     const long long u = blockIdx.x / p.S_t;
-    tail_partial<D>(p, u, static_cast<int>(blockIdx.x % p.S_t), smem);
+    const int ts = static_cast<int>(blockIdx.x % p.S_t);
+    const int ntl = p.c.r + p.P + p.top_k, per = (ntl + p.S_t - 1) / p.S_t;
+    const int t_lo = min(ntl, ts * per), t_hi = min(ntl, t_lo + per);
+    float* wm = reinterpret_cast<float*>(smem + L::WM_OFF);
+    float* wl = reinterpret_cast<float*>(smem + L::WL_OFF);
+    float* wc = reinterpret_cast<float*>(smem + L::WC_OFF);
+    float* wo = reinterpret_cast<float*>(smem + L::WO_OFF);
+    tail_entries<D>(p, u, t_lo, t_hi, wm, wl, wc, wo, 0);
+    __syncthreads();
+    merge_to_partial<D>(p, u, p.S_q + ts, NW, G, wm, wl, wc, wo, reinterpret_cast<float*>(smem + L::FAC_OFF));
     __syncthreads();
     ticket_and_combine<D>(p, u, sh_flag, reinterpret_cast<float*>(smem));
     return;
@@ -452,7 +513,6 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
   const int ntok_chunk = static_cast<int>(max(0LL, t_end - t_begin));
   const int ntiles = (ntok_chunk + M::TT - 1) / M::TT;
   const int per_warp = (ntiles + NW - 1) / NW;
-  constexpr int G = D / NJ;
   constexpr int NPK = D / 8;          // key pairs per lane chunk
   constexpr int KSTEPS = D / 16;
   constexpr float MULT = static_cast<float>(M::MULT);   // INT4 reads the upper nibble: step 16 scale
@@ -524,24 +584,12 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
   const bool has_sel = p.top_k > 0;
   if (has_sel)
     for (int e = tid; e < bm_words; e += blockDim.x) bitmap[e] = 0u;
-  // scaled queries q~ = q * sm_scale * log2(e) (rows >= R are zero)
-  for (int e = tid; e < kMaxRows * D; e += blockDim.x) {
-    const int rho = e / D, d = e % D;
-    float v = 0.f;
-    if (rho < R) {
-      const int i = rho / p.HG, hh = rho % p.HG;
-      const long long qrow = ((static_cast<long long>(b) * p.gamma + i) * p.Hq + kvh * p.HG + hh) * D;
-      v = bf16_to_f32(p.q[qrow + d]) * p.qscale;
-    }
-    qt[e] = v;
-  }
-  __syncthreads();
-  if (warp == 0) {  // max |q~| over the valid rows, for the weight normalizer
-    float qm = 0.f;
-    for (int e = lane; e < R * D; e += 32) qm = fmaxf(qm, fabsf(qt[e]));
+  // scaled queries, and per warp the max |q~| (for the weight normalizer)
+  {
+    float qm = fill_qt<D>(p, b, kvh, qt);
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o2));
-    if (lane == 0) *reinterpret_cast<float*>(smem + L::SRC_OFF + NW * 48) = qm;
+    if (lane == 0) reinterpret_cast<float*>(smem + L::SRC_OFF + NW * 48)[warp] = qm;
   }
   if (has_sel) {
     for (int j = tid; j < p.top_k; j += blockDim.x) {
@@ -562,7 +610,6 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
     // channels, k = tokens).  In m-tile s the lane's rows g and g+8 are the
     // tokens of value pair 2s + (g & 1) of token octet g >> 1, so the P values a
     // lane computes are a whole B register of P.V for one destination lane.
-    const int qbase = q * (D / 4);
     const int oct = 8 * (g >> 1), par = g & 1;
     int tokA[2], tokB[2];
     float vinv[2];          // 1 / value factor of the lane's pair, per m-tile
@@ -632,7 +679,10 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
           const int lpr = 32 / rpow, wrow = lane / lpr, wsub = lane % lpr;
           uint32_t* wb = reinterpret_cast<uint32_t*>(smem + L::WB_OFF) + warp * (4 * D);
           (void)wb; (void)wrow; (void)wsub;
-          const float qmax = *reinterpret_cast<const float*>(smem + L::SRC_OFF + NW * 48);
+          const float* qmw = reinterpret_cast<const float*>(smem + L::SRC_OFF + NW * 48);
+          float qmax = qmw[0];
+#pragma unroll
+          for (int w2 = 1; w2 < NW; ++w2) qmax = fmaxf(qmax, qmw[w2]);
           constexpr int PPR = D / 2;           // channel pairs per row
           constexpr float KW = MULT * kx_weight<MODE>();
           float wsum = 0.f, zsum = 0.f;
@@ -894,20 +944,31 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
               }
             }
           }
-          // The slab's products go into a fresh accumulator, folded into the
-          // running output with one rounding per element: a long MMA chain
+          // Value codes read as 1024 + m c.  The slab's 1024 * sum P' per column
+          // is the same for every channel: one MMA with a constant -1024 A
+          // operand computes it, and it starts every m-tile's accumulator.
+          // The slab's products go into that fresh accumulator, folded into
+          // the running output with one rounding per element: a long MMA chain
           // would accumulate the tensor core's truncation.
+          float koff[4] = {0.f, 0.f, 0.f, 0.f};
+          {
+            const uint32_t aneg[4] = {0xE400E400u, 0xE400E400u, 0xE400E400u, 0xE400E400u};  // f16 -1024
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              mma16816(koff, aneg, bh[s][0], bh[s][1]);
+              if constexpr (NT == 2) mma16816(koff, aneg, bl[s][0], bl[s][1]);
+            }
+          }
 #pragma unroll
           for (int mt = jv * (G / 16); mt < (jv + 1) * (G / 16); ++mt) {
             uint32_t a[2][4];
             const uint8_t* va = vslab + (16 * mt + g) * RW::VROW;
             value_frags_x<MODE>(va, va + 8 * RW::VROW, L::VPLANE, q, a);
-            float os[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-              mma16816(os, a[s], bh[s][0], bh[s][1]);
-              if constexpr (NT == 2) mma16816(os, a[s], bl[s][0], bl[s][1]);
-            }
+            float os[4];
+            mma16816_c(os, a[0], bh[0][0], bh[0][1], koff);
+            if constexpr (NT == 2) mma16816(os, a[0], bl[0][0], bl[0][1]);
+            mma16816(os, a[1], bh[1][0], bh[1][1]);
+            if constexpr (NT == 2) mma16816(os, a[1], bl[1][0], bl[1][1]);
             o[mt][0] = fmaf(o[mt][0], a_lo, os[0]);
             o[mt][1] = fmaf(o[mt][1], a_hi, os[1]);
             o[mt][2] = fmaf(o[mt][2], a_lo, os[2]);
@@ -972,37 +1033,22 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
   }
   __syncthreads();
 
-  // ---- CTA merge of the four warps -> partial ----
-  {
-    const float* wm = reinterpret_cast<const float*>(smem + L::WM_OFF);
-    const float* wl = reinterpret_cast<const float*>(smem + L::WL_OFF);
-    const float* wc = reinterpret_cast<const float*>(smem + L::WC_OFF);
-    const float* wo = reinterpret_cast<const float*>(smem + L::WO_OFF);
-    const int PF = kPartialFloats(D);
-    float* dst = p.partials + (u * (p.S_q + p.S_t) + split) * PF;
-    for (int e = tid; e < R * D; e += blockDim.x) {
-      const int rho = e / D, d = e % D;
-      float Mx = neg_inf();
-#pragma unroll
-      for (int w = 0; w < NW; ++w) Mx = fmaxf(Mx, wm[w * 8 + rho]);
-      float lt = 0.f, ot = 0.f;
-      if (Mx != neg_inf()) {
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float mw = wm[w * 8 + rho];
-          if (mw == neg_inf()) continue;
-          const float f = fast_exp2(mw - Mx);
-          lt += f * wl[w * 8 + rho];
-          ot += f * (wo[(w * 8 + rho) * D + d] + wc[(w * 8 + rho) * 4 + d / G]);
-        }
-      }
-      dst[2 * kMaxRows + rho * D + d] = ot;
-      if (d == 0) {
-        dst[rho] = Mx;
-        dst[kMaxRows + rho] = lt;
-      }
-    }
+  // ---- this CTA's share of the bf16 tail (residual, pending, selected tokens) ----
+  // Without tail CTAs the quantized splits share the tail list: entries
+  // NW .. 2 NW - 1.
+  const float* wm = reinterpret_cast<const float*>(smem + L::WM_OFF);
+  if (p.S_t == 0) {
+    const int ntl = p.c.r + p.P + p.top_k, per = (ntl + p.S_q - 1) / p.S_q;
+    const int t_lo = min(ntl, split * per), t_hi = min(ntl, t_lo + per);
+    tail_entries<D>(p, u, t_lo, t_hi, reinterpret_cast<float*>(smem + L::WM_OFF),
+                    reinterpret_cast<float*>(smem + L::WL_OFF), reinterpret_cast<float*>(smem + L::WC_OFF),
+                    reinterpret_cast<float*>(smem + L::WO_OFF), NW);
+    __syncthreads();
   }
+  // ---- CTA merge of the entries -> partial ----
+  merge_to_partial<D>(p, u, split, (p.S_t == 0) ? 2 * NW : NW, G, wm,
+                      reinterpret_cast<const float*>(smem + L::WL_OFF), reinterpret_cast<const float*>(smem + L::WC_OFF),
+                      reinterpret_cast<const float*>(smem + L::WO_OFF), reinterpret_cast<float*>(smem + L::FAC_OFF));
   __syncthreads();
   ticket_and_combine<D>(p, u, sh_flag, reinterpret_cast<float*>(smem));
 }
@@ -1010,7 +1056,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
 template <int MODE, int D, int NJ, int NT>
 constexpr int smem_bytes() {
   using L = Smem<MODE, D, NJ, NT>;
-  return (L::TOTAL > TailSmem<D>::TOTAL) ? L::TOTAL : TailSmem<D>::TOTAL;
+  return L::TOTAL;
 }
 
 template <int MODE, int D, int NJ, int NT>

@@ -225,27 +225,30 @@ struct XPair<KVQ_MODE_INT8> {
 };
 
 // Value factor of pair i: the power of two at which the pair's codes sit.
+// Every value code sits at mantissa bit 4 or higher (INT8 codes are 8 bits
+// wide), so the encoding's 1024 is at most about 43 times the code term.
 template <int MODE>
 __host__ __device__ constexpr float vx_mult(int i) {
   if constexpr (MODE == KVQ_MODE_INT8) return 1.f;
-  else if constexpr (MODE == KVQ_MODE_INT4) return (i & 1) ? 16.f : 1.f;
-  else if constexpr (MODE == KVQ_MODE_INT2) return static_cast<float>(1 << (2 * i));
-  else return static_cast<float>(1 << i);
+  else if constexpr (MODE == KVQ_MODE_INT4) return 16.f;
+  else if constexpr (MODE == KVQ_MODE_INT2) return (i & 1) ? 64.f : 16.f;
+  else return static_cast<float>(1 << (6 + i));
 }
 
-// Keys for attention.  INT8 keys become exact f16 codes (offset encoding, then
-// the 1024 removed); INT4/INT2/INT1 keys use the top-of-mantissa encoding of
-// key_pairs (1 + c/2^b), whose offset of 1 is at most about twice the code
-// term.  Either way the accumulator never carries an offset much larger than
-// the logit.  kx_weight is the factor that turns a code's scale into the
-// weight of the encoded value; kx_offset the value an all-zero code reads as.
+// Keys for attention.  INT8 keys use the offset encoding (1024 + c): with
+// 8-bit codes the offset is at most about eight times the code term, and the
+// logit's MMA chain is only D/16 steps long.  INT4/INT2/INT1 keys use the
+// top-of-mantissa encoding of key_pairs (1 + c/2^b), whose offset of 1 is at
+// most about twice the code term.  kx_weight is the factor that turns a code's
+// scale into the weight of the encoded value; kx_offset the value an all-zero
+// code reads as.
 template <int MODE>
 __host__ __device__ constexpr float kx_weight() {
   return MODE == KVQ_MODE_INT8 ? 1.f : static_cast<float>(1 << Mode<MODE>::CB);
 }
 template <int MODE>
 __host__ __device__ constexpr float kx_offset() {
-  return MODE == KVQ_MODE_INT8 ? 0.f : 1.f;
+  return MODE == KVQ_MODE_INT8 ? 1024.f : 1.f;
 }
 
 // Channels (relative to the lane chunk) of key pair p.
@@ -286,10 +289,10 @@ __device__ __forceinline__ void key_pairs_x(const uint8_t* k0, int plane_stride,
     for (int w = 0; w < NWD; ++w) {
       const uint32_t E = ((h[w] << 4) & 0xF0F0F0F0u) | (l[w] & 0x0F0F0F0Fu);
       const uint32_t O = (h[w] & 0xF0F0F0F0u) | ((l[w] >> 4) & 0x0F0F0F0Fu);
-      P[4 * w + 0] = xoff(__byte_perm(E, X64B, 0x4140));
-      P[4 * w + 1] = xoff(__byte_perm(E, X64B, 0x4342));
-      P[4 * w + 2] = xoff(__byte_perm(O, X64B, 0x4140));
-      P[4 * w + 3] = xoff(__byte_perm(O, X64B, 0x4342));
+      P[4 * w + 0] = __byte_perm(E, X64B, 0x4140);
+      P[4 * w + 1] = __byte_perm(E, X64B, 0x4342);
+      P[4 * w + 2] = __byte_perm(O, X64B, 0x4140);
+      P[4 * w + 3] = __byte_perm(O, X64B, 0x4342);
     }
   } else {
     key_pairs<MODE, D>(k0, plane_stride, P);
@@ -297,9 +300,10 @@ __device__ __forceinline__ void key_pairs_x(const uint8_t* k0, int plane_stride,
 }
 
 // A fragments of P.V for one channel m-tile (rows ca = 16mt+g and cb = ca+8) of
-// one 32-token slab, as exact f16 values vx_mult(i) * code (the offset removed).  a[s] serves k-step s: a[s][0..1] are pair
-// 2s of rows ca/cb (k = 2q, 2q+1), a[s][2..3] pair 2s+1 (k = 2q+8, 2q+9).
-// `va`/`vb` point at rows ca/cb of plane 0.
+// one 32-token slab, as offset-encoded f16 values 1024 + vx_mult(i) * code.
+// a[s] serves k-step s: a[s][0..1] are pair 2s of rows ca/cb (k = 2q, 2q+1),
+// a[s][2..3] pair 2s+1 (k = 2q+8, 2q+9).  `va`/`vb` point at rows ca/cb of
+// plane 0.  The caller removes the 1024 through the accumulator's start value.
 template <int MODE>
 __device__ __forceinline__ void value_frags_x(const uint8_t* va, const uint8_t* vb, int plane_stride, int q,
                                               uint32_t (&a)[2][4]) {
@@ -318,35 +322,36 @@ __device__ __forceinline__ void value_frags_x(const uint8_t* va, const uint8_t* 
     pb[0] = __byte_perm(Eb, X64B, 0x4140); pb[1] = __byte_perm(Eb, X64B, 0x4342);
     pb[2] = __byte_perm(Ob, X64B, 0x4140); pb[3] = __byte_perm(Ob, X64B, 0x4342);
   } else if constexpr (MODE == KVQ_MODE_INT4) {
+    // nibble i of the word is token 8q + i; every pair lands at mantissa bits 4-7
     const uint32_t wa = *reinterpret_cast<const uint32_t*>(va + 4 * q);
     const uint32_t wb = *reinterpret_cast<const uint32_t*>(vb + 4 * q);
-    const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
-    pa[0] = xsel(wa, 0x000F000Fu); pa[1] = xsel(wa, 0x00F000F0u);
-    pa[2] = xsel(wa8, 0x000F000Fu); pa[3] = xsel(wa8, 0x00F000F0u);
-    pb[0] = xsel(wb, 0x000F000Fu); pb[1] = xsel(wb, 0x00F000F0u);
-    pb[2] = xsel(wb8, 0x000F000Fu); pb[3] = xsel(wb8, 0x00F000F0u);
+    pa[0] = xsel(wa << 4, 0x00F000F0u); pa[1] = xsel(wa, 0x00F000F0u);
+    pa[2] = xsel(wa >> 4, 0x00F000F0u); pa[3] = xsel(wa >> 8, 0x00F000F0u);
+    pb[0] = xsel(wb << 4, 0x00F000F0u); pb[1] = xsel(wb, 0x00F000F0u);
+    pb[2] = xsel(wb >> 4, 0x00F000F0u); pb[3] = xsel(wb >> 8, 0x00F000F0u);
   } else if constexpr (MODE == KVQ_MODE_INT2) {
     const uint32_t xa = *reinterpret_cast<const uint16_t*>(va + 2 * q);
     const uint32_t xb = *reinterpret_cast<const uint16_t*>(vb + 2 * q);
     const uint32_t y = __byte_perm(xa, xb, 0x5140);   // [a.b0, b.b0, a.b1, b.b1]
-    const uint32_t y8 = y >> 8;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      pa[j] = xsel(y, 0x00030003u << (2 * j));
-      pb[j] = xsel(y8, 0x00030003u << (2 * j));
-    }
+    // token j of row a sits at bits 2j and 16+2j, of row b 8 bits higher
+    const uint32_t ya = y << 4, yb = y >> 4, yc = y >> 8;
+    pa[0] = xsel(ya, 0x00300030u); pa[1] = xsel(ya, 0x00C000C0u);
+    pa[2] = xsel(y, 0x00300030u); pa[3] = xsel(y, 0x00C000C0u);
+    pb[0] = xsel(yb, 0x00300030u); pb[1] = xsel(yb, 0x00C000C0u);
+    pb[2] = xsel(yc, 0x00300030u); pb[3] = xsel(yc, 0x00C000C0u);
   } else {
     const uint32_t x = static_cast<uint32_t>(va[q]) | (static_cast<uint32_t>(vb[q]) << 8);
     const uint32_t y = (x & 0x0F0Fu) | ((x & 0xF0F0u) << 12);
-    const uint32_t y8 = y >> 8;
+    // token j of row a at bits j and 16+j, of row b 8 bits higher: move to bits 6-9
+    const uint32_t ya = y << 6, yb = y >> 2;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      pa[j] = xsel(y, 0x00010001u << j);
-      pb[j] = xsel(y8, 0x00010001u << j);
+      pa[j] = xsel(ya, 0x00010001u << (6 + j));
+      pb[j] = xsel(yb, 0x00010001u << (6 + j));
     }
   }
-  a[0][0] = xoff(pa[0]); a[0][1] = xoff(pb[0]); a[0][2] = xoff(pa[1]); a[0][3] = xoff(pb[1]);
-  a[1][0] = xoff(pa[2]); a[1][1] = xoff(pb[2]); a[1][2] = xoff(pa[3]); a[1][3] = xoff(pb[3]);
+  a[0][0] = pa[0]; a[0][1] = pb[0]; a[0][2] = pa[1]; a[0][3] = pb[1];
+  a[1][0] = pa[2]; a[1][1] = pb[2]; a[1][2] = pa[3]; a[1][3] = pb[3];
 }
 
 }  // namespace kvq

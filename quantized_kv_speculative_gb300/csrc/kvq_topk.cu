@@ -36,10 +36,9 @@
 namespace kvq {
 namespace {
 
-constexpr int NW = 4;
-constexpr int SPW = 2;
-constexpr int NSLOT = NW * SPW;
-constexpr int NTHREADS = (NW + 1) * 32;
+constexpr int NW = 4;                  // warps per CTA; each streams and scores its own tiles
+
+constexpr int NTHREADS = NW * 32;
 constexpr int kGather = 64;            // bin size below which keys are ranked directly
 
 template <int MODE, int D>
@@ -47,6 +46,8 @@ struct TopkSmem {
   using M = Mode<MODE>;
   using RW = Rows<MODE, D>;
   static constexpr int TT = M::TT;
+  static constexpr int SPW = TT == 32 ? 4 : 2;                // stage slots per warp
+  static constexpr int NSLOT = NW * SPW;
   static constexpr int KPLANE = TT * RW::KROW;
   static constexpr int KSZ_OFF = KPLANE;                      // only the upper/only plane is read
   static constexpr int KSZ_BYTES = (TT / 32) * 2 * D * 4;
@@ -57,7 +58,7 @@ struct TopkSmem {
   static constexpr int LIST_OFF = HIST_OFF + 256 * 4;         // gathered keys [kGather]
   static constexpr int RED_OFF = LIST_OFF + kGather * 4;      // per-warp min/max, counts [16]
   static constexpr int BAR_OFF = RED_OFF + 16 * 4;
-  static constexpr int MISC_OFF = BAR_OFF + 2 * NSLOT * 8;
+  static constexpr int MISC_OFF = BAR_OFF + NSLOT * 8;
   static constexpr int SC_OFF = MISC_OFF + 64;                // order keys / merge keys (sized per launch)
   static constexpr int MAX_SC = kTopkMaxCand * 8;             // >= kTopkMaxChunk * 4
   static constexpr int MAX_TOTAL = SC_OFF + MAX_SC;
@@ -159,9 +160,13 @@ __device__ void select_kth(int n, int kth, F take, uint32_t* hist, uint32_t* lis
   int remaining = kth;
   while (true) {
     // ---- histogram of the 8 bits at `shift` among keys matching the prefix ----
-    for (int i = tid; i < n; i += blockDim.x) {
-      uint32_t key;
-      if (take(i, key) && (key & mask) == prefix) atomicAdd(hist + ((key >> shift) & 255u), 1u);
+    // (lanes that hit the same bin add once: hot bins would serialize)
+    const int nround = (n + blockDim.x - 1) / blockDim.x * blockDim.x;
+    for (int i = tid; i < nround; i += blockDim.x) {
+      uint32_t key = 0, bin = 0xFFFFFFFFu;
+      if (i < n && take(i, key) && (key & mask) == prefix) bin = (key >> shift) & 255u;
+      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+      if (bin != 0xFFFFFFFFu && (__ffs(peers) - 1) == lane) atomicAdd(hist + bin, static_cast<uint32_t>(__popc(peers)));
     }
     __syncthreads();
     if (warp == 0) {
@@ -263,6 +268,7 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   const int ntiles = (n + M::TT - 1) / M::TT;
   const int per_warp = (ntiles + NW - 1) / NW;
   const int K = p.k;
+  constexpr int SPW = L::SPW;
 
   uint32_t* okeys = reinterpret_cast<uint32_t*>(smem + L::SC_OFF);
   float* qs = reinterpret_cast<float*>(smem + L::QS_OFF);
@@ -270,18 +276,35 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   uint32_t* list = reinterpret_cast<uint32_t*>(smem + L::LIST_OFF);
   uint32_t* red = reinterpret_cast<uint32_t*>(smem + L::RED_OFF);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-  uint64_t* empty = full + NSLOT;
   int* misc = reinterpret_cast<int*>(smem + L::MISC_OFF);   // [0] abort, [1] flag, [2..6] select state
-
-  if (tid == 0) {
-    for (int s = 0; s < NSLOT; ++s) {
-      mbar_init(full + s, 1);
-      mbar_init(empty + s, 1);
-    }
-    misc[0] = 0;
+  const long long u_tok = u * p.c.C;
+  // this warp's tiles: a contiguous run of the chunk
+  const int my_first = warp * per_warp;
+  const int my_tiles = max(0, min(per_warp, ntiles - my_first));
+  // Each warp streams its own tiles: lane 0 puts tile j into slot j % SPW of
+  // the warp's ring with 1-D bulk copies that complete on the slot's mbarrier.
+  auto issue = [&](int j) {
+    const int slot = warp * SPW + (j % SPW);
+    const int rel = (my_first + j) * M::TT;                 // chunk-relative first token
+    const int nt = min(M::TT, n - rel);
+    const long long t0 = t_begin + rel;
+    const uint32_t kb = nt * RW::KROW;
+    const uint32_t kszb = static_cast<uint32_t>((nt + G - 1) / G) * 2 * D * 4;
+    uint8_t* sbase = smem + slot * L::SLOT;
+    const uint64_t pol = policy_evict_first();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(full + slot, kb + kszb);
+    bulk_g2s(sbase, p.c.kplane[0] + (u_tok + t0) * RW::KROW, kb, full + slot, pol);
+    bulk_g2s(sbase + L::KSZ_OFF, p.c.ksz + (u * (p.c.C / G) + t0 / G) * 2 * D, kszb, full + slot, pol);
+  };
+  if (lane == 0) {
+    for (int s2 = 0; s2 < SPW; ++s2) mbar_init(full + warp * SPW + s2, 1);
     fence_mbar_init();
+    for (int j = 0; j < min(SPW, my_tiles); ++j) issue(j);
   }
-  // summed query: ascending head order, fp32
+  int issued = min(SPW, my_tiles), consumed = 0;
+  if (tid == 0) misc[0] = 0;
+  // summed query (ascending head order, fp32) while the first tiles load
   for (int d = tid; d < D; d += blockDim.x) {
     float acc = 0.f;
     for (int hh = 0; hh < p.HG; ++hh) {
@@ -292,35 +315,8 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   }
   __syncthreads();
   volatile int* abort_flag = misc;
-  const long long u_tok = u * p.c.C;
 
-  if (warp == NW) {
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      for (int j = 0; j < per_warp && !*abort_flag; ++j) {
-        for (int w = 0; w < NW; ++w) {
-          const int ti = w * per_warp + j;
-          if (ti >= ntiles) continue;
-          const int slot = w * SPW + (j % SPW);
-          if (!mbar_wait_bounded(empty + slot, ((j / SPW) & 1) ^ 1, p.wait_limit)) {
-            record_status(p.status, KVQ_ERR_DEVICE_TIMEOUT);
-            *abort_flag = 1;
-            break;
-          }
-          const long long t0 = t_begin + static_cast<long long>(ti) * M::TT;
-          const int nt = static_cast<int>(min(static_cast<long long>(M::TT), t_end - t0));
-          const long long g_first = t0 / G, g_last = (t0 + nt - 1) / G;
-          const uint32_t kb = nt * RW::KROW;
-          const uint32_t kszb = static_cast<uint32_t>(g_last - g_first + 1) * 2 * D * 4;
-          uint8_t* sbase = smem + slot * L::SLOT;
-          mbar_arrive_expect_tx(full + slot, kb + kszb);
-          bulk_g2s(sbase, p.c.kplane[0] + (u_tok + t0) * RW::KROW, kb, full + slot, pol);
-          bulk_g2s(sbase + L::KSZ_OFF, p.c.ksz + (u * (p.c.C / G) + g_first) * 2 * D, kszb,
-                   full + slot, pol);
-        }
-      }
-    }
-  } else {
+  {
     // B fragments: lane (g, q) holds column g of W for its channel chunk; only
     // columns 0 (hi) and 1 (lo) are nonzero.
     uint32_t wb[D / 8];
@@ -332,9 +328,8 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
     const float cbmul = static_cast<float>(1 << M::CB);
     uint16_t* whalf = reinterpret_cast<uint16_t*>(smem + L::WB_OFF) + warp * 2 * D;   // [hi D][lo D], pair order
     constexpr int CPL = D / 32;   // channels per lane in the cooperative setup
-    for (int j = 0; j < per_warp; ++j) {
-      const int ti = warp * per_warp + j;
-      if (ti >= ntiles) break;
+    for (int j = 0; j < my_tiles; ++j) {
+      const int ti = my_first + j;
       const int slot = warp * SPW + (j % SPW);
       if (!mbar_wait_bounded(full + slot, (j / SPW) & 1, p.wait_limit)) {
         record_status(p.status, KVQ_ERR_DEVICE_TIMEOUT);
@@ -428,18 +423,18 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty + slot);
-    }
-  }
-  __syncthreads();
-  if (*abort_flag && warp == NW && lane == 0) {
-    for (int w = 0; w < NW; ++w) {
-      const int issued = min(per_warp, max(0, ntiles - w * per_warp));
-      for (int s2 = 0; s2 < SPW && s2 < issued; ++s2) {
-        const int jl = ((issued - 1 - s2) / SPW) * SPW + s2;
-        mbar_wait_bounded(full + w * SPW + s2, (jl / SPW) & 1, p.wait_limit);
+      consumed = j + 1;
+      if (issued < my_tiles) {
+        if (lane == 0) issue(issued);
+        ++issued;
       }
     }
+    // after an abort: let this warp's copies still in flight land before exit
+    if (lane == 0) {
+      for (int jj = consumed; jj < issued; ++jj)
+        mbar_wait_bounded(full + warp * SPW + (jj % SPW), (jj / SPW) & 1, p.wait_limit);
+    }
+    __syncwarp();
   }
   __syncthreads();
 
@@ -509,19 +504,32 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   const float* us = p.cand_score + u * p.S * K;
   const int32_t* ui = p.cand_idx + u * p.S * K;
   int cnt = 0;
-  for (int i = tid; i < NC; i += blockDim.x) {
-    const int32_t idx = __ldcg(ui + i);
-    const bool ok = idx >= 0;
-    khi[i] = ok ? order_key(__ldcg(us + i)) : 0u;
-    klo[i] = ok ? 0xFFFFFFFFu - static_cast<uint32_t>(idx) : 0u;
-    cnt += ok;
+  for (int i0 = tid; i0 < NC; i0 += 4 * NTHREADS) {
+    int32_t idx[4];
+    float sc[4];
+#pragma unroll
+    for (int k2 = 0; k2 < 4; ++k2) {   // four candidates in flight per thread
+      const int i = i0 + k2 * NTHREADS;
+      idx[k2] = (i < NC) ? __ldcg(ui + i) : -1;
+      sc[k2] = (i < NC) ? __ldcg(us + i) : 0.f;
+    }
+#pragma unroll
+    for (int k2 = 0; k2 < 4; ++k2) {
+      const int i = i0 + k2 * NTHREADS;
+      if (i < NC) {
+        const bool ok = idx[k2] >= 0;
+        khi[i] = ok ? order_key(sc[k2]) : 0u;
+        klo[i] = ok ? 0xFFFFFFFFu - static_cast<uint32_t>(idx[k2]) : 0u;
+        cnt += ok;
+      }
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
   if (lane == 0) red[warp] = static_cast<uint32_t>(cnt);
   __syncthreads();
   int nvalid = 0;
-  for (int w = 0; w < NW + 1; ++w) nvalid += static_cast<int>(red[w]);
+  for (int w = 0; w < NW; ++w) nvalid += static_cast<int>(red[w]);
   __syncthreads();
   const int kf = min(K, nvalid);
   uint32_t* whi = reinterpret_cast<uint32_t*>(smem);   // winners, in the (idle) stage area
