@@ -36,7 +36,7 @@
 namespace kvq {
 namespace {
 
-constexpr int NW = 4;                  // warps per CTA; each streams and scores its own tiles
+constexpr int NW = 8;                  // warps per CTA; each streams and scores its own tiles
 
 constexpr int NTHREADS = NW * 32;
 constexpr int kGather = 64;            // bin size below which keys are ranked directly
@@ -46,7 +46,7 @@ struct TopkSmem {
   using M = Mode<MODE>;
   using RW = Rows<MODE, D>;
   static constexpr int TT = M::TT;
-  static constexpr int SPW = TT == 32 ? 4 : 2;                // stage slots per warp
+  static constexpr int SPW = 2;                               // stage slots per warp
   static constexpr int NSLOT = NW * SPW;
   static constexpr int KPLANE = TT * RW::KROW;
   static constexpr int KSZ_OFF = KPLANE;                      // only the upper/only plane is read
@@ -56,8 +56,8 @@ struct TopkSmem {
   static constexpr int WB_OFF = QS_OFF + D * 4;               // per warp: W halves in pair order [2][D] f16
   static constexpr int HIST_OFF = WB_OFF + NW * 2 * D * 2;    // hist[256]
   static constexpr int LIST_OFF = HIST_OFF + 256 * 4;         // gathered keys [kGather]
-  static constexpr int RED_OFF = LIST_OFF + kGather * 4;      // per-warp min/max, counts [16]
-  static constexpr int BAR_OFF = RED_OFF + 16 * 4;
+  static constexpr int RED_OFF = LIST_OFF + kGather * 4;      // per-warp min/max, counts [2 NW]
+  static constexpr int BAR_OFF = RED_OFF + 2 * NW * 4;
   static constexpr int MISC_OFF = BAR_OFF + NSLOT * 8;
   static constexpr int SC_OFF = MISC_OFF + 64;                // order keys / merge keys (sized per launch)
   static constexpr int MAX_SC = kTopkMaxCand * 8;             // >= kTopkMaxChunk * 4
@@ -111,7 +111,7 @@ __device__ __forceinline__ int pair_slot(int local) {
 // Block-wide selection of the kth largest key among the i < n for which
 // take(i, key) holds (1 <= kth <= number taken).  On return st[0] = T and
 // st[2] = how many of the taken keys equal to T belong to the kth largest.
-// Every thread of the block calls it.  hist[256], list[kGather], red[16] and
+// Every thread of the block calls it.  hist[256], list[kGather], red[2 NW] and
 // st[0..4] are shared memory.
 template <typename F>
 __device__ void select_kth(int n, int kth, F take, uint32_t* hist, uint32_t* list, uint32_t* red, int* st) {
@@ -160,13 +160,9 @@ __device__ void select_kth(int n, int kth, F take, uint32_t* hist, uint32_t* lis
   int remaining = kth;
   while (true) {
     // ---- histogram of the 8 bits at `shift` among keys matching the prefix ----
-    // (lanes that hit the same bin add once: hot bins would serialize)
-    const int nround = (n + blockDim.x - 1) / blockDim.x * blockDim.x;
-    for (int i = tid; i < nround; i += blockDim.x) {
-      uint32_t key = 0, bin = 0xFFFFFFFFu;
-      if (i < n && take(i, key) && (key & mask) == prefix) bin = (key >> shift) & 255u;
-      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-      if (bin != 0xFFFFFFFFu && (__ffs(peers) - 1) == lane) atomicAdd(hist + bin, static_cast<uint32_t>(__popc(peers)));
+    for (int i = tid; i < n; i += blockDim.x) {
+      uint32_t key;
+      if (take(i, key) && (key & mask) == prefix) atomicAdd(hist + ((key >> shift) & 255u), 1u);
     }
     __syncthreads();
     if (warp == 0) {
@@ -288,14 +284,17 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
     const int rel = (my_first + j) * M::TT;                 // chunk-relative first token
     const int nt = min(M::TT, n - rel);
     const long long t0 = t_begin + rel;
+    // a tile loads key scales only when it starts a key group (or the run)
+    const bool new_grp = (j == 0) || (M::TT > G) || (t0 % G == 0);
     const uint32_t kb = nt * RW::KROW;
-    const uint32_t kszb = static_cast<uint32_t>((nt + G - 1) / G) * 2 * D * 4;
+    const uint32_t kszb = new_grp ? static_cast<uint32_t>((nt + G - 1) / G) * 2 * D * 4 : 0u;
     uint8_t* sbase = smem + slot * L::SLOT;
     const uint64_t pol = policy_evict_first();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive_expect_tx(full + slot, kb + kszb);
     bulk_g2s(sbase, p.c.kplane[0] + (u_tok + t0) * RW::KROW, kb, full + slot, pol);
-    bulk_g2s(sbase + L::KSZ_OFF, p.c.ksz + (u * (p.c.C / G) + t0 / G) * 2 * D, kszb, full + slot, pol);
+    if (new_grp)
+      bulk_g2s(sbase + L::KSZ_OFF, p.c.ksz + (u * (p.c.C / G) + t0 / G) * 2 * D, kszb, full + slot, pol);
   };
   if (lane == 0) {
     for (int s2 = 0; s2 < SPW; ++s2) mbar_init(full + warp * SPW + s2, 1);
@@ -404,12 +403,17 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
           uint32_t PA[D / 8], PB[D / 8];
           key_pairs<MODE, D>(kslab + (16 * s + g) * RW::KROW, 0, PA);
           key_pairs<MODE, D>(kslab + (16 * s + g + 8) * RW::KROW, 0, PB);
-          float cc[4] = {init0, init1, init0, init1};
+          // two independent chains over the k-steps (every partial sum is exact)
+          float cc[4] = {init0, init1, init0, init1}, c2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
+          for (int kk = 0; kk < D / 16; kk += 2) {
             const uint32_t a[4] = {PA[2 * kk], PB[2 * kk], PA[2 * kk + 1], PB[2 * kk + 1]};
+            const uint32_t a2[4] = {PA[2 * kk + 2], PB[2 * kk + 2], PA[2 * kk + 3], PB[2 * kk + 3]};
             mma16816(cc, a, wb[2 * kk], wb[2 * kk + 1]);
+            mma16816(c2, a2, wb[2 * kk + 2], wb[2 * kk + 3]);
           }
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) cc[e2] += c2[e2];
           if (q == 0) {
             const int rel = static_cast<int>(tok0 - t_begin) + 16 * s + g;
 #pragma unroll
@@ -635,10 +639,10 @@ long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
 // Split plan: over S from the fewest splits the chunk limit allows to the most
 // that the candidate limit and the chunk alignment allow, minimise
 // waves x (chunk + fixed per-CTA cost) + merge cost.  Chunks are multiples of
-// 4 x max(G, tile) tokens, so each consumer warp scores whole key groups.
+// NW x max(G, tile) tokens, so each consumer warp scores whole key groups.
 template <int MODE, int D>
 int plan_t(long long Lq, long long U, int G, int k, long long* chunk_out) {
-  const long long align = std::max<long long>(kChunkAlign, 4LL * std::max(G, Mode<MODE>::TT));
+  const long long align = std::max<long long>(kChunkAlign, static_cast<long long>(NW) * std::max(G, Mode<MODE>::TT));
   const long long s_lo = std::max(1LL, ceil_div_ll(Lq, kTopkMaxChunk));
   const long long s_hi = std::max(s_lo, std::min(ceil_div_ll(Lq, align), static_cast<long long>(kTopkMaxCand / k)));
   const int sms = sm_count();
