@@ -178,11 +178,11 @@ def run_device(args, rank, world):
         c.set_state(st)
 
     # attend, top-k, then the append: one flush kernel when the residual buffer
-    # reaches 2G (it also writes the new residual rows when it flushes a single
-    # group), else one residual-write kernel
+    # reaches 2G (it also writes the new residual rows), else one residual-write
+    # kernel
     T = spec.r0 + spec.n_accept
     f = 0 if T < 2 * spec.G else T // spec.G - 1
-    launches_per_step = 2 + (1 if f > 0 else 0) + (1 if (T - max(spec.r0, f * spec.G)) > 0 and f != 1 else 0)
+    launches_per_step = 2 + (1 if f > 0 else 0) + (1 if (T - max(spec.r0, f * spec.G)) > 0 and f == 0 else 0)
     # warm-up eagerly (also sets kernel attributes outside any capture)
     for i in range(max(args.warmup, spec.copies)):
         step(i)

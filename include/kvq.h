@@ -113,6 +113,9 @@ typedef struct kvq_cache_desc {
  *                oldest first.  residual_start is 0 or G.  At a flush the older
  *                half is quantized in place, and the other half becomes the
  *                oldest.
+ *  flush counters [u] u32: arrival counters of the quantize-append kernel
+ *                (zeroed by the first append into the empty cache, zero again
+ *                after every append).
  *
  * Codes (KIVI-style asymmetric min/max, fp32, round-half-even): scale =
  * (max - min)/(2^b - 1), code = clamp(rint((x - min) * (1/scale)), 0, 2^b - 1),

@@ -33,7 +33,7 @@ bool valid_desc(const kvq_cache_desc* d) {
 
 struct Regions {
   int np;
-  size_t k_plane, v_plane, k_sz, v_sz, res, total;
+  size_t k_plane, v_plane, k_sz, v_sz, res, ctr, total;
 };
 
 Regions regions(const kvq_cache_desc* d) {
@@ -48,7 +48,8 @@ Regions regions(const kvq_cache_desc* d) {
   r.k_sz = align256(U * (C / G) * 2 * D * 4);
   r.v_sz = align256(U * C * 2 * (D / G) * 4);
   r.res = align256(U * 2 * G * D * 2);
-  r.total = r.np * (r.k_plane + r.v_plane) + r.k_sz + r.v_sz + 2 * r.res;
+  r.ctr = align256(U * 4);
+  r.total = r.np * (r.k_plane + r.v_plane) + r.k_sz + r.v_sz + 2 * r.res + r.ctr;
   return r;
 }
 
@@ -232,18 +233,21 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const void* k_new, const void* 
     p.res_start = cache->residual_start;
     p.n = n_new;
     p.nflush = static_cast<int>(f);
-    if (f == 1) {
-      const long long first_new = std::max(r, f * G);
-      p.res_k_w = reinterpret_cast<uint16_t*>(base + cache->off_res_k);
-      p.res_v_w = reinterpret_cast<uint16_t*>(base + cache->off_res_v);
-      p.first_new = static_cast<int>(first_new);
-      p.res_count = static_cast<int>(T - first_new);
-    }
+    const long long first_new = std::max(r, f * G);
+    p.res_k_w = reinterpret_cast<uint16_t*>(base + cache->off_res_k);
+    p.res_v_w = reinterpret_cast<uint16_t*>(base + cache->off_res_v);
+    p.first_new = static_cast<int>(first_new);
+    p.res_count = static_cast<int>(T - first_new);
+    p.ctr = reinterpret_cast<unsigned*>(base + cache->off_res_v + regions(&cache->desc).res);
+    // the arrival counters are zero after every flush; set them on the first append
+    if (cache->quantized_len == 0 && r == 0 &&
+        cudaMemsetAsync(p.ctr, 0, static_cast<size_t>(units_of(cache)) * 4, s) != cudaSuccess)
+      return KVQ_ERR_CUDA;
     if (launch_flush(p, s) != cudaSuccess) return KVQ_ERR_CUDA;
   }
   const long long first_new = std::max(r, f * G);
   const long long count = T - first_new;
-  if (count > 0 && f != 1) {
+  if (count > 0 && f == 0) {
     ResidualWriteParams w{};
     w.res_k = reinterpret_cast<uint16_t*>(base + cache->off_res_k);
     w.res_v = reinterpret_cast<uint16_t*>(base + cache->off_res_v);

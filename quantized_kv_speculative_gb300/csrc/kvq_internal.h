@@ -90,12 +90,35 @@ struct FlushParams {
   long long C, Lq;          // Lq before this call
   int r, res_start, n;      // residual state before this call, tokens in this call
   int nflush;               // groups quantized by this launch
-  // new tokens written into the residual buffer by the same launch (only
-  // with nflush == 1, after each CTA has read its head's old slots)
+  // New tokens written into the residual buffer by the same launch: the CTA
+  // that arrives last at the head's counter (after every CTA of the head has
+  // read its old slots) writes them and resets the counter.
   uint16_t* res_k_w;
   uint16_t* res_v_w;
   int first_new, res_count;
+  unsigned* ctr;            // [B * Hkv] arrival counters, zero between launches
 };
+
+// The CTAs of one flushed group: key parts over 32-channel ranges, then value
+// parts over one block of G channels (all G tokens) or, when the block is all
+// D channels, over one 32-token slab.
+struct FlushSplit {
+  int npk, npv, tv, cv;
+};
+__host__ __device__ inline FlushSplit flush_split(int D, int G) {
+  FlushSplit s{};
+  s.npk = D / 32;
+  if (D / G >= 2) {
+    s.npv = D / G;
+    s.tv = G;
+    s.cv = G;
+  } else {
+    s.npv = G / 32;
+    s.tv = 32;
+    s.cv = D;
+  }
+  return s;
+}
 
 struct ResidualWriteParams {
   uint16_t* res_k;

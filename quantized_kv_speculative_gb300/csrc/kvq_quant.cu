@@ -18,7 +18,9 @@
 namespace kvq {
 namespace {
 
-constexpr int kFlushThreads = 512;
+constexpr int kFlushThreads = 256;
+constexpr int kKeyPart = 32;             // channels of one key part
+constexpr int kStripes = kFlushThreads / (kKeyPart / 2);   // token stripes of the key statistics
 
 __device__ __forceinline__ uint32_t quant_code(float x, float mn, float inv, float levels) {
   float t = rintf(__fmul_rn(__fsub_rn(x, mn), inv));
@@ -31,113 +33,203 @@ __device__ __forceinline__ void scale_inv(float mn, float mx, float levels, floa
   inv = (scale == 0.0f) ? 0.0f : __fdiv_rn(1.0f, scale);
 }
 
-// One CTA quantizes one group of G tokens of one (b, kv head).
-// Stream position p of this call: p < r comes from the residual buffer (slot
-// (res_start + p) mod 2G), otherwise from the new tokens (index p - r).
-// Every phase spreads over all threads: key statistics by (channel pair, token
-// stripe), value statistics by (token, channel block, part of the block).
+// bf16 row of stream position pos: pos < r comes from the residual buffer (slot
+// (res_start + pos) mod 2G), otherwise from the new tokens (index pos - r).
+__device__ __forceinline__ const uint16_t* stream_row(const FlushParams& p, long long u, int pos, bool value) {
+  if (pos < p.r) {
+    const int slot = (p.res_start + pos) % (2 * p.G);
+    return (value ? p.res_v : p.res_k) + (u * 2 * p.G + slot) * p.D;
+  }
+  return (value ? p.v_new : p.k_new) + (u * p.n + (pos - p.r)) * p.D;
+}
+
+// After this CTA has read its old residual slots: arrive at the head's counter;
+// the last CTA of the head writes the new residual tokens and resets it.
+__device__ void residual_ticket(const FlushParams& p, long long u, int ncta, int* sh_flag) {
+  if (p.res_count <= 0) return;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(p.ctr + u, 1u);
+    const int last = prev == static_cast<unsigned>(ncta - 1);
+    if (last) atomicExch(p.ctr + u, 0u);
+    *sh_flag = last;
+  }
+  __syncthreads();
+  if (!*sh_flag) return;
+  __threadfence();
+  const int vec = p.D / 8;
+  const int nv = p.res_count * vec;
+  for (int e = threadIdx.x; e < 2 * nv; e += kFlushThreads) {
+    const int kv = e >= nv, e2 = kv ? e - nv : e;
+    const int j = e2 / vec, c = e2 % vec;
+    const int pos = p.first_new + j;
+    const int slot = (p.res_start + pos) % (2 * p.G);
+    const long long src = (u * p.n + (pos - p.r)) * p.D;
+    const long long dst = (u * 2 * p.G + slot) * p.D;
+    const uint16_t* from = kv ? p.v_new : p.k_new;
+    uint16_t* to = kv ? p.res_v_w : p.res_k_w;
+    reinterpret_cast<uint4*>(to + dst)[c] = reinterpret_cast<const uint4*>(from + src)[c];
+  }
+}
+
+// One CTA quantizes one part of one group of G tokens of one (b, kv head):
+// blockIdx.x = group * (npk + npv) + part.
+//  * key part: channels [32 kp, 32 kp + 32) over the G tokens; statistics by
+//    (channel pair, token stripe), combined through shared memory;
+//  * value part: one block of G channels over its tokens; statistics by
+//    (token, lanes of the block).
 template <int FMT>
 __global__ void __launch_bounds__(kFlushThreads) flush_kernel(FlushParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int sh_flag;
   const int D = p.D, G = p.G, NJ = D / G;
-  const int tid = threadIdx.x;
-  const int gi = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const FlushSplit sp = flush_split(D, G);
+  const int npart = sp.npk + sp.npv;
+  const int gi = blockIdx.x / npart, part = blockIdx.x % npart;
+  const int kvh = blockIdx.y, b = blockIdx.z;
   const long long u = static_cast<long long>(b) * p.Hkv + kvh;
-  uint16_t* Ks = reinterpret_cast<uint16_t*>(smem);            // [G][D]
-  uint16_t* Vs = Ks + G * D;                                    // [G][D]
-  float* kmn = reinterpret_cast<float*>(Vs + G * D);            // [D]
-  float* kinv = kmn + D;                                        // [D]
-  float* vmn = kinv + D;                                        // [G][NJ]
-  float* vinv = vmn + G * NJ;                                   // [G][NJ]
-  float* part = vinv + G * NJ;                                  // [2][kFlushThreads * 2] stripe min/max
-
-  // ---- gather the group's G source tokens (16-byte vectors, 4 in flight per thread) ----
-  const int vec_per_tok = D / 8;
-  const int nvec = G * vec_per_tok;
-  for (int e0 = tid; e0 < nvec; e0 += 4 * kFlushThreads) {
-    uint4 kv[4], vv[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + j * kFlushThreads;
-      if (e < nvec) {
-        const int i = e / vec_per_tok, c = e % vec_per_tok;
-        const int pos = gi * G + i;
-        long long off;
-        const uint16_t *sk, *sv;
-        if (pos < p.r) {
-          const int slot = (p.res_start + pos) % (2 * G);
-          off = (u * 2 * G + slot) * D;
-          sk = p.res_k;
-          sv = p.res_v;
-        } else {
-          off = (u * p.n + (pos - p.r)) * D;
-          sk = p.k_new;
-          sv = p.v_new;
-        }
-        kv[j] = reinterpret_cast<const uint4*>(sk + off)[c];
-        vv[j] = reinterpret_cast<const uint4*>(sv + off)[c];
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + j * kFlushThreads;
-      if (e < nvec) {
-        reinterpret_cast<uint4*>(Ks)[e] = kv[j];
-        reinterpret_cast<uint4*>(Vs)[e] = vv[j];
-      }
-    }
-  }
-  __syncthreads();
-  // A single flushed group reads this head's old slots only in the gather
-  // above, so the new tokens that stay in the buffer can be written now.
-  if (p.res_count > 0) {
-    const int nv = p.res_count * vec_per_tok;
-    for (int e = tid; e < 2 * nv; e += kFlushThreads) {
-      const int kv = e >= nv, e2 = kv ? e - nv : e;
-      const int j = e2 / vec_per_tok, c = e2 % vec_per_tok;
-      const int pos = p.first_new + j;
-      const int slot = (p.res_start + pos) % (2 * G);
-      const long long src = (u * p.n + (pos - p.r)) * D;
-      const long long dst = (u * 2 * G + slot) * D;
-      const uint16_t* from = kv ? p.v_new : p.k_new;
-      uint16_t* to = kv ? p.res_v_w : p.res_k_w;
-      reinterpret_cast<uint4*>(to + dst)[c] = reinterpret_cast<const uint4*>(from + src)[c];
-    }
-  }
-
+  const int tid = threadIdx.x;
   constexpr int BITS = FMT;  // 8, 2 or 1
   const float levels = static_cast<float>((1 << BITS) - 1);
   const long long grp = p.Lq / G + gi;       // global group index
   const long long tok0 = p.Lq + static_cast<long long>(gi) * G;
   const float pinf = __int_as_float(0x7f800000);
 
-  // ---- key statistics: per channel over the G tokens ----
-  // thread = (channel pair cp, token stripe st); stripes combine through shared memory
-  {
-    const int npair = D / 2, nst = kFlushThreads / npair;   // 4 stripes (D=128) or 8 (D=64)
-    const int cp = tid % npair, st = tid / npair;
-    float mn0 = pinf, mx0 = -pinf, mn1 = pinf, mx1 = -pinf;
-    for (int i = st; i < G; i += nst) {
-      const uint32_t w = reinterpret_cast<const uint32_t*>(Ks + i * D)[cp];
-      const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
-      mn0 = fminf(mn0, x0); mx0 = fmaxf(mx0, x0);
-      mn1 = fminf(mn1, x1); mx1 = fmaxf(mx1, x1);
+  if (part < sp.npk) {
+    // ---------------- key part ----------------
+    const int c0 = part * kKeyPart;
+    uint16_t* Ks = reinterpret_cast<uint16_t*>(smem);              // [G][32]
+    float* pmn = reinterpret_cast<float*>(Ks + G * kKeyPart);      // [kStripes][32]
+    float* pmx = pmn + kStripes * kKeyPart;                        // [kStripes][32]
+    float* kmn = pmx + kStripes * kKeyPart;                        // [32]
+    float* kinv = kmn + kKeyPart;                                  // [32]
+    // gather: 4 vectors per token, all in flight (G * 4 <= 2 * kFlushThreads)
+    {
+      uint4 v[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = tid + h * kFlushThreads;
+        if (e < G * 4) v[h] = reinterpret_cast<const uint4*>(stream_row(p, u, gi * G + e / 4, false) + c0)[e % 4];
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = tid + h * kFlushThreads;
+        if (e < G * 4) reinterpret_cast<uint4*>(Ks)[e] = v[h];
+      }
     }
-    part[st * D + 2 * cp] = mn0;
-    part[st * D + 2 * cp + 1] = mn1;
-    part[kFlushThreads * 2 + st * D + 2 * cp] = mx0;
-    part[kFlushThreads * 2 + st * D + 2 * cp + 1] = mx1;
+    residual_ticket(p, u, p.nflush * npart, &sh_flag);
+    __syncthreads();
+    {
+      const int cp = tid % (kKeyPart / 2), st = tid / (kKeyPart / 2);
+      float mn0 = pinf, mx0 = -pinf, mn1 = pinf, mx1 = -pinf;
+      for (int i = st; i < G; i += kStripes) {
+        const uint32_t w = reinterpret_cast<const uint32_t*>(Ks + i * kKeyPart)[cp];
+        const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
+        mn0 = fminf(mn0, x0); mx0 = fmaxf(mx0, x0);
+        mn1 = fminf(mn1, x1); mx1 = fmaxf(mx1, x1);
+      }
+      pmn[st * kKeyPart + 2 * cp] = mn0;
+      pmn[st * kKeyPart + 2 * cp + 1] = mn1;
+      pmx[st * kKeyPart + 2 * cp] = mx0;
+      pmx[st * kKeyPart + 2 * cp + 1] = mx1;
+    }
+    __syncthreads();
+    if (tid < kKeyPart) {
+      float mn = pmn[tid], mx = pmx[tid];
+      for (int s2 = 1; s2 < kStripes; ++s2) {
+        mn = fminf(mn, pmn[s2 * kKeyPart + tid]);
+        mx = fmaxf(mx, pmx[s2 * kKeyPart + tid]);
+      }
+      mn = __fadd_rn(mn, 0.0f);
+      mx = __fadd_rn(mx, 0.0f);
+      float scale, inv;
+      scale_inv(mn, mx, levels, scale, inv);
+      kmn[tid] = mn;
+      kinv[tid] = inv;
+      float* dst = p.ksz + (u * (p.C / G) + grp) * 2 * D;
+      dst[c0 + tid] = scale;
+      dst[D + c0 + tid] = mn;
+    }
+    __syncthreads();
+    // ---- key codes: token-major rows, channels packed ----
+    if constexpr (FMT == KVQ_FMT_HIER8) {
+      // one 32-bit word of both nibble planes = 8 channels; 4 words per token
+      for (int e = tid; e < G * 4; e += kFlushThreads) {
+        const int i = e / 4, w = e % 4;
+        const uint4 x = reinterpret_cast<const uint4*>(Ks + i * kKeyPart)[w];
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+        uint32_t hi = 0, lo = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int d = 8 * w + k;
+          const uint32_t xb = (k & 1) ? (xs[k / 2] & 0xFFFF0000u) : (xs[k / 2] << 16);
+          const uint32_t c = quant_code(__uint_as_float(xb), kmn[d], kinv[d], levels);
+          hi |= (c >> 4) << (4 * k);
+          lo |= (c & 15u) << (4 * k);
+        }
+        const long long row = (u * p.C + tok0 + i) * (D / 2);
+        reinterpret_cast<uint32_t*>(p.kplane[0] + row)[c0 / 8 + w] = hi;
+        reinterpret_cast<uint32_t*>(p.kplane[1] + row)[c0 / 8 + w] = lo;
+      }
+    } else {
+      constexpr int PER = 8 / BITS;             // codes per byte
+      constexpr int CPW = 4 * PER;              // codes per 32-bit word (16 or 32)
+      constexpr int WPT = kKeyPart / CPW;       // words of this part per token
+      const int rowbytes = D * BITS / 8;
+      for (int e = tid; e < G * WPT; e += kFlushThreads) {
+        const int i = e / WPT, w = e % WPT;
+        uint32_t v = 0;
+#pragma unroll
+        for (int k8 = 0; k8 < CPW; k8 += 8) {
+          const uint4 x = reinterpret_cast<const uint4*>(Ks + i * kKeyPart + CPW * w + k8)[0];
+          const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int d = CPW * w + k8 + k;
+            const uint32_t xb = (k & 1) ? (xs[k / 2] & 0xFFFF0000u) : (xs[k / 2] << 16);
+            v |= quant_code(__uint_as_float(xb), kmn[d], kinv[d], levels) << (BITS * (k8 + k));
+          }
+        }
+        reinterpret_cast<uint32_t*>(p.kplane[0] + (u * p.C + tok0 + i) * rowbytes)[c0 / CPW + w] = v;
+      }
+    }
+    return;
   }
-  // ---- value statistics: per token over each block of G channels ----
-  // item = (token i, block jv), D items; `per` adjacent lanes per item, each
-  // over a multiple of 8 channels
+
+  // ---------------- value part ----------------
+  const int vp = part - sp.npk;
+  const int TV = sp.tv, CV = sp.cv;
+  const int t0v = (NJ >= 2) ? 0 : 32 * vp;          // first token of the part (group-relative)
+  const int c0v = (NJ >= 2) ? G * vp : 0;           // first channel (= its block's)
+  const int jv = c0v / G;
+  uint16_t* Vs = reinterpret_cast<uint16_t*>(smem);  // [TV][CV]
+  float* vmn = reinterpret_cast<float*>(Vs + TV * CV);
+  float* vinv = vmn + TV;
   {
-    const int per = min(kFlushThreads / D, G / 8);
-    const int item = tid / per, sub = tid % per;
-    const int i = item / NJ, jv = item % NJ;
-    const int cw = G / per;
-    const bool active = item < D;
-    const uint16_t* src = Vs + (active ? i * D + jv * G + sub * cw : 0);
+    // gather: TV * CV / 8 <= 2 * kFlushThreads vectors, all in flight
+    const int vpt = CV / 8;
+    uint4 v[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = tid + h * kFlushThreads;
+      if (e < TV * vpt) v[h] = reinterpret_cast<const uint4*>(stream_row(p, u, gi * G + t0v + e / vpt, true) + c0v)[e % vpt];
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = tid + h * kFlushThreads;
+      if (e < TV * vpt) reinterpret_cast<uint4*>(Vs)[e] = v[h];
+    }
+  }
+  residual_ticket(p, u, p.nflush * npart, &sh_flag);
+  __syncthreads();
+  // ---- statistics: per token over the block; `per` adjacent lanes per token ----
+  {
+    const int per = min(kFlushThreads / TV, CV / 8);
+    const int i = tid / per, sub = tid % per;
+    const int cw = CV / per;
+    const bool active = i < TV;
+    const uint16_t* src = Vs + (active ? i * CV + sub * cw : 0);
     float mn = pinf, mx = -pinf;
     for (int c = 0; active && c < cw; c += 8) {
       const uint4 w = *reinterpret_cast<const uint4*>(src + c);
@@ -158,96 +250,31 @@ __global__ void __launch_bounds__(kFlushThreads) flush_kernel(FlushParams p) {
       mx = __fadd_rn(mx, 0.0f);
       float scale, inv;
       scale_inv(mn, mx, levels, scale, inv);
-      vmn[i * NJ + jv] = mn;
-      vinv[i * NJ + jv] = inv;
-      float* dst = p.vsz + (u * p.C + tok0 + i) * 2 * NJ;
+      vmn[i] = mn;
+      vinv[i] = inv;
+      float* dst = p.vsz + (u * p.C + tok0 + t0v + i) * 2 * NJ;
       dst[jv] = scale;
       dst[NJ + jv] = mn;
     }
   }
   __syncthreads();
-  if (tid < D) {
-    const int nst = kFlushThreads / (D / 2);
-    float mn = part[tid], mx = part[kFlushThreads * 2 + tid];
-    for (int s2 = 1; s2 < nst; ++s2) {
-      mn = fminf(mn, part[s2 * D + tid]);
-      mx = fmaxf(mx, part[kFlushThreads * 2 + s2 * D + tid]);
-    }
-    mn = __fadd_rn(mn, 0.0f);
-    mx = __fadd_rn(mx, 0.0f);
-    float scale, inv;
-    scale_inv(mn, mx, levels, scale, inv);
-    kmn[tid] = mn;
-    kinv[tid] = inv;
-    float* dst = p.ksz + (u * (p.C / G) + grp) * 2 * D;
-    dst[tid] = scale;
-    dst[D + tid] = mn;
-  }
-  __syncthreads();
-
-  // ---- key codes: token-major rows, channels packed (8/pb per byte) ----
-  if constexpr (FMT == KVQ_FMT_HIER8) {
-    // Each thread writes one 32-bit word of both nibble planes: 8 channels.
-    const int words = D / 8;
-    for (int e = tid; e < G * words; e += kFlushThreads) {
-      const int i = e / words, w = e % words;
-      const uint4 x = reinterpret_cast<const uint4*>(Ks + i * D)[w];
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-      uint32_t hi = 0, lo = 0;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int d = 8 * w + k;
-        const uint32_t xb = (k & 1) ? (xs[k / 2] & 0xFFFF0000u) : (xs[k / 2] << 16);
-        const uint32_t c = quant_code(__uint_as_float(xb), kmn[d], kinv[d], levels);
-        hi |= (c >> 4) << (4 * k);
-        lo |= (c & 15u) << (4 * k);
-      }
-      const long long row = (u * p.C + tok0 + i) * (D / 2);
-      reinterpret_cast<uint32_t*>(p.kplane[0] + row)[w] = hi;
-      reinterpret_cast<uint32_t*>(p.kplane[1] + row)[w] = lo;
-    }
-  } else {
-    constexpr int PER = 8 / BITS;             // codes per byte
-    constexpr int CPW = 4 * PER;              // codes per 32-bit word
-    const int words = D / CPW;                // 2-bit: D/16, 1-bit: D/32
-    const int rowbytes = D * BITS / 8;
-    for (int e = tid; e < G * words; e += kFlushThreads) {
-      const int i = e / words, w = e % words;
-      uint32_t v = 0;
-#pragma unroll
-      for (int k8 = 0; k8 < CPW; k8 += 8) {
-        const uint4 x = reinterpret_cast<const uint4*>(Ks + i * D + CPW * w + k8)[0];
-        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int d = CPW * w + k8 + k;
-          const uint32_t xb = (k & 1) ? (xs[k / 2] & 0xFFFF0000u) : (xs[k / 2] << 16);
-          v |= quant_code(__uint_as_float(xb), kmn[d], kinv[d], levels) << (BITS * (k8 + k));
-        }
-      }
-      reinterpret_cast<uint32_t*>(p.kplane[0] + (u * p.C + tok0 + i) * rowbytes)[w] = v;
-    }
-  }
-
   // ---- value codes: 32-token slabs, rows = channels, tokens packed ----
   {
-    const int nslab = G / 32;
-    const long long slab0 = (u * p.C + tok0) / 32;
+    const int nslab = TV / 32;
+    const long long slab0 = (u * p.C + tok0 + t0v) / 32;
     if constexpr (FMT == KVQ_FMT_HIER8) {
       // row = 16 bytes per plane = 4 words; word w holds tokens 8w..8w+7
-      for (int e = tid; e < nslab * 4 * D; e += kFlushThreads) {
-        const int d = e % D, w = (e / D) % 4, s = e / (4 * D);
-        const int jv = d / G;
+      for (int e = tid; e < nslab * 4 * CV; e += kFlushThreads) {
+        const int d = e % CV, w = (e / CV) % 4, s = e / (4 * CV);
         uint32_t hi = 0, lo = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int i = 32 * s + 8 * w + k;
-          const uint32_t c =
-              quant_code(bf16_to_f32(Vs[i * D + d]), vmn[i * NJ + jv], vinv[i * NJ + jv], levels);
+          const uint32_t c = quant_code(bf16_to_f32(Vs[i * CV + d]), vmn[i], vinv[i], levels);
           hi |= (c >> 4) << (4 * k);
           lo |= (c & 15u) << (4 * k);
         }
-        const long long off = ((slab0 + s) * D + d) * 16;
+        const long long off = ((slab0 + s) * D + c0v + d) * 16;
         reinterpret_cast<uint32_t*>(p.vplane[0] + off)[w] = hi;
         reinterpret_cast<uint32_t*>(p.vplane[1] + off)[w] = lo;
       }
@@ -256,17 +283,15 @@ __global__ void __launch_bounds__(kFlushThreads) flush_kernel(FlushParams p) {
       constexpr int CPW = 4 * PER;            // tokens per word
       constexpr int WPR = 32 / CPW;           // words per slab row (2-bit: 2, 1-bit: 1)
       constexpr int ROWB = 32 * BITS / 8;
-      for (int e = tid; e < nslab * WPR * D; e += kFlushThreads) {
-        const int d = e % D, w = (e / D) % WPR, s = e / (WPR * D);
-        const int jv = d / G;
+      for (int e = tid; e < nslab * WPR * CV; e += kFlushThreads) {
+        const int d = e % CV, w = (e / CV) % WPR, s = e / (WPR * CV);
         uint32_t v = 0;
 #pragma unroll
         for (int k = 0; k < CPW; ++k) {
           const int i = 32 * s + CPW * w + k;
-          v |= quant_code(bf16_to_f32(Vs[i * D + d]), vmn[i * NJ + jv], vinv[i * NJ + jv], levels)
-               << (BITS * k);
+          v |= quant_code(bf16_to_f32(Vs[i * CV + d]), vmn[i], vinv[i], levels) << (BITS * k);
         }
-        reinterpret_cast<uint32_t*>(p.vplane[0] + ((slab0 + s) * D + d) * ROWB)[w] = v;
+        reinterpret_cast<uint32_t*>(p.vplane[0] + ((slab0 + s) * D + c0v + d) * ROWB)[w] = v;
       }
     }
   }
@@ -293,11 +318,13 @@ __global__ void residual_write_kernel(ResidualWriteParams p) {
 
 template <int FMT>
 cudaError_t launch_flush_t(const FlushParams& p, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(2) * p.G * p.D * sizeof(uint16_t) +
-                      (2 * p.D + 2 * p.G * (p.D / p.G) + 4 * kFlushThreads) * sizeof(float);
+  const FlushSplit sp = flush_split(p.D, p.G);
+  const size_t key_smem = static_cast<size_t>(p.G) * kKeyPart * 2 + (2 * kStripes + 2) * kKeyPart * 4;
+  const size_t val_smem = static_cast<size_t>(sp.tv) * sp.cv * 2 + 2 * sp.tv * 4;
+  const size_t smem = key_smem > val_smem ? key_smem : val_smem;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&flush_kernel<FMT>), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(p.nflush, p.Hkv, p.B);
+  dim3 grid(p.nflush * (sp.npk + sp.npv), p.Hkv, p.B);
   flush_kernel<FMT><<<grid, kFlushThreads, smem, s>>>(p);
   return cudaGetLastError();
 }

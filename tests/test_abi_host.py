@@ -76,9 +76,11 @@ def _desc(**kw):
 def test_cache_bytes_and_validation(lib):
     good = _desc()
     n = lib.kvq_cache_bytes(ctypes.byref(good))
-    # 2 key + 2 value nibble planes, key/value scale+zero, 2 residual buffers (each 256-aligned)
+    # 2 key + 2 value nibble planes, key/value scale+zero, 2 residual buffers, the
+    # per-head flush counters (each region 256-aligned)
     U, C, D, G = 4, 512, 64, 32
-    expect = 4 * U * C * D // 2 + U * (C // G) * 2 * D * 4 + U * C * 2 * (D // G) * 4 + 2 * U * 2 * G * D * 2
+    expect = (4 * U * C * D // 2 + U * (C // G) * 2 * D * 4 + U * C * 2 * (D // G) * 4 + 2 * U * 2 * G * D * 2
+              + 256)
     assert n == expect
     for bad in [_desc(head_dim=96), _desc(group_size=16), _desc(group_size=128), _desc(format=4),
                 _desc(capacity_tokens=100), _desc(batch=0), _desc(reserved0=1)]:
