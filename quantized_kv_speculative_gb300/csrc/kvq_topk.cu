@@ -54,8 +54,8 @@ struct TopkSmem {
   static constexpr int SLOT = KSZ_OFF + KSZ_BYTES;
   static constexpr int QS_OFF = NSLOT * SLOT;                 // qs[D]
   static constexpr int WB_OFF = QS_OFF + D * 4;               // per warp: W halves in pair order [2][D] f16
-  static constexpr int HIST_OFF = WB_OFF + NW * 2 * D * 2;    // hist[256]
-  static constexpr int LIST_OFF = HIST_OFF + 256 * 4;         // gathered keys [kGather]
+  static constexpr int HIST_OFF = WB_OFF + NW * 2 * D * 2;    // hist[NW][256]: one per warp
+  static constexpr int LIST_OFF = HIST_OFF + NW * 256 * 4;    // gathered keys [kGather]
   static constexpr int RED_OFF = LIST_OFF + kGather * 4;      // per-warp min/max, counts [2 NW]
   static constexpr int BAR_OFF = RED_OFF + 2 * NW * 4;
   static constexpr int MISC_OFF = BAR_OFF + NSLOT * 8;
@@ -111,8 +111,9 @@ __device__ __forceinline__ int pair_slot(int local) {
 // Block-wide selection of the kth largest key among the i < n for which
 // take(i, key) holds (1 <= kth <= number taken).  On return st[0] = T and
 // st[2] = how many of the taken keys equal to T belong to the kth largest.
-// Every thread of the block calls it.  hist[256], list[kGather], red[2 NW] and
-// st[0..4] are shared memory.
+// Every thread of the block calls it.  hist[NW][256] (one histogram per warp,
+// so that keys crowding into a few bins do not serialize across warps),
+// list[kGather], red[2 NW] and st[0..4] are shared memory.
 template <typename F>
 __device__ void select_kth(int n, int kth, F take, uint32_t* hist, uint32_t* list, uint32_t* red, int* st) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -135,7 +136,7 @@ __device__ void select_kth(int n, int kth, F take, uint32_t* hist, uint32_t* lis
     red[2 * warp] = lo;
     red[2 * warp + 1] = hi;
   }
-  for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0u;
+  for (int i = tid; i < NW * 256; i += blockDim.x) hist[i] = 0u;
   if (tid == 0) st[4] = 0;
   __syncthreads();
   lo = red[0];
@@ -160,9 +161,16 @@ __device__ void select_kth(int n, int kth, F take, uint32_t* hist, uint32_t* lis
   int remaining = kth;
   while (true) {
     // ---- histogram of the 8 bits at `shift` among keys matching the prefix ----
+    uint32_t* hw = hist + warp * 256;
     for (int i = tid; i < n; i += blockDim.x) {
       uint32_t key;
-      if (take(i, key) && (key & mask) == prefix) atomicAdd(hist + ((key >> shift) & 255u), 1u);
+      if (take(i, key) && (key & mask) == prefix) atomicAdd(hw + ((key >> shift) & 255u), 1u);
+    }
+    __syncthreads();
+    for (int bn = tid; bn < 256; bn += blockDim.x) {   // per-warp histograms -> hist[0]
+      uint32_t c = hist[bn];
+      for (int w = 1; w < nw; ++w) c += hist[w * 256 + bn];
+      hist[bn] = c;
     }
     __syncthreads();
     if (warp == 0) {
@@ -207,7 +215,7 @@ __device__ void select_kth(int n, int kth, F take, uint32_t* hist, uint32_t* lis
     const int bin = st[3];
     prefix |= digit << shift;
     mask |= 255u << shift;
-    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0u;
+    for (int i = tid; i < NW * 256; i += blockDim.x) hist[i] = 0u;
     if (shift == 0) {  // the key is fully determined
       __syncthreads();
       if (tid == 0) {
@@ -455,33 +463,41 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
     __syncthreads();
     if (tid == 0) st[3] = 0;
     __syncthreads();
-    const int nround = (n + blockDim.x - 1) / blockDim.x * blockDim.x;
-    for (int i = tid; i < nround; i += blockDim.x) {
-      const uint32_t key = (i < n) ? okeys[i] : 0u;
-      const bool sel = (i < n) && key > T;
+    // Keys above T go anywhere in [0, n_gt); the need_eq ties at T are the
+    // lowest indices: each warp scans a contiguous segment, counts its ties,
+    // and places its own after those of the warps before it.
+    const int seg = (n + NW - 1) / NW;
+    const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
+    int myeq = 0;
+    for (int base = s0; base < s1; base += 32) {
+      const int i = base + lane;
+      const uint32_t key = (i < s1) ? okeys[i] : 0u;
+      const bool sel = (i < s1) && key > T;
       const uint32_t bal = __ballot_sync(0xffffffffu, sel);
-      int base = 0;
-      if (lane == 0 && bal) base = atomicAdd(st + 3, __popc(bal));
-      base = __shfl_sync(0xffffffffu, base, 0);
+      myeq += __popc(__ballot_sync(0xffffffffu, (i < s1) && key == T));
+      int pbase = 0;
+      if (lane == 0 && bal) pbase = atomicAdd(st + 3, __popc(bal));
+      pbase = __shfl_sync(0xffffffffu, pbase, 0);
       if (sel) {
-        const int pos = base + __popc(bal & ((1u << lane) - 1u));
+        const int pos = pbase + __popc(bal & ((1u << lane) - 1u));
         cs[pos] = key_to_score(key);
         ci[pos] = static_cast<int32_t>(t_begin + i);
       }
     }
-    if (warp == 0) {  // ties at T: lowest indices first
-      int taken = 0;
-      for (int base = 0; base < n && taken < need_eq; base += 32) {
-        const int i = base + lane;
-        const bool eq = (i < n) && (okeys[i] == T);
-        const uint32_t bal = __ballot_sync(0xffffffffu, eq);
-        const int before = __popc(bal & ((1u << lane) - 1u));
-        if (eq && taken + before < need_eq) {
-          cs[n_gt + taken + before] = key_to_score(T);
-          ci[n_gt + taken + before] = static_cast<int32_t>(t_begin + i);
-        }
-        taken += __popc(bal);
+    if (lane == 0) red[warp] = static_cast<uint32_t>(myeq);
+    __syncthreads();
+    int taken = 0;
+    for (int w = 0; w < warp; ++w) taken += static_cast<int>(red[w]);
+    for (int base = s0; base < s1 && taken < need_eq; base += 32) {
+      const int i = base + lane;
+      const bool eq = (i < s1) && (okeys[i] == T);
+      const uint32_t bal = __ballot_sync(0xffffffffu, eq);
+      const int before = __popc(bal & ((1u << lane) - 1u));
+      if (eq && taken + before < need_eq) {
+        cs[n_gt + taken + before] = key_to_score(T);
+        ci[n_gt + taken + before] = static_cast<int32_t>(t_begin + i);
       }
+      taken += __popc(bal);
     }
   }
   for (int i = keff + tid; i < K; i += blockDim.x) {
