@@ -592,6 +592,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
     if (lane == 0) reinterpret_cast<float*>(smem + L::SRC_OFF + NW * 48)[warp] = qm;
   }
   if (has_sel) {
+    __syncthreads();   // the bitmap is clear before any bit is set (has_sel is uniform)
     for (int j = tid; j < p.top_k; j += blockDim.x) {
       const long long idx = p.sel_idx[u * p.top_k + j];
       if (idx >= t_begin && idx < t_end) {

@@ -147,6 +147,32 @@ def test_attend_deterministic_and_split_independent():
     assert kvq.kvq_workspace_status(ws) == 0
 
 
+def test_selection_calls_deterministic():
+    """Top-k and attention with selected 16-bit tokens over many CTAs: repeated
+    calls give identical bytes (no call depends on thread timing)."""
+    B, Hkv, Hq, D, G, N, k = 8, 8, 32, 128, 32, 8192 + 40, 64
+    K, V = ki.kv_stream_torch(13, B, Hkv, N, D)
+    gc = kvq.QuantizedKVCache(B, Hkv, D, G, "int2", 8192 + 2 * G)
+    kvq.kvq_quantize_append(gc, K, V)
+    q = dev(ki.queries(13, B, 2, Hq, D))
+    pk, pv = (dev(x) for x in ki.pending(13, B, Hkv, 2, D))
+    ws = kvq.make_workspace(gc, Hq, 2, k)
+    idx0, sc0 = kvq.kvq_topk(gc, "int2", q[:, 1].contiguous(), k, workspace=ws)
+    gi = idx0.long().clamp_min(0)[..., None].expand(-1, -1, -1, D)
+    sk, sv = torch.gather(K, 2, gi).contiguous(), torch.gather(V, 2, gi).contiguous()
+    outs = []
+    for _ in range(5):
+        idx, sc = kvq.kvq_topk(gc, "int2", q[:, 1].contiguous(), k, workspace=ws)
+        assert torch.equal(idx, idx0) and torch.equal(sc.view(torch.int32), sc0.view(torch.int32))
+        o, l = kvq.kvq_attend(gc, "int2", q, pk, pv, idx0, sk, sv, workspace=ws)
+        outs.append((o.clone(), l.clone()))
+    torch.cuda.synchronize()
+    for o, l in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0][0].view(torch.int16))
+        assert torch.equal(l.view(torch.int32), outs[0][1].view(torch.int32))
+    assert kvq.kvq_workspace_status(ws) == 0
+
+
 def test_attend_edge_cases():
     """An empty cache gives out 0 and lse -inf.  Residual only (Lq = 0);
     pending == gamma; selected entries all padding; k > Lq."""
