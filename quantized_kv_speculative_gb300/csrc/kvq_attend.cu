@@ -46,14 +46,15 @@ constexpr int kSmemPerSm = 228 * 1024;
 template <int MODE, int D, int NJ, int NT>
 struct Smem;
 
-// Target CTAs per SM: four with one weight n-tile (rows <= 4); with two n-tiles
-// three when their shared memory fits, else two (which also frees registers).
+// Target CTAs per SM: with one weight n-tile (rows <= 4) as many as fit, up to
+// four; with two n-tiles three when their shared memory fits, else two (which
+// also frees registers).
 template <int MODE, int D, int NJ, int NT>
 constexpr int target_ctas() {
+  constexpr int need = Smem<MODE, D, NJ, NT>::MIN_TOTAL + 1024;
   if constexpr (NT == 1) {
-    return 4;
+    return 4 * need <= 228 * 1024 ? 4 : (3 * need <= 228 * 1024 ? 3 : 2);
   } else {
-    constexpr int need = Smem<MODE, D, NJ, NT>::MIN_TOTAL + 1024;
     return 3 * need <= 228 * 1024 ? 3 : 2;
   }
 }
