@@ -118,6 +118,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// True when the second half of a lane chunk's key pairs uses the first half's
+// channels shifted by one constant (the eight-row weight setup splits the pairs
+// between two lanes that way).
+template <int MODE, int D>
+__host__ __device__ constexpr bool halves_shift() {
+  constexpr int HP = D / 16;
+  for (int k = 0; k < HP; ++k)
+    for (int e = 0; e < 2; ++e)
+      if (kx_chan<MODE, D>(HP + k, e) != kx_chan<MODE, D>(k, e) + kx_chan<MODE, D>(HP, 0)) return false;
+  return kx_chan<MODE, D>(0, 0) == 0;
+}
+
 // Scaled queries q~ = q * sm_scale * log2(e) of unit (b, kvh) into qt [8][D]
 // (rows >= R zero): one 16-byte load of 8 channels per thread, all in flight
 // at once.  Returns the thread's max |q~|.
@@ -690,20 +702,25 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
           float wsum = 0.f, zsum = 0.f;
           float kscale_new, E2;
           if constexpr (NT == 2) {
-            // eight rows: each lane derives its own B fragments (column g of both
-            // n-tiles for channel chunk q); the high-part lane and the low-part
-            // lane of a row both compute the row's weights
-            const float* ksc = ks + q * (D / 4);
-            const float* kzc = kz + q * (D / 4);
-            float kv[D / 4];
-#pragma unroll
-            for (int c4 = 0; c4 < D / 16; ++c4) {
-              const float4 a4 = *reinterpret_cast<const float4*>(ksc + 4 * c4);
-              kv[4 * c4] = a4.x; kv[4 * c4 + 1] = a4.y; kv[4 * c4 + 2] = a4.z; kv[4 * c4 + 3] = a4.w;
-            }
+            // eight rows: lanes g = 2r and 2r + 1 hold the high and the low
+            // part of row 4nt + r (column g).  Each derives both parts for half
+            // of its chunk's channel pairs, and the two swap the part the other
+            // one keeps.
+            constexpr int HP = D / 16;                        // pairs per half chunk
+            constexpr int DELTA = kx_chan<MODE, D>(HP, 0);    // channel offset of the second half
+            static_assert(halves_shift<MODE, D>(), "the second half's pairs are the first half's, shifted");
+            const int cb = q * (D / 4) + par * DELTA;         // this lane's channel base
+            const float* ksc = ks + cb;
+            const float* kzc = kz + cb;
+            float kv[HP][2];
             float smax = 0.f;
 #pragma unroll
-            for (int c = 0; c < D / 4; ++c) smax = fmaxf(smax, kv[c]);
+            for (int k = 0; k < HP; ++k) {
+              kv[k][0] = ksc[kx_chan<MODE, D>(k, 0)];
+              kv[k][1] = ksc[kx_chan<MODE, D>(k, 1)];
+              smax = fmaxf(smax, fmaxf(kv[k][0], kv[k][1]));
+            }
+            smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 4));
             smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1));
             smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 2));
             const float bound = qmax * smax * KW;
@@ -712,28 +729,36 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
             kscale_new = pow2i(-e);
             const float f = E2 * KW;
 #pragma unroll
-            for (int c = 0; c < D / 4; ++c) kv[c] *= f;
+            for (int k = 0; k < HP; ++k) {
+              kv[k][0] *= f;
+              kv[k][1] *= f;
+            }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              const float* qr = qt + (4 * nt + (g >> 1)) * D + q * (D / 4);
+              const float* qr = qt + (4 * nt + (g >> 1)) * D + cb;
               float ws = 0.f, zs = 0.f;
+              uint32_t keep[HP], send[HP];
 #pragma unroll
-              for (int c4 = 0; c4 < D / 16; ++c4) {
-                const float4 q4 = *reinterpret_cast<const float4*>(qr + 4 * c4);
-                const float4 z4 = *reinterpret_cast<const float4*>(kzc + 4 * c4);
-                zs = fmaf(q4.x, z4.x, fmaf(q4.y, z4.y, fmaf(q4.z, z4.z, fmaf(q4.w, z4.w, zs))));
-              }
-#pragma unroll
-              for (int pp = 0; pp < D / 8; ++pp) {
-                const int c0 = kx_chan<MODE, D>(pp, 0), c1 = kx_chan<MODE, D>(pp, 1);
-                const float w0 = qr[c0] * kv[c0], w1 = qr[c1] * kv[c1];
+              for (int k = 0; k < HP; ++k) {
+                const int c0 = kx_chan<MODE, D>(k, 0), c1 = kx_chan<MODE, D>(k, 1);
+                const float q0 = qr[c0], q1 = qr[c1];
+                zs = fmaf(q0, kzc[c0], fmaf(q1, kzc[c1], zs));
+                const float w0 = q0 * kv[k][0], w1 = q1 * kv[k][1];
                 const uint32_t hi = pack_half2(w0, w1);
                 const float2 hf = unpack_half2(hi);
                 const uint32_t lo = pack_half2(w0 - hf.x, w1 - hf.y);
-                W[nt][pp] = par ? lo : hi;
+                keep[k] = par ? lo : hi;
+                send[k] = par ? hi : lo;
                 ws += w0 + w1;
               }
+#pragma unroll
+              for (int k = 0; k < HP; ++k) {
+                const uint32_t recv = __shfl_xor_sync(0xffffffffu, send[k], 4);
+                W[nt][k] = par ? recv : keep[k];
+                W[nt][HP + k] = par ? keep[k] : recv;
+              }
               float cwn = fmaf(zs, E2, -kx_offset<MODE>() * ws);
+              cwn += __shfl_xor_sync(0xffffffffu, cwn, 4);
               cwn += __shfl_xor_sync(0xffffffffu, cwn, 1);
               cwn += __shfl_xor_sync(0xffffffffu, cwn, 2);
               // this lane's C rows belong to row 4nt + q, whose weights lanes g = 2q hold
