@@ -20,10 +20,11 @@
 //
 // One launch: B*Hkv*S CTAs, with S chosen on the host to balance waves against
 // the merge.  Each CTA scores one chunk (bulk-copied tiles on an mbarrier ring,
-// as in attention) into 32-bit order keys and selects its top k by (score desc,
-// index asc).  The last CTA of each (b, kvh), found through an atomic ticket,
-// selects the k best of the S*k candidates under the unique composite key
-// (order key, ~index), then places each winner by counting the winners above it.
+// as in attention) into 32-bit order keys, selects its top k by (score desc,
+// index asc) and writes them in descending order of the unique composite key
+// (order key, ~index).  The last CTA of each (b, kvh), found through an atomic
+// ticket, merges the S sorted lists pairwise (merge path: each output position
+// finds its split by binary search), keeping the top k at every level.
 //
 // Selection (select_kth): the block finds the smallest and largest key,
 // histograms the 8 bits below their common prefix and locates the bin that
@@ -60,18 +61,18 @@ struct TopkSmem {
   static constexpr int BAR_OFF = RED_OFF + 2 * NW * 4;
   static constexpr int MISC_OFF = BAR_OFF + NSLOT * 8;
   static constexpr int SC_OFF = MISC_OFF + 64;                // order keys / merge keys (sized per launch)
-  static constexpr int MAX_SC = kTopkMaxCand * 8;             // >= kTopkMaxChunk * 4
+  static constexpr int MAX_SC = kTopkMaxCand * 16;            // >= kTopkMaxChunk * 4; two merge buffers
   static constexpr int MAX_TOTAL = SC_OFF + MAX_SC;
   static_assert(kTopkMaxChunk * 4 <= MAX_SC, "chunk scores must fit");
   static_assert(SLOT % 16 == 0, "slots must stay 16-byte aligned");
   static_assert(BAR_OFF % 8 == 0, "mbarriers need 8-byte alignment");
-  static_assert(NSLOT * SLOT >= 2 * kMaxTopk * 4, "the merge winners reuse the stage area");
+  static_assert(NSLOT * SLOT >= kMaxTopk * 8, "the split's winners reuse the stage area");
 };
 
 template <int MODE, int D>
 int smem_bytes(long long chunk, int S, int k) {
   using L = TopkSmem<MODE, D>;
-  const long long sc = std::max(chunk * 4, static_cast<long long>(S) * k * 8);
+  const long long sc = std::max(chunk * 4, static_cast<long long>(S) * k * 16);
   return static_cast<int>(L::SC_OFF + ((sc + 15) / 16) * 16);
 }
 
@@ -83,6 +84,12 @@ __device__ __forceinline__ uint32_t order_key(float s) {
 __device__ __forceinline__ float key_to_score(uint32_t k) {
   const uint32_t b = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
   return __uint_as_float(b);
+}
+
+// Unique composite key of a candidate: order key above, ~index below (larger is
+// better; 0 marks padding).
+__device__ __forceinline__ uint64_t composite(uint32_t okey, uint32_t idx) {
+  return (static_cast<uint64_t>(okey) << 32) | (0xFFFFFFFFu - idx);
 }
 
 __device__ __forceinline__ float pow2f(int e) {  // 2^e for -126 <= e <= 127
@@ -463,9 +470,11 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
     __syncthreads();
     if (tid == 0) st[3] = 0;
     __syncthreads();
-    // Keys above T go anywhere in [0, n_gt); the need_eq ties at T are the
-    // lowest indices: each warp scans a contiguous segment, counts its ties,
-    // and places its own after those of the warps before it.
+    // The winners go to shared memory as composite keys (order key, ~index):
+    // keys above T anywhere in [0, n_gt), then the need_eq ties at T with the
+    // lowest indices (each warp scans a contiguous segment, counts its ties,
+    // and places its own after those of the warps before it).
+    uint64_t* wk = reinterpret_cast<uint64_t*>(smem);   // [keff], in the idle stage area
     const int seg = (n + NW - 1) / NW;
     const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
     int myeq = 0;
@@ -480,8 +489,7 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
       pbase = __shfl_sync(0xffffffffu, pbase, 0);
       if (sel) {
         const int pos = pbase + __popc(bal & ((1u << lane) - 1u));
-        cs[pos] = key_to_score(key);
-        ci[pos] = static_cast<int32_t>(t_begin + i);
+        wk[pos] = composite(key, static_cast<uint32_t>(t_begin + i));
       }
     }
     if (lane == 0) red[warp] = static_cast<uint32_t>(myeq);
@@ -493,11 +501,23 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
       const bool eq = (i < s1) && (okeys[i] == T);
       const uint32_t bal = __ballot_sync(0xffffffffu, eq);
       const int before = __popc(bal & ((1u << lane) - 1u));
-      if (eq && taken + before < need_eq) {
-        cs[n_gt + taken + before] = key_to_score(T);
-        ci[n_gt + taken + before] = static_cast<int32_t>(t_begin + i);
-      }
+      if (eq && taken + before < need_eq) wk[n_gt + taken + before] = composite(T, static_cast<uint32_t>(t_begin + i));
       taken += __popc(bal);
+    }
+    __syncthreads();
+    // the candidates in descending order (composite keys are unique): four
+    // lanes count the larger keys of one candidate
+    for (int e0 = tid >> 2; e0 < ((keff + NW * 8 - 1) / (NW * 8)) * (NW * 8); e0 += NW * 8) {
+      const int e = min(e0, keff - 1);
+      const uint64_t key = wk[e];
+      int rank = 0;
+      for (int j = (tid & 3); j < keff; j += 4) rank += wk[j] > key;
+      rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+      rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+      if ((tid & 3) == 0 && e0 < keff) {
+        cs[rank] = key_to_score(static_cast<uint32_t>(key >> 32));
+        ci[rank] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+      }
     }
   }
   for (int i = keff + tid; i < K; i += blockDim.x) {
@@ -517,10 +537,12 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   __syncthreads();
   if (!misc[1]) return;
   __threadfence();
-  // Candidates as unique composite keys (order key, ~index): larger is better.
+  // Each split's candidates are in descending order of the unique composite
+  // key (order key, ~index); padding is 0.  A merge-path tree halves the lists
+  // per level, each output keeping the top K of its two inputs.
   const int NC = p.S * K;
-  uint32_t* khi = okeys;                // [NC] order keys, 0 for padding
-  uint32_t* klo = okeys + NC;           // [NC] ~index, 0 for padding
+  uint64_t* ca = reinterpret_cast<uint64_t*>(okeys);   // [S][K]
+  uint64_t* cb = ca + NC;                              // [S][K]
   const float* us = p.cand_score + u * p.S * K;
   const int32_t* ui = p.cand_idx + u * p.S * K;
   int cnt = 0;
@@ -538,8 +560,7 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
       const int i = i0 + k2 * NTHREADS;
       if (i < NC) {
         const bool ok = idx[k2] >= 0;
-        khi[i] = ok ? order_key(sc[k2]) : 0u;
-        klo[i] = ok ? 0xFFFFFFFFu - static_cast<uint32_t>(idx[k2]) : 0u;
+        ca[i] = ok ? composite(order_key(sc[k2]), static_cast<uint32_t>(idx[k2])) : 0ull;
         cnt += ok;
       }
     }
@@ -550,53 +571,38 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   __syncthreads();
   int nvalid = 0;
   for (int w = 0; w < NW; ++w) nvalid += static_cast<int>(red[w]);
-  __syncthreads();
   const int kf = min(K, nvalid);
-  uint32_t* whi = reinterpret_cast<uint32_t*>(smem);   // winners, in the (idle) stage area
-  uint32_t* wlo = whi + kMaxTopk;
-  if (kf > 0) {
-    select_kth(NC, kf, [&](int i, uint32_t& key) { key = khi[i]; return klo[i] != 0u; }, hist, list, red, st);
-    const uint32_t Thi = static_cast<uint32_t>(st[0]);
-    const int need = st[2];
-    __syncthreads();
-    // the `need` largest ~index among the candidates whose order key is Thi
-    select_kth(NC, need, [&](int i, uint32_t& key) { key = klo[i]; return klo[i] != 0u && khi[i] == Thi; },
-               hist, list, red, st);
-    const uint32_t Tlo = static_cast<uint32_t>(st[0]);
-    __syncthreads();
-    if (tid == 0) st[3] = 0;
-    __syncthreads();
-    const int nround = (NC + blockDim.x - 1) / blockDim.x * blockDim.x;
-    for (int i = tid; i < nround; i += blockDim.x) {
-      uint32_t h = 0, l = 0;
-      if (i < NC) {
-        h = khi[i];
-        l = klo[i];
+  int nl = p.S;
+  uint64_t *src = ca, *dst = cb;
+  while (nl > 1) {
+    const int np = nl / 2;
+    for (int t = tid; t < np * K; t += blockDim.x) {
+      const int j = t / K, i = t % K;                   // output list j, position i
+      const uint64_t* A = src + static_cast<long long>(2 * j) * K;
+      const uint64_t* B = A + K;
+      int lo = max(0, i - K), hi = min(i, K);           // elements of A among the top i
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (A[mid] > B[i - mid - 1]) lo = mid + 1;
+        else hi = mid;
       }
-      const bool win = l != 0u && (h > Thi || (h == Thi && l >= Tlo));
-      const uint32_t bal = __ballot_sync(0xffffffffu, win);
-      int base = 0;
-      if (lane == 0 && bal) base = atomicAdd(st + 3, __popc(bal));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if (win) {
-        const int pos = base + __popc(bal & ((1u << lane) - 1u));
-        whi[pos] = h;
-        wlo[pos] = l;
-      }
+      const int bi = i - lo;
+      const uint64_t va = (lo < K) ? A[lo] : 0ull, vb = (bi < K) ? B[bi] : 0ull;
+      dst[static_cast<long long>(j) * K + i] = va > vb ? va : vb;
     }
+    if (nl & 1)   // an odd list out moves up unchanged
+      for (int i = tid; i < K; i += blockDim.x) dst[static_cast<long long>(np) * K + i] = src[static_cast<long long>(nl - 1) * K + i];
     __syncthreads();
-    // rank sort of the kf winners (all composite keys differ)
-    for (int i = tid; i < kf; i += blockDim.x) {
-      const uint32_t h = whi[i], l = wlo[i];
-      int rank = 0;
-      for (int j = 0; j < kf; ++j) {
-        const uint32_t hj = whi[j], lj = wlo[j];
-        rank += (hj > h || (hj == h && lj > l)) ? 1 : 0;
-      }
-      const long long o = u * K + rank;
-      p.idx_out[o] = static_cast<int32_t>(0xFFFFFFFFu - l);
-      if (p.score_out) p.score_out[o] = key_to_score(h);
-    }
+    nl = np + (nl & 1);
+    uint64_t* tmp = src;
+    src = dst;
+    dst = tmp;
+  }
+  for (int i = tid; i < kf; i += blockDim.x) {
+    const uint64_t key = src[i];
+    const long long o = u * K + i;
+    p.idx_out[o] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+    if (p.score_out) p.score_out[o] = key_to_score(static_cast<uint32_t>(key >> 32));
   }
   for (int i = kf + tid; i < K; i += blockDim.x) {
     const long long o = u * K + i;
