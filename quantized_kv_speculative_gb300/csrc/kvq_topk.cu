@@ -67,6 +67,7 @@ struct TopkSmem {
   static_assert(SLOT % 16 == 0, "slots must stay 16-byte aligned");
   static_assert(BAR_OFF % 8 == 0, "mbarriers need 8-byte alignment");
   static_assert(NSLOT * SLOT >= kMaxTopk * 8, "the split's winners reuse the stage area");
+  static_assert(NSLOT * SLOT >= 2 * NW * 128 * 8, "the warps' sorted lists reuse the stage area");
 };
 
 template <int MODE, int D>
@@ -113,6 +114,73 @@ __device__ __forceinline__ int pair_slot(int local) {
     e = local / HALF;
   }
   return 2 * pp + e;
+}
+
+// Sorts the warp's 128 keys into descending order.  Key x = 32 r + lane sits
+// in v[r]; the bitonic network pairs x with x ^ j (a shuffle for j < 32, a
+// register swap otherwise).
+__device__ __forceinline__ void warp_sort128_desc(uint64_t (&v)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 128; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j < 32) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int x = 32 * r + lane;
+          const uint64_t o = __shfl_xor_sync(0xffffffffu, v[r], j);
+          const bool desc = (x & k) == 0, lower = (x & j) == 0;
+          const uint64_t hi = v[r] > o ? v[r] : o, lo = v[r] > o ? o : v[r];
+          v[r] = (lower == desc) ? hi : lo;
+        }
+      } else {
+        const int jr = j >> 5;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          if (r & jr) continue;
+          const int x = 32 * r + lane;
+          const bool desc = (x & k) == 0;
+          const uint64_t a = v[r], b = v[r | jr];
+          const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+          v[r] = desc ? hi : lo;
+          v[r | jr] = desc ? lo : hi;
+        }
+      }
+    }
+  }
+}
+
+// Merge-path tree: nl lists of len keys each, in descending order, at src
+// (padding 0), merged pairwise per level, each output keeping the top len of
+// its two inputs (an odd list moves up unchanged).  Every thread of the block
+// calls it; dst is scratch of the same size.  Returns the final list.
+__device__ uint64_t* merge_tree(uint64_t* src, uint64_t* dst, int nl, int len) {
+  while (nl > 1) {
+    const int np = nl / 2;
+    for (int t = threadIdx.x; t < np * len; t += blockDim.x) {
+      const int j = t / len, i = t % len;               // output list j, position i
+      const uint64_t* A = src + static_cast<long long>(2 * j) * len;
+      const uint64_t* B = A + len;
+      int lo = 0, hi = i;                               // elements of A among the top i
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (A[mid] > B[i - mid - 1]) lo = mid + 1;
+        else hi = mid;
+      }
+      const uint64_t va = A[lo], vb = B[i - lo];
+      dst[static_cast<long long>(j) * len + i] = va > vb ? va : vb;
+    }
+    if (nl & 1)
+      for (int i = threadIdx.x; i < len; i += blockDim.x)
+        dst[static_cast<long long>(np) * len + i] = src[static_cast<long long>(nl - 1) * len + i];
+    __syncthreads();
+    nl = np + (nl & 1);
+    uint64_t* tmp = src;
+    src = dst;
+    dst = tmp;
+  }
+  return src;
 }
 
 // Block-wide selection of the kth largest key among the i < n for which
@@ -462,7 +530,29 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   int* st = misc + 2;  // st[0] T, st[1] remaining, st[2] ties taken, st[3] bin / count, st[4] gather count
   float* cs = p.cand_score + (u * p.S + split) * K;
   int32_t* ci = p.cand_idx + (u * p.S + split) * K;
-  if (keff > 0) {
+  if (keff > 0 && n <= NW * 128 && K <= 128) {
+    // small chunk: each warp sorts its 128 keys, the warps' top-K lists are
+    // merged by the merge-path tree
+    uint64_t* la = reinterpret_cast<uint64_t*>(smem);   // [NW][K], the idle stage area
+    uint64_t* lb = la + NW * K;
+    uint64_t v[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = warp * 128 + 32 * r + lane;
+      v[r] = (i < n) ? composite(okeys[i], static_cast<uint32_t>(t_begin + i)) : 0ull;
+    }
+    warp_sort128_desc(v);
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      if (32 * r + lane < K) la[warp * K + 32 * r + lane] = v[r];
+    __syncthreads();
+    const uint64_t* top = merge_tree(la, lb, NW, K);
+    for (int i = tid; i < keff; i += blockDim.x) {
+      const uint64_t key = top[i];
+      cs[i] = key_to_score(static_cast<uint32_t>(key >> 32));
+      ci[i] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+    }
+  } else if (keff > 0) {
     select_kth(n, keff, [&](int i, uint32_t& key) { key = okeys[i]; return true; }, hist, list, red, st);
     const uint32_t T = static_cast<uint32_t>(st[0]);
     const int need_eq = st[2];
@@ -572,32 +662,7 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   int nvalid = 0;
   for (int w = 0; w < NW; ++w) nvalid += static_cast<int>(red[w]);
   const int kf = min(K, nvalid);
-  int nl = p.S;
-  uint64_t *src = ca, *dst = cb;
-  while (nl > 1) {
-    const int np = nl / 2;
-    for (int t = tid; t < np * K; t += blockDim.x) {
-      const int j = t / K, i = t % K;                   // output list j, position i
-      const uint64_t* A = src + static_cast<long long>(2 * j) * K;
-      const uint64_t* B = A + K;
-      int lo = max(0, i - K), hi = min(i, K);           // elements of A among the top i
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (A[mid] > B[i - mid - 1]) lo = mid + 1;
-        else hi = mid;
-      }
-      const int bi = i - lo;
-      const uint64_t va = (lo < K) ? A[lo] : 0ull, vb = (bi < K) ? B[bi] : 0ull;
-      dst[static_cast<long long>(j) * K + i] = va > vb ? va : vb;
-    }
-    if (nl & 1)   // an odd list out moves up unchanged
-      for (int i = tid; i < K; i += blockDim.x) dst[static_cast<long long>(np) * K + i] = src[static_cast<long long>(nl - 1) * K + i];
-    __syncthreads();
-    nl = np + (nl & 1);
-    uint64_t* tmp = src;
-    src = dst;
-    dst = tmp;
-  }
+  const uint64_t* src = merge_tree(ca, cb, p.S, K);
   for (int i = tid; i < kf; i += blockDim.x) {
     const uint64_t key = src[i];
     const long long o = u * K + i;
