@@ -329,16 +329,16 @@ kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int3
   long long chunk = 0;
   const long long slots = attend_resident_ctas(mode, cache->desc.head_dim, cache->desc.group_size, gamma * HG);
   // The bf16 tail (residual, pending and selected tokens) goes to CTAs of its
-  // own when they fit in the first wave beside the quantized splits at no more
-  // than one chunk-alignment step of longer chunks; otherwise each quantized
-  // split takes a slice of it after its own tokens.
+  // own when they fit in the first wave beside the quantized splits without
+  // making the chunks longer; otherwise each quantized split takes a slice of
+  // it after its own tokens.
   const long long ntail = static_cast<long long>(cache->residual_len) + n_pend + top_k;
   const int S_t = static_cast<int>(std::min<long long>(kMaxTailSplits, std::max(1LL, ceil_div(ntail, kTailTokensPerSplit))));
   if (cache->quantized_len > 0) {
     long long ch_fused = 0, ch_sep = 0;
     const int sq_fused = attend_splits(cache->quantized_len, U, slots, 0, &ch_fused);
     const int sq_sep = attend_splits(cache->quantized_len, U, slots, S_t, &ch_sep);
-    const bool sep = slots > 0 && (sq_sep + S_t) * U <= slots && ch_sep <= ch_fused + kChunkAlign;
+    const bool sep = slots > 0 && (sq_sep + S_t) * U <= slots && ch_sep <= ch_fused;
     p.S_t = sep ? S_t : 0;
     p.S_q = sep ? sq_sep : sq_fused;
     chunk = sep ? ch_sep : ch_fused;
