@@ -227,7 +227,9 @@ kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int3
  *  q_spec   bf16 [B][Hq][D].
  *  idx_out  int32 [B][Hkv][top_k], in that order.  score_out fp32, same shape,
  *           or NULL.
- *  1 <= top_k <= 1024.  Enqueues one kernel.
+ *  1 <= top_k <= 1024, and ceil(Lq / 8192) * top_k <= 4096 (each split scores
+ *  at most 8192 tokens and the merge holds at most 4096 candidates); a cache
+ *  beyond that returns KVQ_ERR_UNSUPPORTED.  Enqueues one kernel.
  */
 kvq_status kvq_topk(const kvq_cache* cache, kvq_mode mode, const void* q_spec,
                     int32_t num_q_heads, int32_t top_k, int32_t* idx_out, float* score_out,

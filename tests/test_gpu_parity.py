@@ -224,6 +224,9 @@ TOPK_CASES = [
     ("int1", 3, 2, 8, 128, 32, 2100, 64),
     ("int1", 1, 2, 2, 64, 64, 700, 1),
     ("int2", 1, 2, 2, 64, 32, 130, 80),         # k > Lq: padded with -1
+    ("int4", 1, 2, 4, 128, 128, 6000, 128),     # the largest k of the warp-sort selection
+    ("int4", 1, 2, 4, 128, 128, 6000, 300),     # k above it: radix selection on small chunks
+    ("int2", 1, 1, 4, 128, 32, 30000, 1024),    # the largest k: 4 splits x 1024 candidates to merge
 ]
 
 
