@@ -168,13 +168,25 @@ def run_device(args, rank, world):
     idx = torch.empty((spec.B, spec.Hkv, spec.top_k), dtype=torch.int32, device=dev)
     sc = torch.empty((spec.B, spec.Hkv, spec.top_k), dtype=torch.float32, device=dev)
 
+    # The top-k reads only the quantized keys, so it runs on a second stream,
+    # concurrent with the attention (which reads the residual buffer the append
+    # then rewrites, so the append follows it on the first stream).
+    side = torch.cuda.Stream()
+
     def step(i, stream=None):
+        s0 = stream if stream is not None else torch.cuda.current_stream()
         c = caches[i % spec.copies]
         ws = wss[i % spec.copies]
         st = c.state()
-        kvq.kvq_attend(c, "int8", q, pk, pv, out=out, lse=lse, workspace=ws, stream=stream)
-        kvq.kvq_topk(c, "int4", q_spec, spec.top_k, idx_out=idx, score_out=sc, workspace=ws, stream=stream)
-        kvq.kvq_quantize_append(c, kn, vn, stream=stream)
+        fork = torch.cuda.Event()
+        fork.record(s0)
+        side.wait_event(fork)
+        kvq.kvq_attend(c, "int8", q, pk, pv, out=out, lse=lse, workspace=ws, stream=s0)
+        kvq.kvq_topk(c, "int4", q_spec, spec.top_k, idx_out=idx, score_out=sc, workspace=ws, stream=side)
+        join = torch.cuda.Event()
+        join.record(side)
+        kvq.kvq_quantize_append(c, kn, vn, stream=s0)
+        s0.wait_event(join)
         c.set_state(st)
 
     # attend, top-k, then the append: one flush kernel when the residual buffer
@@ -331,7 +343,7 @@ def run_device(args, rank, world):
         "config": {"workload": WORKLOAD, "batch": spec.B, "q_heads": spec.Hq, "kv_heads": spec.Hkv,
                    "head_dim": spec.D, "group": spec.G, "quantized_tokens": spec.Lq, "residual_tokens": spec.r0,
                    "gamma": spec.gamma, "pending": spec.P, "top_k": spec.top_k, "append_per_step": spec.n_accept,
-                   "step": "int8 verify attend + int4 top-k + quantize-append with one group flush",
+                   "step": "int8 verify attend and int4 top-k on two streams, then quantize-append with one group flush",
                    "timing": "CUDA graph per step, CUDA events over the K steps",
                    "l2": f"rotating {spec.copies} cache copies of {spec.attend_bytes() / 1e6:.1f} MB each (> L2)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
