@@ -165,14 +165,6 @@ __device__ __forceinline__ uint32_t cvt4_pair(uint32_t w) {
   return lop_and_or(shl_signed<6 - 4 * I>(w), 0x03C003C0u, F16_ONE2);
 }
 
-// 8-bit codes from an upper-nibble word H and a lower-nibble word L (same
-// positions): code = 16*hi + lo placed at mantissa bits 2..9.
-template <int I>
-__device__ __forceinline__ uint32_t cvt8_pair(uint32_t h, uint32_t l) {
-  const uint32_t t = lop_and_or(shl_signed<6 - 4 * I>(h), 0x03C003C0u, F16_ONE2);
-  return lop_and_or(shl_signed<2 - 4 * I>(l), 0x003C003Cu, t);
-}
-
 // 2-bit codes: code i (bits 2i..2i+1) and code i+8 (bits 16+2i..) -> half2.
 template <int I>
 __device__ __forceinline__ uint32_t cvt2_pair(uint32_t w) {
@@ -193,12 +185,6 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 __device__ __forceinline__ float2 unpack_half2(uint32_t v) {
   __half2 h = *reinterpret_cast<__half2*>(&v);
   return __half22float2(h);
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
 }
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t v) {

@@ -53,19 +53,6 @@ struct Rows {
   static constexpr int KCHUNK = KROW / 4;  // bytes of a key row owned by one lane
 };
 
-// Channels (relative to q*D/4) of pair p.
-template <int MODE, int D>
-__device__ __forceinline__ int2 pair_chan(int p) {
-  if constexpr (Mode<MODE>::PB == 4) {
-    return make_int2(8 * (p / 4) + p % 4, 8 * (p / 4) + p % 4 + 4);
-  } else if constexpr (Mode<MODE>::PB == 2) {
-    return make_int2(16 * (p / 8) + p % 8, 16 * (p / 8) + p % 8 + 8);
-  } else {
-    constexpr int HALF = (D == 128) ? 16 : 8;
-    return make_int2(p, p + HALF);
-  }
-}
-
 template <int I, int N, typename F>
 __device__ __forceinline__ void static_for(F&& f) {
   if constexpr (I < N) {
@@ -74,36 +61,28 @@ __device__ __forceinline__ void static_for(F&& f) {
   }
 }
 
-// Convert this lane's chunk of one key row into D/8 code pairs (1 + c/2^CB).
-// `k0` points at the chunk in plane 0; plane 1 (INT8 lower nibbles) lies
-// `plane_stride` bytes further.
+// Convert this lane's chunk of one key row into D/8 code pairs (1 + c/2^CB)
+// for the single-plane modes (INT4 reads the upper plane).  `k0` points at the
+// chunk in plane 0.
 template <int MODE, int D>
-__device__ __forceinline__ void key_pairs(const uint8_t* k0, int plane_stride, uint32_t (&P)[D / 8]) {
+__device__ __forceinline__ void key_pairs(const uint8_t* k0, int /*plane_stride*/, uint32_t (&P)[D / 8]) {
   using M = Mode<MODE>;
+  static_assert(M::NP == 1, "the INT8 target code converts through key_pairs_x");
   if constexpr (M::PB == 4) {
     constexpr int NWD = D / 32;  // words per chunk
-    uint32_t h[NWD], l[NWD];
+    uint32_t h[NWD];
     if constexpr (NWD == 4) {
       const uint4 v = *reinterpret_cast<const uint4*>(k0);
       h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
-      if constexpr (M::NP == 2) {
-        const uint4 w = *reinterpret_cast<const uint4*>(k0 + plane_stride);
-        l[0] = w.x; l[1] = w.y; l[2] = w.z; l[3] = w.w;
-      }
     } else {
       const uint2 v = *reinterpret_cast<const uint2*>(k0);
       h[0] = v.x; h[1] = v.y;
-      if constexpr (M::NP == 2) {
-        const uint2 w = *reinterpret_cast<const uint2*>(k0 + plane_stride);
-        l[0] = w.x; l[1] = w.y;
-      }
     }
 #pragma unroll
     for (int w = 0; w < NWD; ++w) {
       static_for<0, 4>([&](auto I) {
         constexpr int i = decltype(I)::value;
-        if constexpr (M::NP == 2) P[4 * w + i] = cvt8_pair<i>(h[w], l[w]);
-        else P[4 * w + i] = cvt4_pair<i>(h[w]);
+        P[4 * w + i] = cvt4_pair<i>(h[w]);
       });
     }
   } else if constexpr (M::PB == 2) {
@@ -140,49 +119,6 @@ __device__ __forceinline__ void key_pairs(const uint8_t* k0, int plane_stride, u
   }
 }
 
-// A-operand fragments of P.V for one m-tile (channel rows ca = 16mt+g and
-// cb = ca+8) of one 32-token slab: a[s] for k-steps s = 0, 1.  Lane q's tokens
-// are 8q..8q+7.  k-step s covers the pairs (8q+2s, 8q+2s+4) and
-// (8q+2s+1, 8q+2s+5).  `va`/`vb` point at rows ca/cb of plane 0.
-template <int MODE>
-__device__ __forceinline__ void value_frags(const uint8_t* va, const uint8_t* vb, int plane_stride,
-                                            int q, uint32_t (&a)[2][4]) {
-  using M = Mode<MODE>;
-  if constexpr (M::PB == 4) {
-    const uint32_t wa = *reinterpret_cast<const uint32_t*>(va + 4 * q);
-    const uint32_t wb = *reinterpret_cast<const uint32_t*>(vb + 4 * q);
-    if constexpr (M::NP == 2) {
-      const uint32_t la = *reinterpret_cast<const uint32_t*>(va + plane_stride + 4 * q);
-      const uint32_t lb = *reinterpret_cast<const uint32_t*>(vb + plane_stride + 4 * q);
-      a[0][0] = cvt8_pair<0>(wa, la); a[0][1] = cvt8_pair<0>(wb, lb);
-      a[0][2] = cvt8_pair<1>(wa, la); a[0][3] = cvt8_pair<1>(wb, lb);
-      a[1][0] = cvt8_pair<2>(wa, la); a[1][1] = cvt8_pair<2>(wb, lb);
-      a[1][2] = cvt8_pair<3>(wa, la); a[1][3] = cvt8_pair<3>(wb, lb);
-    } else {
-      a[0][0] = cvt4_pair<0>(wa); a[0][1] = cvt4_pair<0>(wb);
-      a[0][2] = cvt4_pair<1>(wa); a[0][3] = cvt4_pair<1>(wb);
-      a[1][0] = cvt4_pair<2>(wa); a[1][1] = cvt4_pair<2>(wb);
-      a[1][2] = cvt4_pair<3>(wa); a[1][3] = cvt4_pair<3>(wb);
-    }
-  } else if constexpr (M::PB == 2) {
-    const uint32_t xa = *reinterpret_cast<const uint16_t*>(va + 2 * q);
-    const uint32_t xb = *reinterpret_cast<const uint16_t*>(vb + 2 * q);
-    const uint32_t y = prmt(xa, xb, 0x5140u);   // [a.b0, b.b0, a.b1, b.b1]
-    a[0][0] = cvt2_pair<0>(y); a[0][1] = cvt2_pair<4>(y);
-    a[0][2] = cvt2_pair<1>(y); a[0][3] = cvt2_pair<5>(y);
-    a[1][0] = cvt2_pair<2>(y); a[1][1] = cvt2_pair<6>(y);
-    a[1][2] = cvt2_pair<3>(y); a[1][3] = cvt2_pair<7>(y);
-  } else {
-    const uint32_t x = static_cast<uint32_t>(va[q]) | (static_cast<uint32_t>(vb[q]) << 8);
-    const uint32_t y = (x & 0x0F0Fu) | ((x & 0xF0F0u) << 12);
-    a[0][0] = cvt1_pair<0>(y); a[0][1] = cvt1_pair<8>(y);
-    a[0][2] = cvt1_pair<1>(y); a[0][3] = cvt1_pair<9>(y);
-    a[1][0] = cvt1_pair<2>(y); a[1][1] = cvt1_pair<10>(y);
-    a[1][2] = cvt1_pair<3>(y); a[1][3] = cvt1_pair<11>(y);
-  }
-}
-
-
 // ------------------------------------------------------------------------------
 // Offset encoding for attention.  An f16 whose upper byte is 0x64 has exponent
 // 10, so its value is 1024 + m, where m is the 10-bit mantissa field.  A b-bit
@@ -190,8 +126,9 @@ __device__ __forceinline__ void value_frags(const uint8_t* va, const uint8_t* vb
 // as exactly 1024 + 2^k c, and one LOP3 (mask, or with 0x6400) turns two codes
 // 16 bits apart into a half2.  For the 8-bit target code the two nibble planes
 // are first merged into bytes (shift + LOP3 per four codes), then a PRMT drops
-// each byte under 0x64.  An exact f16x2 subtract then removes the 1024, which
-// leaves 2^k c.
+// each byte under 0x64.  The 1024 is removed inside the MMA accumulators:
+// value slabs start from -1024 times the sum of their probabilities, key
+// logits from the encoding's offset times the sum of their weights.
 //
 // For values, a lane reads 8 consecutive tokens 8q..8q+7 of a channel row;
 // pair i covers tokens 8q + VA[i], 8q + VB[i] with factor vx_mult(i).  For the
@@ -203,14 +140,6 @@ constexpr uint32_t X1024 = 0x64006400u;   // half2(1024, 1024)
 constexpr uint32_t X64B = 0x64646464u;    // prmt source of the 0x64 bytes
 
 __device__ __forceinline__ uint32_t xsel(uint32_t w, uint32_t mask) { return (w & mask) | X1024; }
-
-// (1024 + m) - 1024 = m for both halves, exactly: value codes lose the offset
-// before they enter the long P.V accumulation.
-__device__ __forceinline__ uint32_t xoff(uint32_t x) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(X1024));
-  return r;
-}
 
 template <int MODE>
 struct XPair {
