@@ -164,12 +164,17 @@ __device__ __forceinline__ float fill_qt(const AttendParams& p, int b, int kvh, 
 
 // ------------------------------------------------------------------------------
 // Combine: merge the S_total partials of unit u into out/lse.  The split
-// maxima and weights are staged in shared memory (S_total <= 256), then each
-// thread streams float4 rows of the partial outputs with several splits in
-// flight.
+// maxima and weights are staged in shared memory (S_total <= 256); each thread
+// owns up to two float4 items of the output.  With PREFETCH (the eight-row
+// variants, which have the registers to spare) and at most 10 splits the
+// items' partial outputs are loaded first, together with the maxima, so the
+// combine takes one round trip to L2; otherwise they stream after the weights
+// with several splits in flight.
 // ------------------------------------------------------------------------------
-template <int D>
+template <int D, bool PREFETCH>
 __device__ void combine_unit(const AttendParams& p, long long u, int S_total, float* sm) {
+  constexpr int D4 = D / 4;
+  constexpr int kPF = PREFETCH ? 10 : 1;   // partial outputs prefetched per item (up to kPF splits)
   const int PF = kPartialFloats(D);
   const float* base = p.partials + u * static_cast<long long>(S_total) * PF;
   const int b = static_cast<int>(u / p.c.Hkv), kvh = static_cast<int>(u % p.c.Hkv);
@@ -177,6 +182,23 @@ __device__ void combine_unit(const AttendParams& p, long long u, int S_total, fl
   float* wt = sm + kMaxCombine * 8;     // [S_total][8] l, then weights
   float* ml = wt + kMaxCombine * 8;     // M[8], L[8]
   const int tid = threadIdx.x;
+  const int nitems = p.R * D4;          // <= 2 per thread (R <= 8, D <= 128, 128 threads)
+  // With few splits, each thread's partial outputs are loaded before the
+  // weights are known, so that all loads are in flight together.
+  const bool pf = PREFETCH && S_total <= kPF;
+  float4 pre[2][kPF];
+  if (pf) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int item = tid + k * static_cast<int>(blockDim.x);
+      if (item < nitems) {
+        const float4* src = reinterpret_cast<const float4*>(base + 2 * kMaxRows + (item / D4) * D) + item % D4;
+#pragma unroll
+        for (int s = 0; s < kPF; ++s)
+          if (s < S_total) pre[k][s] = __ldcg(src + static_cast<long long>(s) * (PF / 4));
+      }
+    }
+  }
   for (int e = tid; e < S_total * 8; e += blockDim.x) {
     const int s = e >> 3, r = e & 7;
     ms[e] = __ldcg(base + s * PF + r);
@@ -201,19 +223,34 @@ __device__ void combine_unit(const AttendParams& p, long long u, int S_total, fl
     ml[8 + tid] = L;
   }
   __syncthreads();
-  constexpr int D4 = D / 4;
-  for (int item = tid; item < p.R * D4; item += blockDim.x) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int item = tid + k * static_cast<int>(blockDim.x);
+    if (item >= nitems) continue;
     const int rho = item / D4, d4 = item % D4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4* src = reinterpret_cast<const float4*>(base + 2 * kMaxRows + rho * D) + d4;
+    if (pf) {
+#pragma unroll
+      for (int s = 0; s < kPF; ++s) {
+        if (s < S_total) {
+          const float w = wt[s * 8 + rho];
+          acc.x = fmaf(w, pre[k][s].x, acc.x);
+          acc.y = fmaf(w, pre[k][s].y, acc.y);
+          acc.z = fmaf(w, pre[k][s].z, acc.z);
+          acc.w = fmaf(w, pre[k][s].w, acc.w);
+        }
+      }
+    } else {
+      const float4* src = reinterpret_cast<const float4*>(base + 2 * kMaxRows + rho * D) + d4;
 #pragma unroll 8
-    for (int s = 0; s < S_total; ++s) {
-      const float w = wt[s * 8 + rho];
-      const float4 v = __ldcg(src + static_cast<long long>(s) * (PF / 4));
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+      for (int s = 0; s < S_total; ++s) {
+        const float w = wt[s * 8 + rho];
+        const float4 v = __ldcg(src + static_cast<long long>(s) * (PF / 4));
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+      }
     }
     const int i = rho / p.HG, hh = rho % p.HG;
     const int h = kvh * p.HG + hh;
@@ -232,7 +269,7 @@ __device__ void combine_unit(const AttendParams& p, long long u, int S_total, fl
 }
 
 // Arrive at the per-unit ticket; the last arriving CTA merges and resets it.
-template <int D>
+template <int D, bool PREFETCH>
 __device__ void ticket_and_combine(const AttendParams& p, long long u, int* sh_flag, float* combine_scratch) {
   __threadfence();
   __syncthreads();
@@ -246,7 +283,7 @@ __device__ void ticket_and_combine(const AttendParams& p, long long u, int* sh_f
   __syncthreads();
   if (*sh_flag) {
     __threadfence();
-    combine_unit<D>(p, u, S_total, combine_scratch);
+    combine_unit<D, PREFETCH>(p, u, S_total, combine_scratch);
   }
 }
 
@@ -513,7 +550,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
     __syncthreads();
     merge_to_partial<D>(p, u, p.S_q + ts, NW, G, wm, wl, wc, wo, reinterpret_cast<float*>(smem + L::FAC_OFF));
     __syncthreads();
-    ticket_and_combine<D>(p, u, sh_flag, reinterpret_cast<float*>(smem));
+    ticket_and_combine<D, NT == 2>(p, u, sh_flag, reinterpret_cast<float*>(smem));
     return;
   }
 
@@ -1077,7 +1114,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
                       reinterpret_cast<const float*>(smem + L::WL_OFF), reinterpret_cast<const float*>(smem + L::WC_OFF),
                       reinterpret_cast<const float*>(smem + L::WO_OFF), reinterpret_cast<float*>(smem + L::FAC_OFF));
   __syncthreads();
-  ticket_and_combine<D>(p, u, sh_flag, reinterpret_cast<float*>(smem));
+  ticket_and_combine<D, NT == 2>(p, u, sh_flag, reinterpret_cast<float*>(smem));
 }
 
 template <int MODE, int D, int NJ, int NT>
