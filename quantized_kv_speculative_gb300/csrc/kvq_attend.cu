@@ -223,35 +223,8 @@ __device__ void combine_unit(const AttendParams& p, long long u, int S_total, fl
     ml[8 + tid] = L;
   }
   __syncthreads();
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int item = tid + k * static_cast<int>(blockDim.x);
-    if (item >= nitems) continue;
-    const int rho = item / D4, d4 = item % D4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (pf) {
-#pragma unroll
-      for (int s = 0; s < kPF; ++s) {
-        if (s < S_total) {
-          const float w = wt[s * 8 + rho];
-          acc.x = fmaf(w, pre[k][s].x, acc.x);
-          acc.y = fmaf(w, pre[k][s].y, acc.y);
-          acc.z = fmaf(w, pre[k][s].z, acc.z);
-          acc.w = fmaf(w, pre[k][s].w, acc.w);
-        }
-      }
-    } else {
-      const float4* src = reinterpret_cast<const float4*>(base + 2 * kMaxRows + rho * D) + d4;
-#pragma unroll 8
-      for (int s = 0; s < S_total; ++s) {
-        const float w = wt[s * 8 + rho];
-        const float4 v = __ldcg(src + static_cast<long long>(s) * (PF / 4));
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
-      }
-    }
+  // Writes one output item (row rho, channels 4 d4 .. 4 d4 + 3) and its LSE.
+  auto put = [&](int rho, int d4, const float4& acc) {
     const int i = rho / p.HG, hh = rho % p.HG;
     const int h = kvh * p.HG + hh;
     const long long orow = (static_cast<long long>(b) * p.gamma + i) * p.Hq + h;
@@ -265,6 +238,57 @@ __device__ void combine_unit(const AttendParams& p, long long u, int S_total, fl
       const float M = ml[rho], L = ml[8 + rho];
       p.lse[orow] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : neg_inf();
     }
+  };
+  if (pf) {   // items tid and tid + blockDim, from the prefetched partials
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int item = tid + k * static_cast<int>(blockDim.x);
+      if (item >= nitems) continue;
+      const int rho = item / D4, d4 = item % D4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s = 0; s < kPF; ++s) {
+        if (s < S_total) {
+          const float w = wt[s * 8 + rho];
+          acc.x = fmaf(w, pre[k][s].x, acc.x);
+          acc.y = fmaf(w, pre[k][s].y, acc.y);
+          acc.z = fmaf(w, pre[k][s].z, acc.z);
+          acc.w = fmaf(w, pre[k][s].w, acc.w);
+        }
+      }
+      put(rho, d4, acc);
+    }
+    return;
+  }
+  // Streaming: tpi adjacent lanes share an item (few rows leave threads
+  // spare) and split its partials between them.
+  const int spare = static_cast<int>(blockDim.x) / max(1, nitems);
+  const int tpi = spare >= 8 ? 8 : (spare >= 4 ? 4 : (spare >= 2 ? 2 : 1));
+  const int per_round = static_cast<int>(blockDim.x) / tpi;
+  for (int k = 0; k * per_round < nitems; ++k) {
+    const int item = k * per_round + tid / tpi, part = tid % tpi;
+    const bool valid = item < nitems;
+    const int rho = valid ? item / D4 : 0, d4 = valid ? item % D4 : 0;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (valid) {
+      const float4* src = reinterpret_cast<const float4*>(base + 2 * kMaxRows + rho * D) + d4;
+#pragma unroll 8
+      for (int s = part; s < S_total; s += tpi) {
+        const float w = wt[s * 8 + rho];
+        const float4 v = __ldcg(src + static_cast<long long>(s) * (PF / 4));
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+      }
+    }
+    for (int o2 = 1; o2 < tpi; o2 <<= 1) {   // the lanes of one item are adjacent
+      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o2);
+      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o2);
+      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o2);
+      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o2);
+    }
+    if (valid && part == 0) put(rho, d4, acc);
   }
 }
 
