@@ -130,32 +130,37 @@ __host__ __device__ constexpr bool halves_shift() {
   return kx_chan<MODE, D>(0, 0) == 0;
 }
 
-// Scaled queries q~ = q * sm_scale * log2(e) of unit (b, kvh) into qt [8][D]
-// (rows >= R zero): one 16-byte load of 8 channels per thread, all in flight
-// at once.  Returns the thread's max |q~|.
+// The queries of unit (b, kvh) as 16-byte slices of 8 channels: slice e is
+// row e / (D/8) (zero for rows >= R); one slice per thread (8 rows x D/8
+// slices <= 128 threads).  load_q issues the load, so that it is in flight
+// while the copies of the first tiles are issued; store_qt writes the scaled
+// queries q~ = q * sm_scale * log2(e) into qt [8][D] (no store when qt is
+// null) and returns the slice's max |q~|.
 template <int D>
-__device__ __forceinline__ float fill_qt(const AttendParams& p, int b, int kvh, float* qt) {
+__device__ __forceinline__ uint4 load_q(const AttendParams& p, int b, int kvh, int e) {
   constexpr int V8 = D / 8;
-  float qm = 0.f;
-  for (int e = threadIdx.x; e < kMaxRows * V8; e += NTHREADS) {
-    const int rho = e / V8, c = e % V8;
-    float v[8];
+  const int rho = e / V8, c = e % V8;
+  if (e >= kMaxRows * V8 || rho >= p.R) return make_uint4(0u, 0u, 0u, 0u);
+  const int i = rho / p.HG, hh = rho % p.HG;
+  const long long qrow = ((static_cast<long long>(b) * p.gamma + i) * p.Hq + kvh * p.HG + hh) * D;
+  return *reinterpret_cast<const uint4*>(p.q + qrow + 8 * c);
+}
+
+template <int D>
+__device__ __forceinline__ float store_qt(const AttendParams& p, int e, const uint4& w, float* qt) {
+  constexpr int V8 = D / 8;
+  if (e >= kMaxRows * V8) return 0.f;
+  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  float v[8], qm = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) v[k] = 0.f;
-    if (rho < p.R) {
-      const int i = rho / p.HG, hh = rho % p.HG;
-      const long long qrow = ((static_cast<long long>(b) * p.gamma + i) * p.Hq + kvh * p.HG + hh) * D;
-      const uint4 w = *reinterpret_cast<const uint4*>(p.q + qrow + 8 * c);
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  for (int k = 0; k < 4; ++k) {
+    v[2 * k] = __uint_as_float(ww[k] << 16) * p.qscale;
+    v[2 * k + 1] = __uint_as_float(ww[k] & 0xFFFF0000u) * p.qscale;
+  }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        v[2 * k] = __uint_as_float(ww[k] << 16) * p.qscale;
-        v[2 * k + 1] = __uint_as_float(ww[k] & 0xFFFF0000u) * p.qscale;
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) qm = fmaxf(qm, fabsf(v[k]));
-    }
-    float4* dst = reinterpret_cast<float4*>(qt + rho * D + 8 * c);
+  for (int k = 0; k < 8; ++k) qm = fmaxf(qm, fabsf(v[k]));
+  if (qt) {
+    float4* dst = reinterpret_cast<float4*>(qt + (e / V8) * D + 8 * (e % V8));
     dst[0] = make_float4(v[0], v[1], v[2], v[3]);
     dst[1] = make_float4(v[4], v[5], v[6], v[7]);
   }
@@ -647,6 +652,8 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
   };
 
   // ---- setup: each warp's barriers first, so its first tiles load at once ----
+  const uint4 q_slice = load_q<D>(p, b, kvh, tid);
+  static_assert(kMaxRows * (D / 8) <= NTHREADS, "one query slice per thread");
   if (lane == 0) {
     for (int s2 = 0; s2 < SPW; ++s2) mbar_init(full + warp * SPW + s2, 1);
     fence_mbar_init();
@@ -660,7 +667,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
     for (int e = tid; e < bm_words; e += blockDim.x) bitmap[e] = 0u;
   // scaled queries, and per warp the max |q~| (for the weight normalizer)
   {
-    float qm = fill_qt<D>(p, b, kvh, qt);
+    float qm = store_qt<D>(p, tid, q_slice, qt);
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o2));
     if (lane == 0) reinterpret_cast<float*>(smem + L::SRC_OFF + NW * 48)[warp] = qm;

@@ -379,6 +379,13 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
     if (new_grp)
       bulk_g2s(sbase + L::KSZ_OFF, p.c.ksz + (u * (p.c.C / G) + t0 / G) * 2 * D, kszb, full + slot, pol);
   };
+  // the first heads' query values are loaded before the first copies issue
+  constexpr int kQPre = 8;
+  static_assert(D <= NTHREADS, "one query channel per thread");
+  uint16_t qpre[kQPre];
+  const long long qoff = (static_cast<long long>(b) * p.Hq + kvh * p.HG) * D + tid;
+#pragma unroll
+  for (int hh = 0; hh < kQPre; ++hh) qpre[hh] = (tid < D && hh < p.HG) ? p.q[qoff + hh * D] : 0;
   if (lane == 0) {
     for (int s2 = 0; s2 < SPW; ++s2) mbar_init(full + warp * SPW + s2, 1);
     fence_mbar_init();
@@ -387,13 +394,13 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   int issued = min(SPW, my_tiles), consumed = 0;
   if (tid == 0) misc[0] = 0;
   // summed query (ascending head order, fp32) while the first tiles load
-  for (int d = tid; d < D; d += blockDim.x) {
+  if (tid < D) {
     float acc = 0.f;
-    for (int hh = 0; hh < p.HG; ++hh) {
-      const long long off = (static_cast<long long>(b) * p.Hq + kvh * p.HG + hh) * D + d;
-      acc = __fadd_rn(acc, bf16_to_f32(p.q[off]));
-    }
-    qs[d] = acc;
+#pragma unroll
+    for (int hh = 0; hh < kQPre; ++hh)
+      if (hh < p.HG) acc = __fadd_rn(acc, bf16_to_f32(qpre[hh]));
+    for (int hh = kQPre; hh < p.HG; ++hh) acc = __fadd_rn(acc, bf16_to_f32(p.q[qoff + hh * D]));
+    qs[tid] = acc;
   }
   __syncthreads();
   volatile int* abort_flag = misc;
