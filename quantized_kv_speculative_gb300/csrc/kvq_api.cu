@@ -62,21 +62,36 @@ long long units_of(const kvq_cache* c) {
 }
 
 // Quantized splits per (b, kvh) for attention, and the chunk size.  `slots` is
-// how many CTAs of the kernel fit on the device at once; together with the
-// `tail` CTAs per (b, kvh) the splits fill one wave of it where they can.
-int attend_splits(long long Lq, long long U, long long slots, long long tail, long long* chunk) {
+// how many CTAs of the kernel fit on the device at once.  Over the split counts
+// from the fewest the chunk limit allows to the kTargetCtas share, pick the one
+// with the smallest waves x (chunk + per-split overhead), the `tail` CTAs per
+// (b, kvh) counted in the waves; chunks are multiples of kChunkAlign.
+int attend_splits(long long Lq, long long U, long long slots, long long tail, long long max_chunk, long long* chunk) {
   if (Lq <= 0) {
     *chunk = 0;
     return 0;
   }
-  const long long want = slots > 0 ? std::max(1LL, slots / U - tail) : ceil_div(kTargetCtas, U);
-  const long long target = std::min<long long>(kMaxQuantSplits, std::min(want, std::max(1LL, ceil_div(kTargetCtas, U))));
-  long long S = std::min(ceil_div(Lq, kChunkAlign), target);
-  S = std::max(S, ceil_div(Lq, kMaxChunk));
-  S = std::max(S, 1LL);
-  long long ch = ceil_div(ceil_div(Lq, S), kChunkAlign) * kChunkAlign;
-  *chunk = ch;
-  return static_cast<int>(ceil_div(Lq, ch));
+  const long long s_min = std::max(1LL, ceil_div(Lq, max_chunk));
+  const long long s_cap = std::max(
+      s_min, std::min<long long>(kMaxQuantSplits, std::min(ceil_div(Lq, kChunkAlign), std::max(1LL, ceil_div(kTargetCtas, U)))));
+  long long best_s = 0, best_ch = 0, best_cost = 0;
+  for (long long S = s_min; S <= s_cap; ++S) {
+    const long long ch = ceil_div(ceil_div(Lq, S), kChunkAlign) * kChunkAlign;
+    if (ch > max_chunk || ceil_div(Lq, ch) != S) continue;
+    const long long waves = slots > 0 ? ceil_div(U * (S + tail), slots) : 1;
+    const long long cost = waves * (ch + kSplitOverheadTokens);
+    if (best_s == 0 || cost < best_cost || (slots <= 0 && S > best_s)) {
+      best_s = S;
+      best_ch = ch;
+      best_cost = cost;
+    }
+  }
+  if (best_s == 0) {   // no split count meets both limits exactly: the chunk limit wins
+    best_ch = std::min(max_chunk, ceil_div(ceil_div(Lq, s_min), kChunkAlign) * kChunkAlign);
+    best_s = ceil_div(Lq, best_ch);
+  }
+  *chunk = best_ch;
+  return static_cast<int>(best_s);
 }
 
 int attend_splits_max(const kvq_cache_desc* d) {
@@ -328,6 +343,7 @@ kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int3
   p.partials = reinterpret_cast<float*>(ws + kStatusBytes + align256(U * 4));
   long long chunk = 0;
   const long long slots = attend_resident_ctas(mode, cache->desc.head_dim, cache->desc.group_size, gamma * HG);
+  const long long max_chunk = max_chunk_for_rows(gamma * HG);
   // The bf16 tail (residual, pending and selected tokens) goes to CTAs of its
   // own when they fit in the first wave beside the quantized splits without
   // making the chunks longer; otherwise each quantized split takes a slice of
@@ -336,15 +352,15 @@ kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int3
   const int S_t = static_cast<int>(std::min<long long>(kMaxTailSplits, std::max(1LL, ceil_div(ntail, kTailTokensPerSplit))));
   if (cache->quantized_len > 0) {
     long long ch_fused = 0, ch_sep = 0;
-    const int sq_fused = attend_splits(cache->quantized_len, U, slots, 0, &ch_fused);
-    const int sq_sep = attend_splits(cache->quantized_len, U, slots, S_t, &ch_sep);
+    const int sq_fused = attend_splits(cache->quantized_len, U, slots, 0, max_chunk, &ch_fused);
+    const int sq_sep = attend_splits(cache->quantized_len, U, slots, S_t, max_chunk, &ch_sep);
     const bool sep = slots > 0 && (sq_sep + S_t) * U <= slots && ch_sep <= ch_fused;
     p.S_t = sep ? S_t : 0;
     p.S_q = sep ? sq_sep : sq_fused;
     chunk = sep ? ch_sep : ch_fused;
   } else {
     p.S_t = S_t;
-    p.S_q = attend_splits(cache->quantized_len, U, slots, p.S_t, &chunk);
+    p.S_q = attend_splits(cache->quantized_len, U, slots, p.S_t, max_chunk, &chunk);
   }
   p.chunk = chunk;
   p.wait_limit = kDefaultWaitLimit;

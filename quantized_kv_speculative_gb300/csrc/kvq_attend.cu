@@ -75,7 +75,8 @@ struct Smem {
   static constexpr int VSZ_BYTES = TT * 2 * NJ * 4;
   static constexpr int SLOT = VSZ_OFF + VSZ_BYTES;
   static constexpr int WB_BYTES = NT == 1 ? NW * 16 * D : 0;     // staged weight fragments (one n-tile)
-  static constexpr int FIXED = kMaxRows * D * 4 + (kMaxChunk / 32) * 4 + 16 * 8 + WB_BYTES + NW * 48 + 272;
+  static constexpr int BM_WORDS = (NT == 2 ? kMaxChunkWide : kMaxChunk) / 32;   // selection bitmap words
+  static constexpr int FIXED = kMaxRows * D * 4 + BM_WORDS * 4 + 16 * 8 + WB_BYTES + NW * 48 + 272;
   static constexpr int MIN_TOTAL = NW * 2 * SLOT + FIXED;
   // stage slots per warp: as many as fit (2..4) at the target CTAs per SM
   static constexpr int SPW_FIT = (kSmemPerSm / target_ctas<MODE, D, NJ, NT>() - 1024 - FIXED) / (NW * SLOT);
@@ -89,7 +90,6 @@ struct Smem {
   static constexpr int NSLOT = NW * SPW;
   static constexpr int QT_OFF = NSLOT * SLOT;                 // scaled queries q~ [8][D] f32
   static constexpr int BM_OFF = QT_OFF + kMaxRows * D * 4;    // selection bitmap
-  static constexpr int BM_WORDS = kMaxChunk / 32;
   static constexpr int BAR_OFF = BM_OFF + BM_WORDS * 4;
   static constexpr int WB_OFF = (BAR_OFF + NSLOT * 8 + 15) / 16 * 16;   // per warp: staged weight fragments
   static constexpr int SRC_OFF = WB_OFF + WB_BYTES;                 // [8 cols][4 chunks][D/8 pairs] u32 per warp
