@@ -9,16 +9,18 @@
 // the top-k tokens use their 16-bit KV (SpeCache page, "Approach").
 //
 // One launch, grid = B*Hkv*S_t tail CTAs followed by B*Hkv*S_q quantized-split CTAs.
-//  * Quantized split: one producer warp streams 32..64-token tiles of the
-//    mode's planes and scales into shared memory with 1-D bulk (TMA) copies on
-//    an mbarrier ring.  Four consumer warps each own a contiguous run of tiles.
-//    They turn codes into f16 in registers and run QK^T and PV on tensor cores
-//    (m16n8k16): keys are the A operand (16 tokens x 16 channels) against the
-//    folded query weights, values the A operand of O^T = V^T P^T.  The folded
-//    weights and the folded probabilities are each split into high + low f16
-//    parts.  Softmax is online in fp32 (base-2 logits).
-//  * Tail CTA: the bf16 residual buffer, the pending speculative tokens (causal)
-//    and the 16-bit selected tokens, on CUDA cores.
+//  * Quantized split: four warps each own a contiguous run of 32..64-token
+//    tiles; each warp's lane 0 streams its tiles of the mode's planes and
+//    scales into the warp's ring of shared-memory slots with 1-D bulk (TMA)
+//    copies on mbarriers.  The warps turn codes into f16 in registers and run
+//    QK^T and PV on tensor cores (m16n8k16): keys are the A operand (16 tokens
+//    x 16 channels) against the folded query weights, values the A operand of
+//    O^T = V^T P^T.  The folded weights and the folded probabilities are each
+//    split into high + low f16 parts.  Softmax is online in fp32 (base-2
+//    logits).
+//  * The bf16 tail (residual buffer, pending speculative tokens (causal) and
+//    16-bit selected tokens) runs as bf16 m16n8k16 MMAs, either in tail CTAs
+//    or shared out over the quantized splits.
 //  * Every CTA writes an (m, l, o) partial.  The CTA that arrives last at a
 //    per-(b, kvh) atomic ticket merges all partials into the bf16 output and LSE,
 //    then resets the ticket.  No CTA ever waits on another.
