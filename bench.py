@@ -233,13 +233,9 @@ def run_device(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_step = ms_total / args.steps
-    value = spec.kv_tokens_per_step * world / (ms_step * 1e-3)
+    value = whole_job_rate(spec.kv_tokens_per_step, world, ms_step * 1e-3)
 
     # ---- dominant kernel: INT8 verify attention, back-to-back launches ----
     def per_call_ms(fn, reps=64, rounds=8):
@@ -337,11 +333,7 @@ def run_device(args, rank, world):
     t0 = time.perf_counter()
     for i in range(n_e2e):
         e2e_step(i)
-    e2e_s = (time.perf_counter() - t0) / n_e2e
-    if world > 1:
-        tt = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world, dev)
     for ws in wss:
         assert kvq.kvq_workspace_status(ws) == 0, "device status word set"
 
@@ -364,7 +356,7 @@ def run_device(args, rank, world):
                      "peak": peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s", "frac": att_gbs / peak,
                      "traffic": traffic, "algorithmic_bytes_per_launch": spec.attend_bytes(),
                      "timing": "64 back-to-back launches over 4 rotating caches, CUDA events"},
-        "e2e": {"value": spec.kv_tokens_per_step * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_rate(spec.kv_tokens_per_step, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
@@ -376,6 +368,22 @@ def run_device(args, rank, world):
 # --------------------------------------------------------------------------------------
 # oracle (CPU) arm
 # --------------------------------------------------------------------------------------
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The largest of the ranks' values of x (each rank's timed seconds or ms),
+    through the default process group; x itself with one rank."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: float, world: int, seconds_per_step: float) -> float:
+    """Whole-job throughput: every rank's units of one step over the slowest
+    rank's time per step (replicas: per-rank work is fixed as ranks grow)."""
+    return units_per_rank_step * world / seconds_per_step
+
 
 def kernel_source_hash() -> str:
     """sha256 over the sources the attention kernel is built from."""
