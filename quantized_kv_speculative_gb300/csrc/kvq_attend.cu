@@ -558,7 +558,6 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
   using M = Mode<MODE>;
   using RW = Rows<MODE, D>;
   using L = Smem<MODE, D, NJ, NT>;
-  using XP = XPair<MODE>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int g = lane >> 2, q = lane & 3;
@@ -700,8 +699,8 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const int i = 2 * s + par;
-      tokA[s] = oct + (MODE == KVQ_MODE_INT8 ? s + 4 * par : i);
-      tokB[s] = tokA[s] + (MODE == KVQ_MODE_INT8 ? 2 : 4);
+      tokA[s] = oct + xpair_a<MODE>(i);
+      tokB[s] = oct + xpair_b<MODE>(i);
       vinv[s] = 1.0f / vx_mult<MODE>(i);
     }
 

@@ -131,7 +131,7 @@ __device__ __forceinline__ void key_pairs(const uint8_t* k0, int /*plane_stride*
 // logits from the encoding's offset times the sum of their weights.
 //
 // For values, a lane reads 8 consecutive tokens 8q..8q+7 of a channel row;
-// pair i covers tokens 8q + VA[i], 8q + VB[i] with factor vx_mult(i).  For the
+// pair i covers tokens 8q + xpair_a(i), 8q + xpair_b(i) with factor vx_mult(i).  For the
 // key chunk of a lane (D/4 channels of a token row), pair p covers channels
 // kx_chan(p, 0) and kx_chan(p, 1).
 // ------------------------------------------------------------------------------
@@ -141,17 +141,19 @@ constexpr uint32_t X64B = 0x64646464u;    // prmt source of the 0x64 bytes
 
 __device__ __forceinline__ uint32_t xsel(uint32_t w, uint32_t mask) { return (w & mask) | X1024; }
 
+// Value token pair i of a lane's 8 tokens 8q..8q+7: tokens 8q + xpair_a(i)
+// and 8q + xpair_b(i).  INT8: the merged nibble planes give the even tokens'
+// bytes in one word and the odd tokens' in another; pairs (0,2), (1,3), (4,6),
+// (5,7) keep the key rows that the two lanes of a quarter-warp read one row
+// apart (no shared-memory bank conflict).  Others: (0,4), (1,5), (2,6), (3,7).
 template <int MODE>
-struct XPair {
-  // value token pairs per pair index i (tokens relative to 8q)
-  static constexpr int VA[4] = {0, 1, 2, 3};
-  static constexpr int VB[4] = {4, 5, 6, 7};
-};
-template <>
-struct XPair<KVQ_MODE_INT8> {
-  static constexpr int VA[4] = {0, 4, 1, 5};
-  static constexpr int VB[4] = {2, 6, 3, 7};
-};
+__host__ __device__ constexpr int xpair_a(int i) {
+  return MODE == KVQ_MODE_INT8 ? 4 * (i >> 1) + (i & 1) : i;
+}
+template <int MODE>
+__host__ __device__ constexpr int xpair_b(int i) {
+  return xpair_a<MODE>(i) + (MODE == KVQ_MODE_INT8 ? 2 : 4);
+}
 
 // Value factor of pair i: the power of two at which the pair's codes sit.
 // Every value code sits at mantissa bit 4 or higher (INT8 codes are 8 bits
@@ -246,10 +248,11 @@ __device__ __forceinline__ void value_frags_x(const uint8_t* va, const uint8_t* 
     const uint32_t Oa = (ha & 0xF0F0F0F0u) | ((la >> 4) & 0x0F0F0F0Fu);
     const uint32_t Eb = ((hb << 4) & 0xF0F0F0F0u) | (lb & 0x0F0F0F0Fu);
     const uint32_t Ob = (hb & 0xF0F0F0F0u) | ((lb >> 4) & 0x0F0F0F0Fu);
-    pa[0] = __byte_perm(Ea, X64B, 0x4140); pa[1] = __byte_perm(Ea, X64B, 0x4342);
-    pa[2] = __byte_perm(Oa, X64B, 0x4140); pa[3] = __byte_perm(Oa, X64B, 0x4342);
-    pb[0] = __byte_perm(Eb, X64B, 0x4140); pb[1] = __byte_perm(Eb, X64B, 0x4342);
-    pb[2] = __byte_perm(Ob, X64B, 0x4140); pb[3] = __byte_perm(Ob, X64B, 0x4342);
+    // E byte k = token 2k, O byte k = token 2k + 1 (pairs per xpair_a / xpair_b)
+    pa[0] = __byte_perm(Ea, X64B, 0x4140); pa[1] = __byte_perm(Oa, X64B, 0x4140);
+    pa[2] = __byte_perm(Ea, X64B, 0x4342); pa[3] = __byte_perm(Oa, X64B, 0x4342);
+    pb[0] = __byte_perm(Eb, X64B, 0x4140); pb[1] = __byte_perm(Ob, X64B, 0x4140);
+    pb[2] = __byte_perm(Eb, X64B, 0x4342); pb[3] = __byte_perm(Ob, X64B, 0x4342);
   } else if constexpr (MODE == KVQ_MODE_INT4) {
     // nibble i of the word is token 8q + i; every pair lands at mantissa bits 4-7
     const uint32_t wa = *reinterpret_cast<const uint32_t*>(va + 4 * q);
