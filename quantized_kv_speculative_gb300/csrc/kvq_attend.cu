@@ -44,6 +44,11 @@ namespace {
 constexpr int NW = 4;                  // warps per CTA; each streams and consumes its own tiles
 constexpr int NTHREADS = NW * 32;
 constexpr int kSmemPerSm = 228 * 1024;
+// q~ in shared memory: row stride D + 4 floats, each quarter (D/4 channels,
+// one lane chunk) padded by one float, so that the lanes deriving weights
+// (different rows and chunks, the same channel offset) hit different banks.
+template <int D> __host__ __device__ constexpr int qt_row() { return D + 4; }
+template <int D> __host__ __device__ constexpr int qt_chunk() { return D / 4 + 1; }
 
 template <int MODE, int D, int NJ, int NT>
 struct Smem;
@@ -78,7 +83,7 @@ struct Smem {
   static constexpr int SLOT = VSZ_OFF + VSZ_BYTES;
   static constexpr int WB_BYTES = NT == 1 ? NW * 16 * D : 0;     // staged weight fragments (one n-tile)
   static constexpr int BM_WORDS = (NT == 2 ? kMaxChunkWide : kMaxChunk) / 32;   // selection bitmap words
-  static constexpr int FIXED = kMaxRows * D * 4 + BM_WORDS * 4 + 16 * 8 + WB_BYTES + NW * 48 + 272;
+  static constexpr int FIXED = kMaxRows * qt_row<D>() * 4 + BM_WORDS * 4 + 16 * 8 + WB_BYTES + NW * 48 + 272;
   static constexpr int MIN_TOTAL = NW * 2 * SLOT + FIXED;
   // stage slots per warp: as many as fit (2..4) at the target CTAs per SM
   static constexpr int SPW_FIT = (kSmemPerSm / target_ctas<MODE, D, NJ, NT>() - 1024 - FIXED) / (NW * SLOT);
@@ -90,8 +95,8 @@ struct Smem {
   static constexpr int SPW_SCR = (SCRATCH_NEED + NW * SLOT - 1) / (NW * SLOT);
   static constexpr int SPW = SPW_BASE > SPW_SCR ? SPW_BASE : SPW_SCR;
   static constexpr int NSLOT = NW * SPW;
-  static constexpr int QT_OFF = NSLOT * SLOT;                 // scaled queries q~ [8][D] f32
-  static constexpr int BM_OFF = QT_OFF + kMaxRows * D * 4;    // selection bitmap
+  static constexpr int QT_OFF = NSLOT * SLOT;                 // scaled queries q~ [8][qt_row] f32
+  static constexpr int BM_OFF = QT_OFF + kMaxRows * qt_row<D>() * 4;   // selection bitmap
   static constexpr int BAR_OFF = BM_OFF + BM_WORDS * 4;
   static constexpr int WB_OFF = (BAR_OFF + NSLOT * 8 + 15) / 16 * 16;   // per warp: staged weight fragments
   static constexpr int SRC_OFF = WB_OFF + WB_BYTES;                 // [8 cols][4 chunks][D/8 pairs] u32 per warp
@@ -136,7 +141,7 @@ __host__ __device__ constexpr bool halves_shift() {
 // row e / (D/8) (zero for rows >= R); one slice per thread (8 rows x D/8
 // slices <= 128 threads).  load_q issues the load, so that it is in flight
 // while the copies of the first tiles are issued; store_qt writes the scaled
-// queries q~ = q * sm_scale * log2(e) into qt [8][D] (no store when qt is
+// queries q~ = q * sm_scale * log2(e) into qt [8][qt_row] (no store when qt is
 // null) and returns the slice's max |q~|.
 template <int D>
 __device__ __forceinline__ uint4 load_q(const AttendParams& p, int b, int kvh, int e) {
@@ -162,9 +167,10 @@ __device__ __forceinline__ float store_qt(const AttendParams& p, int e, const ui
 #pragma unroll
   for (int k = 0; k < 8; ++k) qm = fmaxf(qm, fabsf(v[k]));
   if (qt) {
-    float4* dst = reinterpret_cast<float4*>(qt + (e / V8) * D + 8 * (e % V8));
-    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+    const int ch = 8 * (e % V8);   // 8 channels within one quarter
+    float* dst = qt + (e / V8) * qt_row<D>() + (ch / (D / 4)) * qt_chunk<D>() + ch % (D / 4);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) dst[k] = v[k];
   }
   return qm;
 }
@@ -804,7 +810,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              const float* qr = qt + (4 * nt + (g >> 1)) * D + cb;
+              const float* qr = qt + (4 * nt + (g >> 1)) * qt_row<D>() + q * qt_chunk<D>() + par * DELTA;
               float ws = 0.f, zs = 0.f;
               uint32_t keep[HP], send[HP];
 #pragma unroll
@@ -847,12 +853,13 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
             E2 = pow2i(e);
             kscale_new = pow2i(-e);
             const float f = E2 * KW;
-            const float* qr = qt + wrow * D;
+            const float* qr = qt + wrow * qt_row<D>();
             const int col = 2 * (wrow & 3), ntw = wrow >> 2;
             for (int it = wsub; it < PPR; it += lpr) {
               const int qq = it / (D / 8), pp = it % (D / 8);
               const int c0 = qq * (D / 4) + kx_chan<MODE, D>(pp, 0), c1 = qq * (D / 4) + kx_chan<MODE, D>(pp, 1);
-              const float q0 = qr[c0], q1 = qr[c1];
+              const float q0 = qr[qq * qt_chunk<D>() + kx_chan<MODE, D>(pp, 0)];
+              const float q1 = qr[qq * qt_chunk<D>() + kx_chan<MODE, D>(pp, 1)];
               const float w0 = q0 * ks[c0] * f, w1 = q1 * ks[c1] * f;
               const uint32_t hi = pack_half2(w0, w1);
               const float2 hf = unpack_half2(hi);
