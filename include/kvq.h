@@ -200,15 +200,41 @@ size_t kvq_workspace_bytes(const kvq_cache* cache, int32_t num_q_heads, int32_t 
  *           query that sees no key gets out = 0 and lse = -inf.
  *  Every residual token is visible to every query.  Results do not depend on
  *  how the work is split.
- * Enqueues one kernel.  It splits the quantized context over CTAs, runs one
- * extra CTA per (b, kvh) for the bf16 tail, and merges the partials in whichever
- * CTA of each (b, kvh) finishes last.
+ * Enqueues one kernel.  It splits the quantized context over CTAs and runs one
+ * or more CTAs per (b, kvh) for the bf16 tail (kvq_attend_plan reports the
+ * split).  When the CTAs of a (b, kvh) number at most 16 and their clusters fit
+ * the device as well as plain CTAs would, they run as one thread-block cluster
+ * and merge their partials through shared memory; otherwise the partials go to
+ * the workspace and whichever CTA of the (b, kvh) finishes last merges them.
+ * Setting the environment variable KVQ_ATTEND_CLUSTERS=0 (read on every call)
+ * selects the second way for every launch.
  */
 kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int32_t num_q_heads,
                       int32_t gamma, const void* pend_k, const void* pend_v, int32_t n_pend,
                       const int32_t* sel_idx, const void* sel_k, const void* sel_v, int32_t top_k,
                       float sm_scale, void* out, float* lse, void* workspace, size_t ws_bytes,
                       kvq_stream_t stream);
+
+/*
+ * How kvq_attend would split a call with these arguments on the current
+ * device.  The paper has no counterpart: this reports the launch plan.
+ *  plan->quant_splits  CTAs per (b, kvh) over the quantized context (0 if empty)
+ *  plan->tail_splits   CTAs per (b, kvh) for the bf16 tail (0: the quantized
+ *                      splits share it out)
+ *  plan->chunk_tokens  quantized tokens per split (a multiple of 128)
+ *  plan->cluster       1 when each (b, kvh) runs as one thread-block cluster
+ * Arguments are checked as kvq_attend checks them; nothing is enqueued.
+ */
+typedef struct kvq_attend_plan_info {
+  int32_t quant_splits;
+  int32_t tail_splits;
+  int64_t chunk_tokens;
+  int32_t cluster;
+  int32_t reserved;
+} kvq_attend_plan_info;
+
+kvq_status kvq_attend_plan(const kvq_cache* cache, kvq_mode mode, int32_t num_q_heads, int32_t gamma,
+                           int32_t n_pend, int32_t top_k, kvq_attend_plan_info* plan);
 
 /*
  * Per KV head, the top_k quantized tokens that score highest under the

@@ -34,7 +34,7 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "K
 EXPORTED = (
     "kvq_status_string", "kvq_cache_bytes", "kvq_cache_init", "kvq_quantize_append",
     "kvq_workspace_bytes", "kvq_attend", "kvq_topk", "kvq_workspace_status",
-    "kvq_selftest_bounded_wait", "kvq_attend_static_scratch",
+    "kvq_selftest_bounded_wait", "kvq_attend_static_scratch", "kvq_attend_plan",
 )
 
 
@@ -53,6 +53,11 @@ class KvqCache(ctypes.Structure):
                 ("quantized_len", ctypes.c_int64), ("residual_len", ctypes.c_int32),
                 ("residual_start", ctypes.c_int32), ("magic", ctypes.c_uint32),
                 ("reserved1", ctypes.c_uint32)]
+
+
+class KvqAttendPlanInfo(ctypes.Structure):
+    _fields_ = [("quant_splits", ctypes.c_int32), ("tail_splits", ctypes.c_int32),
+                ("chunk_tokens", ctypes.c_int64), ("cluster", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class KVQError(RuntimeError):
@@ -91,6 +96,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kvq_attend_static_scratch.argtypes = [cache_p, ctypes.c_int, vp, i32, i32, vp, vp, i32, vp, vp, vp,
                                               i32, f32, vp, vp, vp]
     lib.kvq_attend_static_scratch.restype = ctypes.c_int
+    lib.kvq_attend_plan.argtypes = [cache_p, ctypes.c_int, i32, i32, i32, i32, ctypes.POINTER(KvqAttendPlanInfo)]
+    lib.kvq_attend_plan.restype = ctypes.c_int
     lib.kvq_topk.argtypes = [cache_p, ctypes.c_int, vp, i32, i32, vp, vp, vp, sz, vp]
     lib.kvq_topk.restype = ctypes.c_int
     lib.kvq_workspace_status.argtypes = [vp, sz, vp]
@@ -250,6 +257,19 @@ def kvq_attend(cache: QuantizedKVCache, mode: str, q: torch.Tensor, pend_k=None,
                           workspace.numel(), _stream(stream)),
            "kvq_attend")
     return out, lse
+
+
+def kvq_attend_plan(cache: QuantizedKVCache, mode: str, num_q_heads: int, gamma: int, n_pend: int = 0,
+                    top_k: int = 0) -> dict:
+    """How ``kvq_attend`` would split such a call on the current device:
+    quantized splits, tail splits, chunk tokens and whether each (b, kv head)
+    runs as one thread-block cluster."""
+    info = KvqAttendPlanInfo()
+    lib = load_library()
+    _check(lib.kvq_attend_plan(ctypes.byref(cache.struct), MODES[mode], num_q_heads, gamma, n_pend, top_k,
+                               ctypes.byref(info)), "kvq_attend_plan")
+    return {"quant_splits": info.quant_splits, "tail_splits": info.tail_splits,
+            "chunk_tokens": info.chunk_tokens, "cluster": bool(info.cluster)}
 
 
 def kvq_attend_static_scratch(cache: QuantizedKVCache, mode: str, q: torch.Tensor, pend_k=None, pend_v=None,

@@ -2,6 +2,7 @@
 // 2G double-buffer state machine, split sizing, workspace layout and launches.
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 
 #include "kvq_internal.h"
@@ -94,6 +95,13 @@ int attend_splits(long long Lq, long long U, long long slots, long long tail, lo
   return static_cast<int>(best_s);
 }
 
+// The cluster combine is on unless the environment sets KVQ_ATTEND_CLUSTERS=0
+// (read on every call; the ticket combine then serves every launch).
+bool clusters_enabled() {
+  const char* v = std::getenv("KVQ_ATTEND_CLUSTERS");
+  return !(v && v[0] == '0' && v[1] == '\0');
+}
+
 int attend_splits_max(const kvq_cache_desc* d) {
   const long long U = static_cast<long long>(d->batch) * d->num_kv_heads;
   const long long Lq = d->capacity_tokens;
@@ -159,6 +167,47 @@ bool mode_reads(int mode, int fmt) {
     case KVQ_MODE_INT1: return fmt == KVQ_FMT_INT1;
     default: return false;
   }
+}
+
+// The attention launch plan: quantized splits and chunk, tail CTAs, and
+// whether each (b, kvh) runs as one thread-block cluster.
+struct AttendPlan {
+  int S_q, S_t;
+  long long chunk;
+  int cluster;
+};
+
+AttendPlan plan_attend(const kvq_cache* cache, int mode, int R, int n_pend, int top_k) {
+  AttendPlan pl{};
+  const long long U = units_of(cache);
+  const long long slots = attend_resident_ctas(mode, cache->desc.head_dim, cache->desc.group_size, R);
+  const long long max_chunk = max_chunk_for_rows(R);
+  // The bf16 tail (residual, pending and selected tokens) goes to CTAs of its
+  // own when they fit in the first wave beside the quantized splits without
+  // making the chunks longer; otherwise each quantized split takes a slice of
+  // it after its own tokens.
+  const long long ntail = static_cast<long long>(cache->residual_len) + n_pend + top_k;
+  const int S_t = static_cast<int>(std::min<long long>(kMaxTailSplits, std::max(1LL, ceil_div(ntail, kTailTokensPerSplit))));
+  if (cache->quantized_len > 0) {
+    long long ch_fused = 0, ch_sep = 0;
+    const int sq_fused = attend_splits(cache->quantized_len, U, slots, 0, max_chunk, &ch_fused);
+    const int sq_sep = attend_splits(cache->quantized_len, U, slots, S_t, max_chunk, &ch_sep);
+    const bool sep = slots > 0 && (sq_sep + S_t) * U <= slots && ch_sep <= ch_fused;
+    pl.S_t = sep ? S_t : 0;
+    pl.S_q = sep ? sq_sep : sq_fused;
+    pl.chunk = sep ? ch_sep : ch_fused;
+  } else {
+    pl.S_t = S_t;
+    pl.S_q = attend_splits(cache->quantized_len, U, slots, pl.S_t, max_chunk, &pl.chunk);
+  }
+  // One cluster per (b, kvh), combining in shared memory, when its CTAs fit
+  // the cluster limit and the clusters fill no more waves than the plan counted.
+  const int S_all = pl.S_q + pl.S_t;
+  if (S_all >= 1 && S_all <= kMaxClusterCtas && slots > 0 && clusters_enabled()) {
+    const long long cap = attend_resident_clusters(mode, cache->desc.head_dim, cache->desc.group_size, R, S_all);
+    if (cap > 0 && ceil_div(U, cap) <= ceil_div(U * S_all, slots)) pl.cluster = 1;
+  }
+  return pl;
 }
 
 }  // namespace
@@ -341,31 +390,32 @@ kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int3
   p.status = reinterpret_cast<int*>(ws);
   p.counters = reinterpret_cast<unsigned*>(ws + kStatusBytes);
   p.partials = reinterpret_cast<float*>(ws + kStatusBytes + align256(U * 4));
-  long long chunk = 0;
-  const long long slots = attend_resident_ctas(mode, cache->desc.head_dim, cache->desc.group_size, gamma * HG);
-  const long long max_chunk = max_chunk_for_rows(gamma * HG);
-  // The bf16 tail (residual, pending and selected tokens) goes to CTAs of its
-  // own when they fit in the first wave beside the quantized splits without
-  // making the chunks longer; otherwise each quantized split takes a slice of
-  // it after its own tokens.
-  const long long ntail = static_cast<long long>(cache->residual_len) + n_pend + top_k;
-  const int S_t = static_cast<int>(std::min<long long>(kMaxTailSplits, std::max(1LL, ceil_div(ntail, kTailTokensPerSplit))));
-  if (cache->quantized_len > 0) {
-    long long ch_fused = 0, ch_sep = 0;
-    const int sq_fused = attend_splits(cache->quantized_len, U, slots, 0, max_chunk, &ch_fused);
-    const int sq_sep = attend_splits(cache->quantized_len, U, slots, S_t, max_chunk, &ch_sep);
-    const bool sep = slots > 0 && (sq_sep + S_t) * U <= slots && ch_sep <= ch_fused;
-    p.S_t = sep ? S_t : 0;
-    p.S_q = sep ? sq_sep : sq_fused;
-    chunk = sep ? ch_sep : ch_fused;
-  } else {
-    p.S_t = S_t;
-    p.S_q = attend_splits(cache->quantized_len, U, slots, p.S_t, max_chunk, &chunk);
-  }
-  p.chunk = chunk;
+  const AttendPlan pl = plan_attend(cache, mode, gamma * HG, n_pend, top_k);
+  p.S_q = pl.S_q;
+  p.S_t = pl.S_t;
+  p.chunk = pl.chunk;
+  p.cluster = pl.cluster;
   p.wait_limit = kDefaultWaitLimit;
   if (p.S_q > attend_splits_max(&cache->desc)) return KVQ_ERR_WORKSPACE;
   if (launch_attend(p, mode, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_attend_plan(const kvq_cache* cache, kvq_mode mode, int32_t num_q_heads, int32_t gamma,
+                           int32_t n_pend, int32_t top_k, kvq_attend_plan_info* plan) {
+  if (!cache || cache->magic != kMagic) return KVQ_ERR_NOT_INITIALIZED;
+  if (!valid_desc(&cache->desc) || !plan) return KVQ_ERR_INVALID_ARG;
+  if (!mode_reads(mode, cache->desc.format)) return KVQ_ERR_UNSUPPORTED;
+  const int Hkv = cache->desc.num_kv_heads;
+  if (num_q_heads < Hkv || num_q_heads % Hkv || gamma < 1 || n_pend < 0 || top_k < 0 || top_k > kMaxTopk)
+    return KVQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(gamma) * (num_q_heads / Hkv) > kMaxRows) return KVQ_ERR_UNSUPPORTED;
+  const AttendPlan pl = plan_attend(cache, mode, gamma * (num_q_heads / Hkv), n_pend, top_k);
+  plan->quant_splits = pl.S_q;
+  plan->tail_splits = pl.S_t;
+  plan->chunk_tokens = pl.chunk;
+  plan->cluster = pl.cluster;
+  plan->reserved = 0;
   return KVQ_OK;
 }
 

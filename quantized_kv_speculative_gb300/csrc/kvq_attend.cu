@@ -8,7 +8,10 @@
 // low-bit copy is attended with the output token and a speculative token, and
 // the top-k tokens use their 16-bit KV (SpeCache page, "Approach").
 //
-// One launch, grid = B*Hkv*S_t tail CTAs followed by B*Hkv*S_q quantized-split CTAs.
+// One launch of B*Hkv*(S_q + S_t) CTAs: per (b, kvh) S_q quantized splits and
+// S_t tail CTAs, either as one thread-block cluster per (b, kvh) or (when the
+// clusters would not fit in the waves the split plan assumed, or S_q + S_t > 16)
+// as a plain grid with the tail CTAs first.
 //  * Quantized split: four warps each own a contiguous run of 32..64-token
 //    tiles; each warp's lane 0 streams its tiles of the mode's planes and
 //    scales into the warp's ring of shared-memory slots with 1-D bulk (TMA)
@@ -21,9 +24,11 @@
 //  * The bf16 tail (residual buffer, pending speculative tokens (causal) and
 //    16-bit selected tokens) runs as bf16 m16n8k16 MMAs, either in tail CTAs
 //    or shared out over the quantized splits.
-//  * Every CTA writes an (m, l, o) partial.  The CTA that arrives last at a
-//    per-(b, kvh) atomic ticket merges all partials into the bf16 output and LSE,
-//    then resets the ticket.  No CTA ever waits on another.
+//  * Every CTA makes an (m, l, o) partial.  In a cluster the partials stay in
+//    shared memory: after a cluster barrier each CTA merges its share of the
+//    output items from all of them.  Otherwise they go to the workspace and the
+//    CTA that arrives last at a per-(b, kvh) atomic ticket merges them into the
+//    bf16 output and LSE, then resets the ticket; no CTA waits on another.
 //
 // Folding (no per-element dequant FMA).  A key code c reads as the f16 value
 // E = off + c / kw (INT8: off = 1024, kw = 1; INT4/2/1: off = 1, kw = 2^b), so
@@ -115,6 +120,7 @@ struct Smem {
   static_assert(SCRATCH <= NSLOT * SLOT, "the merge scratch must fit in the slot area");
   static_assert((2 * kMaxCombine * 8 + 16) * 4 <= MISC_OFF, "the combine scratch must not reach the ticket flag");
   static_assert(SLOT % 16 == 0, "slots must stay 16-byte aligned");
+  static_assert(kMaxRows * qt_row<D>() >= kPartialFloats(D), "a CTA's partial must fit in the q~ area");
 };
 
 // 2^x with the hardware approximation (ex2.approx.ftz: relative error near
@@ -184,6 +190,23 @@ __device__ __forceinline__ float store_qt(const AttendParams& p, int e, const ui
 // combine takes one round trip to L2; otherwise they stream after the weights
 // with several splits in flight.
 // ------------------------------------------------------------------------------
+// Writes one output item of unit (b, kvh): row rho, channels 4 d4 .. 4 d4 + 3,
+// and for d4 = 0 the row's LSE from its base-2 max M and sum L.
+template <int D>
+__device__ __forceinline__ void put_item(const AttendParams& p, int b, int kvh, int rho, int d4, const float4& acc,
+                                         float M, float L) {
+  const int i = rho / p.HG, hh = rho % p.HG;
+  const int h = kvh * p.HG + hh;
+  const long long orow = (static_cast<long long>(b) * p.gamma + i) * p.Hq + h;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t*>(&lo);
+  pk.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p.out + orow * D + 4 * d4) = pk;
+  if (p.lse && d4 == 0) p.lse[orow] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : neg_inf();
+}
+
 template <int D, bool PREFETCH>
 __device__ void combine_unit(const AttendParams& p, long long u, int S_total, float* sm) {
   constexpr int D4 = D / 4;
@@ -236,22 +259,7 @@ __device__ void combine_unit(const AttendParams& p, long long u, int S_total, fl
     ml[8 + tid] = L;
   }
   __syncthreads();
-  // Writes one output item (row rho, channels 4 d4 .. 4 d4 + 3) and its LSE.
-  auto put = [&](int rho, int d4, const float4& acc) {
-    const int i = rho / p.HG, hh = rho % p.HG;
-    const int h = kvh * p.HG + hh;
-    const long long orow = (static_cast<long long>(b) * p.gamma + i) * p.Hq + h;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t*>(&lo);
-    pk.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(p.out + orow * D + 4 * d4) = pk;
-    if (p.lse && d4 == 0) {
-      const float M = ml[rho], L = ml[8 + rho];
-      p.lse[orow] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : neg_inf();
-    }
-  };
+  auto put = [&](int rho, int d4, const float4& acc) { put_item<D>(p, b, kvh, rho, d4, acc, ml[rho], ml[8 + rho]); };
   if (pf) {   // items tid and tid + blockDim, from the prefetched partials
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -303,6 +311,77 @@ __device__ void combine_unit(const AttendParams& p, long long u, int S_total, fl
     }
     if (valid && part == 0) put(rho, d4, acc);
   }
+}
+
+// Cluster combine: the S_total CTAs of unit u form one cluster and each holds
+// its partial in shared memory at `part` (the same offset in every CTA).
+// After the cluster barrier, CTA `rank` merges its share of the output items
+// (float4 of one row), reading the maxima, sums and outputs of every CTA
+// through distributed shared memory: tpi adjacent lanes share an item, each
+// taking at most four of the partials, and reduce by shuffles.  The second
+// barrier keeps every CTA's shared memory alive until all reads are done.
+template <int D>
+__device__ void cluster_combine(const AttendParams& p, long long u, int S_total, const float* part) {
+  constexpr int D4 = D / 4;
+  constexpr int KP = kMaxClusterCtas / 4;   // partials per lane
+  static_assert(kMaxClusterCtas % 4 == 0, "four lanes share the partials of an item");
+  cluster_sync();
+  const int b = static_cast<int>(u / p.c.Hkv), kvh = static_cast<int>(u % p.c.Hkv);
+  const int rank = static_cast<int>(cluster_rank());
+  const int n = p.R * D4, per = (n + S_total - 1) / S_total;
+  const int lo = rank * per, hi = min(n, lo + per);
+  const int tpi = S_total <= KP ? 1 : (S_total <= 2 * KP ? 2 : 4);
+  const int tid = threadIdx.x, sub = tid % tpi;
+  for (int base = lo; base < hi; base += NTHREADS / tpi) {   // the same trip count in every warp
+    const int item = base + tid / tpi;
+    const bool valid = item < hi;
+    const int rho = valid ? item / D4 : 0, d4 = valid ? item % D4 : 0;
+    float m[KP], l[KP];
+    float4 o[KP];
+    float M = neg_inf();
+#pragma unroll
+    for (int k = 0; k < KP; ++k) {
+      const int s = sub + k * tpi;
+      if (valid && s < S_total) {
+        m[k] = ld_dsmem(dsmem_addr(part + rho, s));
+        l[k] = ld_dsmem(dsmem_addr(part + kMaxRows + rho, s));
+        o[k] = ld_dsmem4(dsmem_addr(part + 2 * kMaxRows + rho * D + 4 * d4, s));
+      } else {
+        m[k] = neg_inf();
+        l[k] = 0.f;
+        o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      M = fmaxf(M, m[k]);
+    }
+    for (int o2 = 1; o2 < tpi; o2 <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < KP; ++k) {
+      const float f = (m[k] == neg_inf()) ? 0.f : fast_exp2(m[k] - M);
+      L = fmaf(f, l[k], L);
+      acc.x = fmaf(f, o[k].x, acc.x);
+      acc.y = fmaf(f, o[k].y, acc.y);
+      acc.z = fmaf(f, o[k].z, acc.z);
+      acc.w = fmaf(f, o[k].w, acc.w);
+    }
+    for (int o2 = 1; o2 < tpi; o2 <<= 1) {
+      L += __shfl_xor_sync(0xffffffffu, L, o2);
+      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o2);
+      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o2);
+      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o2);
+      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o2);
+    }
+    if (valid && sub == 0) {
+      const float inv = (L > 0.f) ? 1.f / L : 0.f;
+      acc.x *= inv;
+      acc.y *= inv;
+      acc.z *= inv;
+      acc.w *= inv;
+      put_item<D>(p, b, kvh, rho, d4, acc, M, L);
+    }
+  }
+  cluster_sync();
 }
 
 // Arrive at the per-unit ticket; the last arriving CTA merges and resets it.
@@ -508,12 +587,29 @@ __device__ void tail_entries(const AttendParams& p, long long u, int t_lo, int t
   }
 }
 
-// Merge entries [0, nent) of the shared scratch into partial `part` of unit u.
+// Where partial `part` of unit u goes: this CTA's shared memory (`local`) when
+// the unit's CTAs form a cluster, else the workspace.
 template <int D>
-__device__ void merge_to_partial(const AttendParams& p, long long u, int part, int nent, int G, const float* wm,
+__device__ __forceinline__ float* partial_dst(const AttendParams& p, long long u, int part, float* local) {
+  return p.cluster ? local : p.partials + (u * (p.S_q + p.S_t) + part) * kPartialFloats(D);
+}
+
+// The unit's partials into the output: through the cluster's shared memory, or
+// through the workspace and the atomic ticket.
+template <int D, bool PREFETCH>
+__device__ __forceinline__ void finish_unit(const AttendParams& p, long long u, int* sh_flag, float* combine_scratch,
+                                            const float* local) {
+  if (p.cluster)
+    cluster_combine<D>(p, u, p.S_q + p.S_t, local);
+  else
+    ticket_and_combine<D, PREFETCH>(p, u, sh_flag, combine_scratch);
+}
+
+// Merge entries [0, nent) of the shared scratch into the partial at dst.
+template <int D>
+__device__ void merge_to_partial(const AttendParams& p, float* dst, int nent, int G, const float* wm,
                                  const float* wl, const float* wc, const float* wo, float* fac) {
   const int tid = threadIdx.x, R = p.R;
-  float* dst = p.partials + (u * (p.S_q + p.S_t) + part) * kPartialFloats(D);
   if (tid < R) {
     float Mx = neg_inf();
     for (int w = 0; w < nent; ++w) Mx = fmaxf(Mx, wm[w * 8 + tid]);
@@ -556,6 +652,35 @@ __device__ __forceinline__ float pow2i(int e) {   // 2^e, -126 <= e <= 127
   return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 
+// A CTA's role: unit u and quantized split r, or tail slice r.  With clusters,
+// CTA r of unit u's cluster is split r (r < S_q) or tail slice r - S_q;
+// otherwise the B*Hkv*S_t tail CTAs come first (so they start in the first
+// wave), then the quantized splits.  The block index is read through a
+// volatile move so that each call derives the role anew.
+struct CtaRole {
+  long long u;
+  int r;
+  bool tail;
+};
+
+__device__ __forceinline__ CtaRole cta_role(const AttendParams& p, long long nunits) {
+  unsigned bx;
+  asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(bx));
+  const unsigned ntail = p.cluster ? 0u : static_cast<unsigned>(nunits * p.S_t);
+  CtaRole c;
+  c.tail = bx < ntail;
+  const unsigned S = p.cluster ? static_cast<unsigned>(p.S_q + p.S_t) : static_cast<unsigned>(c.tail ? p.S_t : p.S_q);
+  const unsigned rel = c.tail ? bx : bx - ntail;
+  const unsigned uu = rel / S;
+  c.u = static_cast<long long>(uu);
+  c.r = static_cast<int>(rel - uu * S);
+  if (p.cluster && c.r >= p.S_q) {
+    c.tail = true;
+    c.r -= p.S_q;
+  }
+  return c;
+}
+
 // Four CTAs per SM when one weight n-tile serves all rows (rows <= 4); two for
 // the eight-row variant, which keeps two n-tiles of weights and two sets of P
 // fragments.
@@ -572,10 +697,13 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
   int* sh_abort = sh_flag + 1;
 
   constexpr int G = D / NJ;
-  const long long ntail = nunits * p.S_t;
-  if (blockIdx.x < ntail) {  // ---------------- tail CTAs (first, so they start in the first wave) ----
-    const long long u = blockIdx.x / p.S_t;
-    const int ts = static_cast<int>(blockIdx.x % p.S_t);
+  // In either case the partial is staged in the q~ area, which is free once
+  // the loop is done and which tail CTAs never use.
+  float* part_local = reinterpret_cast<float*>(smem + L::QT_OFF);
+  const CtaRole role = cta_role(p, nunits);
+  if (role.tail) {  // ---------------- tail CTAs ----
+    const long long u = role.u;
+    const int ts = role.r;
     const int ntl = p.c.r + p.P + p.top_k, per = (ntl + p.S_t - 1) / p.S_t;
     const int t_lo = min(ntl, ts * per), t_hi = min(ntl, t_lo + per);
     float* wm = reinterpret_cast<float*>(smem + L::WM_OFF);
@@ -584,15 +712,15 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
     float* wo = reinterpret_cast<float*>(smem + L::WO_OFF);
     tail_entries<D>(p, u, t_lo, t_hi, wm, wl, wc, wo, 0);
     __syncthreads();
-    merge_to_partial<D>(p, u, p.S_q + ts, NW, G, wm, wl, wc, wo, reinterpret_cast<float*>(smem + L::FAC_OFF));
+    merge_to_partial<D>(p, partial_dst<D>(p, u, p.S_q + ts, part_local), NW, G, wm, wl, wc, wo,
+                        reinterpret_cast<float*>(smem + L::FAC_OFF));
     __syncthreads();
-    ticket_and_combine<D, NT == 2>(p, u, sh_flag, reinterpret_cast<float*>(smem));
+    finish_unit<D, NT == 2>(p, u, sh_flag, reinterpret_cast<float*>(smem), part_local);
     return;
   }
 
-  const long long qi = blockIdx.x - ntail;
-  const long long u = qi / p.S_q;
-  const int split = static_cast<int>(qi % p.S_q);
+  const long long u = role.u;
+  const int split = role.r;
   const int b = static_cast<int>(u / p.c.Hkv), kvh = static_cast<int>(u % p.c.Hkv);
   const long long t_begin = static_cast<long long>(split) * p.chunk;
   const long long t_end = min(p.c.Lq, t_begin + p.chunk);
@@ -1138,22 +1266,28 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
 
   // ---- this CTA's share of the bf16 tail (residual, pending, selected tokens) ----
   // Without tail CTAs the quantized splits share the tail list: entries
-  // NW .. 2 NW - 1.
-  const float* wm = reinterpret_cast<const float*>(smem + L::WM_OFF);
-  if (p.S_t == 0) {
-    const int ntl = p.c.r + p.P + p.top_k, per = (ntl + p.S_q - 1) / p.S_q;
-    const int t_lo = min(ntl, split * per), t_hi = min(ntl, t_lo + per);
-    tail_entries<D>(p, u, t_lo, t_hi, reinterpret_cast<float*>(smem + L::WM_OFF),
-                    reinterpret_cast<float*>(smem + L::WL_OFF), reinterpret_cast<float*>(smem + L::WC_OFF),
-                    reinterpret_cast<float*>(smem + L::WO_OFF), NW);
+  // NW .. 2 NW - 1.  (The role is derived again rather than kept in registers
+  // through the loop.)
+  {
+    const CtaRole role2 = cta_role(p, nunits);
+    const long long u = role2.u;
+    const int split = role2.r;
+    const float* wm = reinterpret_cast<const float*>(smem + L::WM_OFF);
+    if (p.S_t == 0) {
+      const int ntl = p.c.r + p.P + p.top_k, per = (ntl + p.S_q - 1) / p.S_q;
+      const int t_lo = min(ntl, split * per), t_hi = min(ntl, t_lo + per);
+      tail_entries<D>(p, u, t_lo, t_hi, reinterpret_cast<float*>(smem + L::WM_OFF),
+                      reinterpret_cast<float*>(smem + L::WL_OFF), reinterpret_cast<float*>(smem + L::WC_OFF),
+                      reinterpret_cast<float*>(smem + L::WO_OFF), NW);
+      __syncthreads();
+    }
+    // ---- CTA merge of the entries -> partial ----
+    merge_to_partial<D>(p, partial_dst<D>(p, u, split, part_local), (p.S_t == 0) ? 2 * NW : NW, G, wm,
+                        reinterpret_cast<const float*>(smem + L::WL_OFF), reinterpret_cast<const float*>(smem + L::WC_OFF),
+                        reinterpret_cast<const float*>(smem + L::WO_OFF), reinterpret_cast<float*>(smem + L::FAC_OFF));
     __syncthreads();
+    finish_unit<D, NT == 2>(p, u, sh_flag, reinterpret_cast<float*>(smem), part_local);
   }
-  // ---- CTA merge of the entries -> partial ----
-  merge_to_partial<D>(p, u, split, (p.S_t == 0) ? 2 * NW : NW, G, wm,
-                      reinterpret_cast<const float*>(smem + L::WL_OFF), reinterpret_cast<const float*>(smem + L::WC_OFF),
-                      reinterpret_cast<const float*>(smem + L::WO_OFF), reinterpret_cast<float*>(smem + L::FAC_OFF));
-  __syncthreads();
-  ticket_and_combine<D, NT == 2>(p, u, sh_flag, reinterpret_cast<float*>(smem));
 }
 
 template <int MODE, int D, int NJ, int NT>
@@ -1162,15 +1296,88 @@ constexpr int smem_bytes() {
   return L::TOTAL;
 }
 
+// Lets the variant launch clusters of more than 8 CTAs (up to 16); once per device.
+template <int MODE, int D, int NJ, int NT>
+cudaError_t allow_wide_clusters() {
+  constexpr int kMaxDev = 64;
+  static bool done[kMaxDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDev && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&attend_kernel<MODE, D, NJ, NT>),
+                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDev) done[dev] = true;
+  return e;
+}
+
+// Launch configuration with one cluster of `size` CTAs per (b, kvh).
+inline void cluster_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute& at, long long grid, int smem, int size,
+                           cudaStream_t s) {
+  cfg = cudaLaunchConfig_t{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  at = cudaLaunchAttribute{};
+  at.id = cudaLaunchAttributeClusterDimension;
+  at.val.clusterDim.x = static_cast<unsigned>(size);
+  at.val.clusterDim.y = 1;
+  at.val.clusterDim.z = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+}
+
 template <int MODE, int D, int NJ, int NT>
 cudaError_t launch_t(const AttendParams& p, cudaStream_t s) {
   constexpr int smem = smem_bytes<MODE, D, NJ, NT>();
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&attend_kernel<MODE, D, NJ, NT>), smem);
   if (e != cudaSuccess) return e;
   const long long nunits = static_cast<long long>(p.c.B) * p.c.Hkv;
-  const long long grid = nunits * (p.S_q + p.S_t);
-  attend_kernel<MODE, D, NJ, NT><<<static_cast<unsigned>(grid), NTHREADS, smem, s>>>(p);
-  return cudaGetLastError();
+  const int S_all = p.S_q + p.S_t;
+  const long long grid = nunits * S_all;
+  if (!p.cluster) {
+    attend_kernel<MODE, D, NJ, NT><<<static_cast<unsigned>(grid), NTHREADS, smem, s>>>(p);
+    return cudaGetLastError();
+  }
+  if (S_all < 1 || S_all > kMaxClusterCtas) return cudaErrorInvalidValue;
+  if (S_all > 8 && (e = allow_wide_clusters<MODE, D, NJ, NT>()) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute at;
+  cluster_config(cfg, at, grid, smem, S_all, s);
+  return cudaLaunchKernelEx(&cfg, attend_kernel<MODE, D, NJ, NT>, p);
+}
+
+// Clusters of `size` CTAs of one kernel variant that fit on the device at
+// once, queried once per device and size (0: unknown or not launchable).
+template <int MODE, int D, int NJ, int NT>
+int resident_clusters_t(int size) {
+  if (size < 1 || size > kMaxClusterCtas) return 0;
+  constexpr int kMaxDev = 64;
+  static int cached[kMaxDev][kMaxClusterCtas + 1] = {};   // 0: not queried, -1: none
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  int& c = cached[dev][size];
+  if (c != 0) return c > 0 ? c : 0;
+  constexpr int smem = smem_bytes<MODE, D, NJ, NT>();
+  const void* fn = reinterpret_cast<const void*>(&attend_kernel<MODE, D, NJ, NT>);
+  if (set_smem_once(fn, smem) != cudaSuccess) return 0;
+  if (size > 8 && allow_wide_clusters<MODE, D, NJ, NT>() != cudaSuccess) {
+    cudaGetLastError();
+    c = -1;
+    return 0;
+  }
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute at;
+  cluster_config(cfg, at, size, smem, size, nullptr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    c = -1;
+    return 0;
+  }
+  c = n;
+  return n;
 }
 
 // Resident CTAs per SM of one kernel variant times the SM count, queried once
@@ -1207,6 +1414,17 @@ struct Variant {
     }
     return 0;
   }
+  static int clusters(int D, int NJ, int size) {
+    if (D == 128) {
+      if (NJ == 1) return resident_clusters_t<MODE, 128, 1, NT>(size);
+      if (NJ == 2) return resident_clusters_t<MODE, 128, 2, NT>(size);
+      if (NJ == 4) return resident_clusters_t<MODE, 128, 4, NT>(size);
+    } else if (D == 64) {
+      if (NJ == 1) return resident_clusters_t<MODE, 64, 1, NT>(size);
+      if (NJ == 2) return resident_clusters_t<MODE, 64, 2, NT>(size);
+    }
+    return 0;
+  }
   static cudaError_t launch(const AttendParams& p, cudaStream_t s) {
     const int D = p.c.D, NJ = p.c.D / p.c.G;
     if (D == 128) {
@@ -1227,6 +1445,11 @@ int resident_mode(int D, int NJ, int R) {
 }
 
 template <int MODE>
+int clusters_mode(int D, int NJ, int R, int size) {
+  return R <= 4 ? Variant<MODE, 1>::clusters(D, NJ, size) : Variant<MODE, 2>::clusters(D, NJ, size);
+}
+
+template <int MODE>
 cudaError_t launch_mode(const AttendParams& p, cudaStream_t s) {
   return p.R <= 4 ? Variant<MODE, 1>::launch(p, s) : Variant<MODE, 2>::launch(p, s);
 }
@@ -1240,6 +1463,17 @@ int attend_resident_ctas(int mode, int D, int G, int R) {
     case KVQ_MODE_INT4: return resident_mode<KVQ_MODE_INT4>(D, NJ, R);
     case KVQ_MODE_INT2: return resident_mode<KVQ_MODE_INT2>(D, NJ, R);
     case KVQ_MODE_INT1: return resident_mode<KVQ_MODE_INT1>(D, NJ, R);
+    default: return 0;
+  }
+}
+
+int attend_resident_clusters(int mode, int D, int G, int R, int size) {
+  const int NJ = D / G;
+  switch (mode) {
+    case KVQ_MODE_INT8: return clusters_mode<KVQ_MODE_INT8>(D, NJ, R, size);
+    case KVQ_MODE_INT4: return clusters_mode<KVQ_MODE_INT4>(D, NJ, R, size);
+    case KVQ_MODE_INT2: return clusters_mode<KVQ_MODE_INT2>(D, NJ, R, size);
+    case KVQ_MODE_INT1: return clusters_mode<KVQ_MODE_INT1>(D, NJ, R, size);
     default: return 0;
   }
 }

@@ -87,6 +87,43 @@ __device__ __forceinline__ void record_status(int* status, int code) {
 }
 
 // ------------------------------------------------------------------------------
+// Thread-block clusters: the hardware cluster barrier (every thread of every
+// CTA of the cluster arrives; release / acquire order shared and global memory
+// at cluster scope) and loads from another CTA's shared memory.
+// ------------------------------------------------------------------------------
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of this CTA's shared location `p` in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_dsmem(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_dsmem4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
+
+// ------------------------------------------------------------------------------
 // Tensor-core MMA: D[16x8] += A[16x16] (row) * B[16x8] (col), f16 in, f32 acc.
 //   a[0] = (row g,   k 2q..2q+1)   a[1] = (row g+8, k 2q..2q+1)
 //   a[2] = (row g,   k 2q+8..+9)   a[3] = (row g+8, k 2q+8..+9)

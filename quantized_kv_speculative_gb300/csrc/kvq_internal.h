@@ -23,6 +23,7 @@ constexpr int kMaxTailSplits = 8;      // CTAs per (b, kvh) for the bf16 tail
 constexpr int kMaxCombine = 256;       // partials per (b, kvh) merged by the combine
 constexpr int kMaxQuantSplits = kMaxCombine - kMaxTailSplits;
 constexpr int kTailTokensPerSplit = 320;  // bf16 tail tokens per tail CTA (usually one per (b, kvh))
+constexpr int kMaxClusterCtas = 16;   // CTAs per (b, kvh) that may combine as one thread-block cluster
 constexpr int kStatusBytes = 256;      // workspace header (status word)
 constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s at 2 GHz
 __host__ __device__ constexpr int kPartialFloats(int D) { return 2 * kMaxRows + kMaxRows * D; }
@@ -62,6 +63,7 @@ struct AttendParams {
   int S_t;                  // tail splits per (b, kvh): residual + pending + selected tokens
   long long chunk;          // tokens per split (multiple of kChunkAlign)
   long long wait_limit;
+  int cluster;              // 1: the S_q + S_t CTAs of a unit form one cluster and combine in shared memory
 };
 
 struct TopkParams {
@@ -140,6 +142,9 @@ cudaError_t launch_attend(const AttendParams& p, int mode, cudaStream_t s);
 // CTAs of the attention kernel variant that fit on the current device at once
 // (0 if unknown).
 int attend_resident_ctas(int mode, int D, int G, int R);
+// Clusters of `size` CTAs of that variant that fit on the current device at
+// once (0 if unknown or if the size cannot be launched).
+int attend_resident_clusters(int mode, int D, int G, int R, int size);
 cudaError_t launch_topk(const TopkParams& p, int mode, cudaStream_t s);
 // Top-k split plan for the current device: returns the split count S per
 // (b, kv head) and sets *chunk (tokens per split).

@@ -53,9 +53,10 @@ def test_struct_layout_matches_c(tmp_path):
 #include <stddef.h>
 #include "kvq.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(kvq_cache_desc), sizeof(kvq_cache),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(kvq_cache_desc), sizeof(kvq_cache),
          offsetof(kvq_cache, base), offsetof(kvq_cache, off_k_plane), offsetof(kvq_cache, quantized_len),
-         offsetof(kvq_cache, residual_start), offsetof(kvq_cache, magic));
+         offsetof(kvq_cache, residual_start), offsetof(kvq_cache, magic), sizeof(kvq_attend_plan_info),
+         offsetof(kvq_attend_plan_info, chunk_tokens), offsetof(kvq_attend_plan_info, cluster));
   return 0;
 }
 ''')
@@ -63,8 +64,10 @@ int main(void) {
     subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
     C = kvq.KvqCache
+    P = kvq.KvqAttendPlanInfo
     assert vals == [ctypes.sizeof(kvq.KvqCacheDesc), ctypes.sizeof(C), C.base.offset, C.off_k_plane.offset,
-                    C.quantized_len.offset, C.residual_start.offset, C.magic.offset]
+                    C.quantized_len.offset, C.residual_start.offset, C.magic.offset, ctypes.sizeof(P),
+                    P.chunk_tokens.offset, P.cluster.offset]
 
 
 def _desc(**kw):

@@ -130,6 +130,45 @@ def test_attend_matches_oracle(case):
     assert_attention_close(out, lse, ref_out, ref_lse, what=str(case))
 
 
+# Enough (b, kvh) units that the plan stays within 16 CTAs per unit, and few
+# enough that the clusters fit the device at once (on a 152-SM GB300 with two
+# CTAs per SM, 28 clusters of 10 CTAs), so the launch takes the cluster combine.
+CLUSTER_CASES = [
+    ("int8", 1, 16, 16, 128, 128, 1300, 8, 8, 0, True),     # verify, eight rows, 16 KV heads
+    ("int4", 1, 32, 32, 128, 128, 1500, 1, 1, 0, False),    # draft, one row
+    ("int2", 4, 8, 32, 128, 32, 2100, 2, 2, 16, False),     # SpeCache shape, selected tokens
+    ("int1", 4, 8, 16, 64, 32, 1000, 2, 2, 0, False),
+    ("int8", 2, 2, 8, 128, 128, 1150, 2, 3, 0, False),      # few units, ragged residual
+]
+
+
+@pytest.mark.parametrize("case", CLUSTER_CASES, ids=lambda c: f"{c[0]}-N{c[6]}-g{c[7]}-k{c[9]}")
+def test_attend_cluster_and_ticket_combines(case, monkeypatch):
+    """The same call through both combines: one thread-block cluster per
+    (b, kvh) merging in shared memory, and (KVQ_ATTEND_CLUSTERS=0) partials in
+    the workspace merged by the last CTA.  The plan reports which one ran; both
+    match the oracle."""
+    mode, B, Hkv, Hq, D, G, N, gamma, P, top_k, needles = case
+    gc, oc, q, pk, pv, sel, sk, sv = _attn_case(*case)
+    ref_out, ref_lse = oracle.attend(oc, mode, q, pk, pv, sel, sk, sv)
+    args = (dev(q), None if pk is None else dev(pk), None if pv is None else dev(pv),
+            None if sel is None else torch.from_numpy(sel).cuda(), None if sk is None else dev(sk),
+            None if sv is None else dev(sv))
+    monkeypatch.delenv("KVQ_ATTEND_CLUSTERS", raising=False)
+    plan = kvq.kvq_attend_plan(gc, mode, Hq, gamma, P, top_k)
+    assert plan["cluster"] and plan["quant_splits"] + plan["tail_splits"] <= 16, plan
+    out_c, lse_c = kvq.kvq_attend(gc, mode, *args)
+    monkeypatch.setenv("KVQ_ATTEND_CLUSTERS", "0")
+    plan0 = kvq.kvq_attend_plan(gc, mode, Hq, gamma, P, top_k)
+    assert not plan0["cluster"]
+    assert (plan0["quant_splits"], plan0["tail_splits"], plan0["chunk_tokens"]) == \
+        (plan["quant_splits"], plan["tail_splits"], plan["chunk_tokens"])
+    out_t, lse_t = kvq.kvq_attend(gc, mode, *args)
+    torch.cuda.synchronize()
+    assert_attention_close(out_c, lse_c, ref_out, ref_lse, what=f"cluster {case}")
+    assert_attention_close(out_t, lse_t, ref_out, ref_lse, what=f"ticket {case}")
+
+
 def test_attend_deterministic_and_split_independent():
     """Two calls give identical bytes.  The result does not depend on the
     workspace's history, because the ticket counters reset themselves."""
