@@ -620,7 +620,8 @@ def run_multilayer_spec(layers, lq, r0, gamma, drafts, append, reps=3, seed=0):
 def run_specache(fmt, seed=0, reps=20):
     """SpeCache-style batched decode: batch 36, 32 q / 8 kv heads, D 128, G 32,
     32768 quantized + 32 residual tokens; top-64 from the speculative token,
-    then attention (gamma = 2) with those 64 tokens at 16 bits."""
+    the fetch of those 64 tokens' 16-bit K/V from the full cache in pinned host
+    memory, then attention (gamma = 2) with them at 16 bits."""
     import quantized_kv_speculative_gb300 as kvq
     from quantized_kv_speculative_gb300 import _build
     _build.build()
@@ -637,9 +638,15 @@ def run_specache(fmt, seed=0, reps=20):
     pv = torch.randn((B, H, 2, D), generator=gen, device=dev).to(torch.bfloat16)
     qs = q[:, 1].contiguous()
     idx, sc = kvq.kvq_topk(c, fmt, qs, k, workspace=ws)
+    # the full 16-bit cache, offloaded to pinned host memory
+    hk = torch.empty(K.shape, dtype=torch.bfloat16, pin_memory=True)
+    hv = torch.empty(V.shape, dtype=torch.bfloat16, pin_memory=True)
+    hk.copy_(K)
+    hv.copy_(V)
+    sk, sv = kvq.kvq_gather_selected(hk, hv, idx)
     gi = idx.long().clamp_min(0)[..., None].expand(-1, -1, -1, D)
-    sk, sv = torch.gather(K, 2, gi).contiguous(), torch.gather(V, 2, gi).contiguous()
-    del K, V
+    assert torch.equal(sk, torch.gather(K, 2, gi)) and torch.equal(sv, torch.gather(V, 2, gi))
+    del K, V, gi
     out = torch.empty_like(q)
     lse = torch.empty((B, 2, Hq), device=dev)
     s = torch.cuda.Stream()
@@ -647,8 +654,31 @@ def run_specache(fmt, seed=0, reps=20):
     torch.cuda.synchronize()
     ga = _graph(lambda st: kvq.kvq_attend(c, fmt, q, pk, pv, idx, sk, sv, out=out, lse=lse, workspace=ws, stream=st), s)
     gt = _graph(lambda st: kvq.kvq_topk(c, fmt, qs, k, idx_out=idx, score_out=sc, workspace=ws, stream=st), s)
+    # the fetch over 16 independent index sets (150 MB of rows > L2), per fetch
+    nset = 16
+    sets = [torch.randint(0, lq, (B, H, k), generator=gen, device=dev, dtype=torch.int32) for _ in range(nset)]
+    sk2, sv2 = torch.empty_like(sk), torch.empty_like(sv)
     ta, tt = _time_graph(ga, reps), _time_graph(gt, reps)
+    try:
+        gg = _graph(lambda st: [kvq.kvq_gather_selected(hk, hv, ix, sel_k=sk2, sel_v=sv2, stream=st) for ix in sets], s)
+        tg, fetch_err = _time_graph(gg, reps) / nset, None
+    except Exception as ex:   # reported in the line instead of ending the run
+        torch.cuda.synchronize()
+        tg, fetch_err = float("nan"), f"{type(ex).__name__}: {ex}"[:200]
     assert kvq.kvq_workspace_status(ws) == 0
+    # the link's measured rate for a plain copy: 1 GiB pinned host -> device
+    hb = hk.view(-1)[: 1 << 29]
+    db = torch.empty_like(hb, device=dev)
+    db.copy_(hb, non_blocking=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(3):
+        db.copy_(hb, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    h2d_gbs = 3 * hb.numel() * 2 / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del db, hk, hv
     peak, src = _peak()
     mode = fmt
     ba = B * H * (lq * _bytes_per_token(mode, D, G) + r0 * 2 * D * 2)
@@ -657,7 +687,9 @@ def run_specache(fmt, seed=0, reps=20):
     return {"attend_ms": ta, "attend_gbs": ba / (ta * 1e-3) / 1e9, "attend_frac": ba / (ta * 1e-3) / 1e9 / peak,
             "attend_bytes": ba, "sel_kv_bytes": B * H * k * 2 * D * 2,
             "topk_ms": tt, "topk_gbs": bt / (tt * 1e-3) / 1e9, "topk_frac": bt / (tt * 1e-3) / 1e9 / peak,
-            "step_ms": ta + tt, "kv_tok_per_s": B * (lq + r0 + 2) / ((ta + tt) * 1e-3),
+            "fetch_ms": tg, "fetch_error": fetch_err, "fetch_gbs": B * H * k * 2 * D * 2 / (tg * 1e-3) / 1e9,
+            "fetch_frac_of_h2d_copy": B * H * k * 2 * D * 2 / (tg * 1e-3) / 1e9 / h2d_gbs, "h2d_copy_gbs": h2d_gbs,
+            "step_ms": ta + tt + tg, "kv_tok_per_s": B * (lq + r0 + 2) / ((ta + tt + tg) * 1e-3),
             "peak_gbs": peak, "peak_source": src}
 
 
@@ -756,6 +788,15 @@ def run_profile_case(name, launches):
                 kvq.kvq_topk(c, "int2", q[:, 1].contiguous(), k, idx_out=idx, workspace=ws)
             else:
                 kvq.kvq_attend(c, "int2", q, pk, pv, idx, sk, sv, workspace=ws)
+    elif name == "fetch-specache-host":
+        # the SpeCache batch's fetch: 36 x 8 heads x 64 selected rows out of a
+        # pinned host store of 4096 tokens per head (600 MB per K and V)
+        B, H, D, N, k = 36, 8, 128, 4096, 64
+        hk = torch.zeros((B, H, N, D), dtype=torch.bfloat16, pin_memory=True)
+        hv = torch.zeros((B, H, N, D), dtype=torch.bfloat16, pin_memory=True)
+        sets = [torch.randint(0, N, (B, H, k), generator=gen, device=dev, dtype=torch.int32) for _ in range(4)]
+        for i in range(launches):
+            kvq.kvq_gather_selected(hk, hv, sets[i % 4])
     else:
         raise SystemExit(f"unknown profile case {name}")
     torch.cuda.synchronize()

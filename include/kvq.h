@@ -291,6 +291,30 @@ kvq_status kvq_attend_static_scratch(const kvq_cache* cache, kvq_mode mode, cons
                                      const void* sel_k, const void* sel_v, int32_t top_k,
                                      float sm_scale, void* out, float* lse, kvq_stream_t stream);
 
+/*
+ * Fetch of the selected tokens' 16-bit K/V from the full-precision store, for
+ * kvq_attend's sel_k / sel_v (SpeCache page, "Approach": the full 16-bit
+ * cache lives in CPU memory and the top-k pairs the speculative token
+ * predicts are fetched for the next step; MSpecKV page, abstract: offloaded
+ * KV is reconstructed only in the needed subsets).  The kernel reads pinned
+ * host memory directly (over NVLink-C2C on a Grace-Blackwell node).
+ *  full_k, full_v  bf16 [B][Hkv][full_tokens][D]: pinned host memory
+ *                  (cudaHostAlloc / cudaHostRegister, e.g. a torch pinned
+ *                  tensor) or device memory; 16-byte aligned.  The caller
+ *                  guarantees that extent.  Pageable host memory returns
+ *                  KVQ_ERR_INVALID_ARG before any launch.
+ *  sel_idx         int32 [B][Hkv][top_k], device memory (e.g. kvq_topk's
+ *                  idx_out).  Entry j of (b, kvh) copies row sel_idx[b][kvh][j]
+ *                  of that head; an index outside [0, full_tokens) (the -1
+ *                  padding) gives a zero row.
+ *  sel_k, sel_v    bf16 [B][Hkv][top_k][D], device memory, 16-byte aligned.
+ *  D in {64, 128}; 1 <= top_k <= 1024.  Bit-exact copy.  Enqueues one kernel
+ *  on `stream` and returns without waiting.
+ */
+kvq_status kvq_gather_selected(const void* full_k, const void* full_v, int64_t full_tokens, int32_t batch,
+                               int32_t num_kv_heads, int32_t head_dim, const int32_t* sel_idx, int32_t top_k,
+                               void* sel_k, void* sel_v, kvq_stream_t stream);
+
 /* Synchronously read (and then clear) the device status word of a workspace:
  * KVQ_OK, or KVQ_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait since the
  * last read.  Synchronizes `stream`. */

@@ -12,6 +12,7 @@ from .kvq_oracle import (  # noqa: F401
     OracleCache,
     all_scores,
     attend,
+    gather_selected,
     mode_codes_scale,
     pack_k_plane,
     pack_v_plane,

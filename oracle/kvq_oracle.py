@@ -479,3 +479,33 @@ def all_scores(cache: OracleCache, mode: str, q_spec: np.ndarray, b: int, h: int
             s = (s * F32(16)).astype(F32)
         out[g * G:(g + 1) * G] = score_group(qs, s, cache.k_zero[b, h, g], codes)
     return out
+
+
+# ================================================================================
+# Fetch of the selected 16-bit KV
+# ================================================================================
+
+
+def gather_selected(full_k: np.ndarray, full_v: np.ndarray, sel_idx: np.ndarray):
+    """The selected tokens' 16-bit K/V out of the full-precision store.
+
+    SpeCache keeps the whole 16-bit cache in CPU memory and, each step, fetches
+    the top-k pairs the speculative token predicted (SpeCache page, Approach).
+    ``full_k, full_v [B, Hkv, N, D]`` (any dtype), ``sel_idx [B, Hkv, k]``.
+    Entry j of (b, h) is row ``sel_idx[b, h, j]`` of that head.  Reading: an
+    index outside [0, N), such as the -1 that pads a short top-k list, gives a
+    row of zeros (the attention ignores those entries).
+    Returns ``sel_k, sel_v [B, Hkv, k, D]``.
+    """
+    B, H, N, D = full_k.shape
+    k = sel_idx.shape[2]
+    sel_k = np.zeros((B, H, k, D), full_k.dtype)
+    sel_v = np.zeros((B, H, k, D), full_v.dtype)
+    for b in range(B):
+        for h in range(H):
+            for j in range(k):
+                t = int(sel_idx[b, h, j])
+                if 0 <= t < N:
+                    sel_k[b, h, j] = full_k[b, h, t]
+                    sel_v[b, h, j] = full_v[b, h, t]
+    return sel_k, sel_v

@@ -34,7 +34,7 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "K
 EXPORTED = (
     "kvq_status_string", "kvq_cache_bytes", "kvq_cache_init", "kvq_quantize_append",
     "kvq_workspace_bytes", "kvq_attend", "kvq_topk", "kvq_workspace_status",
-    "kvq_selftest_bounded_wait", "kvq_attend_static_scratch", "kvq_attend_plan",
+    "kvq_selftest_bounded_wait", "kvq_attend_static_scratch", "kvq_attend_plan", "kvq_gather_selected",
 )
 
 
@@ -98,6 +98,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kvq_attend_static_scratch.restype = ctypes.c_int
     lib.kvq_attend_plan.argtypes = [cache_p, ctypes.c_int, i32, i32, i32, i32, ctypes.POINTER(KvqAttendPlanInfo)]
     lib.kvq_attend_plan.restype = ctypes.c_int
+    lib.kvq_gather_selected.argtypes = [vp, vp, i64, i32, i32, i32, vp, i32, vp, vp, vp]
+    lib.kvq_gather_selected.restype = ctypes.c_int
     lib.kvq_topk.argtypes = [cache_p, ctypes.c_int, vp, i32, i32, vp, vp, vp, sz, vp]
     lib.kvq_topk.restype = ctypes.c_int
     lib.kvq_workspace_status.argtypes = [vp, sz, vp]
@@ -270,6 +272,32 @@ def kvq_attend_plan(cache: QuantizedKVCache, mode: str, num_q_heads: int, gamma:
                                ctypes.byref(info)), "kvq_attend_plan")
     return {"quant_splits": info.quant_splits, "tail_splits": info.tail_splits,
             "chunk_tokens": info.chunk_tokens, "cluster": bool(info.cluster)}
+
+
+def kvq_gather_selected(full_k: torch.Tensor, full_v: torch.Tensor, sel_idx: torch.Tensor, sel_k=None, sel_v=None,
+                        stream=None):
+    """The selected tokens' 16-bit K/V, ``sel_idx [B, Hkv, k]`` int32 on the
+    device, from the full store ``full_k, full_v [B, Hkv, N, D]`` bf16 in
+    pinned host memory (or on the device).  Returns ``(sel_k, sel_v)``
+    ``[B, Hkv, k, D]`` bf16 on the device; entries outside [0, N) are zero."""
+    B, Hkv, N, D = full_k.shape
+    if full_v.shape != full_k.shape or full_k.dtype != torch.bfloat16 or full_v.dtype != torch.bfloat16:
+        raise ValueError("full_k and full_v must be bf16 tensors of one shape")
+    if not (full_k.is_contiguous() and full_v.is_contiguous()):
+        raise ValueError("full_k and full_v must be contiguous")
+    if full_k.device.type == "cpu" and not (full_k.is_pinned() and full_v.is_pinned()):
+        raise ValueError("a host store must be in pinned memory")
+    k = sel_idx.shape[2]
+    if sel_k is None:
+        sel_k = torch.empty((B, Hkv, k, D), dtype=torch.bfloat16, device=sel_idx.device)
+    if sel_v is None:
+        sel_v = torch.empty_like(sel_k)
+    lib = load_library()
+    _check(lib.kvq_gather_selected(full_k.data_ptr(), full_v.data_ptr(), N, B, Hkv, D,
+                                   _ptr(sel_idx, torch.int32, "sel_idx"), k, _ptr(sel_k, torch.bfloat16, "sel_k"),
+                                   _ptr(sel_v, torch.bfloat16, "sel_v"), _stream(stream)),
+           "kvq_gather_selected")
+    return sel_k, sel_v
 
 
 def kvq_attend_static_scratch(cache: QuantizedKVCache, mode: str, q: torch.Tensor, pend_k=None, pend_v=None,

@@ -294,9 +294,52 @@ def test_topk_then_attend_specache_step():
     idx, _ = kvq.kvq_topk(gc, "int2", dev(q[:, 1]), k)
     ref_idx, _ = oracle.topk(oc, "int2", q[:, 1], k)
     np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
-    sk = np.take_along_axis(K, ref_idx[..., None].astype(np.int64), axis=2)
-    sv = np.take_along_axis(V, ref_idx[..., None].astype(np.int64), axis=2)
+    # the 16-bit rows come from the full store in pinned host memory
+    sk, sv = oracle.gather_selected(K, V, ref_idx)
+    hk, hv = (torch.from_numpy(x).to(torch.bfloat16).pin_memory() for x in (K, V))
+    gk, gv = kvq.kvq_gather_selected(hk, hv, idx)
+    torch.cuda.synchronize()
+    assert torch.equal(gk.cpu(), torch.from_numpy(sk).to(torch.bfloat16))
+    assert torch.equal(gv.cpu(), torch.from_numpy(sv).to(torch.bfloat16))
     pk, pv = ki.pending(12, B, Hkv, 2, D)
     ref = oracle.attend(oc, "int2", q, pk, pv, ref_idx, sk, sv)
-    out, lse = kvq.kvq_attend(gc, "int2", dev(q), dev(pk), dev(pv), idx, dev(sk), dev(sv))
+    out, lse = kvq.kvq_attend(gc, "int2", dev(q), dev(pk), dev(pv), idx, gk, gv)
     assert_attention_close(out, lse, *ref, what="specache step")
+
+
+@pytest.mark.parametrize("B,Hkv,N,D,k,where", [(3, 2, 2100, 128, 16, "host"), (2, 4, 700, 64, 33, "host"),
+                                              (36, 8, 2048, 128, 64, "host"), (2, 2, 1500, 128, 7, "device")])
+def test_gather_selected_bit_exact(B, Hkv, N, D, k, where):
+    """The fetch of the selected 16-bit rows is a bit-exact copy, from pinned
+    host memory or from device memory, with -1 padding and an index past the
+    end giving zero rows; sizes cover several warps, a ragged last sweep and
+    the SpeCache batch (36 x 8 heads x 64)."""
+    g = ki.rng(51, B * 1000 + k)
+    K = ki.normal_bf16(g, (B, Hkv, N, D))
+    V = ki.normal_bf16(g, (B, Hkv, N, D))
+    sel = np.stack([np.stack([g.choice(N, k, replace=False) for _ in range(Hkv)]) for _ in range(B)]).astype(np.int32)
+    sel[0, 0, -1] = -1
+    sel[-1, -1, 0] = N
+    ref_k, ref_v = oracle.gather_selected(K, V, sel)
+    tk, tv = (torch.from_numpy(x).to(torch.bfloat16) for x in (K, V))
+    if where == "host":
+        tk, tv = tk.pin_memory(), tv.pin_memory()
+    else:
+        tk, tv = tk.cuda(), tv.cuda()
+    sk, sv = kvq.kvq_gather_selected(tk, tv, torch.from_numpy(sel).cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(sk.cpu(), torch.from_numpy(ref_k).to(torch.bfloat16))
+    assert torch.equal(sv.cpu(), torch.from_numpy(ref_v).to(torch.bfloat16))
+
+
+def test_gather_selected_rejects_pageable_memory():
+    """A store in pageable host memory is refused before any launch."""
+    lib = kvq.load_library()
+    K = torch.zeros((1, 1, 64, 128), dtype=torch.bfloat16)          # pageable
+    sel = torch.zeros((1, 1, 4), dtype=torch.int32, device="cuda")
+    out = torch.empty((1, 1, 4, 128), dtype=torch.bfloat16, device="cuda")
+    st = lib.kvq_gather_selected(K.data_ptr(), K.data_ptr(), 64, 1, 1, 128, sel.data_ptr(), 4, out.data_ptr(),
+                                 out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert kvq.STATUS[st] == "KVQ_ERR_INVALID_ARG"
+    with pytest.raises(ValueError):
+        kvq.kvq_gather_selected(K, K, sel)

@@ -27,6 +27,9 @@ MUTATIONS = [
      "out |= (c[..., per - 1 - e] << (pb * e)).astype(np.uint8)"),
     ("values quantized per channel instead of per token",
      "c, s, z = quantize_minmax(x, bits, axis=-1)", "c, s, z = quantize_minmax(x, bits, axis=-2)"),
+    ("fetch lets the -1 padding wrap to the last row", "                if 0 <= t < N:\n                    sel_k",
+     "                if t < N:\n                    sel_k"),
+    ("fetch takes the value row from the key store", "sel_v[b, h, j] = full_v[b, h, t]", "sel_v[b, h, j] = full_k[b, h, t]"),
 ]
 
 

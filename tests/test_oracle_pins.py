@@ -429,3 +429,56 @@ def test_topk_agrees_with_exact_logit_topk_up_to_near_ties():
     diff = set(order[:k].tolist()) ^ set(idx[0, 0].tolist())
     for t in diff:
         assert abs(ex[t] - kth) <= 1e-4 * (1 + abs(kth))
+
+
+# ------------------------------------------------------------------------------------
+# Fetch of the selected 16-bit KV
+# ------------------------------------------------------------------------------------
+
+
+def test_gather_selected_rows_decode_to_their_source():
+    """Every store value encodes its own (b, h, t, d) and (+0.5 for V), so each
+    fetched row is decoded back to its source instead of being compared with
+    another indexing expression.  Padding (-1) and an index past the end give
+    zero rows.  Catches a wrong head or batch stride, K/V swapped, or padding
+    that wraps around to the last row."""
+    B, H, N, D, k = 2, 3, 11, 4, 5
+    b_, h_, t_, d_ = np.meshgrid(np.arange(B), np.arange(H), np.arange(N), np.arange(D), indexing="ij")
+    full_k = (1000.0 * b_ + 100.0 * h_ + t_ + d_ / 8).astype(np.float64)
+    full_v = full_k + 0.5
+    g = ki.rng(41)
+    sel = np.stack([np.stack([g.choice(N, k, replace=False) for _ in range(H)]) for _ in range(B)]).astype(np.int32)
+    sel[0, 1, 3] = -1
+    sel[1, 2, 0] = N
+    sk, sv = oracle.gather_selected(full_k, full_v, sel)
+    for b in range(B):
+        for h in range(H):
+            for j in range(k):
+                t = int(sel[b, h, j])
+                if not 0 <= t < N:
+                    assert not sk[b, h, j].any() and not sv[b, h, j].any()
+                    continue
+                row = sk[b, h, j]
+                assert int(row[0]) // 1000 == b and (int(row[0]) // 100) % 10 == h and int(row[0]) % 100 == t
+                np.testing.assert_array_equal(row - row[0], np.arange(D) / 8)
+                np.testing.assert_array_equal(sv[b, h, j], row + 0.5)
+
+
+def test_gather_every_token_makes_attention_exact():
+    """Selecting every quantized token and fetching its 16-bit rows from the
+    original K/V turns the low-bit cache back into the original: attention then
+    equals dense fp64 SDPA over the original bf16 K/V (SpeCache page, Approach:
+    the selected pairs attend with their 16-bit values).  Catches a fetch that
+    picks the wrong rows as well as an attention that ignores the overrides."""
+    B, Hkv, Hq, D, G = 1, 2, 4, 64, 32
+    N = 3 * G + 9
+    K, V = ki.kv_stream(43, B, Hkv, N, D)
+    c = _cache_from_tokens("int2", G, K, V)
+    q = ki.queries(43, B, 1, Hq, D)
+    sel = np.tile(np.arange(c.Lq, dtype=np.int32)[::-1], (B, Hkv, 1))
+    sk, sv = oracle.gather_selected(K, V, sel)
+    out, _ = oracle.attend(c, "int2", q, None, None, sel, sk, sv)
+    for h in range(Hq):
+        kvh = h // (Hq // Hkv)
+        ref = _sdpa_reference(q[0, 0, h], K[0, kvh], V[0, kvh], np.ones(N, bool), 1 / math.sqrt(D))
+        np.testing.assert_allclose(out[0, 0, h], ref, rtol=1e-10, atol=1e-12)
