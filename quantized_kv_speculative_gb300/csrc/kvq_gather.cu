@@ -14,6 +14,7 @@
 // kvq_attend takes as sel_k / sel_v.  Each warp moves whole rows with 16-byte
 // loads, with eight entries' loads in flight per lane before any store, so
 // that the link sees thousands of independent 256-byte requests at once.
+#include <algorithm>
 #include <cstdint>
 
 #include "kvq.h"
