@@ -161,3 +161,26 @@ def test_host_state_machine_without_launch(lib):
     n_max = (C // G + 2) * G - 1
     assert lib.kvq_quantize_append(ctypes.byref(c), fake, fake, n_max + 1, None) == 3
     assert (c.quantized_len, c.residual_len) == (0, 0)
+
+
+def test_gather_and_plan_argument_errors_need_no_gpu(lib):
+    """The fetch and the plan query refuse bad arguments before touching the
+    device: null pointers, head_dim outside {64, 128}, top_k outside
+    [1, 1024], misaligned rows, and an uninitialized cache."""
+    fake = ctypes.c_void_p(1 << 41)
+    odd = ctypes.c_void_p((1 << 41) + 8)
+
+    def gather(fk=fake, fv=fake, n=64, B=1, H=2, D=128, si=fake, k=4, sk=fake, sv=fake):
+        return lib.kvq_gather_selected(fk, fv, n, B, H, D, si, k, sk, sv, None)
+    assert gather(fk=None) == 1 and gather(si=None) == 1 and gather(sv=None) == 1
+    assert gather(D=96) == 1 and gather(k=0) == 1 and gather(k=1025) == 1
+    assert gather(B=0) == 1 and gather(n=0) == 1
+    assert gather(fk=odd) == 1 and gather(sk=odd) == 1
+    info = kvq.KvqAttendPlanInfo()
+    uninit = kvq.KvqCache()
+    assert lib.kvq_attend_plan(ctypes.byref(uninit), 0, 4, 1, 0, 0, ctypes.byref(info)) == 7
+    c, _ = _host_cache(lib)
+    assert lib.kvq_attend_plan(ctypes.byref(c), 0, 4, 1, 0, 0, None) == 1
+    assert lib.kvq_attend_plan(ctypes.byref(c), 2, 4, 1, 0, 0, ctypes.byref(info)) == 2    # INT2 on hier8
+    assert lib.kvq_attend_plan(ctypes.byref(c), 0, 36, 1, 0, 0, ctypes.byref(info)) == 2   # 9 rows per KV head
+    assert lib.kvq_attend_plan(ctypes.byref(c), 0, 6, 1, 0, 0, ctypes.byref(info)) == 1    # Hq % Hkv != 0
