@@ -368,15 +368,6 @@ W_BITS = 21          # magnitude bits of the integer-rounded folded query weight
 E_MIN = -100         # floor on the weight exponent (keeps the unit a normal fp32)
 
 
-def _ordered_pair_tree(p: Sequence[np.float32]) -> np.float32:
-    """Pairwise (balanced binary tree) fp32 sum in index order:
-    ((p0 + p1) + (p2 + p3)) + ...; the length must be a power of two."""
-    vals = [F32(v) for v in p]
-    while len(vals) > 1:
-        vals = [F32(vals[2 * i] + vals[2 * i + 1]) for i in range(len(vals) // 2)]
-    return vals[0]
-
-
 def score_group(qs: np.ndarray, scale_eff: np.ndarray, zero: np.ndarray,
                 codes: np.ndarray) -> np.ndarray:
     """Top-k score of the G tokens of one key group for one summed query.
@@ -391,13 +382,15 @@ def score_group(qs: np.ndarray, scale_eff: np.ndarray, zero: np.ndarray,
       e     = exponent of max_d |w_d| (max|w| < 2^e), floored at -100
       W_d   = rint(w_d * 2^(21 - e))                         (|W_d| <= 2^21)
       S_t   = sum_d W_d * code_{t,d}                         (exact integer)
-      beta  = pairwise-tree sum over 32 channel chunks of a sequential fp32 sum
-              of fp32(qs_d * zero_d) within each chunk
+      beta  = ((0 + fp32(qs_0 z_0)) + fp32(qs_1 z_1)) + ... + fp32(qs_{D-1} z_{D-1})
+              (fp32 adds in ascending channel order)
       score = fp32( fp32(fp32(S_t) * 2^(e - 21)) + beta )
 
     The integer dot product is exact, so summation order cannot change it.
-    The only roundings are the weights' 2^-21 relative rounding, fp32(S_t), one
-    exact power-of-two scaling and the final add.
+    The zero-point term beta is the plain left-to-right fp32 sum of the
+    rounded products.  The only other roundings are the weights' 2^-21
+    relative rounding, fp32(S_t), one exact power-of-two scaling and the
+    final add.
     """
     D = qs.shape[0]
     w = (qs.astype(F32) * scale_eff.astype(F32)).astype(F32)
@@ -408,14 +401,9 @@ def score_group(qs: np.ndarray, scale_eff: np.ndarray, zero: np.ndarray,
     S = codes.astype(np.int64) @ W                       # exact integer dot products
     Sf = S.astype(np.float64).astype(F32)                # |S| < 2^53: one rounding
     unit = F32(2.0 ** (e - W_BITS))
-    chunk = D // 32
-    partials = []
-    for c in range(32):
-        p = F32(0)
-        for d in range(c * chunk, (c + 1) * chunk):
-            p = F32(p + F32(qs[d] * zero[d]))
-        partials.append(p)
-    beta = _ordered_pair_tree(partials)
+    beta = F32(0)
+    for d in range(D):
+        beta = F32(beta + F32(F32(qs[d]) * F32(zero[d])))
     return ((Sf * unit).astype(F32) + beta).astype(F32)
 
 

@@ -19,6 +19,12 @@ MUTATIONS = [
     ("INT4 scale without the 16x", "scale.astype(np.float64) * 16.0", "scale.astype(np.float64) * 1.0"),
     ("top-k score without the zero-point term",
      "return ((Sf * unit).astype(F32) + beta).astype(F32)", "return (Sf * unit).astype(F32)"),
+    ("top-k zero-point sum in descending channel order",
+     "    for d in range(D):\n        beta = F32(beta + F32(F32(qs[d]) * F32(zero[d])))",
+     "    for d in reversed(range(D)):\n        beta = F32(beta + F32(F32(qs[d]) * F32(zero[d])))"),
+    ("top-k zero-point sum accumulated in fp64",
+     "        beta = F32(beta + F32(F32(qs[d]) * F32(zero[d])))",
+     "        beta = np.float64(beta) + np.float64(qs[d]) * np.float64(zero[d])"),
     ("causal offset off by one", "nvis = (P - gamma + i + 1) if P else 0", "nvis = (P - gamma + i) if P else 0"),
     ("strided instead of consecutive GQA grouping", "hq = h * hg + hh", "hq = hh * H + h"),
     ("flush one token early", "if self.r == 2 * self.G:", "if self.r == 2 * self.G - 1:"),

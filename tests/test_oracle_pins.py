@@ -345,6 +345,26 @@ def _exact_logit(cache, mode, qs, b, h):
     return np.array([math.fsum(q64 * kh[t]) for t in range(kh.shape[0])])
 
 
+@pytest.mark.parametrize("grp", _golden("topk_score_examples.json")["groups"], ids=lambda g: g["name"])
+def test_topk_score_golden(grp):
+    """Hand-derived scores of tiny key groups (tests/golden/topk_score_examples.json).
+    The first group fixes the order of the zero-point sum: added left to right
+    its fp32 sum is 1, added right to left 1 + 2^-22, pairwise 1 + 2^-23.  The
+    all-zero-code tokens score exactly beta.  Catches a reordered or pairwise
+    beta, an fma-contracted product in the weights, a dropped beta and a wrong
+    weight exponent."""
+    qs = np.array(grp["qs"], np.float64).astype(F32)
+    s = np.array(grp["scale"], np.float64).astype(F32)
+    z = np.array(grp["zero"], np.float64).astype(F32)
+    codes = np.array(grp["codes"], np.uint8)
+    got = oracle.score_group(qs, s, z, codes)
+    want = np.array(grp["scores"], np.float64).astype(F32)
+    assert got.dtype == F32
+    np.testing.assert_array_equal(got.view(np.uint32), want.view(np.uint32))
+    zero_rows = np.flatnonzero(codes.sum(1) == 0)
+    assert zero_rows.size and np.all(got[zero_rows] == F32(grp["beta"]))
+
+
 @pytest.mark.parametrize("mode,fmt", [("int4", "hier8"), ("int2", "int2"), ("int1", "int1")])
 def test_topk_score_fidelity(mode, fmt):
     """The canonical score stays within its stated error of the exact logit
