@@ -139,16 +139,21 @@ typedef struct kvq_cache {
   uint32_t reserved1;
 } kvq_cache;
 
-/* Human-readable name of a status code (static string, never NULL). */
+/* Human-readable name of a status code (static string, never NULL).  The pages
+ * have no counterpart: this is part of the library's error reporting. */
 const char* kvq_status_string(kvq_status s);
 
 /* Bytes of device memory a cache with this descriptor needs (0 if the descriptor
- * is invalid). */
+ * is invalid).  The pages have no counterpart: they give no storage layout, and
+ * this one is the library's own (see the layout above). */
 size_t kvq_cache_bytes(const kvq_cache_desc* desc);
 
 /* Lay out a cache in caller memory `dev_mem` (>= kvq_cache_bytes, 256-B aligned)
  * and set it empty (Lq = r = 0).  Writes only the host struct: the device
- * memory's contents are ignored until written by kvq_quantize_append. */
+ * memory's contents are ignored until written by kvq_quantize_append.  The
+ * pages have no counterpart: it sets up the library's own layout.  Errors:
+ * KVQ_ERR_INVALID_ARG for a null struct, an invalid descriptor, null or
+ * misaligned memory, or fewer bytes than kvq_cache_bytes. */
 kvq_status kvq_cache_init(kvq_cache* cache, const kvq_cache_desc* desc, void* dev_mem,
                           size_t bytes);
 
@@ -173,10 +178,14 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const void* k_new, const void* 
                                int32_t n_new, kvq_stream_t stream);
 
 /* Bytes of workspace that kvq_attend / kvq_topk need for this cache, at any fill
- * up to capacity.  Rows per KV head R = gamma * num_q_heads / num_kv_heads must be
- * <= 8.  top_k <= 1024.  The workspace must be zero-filled once before its first
- * use.  Every call that finishes leaves it reusable.  Returns 0 for invalid
- * arguments. */
+ * up to capacity, on the current device (the split count grows with its SM
+ * count; a workspace sized on a device with fewer SMs can be too small, which a
+ * call reports as KVQ_ERR_WORKSPACE).  Rows per KV head R = gamma * num_q_heads /
+ * num_kv_heads must be <= 8.  top_k <= 1024.  The workspace must be zero-filled
+ * once before its first use.  Every call that finishes leaves it reusable.
+ * Returns 0 for invalid arguments.  The pages have no counterpart: the
+ * workspace holds the split-K partials and the merge's ticket counters of the
+ * library's own launch design. */
 size_t kvq_workspace_bytes(const kvq_cache* cache, int32_t num_q_heads, int32_t gamma,
                            int32_t top_k);
 
@@ -244,8 +253,8 @@ kvq_status kvq_attend_plan(const kvq_cache* cache, kvq_mode mode, int32_t num_q_
  *   w_d = fp32(qs_d * s_d)   (s = the mode's key scale: x16 for INT4)
  *   e   = exponent with max_d|w_d| < 2^e, floored at -100
  *   W_d = rint(w_d * 2^(21-e)),  S_t = sum_d W_d * code_{t,d} (exact integer)
- *   beta = pairwise-tree sum of 32 channel-chunk partial sums, each a
- *          sequential fp32 sum of fp32(qs_d * zero_d)
+ *   beta = ((0 + fp32(qs_0 zero_0)) + fp32(qs_1 zero_1)) + ... , fp32 adds in
+ *          ascending channel order
  *   score_t = fp32(fp32(fp32(S_t) * 2^(e-21)) + beta)
  * Tokens are ordered by (score descending, index ascending).  Positions beyond
  * Lq get index -1 and score -inf.
@@ -272,12 +281,16 @@ kvq_status kvq_topk(const kvq_cache* cache, kvq_mode mode, const void* q_spec,
  * is a fixed 16 MiB array compiled into the library, so the call allocates
  * nothing (no cudaMalloc, cudaFree or allocating library routine).  Every GPU
  * that loads the library holds that array until the process exits.
- *  - Limit: the cache must need at most 16 MiB of attention workspace
- *    (kvq_workspace_bytes(cache, num_q_heads, gamma, 0) <= 16 MiB).  Otherwise
- *    the call returns KVQ_ERR_WORKSPACE and enqueues nothing.
+ *  - Limit: the attention workspace kvq_attend would need for this cache
+ *    (256 bytes of status word, the ticket counters and the split partials)
+ *    must be at most 16 MiB.  Otherwise the call returns KVQ_ERR_WORKSPACE and
+ *    enqueues nothing.  Every other argument error returns kvq_attend's status
+ *    code, also before anything is enqueued.
  *  - Set-up: the first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and keeps it.  Make that
- *    first call before any stream capture.
+ *    (cudaGetSymbolAddress, with that device current) and keeps it.  With CUDA's
+ *    lazy module loading, that lookup may load the library's device code and
+ *    reserve the array on the device, which can synchronize it.  Make that first
+ *    call during start-up, before any stream capture.
  *  - Sharing: every call uses the same array and leaves its last contents there.
  *    Each call clears the ticket counters it needs on `stream` first.  Calls
  *    that overlap on the GPU (other streams, other threads) race on the array:

@@ -8,7 +8,10 @@
 // rounded to 22-bit integers, then scaled:
 //   W_d = rint(fp32(qs_d * s_d) * 2^(21-e)), S_t = sum_d W_d c_{t,d},
 //   score_t = fp32(fp32(fp32(S_t) * 2^(e-21)) + beta),
-//   beta = pairwise tree over 32 lane-chunks of sequential fp32 sums of fp32(qs_d * z_d).
+//   beta = ((0 + fp32(qs_0 z_0)) + fp32(qs_1 z_1)) + ... (fp32 adds, ascending d).
+// beta is a sequential chain: one thread per key group of the chunk computes
+// it while the first tiles load, and the scoring loop reads it from shared
+// memory.
 // The dot product runs on tensor cores with the keys as the A operand (rows =
 // tokens) and W as the B operand: column 0 holds hi and column 1 holds lo,
 // where W = 2048 hi + lo and |hi|, |lo| <= 1024 are f16-exact integers.  The
@@ -60,7 +63,8 @@ struct TopkSmem {
   static constexpr int RED_OFF = LIST_OFF + kGather * 4;      // per-warp min/max, counts [2 NW]
   static constexpr int BAR_OFF = RED_OFF + 2 * NW * 4;
   static constexpr int MISC_OFF = BAR_OFF + NSLOT * 8;
-  static constexpr int SC_OFF = MISC_OFF + 64;                // order keys / merge keys (sized per launch)
+  static constexpr int BETA_OFF = MISC_OFF + 64;              // beta per key group of the chunk
+  static constexpr int SC_OFF = BETA_OFF + kTopkMaxChunk / 32 * 4;   // order keys / merge keys (sized per launch)
   static constexpr int MAX_SC = kTopkMaxCand * 16;            // >= kTopkMaxChunk * 4; two merge buffers
   static constexpr int MAX_TOTAL = SC_OFF + MAX_SC;
   static_assert(kTopkMaxChunk * 4 <= MAX_SC, "chunk scores must fit");
@@ -403,6 +407,27 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
     qs[tid] = acc;
   }
   __syncthreads();
+  // beta of every key group of the chunk: fp32(qs_d * z_d) added in ascending
+  // channel order, one thread per group (at most 8192 / 32 = 256 groups)
+  float* beta_s = reinterpret_cast<float*>(smem + L::BETA_OFF);
+  static_assert(kTopkMaxChunk / 32 <= NTHREADS, "one thread per key group");
+  {
+    const int ngrp = (n + G - 1) / G;
+    if (tid < ngrp) {
+      const float4* z4 = reinterpret_cast<const float4*>(p.c.ksz + (u * (p.c.C / G) + t_begin / G + tid) * 2 * D + D);
+      float acc = 0.f;
+#pragma unroll 8
+      for (int d4 = 0; d4 < D / 4; ++d4) {
+        const float4 z = __ldg(z4 + d4);
+        acc = __fadd_rn(acc, __fmul_rn(qs[4 * d4 + 0], z.x));
+        acc = __fadd_rn(acc, __fmul_rn(qs[4 * d4 + 1], z.y));
+        acc = __fadd_rn(acc, __fmul_rn(qs[4 * d4 + 2], z.z));
+        acc = __fadd_rn(acc, __fmul_rn(qs[4 * d4 + 3], z.w));
+      }
+      beta_s[tid] = acc;
+    }
+  }
+  __syncthreads();
   volatile int* abort_flag = misc;
 
   {
@@ -438,22 +463,17 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
           // ---- W of this group: lane l derives channels [l*D/32, (l+1)*D/32) ----
           cur_grp = grp;
           const float* ks = ksz + (grp - g_first) * 2 * D;
-          const float* kz = ks + D;
           float w[CPL];
-          float mxw = 0.f, bp = 0.f;
+          float mxw = 0.f;
 #pragma unroll
           for (int c = 0; c < CPL; ++c) {
             const int d = lane * CPL + c;
             w[c] = __fmul_rn(qs[d], __fmul_rn(ks[d], smul));
             mxw = fmaxf(mxw, fabsf(w[c]));
-            bp = __fadd_rn(bp, __fmul_rn(qs[d], kz[d]));
           }
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            mxw = fmaxf(mxw, __shfl_xor_sync(0xffffffffu, mxw, o));
-            bp = __fadd_rn(bp, __shfl_xor_sync(0xffffffffu, bp, o));
-          }
-          beta = bp;
+          for (int o = 1; o < 32; o <<= 1) mxw = fmaxf(mxw, __shfl_xor_sync(0xffffffffu, mxw, o));
+          beta = beta_s[grp - t_begin / G];
           int e = 0;
           if (mxw > 0.f) frexpf(mxw, &e);
           e = max(e, -100);
@@ -715,19 +735,6 @@ int per_sm_t(int smem) {
   return per_sm;
 }
 
-int sm_count() {
-  constexpr int kMaxDev = 64;
-  static int cached[kMaxDev] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
-  if (cached[dev] == 0) {
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = sms;
-  }
-  return cached[dev];
-}
-
 long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
 
 // Split plan: over S from the fewest splits the chunk limit allows to the most
@@ -739,7 +746,7 @@ int plan_t(long long Lq, long long U, int G, int k, long long* chunk_out) {
   const long long align = std::max<long long>(kChunkAlign, static_cast<long long>(NW) * std::max(G, Mode<MODE>::TT));
   const long long s_lo = std::max(1LL, ceil_div_ll(Lq, kTopkMaxChunk));
   const long long s_hi = std::max(s_lo, std::min(ceil_div_ll(Lq, align), static_cast<long long>(kTopkMaxCand / k)));
-  const int sms = sm_count();
+  const int sms = device_sm_count();
   long long best_s = 0, best_ch = 0;
   double best_cost = 0.0;
   for (long long S = s_lo; S <= s_hi; ++S) {
@@ -748,7 +755,7 @@ int plan_t(long long Lq, long long U, int G, int k, long long* chunk_out) {
     const long long s_eff = ceil_div_ll(Lq, ch);
     if (s_eff != S) continue;
     const int per_sm = per_sm_t<MODE, D>(smem_bytes<MODE, D>(ch, static_cast<int>(S), k));
-    const long long slots = (per_sm > 0 && sms > 0) ? static_cast<long long>(per_sm) * sms : kTargetCtas;
+    const long long slots = (per_sm > 0 && sms > 0) ? static_cast<long long>(per_sm) * sms : target_ctas();
     const long long waves = ceil_div_ll(U * S, slots);
     const double cost = static_cast<double>(waves) * static_cast<double>(ch + 1024) + 0.25 * static_cast<double>(S * k);
     if (best_s == 0 || cost < best_cost) {
