@@ -64,7 +64,7 @@ long long units_of(const kvq_cache* c) {
 
 // Quantized splits per (b, kvh) for attention, and the chunk size.  `slots` is
 // how many CTAs of the kernel fit on the device at once.  Over the split counts
-// from the fewest the chunk limit allows to the kTargetCtas share, pick the one
+// from the fewest the chunk limit allows to the target_ctas() share, pick the one
 // with the smallest waves x (chunk + per-split overhead), the `tail` CTAs per
 // (b, kvh) counted in the waves; chunks are multiples of kChunkAlign.
 int attend_splits(long long Lq, long long U, long long slots, long long tail, long long max_chunk, long long* chunk) {
@@ -74,7 +74,7 @@ int attend_splits(long long Lq, long long U, long long slots, long long tail, lo
   }
   const long long s_min = std::max(1LL, ceil_div(Lq, max_chunk));
   const long long s_cap = std::max(
-      s_min, std::min<long long>(kMaxQuantSplits, std::min(ceil_div(Lq, kChunkAlign), std::max(1LL, ceil_div(kTargetCtas, U)))));
+      s_min, std::min<long long>(kMaxQuantSplits, std::min(ceil_div(Lq, kChunkAlign), std::max(1LL, ceil_div(target_ctas(), U)))));
   long long best_s = 0, best_ch = 0, best_cost = 0;
   for (long long S = s_min; S <= s_cap; ++S) {
     const long long ch = ceil_div(ceil_div(Lq, S), kChunkAlign) * kChunkAlign;
@@ -106,7 +106,7 @@ int attend_splits_max(const kvq_cache_desc* d) {
   const long long U = static_cast<long long>(d->batch) * d->num_kv_heads;
   const long long Lq = d->capacity_tokens;
   if (Lq <= 0) return 0;
-  const long long target = std::min<long long>(kMaxQuantSplits, std::max(1LL, ceil_div(kTargetCtas, U)));
+  const long long target = std::min<long long>(kMaxQuantSplits, std::max(1LL, ceil_div(target_ctas(), U)));
   long long S = std::min(ceil_div(Lq, kChunkAlign), target);
   S = std::max(S, ceil_div(Lq, kMaxChunk));
   return static_cast<int>(std::max(S, 1LL));
@@ -211,6 +211,24 @@ AttendPlan plan_attend(const kvq_cache* cache, int mode, int R, int n_pend, int 
 }
 
 }  // namespace
+
+int kvq::device_sm_count() {
+  constexpr int kMaxDev = 64;
+  static int cached[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  if (cached[dev] == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = sms;
+  }
+  return cached[dev];
+}
+
+long long kvq::target_ctas() {
+  const int sms = device_sm_count();
+  return static_cast<long long>(kCtasPerSmTarget) * (sms > 0 ? sms : 152);
+}
 
 extern "C" {
 
@@ -343,11 +361,14 @@ size_t kvq_workspace_bytes(const kvq_cache* cache, int32_t num_q_heads, int32_t 
   return kStatusBytes + attend_ws_bytes(&cache->desc) + topk_ws_bytes(&cache->desc, std::max(top_k, 1));
 }
 
-kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int32_t num_q_heads,
-                      int32_t gamma, const void* pend_k, const void* pend_v, int32_t n_pend,
-                      const int32_t* sel_idx, const void* sel_k, const void* sel_v, int32_t top_k,
-                      float sm_scale, void* out, float* lse, void* workspace, size_t ws_bytes,
-                      kvq_stream_t stream) {
+}  // extern "C"
+
+// Every argument check of kvq_attend except the workspace's.  On success sets
+// *ws_need to the workspace bytes the call needs.
+kvq_status kvq::attend_check(const kvq_cache* cache, int mode, const void* q, int num_q_heads, int gamma,
+                             const void* pend_k, const void* pend_v, int n_pend, const int32_t* sel_idx,
+                             const void* sel_k, const void* sel_v, int top_k, const void* out, const float* lse,
+                             size_t* ws_need) {
   if (!cache || cache->magic != kMagic) return KVQ_ERR_NOT_INITIALIZED;
   if (!valid_desc(&cache->desc)) return KVQ_ERR_INVALID_ARG;
   if (!mode_reads(mode, cache->desc.format)) return KVQ_ERR_UNSUPPORTED;
@@ -364,7 +385,23 @@ kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int3
   if (top_k > 0 && (!sel_idx || !sel_k || !sel_v || !aligned16(sel_idx) || !aligned16(sel_k) ||
                     !aligned16(sel_v)))
     return KVQ_ERR_INVALID_ARG;
-  const size_t need = kStatusBytes + attend_ws_bytes(&cache->desc);
+  *ws_need = kStatusBytes + attend_ws_bytes(&cache->desc);
+  return KVQ_OK;
+}
+
+extern "C" {
+
+kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int32_t num_q_heads,
+                      int32_t gamma, const void* pend_k, const void* pend_v, int32_t n_pend,
+                      const int32_t* sel_idx, const void* sel_k, const void* sel_v, int32_t top_k,
+                      float sm_scale, void* out, float* lse, void* workspace, size_t ws_bytes,
+                      kvq_stream_t stream) {
+  size_t need = 0;
+  const kvq_status chk = attend_check(cache, mode, q, num_q_heads, gamma, pend_k, pend_v, n_pend, sel_idx, sel_k,
+                                      sel_v, top_k, out, lse, &need);
+  if (chk != KVQ_OK) return chk;
+  const int Hkv = cache->desc.num_kv_heads;
+  const int HG = num_q_heads / Hkv;
   if (!workspace || !aligned16(workspace) || ws_bytes < need) return KVQ_ERR_WORKSPACE;
   if (!(sm_scale > 0.f)) sm_scale = 1.0f / std::sqrt(static_cast<float>(cache->desc.head_dim));
 

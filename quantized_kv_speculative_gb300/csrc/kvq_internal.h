@@ -15,7 +15,7 @@ constexpr int kMaxChunk = 8192;        // tokens per attention split, up to four
 constexpr int kMaxChunkWide = 16384;   // the same for the eight-row variants
 constexpr int kSplitOverheadTokens = 256;  // a split CTA's fixed cost in the split planner, in tokens
 __host__ __device__ constexpr int max_chunk_for_rows(int R) { return R > 4 ? kMaxChunkWide : kMaxChunk; }
-constexpr int kTargetCtas = 608;       // 4 x 152 SMs: split-count target per launch
+constexpr int kCtasPerSmTarget = 4;   // split-count target per launch: this many CTAs per SM
 constexpr int kTopkMaxChunk = 8192;    // tokens per top-k split (scores held in shared memory)
 constexpr int kTopkMaxCand = 4096;     // splits x k candidates merged by the last CTA
 constexpr int kMaxTopk = 1024;
@@ -150,5 +150,16 @@ cudaError_t launch_topk(const TopkParams& p, int mode, cudaStream_t s);
 // (b, kv head) and sets *chunk (tokens per split).
 int topk_plan(int mode, int D, int G, long long Lq, long long U, int k, long long* chunk);
 cudaError_t launch_wait_selftest(int* status, long long limit, cudaStream_t s);
+// SMs of the current device (cached per device; 0 if unknown).
+int device_sm_count();
+// Split-count target of one launch on the current device: kCtasPerSmTarget x
+// its SM count (152 SMs assumed when the count is unknown).
+long long target_ctas();
+// kvq_attend's argument checks (all but the workspace), with kvq_attend's
+// status codes; on KVQ_OK *ws_need holds the workspace bytes the call needs.
+kvq_status attend_check(const kvq_cache* cache, int mode, const void* q, int num_q_heads, int gamma,
+                        const void* pend_k, const void* pend_v, int n_pend, const int32_t* sel_idx,
+                        const void* sel_k, const void* sel_v, int top_k, const void* out, const float* lse,
+                        size_t* ws_need);
 
 }  // namespace kvq

@@ -8,16 +8,16 @@
 //   INT2 / INT1: the 2-/1-bit planes, scale x1
 //
 // Tensor-core mapping (m16n8k16, see kvq_device.cuh).  Lane = 4*g + q.
-// Logits are computed transposed, S^T = W x K^T:
-//  * A = folded query weights (rows g: high f16 part, rows g+8: low part)
-//  * B = key codes (col n = token, k = channel)
-// Thread q owns channels [q*D/4, (q+1)*D/4) of every token.  It turns them into
-// D/8 half2 "pairs" P[p]; k-step kk consumes P[2kk] and P[2kk+1].  pair_chan()
-// gives the channels of pair p, so A is built with the same permutation.
-// In n-tile j the thread's column-n token is 4n + j of the 32-token slab.  So
-// C column 2q holds token 8q + j and column 2q+1 holds token 8q + j + 4.  These
-// are exactly the token pairs the value conversion below produces, so the
-// logit registers become the B operand of P.V with no shuffle.
+// Logits are S = K x W:
+//  * A = key codes (rows = 16 tokens of an m-tile, k = 16 channels of a k-step)
+//  * B = folded query weights (column = query row and high / low f16 part)
+// Thread q owns channels [q*D/4, (q+1)*D/4) of every token row.  It turns them
+// into D/8 half2 "pairs" P[p]; k-step kk consumes P[2kk] and P[2kk+1].
+// kx_chan() gives the channels of pair p, so the weights are laid out over the
+// same permutation.  The token each lane's A rows hold is chosen (xpair_a /
+// xpair_b below) so that the logit registers a lane ends up with are, after one
+// shuffle, a whole B register of P.V, whose A operand is the value codes
+// (rows = channels, k = tokens).
 #pragma once
 
 #include <type_traits>

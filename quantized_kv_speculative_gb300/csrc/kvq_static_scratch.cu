@@ -25,7 +25,10 @@ void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  The array's name
 // in host code is only a host-side stand-in, so its device address is looked
-// up once per device with that device current, and remembered.
+// up once per device with that device current, and remembered.  Under CUDA's
+// lazy module loading this first lookup may load the library's module on the
+// device, which reserves the array there (and can synchronize), so callers
+// make their first call at start-up.
 kvq_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -47,9 +50,12 @@ extern "C" kvq_status kvq_attend_static_scratch(const kvq_cache* cache, kvq_mode
                                                 const void* pend_v, int32_t n_pend, const int32_t* sel_idx,
                                                 const void* sel_k, const void* sel_v, int32_t top_k,
                                                 float sm_scale, void* out, float* lse, kvq_stream_t stream) {
-  if (!cache) return KVQ_ERR_NOT_INITIALIZED;
-  const size_t need = kvq_workspace_bytes(cache, num_q_heads, gamma, 0);
-  if (need == 0) return KVQ_ERR_INVALID_ARG;
+  // Every argument is checked, with kvq_attend's own status codes, before
+  // anything is enqueued on the shared array.
+  size_t need = 0;
+  const kvq_status chk = kvq::attend_check(cache, mode, q, num_q_heads, gamma, pend_k, pend_v, n_pend, sel_idx,
+                                           sel_k, sel_v, top_k, out, lse, &need);
+  if (chk != KVQ_OK) return chk;
   if (need > kStaticScratchBytes) return KVQ_ERR_WORKSPACE;   // this cache needs more than 16 MiB
   void* scratch = nullptr;
   const kvq_status st = scratch_address(&scratch);

@@ -184,3 +184,24 @@ def test_gather_and_plan_argument_errors_need_no_gpu(lib):
     assert lib.kvq_attend_plan(ctypes.byref(c), 2, 4, 1, 0, 0, ctypes.byref(info)) == 2    # INT2 on hier8
     assert lib.kvq_attend_plan(ctypes.byref(c), 0, 36, 1, 0, 0, ctypes.byref(info)) == 2   # 9 rows per KV head
     assert lib.kvq_attend_plan(ctypes.byref(c), 0, 6, 1, 0, 0, ctypes.byref(info)) == 1    # Hq % Hkv != 0
+
+
+def test_static_scratch_argument_errors_need_no_gpu(lib):
+    """The allocation-free attention entry point checks every argument with
+    kvq_attend's own status codes before it touches the shared array: an
+    uninitialized cache (7), mode vs format (2), more than 8 rows per KV head
+    (2), a null or misaligned query and too few pending tokens (1).  None of
+    these needs a GPU, because nothing is enqueued."""
+    c, _ = _host_cache(lib)
+    fake = ctypes.c_void_p(1 << 41)
+
+    def static(cache, mode, q=fake, Hq=4, gamma=1, pk=None, pv=None, P=0, out=fake):
+        return lib.kvq_attend_static_scratch(ctypes.byref(cache), mode, q, Hq, gamma, pk, pv, P, None, None, None,
+                                             0, 0.0, out, None, None)
+    assert static(kvq.KvqCache(), 0) == 7
+    assert static(c, 2) == 2
+    assert static(c, 0, Hq=36) == 2
+    assert static(c, 0, q=None) == 1
+    assert static(c, 0, q=ctypes.c_void_p((1 << 41) + 8)) == 1
+    assert static(c, 0, out=None) == 1
+    assert static(c, 0, gamma=2, pk=fake, pv=fake, P=1) == 1

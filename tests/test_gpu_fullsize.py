@@ -47,6 +47,7 @@ def _compare_units(gc, oc, units):
         np.testing.assert_array_equal(ksz[:, 1].view(np.uint32), oc.k_zero[0, j, :L // G].view(np.uint32))
         vsz = gc.v_scale_zero()[u, :L].cpu().numpy()
         np.testing.assert_array_equal(vsz[:, 0].view(np.uint32), oc.v_scale[0, j, :L].view(np.uint32))
+        np.testing.assert_array_equal(vsz[:, 1].view(np.uint32), oc.v_zero[0, j, :L].view(np.uint32))
 
 
 def _attend_units(out_dev, lse_dev, oc, mode, q, units, hg, pk=None, pv=None, sel=None, sk=None, sv=None):

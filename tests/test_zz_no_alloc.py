@@ -2,11 +2,14 @@
 
 It serves callers that cannot allocate device memory (for example a decode
 loop that must not allocate after start-up).  Its workspace is a fixed array
-inside the library.  Through the C ABI, its output must match kvq_attend with
-a caller workspace, within the attention tolerance the other tests use, on
-two calls in a row: the second call reuses the array the first one left
-behind.  This file is collected last, so a run that stops at the first
-failure has already run every other test.
+inside the library.  Through the C ABI, its output must equal kvq_attend's
+with a caller workspace on two calls in a row: the second call reuses the
+array the first one left behind.  Both run the same deterministic kernel with
+the same launch plan, so the outputs and LSEs must be identical bytes, which
+is stricter than the attention tolerance the other tests use.  A call with a
+bad argument between the two must be refused with kvq_attend's status code
+and leave the next call's result unchanged.  This file is collected last, so
+a run that stops at the first failure has already run every other test.
 """
 import ctypes
 
@@ -18,7 +21,6 @@ import kvq_inputs as ki
 import quantized_kv_speculative_gb300 as kvq
 from quantized_kv_speculative_gb300 import _build
 
-from kvq_testlib import TOL_ABS, TOL_REL, bf16_ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -54,19 +56,24 @@ def test_static_scratch_matches_workspace_version(mode, B, Hkv, Hq, D, G, N, gam
                       for _ in range(B)]).astype(np.int32)
         sel = torch.from_numpy(s).cuda()
         sk, sv = up(ki.normal_bf16(g, (B, Hkv, top_k, D))), up(ki.normal_bf16(g, (B, Hkv, top_k, D)))
-    ref_out, ref_lse = kvq.kvq_attend(cache, mode, up(ki.queries(31, B, gamma, Hq, D)), pk, pv, sel, sk, sv)
+    q = up(ki.queries(31, B, gamma, Hq, D))
+    ref_out, ref_lse = kvq.kvq_attend(cache, mode, q, pk, pv, sel, sk, sv)
     torch.cuda.synchronize()
-    ref = ref_out.float().cpu().numpy().astype(np.float64)
+    ref = ref_out.view(torch.int16).cpu().numpy()
+    ref_l = ref_lse.view(torch.int32).cpu().numpy()
     for call in range(2):
-        q = up(ki.queries(31, B, gamma, Hq, D))
         out = torch.empty_like(q)
         lse = torch.empty((B, gamma, Hq), dtype=torch.float32, device="cuda")
         assert _call_static(lib, cache, mode, q, pk, pv, sel, sk, sv, out, lse) == 0, f"call {call}"
         torch.cuda.synchronize()
-        got = out.float().cpu().numpy().astype(np.float64)
-        tol = TOL_REL * np.abs(ref).max() + TOL_ABS + bf16_ulp(ref)
-        assert np.all(np.abs(got - ref) <= tol), f"call {call}: outputs differ beyond tolerance"
-        assert np.allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), rtol=1e-5, atol=1e-4), f"call {call}: lse"
+        np.testing.assert_array_equal(out.view(torch.int16).cpu().numpy(), ref, err_msg=f"call {call}: out")
+        np.testing.assert_array_equal(lse.view(torch.int32).cpu().numpy(), ref_l, err_msg=f"call {call}: lse")
+        if call == 0:
+            # a refused call (null query) between the two must change nothing
+            bad = lib.kvq_attend_static_scratch(ctypes.byref(cache.struct), kvq.MODES[mode], None, Hq, gamma,
+                                                None, None, 0, None, None, None, 0, 0.0, out.data_ptr(), None,
+                                                torch.cuda.current_stream().cuda_stream)
+            assert bad == 1, "a null query must be refused with KVQ_ERR_INVALID_ARG"
 
 
 def test_static_scratch_rejects_oversized_workspace():
