@@ -996,7 +996,8 @@ def run_profile_case(name, launches):
         idx, _ = kvq.kvq_topk(c, "int2", q[:, 1].contiguous(), k, workspace=ws)
         gi = idx.long().clamp_min(0)[..., None].expand(-1, -1, -1, D)
         sk, sv = torch.gather(K, 2, gi).contiguous(), torch.gather(V, 2, gi).contiguous()
-        del K, V
+        del K, V, gi
+        torch.cuda.empty_cache()
         for i in range(launches):
             if name.startswith("topk"):
                 kvq.kvq_topk(c, "int2", q[:, 1].contiguous(), k, idx_out=idx, workspace=ws)

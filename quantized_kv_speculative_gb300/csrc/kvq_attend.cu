@@ -30,17 +30,17 @@
 //    CTA that arrives last at a per-(b, kvh) atomic ticket merges them into the
 //    bf16 output and LSE, then resets the ticket; no CTA waits on another.
 //
-// Folding (no per-element dequant FMA).  A key code c reads as the f16 value
-// E = off + c / kw (INT8: off = 1024, kw = 1; INT4/2/1: off = 1, kw = 2^b), so
-// with q~ = q * sm_scale * log2(e), step s (MULT x scale) and zero z per group
-// and channel:
-//   logit2 = sum_d q~_d (c s + z) = sum_d w_d E_d + (sum_d q~_d z_d - off sum_d w_d),
-// with w_d = q~_d s_d kw; the bracket starts the accumulator.  Value codes read
-// as 1024 + m c (m a power of two set by the code's bit position); each slab's
-// P.V accumulator starts at -1024 sum_t P'_t, computed by one MMA with a
-// constant A operand, so the running output never carries the offset:
-//   o = sum_t p_t (c s + z) = sum_t P'_t (1024 + m c) - 1024 sum_t P'_t + sum_t p_t z_t,
-// with P'_t = p_t s_t / m_t.
+// Folding (no per-element dequant FMA).  Codes enter the tensor cores as f16
+// subnormals: a key code c of channel d reads as E_d = c f_d 2^-24, with f_d a
+// power of two set by the code's bit position in its word.  With
+// q~ = q * sm_scale * log2(e), step s (MULT x scale) and zero z per group and
+// channel:
+//   logit2 = sum_d q~_d (c s + z) = 2^24 sum_d (q~_d s_d / f_d) E_d + sum_d q~_d z_d,
+// so the B operand holds w_d = q~_d s_d / f_d (scaled by 2^e) and the
+// zero-point sum starts the accumulator.  Value codes read the same way, as
+// c m 2^-24 (m the pair's factor), against P'_t = p_t s_t / m_t:
+//   o = sum_t p_t (c s + z) = 2^24 sum_t P'_t (c m 2^-24) + sum_t p_t z_t.
+// No offset has to be removed, so the accumulators carry only the code terms.
 #include "kvq_modes.cuh"
 
 namespace kvq {
@@ -141,6 +141,16 @@ __host__ __device__ constexpr bool halves_shift() {
     for (int e = 0; e < 2; ++e)
       if (kx_chan<MODE, D>(HP + k, e) != kx_chan<MODE, D>(k, e) + kx_chan<MODE, D>(HP, 0)) return false;
   return kx_chan<MODE, D>(0, 0) == 0;
+}
+
+// True when the second half of a lane chunk's key pairs carries the first
+// half's code factors (the eight-row weight setup scales both halves alike).
+template <int MODE, int D>
+__host__ __device__ constexpr bool halves_same_factors() {
+  constexpr int HP = D / 16;
+  for (int k = 0; k < HP; ++k)
+    if (ks_log2fac<MODE, D>(HP + k) != ks_log2fac<MODE, D>(k)) return false;
+  return true;
 }
 
 // The queries of unit (b, kvh) as 16-byte slices of 8 channels: slice e is
@@ -835,7 +845,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
       const int i = 2 * s + par;
       tokA[s] = oct + xpair_a<MODE>(i);
       tokB[s] = oct + xpair_b<MODE>(i);
-      vinv[s] = 1.0f / vx_mult<MODE>(i);
+      vinv[s] = 1.0f / static_cast<float>(1 << vs_log2fac<MODE>(i));
     }
 
     uint32_t W[NT][NPK];                 // weights: this lane's B column part, per key pair
@@ -881,13 +891,13 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
         const int grp = tok0 / G;
         if (grp != cur_grp) {
           // ---- folded key weights of this group, derived once per warp ----
-          // w_c = q~_c * MULT * s_c * kx_weight, scaled by 2^e so that the
-          // largest possible |w| sits near 2^13, split into f16 high + low
-          // parts.  Lanes split the (row, channel pair) items of the rows in
-          // use (lpr lanes per row), stage the B fragments in the warp's
-          // weight buffer, then each lane loads its column.  The accumulator
-          // starts at 2^e sum_c q~_c z_c minus the encoding's offset times
-          // sum_c w_c.
+          // w_c = q~_c * MULT * s_c / f_c (f_c the channel's code factor),
+          // scaled by 2^e so that the largest possible |w| sits near 2^13,
+          // split into f16 high + low parts.  Lanes split the (row, channel
+          // pair) items of the rows in use (lpr lanes per row), stage the B
+          // fragments in the warp's weight buffer, then each lane loads its
+          // column.  The accumulator starts at 2^(e-24) sum_c q~_c z_c, and
+          // the logit is the accumulator times 2^(24-e).
           cur_grp = grp;
           const float* ks = ksz + (grp - g_first) * 2 * D;
           const float* kz = ks + D;
@@ -901,9 +911,9 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
 #pragma unroll
           for (int w2 = 1; w2 < NW; ++w2) qmax = fmaxf(qmax, qmw[w2]);
           constexpr int PPR = D / 2;           // channel pairs per row
-          constexpr float KW = MULT * kx_weight<MODE>();
-          float wsum = 0.f, zsum = 0.f;
-          float kscale_new, E2;
+          constexpr float KW = MULT;
+          float zsum = 0.f;
+          float kscale_new, Z2;
           if constexpr (NT == 2) {
             // eight rows: lanes g = 2r and 2r + 1 hold the high and the low
             // part of row 4nt + r (column g).  Each derives both parts for half
@@ -912,6 +922,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
             constexpr int HP = D / 16;                        // pairs per half chunk
             constexpr int DELTA = kx_chan<MODE, D>(HP, 0);    // channel offset of the second half
             static_assert(halves_shift<MODE, D>(), "the second half's pairs are the first half's, shifted");
+            static_assert(halves_same_factors<MODE, D>(), "both halves carry the same code factors");
             const int cb = q * (D / 4) + par * DELTA;         // this lane's channel base
             const float* ksc = ks + cb;
             const float* kzc = kz + cb;
@@ -928,18 +939,18 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
             smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 2));
             const float bound = qmax * smax * KW;
             const int e = (bound > 0.f) ? max(-100, min(100, 13 - exp2_floor(bound))) : 0;
-            E2 = pow2i(e);
-            kscale_new = pow2i(-e);
-            const float f = E2 * KW;
+            Z2 = pow2i(e - 24);
+            kscale_new = pow2i(24 - e);
+            const float f = pow2i(e) * KW;
 #pragma unroll
             for (int k = 0; k < HP; ++k) {
-              kv[k][0] *= f;
-              kv[k][1] *= f;
+              kv[k][0] *= f * ks_inv_fac<MODE, D>(k);
+              kv[k][1] *= f * ks_inv_fac<MODE, D>(k);
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               const float* qr = qt + (4 * nt + (g >> 1)) * qt_row<D>() + q * qt_chunk<D>() + par * DELTA;
-              float ws = 0.f, zs = 0.f;
+              float zs = 0.f;
               uint32_t keep[HP], send[HP];
 #pragma unroll
               for (int k = 0; k < HP; ++k) {
@@ -952,7 +963,6 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
                 const uint32_t lo = pack_half2(w0 - hf.x, w1 - hf.y);
                 keep[k] = par ? lo : hi;
                 send[k] = par ? hi : lo;
-                ws += w0 + w1;
               }
 #pragma unroll
               for (int k = 0; k < HP; ++k) {
@@ -960,7 +970,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
                 W[nt][k] = par ? recv : keep[k];
                 W[nt][HP + k] = par ? keep[k] : recv;
               }
-              float cwn = fmaf(zs, E2, -kx_offset<MODE>() * ws);
+              float cwn = zs * Z2;
               cwn += __shfl_xor_sync(0xffffffffu, cwn, 4);
               cwn += __shfl_xor_sync(0xffffffffu, cwn, 1);
               cwn += __shfl_xor_sync(0xffffffffu, cwn, 2);
@@ -978,9 +988,9 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
             for (int o2 = 16; o2 > 0; o2 >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o2));
             const float bound = qmax * smax * KW;
             const int e = (bound > 0.f) ? max(-100, min(100, 13 - exp2_floor(bound))) : 0;
-            E2 = pow2i(e);
-            kscale_new = pow2i(-e);
-            const float f = E2 * KW;
+            Z2 = pow2i(e - 24);
+            kscale_new = pow2i(24 - e);
+            const float f = pow2i(e) * KW;
             const float* qr = qt + wrow * qt_row<D>();
             const int col = 2 * (wrow & 3), ntw = wrow >> 2;
             for (int it = wsub; it < PPR; it += lpr) {
@@ -988,23 +998,20 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
               const int c0 = qq * (D / 4) + kx_chan<MODE, D>(pp, 0), c1 = qq * (D / 4) + kx_chan<MODE, D>(pp, 1);
               const float q0 = qr[qq * qt_chunk<D>() + kx_chan<MODE, D>(pp, 0)];
               const float q1 = qr[qq * qt_chunk<D>() + kx_chan<MODE, D>(pp, 1)];
-              const float w0 = q0 * ks[c0] * f, w1 = q1 * ks[c1] * f;
+              const float fp = f * ks_inv_fac<MODE, D>(pp);
+              const float w0 = q0 * ks[c0] * fp, w1 = q1 * ks[c1] * fp;
               const uint32_t hi = pack_half2(w0, w1);
               const float2 hf = unpack_half2(hi);
               const uint32_t lo = pack_half2(w0 - hf.x, w1 - hf.y);
               wb[((ntw * 8 + col) * 4 + qq) * (D / 8) + pp] = hi;
               wb[((ntw * 8 + col + 1) * 4 + qq) * (D / 8) + pp] = lo;
-              wsum += w0 + w1;
               zsum = fmaf(q0, kz[c0], fmaf(q1, kz[c1], zsum));
             }
           }
           kscale = kscale_new;
           if constexpr (NT == 1) {
-            for (int o2 = 1; o2 < lpr; o2 <<= 1) {
-              wsum += __shfl_xor_sync(0xffffffffu, wsum, o2);
-              zsum += __shfl_xor_sync(0xffffffffu, zsum, o2);
-            }
-            const float cw = fmaf(zsum, E2, -kx_offset<MODE>() * wsum);
+            for (int o2 = 1; o2 < lpr; o2 <<= 1) zsum += __shfl_xor_sync(0xffffffffu, zsum, o2);
+            const float cw = zsum * Z2;
             __syncwarp();
             const int row_b = g >> 1, row_c = q;
             const uint4* src = reinterpret_cast<const uint4*>(wb + (g * 4 + q) * (D / 8));
@@ -1026,8 +1033,8 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           uint32_t PA[NPK], PB[NPK];
-          key_pairs_x<MODE, D>(kslab + tokA[s] * RW::KROW, L::KPLANE, PA);
-          key_pairs_x<MODE, D>(kslab + tokB[s] * RW::KROW, L::KPLANE, PB);
+          key_pairs_s<MODE, D>(kslab + tokA[s] * RW::KROW, L::KPLANE, PA);
+          key_pairs_s<MODE, D>(kslab + tokB[s] * RW::KROW, L::KPLANE, PB);
           float acc[NT][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
@@ -1127,7 +1134,8 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
         // ---- P.V, one channel block (G channels) at a time ----
 #pragma unroll
         for (int jv = 0; jv < NJ; ++jv) {
-          // P' = p * s * MULT * 2^ev / vx_mult as f16 high + low parts, per m-tile
+          // P' = p * s * MULT * 2^ev / m (m the value pair's factor) as f16
+          // high + low parts, per m-tile
           uint32_t H[2][NT], Lo[2][NT];
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
@@ -1175,28 +1183,16 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
               }
             }
           }
-          // Value codes read as 1024 + m c.  The slab's 1024 * sum P' per column
-          // is the same for every channel: one MMA with a constant -1024 A
-          // operand computes it, and it starts every m-tile's accumulator.
-          // The slab's products go into that fresh accumulator, folded into
-          // the running output with one rounding per element: a long MMA chain
+          // The slab's products go into a fresh accumulator, folded into the
+          // running output with one rounding per element: a long MMA chain
           // would accumulate the tensor core's truncation.
-          float koff[4] = {0.f, 0.f, 0.f, 0.f};
-          {
-            const uint32_t aneg[4] = {0xE400E400u, 0xE400E400u, 0xE400E400u, 0xE400E400u};  // f16 -1024
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-              mma16816(koff, aneg, bh[s][0], bh[s][1]);
-              if constexpr (NT == 2) mma16816(koff, aneg, bl[s][0], bl[s][1]);
-            }
-          }
 #pragma unroll
           for (int mt = jv * (G / 16); mt < (jv + 1) * (G / 16); ++mt) {
             uint32_t a[2][4];
             const uint8_t* va = vslab + (16 * mt + g) * RW::VROW;
-            value_frags_x<MODE>(va, va + 8 * RW::VROW, L::VPLANE, q, a);
-            float os[4];
-            mma16816_c(os, a[0], bh[0][0], bh[0][1], koff);
+            value_frags_s<MODE>(va, va + 8 * RW::VROW, L::VPLANE, q, a);
+            float os[4] = {0.f, 0.f, 0.f, 0.f};
+            mma16816(os, a[0], bh[0][0], bh[0][1]);
             if constexpr (NT == 2) mma16816(os, a[0], bl[0][0], bl[0][1]);
             mma16816(os, a[1], bh[1][0], bh[1][1]);
             if constexpr (NT == 2) mma16816(os, a[1], bl[1][0], bl[1][1]);
@@ -1247,7 +1243,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
         for (int jv = 0; jv < NJ; ++jv) wc[(warp * 8 + rho) * 4 + jv] = vcorr[nt][jv];
       }
     }
-    const float oscale = (evs > 0.f) ? 1.0f / evs : 0.f;
+    const float oscale = (evs > 0.f) ? 16777216.0f / evs : 0.f;   // 2^24 / 2^ev
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
       const int ca = 16 * mt + g, cb = ca + 8;

@@ -120,26 +120,24 @@ __device__ __forceinline__ void key_pairs(const uint8_t* k0, int /*plane_stride*
 }
 
 // ------------------------------------------------------------------------------
-// Offset encoding for attention.  An f16 whose upper byte is 0x64 has exponent
-// 10, so its value is 1024 + m, where m is the 10-bit mantissa field.  A b-bit
-// code c whose bits sit at mantissa positions k..k+b-1 (k + b <= 10) thus reads
-// as exactly 1024 + 2^k c, and one LOP3 (mask, or with 0x6400) turns two codes
-// 16 bits apart into a half2.  For the 8-bit target code the two nibble planes
-// are first merged into bytes (shift + LOP3 per four codes), then a PRMT drops
-// each byte under 0x64.  The 1024 is removed inside the MMA accumulators:
-// value slabs start from -1024 times the sum of their probabilities, key
-// logits from the encoding's offset times the sum of their weights.
+// Subnormal encoding for attention.  An f16 whose exponent field is 0 is the
+// subnormal m * 2^-24, m its 10-bit mantissa field, and the tensor cores take
+// it exactly.  A b-bit code c whose bits sit at mantissa positions k..k+b-1
+// (k + b <= 10) therefore reads as exactly c * 2^k * 2^-24: no offset to
+// remove afterwards.  Two codes 16 bits apart in a 32-bit word become one half2
+// with a single AND, and a word's codes above mantissa bit 9 need one shift
+// first.  The power of two 2^k a pair carries (its factor) is divided out of
+// the other operand: out of the folded query weights for keys, out of the
+// folded probabilities for values.  The 8-bit target code first merges its two
+// nibble planes into bytes (shift + LOP3 per four codes), then a PRMT puts each
+// byte into the low half of an f16 (factor 1).
 //
 // For values, a lane reads 8 consecutive tokens 8q..8q+7 of a channel row;
-// pair i covers tokens 8q + xpair_a(i), 8q + xpair_b(i) with factor vx_mult(i).  For the
-// key chunk of a lane (D/4 channels of a token row), pair p covers channels
-// kx_chan(p, 0) and kx_chan(p, 1).
+// pair i covers tokens 8q + xpair_a(i), 8q + xpair_b(i) with factor
+// 2^vs_log2fac(i).  For the key chunk of a lane (D/4 channels of a token row),
+// pair p covers channels kx_chan(p, 0) and kx_chan(p, 1), with factor
+// 2^ks_log2fac(p).
 // ------------------------------------------------------------------------------
-
-constexpr uint32_t X1024 = 0x64006400u;   // half2(1024, 1024)
-constexpr uint32_t X64B = 0x64646464u;    // prmt source of the 0x64 bytes
-
-__device__ __forceinline__ uint32_t xsel(uint32_t w, uint32_t mask) { return (w & mask) | X1024; }
 
 // Value token pair i of a lane's 8 tokens 8q..8q+7: tokens 8q + xpair_a(i)
 // and 8q + xpair_b(i).  INT8: the merged nibble planes give the even tokens'
@@ -155,31 +153,13 @@ __host__ __device__ constexpr int xpair_b(int i) {
   return xpair_a<MODE>(i) + (MODE == KVQ_MODE_INT8 ? 2 : 4);
 }
 
-// Value factor of pair i: the power of two at which the pair's codes sit.
-// Every value code sits at mantissa bit 4 or higher (INT8 codes are 8 bits
-// wide), so the encoding's 1024 is at most about 43 times the code term.
+// log2 of value pair i's factor.
 template <int MODE>
-__host__ __device__ constexpr float vx_mult(int i) {
-  if constexpr (MODE == KVQ_MODE_INT8) return 1.f;
-  else if constexpr (MODE == KVQ_MODE_INT4) return 16.f;
-  else if constexpr (MODE == KVQ_MODE_INT2) return (i & 1) ? 64.f : 16.f;
-  else return static_cast<float>(1 << (6 + i));
-}
-
-// Keys for attention.  INT8 keys use the offset encoding (1024 + c): with
-// 8-bit codes the offset is at most about eight times the code term, and the
-// logit's MMA chain is only D/16 steps long.  INT4/INT2/INT1 keys use the
-// top-of-mantissa encoding of key_pairs (1 + c/2^b), whose offset of 1 is at
-// most about twice the code term.  kx_weight is the factor that turns a code's
-// scale into the weight of the encoded value; kx_offset the value an all-zero
-// code reads as.
-template <int MODE>
-__host__ __device__ constexpr float kx_weight() {
-  return MODE == KVQ_MODE_INT8 ? 1.f : static_cast<float>(1 << Mode<MODE>::CB);
-}
-template <int MODE>
-__host__ __device__ constexpr float kx_offset() {
-  return MODE == KVQ_MODE_INT8 ? 1024.f : 1.f;
+__host__ __device__ constexpr int vs_log2fac(int i) {
+  if constexpr (MODE == KVQ_MODE_INT8) return 0;
+  else if constexpr (MODE == KVQ_MODE_INT4) return (i & 1) ? 4 : 0;
+  else if constexpr (MODE == KVQ_MODE_INT2) return 2 * i;
+  else return i;
 }
 
 // Channels (relative to the lane chunk) of key pair p.
@@ -197,11 +177,26 @@ __host__ __device__ constexpr int kx_chan(int p, int e) {
   }
 }
 
-// The lane's key chunk of one token row as D/8 f16 pairs.  `k0` points at the
-// chunk in plane 0; plane 1 (INT8 lower nibbles) lies `plane_stride` bytes
-// further.
+// log2 of key pair p's factor.  The factors repeat with a period that divides
+// D/16, so both halves of a lane chunk see the same ones.
 template <int MODE, int D>
-__device__ __forceinline__ void key_pairs_x(const uint8_t* k0, int plane_stride, uint32_t (&P)[D / 8]) {
+__host__ __device__ constexpr int ks_log2fac(int p) {
+  if constexpr (MODE == KVQ_MODE_INT8) return 0;
+  else if constexpr (MODE == KVQ_MODE_INT4) return (p & 1) ? 4 : 0;
+  else if constexpr (MODE == KVQ_MODE_INT2) return 2 * (p % 4);
+  else return D == 128 ? p % 8 : p % 4;
+}
+
+template <int MODE, int D>
+__host__ __device__ constexpr float ks_inv_fac(int p) {
+  return 1.0f / static_cast<float>(1 << ks_log2fac<MODE, D>(p));
+}
+
+// The lane's key chunk of one token row as D/8 subnormal f16 pairs.  `k0`
+// points at the chunk in plane 0; plane 1 (INT8 lower nibbles) lies
+// `plane_stride` bytes further.
+template <int MODE, int D>
+__device__ __forceinline__ void key_pairs_s(const uint8_t* k0, int plane_stride, uint32_t (&P)[D / 8]) {
   if constexpr (MODE == KVQ_MODE_INT8) {
     constexpr int NWD = D / 32;
     uint32_t h[NWD], l[NWD];
@@ -220,23 +215,80 @@ __device__ __forceinline__ void key_pairs_x(const uint8_t* k0, int plane_stride,
     for (int w = 0; w < NWD; ++w) {
       const uint32_t E = ((h[w] << 4) & 0xF0F0F0F0u) | (l[w] & 0x0F0F0F0Fu);
       const uint32_t O = (h[w] & 0xF0F0F0F0u) | ((l[w] >> 4) & 0x0F0F0F0Fu);
-      P[4 * w + 0] = __byte_perm(E, X64B, 0x4140);
-      P[4 * w + 1] = __byte_perm(E, X64B, 0x4342);
-      P[4 * w + 2] = __byte_perm(O, X64B, 0x4140);
-      P[4 * w + 3] = __byte_perm(O, X64B, 0x4342);
+      P[4 * w + 0] = __byte_perm(E, 0u, 0x4140);
+      P[4 * w + 1] = __byte_perm(E, 0u, 0x4342);
+      P[4 * w + 2] = __byte_perm(O, 0u, 0x4140);
+      P[4 * w + 3] = __byte_perm(O, 0u, 0x4342);
+    }
+  } else if constexpr (MODE == KVQ_MODE_INT4) {
+    // nibble n of word w is channel 8w + n; pairs (n, n + 4)
+    constexpr int NWD = D / 32;
+    uint32_t h[NWD];
+    if constexpr (NWD == 4) {
+      const uint4 v = *reinterpret_cast<const uint4*>(k0);
+      h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
+    } else {
+      const uint2 v = *reinterpret_cast<const uint2*>(k0);
+      h[0] = v.x; h[1] = v.y;
+    }
+#pragma unroll
+    for (int w = 0; w < NWD; ++w) {
+      const uint32_t t = h[w] >> 8;
+      P[4 * w + 0] = h[w] & 0x000F000Fu;
+      P[4 * w + 1] = h[w] & 0x00F000F0u;
+      P[4 * w + 2] = t & 0x000F000Fu;
+      P[4 * w + 3] = t & 0x00F000F0u;
+    }
+  } else if constexpr (MODE == KVQ_MODE_INT2) {
+    // code n of word w (bits 2n) is channel 16w + n; pairs (n, n + 8)
+    constexpr int NWD = D / 64;
+    uint32_t h[NWD];
+    if constexpr (NWD == 2) {
+      const uint2 v = *reinterpret_cast<const uint2*>(k0);
+      h[0] = v.x; h[1] = v.y;
+    } else {
+      h[0] = *reinterpret_cast<const uint32_t*>(k0);
+    }
+#pragma unroll
+    for (int w = 0; w < NWD; ++w) {
+      const uint32_t t = h[w] >> 8;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        P[8 * w + n] = h[w] & (0x00030003u << (2 * n));
+        P[8 * w + 4 + n] = t & (0x00030003u << (2 * n));
+      }
     }
   } else {
-    key_pairs<MODE, D>(k0, plane_stride, P);
+    if constexpr (D == 128) {
+      // bit n is channel n; pairs (n, n + 16)
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(k0);
+      const uint32_t t = w >> 8;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        P[n] = w & (0x00010001u << n);
+        P[8 + n] = t & (0x00010001u << n);
+      }
+    } else {
+      // channels 0-7 at bits 0-7, 8-15 at bits 16-23; pairs (n, n + 8)
+      const uint32_t h = *reinterpret_cast<const uint16_t*>(k0);
+      const uint32_t w = (h & 0xFFu) | ((h & 0xFF00u) << 8);
+      const uint32_t t = w >> 4;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        P[n] = w & (0x00010001u << n);
+        P[4 + n] = t & (0x00010001u << n);
+      }
+    }
   }
 }
 
 // A fragments of P.V for one channel m-tile (rows ca = 16mt+g and cb = ca+8) of
-// one 32-token slab, as offset-encoded f16 values 1024 + vx_mult(i) * code.
+// one 32-token slab, as subnormal f16 values code * 2^vs_log2fac(i) * 2^-24.
 // a[s] serves k-step s: a[s][0..1] are pair 2s of rows ca/cb (k = 2q, 2q+1),
 // a[s][2..3] pair 2s+1 (k = 2q+8, 2q+9).  `va`/`vb` point at rows ca/cb of
-// plane 0.  The caller removes the 1024 through the accumulator's start value.
+// plane 0.
 template <int MODE>
-__device__ __forceinline__ void value_frags_x(const uint8_t* va, const uint8_t* vb, int plane_stride, int q,
+__device__ __forceinline__ void value_frags_s(const uint8_t* va, const uint8_t* vb, int plane_stride, int q,
                                               uint32_t (&a)[2][4]) {
   uint32_t pa[4], pb[4];
   if constexpr (MODE == KVQ_MODE_INT8) {
@@ -249,37 +301,37 @@ __device__ __forceinline__ void value_frags_x(const uint8_t* va, const uint8_t* 
     const uint32_t Eb = ((hb << 4) & 0xF0F0F0F0u) | (lb & 0x0F0F0F0Fu);
     const uint32_t Ob = (hb & 0xF0F0F0F0u) | ((lb >> 4) & 0x0F0F0F0Fu);
     // E byte k = token 2k, O byte k = token 2k + 1 (pairs per xpair_a / xpair_b)
-    pa[0] = __byte_perm(Ea, X64B, 0x4140); pa[1] = __byte_perm(Oa, X64B, 0x4140);
-    pa[2] = __byte_perm(Ea, X64B, 0x4342); pa[3] = __byte_perm(Oa, X64B, 0x4342);
-    pb[0] = __byte_perm(Eb, X64B, 0x4140); pb[1] = __byte_perm(Ob, X64B, 0x4140);
-    pb[2] = __byte_perm(Eb, X64B, 0x4342); pb[3] = __byte_perm(Ob, X64B, 0x4342);
+    pa[0] = __byte_perm(Ea, 0u, 0x4140); pa[1] = __byte_perm(Oa, 0u, 0x4140);
+    pa[2] = __byte_perm(Ea, 0u, 0x4342); pa[3] = __byte_perm(Oa, 0u, 0x4342);
+    pb[0] = __byte_perm(Eb, 0u, 0x4140); pb[1] = __byte_perm(Ob, 0u, 0x4140);
+    pb[2] = __byte_perm(Eb, 0u, 0x4342); pb[3] = __byte_perm(Ob, 0u, 0x4342);
   } else if constexpr (MODE == KVQ_MODE_INT4) {
-    // nibble i of the word is token 8q + i; every pair lands at mantissa bits 4-7
+    // nibble i of the word is token 8q + i
     const uint32_t wa = *reinterpret_cast<const uint32_t*>(va + 4 * q);
     const uint32_t wb = *reinterpret_cast<const uint32_t*>(vb + 4 * q);
-    pa[0] = xsel(wa << 4, 0x00F000F0u); pa[1] = xsel(wa, 0x00F000F0u);
-    pa[2] = xsel(wa >> 4, 0x00F000F0u); pa[3] = xsel(wa >> 8, 0x00F000F0u);
-    pb[0] = xsel(wb << 4, 0x00F000F0u); pb[1] = xsel(wb, 0x00F000F0u);
-    pb[2] = xsel(wb >> 4, 0x00F000F0u); pb[3] = xsel(wb >> 8, 0x00F000F0u);
+    const uint32_t ta = wa >> 8, tb = wb >> 8;
+    pa[0] = wa & 0x000F000Fu; pa[1] = wa & 0x00F000F0u; pa[2] = ta & 0x000F000Fu; pa[3] = ta & 0x00F000F0u;
+    pb[0] = wb & 0x000F000Fu; pb[1] = wb & 0x00F000F0u; pb[2] = tb & 0x000F000Fu; pb[3] = tb & 0x00F000F0u;
   } else if constexpr (MODE == KVQ_MODE_INT2) {
     const uint32_t xa = *reinterpret_cast<const uint16_t*>(va + 2 * q);
     const uint32_t xb = *reinterpret_cast<const uint16_t*>(vb + 2 * q);
     const uint32_t y = __byte_perm(xa, xb, 0x5140);   // [a.b0, b.b0, a.b1, b.b1]
     // token j of row a sits at bits 2j and 16+2j, of row b 8 bits higher
-    const uint32_t ya = y << 4, yb = y >> 4, yc = y >> 8;
-    pa[0] = xsel(ya, 0x00300030u); pa[1] = xsel(ya, 0x00C000C0u);
-    pa[2] = xsel(y, 0x00300030u); pa[3] = xsel(y, 0x00C000C0u);
-    pb[0] = xsel(yb, 0x00300030u); pb[1] = xsel(yb, 0x00C000C0u);
-    pb[2] = xsel(yc, 0x00300030u); pb[3] = xsel(yc, 0x00C000C0u);
+    const uint32_t yb = y >> 8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      pa[j] = y & (0x00030003u << (2 * j));
+      pb[j] = yb & (0x00030003u << (2 * j));
+    }
   } else {
     const uint32_t x = static_cast<uint32_t>(va[q]) | (static_cast<uint32_t>(vb[q]) << 8);
     const uint32_t y = (x & 0x0F0Fu) | ((x & 0xF0F0u) << 12);
-    // token j of row a at bits j and 16+j, of row b 8 bits higher: move to bits 6-9
-    const uint32_t ya = y << 6, yb = y >> 2;
+    // token j of row a at bits j and 16+j, of row b 8 bits higher
+    const uint32_t yb = y >> 8;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      pa[j] = xsel(ya, 0x00010001u << (6 + j));
-      pb[j] = xsel(yb, 0x00010001u << (6 + j));
+      pa[j] = y & (0x00010001u << j);
+      pb[j] = yb & (0x00010001u << j);
     }
   }
   a[0][0] = pa[0]; a[0][1] = pb[0]; a[0][2] = pa[1]; a[0][3] = pb[1];
