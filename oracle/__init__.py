@@ -7,6 +7,7 @@ computes and which passage of the pages it follows.
 """
 from .kvq_oracle import (  # noqa: F401
     FORMAT_BITS,
+    MID_NIBBLE,
     MODES,
     SLAB,
     OracleCache,
@@ -14,6 +15,7 @@ from .kvq_oracle import (  # noqa: F401
     attend,
     gather_selected,
     mode_codes_scale,
+    mode_zero,
     pack_k_plane,
     pack_v_plane,
     quantize_key_group,

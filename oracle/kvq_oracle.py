@@ -13,7 +13,8 @@ the pages state it, step by step:
   KIVI"; QuantSpec page, Experimental setup: builds on KIVI.)
 * Hierarchical INT8 code.  The upper nibble is the INT4 draft code; upper plus
   lower nibble rebuild the INT8 target code.  No separate draft copy is stored.
-  (QuantSpec page, Approach.)
+  (QuantSpec page, Approach.)  A second INT4 reading puts the draft code at the
+  middle of the 8-bit codes it stands for (lower nibble read as 8).
 * Double full-precision buffer of 2G tokens.  It keeps recent tokens in bf16.
   When full, the oldest G tokens are quantized.  (QuantSpec page, Approach.)
 * Attention.  Softmax attention, in fp64, over the dequantized cache plus the
@@ -42,9 +43,14 @@ FORMAT_BITS = {"hier8": 8, "int2": 2, "int1": 1}
 MODES = {
     "int8": ("hier8", 8, 1),
     "int4": ("hier8", 4, 16),
+    "int4mid": ("hier8", 4, 16),
     "int2": ("int2", 2, 1),
     "int1": ("int1", 1, 1),
 }
+# The midpoint reading of the INT4 draft code: the upper nibble hi stands for
+# the 8-bit codes 16 hi .. 16 hi + 15, and "int4mid" reconstructs it at the
+# middle of that range, 16 hi + MID_NIBBLE, instead of at its bottom.
+MID_NIBBLE = 8
 SLAB = 32  # tokens per value-plane slab (storage layout, see pack_v_plane)
 
 
@@ -111,13 +117,25 @@ def mode_codes_scale(mode: str, codes: np.ndarray, scale: np.ndarray):
 
     INT8 reads the full hierarchical code with its scale.  INT4 reads only the
     upper nibble, with 16 x scale.  So INT4 dequant equals INT8 dequant with the
-    lower nibble zeroed (QuantSpec page, Approach).  INT2/INT1 read their own
-    codes and scale.
+    lower nibble zeroed (QuantSpec page, Approach).  INT4-mid reads the same
+    nibble and scale (its zero point moves, see mode_zero).  INT2/INT1 read
+    their own codes and scale.
     """
     _, _, mult = MODES[mode]
-    if mode == "int4":
+    if mode in ("int4", "int4mid"):
         return (codes >> 4).astype(np.uint8), scale.astype(np.float64) * 16.0
     return codes, scale.astype(np.float64) * mult
+
+
+def mode_zero(mode: str, zero: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """The zero point a read mode sees, in fp64.  INT4-mid adds MID_NIBBLE
+    steps of the 8-bit scale, so that its dequant equals INT8 dequant with the
+    lower nibble set to MID_NIBBLE: (16 hi + 8) s + z = hi (16 s) + (z + 8 s).
+    Every other mode reads the stored zero point."""
+    z = zero.astype(np.float64)
+    if mode == "int4mid":
+        return z + MID_NIBBLE * scale.astype(np.float64)
+    return z
 
 
 # ================================================================================
@@ -268,8 +286,8 @@ class OracleCache:
         L, G, D = self.Lq, self.G, self.D
         kc, ks = mode_codes_scale(mode, self.k_codes[b, h, :L], self.k_scale[b, h, :L // G])
         vc, vs = mode_codes_scale(mode, self.v_codes[b, h, :L], self.v_scale[b, h, :L])
-        kz = self.k_zero[b, h, :L // G].astype(np.float64)
-        vz = self.v_zero[b, h, :L].astype(np.float64)
+        kz = mode_zero(mode, self.k_zero[b, h, :L // G], self.k_scale[b, h, :L // G])
+        vz = mode_zero(mode, self.v_zero[b, h, :L], self.v_scale[b, h, :L])
         khat = kc.astype(np.float64) * np.repeat(ks, G, axis=0) + np.repeat(kz, G, axis=0)
         vhat = (vc.astype(np.float64).reshape(L, D // G, G) * vs[:, :, None] + vz[:, :, None]).reshape(L, D)
         return khat, vhat
@@ -407,6 +425,23 @@ def score_group(qs: np.ndarray, scale_eff: np.ndarray, zero: np.ndarray,
     return ((Sf * unit).astype(F32) + beta).astype(F32)
 
 
+def score_group_inputs(cache: "OracleCache", mode: str, b: int, h: int, g: int):
+    """(codes, effective scale, zero point) of key group g of (b, kv head h) as
+    the top-k score reads them, all fp32: INT4 and INT4-mid read the upper
+    nibble with fp32(16 s); INT4-mid's zero point is fp32(z + fp32(8 s)), one
+    rounding (8 s is exact)."""
+    G = cache.G
+    codes = cache.k_codes[b, h, g * G:(g + 1) * G]
+    s = cache.k_scale[b, h, g].astype(F32)
+    z = cache.k_zero[b, h, g].astype(F32)
+    if mode == "int4mid":
+        z = (z + (F32(MID_NIBBLE) * s).astype(F32)).astype(F32)
+    if mode in ("int4", "int4mid"):
+        codes = codes >> 4
+        s = (s * F32(16)).astype(F32)
+    return codes, s, z
+
+
 def summed_query(q_spec_b: np.ndarray, h: int, hg: int) -> np.ndarray:
     """fp32 sum, ascending head order, of the speculative token's query heads
     that share KV head h.  Under MHA (hg = 1) it is that head's query.  The
@@ -440,12 +475,8 @@ def topk(cache: OracleCache, mode: str, q_spec: np.ndarray, k: int,
         qs = summed_query(q_spec[b], h, hg)
         sc = np.empty(L, F32)
         for g in range(L // G):
-            codes = cache.k_codes[b, h, g * G:(g + 1) * G]
-            s = cache.k_scale[b, h, g].astype(F32)
-            if mode == "int4":
-                codes = codes >> 4
-                s = (s * F32(16)).astype(F32)
-            sc[g * G:(g + 1) * G] = score_group(qs, s, cache.k_zero[b, h, g], codes)
+            codes, s, z = score_group_inputs(cache, mode, b, h, g)
+            sc[g * G:(g + 1) * G] = score_group(qs, s, z, codes)
         order = sorted(range(L), key=lambda t: (-float(sc[t]), t))[:k]
         idx[b, h, :len(order)] = order
         score[b, h, :len(order)] = sc[order]
@@ -460,12 +491,8 @@ def all_scores(cache: OracleCache, mode: str, q_spec: np.ndarray, b: int, h: int
     G = cache.G
     out = np.empty(cache.Lq, F32)
     for g in range(cache.Lq // G):
-        codes = cache.k_codes[b, h, g * G:(g + 1) * G]
-        s = cache.k_scale[b, h, g].astype(F32)
-        if mode == "int4":
-            codes = codes >> 4
-            s = (s * F32(16)).astype(F32)
-        out[g * G:(g + 1) * G] = score_group(qs, s, cache.k_zero[b, h, g], codes)
+        codes, s, z = score_group_inputs(cache, mode, b, h, g)
+        out[g * G:(g + 1) * G] = score_group(qs, s, z, codes)
     return out
 
 

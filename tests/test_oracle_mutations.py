@@ -25,6 +25,9 @@ MUTATIONS = [
     ("top-k zero-point sum accumulated in fp64",
      "        beta = F32(beta + F32(F32(qs[d]) * F32(zero[d])))",
      "        beta = np.float64(beta) + np.float64(qs[d]) * np.float64(zero[d])"),
+    ("INT4 midpoint at 7 instead of 8", "MID_NIBBLE = 8", "MID_NIBBLE = 7"),
+    ("INT4 midpoint zero point left unmoved in the top-k score",
+     "        z = (z + (F32(MID_NIBBLE) * s).astype(F32)).astype(F32)", "        z = z"),
     ("causal offset off by one", "nvis = (P - gamma + i + 1) if P else 0", "nvis = (P - gamma + i) if P else 0"),
     ("strided instead of consecutive GQA grouping", "hq = h * hg + hh", "hq = hh * H + h"),
     ("flush one token early", "if self.r == 2 * self.G:", "if self.r == 2 * self.G - 1:"),

@@ -228,7 +228,65 @@ def _sdpa_reference(q, keys, vals, mask, scale):
     return o[0, 0, 0].numpy()
 
 
-@pytest.mark.parametrize("mode,fmt,G", [("int8", "hier8", 32), ("int4", "hier8", 32),
+def test_int4mid_is_int8_with_lower_nibble_eight():
+    """The midpoint reading of the draft code: INT4-mid dequant equals INT8
+    dequant recomputed here with the lower nibble replaced by 8, i.e. the
+    middle of the sixteen 8-bit codes one upper nibble stands for.  Catches a
+    wrong midpoint, a midpoint in units of the 16x scale, and a zero point
+    that does not move."""
+    K, V = ki.kv_stream(5, 1, 2, 260, 64)
+    c = _cache_from_tokens("hier8", 32, K, V)
+    for h in range(2):
+        km, vm = c.dequant_unit("int4mid", 0, h)
+        L, G = c.Lq, c.G
+        kc = ((c.k_codes[0, h, :L] & 0xF0) | 8).astype(np.float64)
+        ks = np.repeat(c.k_scale[0, h, :L // G].astype(np.float64), G, axis=0)
+        kz = np.repeat(c.k_zero[0, h, :L // G].astype(np.float64), G, axis=0)
+        ref_k = kc * ks + kz
+        np.testing.assert_allclose(km, ref_k, rtol=0, atol=1e-14 * np.abs(ref_k).max())
+        vc = ((c.v_codes[0, h, :L] & 0xF0) | 8).astype(np.float64)
+        vs = np.repeat(c.v_scale[0, h, :L].astype(np.float64), G, axis=1)
+        vz = np.repeat(c.v_zero[0, h, :L].astype(np.float64), G, axis=1)
+        ref_v = vc * vs + vz
+        np.testing.assert_allclose(vm, ref_v, rtol=0, atol=1e-14 * np.abs(ref_v).max())
+
+
+def test_int4mid_error_bound_halves_int4():
+    """Reconstruction error against the original bf16 values: the INT8 code is
+    within half a step of x, and the lower nibble read as 8 is within 8 steps
+    of the true lower nibble, so INT4-mid is within 8.5 steps of x, where the
+    truncating INT4 reading can be 15.5 steps off (and is more than 8.5 steps
+    off somewhere on these inputs)."""
+    G, D = 32, 64
+    K, V = ki.kv_stream(9, 1, 1, 8 * G + 5, D)
+    c = _cache_from_tokens("hier8", G, K, V)
+    L = c.Lq
+    ks = np.repeat(c.k_scale[0, 0, :L // G].astype(np.float64), G, axis=0)
+    km, _ = c.dequant_unit("int4mid", 0, 0)
+    k4, _ = c.dequant_unit("int4", 0, 0)
+    err_mid = np.abs(km - K[0, 0, :L])
+    err_4 = np.abs(k4 - K[0, 0, :L])
+    assert np.all(err_mid <= 8.5 * ks * (1 + 2.0 ** -10) + 1e-30)
+    assert np.all(err_4 <= 15.5 * ks * (1 + 2.0 ** -10) + 1e-30)
+    assert np.any(err_4 > 8.5 * ks * (1 + 2.0 ** -10))
+    assert err_mid.mean() < err_4.mean()
+
+
+def test_int4mid_topk_zero_point_moves_by_eight_steps():
+    """The top-k score of INT4-mid reads zero point fp32(z + 8 s) with the
+    8-bit scale s: equal to the INT4 score of a cache whose zero points were
+    moved by hand."""
+    G, D, N = 32, 64, 5 * 32 + 7
+    K, V = ki.kv_stream(13, 1, 1, N, D)
+    c = _cache_from_tokens("hier8", G, K, V)
+    q = ki.queries(13, 1, 1, 1, D)[:, 0]
+    mid = oracle.all_scores(c, "int4mid", q, 0, 0)
+    c.k_zero[0, 0, :c.Lq // G] = (c.k_zero[0, 0, :c.Lq // G] + F32(8) * c.k_scale[0, 0, :c.Lq // G]).astype(F32)
+    moved = oracle.all_scores(c, "int4", q, 0, 0)
+    np.testing.assert_array_equal(mid.view(np.uint32), moved.view(np.uint32))
+
+
+@pytest.mark.parametrize("mode,fmt,G", [("int8", "hier8", 32), ("int4", "hier8", 32), ("int4mid", "hier8", 64),
                                         ("int2", "int2", 32), ("int1", "int1", 64)])
 def test_attention_equals_library_sdpa(mode, fmt, G):
     """The oracle equals torch's fp64 SDPA on the same key/value lists, for GQA
@@ -365,7 +423,7 @@ def test_topk_score_golden(grp):
     assert zero_rows.size and np.all(got[zero_rows] == F32(grp["beta"]))
 
 
-@pytest.mark.parametrize("mode,fmt", [("int4", "hier8"), ("int2", "int2"), ("int1", "int1")])
+@pytest.mark.parametrize("mode,fmt", [("int4", "hier8"), ("int4mid", "hier8"), ("int2", "int2"), ("int1", "int1")])
 def test_topk_score_fidelity(mode, fmt):
     """The canonical score stays within its stated error of the exact logit
     qs . k_hat, with qs the sum of the group's query heads.  The error budget
@@ -383,7 +441,7 @@ def test_topk_score_fidelity(mode, fmt):
         kc, ks = oracle.mode_codes_scale(mode, c.k_codes[0, h, :c.Lq], c.k_scale[0, h])
         for g in range(c.Lq // G):
             w = np.abs(qs * ks[g])
-            zterm = np.abs(qs * c.k_zero[0, h, g]).sum()
+            zterm = np.abs(qs * oracle.mode_zero(mode, c.k_zero[0, h, g], c.k_scale[0, h, g])).sum()
             cw = (kc[g * G:(g + 1) * G].astype(np.float64) * w[None, :]).sum(1)
             bound = 2.0 ** -21 * w.max() * kc[g * G:(g + 1) * G].sum(1) + 2.0 ** -20 * (cw + zterm) \
                 + 2.0 ** -23 * np.abs(ex[g * G:(g + 1) * G])
