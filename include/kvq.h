@@ -38,7 +38,9 @@
  *   - Element types.  bf16 for keys, values and queries (raw 16-bit patterns),
  *     fp32 for scales, zero points, scores and log-sum-exp, int32 for indices.
  *   - Shapes.  head_dim D in {64, 128}.  Group size G in {32, 64, 128} with G
- *     dividing D.  Every sequence of a batch has the same lengths.
+ *     dividing D.  Every sequence of a batch has the same lengths, unless the
+ *     cache is ragged (kvq_cache_set_ragged): then each sequence keeps its own
+ *     quantized length and residual fill.
  */
 #ifndef KVQ_H_
 #define KVQ_H_
@@ -72,13 +74,20 @@ typedef enum kvq_format {
 
 /* Read mode of attention / top-k.  INT8 and INT4 read KVQ_FMT_HIER8: INT8 both
  * nibble planes, INT4 only the upper plane, with scale x16.  So INT4 dequant
- * equals INT8 dequant with the lower nibble zeroed.  INT2 and INT1 read their
- * own format.  Any other pairing returns KVQ_ERR_UNSUPPORTED. */
+ * equals INT8 dequant with the lower nibble zeroed (QuantSpec page, "Approach":
+ * the upper 4 bits are the INT4 draft cache).  INT4_MID reads the same upper
+ * plane but puts each draft code at the middle of the sixteen 8-bit codes it
+ * stands for: its dequant equals INT8 dequant with the lower nibble set to 8,
+ * i.e. zero point z + 8 s with the 8-bit scale s (the pages do not say where
+ * the draft value lies; this halves the worst-case draft error, 8.5 steps of
+ * s against 15.5).  INT2 and INT1 read their own format.  Any other pairing
+ * returns KVQ_ERR_UNSUPPORTED. */
 typedef enum kvq_mode {
   KVQ_MODE_INT8 = 0,
   KVQ_MODE_INT4 = 1,
   KVQ_MODE_INT2 = 2,
-  KVQ_MODE_INT1 = 3
+  KVQ_MODE_INT1 = 3,
+  KVQ_MODE_INT4_MID = 4
 } kvq_mode;
 
 typedef struct kvq_cache_desc {
@@ -114,14 +123,22 @@ typedef struct kvq_cache_desc {
  *                half is quantized in place, and the other half becomes the
  *                oldest.
  *  flush counters [u] u32: arrival counters of the quantize-append kernel
- *                (zeroed by the first append into the empty cache, zero again
- *                after every append).
+ *                (zeroed on the stream before the cache's first flush, zero
+ *                again after every append).
  *
  * Codes (KIVI-style asymmetric min/max, fp32, round-half-even): scale =
  * (max - min)/(2^b - 1), code = clamp(rint((x - min) * (1/scale)), 0, 2^b - 1),
  * with zero point = min.  A constant group gets scale 0 and codes 0.  Keys are
  * grouped per channel over G tokens, values per token over G channels.
  */
+/* Per-sequence state of a ragged cache (see kvq_cache_set_ragged): the same
+ * three counters as the uniform ones in kvq_cache, for one sequence. */
+typedef struct kvq_seq_state {
+  int64_t quantized_len;      /* Lq of this sequence (multiple of G)              */
+  int32_t residual_len;       /* r of this sequence, 0 <= r < 2G                   */
+  int32_t residual_start;     /* 0 or G                                            */
+} kvq_seq_state;
+
 typedef struct kvq_cache {
   kvq_cache_desc desc;
   void* base;                 /* caller's device memory                            */
@@ -136,7 +153,10 @@ typedef struct kvq_cache {
   int32_t residual_len;       /* r: live residual tokens, 0 <= r < 2G              */
   int32_t residual_start;     /* 0 or G                                            */
   uint32_t magic;             /* set by kvq_cache_init                             */
-  uint32_t reserved1;
+  uint32_t flags;             /* library-owned: bit 0 set once the flush counters
+                                 have been zeroed on the device                    */
+  kvq_seq_state* seqs;        /* NULL: uniform lengths; else [batch] per-sequence state
+                                 (caller-owned host memory, see kvq_cache_set_ragged) */
 } kvq_cache;
 
 /* Human-readable name of a status code (static string, never NULL).  The pages
@@ -158,6 +178,26 @@ kvq_status kvq_cache_init(kvq_cache* cache, const kvq_cache_desc* desc, void* de
                           size_t bytes);
 
 /*
+ * Make an empty cache ragged: every sequence of the batch keeps its own
+ * quantized length, residual fill and residual start, in `seqs`, an array of
+ * `count` == batch entries of caller-owned host memory that must outlive the
+ * cache's use (SpeCache page, "Key results": batched decoding, 36 sequences at
+ * 32K, where real sequences have unequal lengths).  The entries are set to
+ * empty.  From then on kvq_quantize_append_ragged appends a different number
+ * of tokens to each sequence, kvq_quantize_append appends the same number to
+ * all, and kvq_attend, kvq_attend_plan and kvq_topk read each sequence's own
+ * lengths: query row i of sequence b sees its quantized tokens [0, Lq_b), its
+ * r_b residual tokens and the pending tokens, exactly as a batch of one.  The
+ * cache-level quantized_len and residual_len then hold the largest of the
+ * sequences' values (for sizing); residual_start is unused.
+ * Errors: KVQ_ERR_NOT_INITIALIZED; KVQ_ERR_INVALID_ARG for a null array,
+ * count != batch, or a cache that is not empty; KVQ_ERR_UNSUPPORTED for a
+ * batch above 64 (the per-sequence lengths travel in the kernels' parameter
+ * block).  Writes host memory only.
+ */
+kvq_status kvq_cache_set_ragged(kvq_cache* cache, kvq_seq_state* seqs, int32_t count);
+
+/*
  * Append n_new tokens of every sequence.  k_new and v_new are bf16
  * [B][Hkv][n_new][D], contiguous, on the device.
  *
@@ -176,6 +216,23 @@ kvq_status kvq_cache_init(kvq_cache* cache, const kvq_cache_desc* desc, void* de
  */
 kvq_status kvq_quantize_append(kvq_cache* cache, const void* k_new, const void* v_new,
                                int32_t n_new, kvq_stream_t stream);
+
+/*
+ * Append to each sequence of a ragged cache its own number of tokens:
+ * sequence b appends n_new[b] (0 <= n_new[b] <= n_max) tokens, the first
+ * n_new[b] rows of k_new / v_new, bf16 [B][Hkv][n_max][D] (rows past n_new[b]
+ * are not read).  n_new is host memory.  Each sequence runs the double-buffer
+ * state machine of kvq_quantize_append on its own state (QuantSpec page,
+ * "Approach": the 2G full-precision buffer), so sequence b ends with the same
+ * bytes as a batch-of-one cache that appended the same tokens.  Capacity is
+ * checked for every sequence before anything is enqueued (KVQ_ERR_CAPACITY,
+ * nothing changed); KVQ_ERR_INVALID_ARG for a cache that is not ragged, a null
+ * n_new, or a count outside [0, n_max].  Enqueues at most two kernels (one
+ * flush launch for the sequences that flush, one residual copy for those that
+ * do not) and updates the per-sequence host state at once.
+ */
+kvq_status kvq_quantize_append_ragged(kvq_cache* cache, const void* k_new, const void* v_new,
+                                      int32_t n_max, const int32_t* n_new, kvq_stream_t stream);
 
 /* Bytes of workspace that kvq_attend / kvq_topk need for this cache, at any fill
  * up to capacity, on the current device (the split count grows with its SM
@@ -250,7 +307,8 @@ kvq_status kvq_attend_plan(const kvq_cache* cache, kvq_mode mode, int32_t num_q_
  * low-bit keys for the speculative token's query (SpeCache page, "Approach").
  * The query heads sharing a KV head are summed in fp32, in ascending head order.
  * Per key group g the score is exact up to stated roundings:
- *   w_d = fp32(qs_d * s_d)   (s = the mode's key scale: x16 for INT4)
+ *   w_d = fp32(qs_d * s_d)   (s = the mode's key scale: x16 for INT4 and INT4_MID;
+ *                            INT4_MID's zero point is fp32(zero_d + 8 s_d))
  *   e   = exponent with max_d|w_d| < 2^e, floored at -100
  *   W_d = rint(w_d * 2^(21-e)),  S_t = sum_d W_d * code_{t,d} (exact integer)
  *   beta = ((0 + fp32(qs_0 zero_0)) + fp32(qs_1 zero_1)) + ... , fp32 adds in
@@ -258,7 +316,7 @@ kvq_status kvq_attend_plan(const kvq_cache* cache, kvq_mode mode, int32_t num_q_
  *   score_t = fp32(fp32(fp32(S_t) * 2^(e-21)) + beta)
  * Tokens are ordered by (score descending, index ascending).  Positions beyond
  * Lq get index -1 and score -inf.
- *  mode     KVQ_MODE_INT4, INT2 or INT1 (INT8 returns KVQ_ERR_UNSUPPORTED).
+ *  mode     KVQ_MODE_INT4, INT4_MID, INT2 or INT1 (INT8 returns KVQ_ERR_UNSUPPORTED).
  *  q_spec   bf16 [B][Hq][D].
  *  idx_out  int32 [B][Hkv][top_k], in that order.  score_out fp32, same shape,
  *           or NULL.

@@ -24,8 +24,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
 
 FORMATS = {"hier8": 8, "int2": 2, "int1": 1}
-MODES = {"int8": 0, "int4": 1, "int2": 2, "int1": 3}
-MODE_FORMAT = {"int8": "hier8", "int4": "hier8", "int2": "int2", "int1": "int1"}
+MODES = {"int8": 0, "int4": 1, "int2": 2, "int1": 3, "int4mid": 4}
+MODE_FORMAT = {"int8": "hier8", "int4": "hier8", "int2": "int2", "int1": "int1", "int4mid": "hier8"}
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_CAPACITY",
           4: "KVQ_ERR_WORKSPACE", 5: "KVQ_ERR_CUDA", 6: "KVQ_ERR_DEVICE_TIMEOUT",
           7: "KVQ_ERR_NOT_INITIALIZED"}
@@ -35,6 +35,7 @@ EXPORTED = (
     "kvq_status_string", "kvq_cache_bytes", "kvq_cache_init", "kvq_quantize_append",
     "kvq_workspace_bytes", "kvq_attend", "kvq_topk", "kvq_workspace_status",
     "kvq_selftest_bounded_wait", "kvq_attend_static_scratch", "kvq_attend_plan", "kvq_gather_selected",
+    "kvq_cache_set_ragged", "kvq_quantize_append_ragged",
 )
 
 
@@ -45,6 +46,11 @@ class KvqCacheDesc(ctypes.Structure):
                 ("capacity_tokens", ctypes.c_int64)]
 
 
+class KvqSeqState(ctypes.Structure):
+    _fields_ = [("quantized_len", ctypes.c_int64), ("residual_len", ctypes.c_int32),
+                ("residual_start", ctypes.c_int32)]
+
+
 class KvqCache(ctypes.Structure):
     _fields_ = [("desc", KvqCacheDesc), ("base", ctypes.c_void_p), ("bytes", ctypes.c_uint64),
                 ("off_k_plane", ctypes.c_uint64 * 2), ("off_v_plane", ctypes.c_uint64 * 2),
@@ -52,7 +58,7 @@ class KvqCache(ctypes.Structure):
                 ("off_res_k", ctypes.c_uint64), ("off_res_v", ctypes.c_uint64),
                 ("quantized_len", ctypes.c_int64), ("residual_len", ctypes.c_int32),
                 ("residual_start", ctypes.c_int32), ("magic", ctypes.c_uint32),
-                ("reserved1", ctypes.c_uint32)]
+                ("flags", ctypes.c_uint32), ("seqs", ctypes.POINTER(KvqSeqState))]
 
 
 class KvqAttendPlanInfo(ctypes.Structure):
@@ -88,6 +94,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kvq_cache_init.restype = ctypes.c_int
     lib.kvq_quantize_append.argtypes = [cache_p, vp, vp, i32, vp]
     lib.kvq_quantize_append.restype = ctypes.c_int
+    lib.kvq_cache_set_ragged.argtypes = [cache_p, ctypes.POINTER(KvqSeqState), i32]
+    lib.kvq_cache_set_ragged.restype = ctypes.c_int
+    lib.kvq_quantize_append_ragged.argtypes = [cache_p, vp, vp, i32, ctypes.POINTER(ctypes.c_int32), vp]
+    lib.kvq_quantize_append_ragged.restype = ctypes.c_int
     lib.kvq_workspace_bytes.argtypes = [cache_p, i32, i32, i32]
     lib.kvq_workspace_bytes.restype = sz
     lib.kvq_attend.argtypes = [cache_p, ctypes.c_int, vp, i32, i32, vp, vp, i32, vp, vp, vp, i32, f32,
@@ -138,7 +148,7 @@ class QuantizedKVCache:
     """One layer's quantized KV cache in a caller-owned (torch) device buffer."""
 
     def __init__(self, batch: int, num_kv_heads: int, head_dim: int, group_size: int, fmt: str,
-                 capacity_tokens: int, device="cuda"):
+                 capacity_tokens: int, device="cuda", ragged: bool = False):
         lib = load_library()
         self.desc = KvqCacheDesc(batch, num_kv_heads, head_dim, group_size, FORMATS[fmt], 0,
                                  capacity_tokens)
@@ -151,6 +161,12 @@ class QuantizedKVCache:
         _check(lib.kvq_cache_init(ctypes.byref(self.struct), ctypes.byref(self.desc),
                                   self.storage.data_ptr() + self._pad, self.nbytes), "kvq_cache_init")
         self.fmt = fmt
+        self.seq_states = None
+        if ragged:
+            # per-sequence state: host memory the cache struct points at, kept alive here
+            self.seq_states = (KvqSeqState * batch)()
+            _check(lib.kvq_cache_set_ragged(ctypes.byref(self.struct), self.seq_states, batch),
+                   "kvq_cache_set_ragged")
 
     # host-side state
     @property
@@ -166,11 +182,23 @@ class QuantizedKVCache:
         return int(self.struct.residual_start)
 
     def state(self):
-        return (self.quantized_len, self.residual_len, self.residual_start)
+        st = (self.quantized_len, self.residual_len, self.residual_start)
+        if self.seq_states is not None:
+            st = st + (tuple(self.seq_state(b) for b in range(self.desc.batch)),)
+        return st
 
     def set_state(self, st):
         """Restore host counters saved by ``state()`` (device data is not touched)."""
-        self.struct.quantized_len, self.struct.residual_len, self.struct.residual_start = st
+        self.struct.quantized_len, self.struct.residual_len, self.struct.residual_start = st[:3]
+        if self.seq_states is not None:
+            for b, (lq, r, start) in enumerate(st[3]):
+                self.seq_states[b].quantized_len, self.seq_states[b].residual_len = lq, r
+                self.seq_states[b].residual_start = start
+
+    def seq_state(self, b: int):
+        """(Lq, r, residual_start) of sequence b of a ragged cache."""
+        x = self.seq_states[b]
+        return (int(x.quantized_len), int(x.residual_len), int(x.residual_start))
 
     # raw region views (uint8 / float32 / bf16), for inspection and tests
     def _region(self, off: int, nbytes: int) -> torch.Tensor:
@@ -222,6 +250,21 @@ def kvq_quantize_append(cache: QuantizedKVCache, k_new: torch.Tensor, v_new: tor
     _check(lib.kvq_quantize_append(ctypes.byref(cache.struct), _ptr(k_new, torch.bfloat16, "k_new"),
                                    _ptr(v_new, torch.bfloat16, "v_new"), k_new.shape[2], _stream(stream)),
            "kvq_quantize_append")
+
+
+def kvq_quantize_append_ragged(cache: QuantizedKVCache, k_new: torch.Tensor, v_new: torch.Tensor, n_new,
+                               stream=None):
+    """Append ``n_new[b]`` tokens to sequence b of a ragged cache: the first
+    ``n_new[b]`` rows of ``k_new, v_new [B, Hkv, n_max, D]`` (bf16)."""
+    d = cache.desc
+    if k_new.dim() != 4 or k_new.shape != v_new.shape or k_new.shape[0] != d.batch or \
+            k_new.shape[1] != d.num_kv_heads or k_new.shape[3] != d.head_dim:
+        raise ValueError("k_new/v_new must be [B, Hkv, n_max, D]")
+    counts = (ctypes.c_int32 * d.batch)(*[int(x) for x in n_new])
+    _check(load_library().kvq_quantize_append_ragged(ctypes.byref(cache.struct), _ptr(k_new, torch.bfloat16, "k_new"),
+                                                     _ptr(v_new, torch.bfloat16, "v_new"), k_new.shape[2], counts,
+                                                     _stream(stream)),
+           "kvq_quantize_append_ragged")
 
 
 def kvq_workspace_bytes(cache: QuantizedKVCache, num_q_heads: int, gamma: int, top_k: int = 0) -> int:

@@ -12,6 +12,11 @@ using namespace kvq;
 namespace {
 
 constexpr uint32_t kMagic = 0x4B565131u;  // "KVQ1"
+constexpr uint32_t kFlagCountersZeroed = 1u;   // kvq_cache.flags: flush counters zeroed on the device
+
+// The flush kernel's arrival counters start at zero: zeroed on the stream
+// before the cache's first flush, whatever was appended before it.
+kvq_status zero_counters_once(kvq_cache* cache, unsigned* ctr, cudaStream_t s);
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -156,13 +161,40 @@ CacheView view_of(const kvq_cache* c) {
   v.Lq = c->quantized_len;
   v.r = c->residual_len;
   v.res_start = c->residual_start;
+  v.ragged = c->seqs != nullptr;
+  if (v.ragged) {
+    for (int b = 0; b < c->desc.batch; ++b) {
+      v.rag_lq[b] = static_cast<int32_t>(c->seqs[b].quantized_len);
+      v.rag_r[b] = static_cast<int16_t>(c->seqs[b].residual_len);
+      v.rag_start[b] = static_cast<int16_t>(c->seqs[b].residual_start);
+    }
+  }
   return v;
+}
+
+// One sequence's part of an append of n tokens to state (lq, r, start), as
+// the 2G double buffer runs it token by token: f groups flush, and the new
+// tokens from stream position first_new on stay in the residual buffer.
+SeqAppend plan_seq_append(long long lq, int r, int start, int n, int G) {
+  SeqAppend a{};
+  const long long T = static_cast<long long>(r) + n;
+  const long long f = (T < 2LL * G) ? 0 : T / G - 1;
+  const long long first_new = std::max<long long>(r, f * G);
+  a.lq = static_cast<int32_t>(lq);
+  a.r = static_cast<int16_t>(r);
+  a.start = static_cast<int16_t>(start);
+  a.n = n;
+  a.nflush = static_cast<int32_t>(f);
+  a.first_new = static_cast<int32_t>(first_new);
+  a.res_count = static_cast<int32_t>(T - first_new);
+  return a;
 }
 
 bool mode_reads(int mode, int fmt) {
   switch (mode) {
     case KVQ_MODE_INT8:
-    case KVQ_MODE_INT4: return fmt == KVQ_FMT_HIER8;
+    case KVQ_MODE_INT4:
+    case KVQ_MODE_INT4_MID: return fmt == KVQ_FMT_HIER8;
     case KVQ_MODE_INT2: return fmt == KVQ_FMT_INT2;
     case KVQ_MODE_INT1: return fmt == KVQ_FMT_INT1;
     default: return false;
@@ -180,7 +212,7 @@ struct AttendPlan {
 AttendPlan plan_attend(const kvq_cache* cache, int mode, int R, int n_pend, int top_k) {
   AttendPlan pl{};
   const long long U = units_of(cache);
-  const long long slots = attend_resident_ctas(mode, cache->desc.head_dim, cache->desc.group_size, R);
+  const long long slots = attend_resident_ctas(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size, R);
   const long long max_chunk = max_chunk_for_rows(R);
   // The bf16 tail (residual, pending and selected tokens) goes to CTAs of its
   // own when they fit in the first wave beside the quantized splits without
@@ -204,10 +236,18 @@ AttendPlan plan_attend(const kvq_cache* cache, int mode, int R, int n_pend, int 
   // the cluster limit and the clusters fill no more waves than the plan counted.
   const int S_all = pl.S_q + pl.S_t;
   if (S_all >= 1 && S_all <= kMaxClusterCtas && slots > 0 && clusters_enabled()) {
-    const long long cap = attend_resident_clusters(mode, cache->desc.head_dim, cache->desc.group_size, R, S_all);
+    const long long cap =
+        attend_resident_clusters(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size, R, S_all);
     if (cap > 0 && ceil_div(U, cap) <= ceil_div(U * S_all, slots)) pl.cluster = 1;
   }
   return pl;
+}
+
+kvq_status zero_counters_once(kvq_cache* cache, unsigned* ctr, cudaStream_t s) {
+  if (cache->flags & kFlagCountersZeroed) return KVQ_OK;
+  if (cudaMemsetAsync(ctr, 0, static_cast<size_t>(units_of(cache)) * 4, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  cache->flags |= kFlagCountersZeroed;
+  return KVQ_OK;
 }
 
 }  // namespace
@@ -278,12 +318,114 @@ kvq_status kvq_cache_init(kvq_cache* cache, const kvq_cache_desc* desc, void* de
   return KVQ_OK;
 }
 
+kvq_status kvq_cache_set_ragged(kvq_cache* cache, kvq_seq_state* seqs, int32_t count) {
+  if (!cache || cache->magic != kMagic) return KVQ_ERR_NOT_INITIALIZED;
+  if (!valid_desc(&cache->desc) || !seqs || count != cache->desc.batch) return KVQ_ERR_INVALID_ARG;
+  if (cache->quantized_len != 0 || cache->residual_len != 0) return KVQ_ERR_INVALID_ARG;
+  if (count > kMaxRaggedBatch) return KVQ_ERR_UNSUPPORTED;
+  for (int b = 0; b < count; ++b) seqs[b] = kvq_seq_state{0, 0, 0};
+  cache->seqs = seqs;
+  return KVQ_OK;
+}
+
+kvq_status kvq_quantize_append_ragged(kvq_cache* cache, const void* k_new, const void* v_new, int32_t n_max,
+                                      const int32_t* n_new, kvq_stream_t stream) {
+  if (!cache || cache->magic != kMagic) return KVQ_ERR_NOT_INITIALIZED;
+  if (!valid_desc(&cache->desc) || !cache->seqs || !n_new || n_max < 0) return KVQ_ERR_INVALID_ARG;
+  const int B = cache->desc.batch, G = cache->desc.group_size;
+  int nflush_max = 0, count_max = 0, total = 0;
+  SeqAppend plan[kMaxRaggedBatch];
+  for (int b = 0; b < B; ++b) {
+    if (n_new[b] < 0 || n_new[b] > n_max) return KVQ_ERR_INVALID_ARG;
+    const kvq_seq_state& st = cache->seqs[b];
+    plan[b] = plan_seq_append(st.quantized_len, st.residual_len, st.residual_start, n_new[b], G);
+    if (plan[b].lq + static_cast<long long>(plan[b].nflush) * G > cache->desc.capacity_tokens)
+      return KVQ_ERR_CAPACITY;
+    nflush_max = std::max(nflush_max, plan[b].nflush);
+    if (plan[b].nflush == 0) count_max = std::max(count_max, plan[b].res_count);
+    total += n_new[b];
+  }
+  if (total == 0) return KVQ_OK;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(cache->base);
+  if (nflush_max > 0) {
+    FlushParams p{};
+    p.kplane[0] = base + cache->off_k_plane[0];
+    p.kplane[1] = base + cache->off_k_plane[1];
+    p.vplane[0] = base + cache->off_v_plane[0];
+    p.vplane[1] = base + cache->off_v_plane[1];
+    p.ksz = reinterpret_cast<float*>(base + cache->off_k_sz);
+    p.vsz = reinterpret_cast<float*>(base + cache->off_v_sz);
+    p.res_k = reinterpret_cast<const uint16_t*>(base + cache->off_res_k);
+    p.res_v = reinterpret_cast<const uint16_t*>(base + cache->off_res_v);
+    p.k_new = static_cast<const uint16_t*>(k_new);
+    p.v_new = static_cast<const uint16_t*>(v_new);
+    p.B = B;
+    p.Hkv = cache->desc.num_kv_heads;
+    p.D = cache->desc.head_dim;
+    p.G = G;
+    p.fmt = cache->desc.format;
+    p.C = cache->desc.capacity_tokens;
+    p.n = n_max;
+    p.nflush = nflush_max;
+    p.res_k_w = reinterpret_cast<uint16_t*>(base + cache->off_res_k);
+    p.res_v_w = reinterpret_cast<uint16_t*>(base + cache->off_res_v);
+    p.ctr = reinterpret_cast<unsigned*>(base + cache->off_res_v + regions(&cache->desc).res);
+    p.ragged = 1;
+    for (int b = 0; b < B; ++b) {
+      p.seq[b] = plan[b];
+      if (plan[b].nflush == 0) p.seq[b].res_count = 0;   // written by the residual copy below
+    }
+    if (zero_counters_once(cache, p.ctr, s) != KVQ_OK) return KVQ_ERR_CUDA;
+    if (launch_flush(p, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  }
+  if (count_max > 0) {
+    ResidualWriteParams w{};
+    w.res_k = reinterpret_cast<uint16_t*>(base + cache->off_res_k);
+    w.res_v = reinterpret_cast<uint16_t*>(base + cache->off_res_v);
+    w.k_new = static_cast<const uint16_t*>(k_new);
+    w.v_new = static_cast<const uint16_t*>(v_new);
+    w.B = B;
+    w.Hkv = cache->desc.num_kv_heads;
+    w.D = cache->desc.head_dim;
+    w.G = G;
+    w.n = n_max;
+    w.count = count_max;
+    w.ragged = 1;
+    for (int b = 0; b < B; ++b) {
+      w.seq[b] = plan[b];
+      if (plan[b].nflush > 0) w.seq[b].res_count = 0;    // written by the flush launch above
+    }
+    if (launch_residual_write(w, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  }
+  long long lq_max = 0;
+  int r_max = 0;
+  for (int b = 0; b < B; ++b) {
+    kvq_seq_state& st = cache->seqs[b];
+    const long long T = static_cast<long long>(st.residual_len) + n_new[b];
+    st.quantized_len += static_cast<long long>(plan[b].nflush) * G;
+    st.residual_len = static_cast<int32_t>(T - static_cast<long long>(plan[b].nflush) * G);
+    st.residual_start = static_cast<int32_t>((st.residual_start + static_cast<long long>(plan[b].nflush) * G) % (2 * G));
+    lq_max = std::max(lq_max, static_cast<long long>(st.quantized_len));
+    r_max = std::max(r_max, st.residual_len);
+  }
+  cache->quantized_len = lq_max;
+  cache->residual_len = r_max;
+  return KVQ_OK;
+}
+
 kvq_status kvq_quantize_append(kvq_cache* cache, const void* k_new, const void* v_new, int32_t n_new,
                                kvq_stream_t stream) {
   if (!cache || cache->magic != kMagic) return KVQ_ERR_NOT_INITIALIZED;
   if (!valid_desc(&cache->desc)) return KVQ_ERR_INVALID_ARG;
   if (n_new < 0) return KVQ_ERR_INVALID_ARG;
   if (n_new == 0) return KVQ_OK;
+  if (cache->seqs) {   // a ragged cache: the same count for every sequence
+    int32_t counts[kMaxRaggedBatch];
+    for (int b = 0; b < cache->desc.batch; ++b) counts[b] = n_new;
+    return kvq_quantize_append_ragged(cache, k_new, v_new, n_new, counts, stream);
+  }
   if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
   const int G = cache->desc.group_size;
   const long long r = cache->residual_len;
@@ -321,10 +463,8 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const void* k_new, const void* 
     p.first_new = static_cast<int>(first_new);
     p.res_count = static_cast<int>(T - first_new);
     p.ctr = reinterpret_cast<unsigned*>(base + cache->off_res_v + regions(&cache->desc).res);
-    // the arrival counters are zero after every flush; set them on the first append
-    if (cache->quantized_len == 0 && r == 0 &&
-        cudaMemsetAsync(p.ctr, 0, static_cast<size_t>(units_of(cache)) * 4, s) != cudaSuccess)
-      return KVQ_ERR_CUDA;
+    // the arrival counters are zero after every flush; zero them before the first
+    if (zero_counters_once(cache, p.ctr, s) != KVQ_OK) return KVQ_ERR_CUDA;
     if (launch_flush(p, s) != cudaSuccess) return KVQ_ERR_CUDA;
   }
   const long long first_new = std::max(r, f * G);
@@ -420,6 +560,7 @@ kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int3
   p.sel_v = static_cast<const uint16_t*>(sel_v);
   p.top_k = top_k;
   p.qscale = sm_scale * 1.4426950408889634f;
+  p.zshift = mode_zero_shift(mode);
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -434,7 +575,7 @@ kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int3
   p.cluster = pl.cluster;
   p.wait_limit = kDefaultWaitLimit;
   if (p.S_q > attend_splits_max(&cache->desc)) return KVQ_ERR_WORKSPACE;
-  if (launch_attend(p, mode, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (launch_attend(p, kernel_mode(mode), static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
 
@@ -473,7 +614,8 @@ kvq_status kvq_topk(const kvq_cache* cache, kvq_mode mode, const void* q_spec, i
   if (!workspace || !aligned16(workspace) || ws_bytes < need) return KVQ_ERR_WORKSPACE;
   const long long U = units_of(cache);
   long long chunk = 0;
-  const int S = topk_plan(mode, cache->desc.head_dim, cache->desc.group_size, cache->quantized_len, U, top_k, &chunk);
+  const int S = topk_plan(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size, cache->quantized_len, U,
+                          top_k, &chunk);
   if (static_cast<long long>(S) * top_k > kTopkMaxCand) return KVQ_ERR_UNSUPPORTED;
   TopkParams p{};
   p.c = view_of(cache);
@@ -481,6 +623,8 @@ kvq_status kvq_topk(const kvq_cache* cache, kvq_mode mode, const void* q_spec, i
   p.Hq = num_q_heads;
   p.HG = num_q_heads / Hkv;
   p.k = top_k;
+  p.zshift = mode_zero_shift(mode);
+  p.align = topk_align(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size);
   p.idx_out = idx_out;
   p.score_out = score_out;
   uint8_t* ws = static_cast<uint8_t*>(workspace) + kStatusBytes + att;
@@ -493,7 +637,7 @@ kvq_status kvq_topk(const kvq_cache* cache, kvq_mode mode, const void* q_spec, i
   p.chunk = chunk;
   p.wait_limit = kDefaultWaitLimit;
   if (static_cast<size_t>(S) > Smax) return KVQ_ERR_WORKSPACE;
-  if (launch_topk(p, mode, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (launch_topk(p, kernel_mode(mode), static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
 

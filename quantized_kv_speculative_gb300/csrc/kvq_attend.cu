@@ -422,14 +422,16 @@ __device__ void ticket_and_combine(const AttendParams& p, long long u, int* sh_f
 template <int D>
 __device__ __forceinline__ int tail_row(const AttendParams& p, long long u, int t, const uint16_t*& kp,
                                         const uint16_t*& vp) {
-  if (t < p.c.r) {
-    const int slot = (p.c.res_start + t) % (2 * p.c.G);
+  const int b = static_cast<int>(u / p.c.Hkv);
+  const int r = seq_r(p.c, b);
+  if (t < r) {
+    const int slot = (seq_start(p.c, b) + t) % (2 * p.c.G);
     const long long off = (u * 2 * p.c.G + slot) * D;
     kp = p.c.res_k + off;
     vp = p.c.res_v + off;
     return -1;
   }
-  t -= p.c.r;
+  t -= r;
   if (t < p.P) {
     const long long off = (u * p.P + t) * D;
     kp = p.pend_k + off;
@@ -438,7 +440,7 @@ __device__ __forceinline__ int tail_row(const AttendParams& p, long long u, int 
   }
   t -= p.P;
   const int idx = p.sel_idx[u * p.top_k + t];
-  if (idx >= 0 && idx < p.c.Lq) {
+  if (idx >= 0 && idx < seq_lq(p.c, b)) {
     const long long off = (u * p.top_k + t) * D;
     kp = p.sel_k + off;
     vp = p.sel_v + off;
@@ -714,7 +716,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
   if (role.tail) {  // ---------------- tail CTAs ----
     const long long u = role.u;
     const int ts = role.r;
-    const int ntl = p.c.r + p.P + p.top_k, per = (ntl + p.S_t - 1) / p.S_t;
+    const int ntl = seq_r(p.c, static_cast<int>(u / p.c.Hkv)) + p.P + p.top_k, per = (ntl + p.S_t - 1) / p.S_t;
     const int t_lo = min(ntl, ts * per), t_hi = min(ntl, t_lo + per);
     float* wm = reinterpret_cast<float*>(smem + L::WM_OFF);
     float* wl = reinterpret_cast<float*>(smem + L::WL_OFF);
@@ -732,8 +734,12 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
   const long long u = role.u;
   const int split = role.r;
   const int b = static_cast<int>(u / p.c.Hkv), kvh = static_cast<int>(u % p.c.Hkv);
-  const long long t_begin = static_cast<long long>(split) * p.chunk;
-  const long long t_end = min(p.c.Lq, t_begin + p.chunk);
+  // a ragged cache splits each sequence's own length over the S_q splits
+  const long long lq_b = seq_lq(p.c, b);
+  const long long chunk =
+      p.c.ragged ? (((lq_b + p.S_q - 1) / p.S_q + kChunkAlign - 1) / kChunkAlign) * kChunkAlign : p.chunk;
+  const long long t_begin = static_cast<long long>(split) * chunk;
+  const long long t_end = min(lq_b, t_begin + chunk);
   const int ntok_chunk = static_cast<int>(max(0LL, t_end - t_begin));
   const int ntiles = (ntok_chunk + M::TT - 1) / M::TT;
   const int per_warp = (ntiles + NW - 1) / NW;
@@ -912,6 +918,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
           for (int w2 = 1; w2 < NW; ++w2) qmax = fmaxf(qmax, qmw[w2]);
           constexpr int PPR = D / 2;           // channel pairs per row
           constexpr float KW = MULT;
+          const float zsh = p.zshift;   // zero points read as z + zsh * s (the INT4 midpoint reading)
           float zsum = 0.f;
           float kscale_new, Z2;
           if constexpr (NT == 2) {
@@ -956,7 +963,12 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
               for (int k = 0; k < HP; ++k) {
                 const int c0 = kx_chan<MODE, D>(k, 0), c1 = kx_chan<MODE, D>(k, 1);
                 const float q0 = qr[c0], q1 = qr[c1];
-                zs = fmaf(q0, kzc[c0], fmaf(q1, kzc[c1], zs));
+                float z0 = kzc[c0], z1 = kzc[c1];
+                if (zsh != 0.f) {
+                  z0 = fmaf(zsh, ksc[c0], z0);
+                  z1 = fmaf(zsh, ksc[c1], z1);
+                }
+                zs = fmaf(q0, z0, fmaf(q1, z1, zs));
                 const float w0 = q0 * kv[k][0], w1 = q1 * kv[k][1];
                 const uint32_t hi = pack_half2(w0, w1);
                 const float2 hf = unpack_half2(hi);
@@ -1005,7 +1017,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
               const uint32_t lo = pack_half2(w0 - hf.x, w1 - hf.y);
               wb[((ntw * 8 + col) * 4 + qq) * (D / 8) + pp] = hi;
               wb[((ntw * 8 + col + 1) * 4 + qq) * (D / 8) + pp] = lo;
-              zsum = fmaf(q0, kz[c0], fmaf(q1, kz[c1], zsum));
+              zsum = fmaf(q0, fmaf(zsh, ks[c0], kz[c0]), fmaf(q1, fmaf(zsh, ks[c1], kz[c1]), zsum));
             }
           }
           kscale = kscale_new;
@@ -1104,8 +1116,8 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
           const float* vb = vsz + (32 * sl + tokB[s]) * 2 * NJ;
 #pragma unroll
           for (int jv = 0; jv < NJ; ++jv) {
-            sA[s][jv] = va[jv] * MULT; zA[s][jv] = va[NJ + jv];
-            sB[s][jv] = vb[jv] * MULT; zB[s][jv] = vb[NJ + jv];
+            sA[s][jv] = va[jv] * MULT; zA[s][jv] = fmaf(p.zshift, va[jv], va[NJ + jv]);
+            sB[s][jv] = vb[jv] * MULT; zB[s][jv] = fmaf(p.zshift, vb[jv], vb[NJ + jv]);
             smx = fmaxf(smx, fmaxf(sA[s][jv], sB[s][jv]));
           }
         }
@@ -1270,7 +1282,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT>())) at
     const int split = role2.r;
     const float* wm = reinterpret_cast<const float*>(smem + L::WM_OFF);
     if (p.S_t == 0) {
-      const int ntl = p.c.r + p.P + p.top_k, per = (ntl + p.S_q - 1) / p.S_q;
+      const int ntl = seq_r(p.c, static_cast<int>(u / p.c.Hkv)) + p.P + p.top_k, per = (ntl + p.S_q - 1) / p.S_q;
       const int t_lo = min(ntl, split * per), t_hi = min(ntl, t_lo + per);
       tail_entries<D>(p, u, t_lo, t_hi, reinterpret_cast<float*>(smem + L::WM_OFF),
                       reinterpret_cast<float*>(smem + L::WL_OFF), reinterpret_cast<float*>(smem + L::WC_OFF),

@@ -26,6 +26,7 @@ constexpr int kTailTokensPerSplit = 320;  // bf16 tail tokens per tail CTA (usua
 constexpr int kMaxClusterCtas = 16;   // CTAs per (b, kvh) that may combine as one thread-block cluster
 constexpr int kStatusBytes = 256;      // workspace header (status word)
 constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s at 2 GHz
+constexpr int kMaxRaggedBatch = 64;    // sequences of a ragged cache (their lengths ride in the kernel parameters)
 __host__ __device__ constexpr int kPartialFloats(int D) { return 2 * kMaxRows + kMaxRows * D; }
 
 // Device view of one cache (all pointers already offset to the regions).
@@ -38,8 +39,29 @@ struct CacheView {
   const uint16_t* res_v;
   int B, Hkv, D, G, fmt;
   long long C;        // capacity tokens
-  long long Lq;
+  long long Lq;       // ragged: the largest sequence's
   int r, res_start;
+  // Ragged cache: each sequence's own quantized length, residual fill and
+  // residual start (read through seq_lq / seq_r / seq_start below).
+  int ragged;
+  int32_t rag_lq[kMaxRaggedBatch];
+  int16_t rag_r[kMaxRaggedBatch];
+  int16_t rag_start[kMaxRaggedBatch];
+};
+
+__host__ __device__ inline long long seq_lq(const CacheView& c, int b) { return c.ragged ? c.rag_lq[b] : c.Lq; }
+__host__ __device__ inline int seq_r(const CacheView& c, int b) { return c.ragged ? c.rag_r[b] : c.r; }
+__host__ __device__ inline int seq_start(const CacheView& c, int b) { return c.ragged ? c.rag_start[b] : c.res_start; }
+
+// One sequence's part of an append: its state before the call, the groups it
+// flushes, and the new tokens that land in its residual buffer.
+struct SeqAppend {
+  int32_t lq;               // quantized tokens before this call
+  int16_t r, start;         // residual fill and start before this call
+  int32_t n;                // tokens this sequence appends (<= the launch's row stride n)
+  int32_t nflush;           // groups quantized by this call
+  int32_t first_new;        // first stream position (>= r) kept in the residual
+  int32_t res_count;        // new tokens written into the residual buffer
 };
 
 struct AttendParams {
@@ -54,6 +76,7 @@ struct AttendParams {
   const uint16_t* sel_v;
   int top_k;
   float qscale;             // sm_scale * log2(e)
+  float zshift;             // zero points read as z + zshift * s (8: the INT4 midpoint reading)
   uint16_t* out;            // [B][gamma][Hq][D]
   float* lse;               // [B][gamma][Hq] or null
   int* status;
@@ -70,6 +93,7 @@ struct TopkParams {
   CacheView c;
   const uint16_t* q;        // [B][Hq][D]
   int Hq, HG, k;
+  float zshift;             // key zero points read as fp32(z + zshift * s)
   int32_t* idx_out;         // [B][Hkv][k]
   float* score_out;         // [B][Hkv][k] or null
   int* status;
@@ -78,6 +102,7 @@ struct TopkParams {
   int32_t* cand_idx;
   int S;
   long long chunk;
+  long long align;          // chunk alignment of the plan (per-sequence chunks of a ragged cache)
   long long wait_limit;
 };
 
@@ -94,7 +119,7 @@ struct FlushParams {
   int B, Hkv, D, G, fmt;
   long long C, Lq;          // Lq before this call
   int r, res_start, n;      // residual state before this call, tokens in this call
-  int nflush;               // groups quantized by this launch
+  int nflush;               // groups quantized by this launch (ragged: the most any sequence flushes)
   // New tokens written into the residual buffer by the same launch: the CTA
   // that arrives last at the head's counter (after every CTA of the head has
   // read its old slots) writes them and resets the counter.
@@ -102,6 +127,8 @@ struct FlushParams {
   uint16_t* res_v_w;
   int first_new, res_count;
   unsigned* ctr;            // [B * Hkv] arrival counters, zero between launches
+  int ragged;               // 1: per-sequence parts in seq[] (the scalars above are unused)
+  SeqAppend seq[kMaxRaggedBatch];
 };
 
 // The CTAs of one flushed group: key parts over 32-channel ranges, then value
@@ -133,8 +160,15 @@ struct ResidualWriteParams {
   int B, Hkv, D, G, n;
   int r, res_start;         // before this call
   int first_new;            // first stream position (>= r) kept in the residual
-  int count;                // tokens to write
+  int count;                // tokens to write (ragged: the most any sequence writes)
+  int ragged;               // 1: per-sequence r, start, first_new and count (res_count) in seq[]
+  SeqAppend seq[kMaxRaggedBatch];
 };
+
+// The kernel variant a read mode runs (the INT4 midpoint reading runs the INT4
+// kernels with a zero shift) and that shift.
+inline int kernel_mode(int mode) { return mode == KVQ_MODE_INT4_MID ? KVQ_MODE_INT4 : mode; }
+inline float mode_zero_shift(int mode) { return mode == KVQ_MODE_INT4_MID ? 8.0f : 0.0f; }
 
 cudaError_t launch_flush(const FlushParams& p, cudaStream_t s);
 cudaError_t launch_residual_write(const ResidualWriteParams& p, cudaStream_t s);
@@ -149,6 +183,8 @@ cudaError_t launch_topk(const TopkParams& p, int mode, cudaStream_t s);
 // Top-k split plan for the current device: returns the split count S per
 // (b, kv head) and sets *chunk (tokens per split).
 int topk_plan(int mode, int D, int G, long long Lq, long long U, int k, long long* chunk);
+// The chunk alignment topk_plan uses for a variant (whole key groups per warp).
+long long topk_align(int mode, int D, int G);
 cudaError_t launch_wait_selftest(int* status, long long limit, cudaStream_t s);
 // SMs of the current device (cached per device; 0 if unknown).
 int device_sm_count();

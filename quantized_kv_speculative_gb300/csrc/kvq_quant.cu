@@ -33,20 +33,37 @@ __device__ __forceinline__ void scale_inv(float mn, float mx, float levels, floa
   inv = (scale == 0.0f) ? 0.0f : __fdiv_rn(1.0f, scale);
 }
 
+// This CTA's sequence's part of the append: the launch's scalars, or its row
+// of the per-sequence table for a ragged cache.
+__device__ __forceinline__ SeqAppend seq_append(const FlushParams& p, int b) {
+  if (p.ragged) return p.seq[b];
+  SeqAppend a;
+  a.lq = static_cast<int32_t>(p.Lq);
+  a.r = static_cast<int16_t>(p.r);
+  a.start = static_cast<int16_t>(p.res_start);
+  a.n = p.n;
+  a.nflush = p.nflush;
+  a.first_new = p.first_new;
+  a.res_count = p.res_count;
+  return a;
+}
+
 // bf16 row of stream position pos: pos < r comes from the residual buffer (slot
-// (res_start + pos) mod 2G), otherwise from the new tokens (index pos - r).
-__device__ __forceinline__ const uint16_t* stream_row(const FlushParams& p, long long u, int pos, bool value) {
-  if (pos < p.r) {
-    const int slot = (p.res_start + pos) % (2 * p.G);
+// (res_start + pos) mod 2G), otherwise from the new tokens (index pos - r; the
+// new tokens' rows are p.n apart per head).
+__device__ __forceinline__ const uint16_t* stream_row(const FlushParams& p, const SeqAppend& sa, long long u, int pos,
+                                                      bool value) {
+  if (pos < sa.r) {
+    const int slot = (sa.start + pos) % (2 * p.G);
     return (value ? p.res_v : p.res_k) + (u * 2 * p.G + slot) * p.D;
   }
-  return (value ? p.v_new : p.k_new) + (u * p.n + (pos - p.r)) * p.D;
+  return (value ? p.v_new : p.k_new) + (u * p.n + (pos - sa.r)) * p.D;
 }
 
 // After this CTA has read its old residual slots: arrive at the head's counter;
 // the last CTA of the head writes the new residual tokens and resets it.
-__device__ void residual_ticket(const FlushParams& p, long long u, int ncta, int* sh_flag) {
-  if (p.res_count <= 0) return;
+__device__ void residual_ticket(const FlushParams& p, const SeqAppend& sa, long long u, int ncta, int* sh_flag) {
+  if (sa.res_count <= 0) return;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -59,13 +76,13 @@ __device__ void residual_ticket(const FlushParams& p, long long u, int ncta, int
   if (!*sh_flag) return;
   __threadfence();
   const int vec = p.D / 8;
-  const int nv = p.res_count * vec;
+  const int nv = sa.res_count * vec;
   for (int e = threadIdx.x; e < 2 * nv; e += kFlushThreads) {
     const int kv = e >= nv, e2 = kv ? e - nv : e;
     const int j = e2 / vec, c = e2 % vec;
-    const int pos = p.first_new + j;
-    const int slot = (p.res_start + pos) % (2 * p.G);
-    const long long src = (u * p.n + (pos - p.r)) * p.D;
+    const int pos = sa.first_new + j;
+    const int slot = (sa.start + pos) % (2 * p.G);
+    const long long src = (u * p.n + (pos - sa.r)) * p.D;
     const long long dst = (u * 2 * p.G + slot) * p.D;
     const uint16_t* from = kv ? p.v_new : p.k_new;
     uint16_t* to = kv ? p.res_v_w : p.res_k_w;
@@ -90,10 +107,12 @@ __global__ void __launch_bounds__(kFlushThreads) flush_kernel(FlushParams p) {
   const int kvh = blockIdx.y, b = blockIdx.z;
   const long long u = static_cast<long long>(b) * p.Hkv + kvh;
   const int tid = threadIdx.x;
+  const SeqAppend sa = seq_append(p, b);
+  if (gi >= sa.nflush) return;               // a ragged sequence that flushes fewer groups
   constexpr int BITS = FMT;  // 8, 2 or 1
   const float levels = static_cast<float>((1 << BITS) - 1);
-  const long long grp = p.Lq / G + gi;       // global group index
-  const long long tok0 = p.Lq + static_cast<long long>(gi) * G;
+  const long long grp = sa.lq / G + gi;      // global group index
+  const long long tok0 = static_cast<long long>(sa.lq) + static_cast<long long>(gi) * G;
   const float pinf = __int_as_float(0x7f800000);
 
   if (part < sp.npk) {
@@ -110,7 +129,7 @@ __global__ void __launch_bounds__(kFlushThreads) flush_kernel(FlushParams p) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int e = tid + h * kFlushThreads;
-        if (e < G * 4) v[h] = reinterpret_cast<const uint4*>(stream_row(p, u, gi * G + e / 4, false) + c0)[e % 4];
+        if (e < G * 4) v[h] = reinterpret_cast<const uint4*>(stream_row(p, sa, u, gi * G + e / 4, false) + c0)[e % 4];
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -118,7 +137,7 @@ __global__ void __launch_bounds__(kFlushThreads) flush_kernel(FlushParams p) {
         if (e < G * 4) reinterpret_cast<uint4*>(Ks)[e] = v[h];
       }
     }
-    residual_ticket(p, u, p.nflush * npart, &sh_flag);
+    residual_ticket(p, sa, u, sa.nflush * npart, &sh_flag);
     __syncthreads();
     {
       const int cp = tid % (kKeyPart / 2), st = tid / (kKeyPart / 2);
@@ -213,7 +232,7 @@ __global__ void __launch_bounds__(kFlushThreads) flush_kernel(FlushParams p) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int e = tid + h * kFlushThreads;
-      if (e < TV * vpt) v[h] = reinterpret_cast<const uint4*>(stream_row(p, u, gi * G + t0v + e / vpt, true) + c0v)[e % vpt];
+      if (e < TV * vpt) v[h] = reinterpret_cast<const uint4*>(stream_row(p, sa, u, gi * G + t0v + e / vpt, true) + c0v)[e % vpt];
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -221,7 +240,7 @@ __global__ void __launch_bounds__(kFlushThreads) flush_kernel(FlushParams p) {
       if (e < TV * vpt) reinterpret_cast<uint4*>(Vs)[e] = v[h];
     }
   }
-  residual_ticket(p, u, p.nflush * npart, &sh_flag);
+  residual_ticket(p, sa, u, sa.nflush * npart, &sh_flag);
   __syncthreads();
   // ---- statistics: per token over the block; `per` adjacent lanes per token ----
   {
@@ -301,9 +320,14 @@ __global__ void __launch_bounds__(kFlushThreads) flush_kernel(FlushParams p) {
 __global__ void residual_write_kernel(ResidualWriteParams p) {
   const int j = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const long long u = static_cast<long long>(b) * p.Hkv + kvh;
-  const int pos = p.first_new + j;                    // stream position
-  const int slot = (p.res_start + pos) % (2 * p.G);
-  const long long src = (u * p.n + (pos - p.r)) * p.D;
+  const int r = p.ragged ? p.seq[b].r : p.r;
+  const int start = p.ragged ? p.seq[b].start : p.res_start;
+  const int first_new = p.ragged ? p.seq[b].first_new : p.first_new;
+  const int count = p.ragged ? p.seq[b].res_count : p.count;
+  if (j >= count) return;                             // a ragged sequence that keeps fewer tokens
+  const int pos = first_new + j;                      // stream position
+  const int slot = (start + pos) % (2 * p.G);
+  const long long src = (u * p.n + (pos - r)) * p.D;
   const long long dst = (u * 2 * p.G + slot) * p.D;
   const int nvec = p.D / 8;
   for (int c = threadIdx.x; c < 2 * nvec; c += blockDim.x) {

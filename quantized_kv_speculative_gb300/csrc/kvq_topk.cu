@@ -345,8 +345,13 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   const int split = blockIdx.x % p.S;
   const int b = static_cast<int>(u / p.c.Hkv), kvh = static_cast<int>(u % p.c.Hkv);
   const int G = p.c.G;
-  const long long t_begin = static_cast<long long>(split) * p.chunk;
-  const long long t_end = min(p.c.Lq, t_begin + p.chunk);
+  // a ragged cache splits each sequence's own length over the S splits, in
+  // multiples of the plan's alignment
+  const long long lq_b = seq_lq(p.c, b);
+  const long long chunk =
+      p.c.ragged ? ((lq_b + p.S - 1) / p.S + p.align - 1) / p.align * p.align : p.chunk;
+  const long long t_begin = static_cast<long long>(split) * chunk;
+  const long long t_end = min(lq_b, t_begin + chunk);
   const int n = static_cast<int>(max(0LL, t_end - t_begin));
   const int ntiles = (n + M::TT - 1) / M::TT;
   const int per_warp = (ntiles + NW - 1) / NW;
@@ -414,11 +419,20 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   {
     const int ngrp = (n + G - 1) / G;
     if (tid < ngrp) {
-      const float4* z4 = reinterpret_cast<const float4*>(p.c.ksz + (u * (p.c.C / G) + t_begin / G + tid) * 2 * D + D);
+      const float4* s4 = reinterpret_cast<const float4*>(p.c.ksz + (u * (p.c.C / G) + t_begin / G + tid) * 2 * D);
+      const float4* z4 = s4 + D / 4;
+      const float zsh = p.zshift;   // INT4 midpoint reading: zero point fp32(z + 8 s)
       float acc = 0.f;
 #pragma unroll 8
       for (int d4 = 0; d4 < D / 4; ++d4) {
-        const float4 z = __ldg(z4 + d4);
+        float4 z = __ldg(z4 + d4);
+        if (zsh != 0.f) {
+          const float4 sc = __ldg(s4 + d4);
+          z.x = fmaf(zsh, sc.x, z.x);
+          z.y = fmaf(zsh, sc.y, z.y);
+          z.z = fmaf(zsh, sc.z, z.z);
+          z.w = fmaf(zsh, sc.w, z.w);
+        }
         acc = __fadd_rn(acc, __fmul_rn(qs[4 * d4 + 0], z.x));
         acc = __fadd_rn(acc, __fmul_rn(qs[4 * d4 + 1], z.y));
         acc = __fadd_rn(acc, __fmul_rn(qs[4 * d4 + 2], z.z));
@@ -741,9 +755,14 @@ long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
 // that the candidate limit and the chunk alignment allow, minimise
 // waves x (chunk + fixed per-CTA cost) + merge cost.  Chunks are multiples of
 // NW x max(G, tile) tokens, so each consumer warp scores whole key groups.
+template <int MODE>
+long long align_t(int G) {
+  return std::max<long long>(kChunkAlign, static_cast<long long>(NW) * std::max(G, Mode<MODE>::TT));
+}
+
 template <int MODE, int D>
 int plan_t(long long Lq, long long U, int G, int k, long long* chunk_out) {
-  const long long align = std::max<long long>(kChunkAlign, static_cast<long long>(NW) * std::max(G, Mode<MODE>::TT));
+  const long long align = align_t<MODE>(G);
   const long long s_lo = std::max(1LL, ceil_div_ll(Lq, kTopkMaxChunk));
   const long long s_hi = std::max(s_lo, std::min(ceil_div_ll(Lq, align), static_cast<long long>(kTopkMaxCand / k)));
   const int sms = device_sm_count();
@@ -789,6 +808,15 @@ int topk_plan(int mode, int D, int G, long long Lq, long long U, int k, long lon
     default:
       *chunk = 0;
       return 0;
+  }
+}
+
+long long topk_align(int mode, int /*D*/, int G) {
+  switch (mode) {
+    case KVQ_MODE_INT4: return align_t<KVQ_MODE_INT4>(G);
+    case KVQ_MODE_INT2: return align_t<KVQ_MODE_INT2>(G);
+    case KVQ_MODE_INT1: return align_t<KVQ_MODE_INT1>(G);
+    default: return kChunkAlign;
   }
 }
 

@@ -53,10 +53,11 @@ def test_struct_layout_matches_c(tmp_path):
 #include <stddef.h>
 #include "kvq.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(kvq_cache_desc), sizeof(kvq_cache),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(kvq_cache_desc), sizeof(kvq_cache),
          offsetof(kvq_cache, base), offsetof(kvq_cache, off_k_plane), offsetof(kvq_cache, quantized_len),
          offsetof(kvq_cache, residual_start), offsetof(kvq_cache, magic), sizeof(kvq_attend_plan_info),
-         offsetof(kvq_attend_plan_info, chunk_tokens), offsetof(kvq_attend_plan_info, cluster));
+         offsetof(kvq_attend_plan_info, chunk_tokens), offsetof(kvq_attend_plan_info, cluster),
+         offsetof(kvq_cache, seqs), sizeof(kvq_seq_state), offsetof(kvq_seq_state, residual_start));
   return 0;
 }
 ''')
@@ -65,9 +66,11 @@ int main(void) {
     vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
     C = kvq.KvqCache
     P = kvq.KvqAttendPlanInfo
+    S = kvq.KvqSeqState
     assert vals == [ctypes.sizeof(kvq.KvqCacheDesc), ctypes.sizeof(C), C.base.offset, C.off_k_plane.offset,
                     C.quantized_len.offset, C.residual_start.offset, C.magic.offset, ctypes.sizeof(P),
-                    P.chunk_tokens.offset, P.cluster.offset]
+                    P.chunk_tokens.offset, P.cluster.offset, C.seqs.offset, ctypes.sizeof(S),
+                    S.residual_start.offset]
 
 
 def _desc(**kw):
@@ -205,3 +208,31 @@ def test_static_scratch_argument_errors_need_no_gpu(lib):
     assert static(c, 0, q=ctypes.c_void_p((1 << 41) + 8)) == 1
     assert static(c, 0, out=None) == 1
     assert static(c, 0, gamma=2, pk=fake, pv=fake, P=1) == 1
+
+
+def test_ragged_state_machine_without_launch(lib):
+    """A ragged cache: set-up refuses a wrong count or a non-empty cache; the
+    per-sequence appends check every sequence's capacity before anything is
+    enqueued and leave all states unchanged on refusal; counts outside
+    [0, n_max] are refused.  Appends of zero tokens change nothing and need
+    no GPU."""
+    c, _ = _host_cache(lib, batch=3, capacity_tokens=128)
+    seqs = (kvq.KvqSeqState * 3)()
+    assert lib.kvq_cache_set_ragged(ctypes.byref(c), seqs, 2) == 1
+    assert lib.kvq_cache_set_ragged(ctypes.byref(kvq.KvqCache()), seqs, 3) == 7
+    assert lib.kvq_cache_set_ragged(ctypes.byref(c), seqs, 3) == 0
+    assert ctypes.cast(c.seqs, ctypes.c_void_p).value == ctypes.cast(seqs, ctypes.c_void_p).value
+    fake = ctypes.c_void_p(1 << 41)
+    counts = (ctypes.c_int32 * 3)(5, 0, (128 // 32 + 2) * 32)      # the last one overflows its capacity
+    assert lib.kvq_quantize_append_ragged(ctypes.byref(c), fake, fake, 192, counts, None) == 3
+    assert [(s.quantized_len, s.residual_len) for s in seqs] == [(0, 0)] * 3
+    counts = (ctypes.c_int32 * 3)(5, 7, 3)
+    assert lib.kvq_quantize_append_ragged(ctypes.byref(c), fake, fake, 6, counts, None) == 1   # 7 > n_max
+    assert lib.kvq_quantize_append_ragged(ctypes.byref(c), fake, fake, 8, None, None) == 1
+    zeros = (ctypes.c_int32 * 3)(0, 0, 0)
+    assert lib.kvq_quantize_append_ragged(ctypes.byref(c), fake, fake, 8, zeros, None) == 0
+    u, _ = _host_cache(lib, batch=3)
+    assert lib.kvq_quantize_append_ragged(ctypes.byref(u), fake, fake, 8, zeros, None) == 1   # not ragged
+    big, _ = _host_cache(lib, batch=65)
+    many = (kvq.KvqSeqState * 65)()
+    assert lib.kvq_cache_set_ragged(ctypes.byref(big), many, 65) == 2

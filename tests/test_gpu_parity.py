@@ -93,6 +93,9 @@ ATTN_CASES = [
     ("int2", 1, 2, 2, 64, 32, 900, 1, 1, 5, False),
     ("int1", 1, 2, 4, 64, 64, 1000, 2, 2, 0, False),
     ("int4", 2, 2, 8, 128, 32, 1700, 2, 2, 0, False),       # hierarchical format with G = 32
+    ("int4mid", 1, 4, 4, 64, 32, 544, 1, 1, 0, False),      # the midpoint reading of the draft code
+    ("int4mid", 1, 3, 3, 128, 128, 4000, 1, 1, 0, True),    # one row, needles
+    ("int4mid", 2, 2, 8, 128, 64, 1700, 2, 2, 7, False),    # eight rows, selected tokens
 ]
 
 
@@ -139,6 +142,7 @@ CLUSTER_CASES = [
     ("int2", 4, 8, 32, 128, 32, 2100, 2, 2, 16, False),     # SpeCache shape, selected tokens
     ("int1", 4, 8, 16, 64, 32, 1000, 2, 2, 0, False),
     ("int8", 2, 2, 8, 128, 128, 1150, 2, 3, 0, False),      # few units, ragged residual
+    ("int4mid", 1, 32, 32, 128, 128, 1500, 1, 1, 0, False),
 ]
 
 
@@ -266,6 +270,8 @@ TOPK_CASES = [
     ("int4", 1, 2, 4, 128, 128, 6000, 128),     # the largest k of the warp-sort selection
     ("int4", 1, 2, 4, 128, 128, 6000, 300),     # k above it: radix selection on small chunks
     ("int2", 1, 1, 4, 128, 32, 30000, 1024),    # the largest k: 4 splits x 1024 candidates to merge
+    ("int4mid", 1, 2, 2, 128, 128, 3000, 64),   # the midpoint reading: zero points moved by 8 steps
+    ("int4mid", 2, 2, 8, 64, 32, 1500, 17),
 ]
 
 
