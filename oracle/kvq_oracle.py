@@ -383,7 +383,17 @@ def attend(cache: OracleCache, mode: str, q: np.ndarray,
 # ================================================================================
 
 W_BITS = 21          # magnitude bits of the integer-rounded folded query weights
+Z_BITS = 40          # magnitude bits of the integer-rounded zero-point products
 E_MIN = -100         # floor on the weight exponent (keeps the unit a normal fp32)
+
+
+Z_EMIN = -80         # floor on the product exponent (keeps 2^(f - 40) a normal fp32)
+
+
+def _exponent(M: float, floor: int = E_MIN) -> int:
+    """e with M < 2^e (frexp's exponent), floored; 0 for M = 0."""
+    e = math.frexp(M)[1] if M > 0 else 0
+    return max(e, floor)
 
 
 def score_group(qs: np.ndarray, scale_eff: np.ndarray, zero: np.ndarray,
@@ -400,29 +410,37 @@ def score_group(qs: np.ndarray, scale_eff: np.ndarray, zero: np.ndarray,
       e     = exponent of max_d |w_d| (max|w| < 2^e), floored at -100
       W_d   = rint(w_d * 2^(21 - e))                         (|W_d| <= 2^21)
       S_t   = sum_d W_d * code_{t,d}                         (exact integer)
-      beta  = ((0 + fp32(qs_0 z_0)) + fp32(qs_1 z_1)) + ... + fp32(qs_{D-1} z_{D-1})
-              (fp32 adds in ascending channel order)
+      p_d   = fp32(qs_d * z_d)                               (zero-point product)
+      f     = exponent of max_d |p_d| (max|p| < 2^f), floored at -80
+      Z     = sum_d rint(p_d * 2^(40 - f))                   (exact integer)
+      beta  = fp32(Z) * 2^(f - 40)
       score = fp32( fp32(fp32(S_t) * 2^(e - 21)) + beta )
 
-    The integer dot product is exact, so summation order cannot change it.
-    The zero-point term beta is the plain left-to-right fp32 sum of the
-    rounded products.  The only other roundings are the weights' 2^-21
-    relative rounding, fp32(S_t), one exact power-of-two scaling and the
-    final add.
+    Both sums are exact integers, so no summation order can change the
+    score: every implementation, serial or parallel, reaches the same bits.
+    The roundings are the weights' 2^-21 and the products' 2^-40 relative
+    rounding to integers, fp32(S_t), fp32(Z), exact power-of-two scalings and
+    the final add.
     """
     D = qs.shape[0]
     w = (qs.astype(F32) * scale_eff.astype(F32)).astype(F32)
-    M = float(np.max(np.abs(w))) if D else 0.0
-    e = math.frexp(M)[1] if M > 0 else 0
-    e = max(e, E_MIN)
+    e = _exponent(float(np.max(np.abs(w)))) if D else 0
     W = np.rint(w.astype(np.float64) * (2.0 ** (W_BITS - e))).astype(np.int64)
     S = codes.astype(np.int64) @ W                       # exact integer dot products
     Sf = S.astype(np.float64).astype(F32)                # |S| < 2^53: one rounding
     unit = F32(2.0 ** (e - W_BITS))
-    beta = F32(0)
-    for d in range(D):
-        beta = F32(beta + F32(F32(qs[d]) * F32(zero[d])))
+    beta = zero_term(qs, zero)
     return ((Sf * unit).astype(F32) + beta).astype(F32)
+
+
+def zero_term(qs: np.ndarray, zero: np.ndarray) -> np.float32:
+    """beta = fp32(sum_d rint(p_d 2^(40-f))) * 2^(f-40), p_d = fp32(qs_d z_d),
+    f the exponent of max|p| (floored at -80).  The sum of integers is exact
+    (|each| <= 2^40, at most a few thousand terms), so its order is free."""
+    p = (qs.astype(F32) * zero.astype(F32)).astype(F32)
+    f = _exponent(float(np.max(np.abs(p))), Z_EMIN) if p.size else 0
+    Z = int(np.sum(np.rint(p.astype(np.float64) * (2.0 ** (Z_BITS - f))).astype(np.int64)))
+    return F32(F32(float(Z)) * F32(2.0 ** (f - Z_BITS)))
 
 
 def score_group_inputs(cache: "OracleCache", mode: str, b: int, h: int, g: int):

@@ -19,12 +19,10 @@ MUTATIONS = [
     ("INT4 scale without the 16x", "scale.astype(np.float64) * 16.0", "scale.astype(np.float64) * 1.0"),
     ("top-k score without the zero-point term",
      "return ((Sf * unit).astype(F32) + beta).astype(F32)", "return (Sf * unit).astype(F32)"),
-    ("top-k zero-point sum in descending channel order",
-     "    for d in range(D):\n        beta = F32(beta + F32(F32(qs[d]) * F32(zero[d])))",
-     "    for d in reversed(range(D)):\n        beta = F32(beta + F32(F32(qs[d]) * F32(zero[d])))"),
-    ("top-k zero-point sum accumulated in fp64",
-     "        beta = F32(beta + F32(F32(qs[d]) * F32(zero[d])))",
-     "        beta = np.float64(beta) + np.float64(qs[d]) * np.float64(zero[d])"),
+    ("top-k zero-point products summed as a running fp32 sum",
+     "    Z = int(np.sum(np.rint(p.astype(np.float64) * (2.0 ** (Z_BITS - f))).astype(np.int64)))",
+     "    Z = float(np.sum(p, dtype=np.float32)) * 2.0 ** (Z_BITS - f)"),
+    ("top-k zero-point products rounded at 2^-20 instead of 2^-40", "Z_BITS = 40", "Z_BITS = 20"),
     ("INT4 midpoint at 7 instead of 8", "MID_NIBBLE = 8", "MID_NIBBLE = 7"),
     ("INT4 midpoint zero point left unmoved in the top-k score",
      "        z = (z + (F32(MID_NIBBLE) * s).astype(F32)).astype(F32)", "        z = z"),

@@ -423,6 +423,41 @@ def test_topk_score_golden(grp):
     assert zero_rows.size and np.all(got[zero_rows] == F32(grp["beta"]))
 
 
+def test_topk_score_does_not_depend_on_channel_order():
+    """Both sums of the score are exact integers, so permuting the channels
+    (the same permutation applied to the query, scales, zero points and code
+    columns) leaves every score bit unchanged.  An fp32 running sum of the
+    zero-point products fails this on these mixed-magnitude inputs."""
+    g = ki.rng(404)
+    D, G = 128, 32
+    for trial in range(20):
+        qs = (g.standard_normal(D) * np.exp2(g.integers(-6, 7, D))).astype(F32)
+        s = np.abs(g.standard_normal(D) * 0.3).astype(F32) + F32(1e-3)
+        z = (g.standard_normal(D) * np.exp2(g.integers(-8, 6, D))).astype(F32)
+        codes = g.integers(0, 4, (G, D)).astype(np.uint8)
+        perm = g.permutation(D)
+        a = oracle.score_group(qs, s, z, codes)
+        b = oracle.score_group(qs[perm], s[perm], z[perm], codes[:, perm])
+        np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_zero_term_is_within_its_rounding_of_the_exact_sum():
+    """beta against the exact sum of the fp32 products (math.fsum): within the
+    2^-41 relative integer rounding of each product (at the largest product's
+    unit) plus one fp32 rounding.  Catches a dropped product, a wrong unit or a
+    wrong sign."""
+    g = ki.rng(405)
+    for trial in range(50):
+        D = int(g.integers(1, 200))
+        qs = (g.standard_normal(D) * np.exp2(g.integers(-4, 5, D))).astype(F32)
+        z = (g.standard_normal(D) * np.exp2(g.integers(-10, 10, D))).astype(F32)
+        p = (qs * z).astype(F32).astype(np.float64)
+        exact = math.fsum(p)
+        beta = float(ko.zero_term(qs, z))
+        f = math.frexp(np.abs(p).max())[1]
+        assert abs(beta - exact) <= D * 2.0 ** (f - 41) + 2.0 ** -24 * abs(exact) + 1e-300
+
+
 @pytest.mark.parametrize("mode,fmt", [("int4", "hier8"), ("int4mid", "hier8"), ("int2", "int2"), ("int1", "int1")])
 def test_topk_score_fidelity(mode, fmt):
     """The canonical score stays within its stated error of the exact logit
