@@ -218,7 +218,7 @@ def kernel_source_hash() -> str:
     """sha256 over the sources the attention kernel is built from."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("kvq_attend.cu", "kvq_modes.cuh", "kvq_device.cuh", "kvq_internal.h"):
+    for f in ("kvq_attend_kernel.cuh", "kvq_modes.cuh", "kvq_device.cuh", "kvq_internal.h"):
         h.update(open(os.path.join(ROOT, "quantized_kv_speculative_gb300", "csrc", f), "rb").read())
     return h.hexdigest()
 
@@ -856,6 +856,17 @@ def run_specache(fmt, seed=0, reps=20):
     sets = [torch.randint(0, lq, (B, H, k), generator=gen, device=dev, dtype=torch.int32) for _ in range(nset)]
     sk2, sv2 = torch.empty_like(sk), torch.empty_like(sv)
     ta, tt = _time_graph(ga, reps), _time_graph(gt, reps)
+    # attention fused with the next step's top-k (one read of the low-bit keys),
+    # scored by the speculative token (row 1) and by the output token (row 0)
+    idx_f, sc_f = torch.empty_like(idx), torch.empty_like(sc)
+    fused = {}
+    for row in (1, 0):
+        gf = _graph(lambda st: kvq.kvq_attend_topk(c, fmt, q, k, row, pk, pv, idx, sk, sv, out=out, lse=lse,
+                                                   next_idx=idx_f, next_score=sc_f, workspace=ws, stream=st), s)
+        fused[row] = _time_graph(gf, reps)
+    kvq.kvq_topk(c, fmt, qs, k, idx_out=idx, score_out=sc, workspace=ws)
+    torch.cuda.synchronize()
+    fused_same = bool(torch.equal(idx_f, kvq.kvq_topk(c, fmt, q[:, 0].contiguous(), k, workspace=ws)[0]))
     try:
         gg = _graph(lambda st: [kvq.kvq_gather_selected(hk, hv, ix, sel_k=sk2, sel_v=sv2, stream=st) for ix in sets], s)
         tg, fetch_err = _time_graph(gg, reps) / nset, None
@@ -886,8 +897,11 @@ def run_specache(fmt, seed=0, reps=20):
             "topk_ms": tt, "topk_gbs": bt / (tt * 1e-3) / 1e9, "topk_frac": bt / (tt * 1e-3) / 1e9 / peak,
             "fetch_ms": tg, "fetch_error": fetch_err, "fetch_gbs": B * H * k * 2 * D * 2 / (tg * 1e-3) / 1e9,
             "fetch_frac_of_h2d_copy": B * H * k * 2 * D * 2 / (tg * 1e-3) / 1e9 / h2d_gbs, "h2d_copy_gbs": h2d_gbs,
-            "step_ms": ta + tt + tg, "step": "attention + top-k + fetch, each timed on its own",
-            "kv_tok_per_s": B * (lq + r0 + 2) / ((ta + tt + tg) * 1e-3),
+            "fused_attend_topk_ms": fused[1], "fused_attend_topk_row0_ms": fused[0],
+            "fused_matches_separate_topk": fused_same,
+            "step_ms": fused[1] + tg, "step": "fused attention + top-k, then the fetch, each timed on its own",
+            "step_separate_ms": ta + tt + tg,
+            "kv_tok_per_s": B * (lq + r0 + 2) / ((fused[1] + tg) * 1e-3),
             "peak_gbs": peak, "peak_source": src}
 
 
@@ -985,7 +999,7 @@ def run_profile_case(name, launches):
         out = torch.empty_like(q)
         for _ in range(launches):
             kvq.kvq_attend(c, "int4" if gamma == 1 else "int8", q, pk, pv, out=out, workspace=ws)
-    elif name in ("attend-int2-specache-32k", "topk-int2-specache-32k"):
+    elif name in ("attend-int2-specache-32k", "topk-int2-specache-32k", "attend-topk-int2-specache-32k"):
         B, Hq, H, D, G, lq, r0, k = 36, 32, 8, 128, 32, 32768, 32, 64
         K, V = ki.kv_stream_torch(0, B, H, lq + r0, D)
         c = kvq.QuantizedKVCache(B, H, D, G, "int2", lq + 2 * G)
@@ -998,9 +1012,12 @@ def run_profile_case(name, launches):
         sk, sv = torch.gather(K, 2, gi).contiguous(), torch.gather(V, 2, gi).contiguous()
         del K, V, gi
         torch.cuda.empty_cache()
+        nidx = torch.empty_like(idx)
         for i in range(launches):
             if name.startswith("topk"):
                 kvq.kvq_topk(c, "int2", q[:, 1].contiguous(), k, idx_out=idx, workspace=ws)
+            elif name.startswith("attend-topk"):
+                kvq.kvq_attend_topk(c, "int2", q, k, 1, pk, pv, idx, sk, sv, next_idx=nidx, workspace=ws)
             else:
                 kvq.kvq_attend(c, "int2", q, pk, pv, idx, sk, sv, workspace=ws)
     elif name == "fetch-specache-host":

@@ -282,6 +282,36 @@ kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int3
                       kvq_stream_t stream);
 
 /*
+ * kvq_attend plus the next step's top-k, from one read of the low-bit keys
+ * (SpeCache page, "Approach": the speculative token decoded with the output
+ * token predicts the next step's top-k KV pairs; "Measured effects": the
+ * speculative fetch against output-token-based, non-speculative fetching).
+ * The attention pass scores every quantized token with the summed query of
+ * query row `score_row` (1: the speculative token of a gamma = 2 SpeCache step;
+ * 0: the output token, the non-speculative variant) while it streams the keys,
+ * and a selection pass then picks the next_k best per KV head.
+ *  All kvq_attend arguments, with kvq_attend's meaning and results (out, lse).
+ *  mode        KVQ_MODE_INT4, INT4_MID, INT2 or INT1 (INT8 returns
+ *              KVQ_ERR_UNSUPPORTED: the hierarchical cache is ranked by its
+ *              4-bit draft code).
+ *  score_row   0 <= score_row < gamma.
+ *  next_k      1..1024; next_idx int32 [B][Hkv][next_k] (device), next_score
+ *              fp32, same shape, or NULL.  Identical to kvq_topk(cache, mode,
+ *              q[:, score_row], num_q_heads, next_k, ...): same indices, same
+ *              score bits, same order and padding.
+ *  workspace   at least kvq_workspace_bytes(cache, num_q_heads, gamma, next_k),
+ *              which holds the per-token scores between the two passes.
+ * Enqueues two kernels.  Errors as kvq_attend and kvq_topk, returned before
+ * any launch.
+ */
+kvq_status kvq_attend_topk(const kvq_cache* cache, kvq_mode mode, const void* q, int32_t num_q_heads,
+                           int32_t gamma, const void* pend_k, const void* pend_v, int32_t n_pend,
+                           const int32_t* sel_idx, const void* sel_k, const void* sel_v, int32_t top_k,
+                           float sm_scale, void* out, float* lse, int32_t score_row, int32_t next_k,
+                           int32_t* next_idx, float* next_score, void* workspace, size_t ws_bytes,
+                           kvq_stream_t stream);
+
+/*
  * How kvq_attend would split a call with these arguments on the current
  * device.  The paper has no counterpart: this reports the launch plan.
  *  plan->quant_splits  CTAs per (b, kvh) over the quantized context (0 if empty)
@@ -311,8 +341,8 @@ kvq_status kvq_attend_plan(const kvq_cache* cache, kvq_mode mode, int32_t num_q_
  *                            INT4_MID's zero point is fp32(zero_d + 8 s_d))
  *   e   = exponent with max_d|w_d| < 2^e, floored at -100
  *   W_d = rint(w_d * 2^(21-e)),  S_t = sum_d W_d * code_{t,d} (exact integer)
- *   beta = ((0 + fp32(qs_0 zero_0)) + fp32(qs_1 zero_1)) + ... , fp32 adds in
- *          ascending channel order
+ *   p_d = fp32(qs_d * zero_d), f = exponent with max_d|p_d| < 2^f, floored at -80
+ *   beta = fp32(sum_d rint(p_d * 2^(40-f))) * 2^(f-40)   (an exact integer sum)
  *   score_t = fp32(fp32(fp32(S_t) * 2^(e-21)) + beta)
  * Tokens are ordered by (score descending, index ascending).  Positions beyond
  * Lq get index -1 and score -inf.

@@ -35,7 +35,7 @@ EXPORTED = (
     "kvq_status_string", "kvq_cache_bytes", "kvq_cache_init", "kvq_quantize_append",
     "kvq_workspace_bytes", "kvq_attend", "kvq_topk", "kvq_workspace_status",
     "kvq_selftest_bounded_wait", "kvq_attend_static_scratch", "kvq_attend_plan", "kvq_gather_selected",
-    "kvq_cache_set_ragged", "kvq_quantize_append_ragged",
+    "kvq_cache_set_ragged", "kvq_quantize_append_ragged", "kvq_attend_topk",
 )
 
 
@@ -103,6 +103,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kvq_attend.argtypes = [cache_p, ctypes.c_int, vp, i32, i32, vp, vp, i32, vp, vp, vp, i32, f32,
                                vp, vp, vp, sz, vp]
     lib.kvq_attend.restype = ctypes.c_int
+    lib.kvq_attend_topk.argtypes = [cache_p, ctypes.c_int, vp, i32, i32, vp, vp, i32, vp, vp, vp, i32, f32,
+                                    vp, vp, i32, i32, vp, vp, vp, sz, vp]
+    lib.kvq_attend_topk.restype = ctypes.c_int
     lib.kvq_attend_static_scratch.argtypes = [cache_p, ctypes.c_int, vp, i32, i32, vp, vp, i32, vp, vp, vp,
                                               i32, f32, vp, vp, vp]
     lib.kvq_attend_static_scratch.restype = ctypes.c_int
@@ -302,6 +305,41 @@ def kvq_attend(cache: QuantizedKVCache, mode: str, q: torch.Tensor, pend_k=None,
                           workspace.numel(), _stream(stream)),
            "kvq_attend")
     return out, lse
+
+
+def kvq_attend_topk(cache: QuantizedKVCache, mode: str, q: torch.Tensor, next_k: int, score_row: int = 1,
+                    pend_k=None, pend_v=None, sel_idx=None, sel_k=None, sel_v=None, sm_scale: float = 0.0,
+                    out=None, lse=None, next_idx=None, next_score=None, workspace: Optional[torch.Tensor] = None,
+                    want_lse: bool = True, stream=None):
+    """Attention plus the next step's top-k from one read of the low-bit keys;
+    ``score_row`` picks the query token whose summed heads score the tokens
+    (1: the speculative token, 0: the output token).  Returns
+    (out, lse, next_idx, next_score)."""
+    B, gamma, Hq, D = q.shape
+    Hkv = cache.desc.num_kv_heads
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, gamma, Hq), dtype=torch.float32, device=q.device)
+    if next_idx is None:
+        next_idx = torch.empty((B, Hkv, next_k), dtype=torch.int32, device=q.device)
+    if next_score is None:
+        next_score = torch.empty((B, Hkv, next_k), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = make_workspace(cache, Hq, gamma, next_k)
+    n_pend = 0 if pend_k is None else pend_k.shape[2]
+    top_k = 0 if sel_idx is None else sel_idx.shape[2]
+    lib = load_library()
+    _check(lib.kvq_attend_topk(ctypes.byref(cache.struct), MODES[mode], _ptr(q, torch.bfloat16, "q"), Hq, gamma,
+                               _ptr(pend_k, torch.bfloat16, "pend_k"), _ptr(pend_v, torch.bfloat16, "pend_v"), n_pend,
+                               _ptr(sel_idx, torch.int32, "sel_idx"), _ptr(sel_k, torch.bfloat16, "sel_k"),
+                               _ptr(sel_v, torch.bfloat16, "sel_v"), top_k, float(sm_scale),
+                               _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"), int(score_row),
+                               int(next_k), _ptr(next_idx, torch.int32, "next_idx"),
+                               _ptr(next_score, torch.float32, "next_score"), _ptr(workspace, torch.uint8, "workspace"),
+                               workspace.numel(), _stream(stream)),
+           "kvq_attend_topk")
+    return out, lse, next_idx, next_score
 
 
 def kvq_attend_plan(cache: QuantizedKVCache, mode: str, num_q_heads: int, gamma: int, n_pend: int = 0,

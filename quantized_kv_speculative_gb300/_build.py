@@ -18,7 +18,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvq.so")
-SOURCES = ["kvq_api.cu", "kvq_quant.cu", "kvq_attend.cu", "kvq_topk.cu", "kvq_static_scratch.cu", "kvq_gather.cu"]
+SOURCES = ["kvq_api.cu", "kvq_quant.cu", "kvq_attend.cu", "kvq_attend_int8.cu", "kvq_attend_int4.cu",
+           "kvq_attend_int2.cu", "kvq_attend_int1.cu", "kvq_attend_int4_score.cu", "kvq_attend_int2_score.cu",
+           "kvq_attend_int1_score.cu", "kvq_topk.cu", "kvq_static_scratch.cu", "kvq_gather.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -209,10 +209,11 @@ struct AttendPlan {
   int cluster;
 };
 
-AttendPlan plan_attend(const kvq_cache* cache, int mode, int R, int n_pend, int top_k) {
+AttendPlan plan_attend(const kvq_cache* cache, int mode, int R, int n_pend, int top_k, bool score = false) {
   AttendPlan pl{};
   const long long U = units_of(cache);
-  const long long slots = attend_resident_ctas(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size, R);
+  const long long slots =
+      attend_resident_ctas(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size, R, score);
   const long long max_chunk = max_chunk_for_rows(R);
   // The bf16 tail (residual, pending and selected tokens) goes to CTAs of its
   // own when they fit in the first wave beside the quantized splits without
@@ -237,7 +238,7 @@ AttendPlan plan_attend(const kvq_cache* cache, int mode, int R, int n_pend, int 
   const int S_all = pl.S_q + pl.S_t;
   if (S_all >= 1 && S_all <= kMaxClusterCtas && slots > 0 && clusters_enabled()) {
     const long long cap =
-        attend_resident_clusters(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size, R, S_all);
+        attend_resident_clusters(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size, R, S_all, score);
     if (cap > 0 && ceil_div(U, cap) <= ceil_div(U * S_all, slots)) pl.cluster = 1;
   }
   return pl;
@@ -248,6 +249,78 @@ kvq_status zero_counters_once(kvq_cache* cache, unsigned* ctr, cudaStream_t s) {
   if (cudaMemsetAsync(ctr, 0, static_cast<size_t>(units_of(cache)) * 4, s) != cudaSuccess) return KVQ_ERR_CUDA;
   cache->flags |= kFlagCountersZeroed;
   return KVQ_OK;
+}
+
+// Per-token scores that kvq_attend_topk's attention pass writes for its
+// selection pass: [B*Hkv][C] fp32.
+size_t pre_score_bytes(const kvq_cache_desc* d) {
+  return align256(static_cast<size_t>(d->batch) * d->num_kv_heads * static_cast<size_t>(d->capacity_tokens) * 4);
+}
+
+// Launch parameters of an attention call whose arguments are checked.
+AttendParams make_attend_params(const kvq_cache* cache, int mode, const void* q, int num_q_heads, int gamma,
+                                const void* pend_k, const void* pend_v, int n_pend, const int32_t* sel_idx,
+                                const void* sel_k, const void* sel_v, int top_k, float sm_scale, void* out, float* lse,
+                                uint8_t* ws, bool score) {
+  const int HG = num_q_heads / cache->desc.num_kv_heads;
+  if (!(sm_scale > 0.f)) sm_scale = 1.0f / std::sqrt(static_cast<float>(cache->desc.head_dim));
+  AttendParams p{};
+  p.c = view_of(cache);
+  p.q = static_cast<const uint16_t*>(q);
+  p.Hq = num_q_heads;
+  p.gamma = gamma;
+  p.HG = HG;
+  p.R = gamma * HG;
+  p.pend_k = static_cast<const uint16_t*>(pend_k);
+  p.pend_v = static_cast<const uint16_t*>(pend_v);
+  p.P = n_pend;
+  p.sel_idx = sel_idx;
+  p.sel_k = static_cast<const uint16_t*>(sel_k);
+  p.sel_v = static_cast<const uint16_t*>(sel_v);
+  p.top_k = top_k;
+  p.qscale = sm_scale * 1.4426950408889634f;
+  p.zshift = mode_zero_shift(mode);
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  const long long U = units_of(cache);
+  p.status = reinterpret_cast<int*>(ws);
+  p.counters = reinterpret_cast<unsigned*>(ws + kStatusBytes);
+  p.partials = reinterpret_cast<float*>(ws + kStatusBytes + align256(U * 4));
+  const AttendPlan pl = plan_attend(cache, mode, gamma * HG, n_pend, top_k, score);
+  p.S_q = pl.S_q;
+  p.S_t = pl.S_t;
+  p.chunk = pl.chunk;
+  p.cluster = pl.cluster;
+  p.wait_limit = kDefaultWaitLimit;
+  return p;
+}
+
+// Launch parameters of a top-k selection (arguments and plan checked).  The
+// query row of sequence b sits at q + b * q_bstride.
+TopkParams make_topk_params(const kvq_cache* cache, int mode, const uint16_t* q, long long q_bstride, int num_q_heads,
+                            int k, int32_t* idx_out, float* score_out, uint8_t* workspace, int S, long long chunk) {
+  const long long U = units_of(cache);
+  TopkParams p{};
+  p.c = view_of(cache);
+  p.q = q;
+  p.q_bstride = q_bstride;
+  p.Hq = num_q_heads;
+  p.HG = num_q_heads / cache->desc.num_kv_heads;
+  p.k = k;
+  p.zshift = mode_zero_shift(mode);
+  p.align = topk_align(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size);
+  p.idx_out = idx_out;
+  p.score_out = score_out;
+  uint8_t* ws = workspace + kStatusBytes + attend_ws_bytes(&cache->desc);
+  p.status = reinterpret_cast<int*>(workspace);
+  p.counters = reinterpret_cast<unsigned*>(ws);
+  const size_t Smax = static_cast<size_t>(topk_splits_max(&cache->desc, k));
+  p.cand_score = reinterpret_cast<float*>(ws + align256(U * 4));
+  p.cand_idx = reinterpret_cast<int32_t*>(ws + align256(U * 4) + align256(U * Smax * k * 4));
+  p.S = S;
+  p.chunk = chunk;
+  p.wait_limit = kDefaultWaitLimit;
+  return p;
 }
 
 }  // namespace
@@ -498,7 +571,9 @@ size_t kvq_workspace_bytes(const kvq_cache* cache, int32_t num_q_heads, int32_t 
   if (num_q_heads < Hkv || num_q_heads % Hkv) return 0;
   if (gamma < 1 || static_cast<long long>(gamma) * (num_q_heads / Hkv) > kMaxRows) return 0;
   if (top_k < 0 || top_k > kMaxTopk) return 0;
-  return kStatusBytes + attend_ws_bytes(&cache->desc) + topk_ws_bytes(&cache->desc, std::max(top_k, 1));
+  // with a top-k, room for kvq_attend_topk's per-token scores as well
+  return kStatusBytes + attend_ws_bytes(&cache->desc) + topk_ws_bytes(&cache->desc, std::max(top_k, 1)) +
+         (top_k > 0 ? pre_score_bytes(&cache->desc) : 0);
 }
 
 }  // extern "C"
@@ -540,42 +615,52 @@ kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int3
   const kvq_status chk = attend_check(cache, mode, q, num_q_heads, gamma, pend_k, pend_v, n_pend, sel_idx, sel_k,
                                       sel_v, top_k, out, lse, &need);
   if (chk != KVQ_OK) return chk;
-  const int Hkv = cache->desc.num_kv_heads;
-  const int HG = num_q_heads / Hkv;
   if (!workspace || !aligned16(workspace) || ws_bytes < need) return KVQ_ERR_WORKSPACE;
-  if (!(sm_scale > 0.f)) sm_scale = 1.0f / std::sqrt(static_cast<float>(cache->desc.head_dim));
-
-  AttendParams p{};
-  p.c = view_of(cache);
-  p.q = static_cast<const uint16_t*>(q);
-  p.Hq = num_q_heads;
-  p.gamma = gamma;
-  p.HG = HG;
-  p.R = gamma * HG;
-  p.pend_k = static_cast<const uint16_t*>(pend_k);
-  p.pend_v = static_cast<const uint16_t*>(pend_v);
-  p.P = n_pend;
-  p.sel_idx = sel_idx;
-  p.sel_k = static_cast<const uint16_t*>(sel_k);
-  p.sel_v = static_cast<const uint16_t*>(sel_v);
-  p.top_k = top_k;
-  p.qscale = sm_scale * 1.4426950408889634f;
-  p.zshift = mode_zero_shift(mode);
-  p.out = static_cast<uint16_t*>(out);
-  p.lse = lse;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const long long U = units_of(cache);
-  p.status = reinterpret_cast<int*>(ws);
-  p.counters = reinterpret_cast<unsigned*>(ws + kStatusBytes);
-  p.partials = reinterpret_cast<float*>(ws + kStatusBytes + align256(U * 4));
-  const AttendPlan pl = plan_attend(cache, mode, gamma * HG, n_pend, top_k);
-  p.S_q = pl.S_q;
-  p.S_t = pl.S_t;
-  p.chunk = pl.chunk;
-  p.cluster = pl.cluster;
-  p.wait_limit = kDefaultWaitLimit;
+  AttendParams p = make_attend_params(cache, mode, q, num_q_heads, gamma, pend_k, pend_v, n_pend, sel_idx, sel_k,
+                                      sel_v, top_k, sm_scale, out, lse, static_cast<uint8_t*>(workspace), false);
   if (p.S_q > attend_splits_max(&cache->desc)) return KVQ_ERR_WORKSPACE;
-  if (launch_attend(p, kernel_mode(mode), static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (launch_attend(p, kernel_mode(mode), false, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_attend_topk(const kvq_cache* cache, kvq_mode mode, const void* q, int32_t num_q_heads,
+                           int32_t gamma, const void* pend_k, const void* pend_v, int32_t n_pend,
+                           const int32_t* sel_idx, const void* sel_k, const void* sel_v, int32_t top_k,
+                           float sm_scale, void* out, float* lse, int32_t score_row, int32_t next_k,
+                           int32_t* next_idx, float* next_score, void* workspace, size_t ws_bytes,
+                           kvq_stream_t stream) {
+  size_t need = 0;
+  const kvq_status chk = attend_check(cache, mode, q, num_q_heads, gamma, pend_k, pend_v, n_pend, sel_idx, sel_k,
+                                      sel_v, top_k, out, lse, &need);
+  if (chk != KVQ_OK) return chk;
+  if (kernel_mode(mode) == KVQ_MODE_INT8) return KVQ_ERR_UNSUPPORTED;   // no low-bit keys to rank
+  if (score_row < 0 || score_row >= gamma) return KVQ_ERR_INVALID_ARG;
+  if (next_k < 1 || next_k > kMaxTopk || !next_idx || !aligned16(next_idx)) return KVQ_ERR_INVALID_ARG;
+  if (next_score && !aligned16(next_score)) return KVQ_ERR_INVALID_ARG;
+  const size_t tk = topk_ws_bytes(&cache->desc, next_k);
+  need += tk + pre_score_bytes(&cache->desc);
+  if (!workspace || !aligned16(workspace) || ws_bytes < need) return KVQ_ERR_WORKSPACE;
+  const long long U = units_of(cache);
+  long long chunk = 0;
+  const int S = topk_plan(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size, cache->quantized_len, U,
+                          next_k, &chunk);
+  if (static_cast<long long>(S) * next_k > kTopkMaxCand) return KVQ_ERR_UNSUPPORTED;
+  if (static_cast<size_t>(S) > static_cast<size_t>(topk_splits_max(&cache->desc, next_k))) return KVQ_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* pre = reinterpret_cast<float*>(ws + kStatusBytes + attend_ws_bytes(&cache->desc) + tk);
+  AttendParams p = make_attend_params(cache, mode, q, num_q_heads, gamma, pend_k, pend_v, n_pend, sel_idx, sel_k,
+                                      sel_v, top_k, sm_scale, out, lse, ws, true);
+  if (p.S_q > attend_splits_max(&cache->desc)) return KVQ_ERR_WORKSPACE;
+  p.score_row = score_row;
+  p.pre = pre;
+  const uint16_t* q_row = static_cast<const uint16_t*>(q) + static_cast<long long>(score_row) * num_q_heads *
+                                                               cache->desc.head_dim;
+  TopkParams t = make_topk_params(cache, mode, q_row, static_cast<long long>(gamma) * num_q_heads * cache->desc.head_dim,
+                                  num_q_heads, next_k, next_idx, next_score, ws, S, chunk);
+  t.pre = pre;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_attend(p, kernel_mode(mode), true, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (launch_topk(t, kernel_mode(mode), true, s) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
 
@@ -609,35 +694,19 @@ kvq_status kvq_topk(const kvq_cache* cache, kvq_mode mode, const void* q_spec, i
   if (top_k < 1 || top_k > kMaxTopk) return KVQ_ERR_INVALID_ARG;
   if (!q_spec || !idx_out || !aligned16(q_spec) || !aligned16(idx_out)) return KVQ_ERR_INVALID_ARG;
   if (score_out && !aligned16(score_out)) return KVQ_ERR_INVALID_ARG;
-  const size_t att = attend_ws_bytes(&cache->desc);
-  const size_t need = kStatusBytes + att + topk_ws_bytes(&cache->desc, top_k);
+  const size_t need = kStatusBytes + attend_ws_bytes(&cache->desc) + topk_ws_bytes(&cache->desc, top_k);
   if (!workspace || !aligned16(workspace) || ws_bytes < need) return KVQ_ERR_WORKSPACE;
   const long long U = units_of(cache);
   long long chunk = 0;
   const int S = topk_plan(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size, cache->quantized_len, U,
                           top_k, &chunk);
   if (static_cast<long long>(S) * top_k > kTopkMaxCand) return KVQ_ERR_UNSUPPORTED;
-  TopkParams p{};
-  p.c = view_of(cache);
-  p.q = static_cast<const uint16_t*>(q_spec);
-  p.Hq = num_q_heads;
-  p.HG = num_q_heads / Hkv;
-  p.k = top_k;
-  p.zshift = mode_zero_shift(mode);
-  p.align = topk_align(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size);
-  p.idx_out = idx_out;
-  p.score_out = score_out;
-  uint8_t* ws = static_cast<uint8_t*>(workspace) + kStatusBytes + att;
-  p.status = static_cast<int*>(workspace);
-  p.counters = reinterpret_cast<unsigned*>(ws);
   const size_t Smax = static_cast<size_t>(topk_splits_max(&cache->desc, top_k));
-  p.cand_score = reinterpret_cast<float*>(ws + align256(U * 4));
-  p.cand_idx = reinterpret_cast<int32_t*>(ws + align256(U * 4) + align256(U * Smax * top_k * 4));
-  p.S = S;
-  p.chunk = chunk;
-  p.wait_limit = kDefaultWaitLimit;
+  TopkParams p = make_topk_params(cache, mode, static_cast<const uint16_t*>(q_spec),
+                                  static_cast<long long>(num_q_heads) * cache->desc.head_dim, num_q_heads, top_k,
+                                  idx_out, score_out, static_cast<uint8_t*>(workspace), S, chunk);
   if (static_cast<size_t>(S) > Smax) return KVQ_ERR_WORKSPACE;
-  if (launch_topk(p, kernel_mode(mode), static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (launch_topk(p, kernel_mode(mode), false, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
 

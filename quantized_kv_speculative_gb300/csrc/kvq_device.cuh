@@ -230,6 +230,33 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t v) {
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
+// 2^e as an fp32 for -126 <= e <= 127.
+__device__ __forceinline__ float pow2f_exact(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
+
+// The top-k score's zero-point term of one key group, by one warp: lane l
+// holds the products p_d = fp32(qs_d z_d) of CPL channels.  With f the
+// exponent of max|p| (max|p| < 2^f, floored at -80), beta = fp32(Z) 2^(f-40)
+// with Z = sum_d rint(p_d 2^(40-f)), an exact 64-bit integer sum, so the
+// lanes may add in any order.  Every lane returns beta.
+template <int CPL>
+__device__ __forceinline__ float zero_term_warp(const float (&p)[CPL]) {
+  float mx = 0.f;
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) mx = fmaxf(mx, fabsf(p[c]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  int f = 0;
+  if (mx > 0.f) frexpf(mx, &f);
+  f = max(f, -80);
+  const float up = pow2f_exact(40 - f);
+  long long z = 0;
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) z += __float2ll_rn(__fmul_rn(p[c], up));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  return __fmul_rn(__ll2float_rn(z), pow2f_exact(f - 40));
+}
+
 }  // namespace kvq
 
 namespace kvq {

@@ -87,11 +87,17 @@ struct AttendParams {
   long long chunk;          // tokens per split (multiple of kChunkAlign)
   long long wait_limit;
   int cluster;              // 1: the S_q + S_t CTAs of a unit form one cluster and combine in shared memory
+  // Scoring variants only: query row whose heads' summed query scores every
+  // quantized token, and where each token's finished top-k score goes.
+  int score_row;
+  float* pre;               // [B*Hkv][C]
 };
 
 struct TopkParams {
   CacheView c;
-  const uint16_t* q;        // [B][Hq][D]
+  const uint16_t* q;        // query row of sequence b at q + b * q_bstride: [Hq][D]
+  long long q_bstride;      // elements between sequences' query rows
+  const float* pre;         // pre-scored launch: [B*Hkv][C] finished scores from the attention's scoring pass
   int Hq, HG, k;
   float zshift;             // key zero points read as fp32(z + zshift * s)
   int32_t* idx_out;         // [B][Hkv][k]
@@ -172,14 +178,18 @@ inline float mode_zero_shift(int mode) { return mode == KVQ_MODE_INT4_MID ? 8.0f
 
 cudaError_t launch_flush(const FlushParams& p, cudaStream_t s);
 cudaError_t launch_residual_write(const ResidualWriteParams& p, cudaStream_t s);
-cudaError_t launch_attend(const AttendParams& p, int mode, cudaStream_t s);
+// `score`: the variant that also scores every quantized token for the next
+// step's top-k (p.pre, p.score_row).
+cudaError_t launch_attend(const AttendParams& p, int mode, bool score, cudaStream_t s);
 // CTAs of the attention kernel variant that fit on the current device at once
 // (0 if unknown).
-int attend_resident_ctas(int mode, int D, int G, int R);
+int attend_resident_ctas(int mode, int D, int G, int R, bool score);
 // Clusters of `size` CTAs of that variant that fit on the current device at
 // once (0 if unknown or if the size cannot be launched).
-int attend_resident_clusters(int mode, int D, int G, int R, int size);
-cudaError_t launch_topk(const TopkParams& p, int mode, cudaStream_t s);
+int attend_resident_clusters(int mode, int D, int G, int R, int size, bool score);
+// `pre`: select from the scores the attention's scoring variant wrote (p.pre)
+// instead of scoring the key planes.
+cudaError_t launch_topk(const TopkParams& p, int mode, bool pre, cudaStream_t s);
 // Top-k split plan for the current device: returns the split count S per
 // (b, kv head) and sets *chunk (tokens per split).
 int topk_plan(int mode, int D, int G, long long Lq, long long U, int k, long long* chunk);

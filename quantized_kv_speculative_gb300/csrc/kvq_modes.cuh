@@ -177,6 +177,34 @@ __host__ __device__ constexpr int kx_chan(int p, int e) {
   }
 }
 
+// Position of lane-chunk channel `cl` among the chunk's key pairs, in halves:
+// 2 * pair + (0: first channel of the pair, 1: second), the inverse of kx_chan.
+template <int MODE, int D>
+__host__ __device__ constexpr int kx_slot(int cl) {
+  if constexpr (MODE == KVQ_MODE_INT8) {
+    constexpr int INV[8] = {0, 4, 1, 5, 2, 6, 3, 7};   // pair within the octet of kx_chan's A8 order
+    return 2 * (4 * (cl / 8) + INV[cl % 8] % 4) + INV[cl % 8] / 4;
+  } else if constexpr (MODE == KVQ_MODE_INT4) {
+    return 2 * (4 * (cl / 8) + cl % 4) + (cl % 8) / 4;
+  } else if constexpr (MODE == KVQ_MODE_INT2) {
+    return 2 * (8 * (cl / 16) + cl % 8) + (cl % 16) / 8;
+  } else {
+    constexpr int HALF = D == 128 ? 16 : 8;
+    return 2 * (cl % HALF) + cl / HALF;
+  }
+}
+
+template <int MODE, int D>
+__host__ __device__ constexpr bool kx_slot_inverts_chan() {
+  for (int p = 0; p < D / 8; ++p)
+    for (int e = 0; e < 2; ++e)
+      if (kx_slot<MODE, D>(kx_chan<MODE, D>(p, e)) != 2 * p + e) return false;
+  return true;
+}
+static_assert(kx_slot_inverts_chan<KVQ_MODE_INT4, 128>() && kx_slot_inverts_chan<KVQ_MODE_INT4, 64>(), "INT4 slots");
+static_assert(kx_slot_inverts_chan<KVQ_MODE_INT2, 128>() && kx_slot_inverts_chan<KVQ_MODE_INT2, 64>(), "INT2 slots");
+static_assert(kx_slot_inverts_chan<KVQ_MODE_INT1, 128>() && kx_slot_inverts_chan<KVQ_MODE_INT1, 64>(), "INT1 slots");
+
 // log2 of key pair p's factor.  The factors repeat with a period that divides
 // D/16, so both halves of a lane chunk see the same ones.
 template <int MODE, int D>
@@ -185,6 +213,14 @@ __host__ __device__ constexpr int ks_log2fac(int p) {
   else if constexpr (MODE == KVQ_MODE_INT4) return (p & 1) ? 4 : 0;
   else if constexpr (MODE == KVQ_MODE_INT2) return 2 * (p % 4);
   else return D == 128 ? p % 8 : p % 4;
+}
+
+// The largest key pair factor's log2 (the scoring weights are scaled to it).
+template <int MODE, int D>
+__host__ __device__ constexpr int score_log2fac_max() {
+  int m = 0;
+  for (int p = 0; p < D / 8; ++p) m = ks_log2fac<MODE, D>(p) > m ? ks_log2fac<MODE, D>(p) : m;
+  return m;
 }
 
 template <int MODE, int D>

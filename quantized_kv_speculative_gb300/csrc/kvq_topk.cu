@@ -8,10 +8,10 @@
 // rounded to 22-bit integers, then scaled:
 //   W_d = rint(fp32(qs_d * s_d) * 2^(21-e)), S_t = sum_d W_d c_{t,d},
 //   score_t = fp32(fp32(fp32(S_t) * 2^(e-21)) + beta),
-//   beta = ((0 + fp32(qs_0 z_0)) + fp32(qs_1 z_1)) + ... (fp32 adds, ascending d).
-// beta is a sequential chain: one thread per key group of the chunk computes
-// it while the first tiles load, and the scoring loop reads it from shared
-// memory.
+//   beta = fp32(Z) * 2^(f-40), Z = sum_d rint(fp32(qs_d z_d) * 2^(40-f)) (exact),
+// with f the exponent of the group's largest |qs_d z_d|.  Both sums are exact
+// integers, so the warp derives beta with shuffles, in any order, when it
+// derives the group's weights.
 // The dot product runs on tensor cores with the keys as the A operand (rows =
 // tokens) and W as the B operand: column 0 holds hi and column 1 holds lo,
 // where W = 2048 hi + lo and |hi|, |lo| <= 1024 are f16-exact integers.  The
@@ -63,8 +63,7 @@ struct TopkSmem {
   static constexpr int RED_OFF = LIST_OFF + kGather * 4;      // per-warp min/max, counts [2 NW]
   static constexpr int BAR_OFF = RED_OFF + 2 * NW * 4;
   static constexpr int MISC_OFF = BAR_OFF + NSLOT * 8;
-  static constexpr int BETA_OFF = MISC_OFF + 64;              // beta per key group of the chunk
-  static constexpr int SC_OFF = BETA_OFF + kTopkMaxChunk / 32 * 4;   // order keys / merge keys (sized per launch)
+  static constexpr int SC_OFF = MISC_OFF + 64;                // order keys / merge keys (sized per launch)
   static constexpr int MAX_SC = kTopkMaxCand * 16;            // >= kTopkMaxChunk * 4; two merge buffers
   static constexpr int MAX_TOTAL = SC_OFF + MAX_SC;
   static_assert(kTopkMaxChunk * 4 <= MAX_SC, "chunk scores must fit");
@@ -333,7 +332,10 @@ __device__ void select_kth(int n, int kth, F take, uint32_t* hist, uint32_t* lis
   }
 }
 
-template <int MODE, int D>
+// PRE: the scores come from the attention's scoring pass (p.pre holds
+// fp32(fp32(S_t) * unit) per token; this kernel adds beta); otherwise the
+// kernel streams and scores the key planes itself.
+template <int MODE, int D, bool PRE>
 __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   using M = Mode<MODE>;
   using RW = Rows<MODE, D>;
@@ -353,7 +355,7 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   const long long t_begin = static_cast<long long>(split) * chunk;
   const long long t_end = min(lq_b, t_begin + chunk);
   const int n = static_cast<int>(max(0LL, t_end - t_begin));
-  const int ntiles = (n + M::TT - 1) / M::TT;
+  const int ntiles = PRE ? 0 : (n + M::TT - 1) / M::TT;   // a pre-scored launch streams nothing
   const int per_warp = (ntiles + NW - 1) / NW;
   const int K = p.k;
   constexpr int SPW = L::SPW;
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   constexpr int kQPre = 8;
   static_assert(D <= NTHREADS, "one query channel per thread");
   uint16_t qpre[kQPre];
-  const long long qoff = (static_cast<long long>(b) * p.Hq + kvh * p.HG) * D + tid;
+  const long long qoff = static_cast<long long>(b) * p.q_bstride + static_cast<long long>(kvh) * p.HG * D + tid;
 #pragma unroll
   for (int hh = 0; hh < kQPre; ++hh) qpre[hh] = (tid < D && hh < p.HG) ? p.q[qoff + hh * D] : 0;
   if (lane == 0) {
@@ -412,37 +414,30 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
     qs[tid] = acc;
   }
   __syncthreads();
-  // beta of every key group of the chunk: fp32(qs_d * z_d) added in ascending
-  // channel order, one thread per group (at most 8192 / 32 = 256 groups)
-  float* beta_s = reinterpret_cast<float*>(smem + L::BETA_OFF);
-  static_assert(kTopkMaxChunk / 32 <= NTHREADS, "one thread per key group");
-  {
-    const int ngrp = (n + G - 1) / G;
-    if (tid < ngrp) {
-      const float4* s4 = reinterpret_cast<const float4*>(p.c.ksz + (u * (p.c.C / G) + t_begin / G + tid) * 2 * D);
-      const float4* z4 = s4 + D / 4;
-      const float zsh = p.zshift;   // INT4 midpoint reading: zero point fp32(z + 8 s)
-      float acc = 0.f;
-#pragma unroll 8
-      for (int d4 = 0; d4 < D / 4; ++d4) {
-        float4 z = __ldg(z4 + d4);
-        if (zsh != 0.f) {
-          const float4 sc = __ldg(s4 + d4);
-          z.x = fmaf(zsh, sc.x, z.x);
-          z.y = fmaf(zsh, sc.y, z.y);
-          z.z = fmaf(zsh, sc.z, z.z);
-          z.w = fmaf(zsh, sc.w, z.w);
-        }
-        acc = __fadd_rn(acc, __fmul_rn(qs[4 * d4 + 0], z.x));
-        acc = __fadd_rn(acc, __fmul_rn(qs[4 * d4 + 1], z.y));
-        acc = __fadd_rn(acc, __fmul_rn(qs[4 * d4 + 2], z.z));
-        acc = __fadd_rn(acc, __fmul_rn(qs[4 * d4 + 3], z.w));
+  volatile int* abort_flag = misc;
+  if constexpr (PRE) {
+    // the attention's scoring pass wrote the finished scores: n is a multiple
+    // of 128 tokens, so each thread takes float4 runs, all loads in flight
+    static_assert(kTopkMaxChunk % (4 * NTHREADS) == 0, "whole float4 runs per thread");
+    const float4* src = reinterpret_cast<const float4*>(p.pre + u * p.c.C + t_begin);
+    constexpr int kRuns = kTopkMaxChunk / (4 * NTHREADS);
+    float4 v[kRuns];
+#pragma unroll
+    for (int r = 0; r < kRuns; ++r) {
+      const int i4 = tid + r * NTHREADS;
+      if (4 * i4 < n) v[r] = __ldcg(src + i4);
+    }
+#pragma unroll
+    for (int r = 0; r < kRuns; ++r) {
+      const int i4 = tid + r * NTHREADS;
+      if (4 * i4 < n) {
+        okeys[4 * i4] = order_key(v[r].x);
+        okeys[4 * i4 + 1] = order_key(v[r].y);
+        okeys[4 * i4 + 2] = order_key(v[r].z);
+        okeys[4 * i4 + 3] = order_key(v[r].w);
       }
-      beta_s[tid] = acc;
     }
   }
-  __syncthreads();
-  volatile int* abort_flag = misc;
 
   {
     // B fragments: lane (g, q) holds column g of W for its channel chunk; only
@@ -477,17 +472,20 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
           // ---- W of this group: lane l derives channels [l*D/32, (l+1)*D/32) ----
           cur_grp = grp;
           const float* ks = ksz + (grp - g_first) * 2 * D;
-          float w[CPL];
+          const float* kz = ks + D;
+          float w[CPL], zp[CPL];
           float mxw = 0.f;
 #pragma unroll
           for (int c = 0; c < CPL; ++c) {
             const int d = lane * CPL + c;
             w[c] = __fmul_rn(qs[d], __fmul_rn(ks[d], smul));
             mxw = fmaxf(mxw, fabsf(w[c]));
+            // zero point as the mode reads it: fp32(z + zshift * s) (the INT4 midpoint reading)
+            zp[c] = __fmul_rn(qs[d], fmaf(p.zshift, ks[d], kz[d]));
           }
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) mxw = fmaxf(mxw, __shfl_xor_sync(0xffffffffu, mxw, o));
-          beta = beta_s[grp - t_begin / G];
+          beta = zero_term_warp<CPL>(zp);
           int e = 0;
           if (mxw > 0.f) frexpf(mxw, &e);
           e = max(e, -100);
@@ -717,14 +715,21 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   }
 }
 
-template <int MODE, int D>
+template <int MODE, int D, bool PRE>
 cudaError_t launch_t(const TopkParams& p, cudaStream_t s) {
   const int smem = smem_bytes<MODE, D>(p.chunk, p.S, p.k);
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&topk_kernel<MODE, D>), TopkSmem<MODE, D>::MAX_TOTAL);
+  cudaError_t e =
+      set_smem_once(reinterpret_cast<const void*>(&topk_kernel<MODE, D, PRE>), TopkSmem<MODE, D>::MAX_TOTAL);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.c.B) * p.c.Hkv * p.S;
-  topk_kernel<MODE, D><<<static_cast<unsigned>(grid), NTHREADS, smem, s>>>(p);
+  topk_kernel<MODE, D, PRE><<<static_cast<unsigned>(grid), NTHREADS, smem, s>>>(p);
   return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_m(const TopkParams& p, bool pre, cudaStream_t s) {
+  if (p.c.D == 128) return pre ? launch_t<MODE, 128, true>(p, s) : launch_t<MODE, 128, false>(p, s);
+  return pre ? launch_t<MODE, 64, true>(p, s) : launch_t<MODE, 64, false>(p, s);
 }
 
 // CTAs per SM of one variant at `smem` bytes of dynamic shared memory, cached
@@ -739,10 +744,11 @@ int per_sm_t(int smem) {
   const int step = (smem + 1023) / 1024;
   if (step >= kSteps) return 0;
   if (cached[dev][step] > 0) return cached[dev][step];
-  if (set_smem_once(reinterpret_cast<const void*>(&topk_kernel<MODE, D>), TopkSmem<MODE, D>::MAX_TOTAL) != cudaSuccess)
+  if (set_smem_once(reinterpret_cast<const void*>(&topk_kernel<MODE, D, false>), TopkSmem<MODE, D>::MAX_TOTAL) !=
+      cudaSuccess)
     return 0;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<MODE, D>, NTHREADS, step * 1024) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<MODE, D, false>, NTHREADS, step * 1024) !=
       cudaSuccess)
     return 0;
   cached[dev][step] = per_sm;
@@ -820,12 +826,11 @@ long long topk_align(int mode, int /*D*/, int G) {
   }
 }
 
-cudaError_t launch_topk(const TopkParams& p, int mode, cudaStream_t s) {
-  const int D = p.c.D;
+cudaError_t launch_topk(const TopkParams& p, int mode, bool pre, cudaStream_t s) {
   switch (mode) {
-    case KVQ_MODE_INT4: return D == 128 ? launch_t<KVQ_MODE_INT4, 128>(p, s) : launch_t<KVQ_MODE_INT4, 64>(p, s);
-    case KVQ_MODE_INT2: return D == 128 ? launch_t<KVQ_MODE_INT2, 128>(p, s) : launch_t<KVQ_MODE_INT2, 64>(p, s);
-    case KVQ_MODE_INT1: return D == 128 ? launch_t<KVQ_MODE_INT1, 128>(p, s) : launch_t<KVQ_MODE_INT1, 64>(p, s);
+    case KVQ_MODE_INT4: return launch_m<KVQ_MODE_INT4>(p, pre, s);
+    case KVQ_MODE_INT2: return launch_m<KVQ_MODE_INT2>(p, pre, s);
+    case KVQ_MODE_INT1: return launch_m<KVQ_MODE_INT1>(p, pre, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -349,3 +349,58 @@ def test_gather_selected_rejects_pageable_memory():
     assert kvq.STATUS[st] == "KVQ_ERR_INVALID_ARG"
     with pytest.raises(ValueError):
         kvq.kvq_gather_selected(K, K, sel)
+
+
+# ------------------------------------------------------------------------------------
+# attention fused with the next step's top-k
+# ------------------------------------------------------------------------------------
+
+FUSED_CASES = [
+    # mode, B, Hkv, Hq, D, G, N, gamma, P, top_k (selected), next_k, score_row
+    ("int2", 3, 2, 8, 128, 32, 2100, 2, 2, 16, 64, 1),      # SpeCache step: the speculative token scores
+    ("int2", 3, 2, 8, 128, 32, 2100, 2, 2, 16, 64, 0),      # the output token scores (non-speculative fetch)
+    ("int1", 2, 2, 8, 64, 32, 1500, 2, 2, 0, 17, 1),
+    ("int4", 1, 3, 3, 128, 128, 4000, 1, 1, 0, 64, 0),      # MHA draft shape, one row
+    ("int4mid", 2, 2, 8, 128, 64, 1700, 2, 2, 7, 33, 1),
+    ("int2", 1, 1, 4, 128, 32, 20000, 2, 2, 0, 100, 1),     # several top-k splits
+]
+
+
+@pytest.mark.parametrize("case", FUSED_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_attend_topk_matches_oracle_and_topk(case):
+    """kvq_attend_topk: the attention output matches the oracle, and the next
+    step's top-k is identical (indices and score bits) to the oracle's and to
+    kvq_topk on the same query row."""
+    mode, B, Hkv, Hq, D, G, N, gamma, P, top_k, next_k, row = case
+    gc, oc, q, pk, pv, sel, sk, sv = _attn_case(mode, B, Hkv, Hq, D, G, N, gamma, P, top_k, False, seed=3)
+    t = lambda x: None if x is None else dev(x)
+    out, lse, idx, sc = kvq.kvq_attend_topk(gc, mode, dev(q), next_k, row, t(pk), t(pv),
+                                           None if sel is None else torch.from_numpy(sel).cuda(), t(sk), t(sv))
+    idx2, sc2 = kvq.kvq_topk(gc, mode, dev(q[:, row]), next_k)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.attend(oc, mode, q, pk, pv, sel, sk, sv)
+    assert_attention_close(out, lse, ref_out, ref_lse, what=str(case))
+    ridx, rsc = oracle.topk(oc, mode, q[:, row], next_k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), rsc.view(np.uint32))
+    np.testing.assert_array_equal(idx.cpu().numpy(), idx2.cpu().numpy())
+    np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), sc2.cpu().numpy().view(np.uint32))
+
+
+def test_flush_counters_start_from_garbage():
+    """The flush kernel's arrival counters are zeroed before the cache's first
+    flush even when earlier appends flushed nothing: the cache memory is
+    filled with 0xFF first, then tokens that only fill the residual buffer,
+    then tokens that flush.  Bytes must match the oracle."""
+    B, Hkv, D, G = 2, 3, 64, 32
+    K, V = ki.kv_stream(19, B, Hkv, 4 * G + 9, D)
+    gc = kvq.QuantizedKVCache(B, Hkv, D, G, "int2", 6 * G)
+    gc.storage.fill_(255)
+    oc = oracle.OracleCache(B, Hkv, D, G, "int2", 6 * G)
+    pos = 0
+    for n in (5, G, 3 * G + 4):
+        kvq.kvq_quantize_append(gc, dev(K[:, :, pos:pos + n]), dev(V[:, :, pos:pos + n]))
+        oc.append(K[:, :, pos:pos + n], V[:, :, pos:pos + n])
+        pos += n
+    torch.cuda.synchronize()
+    compare_cache(gc, oc)

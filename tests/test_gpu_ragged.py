@@ -116,11 +116,19 @@ def test_ragged_append_attend_topk_match_oracle_per_sequence(fmt, modes, D, G):
             assert_attention_close(out[b:b + 1], lse[b:b + 1], ref, ref_lse, what=f"{mode} sequence {b}")
         if mode != "int8":
             idx, sc = kvq.kvq_topk(gc, mode, dev(q[:, 1]), k)
+            # the fused call: attention plus the next step's top-k from one key read
+            out2, _, idx2, sc2 = kvq.kvq_attend_topk(gc, mode, dev(q), k, 1, dev(pk), dev(pv),
+                                                     torch.from_numpy(sel).cuda(), dev(sk), dev(sv))
             torch.cuda.synchronize()
+            np.testing.assert_array_equal(idx2.cpu().numpy(), idx.cpu().numpy())
+            np.testing.assert_array_equal(sc2.cpu().numpy().view(np.uint32), sc.cpu().numpy().view(np.uint32))
             for b in range(B):
                 ridx, rsc = oracle.topk(ocs[b], mode, q[b:b + 1, 1], k)
                 np.testing.assert_array_equal(idx[b:b + 1].cpu().numpy(), ridx, err_msg=f"{mode} top-k seq {b}")
                 np.testing.assert_array_equal(sc[b:b + 1].cpu().numpy().view(np.uint32), rsc.view(np.uint32))
+                ref, ref_lse = oracle.attend(ocs[b], mode, q[b:b + 1], pk[b:b + 1], pv[b:b + 1], sel[b:b + 1],
+                                             sk[b:b + 1], sv[b:b + 1])
+                assert_attention_close(out2[b:b + 1], None, ref, ref_lse, what=f"fused {mode} sequence {b}")
 
 
 def test_ragged_specache_batch_36():
