@@ -70,7 +70,7 @@ struct TopkSmem {
   static_assert(SLOT % 16 == 0, "slots must stay 16-byte aligned");
   static_assert(BAR_OFF % 8 == 0, "mbarriers need 8-byte alignment");
   static_assert(NSLOT * SLOT >= kMaxTopk * 8, "the split's winners reuse the stage area");
-  static_assert(NSLOT * SLOT >= 2 * NW * 128 * 8, "the warps' sorted lists reuse the stage area");
+  static_assert(NSLOT * SLOT >= 3 * NW * 128 * 8, "the candidates and the warps' sorted lists reuse the stage area");
 };
 
 template <int MODE, int D>
@@ -569,28 +569,89 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   int* st = misc + 2;  // st[0] T, st[1] remaining, st[2] ties taken, st[3] bin / count, st[4] gather count
   float* cs = p.cand_score + (u * p.S + split) * K;
   int32_t* ci = p.cand_idx + (u * p.S + split) * K;
-  if (keff > 0 && n <= NW * 128 && K <= 128) {
-    // small chunk: each warp sorts its 128 keys, the warps' top-K lists are
-    // merged by the merge-path tree
-    uint64_t* la = reinterpret_cast<uint64_t*>(smem);   // [NW][K], the idle stage area
+  // Sorted selection of the top K among m keys, m <= NW * 128 and K <= 128:
+  // warp w sorts keys [128 w, 128 w + 128) (key(i) gives the composite key of
+  // entry i; 0 pads), and the merge-path tree merges the warps' top-K lists.
+  // Warps past the last entry write padding without sorting.
+  auto sorted_select = [&](int m, auto key, uint64_t* area) {
+    const int nl = max(1, (m + 127) / 128);
+    uint64_t* la = area;                                   // [nl][K]
     uint64_t* lb = la + NW * K;
-    uint64_t v[4];
+    if (warp < nl) {
+      uint64_t v[4];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = warp * 128 + 32 * r + lane;
-      v[r] = (i < n) ? composite(okeys[i], static_cast<uint32_t>(t_begin + i)) : 0ull;
+      for (int r = 0; r < 4; ++r) {
+        const int i = warp * 128 + 32 * r + lane;
+        v[r] = (i < m) ? key(i) : 0ull;
+      }
+      warp_sort128_desc(v);
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        if (32 * r + lane < K) la[warp * K + 32 * r + lane] = v[r];
     }
-    warp_sort128_desc(v);
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-      if (32 * r + lane < K) la[warp * K + 32 * r + lane] = v[r];
     __syncthreads();
-    const uint64_t* top = merge_tree(la, lb, NW, K);
+    const uint64_t* top = merge_tree(la, lb, nl, K);
     for (int i = tid; i < keff; i += blockDim.x) {
-      const uint64_t key = top[i];
-      cs[i] = key_to_score(static_cast<uint32_t>(key >> 32));
-      ci[i] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+      const uint64_t key2 = top[i];
+      cs[i] = key_to_score(static_cast<uint32_t>(key2 >> 32));
+      ci[i] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key2));
     }
+  };
+  bool selected = false;
+  if (keff > 0 && n <= NW * 128 && K <= 128) {
+    // small chunk: sort all of it
+    sorted_select(n, [&](int i) { return composite(okeys[i], static_cast<uint32_t>(t_begin + i)); },
+                  reinterpret_cast<uint64_t*>(smem));
+    selected = true;
+  } else if (keff > 0 && K <= 128) {
+    // Long chunk: a lower bound first.  The keys fall into 128 strided segments
+    // (i mod 128); K segment maxima are K distinct keys, so the K-th largest
+    // segment maximum T0 is at most the K-th largest key.  The keys >= T0
+    // (about 1% of them when they are spread out) are then sorted exactly; if
+    // ties leave more than NW * 128 of them, the radix selection below runs.
+    uint32_t* segmax = hist;                                // [256], then [128]
+    {
+      uint32_t mx = 0u;
+      for (int i = tid; i < n; i += NTHREADS) mx = max(mx, okeys[i]);   // segment tid % 128
+      segmax[tid] = mx;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      uint64_t v[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int sg = 32 * r + lane;
+        v[r] = static_cast<uint64_t>(max(segmax[sg], segmax[sg + 128])) << 32;
+      }
+      warp_sort128_desc(v);
+      const int kk = keff - 1;
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        if (32 * r + lane == kk) st[0] = static_cast<int>(static_cast<uint32_t>(v[r] >> 32));
+      if (lane == 0) st[4] = 0;
+    }
+    __syncthreads();
+    const uint32_t T0 = static_cast<uint32_t>(st[0]);
+    uint64_t* cand = reinterpret_cast<uint64_t*>(smem);     // [NW * 128] in the idle stage area
+    for (int base = warp * 32; base < n; base += NTHREADS) {
+      const int i = base + lane;
+      const uint32_t key = (i < n) ? okeys[i] : 0u;
+      const bool take = (i < n) && key >= T0;
+      const uint32_t bal = __ballot_sync(0xffffffffu, take);
+      int pos = 0;
+      if (lane == 0 && bal) pos = atomicAdd(st + 4, __popc(bal));
+      pos = __shfl_sync(0xffffffffu, pos, 0) + __popc(bal & ((1u << lane) - 1u));
+      if (take && pos < NW * 128) cand[pos] = composite(key, static_cast<uint32_t>(t_begin + i));
+    }
+    __syncthreads();
+    const int ncand = st[4];
+    __syncthreads();
+    if (ncand <= NW * 128) {
+      sorted_select(ncand, [&](int i) { return cand[i]; }, cand + NW * 128);
+      selected = true;
+    }
+  }
+  if (selected) {
   } else if (keff > 0) {
     select_kth(n, keff, [&](int i, uint32_t& key) { key = okeys[i]; return true; }, hist, list, red, st);
     const uint32_t T = static_cast<uint32_t>(st[0]);
