@@ -165,6 +165,33 @@ __host__ __device__ constexpr bool halves_same_factors() {
   return true;
 }
 
+// Floats of a lane's first-half key pairs, counted from the half's base and
+// rounded up to whole float4s: the eight-row weight setup loads that window
+// of the key scale and zero rows with 128-bit loads.
+template <int MODE, int D>
+__host__ __device__ constexpr int half_window() {
+  int m = 0;
+  for (int k = 0; k < D / 16; ++k)
+    for (int e = 0; e < 2; ++e) m = kx_chan<MODE, D>(k, e) + 1 > m ? kx_chan<MODE, D>(k, e) + 1 : m;
+  return (m + 3) / 4 * 4;
+}
+
+// A token's value scales then zero points (2 NJ floats, 8 NJ-byte aligned) as
+// 64- or 128-bit shared loads.
+template <int NJ>
+__device__ __forceinline__ void load_vrow(const float* v, float (&out)[2 * NJ]) {
+  if constexpr (NJ == 1) {
+    const float2 x = *reinterpret_cast<const float2*>(v);
+    out[0] = x.x; out[1] = x.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < NJ / 2; ++i) {
+      const float4 x = reinterpret_cast<const float4*>(v)[i];
+      out[4 * i] = x.x; out[4 * i + 1] = x.y; out[4 * i + 2] = x.z; out[4 * i + 3] = x.w;
+    }
+  }
+}
+
 // The queries of unit (b, kvh) as 16-byte slices of 8 channels: slice e is
 // row e / (D/8) (zero for rows >= R); one slice per thread (8 rows x D/8
 // slices <= 128 threads).  load_q issues the load, so that it is in flight
@@ -961,14 +988,22 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
             static_assert(halves_shift<MODE, D>(), "the second half's pairs are the first half's, shifted");
             static_assert(halves_same_factors<MODE, D>(), "both halves carry the same code factors");
             const int cb = q * (D / 4) + par * DELTA;         // this lane's channel base
+            static_assert(DELTA % 4 == 0, "the halves' windows start on float4 boundaries");
+            constexpr int WIN = half_window<MODE, D>();
             const float* ksc = ks + cb;
             const float* kzc = kz + cb;
+            float ksw[WIN];
+#pragma unroll
+            for (int v4 = 0; v4 < WIN / 4; ++v4) {
+              const float4 x = reinterpret_cast<const float4*>(ksc)[v4];
+              ksw[4 * v4] = x.x; ksw[4 * v4 + 1] = x.y; ksw[4 * v4 + 2] = x.z; ksw[4 * v4 + 3] = x.w;
+            }
             float kv[HP][2];
             float smax = 0.f;
 #pragma unroll
             for (int k = 0; k < HP; ++k) {
-              kv[k][0] = ksc[kx_chan<MODE, D>(k, 0)];
-              kv[k][1] = ksc[kx_chan<MODE, D>(k, 1)];
+              kv[k][0] = ksw[kx_chan<MODE, D>(k, 0)];
+              kv[k][1] = ksw[kx_chan<MODE, D>(k, 1)];
               smax = fmaxf(smax, fmaxf(kv[k][0], kv[k][1]));
             }
             smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 4));
@@ -989,14 +1024,20 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
               const float* qr = qt + (4 * nt + (g >> 1)) * qt_row<D>() + q * qt_chunk<D>() + par * DELTA;
               float zs = 0.f;
               uint32_t keep[HP], send[HP];
+              float kzw[WIN];
+#pragma unroll
+              for (int v4 = 0; v4 < WIN / 4; ++v4) {
+                const float4 x = reinterpret_cast<const float4*>(kzc)[v4];
+                kzw[4 * v4] = x.x; kzw[4 * v4 + 1] = x.y; kzw[4 * v4 + 2] = x.z; kzw[4 * v4 + 3] = x.w;
+              }
 #pragma unroll
               for (int k = 0; k < HP; ++k) {
                 const int c0 = kx_chan<MODE, D>(k, 0), c1 = kx_chan<MODE, D>(k, 1);
                 const float q0 = qr[c0], q1 = qr[c1];
-                float z0 = kzc[c0], z1 = kzc[c1];
+                float z0 = kzw[c0], z1 = kzw[c1];
                 if (zsh != 0.f) {
-                  z0 = fmaf(zsh, ksc[c0], z0);
-                  z1 = fmaf(zsh, ksc[c1], z1);
+                  z0 = fmaf(zsh, ksw[c0], z0);
+                  z1 = fmaf(zsh, ksw[c1], z1);
                 }
                 zs = fmaf(q0, z0, fmaf(q1, z1, zs));
                 const float w0 = q0 * kv[k][0], w1 = q1 * kv[k][1];
@@ -1233,8 +1274,9 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
         float smx = 0.f;
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
-          const float* va = vsz + (32 * sl + tokA[s]) * 2 * NJ;
-          const float* vb = vsz + (32 * sl + tokB[s]) * 2 * NJ;
+          float va[2 * NJ], vb[2 * NJ];
+          load_vrow<NJ>(vsz + (32 * sl + tokA[s]) * 2 * NJ, va);
+          load_vrow<NJ>(vsz + (32 * sl + tokB[s]) * 2 * NJ, vb);
 #pragma unroll
           for (int jv = 0; jv < NJ; ++jv) {
             sA[s][jv] = va[jv] * MULT; zA[s][jv] = fmaf(p.zshift, va[jv], va[NJ + jv]);
