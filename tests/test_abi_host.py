@@ -236,3 +236,26 @@ def test_ragged_state_machine_without_launch(lib):
     big, _ = _host_cache(lib, batch=65)
     many = (kvq.KvqSeqState * 65)()
     assert lib.kvq_cache_set_ragged(ctypes.byref(big), many, 65) == 2
+
+
+def test_attend_topk_argument_errors_need_no_gpu(lib):
+    """The fused attention + top-k call refuses, before any launch: an
+    uninitialized cache (7), a mode without low-bit keys to rank (INT8: 2), a
+    score row outside [0, gamma) or a top-k count outside [1, 1024] or a null
+    index buffer (1), and a workspace without room for the per-token scores
+    (4)."""
+    c, _ = _host_cache(lib)
+    fake = ctypes.c_void_p(1 << 41)
+    ws_n = lib.kvq_workspace_bytes(ctypes.byref(c), 4, 2, 16)
+    ws_att = lib.kvq_workspace_bytes(ctypes.byref(c), 4, 2, 0)
+    assert ws_n > ws_att > 0
+
+    def call(cache, mode, gamma=2, row=1, k=16, idx=fake, wsn=ws_n, P=2):
+        return lib.kvq_attend_topk(ctypes.byref(cache), mode, fake, 4, gamma, fake, fake, P, None, None, None, 0,
+                                   0.0, fake, None, row, k, idx, None, fake, wsn, None)
+    assert call(kvq.KvqCache(), 1) == 7
+    assert call(c, 0) == 2
+    assert call(c, 1, row=2) == 1 and call(c, 1, row=-1) == 1
+    assert call(c, 1, k=0) == 1 and call(c, 1, k=1025) == 1
+    assert call(c, 1, idx=None) == 1
+    assert call(c, 1, wsn=ws_att) == 4
