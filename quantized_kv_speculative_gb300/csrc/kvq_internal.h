@@ -13,7 +13,6 @@ constexpr int kMaxRows = 8;            // rows (gamma x query heads per KV head)
 constexpr int kChunkAlign = 128;       // split boundaries are multiples of this many tokens
 constexpr int kMaxChunk = 8192;        // tokens per attention split, up to four rows (bounds the selection bitmap)
 constexpr int kMaxChunkWide = 16384;   // the same for the eight-row variants
-constexpr int kSplitOverheadTokens = 256;  // a split CTA's fixed cost in the split planner, in tokens
 __host__ __device__ constexpr int max_chunk_for_rows(int R) { return R > 4 ? kMaxChunkWide : kMaxChunk; }
 constexpr int kCtasPerSmTarget = 4;   // split-count target per launch: this many CTAs per SM
 constexpr int kTopkMaxChunk = 8192;    // tokens per top-k split (scores held in shared memory)
