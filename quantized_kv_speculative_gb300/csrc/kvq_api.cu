@@ -305,7 +305,7 @@ AttendParams make_attend_params(const kvq_cache* cache, int mode, const void* q,
 // Launch parameters of a top-k selection (arguments and plan checked).  The
 // query row of sequence b sits at q + b * q_bstride.
 TopkParams make_topk_params(const kvq_cache* cache, int mode, const uint16_t* q, long long q_bstride, int num_q_heads,
-                            int k, int32_t* idx_out, float* score_out, uint8_t* workspace, int S, long long chunk) {
+                            int k, int32_t* idx_out, float* score_out, uint8_t* workspace, const TopkPlan& plan) {
   const long long U = units_of(cache);
   TopkParams p{};
   p.c = view_of(cache);
@@ -324,8 +324,10 @@ TopkParams make_topk_params(const kvq_cache* cache, int mode, const uint16_t* q,
   const size_t Smax = static_cast<size_t>(topk_splits_max(&cache->desc, k));
   p.cand_score = reinterpret_cast<float*>(ws + align256(U * 4));
   p.cand_idx = reinterpret_cast<int32_t*>(ws + align256(U * 4) + align256(U * Smax * k * 4));
-  p.S = S;
-  p.chunk = chunk;
+  p.S = plan.S;
+  p.chunk = plan.chunk;
+  p.spw = plan.spw;
+  p.cluster = plan.cluster;
   p.wait_limit = kDefaultWaitLimit;
   return p;
 }
@@ -648,11 +650,10 @@ kvq_status kvq_attend_topk(const kvq_cache* cache, kvq_mode mode, const void* q,
   need += tk + pre_score_bytes(&cache->desc);
   if (!workspace || !aligned16(workspace) || ws_bytes < need) return KVQ_ERR_WORKSPACE;
   const long long U = units_of(cache);
-  long long chunk = 0;
-  const int S = topk_plan(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size, cache->quantized_len, U,
-                          next_k, &chunk);
-  if (static_cast<long long>(S) * next_k > kTopkMaxCand) return KVQ_ERR_UNSUPPORTED;
-  if (static_cast<size_t>(S) > static_cast<size_t>(topk_splits_max(&cache->desc, next_k))) return KVQ_ERR_WORKSPACE;
+  const TopkPlan tp = topk_plan(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size,
+                                cache->quantized_len, U, next_k, true);
+  if (static_cast<long long>(tp.S) * next_k > kTopkMaxCand) return KVQ_ERR_UNSUPPORTED;
+  if (static_cast<size_t>(tp.S) > static_cast<size_t>(topk_splits_max(&cache->desc, next_k))) return KVQ_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* pre = reinterpret_cast<float*>(ws + kStatusBytes + attend_ws_bytes(&cache->desc) + tk);
   AttendParams p = make_attend_params(cache, mode, q, num_q_heads, gamma, pend_k, pend_v, n_pend, sel_idx, sel_k,
@@ -663,7 +664,7 @@ kvq_status kvq_attend_topk(const kvq_cache* cache, kvq_mode mode, const void* q,
   const uint16_t* q_row = static_cast<const uint16_t*>(q) + static_cast<long long>(score_row) * num_q_heads *
                                                                cache->desc.head_dim;
   TopkParams t = make_topk_params(cache, mode, q_row, static_cast<long long>(gamma) * num_q_heads * cache->desc.head_dim,
-                                  num_q_heads, next_k, next_idx, next_score, ws, S, chunk);
+                                  num_q_heads, next_k, next_idx, next_score, ws, tp);
   t.pre = pre;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch_attend(p, kernel_mode(mode), true, s) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -704,15 +705,14 @@ kvq_status kvq_topk(const kvq_cache* cache, kvq_mode mode, const void* q_spec, i
   const size_t need = kStatusBytes + attend_ws_bytes(&cache->desc) + topk_ws_bytes(&cache->desc, top_k);
   if (!workspace || !aligned16(workspace) || ws_bytes < need) return KVQ_ERR_WORKSPACE;
   const long long U = units_of(cache);
-  long long chunk = 0;
-  const int S = topk_plan(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size, cache->quantized_len, U,
-                          top_k, &chunk);
-  if (static_cast<long long>(S) * top_k > kTopkMaxCand) return KVQ_ERR_UNSUPPORTED;
+  const TopkPlan tp = topk_plan(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size,
+                                cache->quantized_len, U, top_k, false);
+  if (static_cast<long long>(tp.S) * top_k > kTopkMaxCand) return KVQ_ERR_UNSUPPORTED;
   const size_t Smax = static_cast<size_t>(topk_splits_max(&cache->desc, top_k));
   TopkParams p = make_topk_params(cache, mode, static_cast<const uint16_t*>(q_spec),
                                   static_cast<long long>(num_q_heads) * cache->desc.head_dim, num_q_heads, top_k,
-                                  idx_out, score_out, static_cast<uint8_t*>(workspace), S, chunk);
-  if (static_cast<size_t>(S) > Smax) return KVQ_ERR_WORKSPACE;
+                                  idx_out, score_out, static_cast<uint8_t*>(workspace), tp);
+  if (static_cast<size_t>(tp.S) > Smax) return KVQ_ERR_WORKSPACE;
   if (launch_topk(p, kernel_mode(mode), false, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }

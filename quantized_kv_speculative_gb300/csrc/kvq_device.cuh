@@ -114,6 +114,12 @@ __device__ __forceinline__ float ld_dsmem(uint32_t a) {
   return v;
 }
 
+__device__ __forceinline__ uint64_t ld_dsmem_u64(uint32_t a) {
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float4 ld_dsmem4(uint32_t a) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"

@@ -108,7 +108,17 @@ struct TopkParams {
   int S;
   long long chunk;
   long long align;          // chunk alignment of the plan (per-sequence chunks of a ragged cache)
+  int spw;                  // stage slots per warp (streaming variant)
+  int cluster;              // 1: the S CTAs of a (b, kv head) form one cluster and merge through shared memory
   long long wait_limit;
+};
+
+// A top-k launch plan.
+struct TopkPlan {
+  int S;                    // splits per (b, kv head)
+  long long chunk;          // tokens per split
+  int spw;                  // stage slots per warp of the streaming variant
+  int cluster;              // 1: one thread-block cluster per (b, kv head)
 };
 
 struct FlushParams {
@@ -189,9 +199,8 @@ int attend_resident_clusters(int mode, int D, int G, int R, int size, bool score
 // `pre`: select from the scores the attention's scoring variant wrote (p.pre)
 // instead of scoring the key planes.
 cudaError_t launch_topk(const TopkParams& p, int mode, bool pre, cudaStream_t s);
-// Top-k split plan for the current device: returns the split count S per
-// (b, kv head) and sets *chunk (tokens per split).
-int topk_plan(int mode, int D, int G, long long Lq, long long U, int k, long long* chunk);
+// Top-k plan for the current device (`pre`: the pre-scored variant).
+TopkPlan topk_plan(int mode, int D, int G, long long Lq, long long U, int k, bool pre);
 // The chunk alignment topk_plan uses for a variant (whole key groups per warp).
 long long topk_align(int mode, int D, int G);
 cudaError_t launch_wait_selftest(int* status, long long limit, cudaStream_t s);

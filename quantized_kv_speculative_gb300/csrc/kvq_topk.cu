@@ -23,16 +23,29 @@
 //
 // One launch: B*Hkv*S CTAs, with S chosen on the host to balance waves against
 // the merge.  Each CTA scores one chunk (bulk-copied tiles on an mbarrier ring,
-// as in attention) into 32-bit order keys, selects its top k by (score desc,
-// index asc) and writes them in descending order of the unique composite key
-// (order key, ~index).  The last CTA of each (b, kvh), found through an atomic
-// ticket, merges the S sorted lists pairwise (merge path: each output position
-// finds its split by binary search), keeping the top k at every level.
+// as in attention; a pre-scored launch reads the attention's scores instead)
+// into 32-bit order keys and selects its top k by (score desc, index asc),
+// as unique composite keys (order key, ~index) in descending order.
 //
-// Selection (select_kth): the block finds the smallest and largest key,
-// histograms the 8 bits below their common prefix and locates the bin that
-// holds the kth key.  When that bin holds few keys they are gathered and ranked
-// directly; otherwise the next 8 bits of that bin are histogrammed, and so on.
+// Selection of a chunk's top k (k <= 128):
+//  * a lower bound T0: the keys fall into 128 strided segments (i mod 128);
+//    the k-th largest segment maximum is at most the k-th largest key, since
+//    k segment maxima are k distinct keys at least that large;
+//  * every warp collects the keys >= T0 of its share into its own region
+//    (ballot + population count, no shared counter);
+//  * the candidates (about 100 when the keys are spread out) are ranked by
+//    counting, each against all, and land at their rank.
+// More candidates than one per thread go through warp bitonic sorts of 128
+// and a merge-path tree; more than 1024, or k > 128, through a radix
+// selection of the k-th key (select_kth).
+//
+// Merge of a unit's S sorted lists (k <= 128): warps merge pairs of lists in
+// registers (a bitonic half-cleaner and merge network), level by level; larger
+// k takes a merge-path tree.
+// With S <= 8 and k <= 128 the S CTAs of a unit form one thread-block cluster,
+// the lists stay in shared memory and the first CTA reads them through
+// distributed shared memory; otherwise every CTA writes its list to the
+// workspace and the last CTA to arrive (an atomic ticket) merges.
 #include <algorithm>
 
 #include "kvq_modes.cuh"
@@ -41,43 +54,61 @@ namespace kvq {
 namespace {
 
 constexpr int NW = 8;                  // warps per CTA; each streams and scores its own tiles
-
 constexpr int NTHREADS = NW * 32;
-constexpr int kGather = 64;            // bin size below which keys are ranked directly
+constexpr int kGather = 64;            // bin size below which select_kth ranks keys directly
+constexpr int kSpwMax = 4;             // stage slots per warp, at most
+constexpr int kRegion = 128;           // candidates per warp region
+constexpr int kClusterMax = 8;         // splits that merge as one cluster, at most
+
+// Post-scoring scratch at the start of shared memory (over the idle stage
+// ring): packed candidates, the warps' candidate regions (later the sort
+// lists of the merge-path fallback), select_kth's histograms.  A merge's S x k
+// list entries (<= kTopkMaxCand) reuse it from offset 0.
+constexpr int kPackOff = 0;                                 // [NW * kRegion + 2] u64
+constexpr int kRegOff = kPackOff + (NW * kRegion + 2) * 8;  // [NW][kRegion] u64
+constexpr int kListOff = kRegOff;                           // [2][NW][k <= 128] u64
+constexpr int kHistOff = kListOff + 2 * NW * 128 * 8;       // [NW][256] u32 (also the 256 segment maxima)
+constexpr int kScratch = kHistOff + NW * 256 * 4;
+static_assert(kRegOff % 16 == 0 && kHistOff % 16 == 0 && kScratch % 16 == 0, "16-byte aligned scratch");
+static_assert(kTopkMaxCand * 8 <= kScratch, "a merge's list entries fit the scratch");
+static_assert(kMaxTopk * 8 <= kRegOff, "select_kth's winners fit below the regions");
 
 template <int MODE, int D>
-struct TopkSmem {
+struct TopkTile {
   using M = Mode<MODE>;
   using RW = Rows<MODE, D>;
   static constexpr int TT = M::TT;
-  static constexpr int SPW = 2;                               // stage slots per warp
-  static constexpr int NSLOT = NW * SPW;
   static constexpr int KPLANE = TT * RW::KROW;
   static constexpr int KSZ_OFF = KPLANE;                      // only the upper/only plane is read
   static constexpr int KSZ_BYTES = (TT / 32) * 2 * D * 4;
   static constexpr int SLOT = KSZ_OFF + KSZ_BYTES;
-  static constexpr int QS_OFF = NSLOT * SLOT;                 // qs[D]
-  static constexpr int WB_OFF = QS_OFF + D * 4;               // per warp: W halves in pair order [2][D] f16
-  static constexpr int HIST_OFF = WB_OFF + NW * 2 * D * 2;    // hist[NW][256]: one per warp
-  static constexpr int LIST_OFF = HIST_OFF + NW * 256 * 4;    // gathered keys [kGather]
-  static constexpr int RED_OFF = LIST_OFF + kGather * 4;      // per-warp min/max, counts [2 NW]
-  static constexpr int BAR_OFF = RED_OFF + 2 * NW * 4;
-  static constexpr int MISC_OFF = BAR_OFF + NSLOT * 8;
-  static constexpr int SC_OFF = MISC_OFF + 64;                // order keys / merge keys (sized per launch)
-  static constexpr int MAX_SC = kTopkMaxCand * 16;            // >= kTopkMaxChunk * 4; two merge buffers
-  static constexpr int MAX_TOTAL = SC_OFF + MAX_SC;
-  static_assert(kTopkMaxChunk * 4 <= MAX_SC, "chunk scores must fit");
   static_assert(SLOT % 16 == 0, "slots must stay 16-byte aligned");
-  static_assert(BAR_OFF % 8 == 0, "mbarriers need 8-byte alignment");
-  static_assert(NSLOT * SLOT >= kMaxTopk * 8, "the split's winners reuse the stage area");
-  static_assert(NSLOT * SLOT >= 3 * NW * 128 * 8, "the candidates and the warps' sorted lists reuse the stage area");
 };
 
+// Shared-memory layout of one launch: the stage ring (or the scratch, if
+// larger), then the fixed parts, then the chunk's order keys (later the
+// CTA's own sorted list).
+struct TopkLayout {
+  int qs, wb, list, red, bar, misc, sc, total;
+};
+
+__host__ __device__ constexpr long long lmax(long long a, long long b) { return a > b ? a : b; }
+
 template <int MODE, int D>
-int smem_bytes(long long chunk, int S, int k) {
-  using L = TopkSmem<MODE, D>;
-  const long long sc = std::max(chunk * 4, static_cast<long long>(S) * k * 16);
-  return static_cast<int>(L::SC_OFF + ((sc + 15) / 16) * 16);
+__host__ __device__ inline TopkLayout topk_layout(bool pre, int spw, long long chunk, int k, int S) {
+  const int ring = pre ? kScratch : static_cast<int>(lmax(NW * spw * TopkTile<MODE, D>::SLOT, kScratch));
+  TopkLayout l;
+  l.qs = ring;                                   // qs[D]
+  l.wb = l.qs + D * 4;                           // per warp: W halves in pair order [2][D] f16
+  l.list = l.wb + NW * 2 * D * 2;                // gathered keys [kGather]
+  l.red = l.list + kGather * 4;                  // per-warp values [2 NW]
+  l.bar = l.red + 2 * NW * 4;                    // mbarriers [NW][kSpwMax]
+  l.misc = l.bar + NW * kSpwMax * 8;             // [0] abort, [1] last, [2..6] select state
+  l.sc = l.misc + 64;                            // order keys [chunk], then the sorted list [k] u64
+  long long sc = lmax(chunk * 4, static_cast<long long>(k) * 8);
+  if (k > 128) sc = lmax(sc, 2LL * S * k * 8);   // the merge-path tree's two buffers (k > 128)
+  l.total = l.sc + static_cast<int>((sc + 15) / 16) * 16;
+  return l;
 }
 
 __device__ __forceinline__ uint32_t order_key(float s) {
@@ -94,6 +125,10 @@ __device__ __forceinline__ float key_to_score(uint32_t k) {
 // better; 0 marks padding).
 __device__ __forceinline__ uint64_t composite(uint32_t okey, uint32_t idx) {
   return (static_cast<uint64_t>(okey) << 32) | (0xFFFFFFFFu - idx);
+}
+
+__device__ __forceinline__ int32_t composite_index(uint64_t key) {
+  return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
 }
 
 __device__ __forceinline__ float pow2f(int e) {  // 2^e for -126 <= e <= 127
@@ -122,7 +157,8 @@ __device__ __forceinline__ int pair_slot(int local) {
 // Sorts the warp's 128 keys into descending order.  Key x = 32 r + lane sits
 // in v[r]; the bitonic network pairs x with x ^ j (a shuffle for j < 32, a
 // register swap otherwise).
-__device__ __forceinline__ void warp_sort128_desc(uint64_t (&v)[4]) {
+template <typename T>
+__device__ __forceinline__ void warp_sort128_desc(T (&v)[4]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int k = 2; k <= 128; k <<= 1) {
@@ -132,9 +168,9 @@ __device__ __forceinline__ void warp_sort128_desc(uint64_t (&v)[4]) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const int x = 32 * r + lane;
-          const uint64_t o = __shfl_xor_sync(0xffffffffu, v[r], j);
+          const T o = __shfl_xor_sync(0xffffffffu, v[r], j);
           const bool desc = (x & k) == 0, lower = (x & j) == 0;
-          const uint64_t hi = v[r] > o ? v[r] : o, lo = v[r] > o ? o : v[r];
+          const T hi = v[r] > o ? v[r] : o, lo = v[r] > o ? o : v[r];
           v[r] = (lower == desc) ? hi : lo;
         }
       } else {
@@ -144,8 +180,8 @@ __device__ __forceinline__ void warp_sort128_desc(uint64_t (&v)[4]) {
           if (r & jr) continue;
           const int x = 32 * r + lane;
           const bool desc = (x & k) == 0;
-          const uint64_t a = v[r], b = v[r | jr];
-          const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+          const T a = v[r], b = v[r | jr];
+          const T hi = a > b ? a : b, lo = a > b ? b : a;
           v[r] = desc ? hi : lo;
           v[r | jr] = desc ? lo : hi;
         }
@@ -332,14 +368,76 @@ __device__ void select_kth(int n, int kth, F take, uint32_t* hist, uint32_t* lis
   }
 }
 
-// PRE: the scores come from the attention's scoring pass (p.pre holds
-// fp32(fp32(S_t) * unit) per token; this kernel adds beta); otherwise the
-// kernel streams and scores the key planes itself.
+// Top 32 KR of two sorted lists A and B (composite keys, 0 pads) in one warp.
+// a[r] holds A's position 32 r + lane (descending); b[r] holds position
+// 32 r + lane of B in ascending order, i.e. B's position 32 KR - 1 - (32 r +
+// lane), so that A then b is a bitonic sequence.  The half-cleaner keeps the
+// larger of each pair, which are the top 32 KR as a bitonic sequence, and the
+// bitonic merge network sorts them into a[] in descending order.
+template <int KR>
+__device__ __forceinline__ void warp_merge_top(uint64_t (&a)[KR], const uint64_t (&b)[KR]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < KR; ++r) a[r] = a[r] > b[r] ? a[r] : b[r];
+#pragma unroll
+  for (int jr = KR / 2; jr > 0; jr >>= 1) {
+#pragma unroll
+    for (int r = 0; r < KR; ++r) {
+      if (r & jr) continue;
+      const uint64_t x = a[r], y = a[r | jr];
+      a[r] = x > y ? x : y;
+      a[r | jr] = x > y ? y : x;
+    }
+  }
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+#pragma unroll
+    for (int r = 0; r < KR; ++r) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, a[r], j);
+      const bool lower = (lane & j) == 0;
+      a[r] = (lower == (a[r] > o)) ? a[r] : o;
+    }
+  }
+}
+
+// The top K (<= 32 KR) of S sorted lists (descending, 0 pads) of K composite
+// keys at M[S][K]: pairs of lists merge in warps, level by level, in place
+// (the pair (i, i + st) into list i).  Every thread of the block calls it;
+// the result is list 0.
+template <int KR>
+__device__ void warp_merge_tree(uint64_t* M, int S, int K) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int N = 32 * KR;
+  for (int st = 1; st < S; st *= 2) {
+    for (int i = 2 * st * warp; i + st < S; i += 2 * st * NW) {
+      uint64_t* A = M + static_cast<long long>(i) * K;
+      const uint64_t* B = M + static_cast<long long>(i + st) * K;
+      uint64_t a[KR], b[KR];
+#pragma unroll
+      for (int r = 0; r < KR; ++r) {
+        const int x = 32 * r + lane, y = N - 1 - x;
+        a[r] = x < K ? A[x] : 0ull;
+        b[r] = y < K ? B[y] : 0ull;
+      }
+      warp_merge_top<KR>(a, b);
+      __syncwarp();
+#pragma unroll
+      for (int r = 0; r < KR; ++r) {
+        const int x = 32 * r + lane;
+        if (x < K) A[x] = a[r];
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// PRE: the attention's scoring pass wrote the finished scores to p.pre;
+// otherwise the kernel streams and scores the key planes itself.
 template <int MODE, int D, bool PRE>
-__global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
+__global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
   using M = Mode<MODE>;
   using RW = Rows<MODE, D>;
-  using L = TopkSmem<MODE, D>;
+  using TL = TopkTile<MODE, D>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int g = lane >> 2, q = lane & 3;
@@ -347,6 +445,7 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   const int split = blockIdx.x % p.S;
   const int b = static_cast<int>(u / p.c.Hkv), kvh = static_cast<int>(u % p.c.Hkv);
   const int G = p.c.G;
+  const TopkLayout L = topk_layout<MODE, D>(PRE, p.spw, p.chunk, p.k, p.S);
   // a ragged cache splits each sequence's own length over the S splits, in
   // multiples of the plan's alignment
   const long long lq_b = seq_lq(p.c, b);
@@ -358,23 +457,23 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
   const int ntiles = PRE ? 0 : (n + M::TT - 1) / M::TT;   // a pre-scored launch streams nothing
   const int per_warp = (ntiles + NW - 1) / NW;
   const int K = p.k;
-  constexpr int SPW = L::SPW;
+  const int spw = p.spw;
 
-  uint32_t* okeys = reinterpret_cast<uint32_t*>(smem + L::SC_OFF);
-  float* qs = reinterpret_cast<float*>(smem + L::QS_OFF);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L::HIST_OFF);
-  uint32_t* list = reinterpret_cast<uint32_t*>(smem + L::LIST_OFF);
-  uint32_t* red = reinterpret_cast<uint32_t*>(smem + L::RED_OFF);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-  int* misc = reinterpret_cast<int*>(smem + L::MISC_OFF);   // [0] abort, [1] flag, [2..6] select state
+  uint32_t* okeys = reinterpret_cast<uint32_t*>(smem + L.sc);
+  float* qs = reinterpret_cast<float*>(smem + L.qs);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kHistOff);
+  uint32_t* list = reinterpret_cast<uint32_t*>(smem + L.list);
+  uint32_t* red = reinterpret_cast<uint32_t*>(smem + L.red);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar);
+  int* misc = reinterpret_cast<int*>(smem + L.misc);   // [0] abort, [1] last, [2..6] select state
   const long long u_tok = u * p.c.C;
   // this warp's tiles: a contiguous run of the chunk
   const int my_first = warp * per_warp;
   const int my_tiles = max(0, min(per_warp, ntiles - my_first));
-  // Each warp streams its own tiles: lane 0 puts tile j into slot j % SPW of
+  // Each warp streams its own tiles: lane 0 puts tile j into slot j % spw of
   // the warp's ring with 1-D bulk copies that complete on the slot's mbarrier.
   auto issue = [&](int j) {
-    const int slot = warp * SPW + (j % SPW);
+    const int slot = warp * spw + (j % spw);
     const int rel = (my_first + j) * M::TT;                 // chunk-relative first token
     const int nt = min(M::TT, n - rel);
     const long long t0 = t_begin + rel;
@@ -382,40 +481,20 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
     const bool new_grp = (j == 0) || (M::TT > G) || (t0 % G == 0);
     const uint32_t kb = nt * RW::KROW;
     const uint32_t kszb = new_grp ? static_cast<uint32_t>((nt + G - 1) / G) * 2 * D * 4 : 0u;
-    uint8_t* sbase = smem + slot * L::SLOT;
+    uint8_t* sbase = smem + slot * TL::SLOT;
+    uint64_t* bar = full + warp * kSpwMax + (j % spw);
     const uint64_t pol = policy_evict_first();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_arrive_expect_tx(full + slot, kb + kszb);
-    bulk_g2s(sbase, p.c.kplane[0] + (u_tok + t0) * RW::KROW, kb, full + slot, pol);
+    mbar_arrive_expect_tx(bar, kb + kszb);
+    bulk_g2s(sbase, p.c.kplane[0] + (u_tok + t0) * RW::KROW, kb, bar, pol);
     if (new_grp)
-      bulk_g2s(sbase + L::KSZ_OFF, p.c.ksz + (u * (p.c.C / G) + t0 / G) * 2 * D, kszb, full + slot, pol);
+      bulk_g2s(sbase + TL::KSZ_OFF, p.c.ksz + (u * (p.c.C / G) + t0 / G) * 2 * D, kszb, bar, pol);
   };
-  // the first heads' query values are loaded before the first copies issue
-  constexpr int kQPre = 8;
-  static_assert(D <= NTHREADS, "one query channel per thread");
-  uint16_t qpre[kQPre];
-  const long long qoff = static_cast<long long>(b) * p.q_bstride + static_cast<long long>(kvh) * p.HG * D + tid;
-#pragma unroll
-  for (int hh = 0; hh < kQPre; ++hh) qpre[hh] = (tid < D && hh < p.HG) ? p.q[qoff + hh * D] : 0;
-  if (lane == 0) {
-    for (int s2 = 0; s2 < SPW; ++s2) mbar_init(full + warp * SPW + s2, 1);
-    fence_mbar_init();
-    for (int j = 0; j < min(SPW, my_tiles); ++j) issue(j);
-  }
-  int issued = min(SPW, my_tiles), consumed = 0;
+  int issued = 0, consumed = 0;
   if (tid == 0) misc[0] = 0;
-  // summed query (ascending head order, fp32) while the first tiles load
-  if (tid < D) {
-    float acc = 0.f;
-#pragma unroll
-    for (int hh = 0; hh < kQPre; ++hh)
-      if (hh < p.HG) acc = __fadd_rn(acc, bf16_to_f32(qpre[hh]));
-    for (int hh = kQPre; hh < p.HG; ++hh) acc = __fadd_rn(acc, bf16_to_f32(p.q[qoff + hh * D]));
-    qs[tid] = acc;
-  }
-  __syncthreads();
   volatile int* abort_flag = misc;
   if constexpr (PRE) {
+    __syncthreads();
     // the attention's scoring pass wrote the finished scores: n is a multiple
     // of 128 tokens, so each thread takes float4 runs, all loads in flight
     static_assert(kTopkMaxChunk % (4 * NTHREADS) == 0, "whole float4 runs per thread");
@@ -437,9 +516,31 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
         okeys[4 * i4 + 3] = order_key(v[r].w);
       }
     }
-  }
+  } else {
+    // the first heads' query values are loaded before the first copies issue
+    constexpr int kQPre = 8;
+    static_assert(D <= NTHREADS, "one query channel per thread");
+    uint16_t qpre[kQPre];
+    const long long qoff = static_cast<long long>(b) * p.q_bstride + static_cast<long long>(kvh) * p.HG * D + tid;
+#pragma unroll
+    for (int hh = 0; hh < kQPre; ++hh) qpre[hh] = (tid < D && hh < p.HG) ? p.q[qoff + hh * D] : 0;
+    if (lane == 0) {
+      for (int s2 = 0; s2 < spw; ++s2) mbar_init(full + warp * kSpwMax + s2, 1);
+      fence_mbar_init();
+      for (int j = 0; j < min(spw, my_tiles); ++j) issue(j);
+    }
+    issued = min(spw, my_tiles);
+    // summed query (ascending head order, fp32) while the first tiles load
+    if (tid < D) {
+      float acc = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < kQPre; ++hh)
+        if (hh < p.HG) acc = __fadd_rn(acc, bf16_to_f32(qpre[hh]));
+      for (int hh = kQPre; hh < p.HG; ++hh) acc = __fadd_rn(acc, bf16_to_f32(p.q[qoff + hh * D]));
+      qs[tid] = acc;
+    }
+    __syncthreads();
 
-  {
     // B fragments: lane (g, q) holds column g of W for its channel chunk; only
     // columns 0 (hi) and 1 (lo) are nonzero.
     uint32_t wb[D / 8];
@@ -449,12 +550,12 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
     long long cur_grp = -1;
     const float smul = static_cast<float>(M::MULT);
     const float cbmul = static_cast<float>(1 << M::CB);
-    uint16_t* whalf = reinterpret_cast<uint16_t*>(smem + L::WB_OFF) + warp * 2 * D;   // [hi D][lo D], pair order
+    uint16_t* whalf = reinterpret_cast<uint16_t*>(smem + L.wb) + warp * 2 * D;   // [hi D][lo D], pair order
     constexpr int CPL = D / 32;   // channels per lane in the cooperative setup
     for (int j = 0; j < my_tiles; ++j) {
       const int ti = my_first + j;
-      const int slot = warp * SPW + (j % SPW);
-      if (!mbar_wait_bounded(full + slot, (j / SPW) & 1, p.wait_limit)) {
+      const int slot = warp * spw + (j % spw);
+      if (!mbar_wait_bounded(full + warp * kSpwMax + (j % spw), (j / spw) & 1, p.wait_limit)) {
         record_status(p.status, KVQ_ERR_DEVICE_TIMEOUT);
         *abort_flag = 1;
         break;
@@ -463,8 +564,8 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
       const long long t0 = t_begin + static_cast<long long>(ti) * M::TT;
       const int nt = static_cast<int>(min(static_cast<long long>(M::TT), t_end - t0));
       const long long g_first = t0 / G;
-      const uint8_t* sbase = smem + slot * L::SLOT;
-      const float* ksz = reinterpret_cast<const float*>(sbase + L::KSZ_OFF);
+      const uint8_t* sbase = smem + slot * TL::SLOT;
+      const float* ksz = reinterpret_cast<const float*>(sbase + TL::KSZ_OFF);
       for (int sl = 0; sl < nt / 32; ++sl) {
         const long long tok0 = t0 + 32 * sl;
         const long long grp = tok0 / G;
@@ -558,101 +659,110 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
     // after an abort: let this warp's copies still in flight land before exit
     if (lane == 0) {
       for (int jj = consumed; jj < issued; ++jj)
-        mbar_wait_bounded(full + warp * SPW + (jj % SPW), (jj / SPW) & 1, p.wait_limit);
+        mbar_wait_bounded(full + warp * kSpwMax + (jj % spw), (jj / spw) & 1, p.wait_limit);
     }
     __syncwarp();
   }
   __syncthreads();
 
-  // ---------------- the chunk's top k ----------------
+  // ---------------- the chunk's top k, sorted, into `mine` ----------------
   const int keff = min(K, n);
   int* st = misc + 2;  // st[0] T, st[1] remaining, st[2] ties taken, st[3] bin / count, st[4] gather count
-  float* cs = p.cand_score + (u * p.S + split) * K;
-  int32_t* ci = p.cand_idx + (u * p.S + split) * K;
-  // Sorted selection of the top K among m keys, m <= NW * 128 and K <= 128:
-  // warp w sorts keys [128 w, 128 w + 128) (key(i) gives the composite key of
-  // entry i; 0 pads), and the merge-path tree merges the warps' top-K lists.
-  // Warps past the last entry write padding without sorting.
-  auto sorted_select = [&](int m, auto key, uint64_t* area) {
-    const int nl = max(1, (m + 127) / 128);
-    uint64_t* la = area;                                   // [nl][K]
-    uint64_t* lb = la + NW * K;
-    if (warp < nl) {
-      uint64_t v[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int i = warp * 128 + 32 * r + lane;
-        v[r] = (i < m) ? key(i) : 0ull;
-      }
-      warp_sort128_desc(v);
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-        if (32 * r + lane < K) la[warp * K + 32 * r + lane] = v[r];
-    }
-    __syncthreads();
-    const uint64_t* top = merge_tree(la, lb, nl, K);
-    for (int i = tid; i < keff; i += blockDim.x) {
-      const uint64_t key2 = top[i];
-      cs[i] = key_to_score(static_cast<uint32_t>(key2 >> 32));
-      ci[i] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key2));
-    }
-  };
-  bool selected = false;
-  if (keff > 0 && n <= NW * 128 && K <= 128) {
-    // small chunk: sort all of it
-    sorted_select(n, [&](int i) { return composite(okeys[i], static_cast<uint32_t>(t_begin + i)); },
-                  reinterpret_cast<uint64_t*>(smem));
-    selected = true;
-  } else if (keff > 0 && K <= 128) {
-    // Long chunk: a lower bound first.  The keys fall into 128 strided segments
-    // (i mod 128); K segment maxima are K distinct keys, so the K-th largest
-    // segment maximum T0 is at most the K-th largest key.  The keys >= T0
-    // (about 1% of them when they are spread out) are then sorted exactly; if
-    // ties leave more than NW * 128 of them, the radix selection below runs.
-    uint32_t* segmax = hist;                                // [256], then [128]
-    {
+  uint64_t* mine = reinterpret_cast<uint64_t*>(smem + L.sc);   // [K] over the order keys, once they are read
+  uint64_t* pk = reinterpret_cast<uint64_t*>(smem + kPackOff);
+  bool selected = keff == 0;
+  if (keff > 0 && K <= 128) {
+    // ---- lower bound T0 (all keys when the chunk is short) ----
+    uint32_t T0 = 0u;
+    if (n > 2 * 128) {
+      uint32_t* segmax = hist;                              // [256]
       uint32_t mx = 0u;
       for (int i = tid; i < n; i += NTHREADS) mx = max(mx, okeys[i]);   // segment tid % 128
       segmax[tid] = mx;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      uint64_t v[4];
+      __syncthreads();
+      if (warp == 0) {
+        uint32_t v[4];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int sg = 32 * r + lane;
-        v[r] = static_cast<uint64_t>(max(segmax[sg], segmax[sg + 128])) << 32;
+        for (int r = 0; r < 4; ++r) {
+          const int sg = 32 * r + lane;
+          v[r] = max(segmax[sg], segmax[sg + 128]);
+        }
+        warp_sort128_desc(v);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          if (32 * r + lane == keff - 1) st[0] = static_cast<int>(v[r]);
       }
-      warp_sort128_desc(v);
-      const int kk = keff - 1;
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-        if (32 * r + lane == kk) st[0] = static_cast<int>(static_cast<uint32_t>(v[r] >> 32));
-      if (lane == 0) st[4] = 0;
+      __syncthreads();
+      T0 = static_cast<uint32_t>(st[0]);
     }
-    __syncthreads();
-    const uint32_t T0 = static_cast<uint32_t>(st[0]);
-    uint64_t* cand = reinterpret_cast<uint64_t*>(smem);     // [NW * 128] in the idle stage area
-    for (int base = warp * 32; base < n; base += NTHREADS) {
+    // ---- each warp's keys >= T0 into its region ----
+    uint64_t* reg = reinterpret_cast<uint64_t*>(smem + kRegOff) + warp * kRegion;
+    int cnt = 0;
+    for (int base = warp * 32; base < n; base += NTHREADS) {   // the same trip count in every lane
       const int i = base + lane;
       const uint32_t key = (i < n) ? okeys[i] : 0u;
       const bool take = (i < n) && key >= T0;
       const uint32_t bal = __ballot_sync(0xffffffffu, take);
-      int pos = 0;
-      if (lane == 0 && bal) pos = atomicAdd(st + 4, __popc(bal));
-      pos = __shfl_sync(0xffffffffu, pos, 0) + __popc(bal & ((1u << lane) - 1u));
-      if (take && pos < NW * 128) cand[pos] = composite(key, static_cast<uint32_t>(t_begin + i));
+      const int pos = cnt + __popc(bal & ((1u << lane) - 1u));
+      if (take && pos < kRegion) reg[pos] = composite(key, static_cast<uint32_t>(t_begin + i));
+      cnt += __popc(bal);
     }
+    if (lane == 0) red[warp] = static_cast<uint32_t>(cnt);
     __syncthreads();
-    const int ncand = st[4];
-    __syncthreads();
-    if (ncand <= NW * 128) {
-      sorted_select(ncand, [&](int i) { return cand[i]; }, cand + NW * 128);
+    int total = 0, off = 0;
+    bool over = false;
+    for (int w = 0; w < NW; ++w) {
+      const int c = static_cast<int>(red[w]);
+      off += (w < warp) ? c : 0;
+      total += c;
+      over = over || c > kRegion;
+    }
+    if (!over && total <= NW * kRegion) {
+      // ---- pack the regions ----
+      for (int j = lane; j < cnt; j += 32) pk[off + j] = reg[j];
+      if (tid == 0) {
+        pk[total] = 0ull;
+        pk[total + 1] = 0ull;
+      }
+      __syncthreads();
+      if (total <= NTHREADS) {
+        // ---- rank by counting: every composite key is unique ----
+        if (tid < total) {
+          const uint64_t x = pk[tid];
+          const ulonglong2* p2 = reinterpret_cast<const ulonglong2*>(pk);
+          int rank = 0;
+          for (int j = 0; j < (total + 1) / 2; ++j) {
+            const ulonglong2 y = p2[j];
+            rank += (y.x > x) + (y.y > x);
+          }
+          if (rank < keff) mine[rank] = x;
+        }
+      } else {
+        // ---- warp sorts of 128 and a merge-path tree ----
+        const int nl = (total + 127) / 128;
+        uint64_t* la = reinterpret_cast<uint64_t*>(smem + kListOff);   // [nl][K]
+        uint64_t* lb = la + NW * K;
+        if (warp < nl) {
+          uint64_t v[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int i = warp * 128 + 32 * r + lane;
+            v[r] = (i < total) ? pk[i] : 0ull;
+          }
+          warp_sort128_desc(v);
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            if (32 * r + lane < K) la[warp * K + 32 * r + lane] = v[r];
+        }
+        __syncthreads();
+        const uint64_t* top = merge_tree(la, lb, nl, K);
+        for (int i = tid; i < keff; i += NTHREADS) mine[i] = top[i];
+      }
       selected = true;
     }
   }
-  if (selected) {
-  } else if (keff > 0) {
+  if (!selected) {
+    // ---- radix selection of the k-th key, then the winners ranked ----
     select_kth(n, keff, [&](int i, uint32_t& key) { key = okeys[i]; return true; }, hist, list, red, st);
     const uint32_t T = static_cast<uint32_t>(st[0]);
     const int need_eq = st[2];
@@ -664,7 +774,7 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
     // keys above T anywhere in [0, n_gt), then the need_eq ties at T with the
     // lowest indices (each warp scans a contiguous segment, counts its ties,
     // and places its own after those of the warps before it).
-    uint64_t* wk = reinterpret_cast<uint64_t*>(smem);   // [keff], in the idle stage area
+    uint64_t* wk = pk;   // [keff]
     const int seg = (n + NW - 1) / NW;
     const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
     int myeq = 0;
@@ -695,8 +805,8 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
       taken += __popc(bal);
     }
     __syncthreads();
-    // the candidates in descending order (composite keys are unique): four
-    // lanes count the larger keys of one candidate
+    // the winners in descending order (composite keys are unique): four lanes
+    // count the larger keys of one winner
     for (int e0 = tid >> 2; e0 < ((keff + NW * 8 - 1) / (NW * 8)) * (NW * 8); e0 += NW * 8) {
       const int e = min(e0, keff - 1);
       const uint64_t key = wk[e];
@@ -704,87 +814,126 @@ __global__ void __launch_bounds__(NTHREADS) topk_kernel(TopkParams p) {
       for (int j = (tid & 3); j < keff; j += 4) rank += wk[j] > key;
       rank += __shfl_xor_sync(0xffffffffu, rank, 1);
       rank += __shfl_xor_sync(0xffffffffu, rank, 2);
-      if ((tid & 3) == 0 && e0 < keff) {
-        cs[rank] = key_to_score(static_cast<uint32_t>(key >> 32));
-        ci[rank] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
-      }
+      if ((tid & 3) == 0 && e0 < keff) mine[rank] = key;
     }
   }
-  for (int i = keff + tid; i < K; i += blockDim.x) {
-    cs[i] = neg_inf();
-    ci[i] = -1;
-  }
+  for (int i = keff + tid; i < K; i += NTHREADS) mine[i] = 0ull;
+  __syncthreads();
 
-  // ---------------- ticket: the last CTA of the unit merges ----------------
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned prev = atomicAdd(p.counters + u, 1u);
-    const int last = (prev == static_cast<unsigned>(p.S - 1));
-    if (last) atomicExch(p.counters + u, 0u);
-    misc[1] = last;
-  }
-  __syncthreads();
-  if (!misc[1]) return;
-  __threadfence();
-  // Each split's candidates are in descending order of the unique composite
-  // key (order key, ~index); padding is 0.  A merge-path tree halves the lists
-  // per level, each output keeping the top K of its two inputs.
-  const int NC = p.S * K;
-  uint64_t* ca = reinterpret_cast<uint64_t*>(okeys);   // [S][K]
-  uint64_t* cb = ca + NC;                              // [S][K]
-  const float* us = p.cand_score + u * p.S * K;
-  const int32_t* ui = p.cand_idx + u * p.S * K;
-  int cnt = 0;
-  for (int i0 = tid; i0 < NC; i0 += 4 * NTHREADS) {
-    int32_t idx[4];
-    float sc[4];
-#pragma unroll
-    for (int k2 = 0; k2 < 4; ++k2) {   // four candidates in flight per thread
-      const int i = i0 + k2 * NTHREADS;
-      idx[k2] = (i < NC) ? __ldcg(ui + i) : -1;
-      sc[k2] = (i < NC) ? __ldcg(us + i) : 0.f;
+  // ---------------- the unit's top k ----------------
+  if (p.S == 1) {
+    for (int i = tid; i < K; i += NTHREADS) {
+      const uint64_t x = mine[i];
+      const long long o = u * K + i;
+      p.idx_out[o] = x ? composite_index(x) : -1;
+      if (p.score_out) p.score_out[o] = x ? key_to_score(static_cast<uint32_t>(x >> 32)) : neg_inf();
     }
+    return;
+  }
+  // the unit's S lists: in the scratch for k <= 128, else in the order-key area
+  // (free once this CTA's list left it) with room for the merge-path tree
+  uint64_t* mb = reinterpret_cast<uint64_t*>(K <= 128 ? smem : smem + L.sc);   // [S][K]
+  if (p.cluster) {
+    // The lists stay in shared memory; the unit's first CTA copies them
+    // through distributed shared memory.  The second barrier keeps every
+    // CTA's list alive until the copy is done.
+    cluster_sync();
+    const bool leader = cluster_rank() == 0;
+    if (leader) {
+      for (int c = tid; c < p.S * K; c += NTHREADS)
+        mb[c] = ld_dsmem_u64(dsmem_addr(mine + c % K, static_cast<uint32_t>(c / K)));
+    }
+    __syncthreads();
+    cluster_sync();
+    if (!leader) return;
+  } else {
+    float* cs = p.cand_score + (u * p.S + split) * K;
+    int32_t* ci = p.cand_idx + (u * p.S + split) * K;
+    for (int i = tid; i < K; i += NTHREADS) {
+      const uint64_t x = mine[i];
+      cs[i] = x ? key_to_score(static_cast<uint32_t>(x >> 32)) : neg_inf();
+      ci[i] = x ? composite_index(x) : -1;
+    }
+    // ticket: the last CTA of the unit merges
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const unsigned prev = atomicAdd(p.counters + u, 1u);
+      const int last = (prev == static_cast<unsigned>(p.S - 1));
+      if (last) atomicExch(p.counters + u, 0u);
+      misc[1] = last;
+    }
+    __syncthreads();
+    if (!misc[1]) return;
+    __threadfence();
+    const int NC = p.S * K;
+    const float* us = p.cand_score + u * p.S * K;
+    const int32_t* ui = p.cand_idx + u * p.S * K;
+    for (int i0 = tid; i0 < NC; i0 += 4 * NTHREADS) {
+      int32_t idx[4];
+      float sc[4];
 #pragma unroll
-    for (int k2 = 0; k2 < 4; ++k2) {
-      const int i = i0 + k2 * NTHREADS;
-      if (i < NC) {
-        const bool ok = idx[k2] >= 0;
-        ca[i] = ok ? composite(order_key(sc[k2]), static_cast<uint32_t>(idx[k2])) : 0ull;
-        cnt += ok;
+      for (int k2 = 0; k2 < 4; ++k2) {   // four entries in flight per thread
+        const int i = i0 + k2 * NTHREADS;
+        idx[k2] = (i < NC) ? __ldcg(ui + i) : -1;
+        sc[k2] = (i < NC) ? __ldcg(us + i) : 0.f;
+      }
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2) {
+        const int i = i0 + k2 * NTHREADS;
+        if (i < NC) mb[i] = idx[k2] >= 0 ? composite(order_key(sc[k2]), static_cast<uint32_t>(idx[k2])) : 0ull;
       }
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-  if (lane == 0) red[warp] = static_cast<uint32_t>(cnt);
   __syncthreads();
-  int nvalid = 0;
-  for (int w = 0; w < NW; ++w) nvalid += static_cast<int>(red[w]);
-  const int kf = min(K, nvalid);
-  const uint64_t* src = merge_tree(ca, cb, p.S, K);
-  for (int i = tid; i < kf; i += blockDim.x) {
-    const uint64_t key = src[i];
+  const uint64_t* top = mb;
+  if (K <= 32) warp_merge_tree<1>(mb, p.S, K);
+  else if (K <= 64) warp_merge_tree<2>(mb, p.S, K);
+  else if (K <= 128) warp_merge_tree<4>(mb, p.S, K);
+  else top = merge_tree(mb, mb + p.S * K, p.S, K);
+  for (int i = tid; i < K; i += NTHREADS) {
+    const uint64_t x = top[i];
     const long long o = u * K + i;
-    p.idx_out[o] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
-    if (p.score_out) p.score_out[o] = key_to_score(static_cast<uint32_t>(key >> 32));
-  }
-  for (int i = kf + tid; i < K; i += blockDim.x) {
-    const long long o = u * K + i;
-    p.idx_out[o] = -1;
-    if (p.score_out) p.score_out[o] = neg_inf();
+    p.idx_out[o] = x ? composite_index(x) : -1;
+    if (p.score_out) p.score_out[o] = x ? key_to_score(static_cast<uint32_t>(x >> 32)) : neg_inf();
   }
 }
 
 template <int MODE, int D, bool PRE>
+int smem_t(const TopkParams& p) {
+  return topk_layout<MODE, D>(PRE, p.spw, p.chunk, p.k, p.S).total;
+}
+
+template <int MODE, int D, bool PRE>
+cudaError_t set_max_smem() {
+  const TopkLayout l = topk_layout<MODE, D>(PRE, kSpwMax, kTopkMaxChunk, kMaxTopk, kTopkMaxCand / kMaxTopk);
+  return set_smem_once(reinterpret_cast<const void*>(&topk_kernel<MODE, D, PRE>), l.total);
+}
+
+template <int MODE, int D, bool PRE>
 cudaError_t launch_t(const TopkParams& p, cudaStream_t s) {
-  const int smem = smem_bytes<MODE, D>(p.chunk, p.S, p.k);
-  cudaError_t e =
-      set_smem_once(reinterpret_cast<const void*>(&topk_kernel<MODE, D, PRE>), TopkSmem<MODE, D>::MAX_TOTAL);
+  const int smem = smem_t<MODE, D, PRE>(p);
+  cudaError_t e = set_max_smem<MODE, D, PRE>();
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.c.B) * p.c.Hkv * p.S;
-  topk_kernel<MODE, D, PRE><<<static_cast<unsigned>(grid), NTHREADS, smem, s>>>(p);
-  return cudaGetLastError();
+  if (!p.cluster) {
+    topk_kernel<MODE, D, PRE><<<static_cast<unsigned>(grid), NTHREADS, smem, s>>>(p);
+    return cudaGetLastError();
+  }
+  if (p.S < 2 || p.S > kClusterMax || p.k > 128) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute at{};
+  at.id = cudaLaunchAttributeClusterDimension;
+  at.val.clusterDim.x = static_cast<unsigned>(p.S);
+  at.val.clusterDim.y = 1;
+  at.val.clusterDim.z = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_kernel<MODE, D, PRE>, p);
 }
 
 template <int MODE>
@@ -795,86 +944,129 @@ cudaError_t launch_m(const TopkParams& p, bool pre, cudaStream_t s) {
 
 // CTAs per SM of one variant at `smem` bytes of dynamic shared memory, cached
 // per device in 1 KB steps (0 if unknown).
-template <int MODE, int D>
+template <int MODE, int D, bool PRE>
 int per_sm_t(int smem) {
   constexpr int kMaxDev = 64;
-  constexpr int kSteps = TopkSmem<MODE, D>::MAX_TOTAL / 1024 + 2;
+  constexpr int kSteps = 240;
   static int cached[kMaxDev][kSteps] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
   const int step = (smem + 1023) / 1024;
   if (step >= kSteps) return 0;
   if (cached[dev][step] > 0) return cached[dev][step];
-  if (set_smem_once(reinterpret_cast<const void*>(&topk_kernel<MODE, D, false>), TopkSmem<MODE, D>::MAX_TOTAL) !=
-      cudaSuccess)
-    return 0;
+  if (set_max_smem<MODE, D, PRE>() != cudaSuccess) return 0;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<MODE, D, false>, NTHREADS, step * 1024) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<MODE, D, PRE>, NTHREADS, step * 1024) !=
       cudaSuccess)
     return 0;
   cached[dev][step] = per_sm;
   return per_sm;
 }
 
+// Clusters of `size` CTAs of one variant at `smem` bytes that fit on the
+// device at once, cached per device, size and 1 KB step (0: none or unknown).
+template <int MODE, int D, bool PRE>
+int clusters_t(int size, int smem) {
+  constexpr int kMaxDev = 64;
+  constexpr int kSteps = 240;
+  static int cached[kMaxDev][kClusterMax + 1][kSteps] = {};   // 0: not queried, -1: none
+  int dev = 0;
+  if (size < 2 || size > kClusterMax) return 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  const int step = (smem + 1023) / 1024;
+  if (step >= kSteps) return 0;
+  int& c = cached[dev][size][step];
+  if (c != 0) return c > 0 ? c : 0;
+  if (set_max_smem<MODE, D, PRE>() != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(size), 1, 1);
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(step) * 1024;
+  cudaLaunchAttribute at{};
+  at.id = cudaLaunchAttributeClusterDimension;
+  at.val.clusterDim.x = static_cast<unsigned>(size);
+  at.val.clusterDim.y = 1;
+  at.val.clusterDim.z = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, topk_kernel<MODE, D, PRE>, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    c = -1;
+    return 0;
+  }
+  c = n;
+  return n;
+}
+
 long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
 
 // Split plan: over S from the fewest splits the chunk limit allows to the most
 // that the candidate limit and the chunk alignment allow, minimise
-// waves x (chunk + fixed per-CTA cost) + merge cost.  Chunks are multiples of
-// NW x max(G, tile) tokens, so each consumer warp scores whole key groups.
+// waves x (chunk x per-token cost + fixed per-CTA cost) + merge cost.  Chunks
+// are multiples of NW x max(G, tile) tokens, so each consumer warp scores
+// whole key groups.  The streaming variant keeps kSpwMax tiles per warp in
+// flight when two CTAs still fit on an SM, else two.
 template <int MODE>
 long long align_t(int G) {
   return std::max<long long>(kChunkAlign, static_cast<long long>(NW) * std::max(G, Mode<MODE>::TT));
 }
 
-template <int MODE, int D>
-int plan_t(long long Lq, long long U, int G, int k, long long* chunk_out) {
+template <int MODE, int D, bool PRE>
+TopkPlan plan_t(long long Lq, long long U, int G, int k) {
+  constexpr int kTwoPerSm = 112 * 1024;   // dynamic shared memory that still lets two CTAs share an SM
   const long long align = align_t<MODE>(G);
   const long long s_lo = std::max(1LL, ceil_div_ll(Lq, kTopkMaxChunk));
   const long long s_hi = std::max(s_lo, std::min(ceil_div_ll(Lq, align), static_cast<long long>(kTopkMaxCand / k)));
   const int sms = device_sm_count();
-  long long best_s = 0, best_ch = 0;
+  const double per_token = PRE ? 0.125 : 1.0;
+  TopkPlan best{0, 0, 2, 0};
   double best_cost = 0.0;
   for (long long S = s_lo; S <= s_hi; ++S) {
     const long long ch = ceil_div_ll(ceil_div_ll(Lq, S), align) * align;
     if (ch > kTopkMaxChunk && S < s_hi) continue;
     const long long s_eff = ceil_div_ll(Lq, ch);
     if (s_eff != S) continue;
-    const int per_sm = per_sm_t<MODE, D>(smem_bytes<MODE, D>(ch, static_cast<int>(S), k));
+    int spw = kSpwMax;
+    if (!PRE && topk_layout<MODE, D>(false, spw, ch, k, static_cast<int>(S)).total > kTwoPerSm) spw = 2;
+    const int smem = topk_layout<MODE, D>(PRE, spw, ch, k, static_cast<int>(S)).total;
+    const int per_sm = per_sm_t<MODE, D, PRE>(smem);
     const long long slots = (per_sm > 0 && sms > 0) ? static_cast<long long>(per_sm) * sms : target_ctas();
     const long long waves = ceil_div_ll(U * S, slots);
-    const double cost = static_cast<double>(waves) * static_cast<double>(ch + 1024) + 0.25 * static_cast<double>(S * k);
-    if (best_s == 0 || cost < best_cost) {
-      best_s = S;
-      best_ch = ch;
+    const double cost = static_cast<double>(waves) * (static_cast<double>(ch) * per_token + 1024.0) +
+                        0.25 * static_cast<double>(S * k);
+    if (best.S == 0 || cost < best_cost) {
+      best = TopkPlan{static_cast<int>(S), ch, spw, 0};
       best_cost = cost;
     }
   }
-  if (best_s == 0) {  // the chunk limit alone
-    best_ch = std::min<long long>(kTopkMaxChunk, ceil_div_ll(ceil_div_ll(Lq, s_lo), kChunkAlign) * kChunkAlign);
-    best_s = ceil_div_ll(Lq, best_ch);
+  if (best.S == 0) {  // the chunk limit alone
+    best.chunk = std::min<long long>(kTopkMaxChunk, ceil_div_ll(ceil_div_ll(Lq, s_lo), kChunkAlign) * kChunkAlign);
+    best.S = static_cast<int>(ceil_div_ll(Lq, best.chunk));
+    best.spw = 2;
   }
-  *chunk_out = best_ch;
-  return static_cast<int>(best_s);
+  if (best.S >= 2 && best.S <= kClusterMax && k <= 128) {
+    const int smem = topk_layout<MODE, D>(PRE, best.spw, best.chunk, k, best.S).total;
+    best.cluster = clusters_t<MODE, D, PRE>(best.S, smem) > 0 ? 1 : 0;
+  }
+  return best;
+}
+
+template <int MODE>
+TopkPlan plan_m(int D, long long Lq, long long U, int G, int k, bool pre) {
+  if (D == 128) return pre ? plan_t<MODE, 128, true>(Lq, U, G, k) : plan_t<MODE, 128, false>(Lq, U, G, k);
+  return pre ? plan_t<MODE, 64, true>(Lq, U, G, k) : plan_t<MODE, 64, false>(Lq, U, G, k);
 }
 
 }  // namespace
 
-int topk_plan(int mode, int D, int G, long long Lq, long long U, int k, long long* chunk) {
-  if (Lq <= 0) {
-    *chunk = 0;
-    return 1;
-  }
+TopkPlan topk_plan(int mode, int D, int G, long long Lq, long long U, int k, bool pre) {
+  if (Lq <= 0) return TopkPlan{1, 0, 2, 0};
   switch (mode) {
-    case KVQ_MODE_INT4:
-      return D == 128 ? plan_t<KVQ_MODE_INT4, 128>(Lq, U, G, k, chunk) : plan_t<KVQ_MODE_INT4, 64>(Lq, U, G, k, chunk);
-    case KVQ_MODE_INT2:
-      return D == 128 ? plan_t<KVQ_MODE_INT2, 128>(Lq, U, G, k, chunk) : plan_t<KVQ_MODE_INT2, 64>(Lq, U, G, k, chunk);
-    case KVQ_MODE_INT1:
-      return D == 128 ? plan_t<KVQ_MODE_INT1, 128>(Lq, U, G, k, chunk) : plan_t<KVQ_MODE_INT1, 64>(Lq, U, G, k, chunk);
-    default:
-      *chunk = 0;
-      return 0;
+    case KVQ_MODE_INT4: return plan_m<KVQ_MODE_INT4>(D, Lq, U, G, k, pre);
+    case KVQ_MODE_INT2: return plan_m<KVQ_MODE_INT2>(D, Lq, U, G, k, pre);
+    case KVQ_MODE_INT1: return plan_m<KVQ_MODE_INT1>(D, Lq, U, G, k, pre);
+    default: return TopkPlan{0, 0, 2, 0};
   }
 }
 

@@ -290,6 +290,34 @@ def test_topk_matches_oracle(case):
     np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), ref_sc.view(np.uint32))
 
 
+@pytest.mark.parametrize("pattern,mode,G,N,k", [
+    ("zero_query", "int4", 128, 9000, 64),     # every score equal: every key passes the lower bound
+    ("zero_query", "int2", 32, 700, 17),
+    ("two_keys", "int4", 128, 9000, 64),       # half of the tokens tie at the top score
+    ("two_keys", "int2", 32, 3000, 100),
+    ("two_keys", "int1", 64, 2000, 128),
+])
+def test_topk_heavy_ties(pattern, mode, G, N, k):
+    """Massive score ties: the selection's lower bound admits far more
+    candidates than k (a whole chunk, or half of it), so the sorted and the
+    radix fallbacks run; ties still go to the lowest index, as in the oracle."""
+    B, Hkv, Hq, D = 1, 2, 4, 128
+    fmt = kvq.MODE_FORMAT[mode]
+    K, V = ki.kv_stream(13, B, Hkv, N, D)
+    if pattern == "two_keys":
+        K[:, :, 2::2] = K[:, :, 0:1]
+        K[:, :, 3::2] = K[:, :, 1:2]
+    gc, oc = build_pair(fmt, B, Hkv, D, G, (N // G + 1) * G, K, V, [N])
+    qspec = ki.queries(13, B, 1, Hq, D)[:, 0]
+    if pattern == "zero_query":
+        qspec = np.zeros_like(qspec)
+    ref_idx, ref_sc = oracle.topk(oc, mode, qspec, k)
+    idx, sc = kvq.kvq_topk(gc, mode, dev(qspec), k)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), ref_sc.view(np.uint32))
+
+
 def test_topk_then_attend_specache_step():
     """One SpeCache step: top-k from the speculative token (query row 1), then
     attention that uses those tokens at 16 bits.  Both match the oracle."""
