@@ -905,13 +905,8 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
     }
 
     uint32_t W[NT][NPK];                 // weights: this lane's B column part, per key pair
-    uint32_t WS[SC ? NPK : 1];           // scoring: integer weight parts (columns 0..2), per key pair
     float sc_unit = 0.f;                 // scoring: 2^(e-21) of the current group
     float sc_beta = 0.f;                 // scoring: the group's zero-point term
-    if constexpr (SC) {
-#pragma unroll
-      for (int pp = 0; pp < NPK; ++pp) WS[pp] = 0u;
-    }
     float cinit[NT];                     // accumulator start (correction x 2^e) for row 4nt + q
     float kscale = 1.f;                  // 2^-e of the current group
     float o[D / 16][4];                  // O^T, channel m-tile x (col 2q, 2q+1)
@@ -1165,15 +1160,6 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
               for (int k3 = 0; k3 < 3; ++k3) whs[k3 * (D / 2) + word] = part[k3];
             }
             __syncwarp();
-            if (g < 3) {
-              const uint4* src = reinterpret_cast<const uint4*>(whs + g * (D / 2) + q * (D / 8));
-#pragma unroll
-              for (int v4 = 0; v4 < NPK / 4; ++v4) {
-                const uint4 x4 = src[v4];
-                WS[4 * v4] = x4.x; WS[4 * v4 + 1] = x4.y; WS[4 * v4 + 2] = x4.z; WS[4 * v4 + 3] = x4.w;
-              }
-            }
-            __syncwarp();
           }
         }
         const uint8_t* kslab = sbase + L::K_OFF + (32 * sl) * RW::KROW + q * RW::KCHUNK;
@@ -1206,11 +1192,17 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
             // ---- the top-k score of the m-tile's tokens, from the same key fragments ----
             // columns 0, 1 (lanes q = 0) hold the h and m parts, column 2 (lanes
             // q = 1) the l part; S_t = 2^14 S_h + 2^7 S_m + S_l exactly in 64 bits
+            // lane (g, q) reads column g of the weight parts (zero past column 2)
+            // from the warp's staging area at each k-step: no registers held
+            // across the slab
             float cs[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint2* wsrc = reinterpret_cast<const uint2*>(
+                reinterpret_cast<const uint32_t*>(smem + L::SW_OFF) + warp * 3 * (D / 2) + min(g, 2) * (D / 2) + q * (D / 8));
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
               const uint32_t a[4] = {PA[2 * kk], PB[2 * kk], PA[2 * kk + 1], PB[2 * kk + 1]};
-              mma16816(cs, a, WS[2 * kk], WS[2 * kk + 1]);
+              const uint2 w2 = wsrc[kk];
+              mma16816(cs, a, g < 3 ? w2.x : 0u, g < 3 ? w2.y : 0u);
             }
             const float lA = __shfl_down_sync(0xffffffffu, cs[0], 1);
             const float lB = __shfl_down_sync(0xffffffffu, cs[2], 1);
