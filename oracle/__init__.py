@@ -7,6 +7,7 @@ computes and which passage of the pages it follows.
 """
 from .kvq_oracle import (  # noqa: F401
     FORMAT_BITS,
+    CENTER_SHIFT,
     MID_NIBBLE,
     MODES,
     SLAB,

@@ -46,11 +46,20 @@ MODES = {
     "int4mid": ("hier8", 4, 16),
     "int2": ("int2", 2, 1),
     "int1": ("int1", 1, 1),
+    "int1c": ("int1", 1, 0.5),
 }
 # The midpoint reading of the INT4 draft code: the upper nibble hi stands for
 # the 8-bit codes 16 hi .. 16 hi + 15, and "int4mid" reconstructs it at the
 # middle of that range, 16 hi + MID_NIBBLE, instead of at its bottom.
 MID_NIBBLE = 8
+# The centred reading of the 1-bit KIVI code (SpeCache page, Approach: 1-bit
+# KIVI gets a new zero point and scale; the pages give no formula).  Plain
+# 1-bit min/max puts the two levels at the group's min and max.  "int1c"
+# reads the same codes (1 above the midpoint of [min, max]) with the levels at
+# the centres of the two halves, min + r/4 and min + 3r/4 (r = max - min, the
+# stored scale): zero point z + CENTER_SHIFT s and scale s/2.  For values
+# spread evenly over [min, max] that cuts the mean squared error by four.
+CENTER_SHIFT = 0.25
 SLAB = 32  # tokens per value-plane slab (storage layout, see pack_v_plane)
 
 
@@ -119,7 +128,8 @@ def mode_codes_scale(mode: str, codes: np.ndarray, scale: np.ndarray):
     upper nibble, with 16 x scale.  So INT4 dequant equals INT8 dequant with the
     lower nibble zeroed (QuantSpec page, Approach).  INT4-mid reads the same
     nibble and scale (its zero point moves, see mode_zero).  INT2/INT1 read
-    their own codes and scale.
+    their own codes and scale; INT1-centred reads the 1-bit codes with half
+    the scale.
     """
     _, _, mult = MODES[mode]
     if mode in ("int4", "int4mid"):
@@ -131,10 +141,13 @@ def mode_zero(mode: str, zero: np.ndarray, scale: np.ndarray) -> np.ndarray:
     """The zero point a read mode sees, in fp64.  INT4-mid adds MID_NIBBLE
     steps of the 8-bit scale, so that its dequant equals INT8 dequant with the
     lower nibble set to MID_NIBBLE: (16 hi + 8) s + z = hi (16 s) + (z + 8 s).
-    Every other mode reads the stored zero point."""
+    INT1-centred adds a quarter of the 1-bit scale (the range).  Every other
+    mode reads the stored zero point."""
     z = zero.astype(np.float64)
     if mode == "int4mid":
         return z + MID_NIBBLE * scale.astype(np.float64)
+    if mode == "int1c":
+        return z + CENTER_SHIFT * scale.astype(np.float64)
     return z
 
 
@@ -447,7 +460,8 @@ def score_group_inputs(cache: "OracleCache", mode: str, b: int, h: int, g: int):
     """(codes, effective scale, zero point) of key group g of (b, kv head h) as
     the top-k score reads them, all fp32: INT4 and INT4-mid read the upper
     nibble with fp32(16 s); INT4-mid's zero point is fp32(z + fp32(8 s)), one
-    rounding (8 s is exact)."""
+    rounding (8 s is exact).  INT1-centred reads fp32(s / 2) and
+    fp32(z + fp32(s / 4)) (both products exact)."""
     G = cache.G
     codes = cache.k_codes[b, h, g * G:(g + 1) * G]
     s = cache.k_scale[b, h, g].astype(F32)
@@ -457,6 +471,9 @@ def score_group_inputs(cache: "OracleCache", mode: str, b: int, h: int, g: int):
     if mode in ("int4", "int4mid"):
         codes = codes >> 4
         s = (s * F32(16)).astype(F32)
+    if mode == "int1c":
+        z = (z + (F32(CENTER_SHIFT) * s).astype(F32)).astype(F32)
+        s = (s * F32(0.5)).astype(F32)
     return codes, s, z
 
 

@@ -26,6 +26,10 @@ MUTATIONS = [
     ("INT4 midpoint at 7 instead of 8", "MID_NIBBLE = 8", "MID_NIBBLE = 7"),
     ("INT4 midpoint zero point left unmoved in the top-k score",
      "        z = (z + (F32(MID_NIBBLE) * s).astype(F32)).astype(F32)", "        z = z"),
+    ("1-bit centred levels at a half of the range instead of a quarter", "CENTER_SHIFT = 0.25", "CENTER_SHIFT = 0.5"),
+    ("1-bit centred reading without the halved scale", '"int1c": ("int1", 1, 0.5),', '"int1c": ("int1", 1, 1),'),
+    ("1-bit centred zero point left unmoved in the top-k score",
+     "        z = (z + (F32(CENTER_SHIFT) * s).astype(F32)).astype(F32)", "        z = z"),
     ("causal offset off by one", "nvis = (P - gamma + i + 1) if P else 0", "nvis = (P - gamma + i) if P else 0"),
     ("strided instead of consecutive GQA grouping", "hq = h * hg + hh", "hq = hh * H + h"),
     ("flush one token early", "if self.r == 2 * self.G:", "if self.r == 2 * self.G - 1:"),

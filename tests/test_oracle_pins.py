@@ -286,8 +286,74 @@ def test_int4mid_topk_zero_point_moves_by_eight_steps():
     np.testing.assert_array_equal(mid.view(np.uint32), moved.view(np.uint32))
 
 
+def test_int1c_levels_golden():
+    """The centred 1-bit reading on a hand-worked key group: one channel over
+    G = 32 tokens holds -1 (token 0), 3 (token 1) and 0 elsewhere.  Stored:
+    min -1, scale (range) 4; codes round((x + 1) / 4): -1 -> 0, 0 -> 0 (0.25
+    rounds down), 3 -> 1.  Plain 1-bit reads the levels -1 and 3; the centred
+    reading reads -1 + 4/4 = 0 and -1 + 3 * 4/4 = 2, so the zeros come back
+    exact and the outliers at 0 and 2.  Catches a shift of a half (levels 1
+    and 3), an unhalved scale (0 and 4), and codes that moved."""
+    G, D = 32, 64
+    K = np.zeros((1, 1, 2 * G, D), F32)              # the first group flushes once 2G tokens arrived
+    V = np.zeros((1, 1, 2 * G, D), F32)
+    K[0, 0, 0, 5], K[0, 0, 1, 5] = -1.0, 3.0
+    c = _cache_from_tokens("int1", G, K, V)
+    assert c.Lq == G
+    assert c.k_zero[0, 0, 0, 5] == F32(-1) and c.k_scale[0, 0, 0, 5] == F32(4)
+    assert list(c.k_codes[0, 0, :3, 5]) == [0, 1, 0]
+    k1, _ = c.dequant_unit("int1", 0, 0)
+    kc, _ = c.dequant_unit("int1c", 0, 0)
+    assert list(k1[:3, 5]) == [-1.0, 3.0, -1.0]
+    assert list(kc[:3, 5]) == [0.0, 2.0, 0.0]
+    assert np.all(kc[2:, 5] == 0.0)
+    assert np.all(kc[:, :5] == 0.0)                    # constant channels stay exact
+
+
+def test_int1c_quarters_the_error_on_evenly_spread_values():
+    """For values spread evenly over [min, max] the two halves' centres are the
+    best two levels given the midpoint threshold: the mean squared error drops
+    from r^2/12 (levels at min and max) to r^2/48."""
+    G, D = 32, 64
+    g = ki.rng(71, 0)
+    vals = np.linspace(0.0, 1.0, G, dtype=np.float64)
+    K = np.stack([g.permutation(vals) for _ in range(D)], axis=1)[None, None].astype(F32)
+    K = np.concatenate([K, K], axis=2)                 # 2G tokens: the first group flushes
+    c = _cache_from_tokens("int1", G, K, np.zeros_like(K))
+    assert c.Lq == G
+    k1, _ = c.dequant_unit("int1", 0, 0)
+    kc, _ = c.dequant_unit("int1c", 0, 0)
+    e1 = float(np.mean((k1 - K[0, 0, :G]) ** 2))
+    ec = float(np.mean((kc - K[0, 0, :G]) ** 2))
+    # the 32 evenly spaced points make the ratio slightly above a quarter
+    assert 0.2 < ec / e1 < 0.3
+
+
+def test_int1c_is_int1_with_moved_levels():
+    """Attention under the centred reading equals plain 1-bit attention on a
+    cache whose zero points were moved by a quarter of the scale and whose
+    scales were halved by hand; the top-k score reads the same fp32 zero point
+    z + s/4 and scale s/2."""
+    G, D, N = 32, 64, 4 * 32 + 9
+    K, V = ki.kv_stream(23, 1, 2, N, D)
+    c = _cache_from_tokens("int1", G, K, V)
+    q = ki.queries(23, 1, 2, 4, D)
+    out_c, lse_c = oracle.attend(c, "int1c", q)
+    sc_c = oracle.all_scores(c, "int1c", q[:, 1], 0, 1)
+    L = c.Lq
+    c.k_zero[:, :, :L // G] = (c.k_zero[:, :, :L // G] + F32(0.25) * c.k_scale[:, :, :L // G]).astype(F32)
+    c.k_scale[:, :, :L // G] = (c.k_scale[:, :, :L // G] * F32(0.5)).astype(F32)
+    c.v_zero[:, :, :L] = (c.v_zero[:, :, :L] + F32(0.25) * c.v_scale[:, :, :L]).astype(F32)
+    c.v_scale[:, :, :L] = (c.v_scale[:, :, :L] * F32(0.5)).astype(F32)
+    out_1, lse_1 = oracle.attend(c, "int1", q)
+    sc_1 = oracle.all_scores(c, "int1", q[:, 1], 0, 1)
+    np.testing.assert_allclose(out_c, out_1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse_c, lse_1, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(sc_c.view(np.uint32), sc_1.view(np.uint32))
+
+
 @pytest.mark.parametrize("mode,fmt,G", [("int8", "hier8", 32), ("int4", "hier8", 32), ("int4mid", "hier8", 64),
-                                        ("int2", "int2", 32), ("int1", "int1", 64)])
+                                        ("int2", "int2", 32), ("int1", "int1", 64), ("int1c", "int1", 32)])
 def test_attention_equals_library_sdpa(mode, fmt, G):
     """The oracle equals torch's fp64 SDPA on the same key/value lists, for GQA
     with causal pending tokens and selected 16-bit overrides.  Catches a
