@@ -80,14 +80,20 @@ typedef enum kvq_format {
  * stands for: its dequant equals INT8 dequant with the lower nibble set to 8,
  * i.e. zero point z + 8 s with the 8-bit scale s (the pages do not say where
  * the draft value lies; this halves the worst-case draft error, 8.5 steps of
- * s against 15.5).  INT2 and INT1 read their own format.  Any other pairing
- * returns KVQ_ERR_UNSUPPORTED. */
+ * s against 15.5).  INT2 and INT1 read their own format.  INT1_CENTER reads
+ * KVQ_FMT_INT1 with the levels at the centres of the two halves of each
+ * group's [min, max]: zero point z + s/4 and scale s/2, with the stored 1-bit
+ * scale s = max - min and the same codes (SpeCache page, "Approach", gives
+ * 1-bit KIVI a new zero point and scale but no formula; this is the library's
+ * reading: for values spread evenly over the range it cuts the mean squared
+ * error by four).  Any other pairing returns KVQ_ERR_UNSUPPORTED. */
 typedef enum kvq_mode {
   KVQ_MODE_INT8 = 0,
   KVQ_MODE_INT4 = 1,
   KVQ_MODE_INT2 = 2,
   KVQ_MODE_INT1 = 3,
-  KVQ_MODE_INT4_MID = 4
+  KVQ_MODE_INT4_MID = 4,
+  KVQ_MODE_INT1_CENTER = 5
 } kvq_mode;
 
 typedef struct kvq_cache_desc {
@@ -291,7 +297,7 @@ kvq_status kvq_attend(const kvq_cache* cache, kvq_mode mode, const void* q, int3
  * 0: the output token, the non-speculative variant) while it streams the keys,
  * and a selection pass then picks the next_k best per KV head.
  *  All kvq_attend arguments, with kvq_attend's meaning and results (out, lse).
- *  mode        KVQ_MODE_INT4, INT4_MID, INT2 or INT1 (INT8 returns
+ *  mode        KVQ_MODE_INT4, INT4_MID, INT2, INT1 or INT1_CENTER (INT8 returns
  *              KVQ_ERR_UNSUPPORTED: the hierarchical cache is ranked by its
  *              4-bit draft code).
  *  score_row   0 <= score_row < gamma.
@@ -337,8 +343,10 @@ kvq_status kvq_attend_plan(const kvq_cache* cache, kvq_mode mode, int32_t num_q_
  * low-bit keys for the speculative token's query (SpeCache page, "Approach").
  * The query heads sharing a KV head are summed in fp32, in ascending head order.
  * Per key group g the score is exact up to stated roundings:
- *   w_d = fp32(qs_d * s_d)   (s = the mode's key scale: x16 for INT4 and INT4_MID;
- *                            INT4_MID's zero point is fp32(zero_d + 8 s_d))
+ *   w_d = fp32(qs_d * s_d)   (s = the mode's key scale: x16 for INT4 and INT4_MID,
+ *                            x1/2 for INT1_CENTER; INT4_MID's zero point is
+ *                            fp32(zero_d + 8 s_d), INT1_CENTER's fp32(zero_d + s_d/4)
+ *                            with the stored scale s_d)
  *   e   = exponent with max_d|w_d| < 2^e, floored at -100
  *   W_d = rint(w_d * 2^(21-e)),  S_t = sum_d W_d * code_{t,d} (exact integer)
  *   p_d = fp32(qs_d * zero_d), f = exponent with max_d|p_d| < 2^f, floored at -80
@@ -346,7 +354,8 @@ kvq_status kvq_attend_plan(const kvq_cache* cache, kvq_mode mode, int32_t num_q_
  *   score_t = fp32(fp32(fp32(S_t) * 2^(e-21)) + beta)
  * Tokens are ordered by (score descending, index ascending).  Positions beyond
  * Lq get index -1 and score -inf.
- *  mode     KVQ_MODE_INT4, INT4_MID, INT2 or INT1 (INT8 returns KVQ_ERR_UNSUPPORTED).
+ *  mode     KVQ_MODE_INT4, INT4_MID, INT2, INT1 or INT1_CENTER (INT8 returns
+ *           KVQ_ERR_UNSUPPORTED).
  *  q_spec   bf16 [B][Hq][D].
  *  idx_out  int32 [B][Hkv][top_k], in that order.  score_out fp32, same shape,
  *           or NULL.

@@ -24,8 +24,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
 
 FORMATS = {"hier8": 8, "int2": 2, "int1": 1}
-MODES = {"int8": 0, "int4": 1, "int2": 2, "int1": 3, "int4mid": 4}
-MODE_FORMAT = {"int8": "hier8", "int4": "hier8", "int2": "int2", "int1": "int1", "int4mid": "hier8"}
+MODES = {"int8": 0, "int4": 1, "int2": 2, "int1": 3, "int4mid": 4, "int1c": 5}
+MODE_FORMAT = {"int8": "hier8", "int4": "hier8", "int2": "int2", "int1": "int1", "int4mid": "hier8", "int1c": "int1"}
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_CAPACITY",
           4: "KVQ_ERR_WORKSPACE", 5: "KVQ_ERR_CUDA", 6: "KVQ_ERR_DEVICE_TIMEOUT",
           7: "KVQ_ERR_NOT_INITIALIZED"}

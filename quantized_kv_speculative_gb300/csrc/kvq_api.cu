@@ -203,7 +203,8 @@ bool mode_reads(int mode, int fmt) {
     case KVQ_MODE_INT4:
     case KVQ_MODE_INT4_MID: return fmt == KVQ_FMT_HIER8;
     case KVQ_MODE_INT2: return fmt == KVQ_FMT_INT2;
-    case KVQ_MODE_INT1: return fmt == KVQ_FMT_INT1;
+    case KVQ_MODE_INT1:
+    case KVQ_MODE_INT1_CENTER: return fmt == KVQ_FMT_INT1;
     default: return false;
   }
 }
@@ -287,6 +288,7 @@ AttendParams make_attend_params(const kvq_cache* cache, int mode, const void* q,
   p.top_k = top_k;
   p.qscale = sm_scale * 1.4426950408889634f;
   p.zshift = mode_zero_shift(mode);
+  p.smul = mode_scale_mul(mode);
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   const long long U = units_of(cache);
@@ -315,6 +317,7 @@ TopkParams make_topk_params(const kvq_cache* cache, int mode, const uint16_t* q,
   p.HG = num_q_heads / cache->desc.num_kv_heads;
   p.k = k;
   p.zshift = mode_zero_shift(mode);
+  p.smul = mode_scale_mul(mode);
   p.align = topk_align(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size);
   p.idx_out = idx_out;
   p.score_out = score_out;

@@ -784,7 +784,8 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
   const int per_warp = (ntiles + NW - 1) / NW;
   constexpr int NPK = D / 8;          // key pairs per lane chunk
   constexpr int KSTEPS = D / 16;
-  constexpr float MULT = static_cast<float>(M::MULT);   // INT4 reads the upper nibble: step 16 scale
+  // INT4 reads the upper nibble: step 16 scale; the centred 1-bit reading halves the scale
+  const float MULT = (MODE == KVQ_MODE_INT1) ? p.smul : static_cast<float>(M::MULT);
   const int R = p.R;
 
   float* qt = reinterpret_cast<float*>(smem + L::QT_OFF);
@@ -969,7 +970,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
 #pragma unroll
           for (int w2 = 1; w2 < NW; ++w2) qmax = fmaxf(qmax, qmw[w2]);
           constexpr int PPR = D / 2;           // channel pairs per row
-          constexpr float KW = MULT;
+          const float KW = MULT;
           const float zsh = p.zshift;   // zero points read as z + zsh * s (the INT4 midpoint reading)
           float zsum = 0.f;
           float kscale_new, Z2;

@@ -76,6 +76,7 @@ struct AttendParams {
   int top_k;
   float qscale;             // sm_scale * log2(e)
   float zshift;             // zero points read as z + zshift * s (8: the INT4 midpoint reading)
+  float smul;               // INT1 variants: scales read as smul * s (1/2: the centred 1-bit reading)
   uint16_t* out;            // [B][gamma][Hq][D]
   float* lse;               // [B][gamma][Hq] or null
   int* status;
@@ -99,6 +100,7 @@ struct TopkParams {
   const float* pre;         // pre-scored launch: [B*Hkv][C] finished scores from the attention's scoring pass
   int Hq, HG, k;
   float zshift;             // key zero points read as fp32(z + zshift * s)
+  float smul;               // INT1 variants: key scales read as smul * s
   int32_t* idx_out;         // [B][Hkv][k]
   float* score_out;         // [B][Hkv][k] or null
   int* status;
@@ -182,8 +184,16 @@ struct ResidualWriteParams {
 
 // The kernel variant a read mode runs (the INT4 midpoint reading runs the INT4
 // kernels with a zero shift) and that shift.
-inline int kernel_mode(int mode) { return mode == KVQ_MODE_INT4_MID ? KVQ_MODE_INT4 : mode; }
-inline float mode_zero_shift(int mode) { return mode == KVQ_MODE_INT4_MID ? 8.0f : 0.0f; }
+// A read mode's kernel variant, and its zero-point shift and scale multiplier
+// on top of the variant's own: INT4_MID reads zero point z + 8 s; INT1_CENTER
+// reads zero point z + s/4 and scale s/2.
+inline int kernel_mode(int mode) {
+  return mode == KVQ_MODE_INT4_MID ? KVQ_MODE_INT4 : (mode == KVQ_MODE_INT1_CENTER ? KVQ_MODE_INT1 : mode);
+}
+inline float mode_zero_shift(int mode) {
+  return mode == KVQ_MODE_INT4_MID ? 8.0f : (mode == KVQ_MODE_INT1_CENTER ? 0.25f : 0.0f);
+}
+inline float mode_scale_mul(int mode) { return mode == KVQ_MODE_INT1_CENTER ? 0.5f : 1.0f; }
 
 cudaError_t launch_flush(const FlushParams& p, cudaStream_t s);
 cudaError_t launch_residual_write(const ResidualWriteParams& p, cudaStream_t s);

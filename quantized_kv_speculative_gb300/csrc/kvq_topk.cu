@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
     for (int pp = 0; pp < D / 8; ++pp) wb[pp] = 0u;
     float init0 = 0.f, init1 = 0.f, unit = 1.f, beta = 0.f;
     long long cur_grp = -1;
-    const float smul = static_cast<float>(M::MULT);
+    const float smul = static_cast<float>(M::MULT) * (MODE == KVQ_MODE_INT1 ? p.smul : 1.0f);
     const float cbmul = static_cast<float>(1 << M::CB);
     uint16_t* whalf = reinterpret_cast<uint16_t*>(smem + L.wb) + warp * 2 * D;   // [hi D][lo D], pair order
     constexpr int CPL = D / 32;   // channels per lane in the cooperative setup

@@ -96,6 +96,9 @@ ATTN_CASES = [
     ("int4mid", 1, 4, 4, 64, 32, 544, 1, 1, 0, False),      # the midpoint reading of the draft code
     ("int4mid", 1, 3, 3, 128, 128, 4000, 1, 1, 0, True),    # one row, needles
     ("int4mid", 2, 2, 8, 128, 64, 1700, 2, 2, 7, False),    # eight rows, selected tokens
+    ("int1c", 3, 2, 8, 128, 32, 2100, 2, 2, 16, True),      # the centred 1-bit reading, SpeCache shape
+    ("int1c", 1, 2, 4, 64, 64, 1000, 2, 2, 0, False),
+    ("int1c", 1, 3, 3, 128, 32, 1500, 1, 1, 0, False),      # one row
 ]
 
 
@@ -143,6 +146,7 @@ CLUSTER_CASES = [
     ("int1", 4, 8, 16, 64, 32, 1000, 2, 2, 0, False),
     ("int8", 2, 2, 8, 128, 128, 1150, 2, 3, 0, False),      # few units, ragged residual
     ("int4mid", 1, 32, 32, 128, 128, 1500, 1, 1, 0, False),
+    ("int1c", 4, 8, 32, 128, 32, 2100, 2, 2, 16, False),
 ]
 
 
@@ -272,6 +276,8 @@ TOPK_CASES = [
     ("int2", 1, 1, 4, 128, 32, 30000, 1024),    # the largest k: 4 splits x 1024 candidates to merge
     ("int4mid", 1, 2, 2, 128, 128, 3000, 64),   # the midpoint reading: zero points moved by 8 steps
     ("int4mid", 2, 2, 8, 64, 32, 1500, 17),
+    ("int1c", 3, 2, 8, 128, 32, 2100, 64),      # the centred 1-bit reading: zero point z + s/4, scale s/2
+    ("int1c", 1, 2, 2, 64, 64, 700, 5),
 ]
 
 
@@ -390,6 +396,7 @@ FUSED_CASES = [
     ("int1", 2, 2, 8, 64, 32, 1500, 2, 2, 0, 17, 1),
     ("int4", 1, 3, 3, 128, 128, 4000, 1, 1, 0, 64, 0),      # MHA draft shape, one row
     ("int4mid", 2, 2, 8, 128, 64, 1700, 2, 2, 7, 33, 1),
+    ("int1c", 3, 2, 8, 128, 32, 2100, 2, 2, 16, 64, 1),
     ("int2", 1, 1, 4, 128, 32, 20000, 2, 2, 0, 100, 1),     # several top-k splits
 ]
 

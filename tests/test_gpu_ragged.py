@@ -92,7 +92,7 @@ def _selected(ocs, Hkv, k, g):
 
 
 @pytest.mark.parametrize("fmt,modes,D,G", [("int2", ("int2",), 128, 32), ("hier8", ("int8", "int4", "int4mid"), 128, 64),
-                                           ("int1", ("int1",), 64, 32)])
+                                           ("int1", ("int1", "int1c"), 64, 32)])
 def test_ragged_append_attend_topk_match_oracle_per_sequence(fmt, modes, D, G):
     B, Hkv, Hq, gamma, P, k = 5, 2, 8, 2, 2, 9
     steps = [[700, 130, 2 * G + 5, 33, 0],          # bulk prefill: flushes, residual only, nothing
