@@ -1107,7 +1107,9 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
             // ---- integer score weights and zero-point term of this group (the top-k score) ----
             // w_d = fp32(qs_d * fp32(MULT s_d)); e with max|w| < 2^e (floored at
             // -100); W_d = rint(w_d 2^(21-e)) = 2^14 h + 2^7 m + l with
-            // |h| <= 128 and |m|, |l| <= 64.  The parts times 2^(SLF - f_p)
+            // |h| <= 128 and |m|, |l| <= 64 (h = rint(W 2^-14), m = rint(r 2^-7)
+            // with r = W - 2^14 h, l = r - 2^7 m: all exact fp32 steps, the
+            // roundings by adding and subtracting 1.5 * 2^23).  The parts times 2^(SLF - f_p)
             // (f_p the pair's code factor) are exact f16 values, so the MMA
             // over the subnormal codes sums c * part * 2^(SLF-24) exactly.
             // Lane l derives key pairs l and l + 32 (quarter (l + 32 i) / (D/8),
@@ -1141,21 +1143,25 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
             es = max(es, -100);
             const float up = pow2i(21 - es);
             sc_unit = pow2i(es - 21);
+            constexpr float kRnd = 12582912.0f;        // 1.5 * 2^23: x + kRnd - kRnd = rint(x) for |x| < 2^22
+            const float fsh = pow2i(sh);
 #pragma unroll
             for (int i = 0; i < NIT; ++i) {
-              uint32_t part[3] = {0u, 0u, 0u};
+              float v[2][3];
 #pragma unroll
               for (int e2 = 0; e2 < 2; ++e2) {
-                const int Wi = __float2int_rn(__fmul_rn(wv[2 * i + e2], up));   // |W| <= 2^21
-                const int lp = ((Wi + 64) & 127) - 64;
-                const int W1 = (Wi - lp) >> 7;
-                const int mp = ((W1 + 64) & 127) - 64;
-                const int hp = (W1 - mp) >> 7;
-                const int v[3] = {hp, mp, lp};
-#pragma unroll
-                for (int k3 = 0; k3 < 3; ++k3)
-                  part[k3] |= static_cast<uint32_t>(__half_as_ushort(__int2half_rn(v[k3] * (1 << sh)))) << (16 * e2);
+                const float W = __fsub_rn(__fadd_rn(__fmul_rn(wv[2 * i + e2], up), kRnd), kRnd);   // |W| <= 2^21
+                const float h = __fsub_rn(__fadd_rn(__fmul_rn(W, 1.0f / 16384.f), kRnd), kRnd);
+                const float r = __fmaf_rn(h, -16384.f, W);
+                const float m = __fsub_rn(__fadd_rn(__fmul_rn(r, 1.0f / 128.f), kRnd), kRnd);
+                const float l = __fmaf_rn(m, -128.f, r);
+                v[e2][0] = __fmul_rn(h, fsh);
+                v[e2][1] = __fmul_rn(m, fsh);
+                v[e2][2] = __fmul_rn(l, fsh);
               }
+              uint32_t part[3];
+#pragma unroll
+              for (int k3 = 0; k3 < 3; ++k3) part[k3] = pack_half2(v[0][k3], v[1][k3]);   // exact f16 values
               const int word = lane + 32 * i;          // quarter * (D/8) + pair
 #pragma unroll
               for (int k3 = 0; k3 < 3; ++k3) whs[k3 * (D / 2) + word] = part[k3];
@@ -1208,14 +1214,15 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
             const float lA = __shfl_down_sync(0xffffffffu, cs[0], 1);
             const float lB = __shfl_down_sync(0xffffffffu, cs[2], 1);
             if (q == 0) {
+              // The part sums are exact: S_x = cs_x * 2^(24 - SLF).  2^14 S_h is an
+              // exact fp32 value and so is 2^7 S_m + S_l (below 2^24), so one
+              // correctly rounded add gives fp32(S_t).
               constexpr float INV = static_cast<float>(1 << (24 - score_log2fac_max<MODE, D>()));
-              const long long SA = static_cast<long long>(__float2int_rn(cs[0] * INV)) * 16384LL +
-                                   static_cast<long long>(__float2int_rn(cs[1] * INV)) * 128LL + __float2int_rn(lA * INV);
-              const long long SB = static_cast<long long>(__float2int_rn(cs[2] * INV)) * 16384LL +
-                                   static_cast<long long>(__float2int_rn(cs[3] * INV)) * 128LL + __float2int_rn(lB * INV);
+              const float SA = __fadd_rn(__fmul_rn(cs[0], INV * 16384.f), __fmaf_rn(cs[1], INV * 128.f, __fmul_rn(lA, INV)));
+              const float SB = __fadd_rn(__fmul_rn(cs[2], INV * 16384.f), __fmaf_rn(cs[3], INV * 128.f, __fmul_rn(lB, INV)));
               float* dst = p.pre + u * p.c.C + t_begin + tok0;
-              dst[tokA[s]] = __fadd_rn(__fmul_rn(__ll2float_rn(SA), sc_unit), sc_beta);
-              dst[tokB[s]] = __fadd_rn(__fmul_rn(__ll2float_rn(SB), sc_unit), sc_beta);
+              dst[tokA[s]] = __fadd_rn(__fmul_rn(SA, sc_unit), sc_beta);
+              dst[tokB[s]] = __fadd_rn(__fmul_rn(SB, sc_unit), sc_beta);
             }
           }
         }
