@@ -1063,8 +1063,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
               const int c0 = qq * (D / 4) + kx_chan<MODE, D>(pp, 0), c1 = qq * (D / 4) + kx_chan<MODE, D>(pp, 1);
               smax = fmaxf(smax, fmaxf(ks[c0], ks[c1]));
             }
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o2));
+            smax = warp_max_nonneg(smax);        // scales are >= 0
             const float bound = qmax * smax * KW;
             const int e = (bound > 0.f) ? max(-100, min(100, 13 - exp2_floor(bound))) : 0;
             Z2 = pow2i(e - 24);
@@ -1134,8 +1133,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
               zp[2 * i + 1] = __fmul_rn(qsum[d1], fmaf(zsh, ks[d1], kz[d1]));
               mxw = fmaxf(mxw, fmaxf(fabsf(wv[2 * i]), fabsf(wv[2 * i + 1])));
             }
-#pragma unroll
-            for (int o2 = 1; o2 < 32; o2 <<= 1) mxw = fmaxf(mxw, __shfl_xor_sync(0xffffffffu, mxw, o2));
+            mxw = warp_max_nonneg(mxw);
             // beta: the products rounded to integers at the largest one's unit, summed exactly
             sc_beta = zero_term_warp<2 * NIT>(zp);
             int es = 0;

@@ -239,27 +239,41 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 // 2^e as an fp32 for -126 <= e <= 127.
 __device__ __forceinline__ float pow2f_exact(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
 
+// Largest value over the warp of a non-negative finite fp32 (its bit pattern
+// orders like its value): one warp reduction.
+__device__ __forceinline__ float warp_max_nonneg(float x) {
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(x)));
+}
+
 // The top-k score's zero-point term of one key group, by one warp: lane l
 // holds the products p_d = fp32(qs_d z_d) of CPL channels.  With f the
 // exponent of max|p| (max|p| < 2^f, floored at -80), beta = fp32(Z) 2^(f-40)
 // with Z = sum_d rint(p_d 2^(40-f)), an exact 64-bit integer sum, so the
-// lanes may add in any order.  Every lane returns beta.
+// lanes may add in any order.  Each term (|t| < 2^40) is split as
+// hi 2^20 + lo with 0 <= lo < 2^20; the warp sums hi and lo in 32-bit
+// integer reductions (both stay below 2^27 for at most 128 channels), then
+// recombines.  Every lane returns beta.
 template <int CPL>
 __device__ __forceinline__ float zero_term_warp(const float (&p)[CPL]) {
+  static_assert(CPL * 32 <= 128, "the 32-bit partial sums assume at most 128 channels");
   float mx = 0.f;
 #pragma unroll
   for (int c = 0; c < CPL; ++c) mx = fmaxf(mx, fabsf(p[c]));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  mx = warp_max_nonneg(mx);
   int f = 0;
   if (mx > 0.f) frexpf(mx, &f);
   f = max(f, -80);
   const float up = pow2f_exact(40 - f);
-  long long z = 0;
+  int hs = 0, ls = 0;
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) z += __float2ll_rn(__fmul_rn(p[c], up));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  for (int c = 0; c < CPL; ++c) {
+    const long long t = __float2ll_rn(__fmul_rn(p[c], up));
+    hs += static_cast<int>(t >> 20);
+    ls += static_cast<int>(t & 0xFFFFFLL);
+  }
+  hs = __reduce_add_sync(0xffffffffu, hs);
+  ls = __reduce_add_sync(0xffffffffu, ls);
+  const long long z = (static_cast<long long>(hs) << 20) + ls;
   return __fmul_rn(__ll2float_rn(z), pow2f_exact(f - 40));
 }
 

@@ -584,8 +584,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
             // zero point as the mode reads it: fp32(z + zshift * s) (the INT4 midpoint reading)
             zp[c] = __fmul_rn(qs[d], fmaf(p.zshift, ks[d], kz[d]));
           }
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) mxw = fmaxf(mxw, __shfl_xor_sync(0xffffffffu, mxw, o));
+          mxw = warp_max_nonneg(mxw);
           beta = zero_term_warp<CPL>(zp);
           int e = 0;
           if (mxw > 0.f) frexpf(mxw, &e);
@@ -605,6 +604,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
             whalf[pos] = __half_as_ushort(__float2half_rn(h));
             whalf[D + pos] = __half_as_ushort(__float2half_rn(l));
           }
+          // integer-valued sums below 2^18: exact in fp32 in any order
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
             shi += __shfl_xor_sync(0xffffffffu, shi, o);
