@@ -1,7 +1,7 @@
 // Device-side building blocks shared by the kernels of this library:
-// mbarrier + 1-D bulk (TMA) copies, bounded waits, the m16n8k16 tensor-core
-// MMA, and the integer-code -> f16 conversions used for in-register
-// dequantization.
+// mbarrier + 1-D bulk (TMA) copies, bounded waits, thread-block cluster
+// helpers, the m16n8k16 tensor-core MMA, f16 packing, and the warp reductions
+// of the exact top-k score.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -177,47 +177,6 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t a) {
   uint32_t d;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
   return d;
-}
-
-// ------------------------------------------------------------------------------
-// Code -> f16 conversion.  A b-bit code c placed in the top b mantissa bits of
-// an f16 whose exponent field encodes 1.0 gives exactly 1 + c / 2^b.  Two codes
-// that sit 16 bits apart in a 32-bit word become one half2 with one shift and
-// one LOP3.  The constant 1 is removed algebraically by the callers (weights
-// pre-scaled by 2^b and a per-row correction).
-// ------------------------------------------------------------------------------
-
-template <int SH>
-__device__ __forceinline__ uint32_t shl_signed(uint32_t x) {
-  if constexpr (SH >= 0) return x << SH;
-  else return x >> (-SH);
-}
-
-__device__ __forceinline__ uint32_t lop_and_or(uint32_t x, uint32_t m, uint32_t c) {
-  uint32_t r;
-  // r = (x & m) | c
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(m), "r"(c));
-  return r;
-}
-
-constexpr uint32_t F16_ONE2 = 0x3C003C00u;
-
-// 4-bit codes: nibble i (bits 4i..4i+3) and nibble i+4 (bits 16+4i..) -> half2.
-template <int I>
-__device__ __forceinline__ uint32_t cvt4_pair(uint32_t w) {
-  return lop_and_or(shl_signed<6 - 4 * I>(w), 0x03C003C0u, F16_ONE2);
-}
-
-// 2-bit codes: code i (bits 2i..2i+1) and code i+8 (bits 16+2i..) -> half2.
-template <int I>
-__device__ __forceinline__ uint32_t cvt2_pair(uint32_t w) {
-  return lop_and_or(shl_signed<8 - 2 * I>(w), 0x03000300u, F16_ONE2);
-}
-
-// 1-bit codes: bit i and bit i+16 -> half2.
-template <int I>
-__device__ __forceinline__ uint32_t cvt1_pair(uint32_t w) {
-  return lop_and_or(shl_signed<9 - I>(w), 0x02000200u, F16_ONE2);
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {

@@ -20,8 +20,6 @@
 // (rows = channels, k = tokens).
 #pragma once
 
-#include <type_traits>
-
 #include "kvq_device.cuh"
 
 namespace kvq {
@@ -53,75 +51,9 @@ struct Rows {
   static constexpr int KCHUNK = KROW / 4;  // bytes of a key row owned by one lane
 };
 
-template <int I, int N, typename F>
-__device__ __forceinline__ void static_for(F&& f) {
-  if constexpr (I < N) {
-    f(std::integral_constant<int, I>{});
-    static_for<I + 1, N>(f);
-  }
-}
-
-// Convert this lane's chunk of one key row into D/8 code pairs (1 + c/2^CB)
-// for the single-plane modes (INT4 reads the upper plane).  `k0` points at the
-// chunk in plane 0.
-template <int MODE, int D>
-__device__ __forceinline__ void key_pairs(const uint8_t* k0, int /*plane_stride*/, uint32_t (&P)[D / 8]) {
-  using M = Mode<MODE>;
-  static_assert(M::NP == 1, "the INT8 target code converts through key_pairs_x");
-  if constexpr (M::PB == 4) {
-    constexpr int NWD = D / 32;  // words per chunk
-    uint32_t h[NWD];
-    if constexpr (NWD == 4) {
-      const uint4 v = *reinterpret_cast<const uint4*>(k0);
-      h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
-    } else {
-      const uint2 v = *reinterpret_cast<const uint2*>(k0);
-      h[0] = v.x; h[1] = v.y;
-    }
-#pragma unroll
-    for (int w = 0; w < NWD; ++w) {
-      static_for<0, 4>([&](auto I) {
-        constexpr int i = decltype(I)::value;
-        P[4 * w + i] = cvt4_pair<i>(h[w]);
-      });
-    }
-  } else if constexpr (M::PB == 2) {
-    constexpr int NWD = D / 64;
-    uint32_t h[NWD];
-    if constexpr (NWD == 2) {
-      const uint2 v = *reinterpret_cast<const uint2*>(k0);
-      h[0] = v.x; h[1] = v.y;
-    } else {
-      h[0] = *reinterpret_cast<const uint32_t*>(k0);
-    }
-#pragma unroll
-    for (int w = 0; w < NWD; ++w) {
-      static_for<0, 8>([&](auto I) {
-        constexpr int i = decltype(I)::value;
-        P[8 * w + i] = cvt2_pair<i>(h[w]);
-      });
-    }
-  } else {
-    if constexpr (D == 128) {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(k0);
-      static_for<0, 16>([&](auto I) {
-        constexpr int i = decltype(I)::value;
-        P[i] = cvt1_pair<i>(w);
-      });
-    } else {
-      const uint32_t h = *reinterpret_cast<const uint16_t*>(k0);
-      const uint32_t w = (h & 0xFFu) | ((h & 0xFF00u) << 8);
-      static_for<0, 8>([&](auto I) {
-        constexpr int i = decltype(I)::value;
-        P[i] = cvt1_pair<i>(w);
-      });
-    }
-  }
-}
-
 // ------------------------------------------------------------------------------
-// Subnormal encoding for attention.  An f16 whose exponent field is 0 is the
-// subnormal m * 2^-24, m its 10-bit mantissa field, and the tensor cores take
+// Subnormal encoding (attention and top-k).  An f16 whose exponent field is 0
+// is the subnormal m * 2^-24, m its 10-bit mantissa field, and the tensor cores take
 // it exactly.  A b-bit code c whose bits sit at mantissa positions k..k+b-1
 // (k + b <= 10) therefore reads as exactly c * 2^k * 2^-24: no offset to
 // remove afterwards.  Two codes 16 bits apart in a 32-bit word become one half2

@@ -13,13 +13,16 @@
 // integers, so the warp derives beta with shuffles, in any order, when it
 // derives the group's weights.
 // The dot product runs on tensor cores with the keys as the A operand (rows =
-// tokens) and W as the B operand: column 0 holds hi and column 1 holds lo,
-// where W = 2048 hi + lo and |hi|, |lo| <= 1024 are f16-exact integers.  The
-// codes are exact f16 values 1 + c/2^b.  Every partial sum is a multiple of
-// 2^-b below 2^18, so the fp32 accumulation is exact in any order.
-// fp32(S_t) = fp32(2048 S_hi + S_lo) is then a single correctly rounded fp32 add
-// of two exact values.  Each warp derives W for a key group cooperatively (D/32
-// channels per lane) and shares it through shared memory.
+// tokens) in the subnormal f16 encoding of the attention (code c at mantissa
+// bits k.., read as c 2^k 2^-24 with the pair's factor 2^k), and W as the B
+// operand split into three integer parts, W = 2^14 h + 2^7 m + l with
+// |h| <= 128 and |m|, |l| <= 64, each times 2^(SLF - k) (SLF the largest pair
+// factor) an exact f16 value in columns 0, 1 and 2.  Every product is an
+// integer times 2^(SLF-24) and every partial sum stays below 2^24 such units,
+// so the fp32 accumulation is exact in any order; 2^14 S_h and 2^7 S_m + S_l
+// are then exact fp32 values and one correctly rounded add gives fp32(S_t).
+// Each warp derives W for a key group cooperatively (two key pairs per lane)
+// and stages the parts in shared memory in the B fragments' order.
 //
 // One launch: B*Hkv*S CTAs, with S chosen on the host to balance waves against
 // the merge.  Each CTA scores one chunk (bulk-copied tiles on an mbarrier ring,
@@ -99,8 +102,8 @@ __host__ __device__ inline TopkLayout topk_layout(bool pre, int spw, long long c
   const int ring = pre ? kScratch : static_cast<int>(lmax(NW * spw * TopkTile<MODE, D>::SLOT, kScratch));
   TopkLayout l;
   l.qs = ring;                                   // qs[D]
-  l.wb = l.qs + D * 4;                           // per warp: W halves in pair order [2][D] f16
-  l.list = l.wb + NW * 2 * D * 2;                // gathered keys [kGather]
+  l.wb = l.qs + D * 4;                           // per warp: weight parts [3][D/2] half2 in pair order
+  l.list = l.wb + NW * 3 * (D / 2) * 4;          // gathered keys [kGather]
   l.red = l.list + kGather * 4;                  // per-warp values [2 NW]
   l.bar = l.red + 2 * NW * 4;                    // mbarriers [NW][kSpwMax]
   l.misc = l.bar + NW * kSpwMax * 8;             // [0] abort, [1] last, [2..6] select state
@@ -133,25 +136,6 @@ __device__ __forceinline__ int32_t composite_index(uint64_t key) {
 
 __device__ __forceinline__ float pow2f(int e) {  // 2^e for -126 <= e <= 127
   return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-}
-
-// Position, in halves, of channel `local` (within a lane chunk of D/4
-// channels) in the pair order of key_pairs: 2 * pair + (0: low half, 1: high).
-template <int MODE, int D>
-__device__ __forceinline__ int pair_slot(int local) {
-  int pp, e;
-  if constexpr (Mode<MODE>::PB == 4) {
-    pp = 4 * (local / 8) + local % 4;
-    e = (local % 8) / 4;
-  } else if constexpr (Mode<MODE>::PB == 2) {
-    pp = 8 * (local / 16) + local % 8;
-    e = (local % 16) / 8;
-  } else {
-    constexpr int HALF = (D == 128) ? 16 : 8;
-    pp = local % HALF;
-    e = local / HALF;
-  }
-  return 2 * pp + e;
 }
 
 // Sorts the warp's 128 keys into descending order.  Key x = 32 r + lane sits
@@ -541,17 +525,20 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
     }
     __syncthreads();
 
-    // B fragments: lane (g, q) holds column g of W for its channel chunk; only
-    // columns 0 (hi) and 1 (lo) are nonzero.
-    uint32_t wb[D / 8];
-#pragma unroll
-    for (int pp = 0; pp < D / 8; ++pp) wb[pp] = 0u;
-    float init0 = 0.f, init1 = 0.f, unit = 1.f, beta = 0.f;
+    // Lane (g, q) reads column g of the weight parts (zero past column 2) from
+    // the warp's staging area at each k-step.
+    float unit = 1.f, beta = 0.f;
     long long cur_grp = -1;
     const float smul = static_cast<float>(M::MULT) * (MODE == KVQ_MODE_INT1 ? p.smul : 1.0f);
-    const float cbmul = static_cast<float>(1 << M::CB);
-    uint16_t* whalf = reinterpret_cast<uint16_t*>(smem + L.wb) + warp * 2 * D;   // [hi D][lo D], pair order
-    constexpr int CPL = D / 32;   // channels per lane in the cooperative setup
+    uint32_t* whs = reinterpret_cast<uint32_t*>(smem + L.wb) + warp * 3 * (D / 2);   // [3][D/2]
+    const uint2* wsrc = reinterpret_cast<const uint2*>(whs + min(g, 2) * (D / 2) + q * (D / 8));
+    constexpr int NIT = D / 64;                  // key pairs per lane in the derivation
+    constexpr int SLF = score_log2fac_max<MODE, D>();
+    constexpr float INV = static_cast<float>(1 << (24 - SLF));
+    constexpr float kRnd = 12582912.0f;          // 1.5 * 2^23: x + kRnd - kRnd = rint(x) for |x| < 2^22
+    const int pp = lane % (D / 8);
+    const int c0 = kx_chan<MODE, D>(pp, 0), c1 = kx_chan<MODE, D>(pp, 1);
+    const float fsh = pow2f(SLF - ks_log2fac<MODE, D>(pp));
     for (int j = 0; j < my_tiles; ++j) {
       const int ti = my_first + j;
       const int slot = warp * spw + (j % spw);
@@ -570,53 +557,50 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
         const long long tok0 = t0 + 32 * sl;
         const long long grp = tok0 / G;
         if (grp != cur_grp) {
-          // ---- W of this group: lane l derives channels [l*D/32, (l+1)*D/32) ----
+          // ---- W of this group: lane l derives key pairs l and l + 32 ----
+          // w_d = fp32(qs_d * fp32(MULT s_d)); e with max|w| < 2^e (floored
+          // at -100); W_d = rint(w_d 2^(21-e)); h = rint(W 2^-14), r = W - 2^14 h,
+          // m = rint(r 2^-7), l = r - 2^7 m, all exact fp32 steps.
           cur_grp = grp;
+          __syncwarp();                          // every lane is done with the previous group's parts
           const float* ks = ksz + (grp - g_first) * 2 * D;
           const float* kz = ks + D;
-          float w[CPL], zp[CPL];
+          float wv[2 * NIT], zp[2 * NIT];
           float mxw = 0.f;
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            const int d = lane * CPL + c;
-            w[c] = __fmul_rn(qs[d], __fmul_rn(ks[d], smul));
-            mxw = fmaxf(mxw, fabsf(w[c]));
-            // zero point as the mode reads it: fp32(z + zshift * s) (the INT4 midpoint reading)
-            zp[c] = __fmul_rn(qs[d], fmaf(p.zshift, ks[d], kz[d]));
+          for (int i = 0; i < NIT; ++i) {
+            const int base = ((lane + 32 * i) / (D / 8)) * (D / 4);
+            const int d0 = base + c0, d1 = base + c1;
+            wv[2 * i] = __fmul_rn(qs[d0], __fmul_rn(ks[d0], smul));
+            wv[2 * i + 1] = __fmul_rn(qs[d1], __fmul_rn(ks[d1], smul));
+            // zero points as the mode reads them: fp32(z + zshift * s)
+            zp[2 * i] = __fmul_rn(qs[d0], fmaf(p.zshift, ks[d0], kz[d0]));
+            zp[2 * i + 1] = __fmul_rn(qs[d1], fmaf(p.zshift, ks[d1], kz[d1]));
+            mxw = fmaxf(mxw, fmaxf(fabsf(wv[2 * i]), fabsf(wv[2 * i + 1])));
           }
           mxw = warp_max_nonneg(mxw);
-          beta = zero_term_warp<CPL>(zp);
+          beta = zero_term_warp<2 * NIT>(zp);
           int e = 0;
           if (mxw > 0.f) frexpf(mxw, &e);
           e = max(e, -100);
           const float up = pow2f(21 - e);
           unit = pow2f(e - 21);
-          float shi = 0.f, slo = 0.f;
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            const int d = lane * CPL + c;
-            const float W = rintf(__fmul_rn(w[c], up));
-            const float h = floorf(__fmul_rn(__fadd_rn(W, 1024.f), 1.0f / 2048.f));
-            const float l = __fsub_rn(W, __fmul_rn(2048.f, h));
-            shi += h;
-            slo += l;
-            const int pos = (d / (D / 4)) * (D / 4) + pair_slot<MODE, D>(d % (D / 4));
-            whalf[pos] = __half_as_ushort(__float2half_rn(h));
-            whalf[D + pos] = __half_as_ushort(__float2half_rn(l));
-          }
-          // integer-valued sums below 2^18: exact in fp32 in any order
+          for (int i = 0; i < NIT; ++i) {
+            float v[2][3];
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            shi += __shfl_xor_sync(0xffffffffu, shi, o);
-            slo += __shfl_xor_sync(0xffffffffu, slo, o);
-          }
-          init0 = -shi;
-          init1 = -slo;
-          __syncwarp();
-          if (g < 2) {
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(whalf + g * D) + q * (D / 8);
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const float W = __fsub_rn(__fadd_rn(__fmul_rn(wv[2 * i + e2], up), kRnd), kRnd);   // |W| <= 2^21
+              const float h = __fsub_rn(__fadd_rn(__fmul_rn(W, 1.0f / 16384.f), kRnd), kRnd);
+              const float r = __fmaf_rn(h, -16384.f, W);
+              const float m = __fsub_rn(__fadd_rn(__fmul_rn(r, 1.0f / 128.f), kRnd), kRnd);
+              const float l = __fmaf_rn(m, -128.f, r);
+              v[e2][0] = __fmul_rn(h, fsh);
+              v[e2][1] = __fmul_rn(m, fsh);
+              v[e2][2] = __fmul_rn(l, fsh);
+            }
 #pragma unroll
-            for (int pp = 0; pp < D / 8; ++pp) wb[pp] = src[pp];
+            for (int k3 = 0; k3 < 3; ++k3) whs[k3 * (D / 2) + lane + 32 * i] = pack_half2(v[0][k3], v[1][k3]);
           }
           __syncwarp();
         }
@@ -624,28 +608,30 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           uint32_t PA[D / 8], PB[D / 8];
-          key_pairs<MODE, D>(kslab + (16 * s + g) * RW::KROW, 0, PA);
-          key_pairs<MODE, D>(kslab + (16 * s + g + 8) * RW::KROW, 0, PB);
+          key_pairs_s<MODE, D>(kslab + (16 * s + g) * RW::KROW, 0, PA);
+          key_pairs_s<MODE, D>(kslab + (16 * s + g + 8) * RW::KROW, 0, PB);
           // two independent chains over the k-steps (every partial sum is exact)
-          float cc[4] = {init0, init1, init0, init1}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+          float cc[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int kk = 0; kk < D / 16; kk += 2) {
             const uint32_t a[4] = {PA[2 * kk], PB[2 * kk], PA[2 * kk + 1], PB[2 * kk + 1]};
             const uint32_t a2[4] = {PA[2 * kk + 2], PB[2 * kk + 2], PA[2 * kk + 3], PB[2 * kk + 3]};
-            mma16816(cc, a, wb[2 * kk], wb[2 * kk + 1]);
-            mma16816(c2, a2, wb[2 * kk + 2], wb[2 * kk + 3]);
+            const uint2 w0 = wsrc[kk], w1 = wsrc[kk + 1];
+            mma16816(cc, a, g < 3 ? w0.x : 0u, g < 3 ? w0.y : 0u);
+            mma16816(c2, a2, g < 3 ? w1.x : 0u, g < 3 ? w1.y : 0u);
           }
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) cc[e2] += c2[e2];
+          // columns 0, 1 (lanes q = 0) hold the h and m part sums, column 2
+          // (lanes q = 1) the l part sum
+          const float lA = __shfl_down_sync(0xffffffffu, cc[0], 1);
+          const float lB = __shfl_down_sync(0xffffffffu, cc[2], 1);
           if (q == 0) {
             const int rel = static_cast<int>(tok0 - t_begin) + 16 * s + g;
-#pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-              const float shi_t = __fmul_rn(cc[2 * e2], cbmul);       // exact integer
-              const float slo_t = __fmul_rn(cc[2 * e2 + 1], cbmul);
-              const float sf = __fadd_rn(__fmul_rn(2048.f, shi_t), slo_t);
-              okeys[rel + 8 * e2] = order_key(__fadd_rn(__fmul_rn(sf, unit), beta));
-            }
+            const float SA = __fadd_rn(__fmul_rn(cc[0], INV * 16384.f), __fmaf_rn(cc[1], INV * 128.f, __fmul_rn(lA, INV)));
+            const float SB = __fadd_rn(__fmul_rn(cc[2], INV * 16384.f), __fmaf_rn(cc[3], INV * 128.f, __fmul_rn(lB, INV)));
+            okeys[rel] = order_key(__fadd_rn(__fmul_rn(SA, unit), beta));
+            okeys[rel + 8] = order_key(__fadd_rn(__fmul_rn(SB, unit), beta));
           }
         }
       }
