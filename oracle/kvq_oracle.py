@@ -15,6 +15,11 @@ the pages state it, step by step:
   lower nibble rebuild the INT8 target code.  No separate draft copy is stored.
   (QuantSpec page, Approach.)  A second INT4 reading puts the draft code at the
   middle of the 8-bit codes it stands for (lower nibble read as 8).
+* Centred 1-bit reading.  The 1-bit KIVI codes read with the two levels at the
+  centres of the two halves of each group's range.  SpeCache (Approach) gives
+  1-bit KIVI a new zero point and scale without a formula; this reading is the
+  library's, pinned against its own closed form, so its agreement with the
+  pages' variant is unknown.
 * Double full-precision buffer of 2G tokens.  It keeps recent tokens in bf16.
   When full, the oldest G tokens are quantized.  (QuantSpec page, Approach.)
 * Attention.  Softmax attention, in fp64, over the dequantized cache plus the
