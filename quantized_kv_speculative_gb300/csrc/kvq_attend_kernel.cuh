@@ -272,6 +272,23 @@ __device__ void combine_unit(const AttendParams& p, long long u, int S_total, fl
   // weights are known, so that all loads are in flight together.
   const bool pf = PREFETCH && S_total <= kPF;
   float4 pre[2][kPF];
+  // Otherwise tpi adjacent lanes share an item (few rows leave threads spare)
+  // and split its partials between them; the first round's first kPFS partial
+  // outputs per lane are loaded here too, before the weights are known.
+  constexpr int kPFS = 8;
+  const int spare = static_cast<int>(blockDim.x) / max(1, nitems);
+  const int tpi = spare >= 8 ? 8 : (spare >= 4 ? 4 : (spare >= 2 ? 2 : 1));
+  const int per_round = static_cast<int>(blockDim.x) / tpi;
+  float4 pre0[kPFS];
+  if (!pf && tid / tpi < nitems) {
+    const int item = tid / tpi, part = tid % tpi;
+    const float4* src = reinterpret_cast<const float4*>(base + 2 * kMaxRows + (item / D4) * D) + item % D4;
+#pragma unroll
+    for (int i = 0; i < kPFS; ++i) {
+      const int s = part + i * tpi;
+      if (s < S_total) pre0[i] = __ldcg(src + static_cast<long long>(s) * (PF / 4));
+    }
+  }
   if (pf) {
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -330,11 +347,8 @@ __device__ void combine_unit(const AttendParams& p, long long u, int S_total, fl
     }
     return;
   }
-  // Streaming: tpi adjacent lanes share an item (few rows leave threads
-  // spare) and split its partials between them.
-  const int spare = static_cast<int>(blockDim.x) / max(1, nitems);
-  const int tpi = spare >= 8 ? 8 : (spare >= 4 ? 4 : (spare >= 2 ? 2 : 1));
-  const int per_round = static_cast<int>(blockDim.x) / tpi;
+  // Streaming: the first round takes its prefetched partials, then every
+  // round streams the rest.
   for (int k = 0; k * per_round < nitems; ++k) {
     const int item = k * per_round + tid / tpi, part = tid % tpi;
     const bool valid = item < nitems;
@@ -342,8 +356,23 @@ __device__ void combine_unit(const AttendParams& p, long long u, int S_total, fl
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (valid) {
       const float4* src = reinterpret_cast<const float4*>(base + 2 * kMaxRows + rho * D) + d4;
+      int s0 = part;
+      if (k == 0) {
+#pragma unroll
+        for (int i = 0; i < kPFS; ++i) {
+          const int s = part + i * tpi;
+          if (s < S_total) {
+            const float w = wt[s * 8 + rho];
+            acc.x = fmaf(w, pre0[i].x, acc.x);
+            acc.y = fmaf(w, pre0[i].y, acc.y);
+            acc.z = fmaf(w, pre0[i].z, acc.z);
+            acc.w = fmaf(w, pre0[i].w, acc.w);
+          }
+        }
+        s0 = part + kPFS * tpi;
+      }
 #pragma unroll 8
-      for (int s = part; s < S_total; s += tpi) {
+      for (int s = s0; s < S_total; s += tpi) {
         const float w = wt[s * 8 + rho];
         const float4 v = __ldcg(src + static_cast<long long>(s) * (PF / 4));
         acc.x = fmaf(w, v.x, acc.x);
@@ -851,6 +880,23 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
     for (int j = 0; j < min(SPW, my_tiles); ++j) issue(j);
   }
   int issued = min(SPW, my_tiles), consumed = 0;
+  if (p.S_t == 0) {
+    // This CTA's share of the bf16 tail comes after its quantized tokens; its
+    // residual and pending rows are pulled into L2 now, so that the share's
+    // loads at the end of the CTA hit L2.  (Selected rows need their index
+    // first and are left alone.)
+    constexpr int LPR = D / 64;                              // 128-byte lines per bf16 row
+    const int r_b = seq_r(p.c, b);
+    const int ntl = r_b + p.P + p.top_k, per = (ntl + p.S_q - 1) / p.S_q;
+    const int t_lo = min(ntl, split * per), t_hi = min(ntl, t_lo + per);
+    const int t_pf = min(t_hi, r_b + p.P);
+    for (int i = tid; i < (t_pf - t_lo) * 2 * LPR; i += NTHREADS) {
+      const uint16_t *kp = nullptr, *vp = nullptr;
+      tail_row<D>(p, u, t_lo + i / (2 * LPR), kp, vp);
+      const int j = i % (2 * LPR);
+      prefetch_l2((j < LPR ? kp : vp) + (j % LPR) * 64);
+    }
+  }
   const int bm_words = (ntok_chunk + 31) / 32;
   if (tid == 0) *sh_abort = 0;
   const bool has_sel = p.top_k > 0;
