@@ -177,6 +177,23 @@ def test_attend_cluster_and_ticket_combines(case, monkeypatch):
     assert_attention_close(out_t, lse_t, ref_out, ref_lse, what=f"ticket {case}")
 
 
+@pytest.mark.parametrize("mode,Hq,gamma,P", [("int4", 1, 1, 1), ("int8", 4, 1, 2), ("int8", 4, 2, 2)])
+def test_attend_many_splits_ticket_combine(mode, Hq, gamma, P):
+    """One (b, kv head) over a long cache: the plan takes far more splits than
+    the combine prefetches per lane (eight per lane, with one to eight lanes
+    per output item), so the ticket combine's prefetched and streamed partials
+    both take part.  One, four and eight rows."""
+    B, Hkv, D, G, N = 1, 1, 128, 128, 20000
+    case = (mode, B, Hkv, Hq, D, G, N, gamma, P, 0, False)
+    gc, oc, q, pk, pv, _, _, _ = _attn_case(*case)
+    plan = kvq.kvq_attend_plan(gc, mode, Hq, gamma, P, 0)
+    assert not plan["cluster"] and plan["quant_splits"] + plan["tail_splits"] > 32, plan
+    ref_out, ref_lse = oracle.attend(oc, mode, q, pk, pv)
+    out, lse = kvq.kvq_attend(gc, mode, dev(q), dev(pk), dev(pv))
+    torch.cuda.synchronize()
+    assert_attention_close(out, lse, ref_out, ref_lse, what=f"{mode} rows {Hq * gamma}")
+
+
 def test_attend_deterministic_and_split_independent():
     """Two calls give identical bytes.  The result does not depend on the
     workspace's history, because the ticket counters reset themselves."""
