@@ -225,8 +225,9 @@ AttendPlan plan_attend(const kvq_cache* cache, int mode, int R, int n_pend, int 
   const long long max_chunk = max_chunk_for_rows(R);
   // The bf16 tail (residual, pending and selected tokens) goes to CTAs of its
   // own when they fit in the first wave beside the quantized splits without
-  // making the chunks longer; otherwise each quantized split takes a slice of
-  // it after its own tokens.
+  // making the chunks longer (or, below, when the splits fill the first wave
+  // and combine through the workspace); otherwise each quantized split takes
+  // a slice of it after its own tokens.
   const long long ntail = static_cast<long long>(cache->residual_len) + n_pend + top_k;
   const int S_t = static_cast<int>(std::min<long long>(kMaxTailSplits, std::max(1LL, ceil_div(ntail, kTailTokensPerSplit))));
   if (cache->quantized_len > 0) {
@@ -249,6 +250,13 @@ AttendPlan plan_attend(const kvq_cache* cache, int mode, int R, int n_pend, int 
         attend_resident_clusters(kernel_mode(mode), cache->desc.head_dim, cache->desc.group_size, R, S_all, score);
     if (cap > 0 && ceil_div(U, cap) <= ceil_div(U * S_all, slots)) pl.cluster = 1;
   }
+  // Without clusters, a tail that did not fit beside quantized splits filling
+  // the first wave still goes to CTAs of its own: launched after the splits,
+  // they take the slots of the first splits to finish (a unit's last split is
+  // usually shorter, and the CTAs that started first on an SM stream fastest),
+  // and the splits no longer end with a share of the tail.  Measured at 32K
+  // and 128K: 8% and 3% faster draft calls.
+  if (!pl.cluster && pl.S_t == 0 && cache->quantized_len > 0 && slots > 0 && pl.S_q * U >= slots) pl.S_t = S_t;
   return pl;
 }
 

@@ -734,9 +734,10 @@ __device__ __forceinline__ float pow2i(int e) {   // 2^e, -126 <= e <= 127
 
 // A CTA's role: unit u and quantized split r, or tail slice r.  With clusters,
 // CTA r of unit u's cluster is split r (r < S_q) or tail slice r - S_q;
-// otherwise the B*Hkv*S_t tail CTAs come first (so they start in the first
-// wave), then the quantized splits.  The block index is read through a
-// volatile move so that each call derives the role anew.
+// otherwise the B*Hkv*S_q quantized splits come first and the B*Hkv*S_t tail
+// CTAs after them: when the grid is larger than one wave, the short tail CTAs
+// take the slots of the first quantized CTAs to finish.  The block index is
+// read through a volatile move so that each call derives the role anew.
 struct CtaRole {
   long long u;
   int r;
@@ -746,11 +747,11 @@ struct CtaRole {
 __device__ __forceinline__ CtaRole cta_role(const AttendParams& p, long long nunits) {
   unsigned bx;
   asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(bx));
-  const unsigned ntail = p.cluster ? 0u : static_cast<unsigned>(nunits * p.S_t);
+  const unsigned nquant = static_cast<unsigned>(nunits * p.S_q);
   CtaRole c;
-  c.tail = bx < ntail;
+  c.tail = !p.cluster && bx >= nquant;
   const unsigned S = p.cluster ? static_cast<unsigned>(p.S_q + p.S_t) : static_cast<unsigned>(c.tail ? p.S_t : p.S_q);
-  const unsigned rel = c.tail ? bx : bx - ntail;
+  const unsigned rel = c.tail ? bx - nquant : bx;
   const unsigned uu = rel / S;
   c.u = static_cast<long long>(uu);
   c.r = static_cast<int>(rel - uu * S);
