@@ -138,15 +138,16 @@ def test_attend_matches_oracle(case):
 
 # Enough (b, kvh) units that the plan stays within 16 CTAs per unit, and few
 # enough that the clusters fit the device at once (on a 152-SM GB300 with two
-# CTAs per SM, 28 clusters of 10 CTAs), so the launch takes the cluster combine.
+# CTAs per SM, 28 clusters of 10 CTAs) and that the splits do not fill the
+# first wave on their own, so the launch takes the cluster combine.
 CLUSTER_CASES = [
     ("int8", 1, 16, 16, 128, 128, 1300, 8, 8, 0, True),     # verify, eight rows, 16 KV heads
     ("int4", 1, 32, 32, 128, 128, 1500, 1, 1, 0, False),    # draft, one row
-    ("int2", 4, 8, 32, 128, 32, 2100, 2, 2, 16, False),     # SpeCache shape, selected tokens
-    ("int1", 4, 8, 16, 64, 32, 1000, 2, 2, 0, False),
+    ("int2", 2, 8, 32, 128, 32, 1500, 2, 2, 16, False),     # SpeCache shape, selected tokens
+    ("int1", 2, 8, 16, 64, 32, 1000, 2, 2, 0, False),
     ("int8", 2, 2, 8, 128, 128, 1150, 2, 3, 0, False),      # few units, ragged residual
     ("int4mid", 1, 32, 32, 128, 128, 1500, 1, 1, 0, False),
-    ("int1c", 4, 8, 32, 128, 32, 2100, 2, 2, 16, False),
+    ("int1c", 2, 8, 32, 128, 32, 1500, 2, 2, 16, False),
 ]
 
 
