@@ -225,9 +225,9 @@ AttendPlan plan_attend(const kvq_cache* cache, int mode, int R, int n_pend, int 
   const long long max_chunk = max_chunk_for_rows(R);
   // The bf16 tail (residual, pending and selected tokens) goes to CTAs of its
   // own when they fit in the first wave beside the quantized splits without
-  // making the chunks longer (or, below, when the splits fill the first wave
-  // and combine through the workspace); otherwise each quantized split takes
-  // a slice of it after its own tokens.
+  // making the chunks longer, or (below) when they would not fit beside the
+  // splits at all; otherwise each quantized split takes a slice of it after
+  // its own tokens.
   const long long ntail = static_cast<long long>(cache->residual_len) + n_pend + top_k;
   const int S_t = static_cast<int>(std::min<long long>(kMaxTailSplits, std::max(1LL, ceil_div(ntail, kTailTokensPerSplit))));
   if (cache->quantized_len > 0) {

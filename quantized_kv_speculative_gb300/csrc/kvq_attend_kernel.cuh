@@ -18,7 +18,7 @@
 // One launch of B*Hkv*(S_q + S_t) CTAs: per (b, kvh) S_q quantized splits and
 // S_t tail CTAs, either as one thread-block cluster per (b, kvh) or (when the
 // clusters would not fit in the waves the split plan assumed, or S_q + S_t > 16)
-// as a plain grid with the tail CTAs first.
+// as a plain grid with the tail CTAs after the quantized splits.
 //  * Quantized split: four warps each own a contiguous run of 32..64-token
 //    tiles; each warp's lane 0 streams its tiles of the mode's planes and
 //    scales into the warp's ring of shared-memory slots with 1-D bulk (TMA)
