@@ -116,8 +116,8 @@ struct Smem {
   static constexpr int WB_OFF = (BAR_OFF + NSLOT * 8 + 15) / 16 * 16;   // per warp: staged weight fragments
   static constexpr int SQ_OFF = WB_OFF + WB_BYTES;                  // scoring: summed query [D] f32
   static constexpr int SW_OFF = SQ_OFF + SQ_BYTES;                  // scoring: per warp [3][D] f16, pair order
-  static constexpr int SRC_OFF = SW_OFF + SW_BYTES;                 // [8 cols][4 chunks][D/8 pairs] u32 per warp
-  static constexpr int RING_END = SRC_OFF + NW * 6 * 8 + NW * 4;     // per warp: copy source pointers; max |q~|
+  static constexpr int QM_OFF = SW_OFF + SW_BYTES;                  // per warp: max |q~| (f32)
+  static constexpr int RING_END = QM_OFF + NW * 4;
   static constexpr int COMBINE_END = (2 * kMaxCombine * 8 + 16) * 4;
   // the ticket flag sits after whichever layout (ring, combine) is largest
   static constexpr int MISC_OFF = (RING_END > COMBINE_END ? RING_END + 15 : COMBINE_END + 15) / 16 * 16;
@@ -803,8 +803,11 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
   const long long u = role.u;
   const int split = role.r;
   const int b = static_cast<int>(u / p.c.Hkv), kvh = static_cast<int>(u % p.c.Hkv);
-  // a ragged cache splits each sequence's own length over the S_q splits
-  const long long lq_b = seq_lq(p.c, b);
+  // a ragged cache splits each sequence's own length over the S_q splits (the
+  // length is broadcast from lane 0 so that the copy operands below are
+  // warp-uniform values for the compiler)
+  const long long lq_b = __shfl_sync(0xffffffffu, seq_lq(p.c, b), 0);
+  const int wu = __shfl_sync(0xffffffffu, warp, 0);
   const long long chunk =
       p.c.ragged ? (((lq_b + p.S_q - 1) / p.S_q + kChunkAlign - 1) / kChunkAlign) * kChunkAlign : p.chunk;
   const long long t_begin = static_cast<long long>(split) * chunk;
@@ -823,63 +826,58 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   constexpr int SPW = L::SPW;
   // this warp's tiles: a contiguous run of the chunk
-  const int my_first = warp * per_warp;
+  const int my_first = wu * per_warp;
   const int my_tiles = max(0, min(per_warp, ntiles - my_first));
   const long long u_tok = u * p.c.C;  // first token row of this unit in the planes
 
-  // Each warp streams its own tiles: lane 0 puts tile j into slot j % SPW of
-  // the warp's ring with 1-D bulk copies that complete on the slot's mbarrier.
-  // Source pointers of this warp's first tile; tile j adds j tiles.  Chunk
-  // starts are multiples of kChunkAlign, so of G, and offsets inside a chunk
-  // fit in 32 bits.
-  // (kept in shared memory: only lane 0 of the warp issues copies)
+  // Each warp streams its own tiles: one elected lane puts tile j into slot
+  // j % SPW of the warp's ring with 1-D bulk copies that complete on the slot's
+  // mbarrier.  Every copy operand is computed by the whole (converged) warp from
+  // warp-uniform values only: the unit and split of the CTA, kernel parameters,
+  // the warp index and the tile counter.  Chunk starts are multiples of
+  // kChunkAlign, so of G.
   const int rel0 = my_first * M::TT;                       // first token of the run, chunk-relative
-  const uint8_t** src_tab = reinterpret_cast<const uint8_t**>(smem + L::SRC_OFF) + warp * 6;
-  if (lane == 0) {
-    const long long tok_first = u_tok + t_begin + rel0;
-#pragma unroll
-    for (int pl = 0; pl < M::NP; ++pl) {
-      src_tab[pl] = p.c.kplane[pl] + tok_first * RW::KROW;
-      src_tab[2 + pl] = p.c.vplane[pl] + (tok_first / 32) * D * RW::VROW;
-    }
-    src_tab[4] = reinterpret_cast<const uint8_t*>(p.c.vsz + tok_first * 2 * NJ);
-    src_tab[5] = reinterpret_cast<const uint8_t*>(p.c.ksz + (u * (p.c.C / G) + (t_begin + rel0) / G) * 2 * D);
-  }
+  const long long tok_first = u_tok + t_begin + rel0;      // its token row in the planes
+  const uint64_t pol = __shfl_sync(0xffffffffu, policy_evict_first(), 0);
   // A tile loads key scales only when it starts a key group (or is the run's
   // first tile): the group's weights are derived from that tile's copy.
   auto issue = [&](int j) {
-    const int slot = warp * SPW + (j % SPW);
+    const int slot = wu * SPW + (j % SPW);
     const int rel = rel0 + j * M::TT;                        // chunk-relative first token
     const int nt = min(M::TT, ntok_chunk - rel);
     const bool new_grp = (j == 0) || (M::TT > G) || (rel % G == 0);
     const uint32_t kb = nt * RW::KROW, vb = (nt / 32) * D * RW::VROW;
     const uint32_t kszb = new_grp ? static_cast<uint32_t>((nt + G - 1) / G) * 2 * D * 4 : 0u;
     const uint32_t vszb = nt * 2 * NJ * 4;
+    const long long tok = tok_first + static_cast<long long>(j) * M::TT;
     uint8_t* sbase = smem + slot * L::SLOT;
-    const uint64_t pol = policy_evict_first();
-    // order this warp's earlier reads of the slot before the async-proxy writes
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_arrive_expect_tx(full + slot, M::NP * (kb + vb) + kszb + vszb);
+    if (elect_one()) {
+      // order this warp's earlier reads of the slot before the async-proxy writes
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive_expect_tx(full + slot, M::NP * (kb + vb) + kszb + vszb);
 #pragma unroll
-    for (int pl = 0; pl < M::NP; ++pl) {
-      bulk_g2s(sbase + L::K_OFF + pl * L::KPLANE, src_tab[pl] + j * (M::TT * RW::KROW), kb, full + slot, pol);
-      bulk_g2s(sbase + L::V_OFF + pl * L::VPLANE, src_tab[2 + pl] + j * ((M::TT / 32) * D * RW::VROW), vb,
-               full + slot, pol);
+      for (int pl = 0; pl < M::NP; ++pl) {
+        bulk_g2s(sbase + L::K_OFF + pl * L::KPLANE, p.c.kplane[pl] + tok * RW::KROW, kb, full + slot, pol);
+        bulk_g2s(sbase + L::V_OFF + pl * L::VPLANE, p.c.vplane[pl] + (tok / 32) * D * RW::VROW, vb, full + slot,
+                 pol);
+      }
+      if (new_grp)
+        bulk_g2s(sbase + L::KSZ_OFF, p.c.ksz + (u * (p.c.C / G) + (t_begin + rel) / G) * 2 * D, kszb, full + slot,
+                 pol);
+      bulk_g2s(sbase + L::VSZ_OFF, p.c.vsz + tok * 2 * NJ, vszb, full + slot, pol);
     }
-    if (new_grp)
-      bulk_g2s(sbase + L::KSZ_OFF, src_tab[5] + ((rel0 + j * M::TT) / G - rel0 / G) * (2 * D * 4), kszb,
-               full + slot, pol);
-    bulk_g2s(sbase + L::VSZ_OFF, src_tab[4] + j * (M::TT * 2 * NJ * 4), vszb, full + slot, pol);
+    __syncwarp();
   };
 
   // ---- setup: each warp's barriers first, so its first tiles load at once ----
   const uint4 q_slice = load_q<D>(p, b, kvh, tid);
   static_assert(kMaxRows * (D / 8) <= NTHREADS, "one query slice per thread");
   if (lane == 0) {
-    for (int s2 = 0; s2 < SPW; ++s2) mbar_init(full + warp * SPW + s2, 1);
+    for (int s2 = 0; s2 < SPW; ++s2) mbar_init(full + wu * SPW + s2, 1);
     fence_mbar_init();
-    for (int j = 0; j < min(SPW, my_tiles); ++j) issue(j);
   }
+  __syncwarp();
+  for (int j = 0; j < min(SPW, my_tiles); ++j) issue(j);
   int issued = min(SPW, my_tiles), consumed = 0;
   if (p.S_t == 0) {
     // This CTA's share of the bf16 tail comes after its quantized tokens; its
@@ -908,7 +906,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
     float qm = store_qt<D>(p, tid, q_slice, qt);
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o2));
-    if (lane == 0) reinterpret_cast<float*>(smem + L::SRC_OFF + NW * 48)[warp] = qm;
+    if (lane == 0) reinterpret_cast<float*>(smem + L::QM_OFF)[warp] = qm;
   }
   if constexpr (SC) {
     // the score row's query heads that share this KV head, summed in fp32 in
@@ -977,7 +975,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
 
     for (int j = 0; j < my_tiles; ++j) {
       const int ti = my_first + j;
-      const int slot = warp * SPW + (j % SPW);
+      const int slot = wu * SPW + (j % SPW);
       const uint32_t parity = (j / SPW) & 1;
       if (!mbar_wait_bounded(full + slot, parity, p.wait_limit)) {
         record_status(p.status, KVQ_ERR_DEVICE_TIMEOUT);
@@ -1012,7 +1010,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
           const int lpr = 32 / rpow, wrow = lane / lpr, wsub = lane % lpr;
           uint32_t* wb = reinterpret_cast<uint32_t*>(smem + L::WB_OFF) + warp * (4 * D);
           (void)wb; (void)wrow; (void)wsub;
-          const float* qmw = reinterpret_cast<const float*>(smem + L::SRC_OFF + NW * 48);
+          const float* qmw = reinterpret_cast<const float*>(smem + L::QM_OFF);
           float qmax = qmw[0];
 #pragma unroll
           for (int w2 = 1; w2 < NW; ++w2) qmax = fmaxf(qmax, qmw[w2]);
@@ -1426,14 +1424,14 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
       __syncwarp();
       consumed = j + 1;
       if (issued < my_tiles) {
-        if (lane == 0) issue(issued);
+        issue(issued);
         ++issued;
       }
     }
     // after an abort: let this warp's copies still in flight land before exit
     if (lane == 0) {
       for (int jj = consumed; jj < issued; ++jj)
-        mbar_wait_bounded(full + warp * SPW + (jj % SPW), (jj / SPW) & 1, p.wait_limit);
+        mbar_wait_bounded(full + wu * SPW + (jj % SPW), (jj / SPW) & 1, p.wait_limit);
     }
     __syncwarp();
 
