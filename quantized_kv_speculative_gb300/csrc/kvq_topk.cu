@@ -431,8 +431,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
   const int G = p.c.G;
   const TopkLayout L = topk_layout<MODE, D>(PRE, p.spw, p.chunk, p.k, p.S);
   // a ragged cache splits each sequence's own length over the S splits, in
-  // multiples of the plan's alignment
-  const long long lq_b = seq_lq(p.c, b);
+  // multiples of the plan's alignment (the length is broadcast from lane 0 so
+  // that the copy operands below are warp-uniform values for the compiler)
+  const long long lq_b = __shfl_sync(0xffffffffu, seq_lq(p.c, b), 0);
+  const int wu = __shfl_sync(0xffffffffu, warp, 0);
   const long long chunk =
       p.c.ragged ? ((lq_b + p.S - 1) / p.S + p.align - 1) / p.align * p.align : p.chunk;
   const long long t_begin = static_cast<long long>(split) * chunk;
@@ -452,12 +454,15 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
   int* misc = reinterpret_cast<int*>(smem + L.misc);   // [0] abort, [1] last, [2..6] select state
   const long long u_tok = u * p.c.C;
   // this warp's tiles: a contiguous run of the chunk
-  const int my_first = warp * per_warp;
+  const int my_first = wu * per_warp;
   const int my_tiles = max(0, min(per_warp, ntiles - my_first));
-  // Each warp streams its own tiles: lane 0 puts tile j into slot j % spw of
-  // the warp's ring with 1-D bulk copies that complete on the slot's mbarrier.
+  // Each warp streams its own tiles: one elected lane puts tile j into slot
+  // j % spw of the warp's ring with 1-D bulk copies that complete on the slot's
+  // mbarrier.  The whole (converged) warp computes the copy operands from
+  // warp-uniform values only.
+  const uint64_t pol = __shfl_sync(0xffffffffu, policy_evict_first(), 0);
   auto issue = [&](int j) {
-    const int slot = warp * spw + (j % spw);
+    const int slot = wu * spw + (j % spw);
     const int rel = (my_first + j) * M::TT;                 // chunk-relative first token
     const int nt = min(M::TT, n - rel);
     const long long t0 = t_begin + rel;
@@ -466,13 +471,15 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
     const uint32_t kb = nt * RW::KROW;
     const uint32_t kszb = new_grp ? static_cast<uint32_t>((nt + G - 1) / G) * 2 * D * 4 : 0u;
     uint8_t* sbase = smem + slot * TL::SLOT;
-    uint64_t* bar = full + warp * kSpwMax + (j % spw);
-    const uint64_t pol = policy_evict_first();
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_arrive_expect_tx(bar, kb + kszb);
-    bulk_g2s(sbase, p.c.kplane[0] + (u_tok + t0) * RW::KROW, kb, bar, pol);
-    if (new_grp)
-      bulk_g2s(sbase + TL::KSZ_OFF, p.c.ksz + (u * (p.c.C / G) + t0 / G) * 2 * D, kszb, bar, pol);
+    uint64_t* bar = full + wu * kSpwMax + (j % spw);
+    if (elect_one()) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive_expect_tx(bar, kb + kszb);
+      bulk_g2s(sbase, p.c.kplane[0] + (u_tok + t0) * RW::KROW, kb, bar, pol);
+      if (new_grp)
+        bulk_g2s(sbase + TL::KSZ_OFF, p.c.ksz + (u * (p.c.C / G) + t0 / G) * 2 * D, kszb, bar, pol);
+    }
+    __syncwarp();
   };
   int issued = 0, consumed = 0;
   if (tid == 0) misc[0] = 0;
@@ -509,10 +516,11 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
 #pragma unroll
     for (int hh = 0; hh < kQPre; ++hh) qpre[hh] = (tid < D && hh < p.HG) ? p.q[qoff + hh * D] : 0;
     if (lane == 0) {
-      for (int s2 = 0; s2 < spw; ++s2) mbar_init(full + warp * kSpwMax + s2, 1);
+      for (int s2 = 0; s2 < spw; ++s2) mbar_init(full + wu * kSpwMax + s2, 1);
       fence_mbar_init();
-      for (int j = 0; j < min(spw, my_tiles); ++j) issue(j);
     }
+    __syncwarp();
+    for (int j = 0; j < min(spw, my_tiles); ++j) issue(j);
     issued = min(spw, my_tiles);
     // summed query (ascending head order, fp32) while the first tiles load
     if (tid < D) {
@@ -541,8 +549,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
     const float fsh = pow2f(SLF - ks_log2fac<MODE, D>(pp));
     for (int j = 0; j < my_tiles; ++j) {
       const int ti = my_first + j;
-      const int slot = warp * spw + (j % spw);
-      if (!mbar_wait_bounded(full + warp * kSpwMax + (j % spw), (j / spw) & 1, p.wait_limit)) {
+      const int slot = wu * spw + (j % spw);
+      if (!mbar_wait_bounded(full + wu * kSpwMax + (j % spw), (j / spw) & 1, p.wait_limit)) {
         record_status(p.status, KVQ_ERR_DEVICE_TIMEOUT);
         *abort_flag = 1;
         break;
@@ -638,14 +646,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
       __syncwarp();
       consumed = j + 1;
       if (issued < my_tiles) {
-        if (lane == 0) issue(issued);
+        issue(issued);
         ++issued;
       }
     }
     // after an abort: let this warp's copies still in flight land before exit
     if (lane == 0) {
       for (int jj = consumed; jj < issued; ++jj)
-        mbar_wait_bounded(full + warp * kSpwMax + (jj % spw), (jj / spw) & 1, p.wait_limit);
+        mbar_wait_bounded(full + wu * kSpwMax + (jj % spw), (jj / spw) & 1, p.wait_limit);
     }
     __syncwarp();
   }
