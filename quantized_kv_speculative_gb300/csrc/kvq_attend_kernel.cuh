@@ -307,22 +307,32 @@ __device__ void combine_unit(const AttendParams& p, long long u, int S_total, fl
     wt[e] = __ldcg(base + s * PF + kMaxRows + r);
   }
   __syncthreads();
-  if (tid < p.R) {
-    float M = neg_inf();
-    for (int s = 0; s < S_total; ++s) M = fmaxf(M, ms[s * 8 + tid]);
-    float L = 0.f;
-    if (M != neg_inf()) {
-      for (int s = 0; s < S_total; ++s) {
-        const float m = ms[s * 8 + tid];
-        const float f = (m == neg_inf()) ? 0.f : fast_exp2(m - M);
-        L += f * wt[s * 8 + tid];
-        wt[s * 8 + tid] = f;
+  // the split weights of each row: warp w takes rows w, w + NW, its lanes the splits
+  {
+    const int lane = tid % 32;
+    for (int rho = tid / 32; rho < p.R; rho += NW) {
+      float M = neg_inf();
+      for (int s = lane; s < S_total; s += 32) M = fmaxf(M, ms[s * 8 + rho]);
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+      float L = 0.f;
+      if (M != neg_inf()) {
+        for (int s = lane; s < S_total; s += 32) {
+          const float m = ms[s * 8 + rho];
+          const float f = (m == neg_inf()) ? 0.f : fast_exp2(m - M);
+          L = fmaf(f, wt[s * 8 + rho], L);
+          wt[s * 8 + rho] = f;
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+      }
+      const float inv = (L > 0.f) ? 1.f / L : 0.f;
+      for (int s = lane; s < S_total; s += 32) wt[s * 8 + rho] = (M == neg_inf()) ? 0.f : wt[s * 8 + rho] * inv;
+      if (lane == 0) {
+        ml[rho] = M;
+        ml[8 + rho] = L;
       }
     }
-    const float inv = (L > 0.f) ? 1.f / L : 0.f;
-    for (int s = 0; s < S_total; ++s) wt[s * 8 + tid] = (M == neg_inf()) ? 0.f : wt[s * 8 + tid] * inv;
-    ml[tid] = M;
-    ml[8 + tid] = L;
   }
   __syncthreads();
   auto put = [&](int rho, int d4, const float4& acc) { put_item<D>(p, b, kvh, rho, d4, acc, ml[rho], ml[8 + rho]); };
@@ -686,22 +696,30 @@ __device__ __forceinline__ void finish_unit(const AttendParams& p, long long u, 
 }
 
 // Merge entries [0, nent) of the shared scratch into the partial at dst.
+static_assert(2 * NW <= 8, "a CTA's merge entries fit in eight lanes");
 template <int D>
 __device__ void merge_to_partial(const AttendParams& p, float* dst, int nent, int G, const float* wm,
                                  const float* wl, const float* wc, const float* wo, float* fac) {
   const int tid = threadIdx.x, R = p.R;
-  if (tid < R) {
-    float Mx = neg_inf();
-    for (int w = 0; w < nent; ++w) Mx = fmaxf(Mx, wm[w * 8 + tid]);
-    float lt = 0.f;
-    for (int w = 0; w < nent; ++w) {
-      const float mw = wm[w * 8 + tid];
+  {
+    // the entries' factors of each row: warp w takes rows w, w + NW, lane i
+    // entry i (nent <= 2 NW <= 8)
+    const int lane = tid % 32;
+    for (int rho = tid / 32; rho < R; rho += NW) {
+      const float mw = lane < nent ? wm[lane * 8 + rho] : neg_inf();
+      float Mx = mw;
+#pragma unroll
+      for (int o2 = 4; o2 > 0; o2 >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o2));
       const float f = (mw == neg_inf()) ? 0.f : fast_exp2(mw - Mx);
-      fac[w * 8 + tid] = f;
-      lt += f * wl[w * 8 + tid];
+      float lt = lane < nent ? f * wl[lane * 8 + rho] : 0.f;
+#pragma unroll
+      for (int o2 = 4; o2 > 0; o2 >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o2);
+      if (lane < nent) fac[lane * 8 + rho] = f;
+      if (lane == 0) {
+        dst[rho] = Mx;
+        dst[kMaxRows + rho] = lt;
+      }
     }
-    dst[tid] = Mx;
-    dst[kMaxRows + tid] = lt;
   }
   __syncthreads();
   for (int e = 4 * tid; e < R * D; e += 4 * NTHREADS) {

@@ -390,7 +390,7 @@ __device__ __forceinline__ void warp_merge_top(uint64_t (&a)[KR], const uint64_t
 // the result is list 0.
 template <int KR>
 __device__ void warp_merge_tree(uint64_t* M, int S, int K) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
   constexpr int N = 32 * KR;
   for (int st = 1; st < S; st *= 2) {
     for (int i = 2 * st * warp; i + st < S; i += 2 * st * NW) {
@@ -423,7 +423,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
   using RW = Rows<MODE, D>;
   using TL = TopkTile<MODE, D>;
   extern __shared__ __align__(128) uint8_t smem[];
-  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  // the warp index broadcast from lane 0: a warp-uniform value for the compiler
+  const int tid = threadIdx.x, lane = tid % 32, warp = __shfl_sync(0xffffffffu, tid / 32, 0);
   const int g = lane >> 2, q = lane & 3;
   const long long u = blockIdx.x / p.S;
   const int split = blockIdx.x % p.S;
@@ -434,7 +435,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
   // multiples of the plan's alignment (the length is broadcast from lane 0 so
   // that the copy operands below are warp-uniform values for the compiler)
   const long long lq_b = __shfl_sync(0xffffffffu, seq_lq(p.c, b), 0);
-  const int wu = __shfl_sync(0xffffffffu, warp, 0);
   const long long chunk =
       p.c.ragged ? ((lq_b + p.S - 1) / p.S + p.align - 1) / p.align * p.align : p.chunk;
   const long long t_begin = static_cast<long long>(split) * chunk;
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
   int* misc = reinterpret_cast<int*>(smem + L.misc);   // [0] abort, [1] last, [2..6] select state
   const long long u_tok = u * p.c.C;
   // this warp's tiles: a contiguous run of the chunk
-  const int my_first = wu * per_warp;
+  const int my_first = warp * per_warp;
   const int my_tiles = max(0, min(per_warp, ntiles - my_first));
   // Each warp streams its own tiles: one elected lane puts tile j into slot
   // j % spw of the warp's ring with 1-D bulk copies that complete on the slot's
@@ -462,7 +462,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
   // warp-uniform values only.
   const uint64_t pol = __shfl_sync(0xffffffffu, policy_evict_first(), 0);
   auto issue = [&](int j) {
-    const int slot = wu * spw + (j % spw);
+    const int slot = warp * spw + (j % spw);
     const int rel = (my_first + j) * M::TT;                 // chunk-relative first token
     const int nt = min(M::TT, n - rel);
     const long long t0 = t_begin + rel;
@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
     const uint32_t kb = nt * RW::KROW;
     const uint32_t kszb = new_grp ? static_cast<uint32_t>((nt + G - 1) / G) * 2 * D * 4 : 0u;
     uint8_t* sbase = smem + slot * TL::SLOT;
-    uint64_t* bar = full + wu * kSpwMax + (j % spw);
+    uint64_t* bar = full + warp * kSpwMax + (j % spw);
     if (elect_one()) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive_expect_tx(bar, kb + kszb);
@@ -516,7 +516,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
 #pragma unroll
     for (int hh = 0; hh < kQPre; ++hh) qpre[hh] = (tid < D && hh < p.HG) ? p.q[qoff + hh * D] : 0;
     if (lane == 0) {
-      for (int s2 = 0; s2 < spw; ++s2) mbar_init(full + wu * kSpwMax + s2, 1);
+      for (int s2 = 0; s2 < spw; ++s2) mbar_init(full + warp * kSpwMax + s2, 1);
       fence_mbar_init();
     }
     __syncwarp();
@@ -549,8 +549,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
     const float fsh = pow2f(SLF - ks_log2fac<MODE, D>(pp));
     for (int j = 0; j < my_tiles; ++j) {
       const int ti = my_first + j;
-      const int slot = wu * spw + (j % spw);
-      if (!mbar_wait_bounded(full + wu * kSpwMax + (j % spw), (j / spw) & 1, p.wait_limit)) {
+      const int slot = warp * spw + (j % spw);
+      if (!mbar_wait_bounded(full + warp * kSpwMax + (j % spw), (j / spw) & 1, p.wait_limit)) {
         record_status(p.status, KVQ_ERR_DEVICE_TIMEOUT);
         *abort_flag = 1;
         break;
@@ -653,7 +653,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) topk_kernel(TopkParams p) {
     // after an abort: let this warp's copies still in flight land before exit
     if (lane == 0) {
       for (int jj = consumed; jj < issued; ++jj)
-        mbar_wait_bounded(full + wu * kSpwMax + (jj % spw), (jj / spw) & 1, p.wait_limit);
+        mbar_wait_bounded(full + warp * kSpwMax + (jj % spw), (jj / spw) & 1, p.wait_limit);
     }
     __syncwarp();
   }
