@@ -1015,24 +1015,23 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
           // ---- folded key weights of this group, derived once per warp ----
           // w_c = q~_c * MULT * s_c / f_c (f_c the channel's code factor),
           // scaled by 2^e so that the largest possible |w| sits near 2^13,
-          // split into f16 high + low parts.  Lanes split the (row, channel
-          // pair) items of the rows in use (lpr lanes per row), stage the B
-          // fragments in the warp's weight buffer, then each lane loads its
-          // column.  The accumulator starts at 2^(e-24) sum_c q~_c z_c, and
-          // the logit is the accumulator times 2^(24-e).
+          // split into f16 high + low parts.  With one n-tile the lanes split
+          // the channels, stage the B fragments of the rows in use in the
+          // warp's weight buffer, then each lane loads its column; with two the
+          // lanes derive their own columns.  The accumulator starts at
+          // 2^(e-24) sum_c q~_c z_c, and the logit is the accumulator times
+          // 2^(24-e).
           cur_grp = grp;
           const float* ks = ksz + (grp - g_first) * 2 * D;
           const float* kz = ks + D;
-          // rows in use rounded up to a power of two, lpr lanes per row
+          // rows in use rounded up to a power of two
           const int rpow = R <= 1 ? 1 : (R <= 2 ? 2 : (R <= 4 ? 4 : 8));
-          const int lpr = 32 / rpow, wrow = lane / lpr, wsub = lane % lpr;
           uint32_t* wb = reinterpret_cast<uint32_t*>(smem + L::WB_OFF) + warp * (4 * D);
-          (void)wb; (void)wrow; (void)wsub;
+          (void)wb;
           const float* qmw = reinterpret_cast<const float*>(smem + L::QM_OFF);
           float qmax = qmw[0];
 #pragma unroll
           for (int w2 = 1; w2 < NW; ++w2) qmax = fmaxf(qmax, qmw[w2]);
-          constexpr int PPR = D / 2;           // channel pairs per row
           const float KW = MULT;
           const float zsh = p.zshift;   // zero points read as z + zsh * s (the INT4 midpoint reading)
           float zsum = 0.f;
@@ -1120,39 +1119,59 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
               cinit[nt] = __shfl_sync(0xffffffffu, cwn, 8 * q);
             }
           } else {
-            float smax = 0.f;
-            for (int it = wsub; it < PPR; it += lpr) {
-              const int qq = it / (D / 8), pp = it % (D / 8);
-              const int c0 = qq * (D / 4) + kx_chan<MODE, D>(pp, 0), c1 = qq * (D / 4) + kx_chan<MODE, D>(pp, 1);
-              smax = fmaxf(smax, fmaxf(ks[c0], ks[c1]));
+            // Lane l takes channels CPL l .. CPL l + CPL - 1 (CPL = D / 32) of
+            // every row in use: their scales and zero points are read once, and
+            // each row's high and low weight parts go to those channels' halves
+            // of the staged B fragments (column 2 rho + part, chunk qq, half
+            // kx_slot of the channel).
+            constexpr int CPL = D / 32;
+            static_assert(CPL == 4 || CPL == 2, "four or two channels per lane");
+            const int c_lo = CPL * lane, qq = c_lo / (D / 4), cl0 = c_lo % (D / 4);
+            float ksv[CPL], kzv[CPL];
+            if constexpr (CPL == 4) {
+              const float4 a = *reinterpret_cast<const float4*>(ks + c_lo);
+              const float4 z = *reinterpret_cast<const float4*>(kz + c_lo);
+              ksv[0] = a.x; ksv[1] = a.y; ksv[2] = a.z; ksv[3] = a.w;
+              kzv[0] = z.x; kzv[1] = z.y; kzv[2] = z.z; kzv[3] = z.w;
+            } else {
+              const float2 a = *reinterpret_cast<const float2*>(ks + c_lo);
+              const float2 z = *reinterpret_cast<const float2*>(kz + c_lo);
+              ksv[0] = a.x; ksv[1] = a.y;
+              kzv[0] = z.x; kzv[1] = z.y;
             }
+            float smax = 0.f;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) smax = fmaxf(smax, ksv[i]);
             smax = warp_max_nonneg(smax);        // scales are >= 0
             const float bound = qmax * smax * KW;
             const int e = (bound > 0.f) ? max(-100, min(100, 13 - exp2_floor(bound))) : 0;
             Z2 = pow2i(e - 24);
             kscale_new = pow2i(24 - e);
             const float f = pow2i(e) * KW;
-            const float* qr = qt + wrow * qt_row<D>();
-            const int col = 2 * (wrow & 3), ntw = wrow >> 2;
-            for (int it = wsub; it < PPR; it += lpr) {
-              const int qq = it / (D / 8), pp = it % (D / 8);
-              const int c0 = qq * (D / 4) + kx_chan<MODE, D>(pp, 0), c1 = qq * (D / 4) + kx_chan<MODE, D>(pp, 1);
-              const float q0 = qr[qq * qt_chunk<D>() + kx_chan<MODE, D>(pp, 0)];
-              const float q1 = qr[qq * qt_chunk<D>() + kx_chan<MODE, D>(pp, 1)];
-              const float fp = f * ks_inv_fac<MODE, D>(pp);
-              const float w0 = q0 * ks[c0] * fp, w1 = q1 * ks[c1] * fp;
-              const uint32_t hi = pack_half2(w0, w1);
-              const float2 hf = unpack_half2(hi);
-              const uint32_t lo = pack_half2(w0 - hf.x, w1 - hf.y);
-              wb[((ntw * 8 + col) * 4 + qq) * (D / 8) + pp] = hi;
-              wb[((ntw * 8 + col + 1) * 4 + qq) * (D / 8) + pp] = lo;
-              zsum = fmaf(q0, fmaf(zsh, ks[c0], kz[c0]), fmaf(q1, fmaf(zsh, ks[c1], kz[c1]), zsum));
+            uint16_t* wbh = reinterpret_cast<uint16_t*>(wb);
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) kzv[i] = fmaf(zsh, ksv[i], kzv[i]);   // zero points as the mode reads them
+            for (int rho = 0; rho < rpow; ++rho) {
+              const float* qr = qt + rho * qt_row<D>() + qq * qt_chunk<D>() + cl0;
+              float zs = 0.f;
+#pragma unroll
+              for (int i = 0; i < CPL; ++i) {
+                const int slot = kx_slot<MODE, D>(cl0 + i);
+                const float qv = qr[i];
+                const float w = qv * ksv[i] * (f * pow2i(-ks_log2fac<MODE, D>(slot >> 1)));
+                const __half hi = __float2half_rn(w);
+                const __half lo = __float2half_rn(w - __half2float(hi));
+                wbh[(2 * rho) * D + qq * (D / 4) + slot] = __half_as_ushort(hi);
+                wbh[(2 * rho + 1) * D + qq * (D / 4) + slot] = __half_as_ushort(lo);
+                zs = fmaf(qv, kzv[i], zs);
+              }
+#pragma unroll
+              for (int o2 = 16; o2 > 0; o2 >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o2);
+              if (rho == q) zsum = zs;       // the rows of this lane's accumulator (row q)
             }
           }
           kscale = kscale_new;
           if constexpr (NT == 1) {
-            for (int o2 = 1; o2 < lpr; o2 <<= 1) zsum += __shfl_xor_sync(0xffffffffu, zsum, o2);
-            const float cw = zsum * Z2;
             __syncwarp();
             const int row_b = g >> 1, row_c = q;
             const uint4* src = reinterpret_cast<const uint4*>(wb + (g * 4 + q) * (D / 8));
@@ -1161,8 +1180,7 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
               const uint4 x4 = (row_b < rpow) ? src[v] : make_uint4(0u, 0u, 0u, 0u);
               W[0][4 * v] = x4.x; W[0][4 * v + 1] = x4.y; W[0][4 * v + 2] = x4.z; W[0][4 * v + 3] = x4.w;
             }
-            const float cv = __shfl_sync(0xffffffffu, cw, min(row_c, rpow - 1) * lpr);
-            cinit[0] = (row_c < rpow) ? cv : 0.f;
+            cinit[0] = (row_c < rpow) ? zsum * Z2 : 0.f;
             __syncwarp();
           }
           if constexpr (SC) {

@@ -114,8 +114,8 @@ __host__ __device__ constexpr int kx_chan(int p, int e) {
 template <int MODE, int D>
 __host__ __device__ constexpr int kx_slot(int cl) {
   if constexpr (MODE == KVQ_MODE_INT8) {
-    constexpr int INV[8] = {0, 4, 1, 5, 2, 6, 3, 7};   // pair within the octet of kx_chan's A8 order
-    return 2 * (4 * (cl / 8) + INV[cl % 8] % 4) + INV[cl % 8] / 4;
+    constexpr int SL8[8] = {0, 4, 1, 5, 2, 6, 3, 7};   // 2 * (pair within the octet) + e, per channel of the octet
+    return 8 * (cl / 8) + SL8[cl % 8];
   } else if constexpr (MODE == KVQ_MODE_INT4) {
     return 2 * (4 * (cl / 8) + cl % 4) + (cl % 8) / 4;
   } else if constexpr (MODE == KVQ_MODE_INT2) {
@@ -133,6 +133,7 @@ __host__ __device__ constexpr bool kx_slot_inverts_chan() {
       if (kx_slot<MODE, D>(kx_chan<MODE, D>(p, e)) != 2 * p + e) return false;
   return true;
 }
+static_assert(kx_slot_inverts_chan<KVQ_MODE_INT8, 128>() && kx_slot_inverts_chan<KVQ_MODE_INT8, 64>(), "INT8 slots");
 static_assert(kx_slot_inverts_chan<KVQ_MODE_INT4, 128>() && kx_slot_inverts_chan<KVQ_MODE_INT4, 64>(), "INT4 slots");
 static_assert(kx_slot_inverts_chan<KVQ_MODE_INT2, 128>() && kx_slot_inverts_chan<KVQ_MODE_INT2, 64>(), "INT2 slots");
 static_assert(kx_slot_inverts_chan<KVQ_MODE_INT1, 128>() && kx_slot_inverts_chan<KVQ_MODE_INT1, 64>(), "INT1 slots");
