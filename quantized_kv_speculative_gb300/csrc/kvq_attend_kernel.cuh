@@ -919,6 +919,11 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
   const bool has_sel = p.top_k > 0;
   if (has_sel)
     for (int e = tid; e < bm_words; e += blockDim.x) bitmap[e] = 0u;
+  if constexpr (NT == 1) {
+    // the staged weight columns of rows that are not in use stay zero
+    uint4* wz = reinterpret_cast<uint4*>(smem + L::WB_OFF);
+    for (int e = tid; e < L::WB_BYTES / 16; e += NTHREADS) wz[e] = make_uint4(0u, 0u, 0u, 0u);
+  }
   // scaled queries, and per warp the max |q~| (for the weight normalizer)
   {
     float qm = store_qt<D>(p, tid, q_slice, qt);
@@ -1173,14 +1178,14 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
           kscale = kscale_new;
           if constexpr (NT == 1) {
             __syncwarp();
-            const int row_b = g >> 1, row_c = q;
+            // columns of rows past rpow were zeroed at the start and are never written
             const uint4* src = reinterpret_cast<const uint4*>(wb + (g * 4 + q) * (D / 8));
 #pragma unroll
             for (int v = 0; v < D / 32; ++v) {
-              const uint4 x4 = (row_b < rpow) ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+              const uint4 x4 = src[v];
               W[0][4 * v] = x4.x; W[0][4 * v + 1] = x4.y; W[0][4 * v + 2] = x4.z; W[0][4 * v + 3] = x4.w;
             }
-            cinit[0] = (row_c < rpow) ? zsum * Z2 : 0.f;
+            cinit[0] = zsum * Z2;                // zero for rows q >= rpow
             __syncwarp();
           }
           if constexpr (SC) {
