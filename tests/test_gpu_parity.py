@@ -99,6 +99,11 @@ ATTN_CASES = [
     ("int1c", 3, 2, 8, 128, 32, 2100, 2, 2, 16, True),      # the centred 1-bit reading, SpeCache shape
     ("int1c", 1, 2, 4, 64, 64, 1000, 2, 2, 0, False),
     ("int1c", 1, 3, 3, 128, 32, 1500, 1, 1, 0, False),      # one row
+    # one weight n-tile with two to four rows (rows past R up to a power of two stay zero)
+    ("int8", 1, 2, 4, 128, 64, 1300, 1, 1, 0, False),       # 2 rows
+    ("int2", 1, 1, 3, 128, 32, 1100, 1, 1, 4, False),       # 3 rows (padded to 4), selected tokens
+    ("int4", 2, 2, 4, 128, 128, 1400, 2, 2, 0, False),      # 4 rows
+    ("int1", 1, 2, 2, 128, 32, 900, 2, 2, 0, True),         # 2 rows, needles
 ]
 
 
