@@ -1,7 +1,8 @@
-"""GPU parity on seeded random shapes: attention and top-k through the C ABI
-against the CPU oracle, over combinations that the hand-picked cases do not
-enumerate (every read mode, head size, group size, query rows per KV head,
-draft length, pending and selected tokens, context length).
+"""GPU parity on seeded random shapes: attention, top-k and the two fused,
+through the C ABI, against the CPU oracle, over combinations that the
+hand-picked cases do not enumerate (every read mode, head size, group size,
+query rows per KV head, draft length, pending and selected tokens, context
+length).
 
 The shapes are drawn once from a fixed seed, so a run always tests the same
 cases; the tolerances are those of the hand-picked parity tests.
@@ -72,8 +73,31 @@ def _topk_shapes(n, seed=4048):
     return out
 
 
+def _fused_shapes(n, seed=8096):
+    """(mode, B, Hkv, Hq, D, G, N, gamma, P, top_k, next_k, row) for the
+    attention fused with the next step's top-k (the top-k read modes only)."""
+    g = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        mode = str(g.choice(["int4", "int4mid", "int2", "int1", "int1c"]))
+        D = int(g.choice([64, 128]))
+        G = int(g.choice(_groups(D)))
+        HG = int(g.choice([1, 2, 4]))
+        gamma = int(g.choice([x for x in (1, 2, 3, 4, 6, 8) if x * HG <= 8]))
+        Hkv = int(g.integers(1, 4))
+        B = int(g.integers(1, 3))
+        N = int(g.integers(2 * G + 8, 5000))
+        P = gamma + int(g.integers(0, 2))
+        top_k = int(g.choice([0, 8]))
+        next_k = int(g.choice([1, 16, 64, 128]))
+        row = int(g.integers(0, gamma))
+        out.append((mode, B, Hkv, Hkv * HG, D, G, N, gamma, P, top_k, next_k, row))
+    return out
+
+
 RANDOM_ATTN = _attn_shapes(24)
 RANDOM_TOPK = _topk_shapes(16)
+RANDOM_FUSED = _fused_shapes(12)
 
 
 @pytest.mark.parametrize("case", RANDOM_ATTN, ids=lambda c: "-".join(map(str, c)))
@@ -100,3 +124,23 @@ def test_topk_random_shapes(case):
     torch.cuda.synchronize()
     np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
     np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), ref_sc.view(np.uint32))
+
+
+@pytest.mark.parametrize("case", RANDOM_FUSED, ids=lambda c: "-".join(map(str, c)))
+def test_attend_topk_random_shapes(case):
+    """The fused call: attention against the oracle, the next step's top-k
+    bit-exact against the oracle and against kvq_topk on the same row."""
+    mode, B, Hkv, Hq, D, G, N, gamma, P, top_k, next_k, row = case
+    gc, oc, q, pk, pv, sel, sk, sv = _attn_case(mode, B, Hkv, Hq, D, G, N, gamma, P, top_k, False, seed=53)
+    t = lambda x: None if x is None else dev(x)
+    out, lse, idx, sc = kvq.kvq_attend_topk(gc, mode, dev(q), next_k, row, t(pk), t(pv),
+                                           None if sel is None else torch.from_numpy(sel).cuda(), t(sk), t(sv))
+    idx2, sc2 = kvq.kvq_topk(gc, mode, dev(q[:, row]), next_k)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.attend(oc, mode, q, pk, pv, sel, sk, sv)
+    assert_attention_close(out, lse, ref_out, ref_lse, what=str(case))
+    ridx, rsc = oracle.topk(oc, mode, q[:, row], next_k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), rsc.view(np.uint32))
+    np.testing.assert_array_equal(idx.cpu().numpy(), idx2.cpu().numpy())
+    np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), sc2.cpu().numpy().view(np.uint32))
