@@ -36,6 +36,19 @@ def compare_cache(gc: kvq.QuantizedKVCache, oc: oracle.OracleCache):
     """Bit-exact comparison of codes, scales, zeros and the residual buffer."""
     L, G = oc.Lq, oc.G
     U = oc.B * oc.H
+    if L > 0:
+        _compare_quantized(gc, oc, L, G, U)
+    rk, rv = gc.residual()
+    slots = [(gc.residual_start + i) % (2 * G) for i in range(gc.residual_len)]
+    ork, orv = oc.residual()
+    got_k = ki.bf16_tensor_to_f32(rk[:, slots]) if slots else np.zeros((U, 0, oc.D), np.float32)
+    got_v = ki.bf16_tensor_to_f32(rv[:, slots]) if slots else np.zeros((U, 0, oc.D), np.float32)
+    np.testing.assert_array_equal(got_k, ork.reshape(U, -1, oc.D))
+    np.testing.assert_array_equal(got_v, orv.reshape(U, -1, oc.D))
+
+
+def _compare_quantized(gc, oc, L, G, U):
+    """The L quantized tokens: code planes, key scale/zero, value scale/zero."""
     for i, plane in enumerate(oc.packed_k_planes()):
         got = gc.k_plane(i)[:, :L].cpu().numpy()
         np.testing.assert_array_equal(got, plane.reshape(U, L, -1), err_msg=f"key plane {i}")
@@ -48,13 +61,6 @@ def compare_cache(gc: kvq.QuantizedKVCache, oc: oracle.OracleCache):
     vsz = gc.v_scale_zero()[:, :L].cpu().numpy()
     np.testing.assert_array_equal(vsz[:, :, 0].view(np.uint32), oc.v_scale[:, :, :L].reshape(U, L, -1).view(np.uint32))
     np.testing.assert_array_equal(vsz[:, :, 1].view(np.uint32), oc.v_zero[:, :, :L].reshape(U, L, -1).view(np.uint32))
-    rk, rv = gc.residual()
-    slots = [(gc.residual_start + i) % (2 * G) for i in range(gc.residual_len)]
-    ork, orv = oc.residual()
-    got_k = ki.bf16_tensor_to_f32(rk[:, slots]) if slots else np.zeros((U, 0, oc.D), np.float32)
-    got_v = ki.bf16_tensor_to_f32(rv[:, slots]) if slots else np.zeros((U, 0, oc.D), np.float32)
-    np.testing.assert_array_equal(got_k, ork.reshape(U, -1, oc.D))
-    np.testing.assert_array_equal(got_v, orv.reshape(U, -1, oc.D))
 
 
 def bf16_ulp(x: np.ndarray) -> np.ndarray:

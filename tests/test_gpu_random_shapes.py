@@ -16,7 +16,7 @@ import oracle
 import quantized_kv_speculative_gb300 as kvq
 from quantized_kv_speculative_gb300 import _build
 
-from kvq_testlib import assert_attention_close, build_pair, dev
+from kvq_testlib import assert_attention_close, build_pair, compare_cache, dev
 from test_gpu_parity import _attn_case
 
 pytestmark = pytest.mark.gpu
@@ -95,6 +95,23 @@ def _fused_shapes(n, seed=8096):
     return out
 
 
+def _append_patterns(n, seed=1234):
+    """(fmt, B, Hkv, D, G, chunk sizes): appends of 1 token up to several
+    groups at a time, crossing zero, one or many flushes per call."""
+    g = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        fmt = ("hier8", "int2", "int1")[len(out) % 3]   # every format in turn
+        D = int(g.choice([64, 128]))
+        G = int(g.choice(_groups(D)))
+        B = int(g.integers(1, 3))
+        Hkv = int(g.integers(1, 4))
+        chunks = [int(x) for x in g.choice([1, 2, 3, G - 1, G, G + 1, 3 * G + 5, 7 * G], size=int(g.integers(4, 9)))]
+        out.append((fmt, B, Hkv, D, G, tuple(chunks)))
+    return out
+
+
+RANDOM_APPEND = _append_patterns(9)
 RANDOM_ATTN = _attn_shapes(24)
 RANDOM_TOPK = _topk_shapes(16)
 RANDOM_FUSED = _fused_shapes(12)
@@ -144,3 +161,23 @@ def test_attend_topk_random_shapes(case):
     np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), rsc.view(np.uint32))
     np.testing.assert_array_equal(idx.cpu().numpy(), idx2.cpu().numpy())
     np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), sc2.cpu().numpy().view(np.uint32))
+
+
+@pytest.mark.parametrize("case", RANDOM_APPEND, ids=lambda c: "-".join(map(str, c[:5])) + "-" + ".".join(map(str, c[5])))
+def test_append_random_patterns(case):
+    """Codes, scales, zero points and the residual buffer stay bit-exact after
+    every append of a random chunk sequence."""
+    fmt, B, Hkv, D, G, chunks = case
+    N = sum(chunks)
+    K, V = ki.kv_stream(61, B, Hkv, N, D)
+    cap = (N // G + 1) * G
+    gc = kvq.QuantizedKVCache(B, Hkv, D, G, fmt, cap)
+    oc = oracle.OracleCache(B, Hkv, D, G, fmt, cap)
+    pos = 0
+    for n in chunks:
+        kvq.kvq_quantize_append(gc, dev(K[:, :, pos:pos + n]), dev(V[:, :, pos:pos + n]))
+        oc.append(K[:, :, pos:pos + n], V[:, :, pos:pos + n])
+        pos += n
+        torch.cuda.synchronize()
+        assert (gc.quantized_len, gc.residual_len) == (oc.Lq, oc.r)
+        compare_cache(gc, oc)
