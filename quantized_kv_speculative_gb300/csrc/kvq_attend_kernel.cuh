@@ -794,6 +794,13 @@ __global__ void __launch_bounds__(NTHREADS, (target_ctas<MODE, D, NJ, NT, SC>())
   const long long nunits = static_cast<long long>(p.c.B) * p.c.Hkv;
   int* sh_flag = reinterpret_cast<int*>(smem + L::MISC_OFF);
   int* sh_abort = sh_flag + 1;
+  // Programmatic dependent launch: nothing in global memory is touched before
+  // the grids this launch depends on have completed and their writes are
+  // visible; every CTA then lets the next dependent launch begin its own
+  // start-up (it waits here in turn), which hides the launch gap between
+  // back-to-back calls.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   constexpr int G = D / NJ;
   // In either case the partial is staged in the q~ area, which is free once
@@ -1592,8 +1599,19 @@ cudaError_t launch_t(const AttendParams& p, cudaStream_t s) {
   const int S_all = p.S_q + p.S_t;
   const long long grid = nunits * S_all;
   if (!p.cluster) {
-    attend_kernel<MODE, D, NJ, NT, SC><<<static_cast<unsigned>(grid), NTHREADS, smem, s>>>(p);
-    return cudaGetLastError();
+    // a plain grid may start while the previous kernel in the stream finishes
+    // (the kernel waits for it before any global access)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute at = {};
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attend_kernel<MODE, D, NJ, NT, SC>, p);
   }
   if (S_all < 1 || S_all > kMaxClusterCtas) return cudaErrorInvalidValue;
   if (S_all > 8 && (e = allow_wide_clusters<MODE, D, NJ, NT, SC>()) != cudaSuccess) return e;
